@@ -1,0 +1,481 @@
+/*
+ * CPU oracle for the W4A16 INT4 mixture-of-experts expert GEMM described in
+ * "vLLM x Novita AI: Chord, a faster INT4 MoE for Kimi K2.x" (sections
+ * "Two kernel families", "Indexed kernels", "Grouped SM90 kernels").
+ *
+ * TEST INFRASTRUCTURE.  Only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg load this library.  It shares no code, header, table or
+ * constant generator with the CUDA library, and neither includes the other.
+ *
+ * It is deliberately plain and slow: every result is the definition written
+ * out, one output element at a time, with a sequential FP32 sum in ascending
+ * k.  OpenMP only spreads independent output elements over threads; it never
+ * splits or reorders a sum.  Build with -ffp-contract=off so that every
+ * product and every sum is rounded exactly where the C source says.
+ *
+ * What is computed (the article fixes the data types; the reading of each
+ * point the article leaves open is listed with the function):
+ *   dequant   w = bf16_rne( (q - 8) * s ), q a uint4 code, s the BF16 scale of
+ *             its group of 32 along K ("subtract then scale", section "H200 and
+ *             Blackwell indexed decode"; weight and scale shapes [G,N,K] and
+ *             [G,N,K/32] from the grouped operator example).
+ *   align     vLLM moe_align_block_size contract: sorted_ids / expert_ids /
+ *             num_tokens_padded, padding carried by sentinels in the index
+ *             arrays, activations never padded (section "Grouped SM90
+ *             kernels", figure 3, and the deployment notes on the indexed
+ *             fast path).
+ *   gemm      C[p, n] = bf16_rne( sum_k x[p / d, k] * w[e, n, k] ), FP32 sum
+ *             (F16 accumulation is not implemented by either backend,
+ *             deployment notes), BF16 output.
+ *   act       h = bf16_rne( silu(g) * u ), gate rows 0..I-1, up rows I..2I-1.
+ *   combine   out[t, n] = bf16_rne( sum over local k, ascending, of
+ *             w[t, k] * C2[t * topk + k, n] ).
+ *   pack      the byte layout the CUDA library reads (its own specification,
+ *             written out below), so the GPU packer can be checked byte for
+ *             byte; and its inverse.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_OK 0
+#define ORC_EINVAL (-1)   /* bad shape or argument */
+#define ORC_ELAYOUT (-2)  /* packed blob header does not match */
+#define ORC_ERANGE (-3)   /* an index or code is out of range */
+#define ORC_ENOMEM (-4)
+
+#define ORC_GROUP 32
+
+int orc_version(void) { return 1; }
+
+/* ------------------------------------------------------------------------ */
+/* BF16 <-> FP32.  A bf16 value is the upper half of an IEEE binary32.       */
+
+static float f32_from_bf16(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* Round a binary32 to the nearest bf16, ties to even.  NaN stays NaN (quiet
+ * bit set, sign kept); overflow rounds to infinity as IEEE rounding does. */
+static uint16_t bf16_from_f32(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7fffffffu) > 0x7f800000u)
+        return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t keep = u >> 16;
+    uint32_t rest = u & 0xffffu;
+    if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u)))
+        keep += 1u;
+    return (uint16_t)keep;
+}
+
+uint16_t orc_bf16_round(float f) { return bf16_from_f32(f); }
+
+/* ------------------------------------------------------------------------ */
+/* Dequantisation: subtract the offset 8, then multiply by the group scale,
+ * then round once to bf16.  (q - 8) is an integer in [-8, 7] and s carries 8
+ * significant bits, so the binary32 product is exact and the only rounding is
+ * the final one. */
+
+uint16_t orc_dequant(uint8_t q, uint16_t s)
+{
+    float d = (float)((int)q - 8);
+    float p = d * f32_from_bf16(s);
+    return bf16_from_f32(p);
+}
+
+void orc_dequant_pairs(const uint8_t *q, const uint16_t *s, size_t n, uint16_t *out)
+{
+    for (size_t i = 0; i < n; ++i)
+        out[i] = orc_dequant(q[i], s[i]);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Packed weight layout, version 1 ("m16 x k64 fragment chunks").
+ *
+ * blob  = 256-byte header, then E expert regions of N*K*9/16 bytes each.
+ * header (little endian): u32 magic 0x44524843 ("CHRD"), u32 version 1,
+ *        u32 layout 1, u32 group 32, u32 E, u32 N, u32 K, u32 0,
+ *        u64 expert_stride = N*K*9/16, u64 data_offset = 256, then zeros.
+ * An expert region is a sequence of 576-byte chunks, chunk (kc, mt) at
+ * ((kc * N/16) + mt) * 576, for kc < K/64 (64 columns of K) and mt < N/16
+ * (16 rows of N).  Within a chunk:
+ *   bytes [0, 512): 128 little-endian 32-bit words, word (lane*4 + j) for
+ *       lane < 32 and j < 4 (16 columns each).  With g = lane/4, c = lane%4,
+ *       nibble i (bits 4i..4i+3) of that word holds the code of
+ *         i=0: row g,   col 16j+2c      i=4: row g,   col 16j+2c+1
+ *         i=1: row g+8, col 16j+2c      i=5: row g+8, col 16j+2c+1
+ *         i=2: row g,   col 16j+2c+8    i=6: row g,   col 16j+2c+9
+ *         i=3: row g+8, col 16j+2c+8    i=7: row g+8, col 16j+2c+9
+ *       (rows relative to 16*mt, columns relative to 64*kc).
+ *   bytes [512, 576): 16 words, word (h*8 + g) for h < 2, g < 8 holds the bf16
+ *       scale of row g in its low half and of row g+8 in its high half, for
+ *       the group of 32 columns 64*kc + 32*h .. +31.
+ */
+
+#define ORC_HDR 256u
+#define ORC_MAGIC 0x44524843u
+#define ORC_CHUNK 576u
+
+size_t orc_packed_bytes(int E, int N, int K)
+{
+    if (E < 0 || N <= 0 || K <= 0 || N % 16 || K % 64)
+        return 0;
+    return (size_t)ORC_HDR + (size_t)E * (size_t)N * (size_t)K * 9u / 16u;
+}
+
+static void put32(uint8_t *p, uint32_t v)
+{
+    p[0] = (uint8_t)v; p[1] = (uint8_t)(v >> 8); p[2] = (uint8_t)(v >> 16); p[3] = (uint8_t)(v >> 24);
+}
+static uint32_t get32(const uint8_t *p)
+{
+    return (uint32_t)p[0] | (uint32_t)p[1] << 8 | (uint32_t)p[2] << 16 | (uint32_t)p[3] << 24;
+}
+static void put64(uint8_t *p, uint64_t v) { put32(p, (uint32_t)v); put32(p + 4, (uint32_t)(v >> 32)); }
+static uint64_t get64(const uint8_t *p) { return (uint64_t)get32(p) | (uint64_t)get32(p + 4) << 32; }
+
+/* Byte offset (from the start of the expert region) and nibble shift of the
+ * code of row n, column k. */
+static void code_pos(int N, int n, int k, size_t *byte, int *shift)
+{
+    int mt = n / 16, r = n % 16, kc = k / 64, kk = k % 64;
+    int j = kk / 16, kq = kk % 16;
+    int g = r % 8, lower = r / 8;             /* lower: 0 = row g, 1 = row g+8 */
+    int kpart = kq / 8, c = (kq % 8) / 2, odd = kq % 2;
+    int lane = 4 * g + c;
+    int word = lane * 4 + j;
+    int i = kpart * 2 + lower + 4 * odd;
+    *byte = ((size_t)kc * (size_t)(N / 16) + (size_t)mt) * ORC_CHUNK + (size_t)word * 4u + (size_t)(i / 2);
+    *shift = (i % 2) * 4;
+}
+
+/* Byte offset (from the start of the expert region) of the scale of row n,
+ * group grp (columns 32*grp .. 32*grp+31). */
+static size_t scale_pos(int N, int n, int grp)
+{
+    int mt = n / 16, r = n % 16, kc = grp / 2, h = grp % 2;
+    int g = r % 8, lower = r / 8;
+    return ((size_t)kc * (size_t)(N / 16) + (size_t)mt) * ORC_CHUNK + 512u
+           + (size_t)(h * 8 + g) * 4u + (size_t)lower * 2u;
+}
+
+int orc_pack(const uint8_t *codes, const uint16_t *scales, int E, int N, int K,
+             uint8_t *out, size_t out_bytes)
+{
+    size_t need = orc_packed_bytes(E, N, K);
+    if (need == 0 || out_bytes < need)
+        return ORC_EINVAL;
+    memset(out, 0, need);
+    uint64_t stride = (uint64_t)N * (uint64_t)K * 9u / 16u;
+    put32(out + 0, ORC_MAGIC);
+    put32(out + 4, 1u);
+    put32(out + 8, 1u);
+    put32(out + 12, ORC_GROUP);
+    put32(out + 16, (uint32_t)E);
+    put32(out + 20, (uint32_t)N);
+    put32(out + 24, (uint32_t)K);
+    put64(out + 32, stride);
+    put64(out + 40, ORC_HDR);
+    int G = K / ORC_GROUP;
+    for (int e = 0; e < E; ++e) {
+        uint8_t *reg = out + ORC_HDR + (size_t)e * stride;
+        for (int n = 0; n < N; ++n) {
+            for (int k = 0; k < K; ++k) {
+                uint8_t q = codes[((size_t)e * N + n) * K + k];
+                if (q > 15)
+                    return ORC_ERANGE;
+                size_t b; int sh;
+                code_pos(N, n, k, &b, &sh);
+                reg[b] |= (uint8_t)(q << sh);
+            }
+            for (int grp = 0; grp < G; ++grp) {
+                uint16_t s = scales[((size_t)e * N + n) * G + grp];
+                size_t b = scale_pos(N, n, grp);
+                reg[b] = (uint8_t)s;
+                reg[b + 1] = (uint8_t)(s >> 8);
+            }
+        }
+    }
+    return ORC_OK;
+}
+
+int orc_check_header(const uint8_t *blob, int E, int N, int K)
+{
+    if (get32(blob + 0) != ORC_MAGIC || get32(blob + 4) != 1u || get32(blob + 8) != 1u
+        || get32(blob + 12) != ORC_GROUP || get32(blob + 16) != (uint32_t)E
+        || get32(blob + 20) != (uint32_t)N || get32(blob + 24) != (uint32_t)K
+        || get64(blob + 32) != (uint64_t)N * (uint64_t)K * 9u / 16u || get64(blob + 40) != ORC_HDR)
+        return ORC_ELAYOUT;
+    return ORC_OK;
+}
+
+int orc_unpack(const uint8_t *blob, size_t blob_bytes, int E, int N, int K,
+               uint8_t *codes, uint16_t *scales)
+{
+    size_t need = orc_packed_bytes(E, N, K);
+    if (need == 0 || blob_bytes < need)
+        return ORC_EINVAL;
+    if (orc_check_header(blob, E, N, K) != ORC_OK)
+        return ORC_ELAYOUT;
+    uint64_t stride = (uint64_t)N * (uint64_t)K * 9u / 16u;
+    int G = K / ORC_GROUP;
+    for (int e = 0; e < E; ++e) {
+        const uint8_t *reg = blob + ORC_HDR + (size_t)e * stride;
+        for (int n = 0; n < N; ++n) {
+            for (int k = 0; k < K; ++k) {
+                size_t b; int sh;
+                code_pos(N, n, k, &b, &sh);
+                codes[((size_t)e * N + n) * K + k] = (uint8_t)((reg[b] >> sh) & 0xf);
+            }
+            for (int grp = 0; grp < G; ++grp) {
+                size_t b = scale_pos(N, n, grp);
+                scales[((size_t)e * N + n) * G + grp] = (uint16_t)(reg[b] | (uint16_t)reg[b + 1] << 8);
+            }
+        }
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* moe_align_block_size.
+ *
+ * Pairs p = t*topk + k with topk_ids[p] = e in [0, E) are local; any other id
+ * (the value -1 marks an expert on another GPU) is dropped.  Experts are laid
+ * out in ascending order; within an expert its pair ids appear in ascending
+ * order (the article does not fix this order; ascending makes the result
+ * unique).  Each expert's run is padded with the sentinel P = T*topk up to a
+ * multiple of block_m; an expert with no pair gets no block.  expert_ids[b]
+ * names the expert of block b; num_tokens_padded is the padded total.  The
+ * arrays are over-allocated to the capacity below; entries past the padded
+ * total hold the sentinel (sorted_ids) and -1 (expert_ids). */
+
+int64_t orc_align_capacity(int T, int topk, int E, int block_m)
+{
+    if (T < 0 || topk <= 0 || E <= 0 || block_m <= 0)
+        return -1;
+    int64_t P = (int64_t)T * topk;
+    int64_t m = P < E ? P : E;
+    int64_t c = P + m * (block_m - 1);
+    return (c + block_m - 1) / block_m * block_m;
+}
+
+int orc_moe_align(const int32_t *topk_ids, int T, int topk, int E, int block_m,
+                  int32_t *sorted_ids, int32_t *expert_ids, int32_t *num_tokens_padded,
+                  int64_t capacity)
+{
+    int64_t cap = orc_align_capacity(T, topk, E, block_m);
+    if (cap < 0 || capacity < cap)
+        return ORC_EINVAL;
+    int64_t P = (int64_t)T * topk;
+    int32_t sentinel = (int32_t)P;
+    int64_t pos = 0;
+    for (int e = 0; e < E; ++e) {
+        int64_t start = pos;
+        for (int64_t p = 0; p < P; ++p)
+            if (topk_ids[p] == e)
+                sorted_ids[pos++] = (int32_t)p;
+        if (pos == start)
+            continue;
+        while ((pos - start) % block_m)
+            sorted_ids[pos++] = sentinel;
+        for (int64_t b = start / block_m; b < pos / block_m; ++b)
+            expert_ids[b] = e;
+    }
+    *num_tokens_padded = (int32_t)pos;
+    for (int64_t i = pos; i < capacity; ++i)
+        sorted_ids[i] = sentinel;
+    for (int64_t b = pos / block_m; b < capacity / block_m; ++b)
+        expert_ids[b] = -1;
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Indexed grouped GEMM.  For every block b below num_tokens_padded/block_m,
+ * with e = expert_ids[b], and every non-sentinel pair id p in that block:
+ *     C[p, n] = bf16_rne( sum_{k=0..K-1} float(A[p / d, k]) * float(w[e, n, k]) )
+ * where w is the dequantised weight and d = a_row_divisor (topk when A holds
+ * one row per token, 1 when it holds one row per pair).  The sum runs in
+ * ascending k in binary32.  Each bf16 x bf16 product is exact in binary32.
+ * Rows of C that no block names are left untouched. */
+
+static void dequant_expert(const uint8_t *codes, const uint16_t *scales, int e, int N, int K,
+                           float *wq, int nthreads)
+{
+    int G = K / ORC_GROUP;
+#pragma omp parallel for num_threads(nthreads) schedule(static)
+    for (int n = 0; n < N; ++n)
+        for (int k = 0; k < K; ++k) {
+            uint8_t q = codes[((size_t)e * N + n) * K + k];
+            uint16_t s = scales[((size_t)e * N + n) * G + k / ORC_GROUP];
+            wq[(size_t)n * K + k] = f32_from_bf16(orc_dequant(q, s));
+        }
+}
+
+int orc_moe_gemm(const uint16_t *A, int64_t a_rows, int a_row_divisor,
+                 const uint8_t *codes, const uint16_t *scales, int E, int N, int K,
+                 const int32_t *sorted_ids, const int32_t *expert_ids, int32_t num_tokens_padded,
+                 int block_m, int64_t num_pairs, uint16_t *C, int nthreads)
+{
+    if (N <= 0 || K <= 0 || K % ORC_GROUP || block_m <= 0 || a_row_divisor <= 0
+        || num_tokens_padded < 0 || num_tokens_padded % block_m)
+        return ORC_EINVAL;
+    int64_t nblocks = num_tokens_padded / block_m;
+    for (int64_t b = 0; b < nblocks; ++b) {
+        if (expert_ids[b] < 0 || expert_ids[b] >= E)
+            return ORC_ERANGE;
+        for (int i = 0; i < block_m; ++i) {
+            int32_t p = sorted_ids[b * block_m + i];
+            if (p == (int32_t)num_pairs)
+                continue;
+            if (p < 0 || p > num_pairs || (int64_t)(p / a_row_divisor) >= a_rows)
+                return ORC_ERANGE;
+        }
+    }
+    float *wq = (float *)malloc((size_t)N * (size_t)K * sizeof(float));
+    int32_t *rows = (int32_t *)malloc((size_t)(num_tokens_padded > 0 ? num_tokens_padded : 1) * sizeof(int32_t));
+    if (!wq || !rows) {
+        free(wq); free(rows);
+        return ORC_ENOMEM;
+    }
+    for (int e = 0; e < E; ++e) {
+        int64_t nr = 0;
+        for (int64_t b = 0; b < nblocks; ++b) {
+            if (expert_ids[b] != e)
+                continue;
+            for (int i = 0; i < block_m; ++i) {
+                int32_t p = sorted_ids[b * block_m + i];
+                if (p != (int32_t)num_pairs)
+                    rows[nr++] = p;
+            }
+        }
+        if (nr == 0)
+            continue;
+        dequant_expert(codes, scales, e, N, K, wq, nthreads);
+#pragma omp parallel for num_threads(nthreads) schedule(static) collapse(2)
+        for (int64_t r = 0; r < nr; ++r)
+            for (int n = 0; n < N; ++n) {
+                int32_t p = rows[r];
+                const uint16_t *a = A + (size_t)(p / a_row_divisor) * (size_t)K;
+                const float *w = wq + (size_t)n * K;
+                float acc = 0.0f;
+                for (int k = 0; k < K; ++k)
+                    acc += f32_from_bf16(a[k]) * w[k];
+                C[(size_t)p * N + n] = bf16_from_f32(acc);
+            }
+    }
+    free(wq);
+    free(rows);
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* SiLU * up.  C1 holds 2I columns per pair: gate in 0..I-1, up in I..2I-1
+ * (the usual concatenation of w1 and w3; the article does not show it).
+ *     h[p, j] = bf16_rne( (g / (1 + exp(-g))) * u ),  g = C1[p, j], u = C1[p, I + j]
+ * in binary32, for the pairs whose id names a local expert. */
+
+int orc_silu_mul(const uint16_t *C1, const int32_t *topk_ids, int64_t P, int E, int I,
+                 uint16_t *h, int nthreads)
+{
+    if (I <= 0 || P < 0)
+        return ORC_EINVAL;
+#pragma omp parallel for num_threads(nthreads) schedule(static)
+    for (int64_t p = 0; p < P; ++p) {
+        if (topk_ids[p] < 0 || topk_ids[p] >= E)
+            continue;
+        for (int j = 0; j < I; ++j) {
+            float g = f32_from_bf16(C1[(size_t)p * 2 * I + j]);
+            float u = f32_from_bf16(C1[(size_t)p * 2 * I + I + j]);
+            float s = g / (1.0f + expf(-g));
+            h[(size_t)p * I + j] = bf16_from_f32(s * u);
+        }
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Top-k weighted combine.
+ *     out[t, n] = bf16_rne( sum over k ascending with topk_ids[t, k] local of
+ *                           topk_w[t, k] * float(C2[t*topk + k, n]) )
+ * in binary32, starting from +0.  A token with no local pair outputs +0. */
+
+int orc_combine(const uint16_t *C2, const int32_t *topk_ids, const float *topk_w,
+                int T, int topk, int E, int H, uint16_t *out, int nthreads)
+{
+    if (T < 0 || topk <= 0 || H <= 0)
+        return ORC_EINVAL;
+#pragma omp parallel for num_threads(nthreads) schedule(static)
+    for (int t = 0; t < T; ++t)
+        for (int n = 0; n < H; ++n) {
+            float acc = 0.0f;
+            for (int k = 0; k < topk; ++k) {
+                int64_t p = (int64_t)t * topk + k;
+                if (topk_ids[p] < 0 || topk_ids[p] >= E)
+                    continue;
+                acc += topk_w[p] * f32_from_bf16(C2[(size_t)p * H + n]);
+            }
+            out[(size_t)t * H + n] = bf16_from_f32(acc);
+        }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* One MoE layer: align -> gate_up GEMM (A = x, one row per token) -> SiLU*up
+ * -> down GEMM (A = h, one row per pair) -> top-k combine.  Intermediates are
+ * rounded to bf16 at each step, as the separate steps above define. */
+
+int orc_moe_layer(const uint16_t *x, const int32_t *topk_ids, const float *topk_w,
+                  int T, int topk, int E, int H, int I,
+                  const uint8_t *codes13, const uint16_t *scales13,
+                  const uint8_t *codes2, const uint16_t *scales2,
+                  int block_m, uint16_t *out, int nthreads)
+{
+    int64_t cap = orc_align_capacity(T, topk, E, block_m);
+    if (cap < 0 || H <= 0 || I <= 0 || H % ORC_GROUP || I % ORC_GROUP)
+        return ORC_EINVAL;
+    int64_t P = (int64_t)T * topk;
+    int32_t *sorted_ids = (int32_t *)malloc((size_t)(cap > 0 ? cap : 1) * sizeof(int32_t));
+    int32_t *expert_ids = (int32_t *)malloc((size_t)(cap / block_m > 0 ? cap / block_m : 1) * sizeof(int32_t));
+    uint16_t *C1 = (uint16_t *)calloc((size_t)(P > 0 ? P : 1) * 2 * I, sizeof(uint16_t));
+    uint16_t *hb = (uint16_t *)calloc((size_t)(P > 0 ? P : 1) * I, sizeof(uint16_t));
+    uint16_t *C2 = (uint16_t *)calloc((size_t)(P > 0 ? P : 1) * H, sizeof(uint16_t));
+    int rc = ORC_ENOMEM;
+    int32_t ntp = 0;
+    if (!sorted_ids || !expert_ids || !C1 || !hb || !C2)
+        goto done;
+    rc = orc_moe_align(topk_ids, T, topk, E, block_m, sorted_ids, expert_ids, &ntp, cap);
+    if (rc) goto done;
+    rc = orc_moe_gemm(x, T, topk, codes13, scales13, E, 2 * I, H, sorted_ids, expert_ids, ntp,
+                      block_m, P, C1, nthreads);
+    if (rc) goto done;
+    rc = orc_silu_mul(C1, topk_ids, P, E, I, hb, nthreads);
+    if (rc) goto done;
+    rc = orc_moe_gemm(hb, P, 1, codes2, scales2, E, H, I, sorted_ids, expert_ids, ntp,
+                      block_m, P, C2, nthreads);
+    if (rc) goto done;
+    rc = orc_combine(C2, topk_ids, topk_w, T, topk, E, H, out, nthreads);
+done:
+    free(sorted_ids); free(expert_ids); free(C1); free(hb); free(C2);
+    return rc;
+}
+
+int orc_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

@@ -1,0 +1,445 @@
+"""Pins of the CPU oracle against things other than itself.
+
+Every check compares the oracle with an independent source: a value printed on
+the pages or derived by hand (tests/golden/), a library routine (torch's
+float32 -> bf16 conversion, numpy integer and float64 matmul, scipy's expit,
+Python's sort), exact integer arithmetic, a closed form, or an invariant.
+Each test names the mistake it is there to catch.
+"""
+import numpy as np
+import pytest
+import torch
+from scipy.special import expit
+
+import workloads as wl
+from conftest import read_golden
+
+GROUP = 32
+
+
+# --- independent helpers (library routines, not the oracle's code) --------
+
+def to_bf16(f):
+    """float32 values -> bf16 bits via torch's round-to-nearest-even conversion."""
+    t = torch.from_numpy(np.ascontiguousarray(np.asarray(f, dtype=np.float32)))
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def f64(bits):
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def bf16r(v):
+    """Round float64 values to bf16 (through an exact-or-nearest float32) and widen."""
+    return f64(to_bf16(np.asarray(v, np.float64).astype(np.float32)))
+
+
+def dequant_ref(codes, scales):
+    """(q - 8) * s in float64 (exact), rounded to bf16 by torch."""
+    s = np.repeat(f64(scales), GROUP, axis=-1)
+    return to_bf16(((codes.astype(np.float64) - 8.0) * s).astype(np.float32))
+
+
+# --- bf16 rounding ----------------------------------------------------------
+
+def test_bf16_round_page_example(orc):
+    """Worked example of the rounding table on the MI355X page: 256.5 -> 256."""
+    rows = read_golden("bf16_rounding.txt")
+    for r in rows:
+        if len(r) == 2:
+            assert orc.bf16_round(float(r[0])) == int(r[1], 16)
+        else:
+            a, b, d_fp32, d_bf16 = map(float, r)
+            assert np.float32(a) - np.float32(b) == d_fp32
+            assert f64([orc.bf16_round(a)])[0] - f64([orc.bf16_round(b)])[0] == d_bf16
+
+
+def test_bf16_round_matches_torch(orc):
+    """Catches a wrong tie rule, a truncation, or mishandled subnormals/overflow."""
+    rng = np.random.default_rng(7)
+    bits = rng.integers(0, 2**32, size=20000, dtype=np.uint64).astype(np.uint32)
+    # add exact ties, near-ties, subnormals, overflow boundary, infinities
+    extra = [0x3F808000, 0x3F818000, 0x3F807FFF, 0x3F808001, 0x00008000, 0x00018000,
+             0x7F7FFFFF, 0x7F7F7FFF, 0x7F7F8000, 0xFF7F8000, 0x7F800000, 0xFF800000, 0, 0x80000000]
+    bits = np.concatenate([bits, np.array(extra, np.uint32)])
+    vals = bits.view(np.float32)
+    vals = vals[~np.isnan(vals)]
+    want = to_bf16(vals)
+    got = np.array([orc.bf16_round(float(v)) for v in vals], np.uint16)
+    np.testing.assert_array_equal(got, want)
+
+
+# --- dequantisation ---------------------------------------------------------
+
+def test_dequant_closed_forms(orc):
+    for q, s, want, *_ in read_golden("dequant_closed_forms.txt"):
+        assert orc.dequant(int(q), int(s, 16)) == int(want, 16), (q, s)
+
+
+def test_dequant_exhaustive(orc):
+    """All 16 codes x all 65536 bf16 scale patterns against an exact float64
+    product rounded by torch.  Catches a missing offset, add-instead-of-subtract,
+    scale-then-subtract order, double rounding, a wrong NaN/Inf path."""
+    q = np.repeat(np.arange(16, dtype=np.uint8), 65536)
+    s = np.tile(np.arange(65536, dtype=np.uint32).astype(np.uint16), 16)
+    got = orc.dequant_pairs(q, s)
+    prod = (q.astype(np.float64) - 8.0) * f64(s)
+    with np.errstate(invalid="ignore", over="ignore"):
+        want = to_bf16(prod.astype(np.float32))
+    nan_g = np.isnan(f64(got))
+    nan_w = np.isnan(f64(want))
+    np.testing.assert_array_equal(nan_g, nan_w)
+    np.testing.assert_array_equal(got[~nan_w], want[~nan_w])
+
+
+# --- packing ----------------------------------------------------------------
+
+def test_packed_bytes_closed_form(orc):
+    for E, N, K in [(1, 16, 64), (8, 256, 256), (8, 256, 128), (48, 4096, 7168), (384, 7168, 256)]:
+        assert orc.packed_bytes(E, N, K) == 256 + E * N * K * 9 // 16
+    for bad in [(1, 8, 64), (1, 16, 32), (1, 0, 64)]:
+        assert orc.packed_bytes(*bad) == 0
+
+
+def test_pack_header(orc):
+    codes = wl.random_codes(1, (3, 32, 128))
+    scales = wl.random_scales(2, (3, 32, 4))
+    blob = orc.pack(codes, scales)
+    h = blob[:256]
+    u32 = h[:32].view(np.uint32)
+    assert bytes(h[:4]) == b"CHRD"
+    assert list(u32[1:8]) == [1, 1, 32, 3, 32, 128, 0]
+    assert list(h[32:48].view(np.uint64)) == [32 * 128 * 9 // 16, 256]
+    assert not h[48:].any()
+    assert orc.check_header(blob, 3, 32, 128)
+    assert not orc.check_header(blob, 3, 128, 32)
+
+
+def test_pack_positions_golden(orc):
+    """Hand-derived byte/nibble positions of the layout specification."""
+    E, N, K = 1, 32, 128
+    for r in read_golden("layout_v1_positions.txt"):
+        codes = np.zeros((E, N, K), np.uint8)
+        scales = np.zeros((E, N, K // GROUP), np.uint16)
+        if len(r) == 4:
+            n, k, off, sh = map(int, r)
+            codes[0, n, k] = 0xF
+            data = orc.pack(codes, scales)[256:]
+            nz = np.nonzero(data)[0]
+            assert list(nz) == [off], (n, k, list(nz))
+            assert data[off] == (0xF << sh), (n, k)
+        else:
+            n, grp, off = map(int, r)
+            scales[0, n, grp] = 0xABCD
+            data = orc.pack(codes, scales)[256:]
+            assert list(np.nonzero(data)[0]) == [off, off + 1], (n, grp)
+            assert data[off] == 0xCD and data[off + 1] == 0xAB
+
+
+@pytest.mark.parametrize("shape", [(1, 16, 64), (3, 32, 128), (2, 256, 256), (2, 128, 192)])
+def test_pack_roundtrip_and_coverage(orc, shape):
+    """unpack(pack(x)) == x for random data, and all-ones data fills the data region
+    completely: together the placement is a bijection (no overlap, no gap)."""
+    E, N, K = shape
+    codes = wl.random_codes(3, shape)
+    scales = wl.random_scales(4, (E, N, K // GROUP))
+    blob = orc.pack(codes, scales)
+    c2, s2 = orc.unpack(blob, E, N, K)
+    np.testing.assert_array_equal(c2, codes)
+    np.testing.assert_array_equal(s2, scales)
+    full = orc.pack(np.full(shape, 15, np.uint8), np.full((E, N, K // GROUP), 0xFFFF, np.uint16))
+    assert (full[256:] == 0xFF).all()
+    assert full.size == 256 + E * N * K * 9 // 16
+
+
+def test_pack_rejects_bad_codes_and_header(orc):
+    codes = np.zeros((1, 16, 64), np.uint8)
+    codes[0, 3, 5] = 16
+    with pytest.raises(orc.OracleError):
+        orc.pack(codes, np.zeros((1, 16, 2), np.uint16))
+    blob = orc.pack(np.zeros((1, 16, 64), np.uint8), np.zeros((1, 16, 2), np.uint16))
+    blob[0] ^= 1
+    with pytest.raises(orc.OracleError):
+        orc.unpack(blob, 1, 16, 64)
+
+
+# --- align ------------------------------------------------------------------
+
+def align_by_sort(ids, E, bm):
+    """Independent construction with Python's sort over (expert, pair id)."""
+    T, topk = ids.shape
+    P = T * topk
+    pairs = sorted((int(e), p) for p, e in enumerate(ids.ravel()) if 0 <= e < E)
+    sorted_ids, expert_ids = [], []
+    i = 0
+    while i < len(pairs):
+        e = pairs[i][0]
+        seg = []
+        while i < len(pairs) and pairs[i][0] == e:
+            seg.append(pairs[i][1])
+            i += 1
+        while len(seg) % bm:
+            seg.append(P)
+        sorted_ids += seg
+        expert_ids += [e] * (len(seg) // bm)
+    ntp = len(sorted_ids)
+    cap = -(-(P + min(E, P) * (bm - 1)) // bm) * bm
+    sorted_ids += [P] * (cap - ntp)
+    expert_ids += [-1] * (cap // bm - len(expert_ids))
+    return np.array(sorted_ids, np.int32), np.array(expert_ids, np.int32), ntp
+
+
+@pytest.mark.parametrize("T,topk,E,bm,pnl", [(16, 2, 8, 4, 0.0), (33, 8, 48, 16, 0.5), (7, 3, 5, 1, 0.2),
+                                             (64, 8, 384, 8, 0.0), (1, 8, 384, 16, 0.0),
+                                             (128, 4, 6, 64, 0.3), (200, 6, 12, 256, 0.1)])
+def test_align_vs_sort(orc, T, topk, E, bm, pnl):
+    ids = wl.random_ids(T * 31 + E, T, topk, E, p_nonlocal=pnl)
+    s, e, ntp = orc.moe_align(ids, E, bm)
+    s2, e2, ntp2 = align_by_sort(ids, E, bm)
+    assert ntp == ntp2
+    np.testing.assert_array_equal(s, s2)
+    np.testing.assert_array_equal(e, e2)
+
+
+def test_align_edge_counts(orc):
+    """Experts with 0, 1, 2, bm-1, bm, bm+1 rows; ids >= E and -1 are dropped."""
+    bm = 8
+    counts = {0: 0, 1: 1, 2: 2, 3: bm - 1, 4: bm, 5: bm + 1}
+    E = 6
+    flat = []
+    for e, c in counts.items():
+        flat += [e] * c
+    flat += [-1, -1, E, E + 3]
+    rng = np.random.default_rng(0)
+    flat = np.array(flat, np.int32)[rng.permutation(len(flat))]
+    if flat.size % 2:
+        flat = np.append(flat, -1)
+    ids = flat.astype(np.int32).reshape(-1, 2)
+    s, e, ntp = orc.moe_align(ids, E, bm)
+    P = ids.size
+    want_ntp = sum(-(-c // bm) * bm for c in counts.values())
+    assert ntp == want_ntp
+    s2, e2, _ = align_by_sort(ids, E, bm)
+    np.testing.assert_array_equal(s, s2)
+    np.testing.assert_array_equal(e, e2)
+    assert 0 not in e[: ntp // bm]
+    assert (s[ntp:] == P).all()
+
+
+def test_align_empty_and_all_nonlocal(orc):
+    s, e, ntp = orc.moe_align(np.zeros((0, 8), np.int32), 48, 16)
+    assert ntp == 0 and s.size == 0 and e.size == 0
+    ids = np.full((5, 4), -1, np.int32)
+    s, e, ntp = orc.moe_align(ids, 8, 4)
+    assert ntp == 0 and (s == 20).all() and (e == -1).all()
+    assert s.size == orc.align_capacity(5, 4, 8, 4)
+
+
+def test_align_invariants_large(orc):
+    """Every local pair exactly once, each segment ascending, padding only at
+    segment ends, capacity formula."""
+    w = wl.EP8_DECODE
+    ids, _ = wl.make_routing(w)
+    bm = 16
+    s, e, ntp = orc.moe_align(ids, w.E, bm)
+    P = w.P
+    assert s.size == -(-(P + min(P, w.E) * (bm - 1)) // bm) * bm
+    local = np.nonzero((ids.ravel() >= 0) & (ids.ravel() < w.E))[0]
+    valid = s[:ntp][s[:ntp] != P]
+    np.testing.assert_array_equal(np.sort(valid), local)
+    for b in range(ntp // bm):
+        blk = s[b * bm:(b + 1) * bm]
+        v = blk[blk != P]
+        assert (ids.ravel()[v] == e[b]).all()
+        assert (np.diff(v) > 0).all()
+        if v.size < bm:
+            assert (blk[v.size:] == P).all()
+    assert (np.diff(e[: ntp // bm]) >= 0).all()
+
+
+# --- GEMM -------------------------------------------------------------------
+
+def _gemm_via_align(orc, A, div, codes, scales, ids, bm=8):
+    E = codes.shape[0]
+    s, e, ntp = orc.moe_align(ids, E, bm)
+    C = np.full((ids.size, codes.shape[1]), 0xFFFF, np.uint16)
+    return orc.moe_gemm(A, div, codes, scales, s, e, ntp, bm, ids.size, C)
+
+
+@pytest.mark.parametrize("K", [256, 2048])
+def test_gemm_exact_integer_regime(orc, K):
+    """x in {-1,0,1}, scale 1: every partial sum is an integer below 2^24, so the
+    result is exact in any order; compare with numpy's integer matmul.  Catches a
+    wrong sign, a transposed operand, a wrong row index or a dropped term."""
+    T, topk, E, N = 12, 2, 3, 48
+    rng = np.random.default_rng(K)
+    xi = rng.integers(-1, 2, size=(T, K))
+    x = to_bf16(xi.astype(np.float32))
+    codes = wl.random_codes(K + 1, (E, N, K))
+    scales = np.full((E, N, K // GROUP), 0x3F80, np.uint16)
+    ids = wl.random_ids(K + 2, T, topk, E, p_nonlocal=0.25)
+    C = _gemm_via_align(orc, x, topk, codes, scales, ids)
+    Wi = codes.astype(np.int64) - 8
+    for p in range(T * topk):
+        e = ids.ravel()[p]
+        if e < 0:
+            assert (C[p] == 0xFFFF).all()
+            continue
+        exact = Wi[e] @ xi[p // topk]
+        np.testing.assert_array_equal(C[p], to_bf16(exact.astype(np.float32)))
+
+
+def test_gemm_identity(orc):
+    """Code 9 on the diagonal, 8 elsewhere, scale 1: W = I, so C = x exactly."""
+    T, topk, E, K = 5, 2, 2, 64
+    codes = np.full((E, K, K), 8, np.uint8)
+    for e in range(E):
+        np.fill_diagonal(codes[e], 9)
+    scales = np.full((E, K, K // GROUP), 0x3F80, np.uint16)
+    x = wl.random_bf16(11, (T, K))
+    ids = wl.random_ids(12, T, topk, E)
+    C = _gemm_via_align(orc, x, topk, codes, scales, ids, bm=4)
+    for p in range(T * topk):
+        np.testing.assert_array_equal(C[p], x[p // topk])
+    # one row per pair (down projection): A indexed by pair id directly
+    A = wl.random_bf16(13, (T * topk, K))
+    C = _gemm_via_align(orc, A, 1, codes, scales, ids, bm=4)
+    np.testing.assert_array_equal(C, A)
+
+
+def test_gemm_float_bound(orc):
+    """Random data against a float64 matmul of independently dequantised
+    weights: |C - ref| <= half a bf16 ulp of ref plus the FP32 summation bound
+    K * 2^-24 * sum|x*w|.  Catches a wrong group index (scales differ per
+    group), a wrong expert, an off-by-one in K."""
+    T, topk, E, N, K = 9, 3, 4, 64, 320
+    x = wl.random_bf16(21, (T, K))
+    codes = wl.random_codes(22, (E, N, K))
+    scales = wl.random_scales(23, (E, N, K // GROUP))
+    ids = wl.random_ids(24, T, topk, E, p_nonlocal=0.2)
+    C = _gemm_via_align(orc, x, topk, codes, scales, ids)
+    W = f64(dequant_ref(codes, scales))
+    X = f64(x)
+    for p in range(T * topk):
+        e = ids.ravel()[p]
+        if e < 0:
+            continue
+        ref = W[e] @ X[p // topk]
+        mag = np.abs(W[e]) @ np.abs(X[p // topk])
+        tol = np.abs(ref) * 2.0 ** -8 + K * 2.0 ** -24 * mag + 1e-30
+        assert (np.abs(f64(C[p]) - ref) <= tol).all()
+
+
+# --- activation -------------------------------------------------------------
+
+def test_silu_mul_vs_expit(orc):
+    """silu(g) * u against scipy's expit in float64: catches swapped gate/up
+    halves, a missing factor g, exp(+g) instead of exp(-g)."""
+    P, I, E = 40, 96, 4
+    C1 = wl.random_bf16(31, (P, 2 * I), std=3.0)
+    ids = wl.random_ids(32, P, 1, E, p_nonlocal=0.2).ravel()
+    h = np.full((P, I), 0xFFFF, np.uint16)
+    h = orc.silu_mul(C1, ids, E, h)
+    g, u = f64(C1[:, :I]), f64(C1[:, I:])
+    ref = g * expit(g) * u
+    for p in range(P):
+        if ids[p] < 0:
+            assert (h[p] == 0xFFFF).all()
+            continue
+        err = np.abs(f64(h[p]) - ref[p])
+        assert (err <= np.abs(ref[p]) * 2.0 ** -7 + 1e-30).all()
+
+
+def test_silu_mul_closed_forms(orc):
+    g = np.array([0.0, 100.0, -100.0, 2.0, 5.0], np.float32)
+    u = np.array([3.0, 0.5, 4.0, 0.0, -1.0], np.float32)
+    C1 = np.concatenate([to_bf16(g), to_bf16(u)])[None, :]
+    h = f64(orc.silu_mul(C1, np.zeros(1, np.int32), 1)[0])
+    assert h[0] == 0.0                      # silu(0) = 0
+    assert h[1] == f64(to_bf16([100.0 * 0.5]))[0]   # silu(g) -> g for large g
+    assert h[2] == 0.0                      # silu(g) -> 0 for very negative g
+    assert h[3] == 0.0                      # u = 0
+    assert h[4] == f64(to_bf16([-5.0 * expit(5.0)]))[0]
+
+
+# --- combine ----------------------------------------------------------------
+
+def test_combine_one_hot_and_nonlocal(orc):
+    """A one-hot weight reproduces that pair's row exactly; tokens with no local
+    pair give +0; non-local pairs never contribute even with a weight."""
+    T, topk, E, H = 6, 4, 5, 64
+    C2 = wl.random_bf16(41, (T * topk, H))
+    ids = wl.random_ids(42, T, topk, E)
+    ids[5, :] = -1
+    w = np.zeros((T, topk), np.float32)
+    pick = np.array([0, 1, 2, 3, 1, 0])
+    w[np.arange(T), pick] = 1.0
+    ids[2, 0] = -1            # weight on a non-local pair must not count
+    w[2, 0] = 5.0
+    out = orc.combine(C2, ids, w, E)
+    for t in range(5):
+        np.testing.assert_array_equal(out[t], C2[t * topk + pick[t]])
+    assert (out[5] == 0).all()
+
+
+def test_combine_float_bound(orc):
+    T, topk, E, H = 10, 8, 16, 128
+    C2 = wl.random_bf16(51, (T * topk, H), std=50.0)
+    ids = wl.random_ids(52, T, topk, E, p_nonlocal=0.3)
+    w = wl.random_weights(53, T, topk)
+    out = f64(orc.combine(C2, ids, w, E))
+    Y = f64(C2).reshape(T, topk, H)
+    mask = (ids >= 0)[:, :, None]
+    ref = (w.astype(np.float64)[:, :, None] * Y * mask).sum(1)
+    mag = (np.abs(w.astype(np.float64))[:, :, None] * np.abs(Y) * mask).sum(1)
+    assert (np.abs(out - ref) <= np.abs(ref) * 2.0 ** -8 + topk * 2.0 ** -23 * mag + 1e-30).all()
+
+
+# --- layer ------------------------------------------------------------------
+
+def layer_dense_reference(x, ids, w, c13, s13, c2, s2, E):
+    """Dense per-token loop over each token's experts in float64, with bf16
+    rounding (torch) after gate_up, after SiLU*up and after down."""
+    W13 = f64(dequant_ref(c13, s13))
+    W2 = f64(dequant_ref(c2, s2))
+    X = f64(x)
+    T, topk = ids.shape
+    I = c2.shape[2]
+    out = np.zeros((T, X.shape[1]))
+    for t in range(T):
+        acc = np.zeros(X.shape[1])
+        for k in range(topk):
+            e = ids[t, k]
+            if not 0 <= e < E:
+                continue
+            gu = bf16r(W13[e] @ X[t])
+            h = bf16r(gu[:I] * expit(gu[:I]) * gu[I:])
+            y = bf16r(W2[e] @ h)
+            acc += float(w[t, k]) * y
+        out[t] = bf16r(acc)
+    return out
+
+
+def test_layer_tiny_vs_dense_loop(orc):
+    w = wl.TINY
+    ids, wts = wl.make_routing(w)
+    x = wl.make_x(w)
+    c13, s13 = wl.make_w13(w)
+    c2, s2 = wl.make_w2(w)
+    got = f64(orc.moe_layer(x, ids, wts, (c13, s13), (c2, s2), w.E, block_m=4))
+    ref = layer_dense_reference(x, ids, wts, c13, s13, c2, s2, w.E)
+    err = np.abs(got - ref)
+    assert (err <= 1e-2 + 1e-2 * np.abs(ref)).all(), err.max()
+    # the two differ only by FP32-vs-FP64 summation order near rounding ties
+    assert np.mean(got == ref) > 0.9
+
+
+def test_layer_block_m_invariance(orc):
+    """The layer result does not depend on the align block size."""
+    w = wl.TINY
+    ids, wts = wl.make_routing(w)
+    x = wl.make_x(w)
+    w13, w2 = wl.make_w13(w), wl.make_w2(w)
+    a = orc.moe_layer(x, ids, wts, w13, w2, w.E, block_m=1)
+    b = orc.moe_layer(x, ids, wts, w13, w2, w.E, block_m=16)
+    np.testing.assert_array_equal(a, b)
