@@ -1,0 +1,448 @@
+"""Benchmark of the W4A16 INT4 MoE expert layer on GB300 (one JSON line).
+
+A step is one pass of the whole hot path over one batch: moe_align ->
+gate_up GEMM -> SiLU*up -> down GEMM -> top-k combine, every step of it a
+libchord.so kernel launched through the C ABI.  The default workload is the
+Kimi-K2-shaped EP8 decode layer (48 local experts of 384, T = 512 tokens,
+top-8, H = 7168, I = 2048); ``--workload`` picks another of the five.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Under torchrun (N > 1) every rank runs an independent replica of the same
+expert-parallel share (the EP8 configs are one GPU's slice of the experts);
+no data crosses ranks; the reported value is the max-over-ranks time divided
+by the calls all ranks made.  ``--impl reference`` times the CPU oracle on
+the host cores instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "W4A16 MoE µs/call; achieved HBM GB/s (decode) & BF16 TFLOP/s (prefill)"
+UNIT = "µs/call"
+WORKLOADS = {
+    "ep8_decode": wl.EP8_DECODE, "ep8_prefill": wl.EP8_PREFILL, "skewed": wl.SKEWED, "tiny": wl.TINY,
+    **{f"tp8_T{t}": wl.tp8(t) for t in wl.TP8_T},
+}
+L2_BYTES = 129 * 2 ** 20
+KERNEL_SRC = {
+    "decode": os.path.join(ROOT, "w4a16_int4_mixture_moe_gb300", "csrc", "chord_gemm_decode.cu"),
+    "prefill": os.path.join(ROOT, "w4a16_int4_mixture_moe_gb300", "csrc", "chord_gemm_prefill.cu"),
+}
+
+
+# ----------------------------------------------------------------- accounting
+
+def routing_stats(ids, E):
+    flat = ids.ravel()
+    local = flat[(flat >= 0) & (flat < E)]
+    rows_per_expert = np.bincount(local, minlength=E)
+    return rows_per_expert
+
+
+def gemm_algorithmic(rows_per_expert, N, K):
+    """Bytes and FLOPs one GEMM launch must move / do: packed INT4 + scales of
+    every expert with at least one row, activations read, outputs written,
+    sorted ids read; FLOPs over real rows only."""
+    rows = int(rows_per_expert.sum())
+    used = int((rows_per_expert > 0).sum())
+    wbytes = used * N * K * 9 // 16
+    nbytes = wbytes + rows * K * 2 + rows * N * 2 + rows * 4
+    flops = 2 * rows * N * K
+    return nbytes, flops
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "src": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "src": "fallback"}
+
+
+def kernel_sha(kind):
+    h = hashlib.sha256()
+    for p in (KERNEL_SRC[kind], os.path.join(os.path.dirname(KERNEL_SRC[kind]), "chord_common.cuh")):
+        h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kind, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{kind}_gemm_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m_sha = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", txt)
+    m_b = re.search(r"dram_bytes_per_launch_gate_up:\s*([0-9.eE+]+)", txt)
+    if not (m_sha and m_b) or m_sha.group(1) != kernel_sha(kind):
+        return None
+    return float(m_b.group(1))
+
+
+# --------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons around a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.samples = []
+        self.proc = None
+        self.gpu_id = gpu_id
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", self.gpu_id], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+        t0 = time.time()
+        while not self.samples and time.time() - t0 < 5:
+            time.sleep(0.02)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t_lo, t_hi):
+        win = [p for t, p in self.samples if t_lo - 0.25 <= t <= t_hi + 0.25]
+        if not win and self.samples:  # region shorter than the sampling period: nearest samples
+            win = [min(self.samples, key=lambda s: abs(s[0] - (t_lo + t_hi) / 2))[1]]
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in win if num(p[1]) is not None]
+        mx = [num(p[2]) for p in win if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for p in win for n, v in zip(names, p[5:9]) if v.strip().lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(win)}
+
+
+def gpu_id_for(torch, dev):
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        return vis.split(",")[dev] if vis else str(dev)
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def oracle_sample(w, target_s, nthreads=None):
+    """Time the oracle layer on a token sample sized to about target_s seconds;
+    return (us per full call, sample description, cores, seconds per sample)."""
+    import oracle
+    oracle.build()
+    ids, wts = wl.make_routing(w)
+    x = wl.make_x(w)
+    w13, w2 = wl.make_w13(w), wl.make_w2(w)
+    cores = oracle.threads(nthreads)
+    local = (ids >= 0) & (ids < w.E)
+    total_pairs = int(local.sum())
+
+    def run(nt):
+        t0 = time.perf_counter()
+        oracle.moe_layer(x[:nt], ids[:nt], wts[:nt], w13, w2, w.E, block_m=8, nthreads=cores)
+        return time.perf_counter() - t0
+
+    nt = min(w.T, 4)
+    dt = run(nt)
+    while nt < w.T and dt < target_s / 4:
+        nt = min(w.T, nt * 4)
+        dt = run(nt)
+    pairs = int(local[:nt].sum())
+    us_full = dt * 1e6 * (total_pairs / max(pairs, 1))
+    desc = (f"oracle layer on the first {nt} of {w.T} tokens ({pairs} of {total_pairs} local pairs), "
+            f"{dt:.2f} s; scaled to the full call by local pairs")
+    return us_full, desc, cores, dt, nt
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    steps, warmup = args.steps, args.warmup
+    budget = 150.0
+    per_step = max(0.5, min(20.0, budget / max(1, steps + warmup)))
+    us0, desc, cores, dt, nt = oracle_sample(w, per_step)
+    import oracle
+    ids, wts = wl.make_routing(w)
+    x = wl.make_x(w)
+    w13, w2 = wl.make_w13(w), wl.make_w2(w)
+    local = (ids >= 0) & (ids < w.E)
+    scale = local.sum() / max(1, local[:nt].sum())
+    for _ in range(warmup):
+        oracle.moe_layer(x[:nt], ids[:nt], wts[:nt], w13, w2, w.E, block_m=8, nthreads=cores)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle.moe_layer(x[:nt], ids[:nt], wts[:nt], w13, w2, w.E, block_m=8, nthreads=cores)
+    el = time.perf_counter() - t0
+    us = el / max(steps, 1) * 1e6 * scale
+    line = {"impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": UNIT, "n_gpus": args.gpus,
+            "steps": steps, "warmup": warmup, "ms_per_step": round(el / max(steps, 1) * 1e3, 3),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": {"workload": w.name},
+            "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------- GPU arm
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="ep8_decode", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="chord", choices=["chord", "reference"])
+    ap.add_argument("--block-m", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    args.warmup = max(args.warmup, 3)
+
+    import torch
+    import w4a16_int4_mixture_moe_gb300 as chord
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    chord.build()
+    chord.load()
+
+    # ---- inputs (seeded, synthetic), weights packed once (offline step)
+    ids, wts = wl.make_routing(w)
+    x = wl.make_x(w)
+    c13, s13 = wl.make_w13(w)
+    p13 = torch.empty(chord.chord_packed_weight_bytes(w.E, 2 * w.I, w.H), dtype=torch.uint8, device=dev)
+    chord.chord_pack_weights(torch.from_numpy(c13).to(dev),
+                             torch.from_numpy(s13.view(np.int16)).to(dev).view(torch.bfloat16), p13)
+    del c13, s13
+    c2, s2 = wl.make_w2(w)
+    p2 = torch.empty(chord.chord_packed_weight_bytes(w.E, w.H, w.I), dtype=torch.uint8, device=dev)
+    chord.chord_pack_weights(torch.from_numpy(c2).to(dev),
+                             torch.from_numpy(s2.view(np.int16)).to(dev).view(torch.bfloat16), p2)
+    del c2, s2
+    torch.cuda.synchronize()
+
+    T, topk, E, H, I = w.T, w.topk, w.E, w.H, w.I
+    P = T * topk
+    bm = args.block_m or chord.chord_select_block_m(T, topk, E, w.E_global, 2 * I, H)
+    cap = chord.chord_align_capacity(T, topk, E, bm)
+    xd = torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
+    idd = torch.from_numpy(ids).to(dev)
+    wd = torch.from_numpy(wts).to(dev)
+    sorted_ids = torch.empty(cap, dtype=torch.int32, device=dev)
+    expert_ids = torch.empty(cap // bm, dtype=torch.int32, device=dev)
+    ntp = torch.empty(1, dtype=torch.int32, device=dev)
+    aws = torch.empty(max(4, chord.chord_align_workspace_bytes(T, topk, E)), dtype=torch.uint8, device=dev)
+    C1 = torch.empty((P, 2 * I), dtype=torch.bfloat16, device=dev)
+    h = torch.empty((P, I), dtype=torch.bfloat16, device=dev)
+    C2 = torch.empty((P, H), dtype=torch.float32, device=dev)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    f32_out = chord.ChordOpts(out_dtype=chord.DTYPE_F32)
+
+    def step(timed_gemms=None):
+        chord.chord_moe_align(idd, E, bm, sorted_ids, expert_ids, ntp, aws, stream=stream)
+        if timed_gemms is not None:
+            ev[0].record(stream)
+        chord.chord_w4a16_moe_gemm(xd, topk, p13, E, 2 * I, H, sorted_ids, expert_ids, ntp, bm, P, C1,
+                                   stream=stream)
+        if timed_gemms is not None:
+            ev[1].record(stream)
+        chord.chord_silu_mul(C1, idd, E, h, stream=stream)
+        if timed_gemms is not None:
+            ev[2].record(stream)
+        chord.chord_w4a16_moe_gemm(h, 1, p2, E, H, I, sorted_ids, expert_ids, ntp, bm, P, C2, opts=f32_out,
+                                   stream=stream)
+        if timed_gemms is not None:
+            ev[3].record(stream)
+        chord.chord_moe_combine(C2, idd, wd, E, out, stream=stream)
+
+    launches_per_step = (3 if P > 0 else 2) + 4
+
+    def barrier():
+        if pg:
+            pg.barrier()
+        torch.cuda.synchronize()
+
+    # ---- device-resident timing of the whole step
+    for _ in range(args.warmup):
+        step()
+    assert chord.chord_get_device_error(stream) == 0
+    sampler = ClockSampler(gpu_id_for(torch, local_rank))
+    sampler.start()
+    barrier()
+    t_lo = time.time()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    barrier()
+    t_hi = time.time()
+    sampler.stop()
+    total_ms = e0.elapsed_time(e1)
+
+    # ---- per-GEMM durations, measured live with events on the launching stream
+    g1 = g2 = 0.0
+    nrep = max(1, min(args.steps, 200))
+    for _ in range(nrep):
+        step(timed_gemms=True)
+        ev[3].synchronize()
+        g1 += ev[0].elapsed_time(ev[1])
+        g2 += ev[2].elapsed_time(ev[3])
+    g1 /= nrep
+    g2 /= nrep
+
+    # ---- end to end through the public layer call, host buffers, copies timed
+    x_h = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    ids_h = torch.from_numpy(ids).pin_memory()
+    w_h = torch.from_numpy(wts).pin_memory()
+    out_h = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    lws = torch.empty(chord.chord_layer_workspace_bytes(T, topk, E, H, I, bm), dtype=torch.uint8, device=dev)
+    x_e, ids_e, w_e = torch.empty_like(xd), torch.empty_like(idd), torch.empty_like(wd)
+
+    def e2e_step():
+        x_e.copy_(x_h, non_blocking=True)
+        ids_e.copy_(ids_h, non_blocking=True)
+        w_e.copy_(w_h, non_blocking=True)
+        chord.chord_moe_layer(x_e, ids_e, w_e, E, w.E_global, I, p13, p2, lws, out, block_m=bm, stream=stream)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    barrier()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    f1.record(stream)
+    barrier()
+    e2e_ms = f0.elapsed_time(f1)
+    assert chord.chord_get_device_error(stream) == 0
+
+    if pg:
+        t = torch.tensor([total_ms, e2e_ms], device=dev, dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms, e2e_ms = float(t[0]), float(t[1])
+
+    us_per_call = total_ms * 1e3 / args.steps / world
+    e2e_us = e2e_ms * 1e3 / args.steps / world
+
+    rpe = routing_stats(ids, E)
+    b1, f1_ = gemm_algorithmic(rpe, 2 * I, H)
+    b2, f2_ = gemm_algorithmic(rpe, H, I)
+    peaks = load_peaks()
+    tok_e = float(rpe.sum()) / E
+    regime = "prefill" if (bm > 64 and chord_prefill(chord)) else "decode"
+    if regime == "decode":
+        ach = b1 / (g1 * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": profiled_traffic("decode", w.name),
+                "kernel": "gemm_decode_kernel (gate_up)", "peak_src": peaks["src"]}
+    else:
+        ach = f1_ / (g1 * 1e-3) / 1e12
+        pk = peaks["bf16_tflops_sustained"]
+        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": pk, "unit": "TFLOP/s",
+                "frac": round(ach / pk, 4), "traffic": profiled_traffic("prefill", w.name),
+                "kernel": "gemm_prefill_kernel (gate_up)", "peak_src": peaks["src"]}
+    clk = sampler.summary(t_lo, t_hi)
+    line = {
+        "metric": METRIC, "value": round(us_per_call, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "T": T, "E_local": E, "E_global": w.E_global, "topk": topk, "H": H,
+                   "I": I, "block_m": bm, "regime": regime, "local_pairs": int(rpe.sum()),
+                   "tok_e": round(tok_e, 2), "parallelism": f"ep-replica x{world}",
+                   "l2": f"inputs larger than L2: {(p13.numel() + p2.numel()) / 1e6:.0f} MB of packed weights "
+                         f"streamed per step vs {L2_BYTES / 1e6:.0f} MB L2"},
+        "gemm_us": {"gate_up": round(g1 * 1e3, 2), "down": round(g2 * 1e3, 2)},
+        "gemm_achieved": {
+            "gate_up_GBps": round(b1 / (g1 * 1e-3) / 1e9, 1), "down_GBps": round(b2 / (g2 * 1e-3) / 1e9, 1),
+            "gate_up_TFLOPs": round(f1_ / (g1 * 1e-3) / 1e12, 2), "down_TFLOPs": round(f2_ / (g2 * 1e-3) / 1e12, 2),
+            "gate_up_bytes": b1, "down_bytes": b2, "gate_up_flops": f1_, "down_flops": f2_},
+        "roofline": roof,
+        "clocks": clk,
+        "e2e": {"value": round(e2e_us, 2), "unit": UNIT, "h2d_bytes_per_step": x.nbytes + ids.nbytes + wts.nbytes,
+                "d2h_bytes_per_step": T * H * 2},
+        "gpu_launches": launches_per_step * args.steps,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        us_cpu, desc, cores, _, _ = oracle_sample(w, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(us_cpu, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+def chord_prefill(chord):
+    """True when the library routes block sizes above 64 to the tensor-core kernel."""
+    return chord.chord_select_block_m(8192, 8, 48, 384, 4096, 7168) > 64
+
+
+if __name__ == "__main__":
+    main()

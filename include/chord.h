@@ -1,0 +1,245 @@
+/*
+ * chord.h - C ABI of the GB300 (sm_103a) W4A16 INT4 mixture-of-experts library.
+ *
+ * The operation is the expert GEMM of a mixture-of-experts layer with BF16
+ * activations and INT4 weights ("vLLM x Novita AI: Chord, a faster INT4 MoE
+ * for Kimi K2.x"):
+ *   - weights are unsigned 4-bit codes q (offset 8) with one BF16 scale s per
+ *     group of 32 consecutive K elements; a weight's value is
+ *     bf16_rne((q - 8) * s), subtract first, then scale (section "H200 and
+ *     Blackwell indexed decode"; logical shapes codes [G, N, K] and scales
+ *     [G, N, K/32] from the grouped operator example in section "Grouped SM90
+ *     kernels");
+ *   - routed rows reach the GEMM through vLLM's moe_align_block_size buffers
+ *     sorted_ids / expert_ids / num_tokens_padded; activations are never
+ *     padded, padding lives in the index arrays as sentinels (section "Grouped
+ *     SM90 kernels", figure 3 "where padding lives"); the buffers are
+ *     over-allocated so no routed count is read back to the host and every
+ *     call can be captured in a CUDA graph (deployment notes);
+ *   - accumulation is FP32 (the F16-accumulation option is not implemented,
+ *     deployment notes), outputs are BF16.
+ *
+ * Conventions for every call:
+ *   - All tensor arguments are DEVICE pointers owned by the caller; the
+ *     library never allocates device memory.  Sizes are element counts unless
+ *     named *_bytes.  Matrices are row-major and densely packed.
+ *   - BF16 buffers are passed as void* holding IEEE bfloat16 bit patterns.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every
+ *     call only enqueues work on it and returns without synchronising, except
+ *     chord_get_device_error and calls made with opts->validate != 0.
+ *   - Argument errors are reported synchronously through the return value,
+ *     before anything is enqueued.  Unsupported configurations (a group size
+ *     other than 32, N not a multiple of 16 or K not a multiple of 64) return
+ *     CHORD_ERR_UNSUPPORTED; nothing ever falls back to another kernel.
+ *   - Problems found on the device (an expert id or pair id out of range, a
+ *     packed blob whose header does not match the call, a pipeline wait that
+ *     ran out) set a sticky per-device error word and the affected work is
+ *     skipped; read and clear it with chord_get_device_error.
+ *   - Pointers passed as A, C, x, out and the packed blob must be 16-byte
+ *     aligned.
+ */
+#ifndef CHORD_H
+#define CHORD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum chord_status {
+    CHORD_OK = 0,
+    CHORD_ERR_INVALID_ARG = 1,       /* null pointer, negative size, misaligned pointer */
+    CHORD_ERR_UNSUPPORTED = 2,       /* shape or option this library does not implement */
+    CHORD_ERR_LAYOUT_MISMATCH = 3,   /* packed blob size does not match E, N, K */
+    CHORD_ERR_BUFFER_TOO_SMALL = 4,  /* a capacity or workspace below the required size */
+    CHORD_ERR_CUDA = 5,              /* a CUDA runtime call failed */
+    CHORD_ERR_DEVICE_VALIDATION = 6, /* validate mode: the device found bad routing or a bad blob */
+    CHORD_ERR_TIMEOUT = 7            /* validate mode: a bounded device wait gave up */
+} chord_status;
+
+/* Device error word values (chord_get_device_error). */
+#define CHORD_DEV_OK 0
+#define CHORD_DEV_BAD_EXPERT 1   /* topk_ids / expert_ids entry outside its range */
+#define CHORD_DEV_BAD_ROW 2      /* sorted_ids entry neither a pair id nor the sentinel */
+#define CHORD_DEV_BAD_HEADER 3   /* packed blob header does not describe (E, N, K) */
+#define CHORD_DEV_TIMEOUT 4      /* a pipeline wait exceeded its bound */
+#define CHORD_DEV_BAD_CODE 5     /* pack: a code above 15 */
+#define CHORD_DEV_BAD_PADDED 6   /* num_tokens_padded above capacity or not a multiple of block_m */
+
+typedef enum chord_regime {
+    CHORD_REGIME_AUTO = 0,     /* from block_m: <= 64 decode, larger prefill */
+    CHORD_REGIME_DECODE = 1,   /* HBM-streaming kernel, tokens in the MMA N dimension */
+    CHORD_REGIME_PREFILL = 2   /* tensor-core kernel (tcgen05, accumulators in TMEM) */
+} chord_regime;
+
+typedef enum chord_dtype {
+    CHORD_DTYPE_BF16 = 0,
+    CHORD_DTYPE_F32 = 1
+} chord_dtype;
+
+typedef struct chord_opts {
+    int32_t regime;      /* chord_regime */
+    int32_t validate;    /* nonzero: synchronise after the call and turn a set device
+                            error word into CHORD_ERR_DEVICE_VALIDATION / _TIMEOUT
+                            ("trusted routing validation" of the deployment notes) */
+    int32_t split_k;     /* 0 = automatic, 1 = off, > 1 = number of K slices (decode) */
+    int32_t out_dtype;   /* GEMM output: CHORD_DTYPE_BF16 (default) or CHORD_DTYPE_F32,
+                            the FP32 sums unrounded (for a consumer that keeps FP32) */
+    int32_t reserved[4]; /* must be zero */
+} chord_opts;
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int chord_version(void);
+
+/* Human-readable name of a status. Never NULL. */
+const char *chord_status_string(chord_status status);
+
+/* ---------------------------------------------------------------- packing */
+
+/* Bytes of the packed blob for E experts of an N x K weight: a 256-byte header
+ * followed by E * N * K * 9 / 16 bytes (4-bit codes plus one BF16 scale per 32
+ * codes).  Returns 0 when N % 16 or K % 64 is nonzero or a size is not
+ * positive.  The byte layout (layout 1) is the one written out in the
+ * library's packer; it places each 16 x 16 block of codes so that one 32-bit
+ * load per lane yields a tensor-core A fragment. */
+size_t chord_packed_weight_bytes(int E, int N, int K);
+
+/* Offline packing of canonical weights into the sm_103a layout (the article's
+ * pack step, section "Grouped SM90 kernels": weights are prepared once at load
+ * time and the prepared layout is checked when it is used).
+ *   codes   device uint8 [E, N, K], each 0..15 (uint4, offset 8)
+ *   scales  device bf16 [E, N, K / group_size]
+ *   packed  device output of packed_bytes >= chord_packed_weight_bytes(E, N, K)
+ * group_size must be 32.  A code above 15 sets CHORD_DEV_BAD_CODE. */
+chord_status chord_pack_weights(const uint8_t *codes, const void *scales, int E, int N, int K,
+                                int group_size, void *packed, size_t packed_bytes, void *stream);
+
+/* ---------------------------------------------------------------- routing */
+
+/* Length of sorted_ids for moe_align_block_size: round_up(P + min(E, P) *
+ * (block_m - 1), block_m) with P = T * topk; expert_ids has capacity / block_m
+ * entries.  Returns -1 on bad arguments. */
+int64_t chord_align_capacity(int T, int topk, int E, int block_m);
+
+/* Scratch bytes chord_moe_align needs (per-slice expert histograms). */
+size_t chord_align_workspace_bytes(int T, int topk, int E);
+
+/* moe_align_block_size (the indexed routing contract of the article's
+ * indexed family, section "Two kernel families", and figure 3):
+ *   topk_ids  device int32 [T, topk]; entry e in [0, E) routes pair
+ *             p = t * topk + k to local expert e; -1 marks an expert that
+ *             lives on another GPU (dropped here, and in the combine).
+ *   sorted_ids  device int32 [capacity]: for e = 0..E-1 the pair ids routed
+ *             to e in ascending order, padded with the sentinel T * topk to a
+ *             multiple of block_m; an expert with no pair gets no block;
+ *             entries past num_tokens_padded hold the sentinel.
+ *   expert_ids  device int32 [capacity / block_m]: expert of each block, -1
+ *             past num_tokens_padded / block_m.
+ *   num_tokens_padded  device int32 [1].
+ * The result is unique (bit-for-bit deterministic).  1 <= block_m <= 256,
+ * E <= 1024.  With opts->validate, an id outside [-1, E) is reported; without
+ * it such ids are dropped like -1. */
+chord_status chord_moe_align(const int32_t *topk_ids, int T, int topk, int E, int block_m,
+                             int32_t *sorted_ids, int32_t *expert_ids,
+                             int32_t *num_tokens_padded, int64_t capacity,
+                             void *workspace, size_t workspace_bytes,
+                             const chord_opts *opts, void *stream);
+
+/* Host-side block size choice from tokens per expert (the article's tok_e =
+ * routed rows / experts rule, section "Indexed kernels"): tok_e = T * topk /
+ * E_global is the expected number of rows per local expert, known without
+ * reading anything back.  Small tok_e gives a decode block (8..64), large
+ * tok_e a prefill block.  Always returns a valid block_m. */
+int chord_select_block_m(int T, int topk, int E_local, int E_global, int N, int K);
+
+/* ------------------------------------------------------------------- GEMM */
+
+/* Scratch bytes chord_w4a16_moe_gemm needs for the given call shape (split-K
+ * partial sums); 0 when the chosen schedule needs none. */
+size_t chord_gemm_workspace_bytes(int64_t num_pairs, int N, int K, int block_m,
+                                  const chord_opts *opts);
+
+/* Indexed W4A16 grouped GEMM, one projection (gate_up or down):
+ *   C[p, n] = bf16_rne( sum_k A[p / a_row_divisor, k] * w[e, n, k] )
+ * for every block b < num_tokens_padded / block_m, e = expert_ids[b], and every
+ * pair id p != num_pairs in sorted_ids[b * block_m .. + block_m); w is the
+ * dequantised weight bf16_rne((q - 8) * s); the sum is FP32.
+ *   A        device bf16 [a_rows, K]; a_row_divisor = topk when A has one row
+ *            per token (gate_up), 1 when it has one row per pair (down).
+ *   packed   blob from chord_pack_weights for (E, N, K).
+ *   C        device bf16 [num_pairs, N] (float [num_pairs, N] with
+ *            opts->out_dtype = CHORD_DTYPE_F32, the sum left unrounded);
+ *            rows no block names are not written.
+ *   capacity length of sorted_ids (expert_ids has capacity / block_m entries).
+ * block_m must equal the value given to chord_moe_align and be a multiple of 8
+ * (decode regime: <= 64; prefill regime: a multiple of 16, <= 256). */
+chord_status chord_w4a16_moe_gemm(const void *A, int64_t a_rows, int a_row_divisor,
+                                  const void *packed, size_t packed_bytes, int E, int N, int K,
+                                  const int32_t *sorted_ids, const int32_t *expert_ids,
+                                  const int32_t *num_tokens_padded, int64_t capacity,
+                                  int block_m, int64_t num_pairs, void *C,
+                                  void *workspace, size_t workspace_bytes,
+                                  const chord_opts *opts, void *stream);
+
+/* ------------------------------------------------------------- epilogues */
+
+/* SiLU * up on the gate_up output:
+ *   h[p, j] = bf16_rne( g / (1 + exp(-g)) * u ),  g = C1[p, j], u = C1[p, I + j]
+ * (FP32 math), for every pair p whose topk_ids entry is a local expert.
+ *   C1  device bf16 [P, 2 * I] (gate in columns 0..I-1, up in I..2I-1)
+ *   h   device bf16 [P, I];  P = T * topk; I % 8 == 0. */
+chord_status chord_silu_mul(const void *C1, const int32_t *topk_ids, int64_t P, int E, int I,
+                            void *h, void *stream);
+
+/* Top-k weighted combine (gather of each token's pair rows, weighted sum):
+ *   out[t, n] = bf16_rne( sum over k ascending with topk_ids[t, k] in [0, E) of
+ *                         topk_w[t, k] * C2[t * topk + k, n] ),  FP32, from +0,
+ *               each product and each sum rounded separately (no fused multiply-add)
+ *   C2 device [T * topk, H] of c2_dtype (CHORD_DTYPE_BF16 or CHORD_DTYPE_F32),
+ *   topk_w device float [T, topk], out bf16 [T, H];
+ * tokens with no local pair get +0.  H % 8 == 0. */
+chord_status chord_moe_combine(const void *C2, int c2_dtype, const int32_t *topk_ids,
+                               const float *topk_w, int T, int topk, int E, int H, void *out,
+                               void *stream);
+
+/* ------------------------------------------------------------------ layer */
+
+/* Scratch bytes chord_moe_layer needs for this shape and block_m (0 = the
+ * block size chord_select_block_m picks with E_global = E). */
+size_t chord_layer_workspace_bytes(int T, int topk, int E, int H, int I, int block_m);
+
+/* One MoE expert layer on this GPU's E local experts:
+ *   align -> gate_up GEMM (x rows gathered by pair id / topk) -> SiLU * up
+ *   -> down GEMM -> top-k weighted combine, BF16 out [T, H].
+ * The gate_up result and SiLU * up are rounded to BF16 (the GEMM output type
+ * and the BF16 activation operand of the down GEMM); the down projection's
+ * FP32 sums enter the weighted top-k sum unrounded and the output is rounded
+ * to BF16 once.
+ *   x          device bf16 [T, H]
+ *   topk_ids   device int32 [T, topk] (local id or -1), topk_w device float [T, topk]
+ *   packed_w13 blob for (E, 2 * I, H): rows 0..I-1 gate, I..2I-1 up
+ *   packed_w2  blob for (E, H, I)
+ *   E_global   number of experts the router chooses from (for tok_e)
+ *   block_m    0 = chord_select_block_m(T, topk, E, E_global, 2 * I, H)
+ *   workspace  >= chord_layer_workspace_bytes(T, topk, E, H, I, block_m) bytes
+ * Tokens with no local pair get +0 (this GPU's partial sum of the layer). */
+chord_status chord_moe_layer(const void *x, const int32_t *topk_ids, const float *topk_w,
+                             int T, int topk, int E, int E_global, int H, int I,
+                             const void *packed_w13, size_t w13_bytes,
+                             const void *packed_w2, size_t w2_bytes, int block_m,
+                             void *workspace, size_t workspace_bytes, void *out,
+                             const chord_opts *opts, void *stream);
+
+/* ------------------------------------------------------------------ errors */
+
+/* Synchronises `stream`, returns the current device's sticky error word in
+ * *code (CHORD_DEV_*) and clears it. */
+chord_status chord_get_device_error(void *stream, int32_t *code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CHORD_H */

@@ -83,8 +83,11 @@ def lib():
                 "orc_moe_align": (c_int, [i32p, c_int, c_int, c_int, c_int, i32p, i32p, i32p, c_i64]),
                 "orc_moe_gemm": (c_int, [u16p, c_i64, c_int, u8p, u16p, c_int, c_int, c_int,
                                          i32p, i32p, ctypes.c_int32, c_int, c_i64, u16p, c_int]),
+                "orc_moe_gemm_f32": (c_int, [u16p, c_i64, c_int, u8p, u16p, c_int, c_int, c_int,
+                                             i32p, i32p, ctypes.c_int32, c_int, c_i64, f32p, c_int]),
                 "orc_silu_mul": (c_int, [u16p, i32p, c_i64, c_int, c_int, u16p, c_int]),
                 "orc_combine": (c_int, [u16p, i32p, f32p, c_int, c_int, c_int, c_int, u16p, c_int]),
+                "orc_combine_f32": (c_int, [f32p, i32p, f32p, c_int, c_int, c_int, c_int, u16p, c_int]),
                 "orc_moe_layer": (c_int, [u16p, i32p, f32p, c_int, c_int, c_int, c_int, c_int,
                                           u8p, u16p, u8p, u16p, c_int, u16p, c_int]),
             }
@@ -214,6 +217,28 @@ def moe_gemm(A: np.ndarray, a_row_divisor: int, codes: np.ndarray, scales: np.nd
     return C
 
 
+def moe_gemm_f32(A: np.ndarray, a_row_divisor: int, codes: np.ndarray, scales: np.ndarray,
+                 sorted_ids: np.ndarray, expert_ids: np.ndarray, num_tokens_padded: int,
+                 block_m: int, num_pairs: int, C: np.ndarray = None, nthreads=None) -> np.ndarray:
+    """As moe_gemm, but C holds the FP32 sums unrounded (float32 [num_pairs, N])."""
+    A = _c(A, np.uint16)
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.uint16)
+    E, N, K = codes.shape
+    assert A.shape[1] == K
+    sorted_ids = _c(sorted_ids, np.int32)
+    expert_ids = _c(expert_ids, np.int32)
+    if C is None:
+        C = np.zeros((max(num_pairs, 1), N), np.float32)[:num_pairs]
+    C = _c(C, np.float32)
+    _check(lib().orc_moe_gemm_f32(_ptr(A, ctypes.c_uint16), A.shape[0], a_row_divisor,
+                                  _ptr(codes, ctypes.c_uint8), _ptr(scales, ctypes.c_uint16), E, N, K,
+                                  _ptr(sorted_ids, ctypes.c_int32), _ptr(expert_ids, ctypes.c_int32),
+                                  num_tokens_padded, block_m, num_pairs, _ptr(C, ctypes.c_float),
+                                  threads(nthreads)), "moe_gemm_f32")
+    return C
+
+
 def silu_mul(C1: np.ndarray, topk_ids: np.ndarray, E: int, h: np.ndarray = None, nthreads=None):
     C1 = _c(C1, np.uint16)
     ids = _c(topk_ids, np.int32).ravel()
@@ -227,15 +252,23 @@ def silu_mul(C1: np.ndarray, topk_ids: np.ndarray, E: int, h: np.ndarray = None,
 
 
 def combine(C2: np.ndarray, topk_ids: np.ndarray, topk_w: np.ndarray, E: int, nthreads=None):
-    C2 = _c(C2, np.uint16)
+    """C2 as bf16 bits (uint16) or float32; returns bf16 bits [T, H]."""
+    C2 = np.ascontiguousarray(C2)
     ids = _c(topk_ids, np.int32)
     w = _c(topk_w, np.float32)
     T, topk = ids.shape
     H = C2.shape[1]
     out = np.empty((T, H), np.uint16)
-    _check(lib().orc_combine(_ptr(C2, ctypes.c_uint16), _ptr(ids, ctypes.c_int32),
-                             _ptr(w, ctypes.c_float), T, topk, E, H, _ptr(out, ctypes.c_uint16),
-                             threads(nthreads)), "combine")
+    if C2.dtype == np.float32:
+        rc = lib().orc_combine_f32(_ptr(C2, ctypes.c_float), _ptr(ids, ctypes.c_int32),
+                                   _ptr(w, ctypes.c_float), T, topk, E, H, _ptr(out, ctypes.c_uint16),
+                                   threads(nthreads))
+    else:
+        C2 = _c(C2, np.uint16)
+        rc = lib().orc_combine(_ptr(C2, ctypes.c_uint16), _ptr(ids, ctypes.c_int32),
+                               _ptr(w, ctypes.c_float), T, topk, E, H, _ptr(out, ctypes.c_uint16),
+                               threads(nthreads))
+    _check(rc, "combine")
     return out
 
 

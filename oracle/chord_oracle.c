@@ -29,7 +29,9 @@
  *             deployment notes), BF16 output.
  *   act       h = bf16_rne( silu(g) * u ), gate rows 0..I-1, up rows I..2I-1.
  *   combine   out[t, n] = bf16_rne( sum over local k, ascending, of
- *             w[t, k] * C2[t * topk + k, n] ).
+ *             w[t, k] * C2[t * topk + k, n] ), C2 in bf16 or binary32.
+ *   layer     the steps above, with the down projection's FP32 sums fed to
+ *             the combine unrounded (see orc_moe_layer).
  *   pack      the byte layout the CUDA library reads (its own specification,
  *             written out below), so the GPU packer can be checked byte for
  *             byte; and its inverse.
@@ -323,10 +325,12 @@ static void dequant_expert(const uint8_t *codes, const uint16_t *scales, int e, 
         }
 }
 
-int orc_moe_gemm(const uint16_t *A, int64_t a_rows, int a_row_divisor,
-                 const uint8_t *codes, const uint16_t *scales, int E, int N, int K,
-                 const int32_t *sorted_ids, const int32_t *expert_ids, int32_t num_tokens_padded,
-                 int block_m, int64_t num_pairs, uint16_t *C, int nthreads)
+/* Shared body of the two output precisions: exactly one of Cb (bf16, one
+ * rounding of the FP32 sum) and Cf (the FP32 sum itself) is non-NULL. */
+static int gemm_indexed(const uint16_t *A, int64_t a_rows, int a_row_divisor,
+                        const uint8_t *codes, const uint16_t *scales, int E, int N, int K,
+                        const int32_t *sorted_ids, const int32_t *expert_ids, int32_t num_tokens_padded,
+                        int block_m, int64_t num_pairs, uint16_t *Cb, float *Cf, int nthreads)
 {
     if (N <= 0 || K <= 0 || K % ORC_GROUP || block_m <= 0 || a_row_divisor <= 0
         || num_tokens_padded < 0 || num_tokens_padded % block_m)
@@ -372,12 +376,36 @@ int orc_moe_gemm(const uint16_t *A, int64_t a_rows, int a_row_divisor,
                 float acc = 0.0f;
                 for (int k = 0; k < K; ++k)
                     acc += f32_from_bf16(a[k]) * w[k];
-                C[(size_t)p * N + n] = bf16_from_f32(acc);
+                if (Cb)
+                    Cb[(size_t)p * N + n] = bf16_from_f32(acc);
+                else
+                    Cf[(size_t)p * N + n] = acc;
             }
     }
     free(wq);
     free(rows);
     return ORC_OK;
+}
+
+/* BF16 output: the GEMM operation as the article's kernels expose it. */
+int orc_moe_gemm(const uint16_t *A, int64_t a_rows, int a_row_divisor,
+                 const uint8_t *codes, const uint16_t *scales, int E, int N, int K,
+                 const int32_t *sorted_ids, const int32_t *expert_ids, int32_t num_tokens_padded,
+                 int block_m, int64_t num_pairs, uint16_t *C, int nthreads)
+{
+    return gemm_indexed(A, a_rows, a_row_divisor, codes, scales, E, N, K, sorted_ids, expert_ids,
+                        num_tokens_padded, block_m, num_pairs, C, NULL, nthreads);
+}
+
+/* FP32 output: the sum before any rounding, for a consumer that keeps FP32
+ * (the layer's down projection feeding the top-k weighted sum). */
+int orc_moe_gemm_f32(const uint16_t *A, int64_t a_rows, int a_row_divisor,
+                     const uint8_t *codes, const uint16_t *scales, int E, int N, int K,
+                     const int32_t *sorted_ids, const int32_t *expert_ids, int32_t num_tokens_padded,
+                     int block_m, int64_t num_pairs, float *C, int nthreads)
+{
+    return gemm_indexed(A, a_rows, a_row_divisor, codes, scales, E, N, K, sorted_ids, expert_ids,
+                        num_tokens_padded, block_m, num_pairs, NULL, C, nthreads);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -408,11 +436,12 @@ int orc_silu_mul(const uint16_t *C1, const int32_t *topk_ids, int64_t P, int E, 
 /* ------------------------------------------------------------------------ */
 /* Top-k weighted combine.
  *     out[t, n] = bf16_rne( sum over k ascending with topk_ids[t, k] local of
- *                           topk_w[t, k] * float(C2[t*topk + k, n]) )
- * in binary32, starting from +0.  A token with no local pair outputs +0. */
+ *                           topk_w[t, k] * C2[t*topk + k, n] )
+ * in binary32, starting from +0, C2 given in bf16 or in binary32.  A token
+ * with no local pair outputs +0. */
 
-int orc_combine(const uint16_t *C2, const int32_t *topk_ids, const float *topk_w,
-                int T, int topk, int E, int H, uint16_t *out, int nthreads)
+static int combine_any(const uint16_t *C2b, const float *C2f, const int32_t *topk_ids,
+                       const float *topk_w, int T, int topk, int E, int H, uint16_t *out, int nthreads)
 {
     if (T < 0 || topk <= 0 || H <= 0)
         return ORC_EINVAL;
@@ -424,17 +453,38 @@ int orc_combine(const uint16_t *C2, const int32_t *topk_ids, const float *topk_w
                 int64_t p = (int64_t)t * topk + k;
                 if (topk_ids[p] < 0 || topk_ids[p] >= E)
                     continue;
-                acc += topk_w[p] * f32_from_bf16(C2[(size_t)p * H + n]);
+                float v = C2b ? f32_from_bf16(C2b[(size_t)p * H + n]) : C2f[(size_t)p * H + n];
+                acc += topk_w[p] * v;
             }
             out[(size_t)t * H + n] = bf16_from_f32(acc);
         }
     return ORC_OK;
 }
 
+int orc_combine(const uint16_t *C2, const int32_t *topk_ids, const float *topk_w,
+                int T, int topk, int E, int H, uint16_t *out, int nthreads)
+{
+    return combine_any(C2, NULL, topk_ids, topk_w, T, topk, E, H, out, nthreads);
+}
+
+int orc_combine_f32(const float *C2, const int32_t *topk_ids, const float *topk_w,
+                    int T, int topk, int E, int H, uint16_t *out, int nthreads)
+{
+    return combine_any(NULL, C2, topk_ids, topk_w, T, topk, E, H, out, nthreads);
+}
+
 /* ------------------------------------------------------------------------ */
 /* One MoE layer: align -> gate_up GEMM (A = x, one row per token) -> SiLU*up
- * -> down GEMM (A = h, one row per pair) -> top-k combine.  Intermediates are
- * rounded to bf16 at each step, as the separate steps above define. */
+ * -> down GEMM (A = h, one row per pair) -> top-k combine.  The gate_up
+ * result is rounded to bf16 (the GEMM's output type) and so is SiLU*up (the
+ * bf16 activation operand of the down GEMM).  The down result of each pair
+ * goes into the weighted sum in binary32 and the layer output is rounded to
+ * bf16 once: the pages fix BF16 for the activations a GEMM consumes and for
+ * the output, and say nothing of a rounding between the down projection and
+ * the weighted sum.  Rounding there would let a last-place difference
+ * between two valid FP32 summation orders flip a pair result by one bf16 ulp
+ * (0.5 at magnitude 100) and move a combined output near zero by that ulp
+ * times the pair's weight. */
 
 int orc_moe_layer(const uint16_t *x, const int32_t *topk_ids, const float *topk_w,
                   int T, int topk, int E, int H, int I,
@@ -450,7 +500,7 @@ int orc_moe_layer(const uint16_t *x, const int32_t *topk_ids, const float *topk_
     int32_t *expert_ids = (int32_t *)malloc((size_t)(cap / block_m > 0 ? cap / block_m : 1) * sizeof(int32_t));
     uint16_t *C1 = (uint16_t *)calloc((size_t)(P > 0 ? P : 1) * 2 * I, sizeof(uint16_t));
     uint16_t *hb = (uint16_t *)calloc((size_t)(P > 0 ? P : 1) * I, sizeof(uint16_t));
-    uint16_t *C2 = (uint16_t *)calloc((size_t)(P > 0 ? P : 1) * H, sizeof(uint16_t));
+    float *C2 = (float *)calloc((size_t)(P > 0 ? P : 1) * H, sizeof(float));
     int rc = ORC_ENOMEM;
     int32_t ntp = 0;
     if (!sorted_ids || !expert_ids || !C1 || !hb || !C2)
@@ -462,10 +512,10 @@ int orc_moe_layer(const uint16_t *x, const int32_t *topk_ids, const float *topk_
     if (rc) goto done;
     rc = orc_silu_mul(C1, topk_ids, P, E, I, hb, nthreads);
     if (rc) goto done;
-    rc = orc_moe_gemm(hb, P, 1, codes2, scales2, E, H, I, sorted_ids, expert_ids, ntp,
-                      block_m, P, C2, nthreads);
+    rc = orc_moe_gemm_f32(hb, P, 1, codes2, scales2, E, H, I, sorted_ids, expert_ids, ntp,
+                          block_m, P, C2, nthreads);
     if (rc) goto done;
-    rc = orc_combine(C2, topk_ids, topk_w, T, topk, E, H, out, nthreads);
+    rc = orc_combine_f32(C2, topk_ids, topk_w, T, topk, E, H, out, nthreads);
 done:
     free(sorted_ids); free(expert_ids); free(C1); free(hb); free(C2);
     return rc;

@@ -1,0 +1,85 @@
+"""Helpers for the GPU parity tests: device copies, calls through the C ABI
+binding, and the element-wise tolerance check |gpu - ref| <= 1e-2 + 1e-2 |ref|."""
+import numpy as np
+import torch
+
+import w4a16_int4_mixture_moe_gb300 as chord
+import workloads as wl
+
+DEV = "cuda:0"
+ATOL = 1e-2
+RTOL = 1e-2
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def dbf(bits):
+    return dev(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+
+def host_bits(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def f64(bits):
+    return wl.bf16_bits_to_f32(bits).astype(np.float64)
+
+
+def assert_close(got_bits, ref_bits, what=""):
+    g, r = f64(got_bits), f64(ref_bits)
+    err = np.abs(g - r)
+    bad = ~(err <= ATOL + RTOL * np.abs(r))
+    if bad.any():
+        idx = np.argwhere(bad)[:5].tolist()
+        raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} elements outside "
+                             f"{ATOL} + {RTOL}|ref|; max err {np.nanmax(err):.4g}; first {idx}; "
+                             f"got {g[bad][:5]} ref {r[bad][:5]}")
+    return float(err.max()) if err.size else 0.0
+
+
+def pack(codes, scales):
+    E, N, K = codes.shape
+    out = torch.empty(chord.chord_packed_weight_bytes(E, N, K), dtype=torch.uint8, device=DEV)
+    chord.chord_pack_weights(dev(codes), dbf(scales), out)
+    return out
+
+
+def align(ids, E, bm, opts=None):
+    ids_d = ids if isinstance(ids, torch.Tensor) else dev(ids)
+    T, topk = ids_d.shape
+    cap = chord.chord_align_capacity(T, topk, E, bm)
+    s = torch.empty(max(cap, 1), dtype=torch.int32, device=DEV)[:cap]
+    e = torch.empty(max(cap // bm, 1), dtype=torch.int32, device=DEV)[:cap // bm]
+    n = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ws = torch.empty(max(chord.chord_align_workspace_bytes(T, topk, E), 4), dtype=torch.uint8, device=DEV)
+    chord.chord_moe_align(ids_d, E, bm, s, e, n, ws, opts=opts)
+    return s, e, n
+
+
+def gemm(A_bits, div, packed, E, N, K, s, e, n, bm, P, regime=0, C=None):
+    """C rows that no block names keep the fill pattern 0xFFFF (a NaN)."""
+    A = A_bits if isinstance(A_bits, torch.Tensor) else dbf(A_bits)
+    if C is None:
+        C = torch.full((max(P, 1), N), -1, dtype=torch.int16, device=DEV)[:P].view(torch.bfloat16)
+    opts = chord.ChordOpts(regime=regime)
+    chord.chord_w4a16_moe_gemm(A, div, packed, E, N, K, s, e, n, bm, P, C, opts=opts)
+    return C
+
+
+def layer(x_bits, ids, wts, E, E_global, I, p13, p2, bm=0, opts=None):
+    T, H = x_bits.shape
+    topk = ids.shape[1]
+    if bm <= 0:
+        bm = chord.chord_select_block_m(T, topk, E, E_global, 2 * I, H)
+    ws = torch.empty(chord.chord_layer_workspace_bytes(T, topk, E, H, I, bm), dtype=torch.uint8, device=DEV)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+    chord.chord_moe_layer(dbf(x_bits), dev(ids), dev(wts), E, E_global, I, p13, p2, ws, out, block_m=bm,
+                          opts=opts)
+    return out, bm
+
+
+def valid_rows(ids, E):
+    flat = ids.ravel()
+    return np.nonzero((flat >= 0) & (flat < E))[0]

@@ -1,0 +1,115 @@
+"""CPU-side checks of the C ABI: the library builds for sm_103a, loads, exports
+every function include/chord.h declares, and its host-only logic (sizes,
+capacities, block size choice, argument checks that return before any CUDA
+call) behaves as documented.  No GPU is touched."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+import w4a16_int4_mixture_moe_gb300 as chord
+
+HEADER = os.path.join(ROOT, "include", "chord.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    chord.build()
+    return chord.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(chord_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ["chord_pack_weights", "chord_moe_align", "chord_w4a16_moe_gemm", "chord_moe_layer"]:
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in chord._SIGS, f"binding lacks {n}"
+
+
+def test_sizes_and_capacity(lib):
+    assert chord.chord_packed_weight_bytes(48, 4096, 7168) == 256 + 48 * 4096 * 7168 * 9 // 16
+    assert chord.chord_packed_weight_bytes(1, 8, 64) == 0
+    assert chord.chord_packed_weight_bytes(1, 16, 96) == 0
+    P = 512 * 8
+    assert chord.chord_align_capacity(512, 8, 48, 16) == -(-(P + 48 * 15) // 16) * 16
+    assert chord.chord_align_capacity(1, 8, 384, 8) == -(-(8 + 8 * 7) // 8) * 8
+    assert chord.chord_align_capacity(0, 8, 48, 16) == 0
+    assert chord.chord_align_capacity(1, 0, 48, 16) == -1
+    assert chord.chord_align_workspace_bytes(16384, 8, 48) == 32 * 48 * 4
+
+
+def test_status_strings(lib):
+    for s in range(8):
+        assert chord.chord_status_string(s)
+    assert chord.chord_status_string(99) == "unknown status"
+
+
+def test_select_block_m(lib):
+    # tokens per expert (tok_e = T * topk / E_global) decides, not the token count
+    assert chord.chord_select_block_m(512, 8, 48, 384, 4096, 7168) in (16, 32)   # tok_e ~ 10.7
+    assert chord.chord_select_block_m(1, 8, 384, 384, 512, 7168) == 8
+    assert chord.chord_select_block_m(16, 2, 8, 8, 256, 256) in (8, 16)          # tok_e = 4
+    prev = 0
+    for T in (1, 16, 128, 512, 1024, 4096, 8192, 16384):
+        bm = chord.chord_select_block_m(T, 8, 48, 384, 4096, 7168)
+        assert bm % 8 == 0 and 8 <= bm <= 256
+        assert bm >= prev, "block size must not shrink as tokens per expert grow"
+        assert bm >= min(T * 8 / 384, 64)
+        prev = bm
+
+
+def test_layer_workspace_formula(lib):
+    T, topk, E, H, I, bm = 512, 8, 48, 7168, 2048, 16
+    P = T * topk
+    cap = chord.chord_align_capacity(T, topk, E, bm)
+    up = lambda x: (x + 255) // 256 * 256
+    want = up(chord.chord_align_workspace_bytes(T, topk, E))
+    want = up(want + cap * 4)
+    want = up(want + cap // bm * 4)
+    want = up(want + 4)
+    want = up(want + P * 2 * I * 2)
+    want = up(want + P * I * 2)
+    want = up(want + P * H * 4)   # the down projection's FP32 sums
+    assert chord.chord_layer_workspace_bytes(T, topk, E, H, I, bm) == want
+
+
+def test_argument_errors_before_any_launch(lib):
+    """Unsupported shapes and bad sizes are refused synchronously, before the
+    library touches CUDA (so this runs without a GPU)."""
+    vp = ctypes.c_void_p
+    big = vp(1 << 20)
+    # group size other than 32
+    assert lib.chord_pack_weights(big, big, 1, 16, 64, 64, big, 10 ** 6, None) == 2
+    # N not a multiple of 16
+    assert lib.chord_pack_weights(big, big, 1, 8, 64, 32, big, 10 ** 6, None) == 2
+    # packed buffer too small
+    assert lib.chord_pack_weights(big, big, 1, 16, 64, 32, big, 100, None) == 4
+    # GEMM: packed size does not match (E, N, K) -> layout mismatch
+    args = [big, 16, 1, big, 12345, 2, 128, 64, big, big, big, 16, 8, 16, big, None, 0, None, None]
+    assert lib.chord_w4a16_moe_gemm(*args) == 3
+    # GEMM: K not a multiple of 64 -> unsupported
+    args = [big, 16, 1, big, 12345, 2, 128, 96, big, big, big, 16, 8, 16, big, None, 0, None, None]
+    assert lib.chord_w4a16_moe_gemm(*args) == 2
+    # align: capacity too small
+    assert lib.chord_moe_align(big, 4, 2, 4, 8, big, big, big, 8, big, 10 ** 6, None, None) == 4
+    # align: too many experts for the scan
+    assert lib.chord_moe_align(big, 4, 2, 2000, 8, big, big, big, 10 ** 6, big, 10 ** 8, None, None) == 2
+    # misaligned activation pointer
+    nb = chord.chord_packed_weight_bytes(2, 128, 64)
+    args = [vp((1 << 20) + 2), 16, 1, big, nb, 2, 128, 64, big, big, big, 16, 8, 16, big, None, 0, None, None]
+    assert lib.chord_w4a16_moe_gemm(*args) == 1

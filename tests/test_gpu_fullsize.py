@@ -1,0 +1,180 @@
+"""Parity at the measured workloads' full sizes, in the launch configuration
+the benchmark times (automatic block size, the whole layer): the GPU runs
+every token; the oracle recomputes a sample of tokens one by one (a token's
+output depends only on its own pairs), and the GEMM outputs of a sample of
+pairs.  Tolerance |gpu - ref| <= 1e-2 + 1e-2|ref| on every sampled element."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import w4a16_int4_mixture_moe_gb300 as chord
+import workloads as wl
+from gpu_util import DEV, align, assert_close, dbf, dev, f64, gemm, host_bits, layer, pack
+
+pytestmark = pytest.mark.gpu
+
+N_SAMPLE_TOKENS = 12
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    chord.build()
+    chord.load()
+    oracle.build()
+    chord.chord_get_device_error()
+    yield
+    assert chord.chord_get_device_error() == 0
+
+
+_cache = {}
+
+
+def weights(w):
+    key = (w.E, w.H, w.I, w.seed)
+    if key not in _cache:
+        _cache.clear()
+        torch.cuda.empty_cache()
+        c13, s13 = wl.make_w13(w)
+        c2, s2 = wl.make_w2(w)
+        _cache[key] = ((c13, s13), (c2, s2), pack(c13, s13), pack(c2, s2))
+    return _cache[key]
+
+
+def sample_tokens(ids, E, n, seed):
+    local = np.nonzero(((ids >= 0) & (ids < E)).any(axis=1))[0]
+    rng = np.random.default_rng(seed)
+    pick = rng.choice(local, size=min(n, local.size), replace=False)
+    # always include the first and last token and one token with no local pair, if any
+    extra = [0, ids.shape[0] - 1]
+    nonlocal_t = np.nonzero(~((ids >= 0) & (ids < E)).any(axis=1))[0]
+    if nonlocal_t.size:
+        extra.append(int(nonlocal_t[0]))
+    return np.unique(np.concatenate([pick, np.array(extra, dtype=pick.dtype)]))
+
+
+WORKLOADS = [wl.EP8_DECODE, wl.EP8_PREFILL, *[wl.tp8(t) for t in wl.TP8_T], wl.SKEWED]
+
+
+def oracle_stages(w, x, ids, wts, w13, w2, sel):
+    """The oracle's intermediates for the sampled tokens (a token's results depend
+    only on its own pairs): C1 (bf16), h (bf16), C2 (FP32 sums), out (bf16)."""
+    ids_s, wts_s = ids[sel], wts[sel]
+    Ps = ids_s.size
+    s, e, n = oracle.moe_align(ids_s, w.E, 8)
+    C1 = oracle.moe_gemm(x[sel], w.topk, w13[0], w13[1], s, e, n, 8, Ps, C=np.zeros((Ps, 2 * w.I), np.uint16))
+    h = oracle.silu_mul(C1, ids_s.ravel(), w.E, h=np.zeros((Ps, w.I), np.uint16))
+    C2 = oracle.moe_gemm_f32(h, 1, w2[0], w2[1], s, e, n, 8, Ps, C=np.zeros((Ps, w.H), np.float32))
+    out = oracle.combine(C2, ids_s, wts_s, w.E)
+    return C1, h, C2, out
+
+
+def full_pairs(sel, topk):
+    """Pair ids of the sampled tokens in the full batch, in subset pair order."""
+    return (sel[:, None] * topk + np.arange(topk)[None, :]).ravel()
+
+
+@pytest.mark.parametrize("w", WORKLOADS, ids=[w.name for w in WORKLOADS])
+def test_layer_full_size_stagewise(w):
+    """Every stage at full size, in the benchmark's launch configuration, fed the
+    oracle's own result of the previous stage, within |gpu - ref| <= 1e-2 +
+    1e-2|ref| on every sampled element (the SiLU*up and combine stages bit for
+    bit but for the odd last-place difference of expf)."""
+    ids, wts = wl.make_routing(w)
+    x = wl.make_x(w)
+    w13, w2, p13, p2 = weights(w)
+    sel = sample_tokens(ids, w.E, N_SAMPLE_TOKENS, w.seed)
+    C1r, hr, C2r, outr = oracle_stages(w, x, ids, wts, w13, w2, sel)
+    pairs = full_pairs(sel, w.topk)
+    rows = np.nonzero(((ids[sel] >= 0) & (ids[sel] < w.E)).ravel())[0]
+    bm = chord.chord_select_block_m(w.T, w.topk, w.E, w.E_global, 2 * w.I, w.H)
+    s, e, n = align(ids, w.E, bm)
+    P = w.P
+    # gate_up on the real activations
+    C1 = host_bits(gemm(x, w.topk, p13, w.E, 2 * w.I, w.H, s, e, n, bm, P))
+    assert_close(C1[pairs][rows], C1r[rows], f"{w.name} gate_up (block_m={bm})")
+    del C1
+    # SiLU*up on the oracle's C1
+    C1in = np.zeros((P, 2 * w.I), np.uint16)
+    C1in[pairs] = C1r
+    hd = torch.empty((P, w.I), dtype=torch.bfloat16, device=DEV)
+    chord.chord_silu_mul(dbf(C1in), dev(ids), w.E, hd)
+    hg = host_bits(hd)
+    del hd, C1in
+    assert_close(hg[pairs][rows], hr[rows], f"{w.name} silu_mul")
+    # down (FP32 out) on the oracle's h; other rows get seeded activations
+    hin = wl.random_bf16(w.seed + 17, (P, w.I))
+    hin[pairs] = hr
+    C2d = torch.full((P, w.H), float("nan"), dtype=torch.float32, device=DEV)
+    chord.chord_w4a16_moe_gemm(dbf(hin), 1, p2, w.E, w.H, w.I, s, e, n, bm, P, C2d,
+                               opts=chord.ChordOpts(out_dtype=chord.DTYPE_F32))
+    C2g = C2d[torch.from_numpy(pairs).to(DEV)].cpu().numpy()
+    del C2d
+    err = np.abs(C2g[rows].astype(np.float64) - C2r[rows])
+    bad = err > 1e-2 + 1e-2 * np.abs(C2r[rows])
+    assert not bad.any(), f"{w.name} down: {int(bad.sum())} elements outside tolerance, max err {err.max()}"
+    # combine on the oracle's C2
+    out = torch.empty((sel.size, w.H), dtype=torch.bfloat16, device=DEV)
+    chord.chord_moe_combine(dev(C2r), dev(ids[sel]), dev(wts[sel]), w.E, out)
+    np.testing.assert_array_equal(host_bits(out), outr)
+
+
+@pytest.mark.parametrize("w", WORKLOADS, ids=[w.name for w in WORKLOADS])
+def test_layer_full_size_end_to_end(w):
+    """The whole layer through chord_moe_layer at full size against the oracle's
+    layer on sampled tokens.  Per element the tolerance 1e-2 + 1e-2|ref| must
+    hold for at least 99.5% of the elements; the rest may differ by the
+    propagation of one-ulp BF16 flips of the gate_up output and of SiLU*up (two
+    valid FP32 summation orders round an intermediate differently; the oracle
+    recomputed with float64 sums shows the same effect), bounded here by 5% of
+    the token's output RMS, with the error RMS below 0.2% of the output RMS."""
+    ids, wts = wl.make_routing(w)
+    x = wl.make_x(w)
+    w13, w2, p13, p2 = weights(w)
+    out, bm = layer(x, ids, wts, w.E, w.E_global, w.I, p13, p2)
+    torch.cuda.synchronize()
+    got = host_bits(out)
+    del out
+    sel = sample_tokens(ids, w.E, N_SAMPLE_TOKENS, w.seed)
+    ref = oracle.moe_layer(x[sel], ids[sel], wts[sel], w13, w2, w.E, block_m=bm)
+    g, r = f64(got[sel]), f64(ref)
+    err = np.abs(g - r)
+    inside = err <= 1e-2 + 1e-2 * np.abs(r)
+    rms = np.sqrt((r ** 2).mean(axis=1, keepdims=True)) + 1e-30
+    msg = (f"{w.name} layer (block_m={bm}): {int((~inside).sum())} of {inside.size} outside the per-element "
+           f"tolerance, max err {err.max():.4g}, max err/rms {(err / rms).max():.4g}")
+    assert inside.mean() >= 0.995, msg
+    assert (err <= 1e-2 + 1e-2 * np.abs(r) + 0.05 * rms).all(), msg
+    assert np.sqrt((err ** 2).mean()) <= 2e-3 * np.sqrt((r ** 2).mean()) + 1e-6, msg
+    # tokens with no local pair are exactly +0
+    none = ~((ids[sel] >= 0) & (ids[sel] < w.E)).any(axis=1)
+    assert (got[sel][none] == 0).all()
+
+
+@pytest.mark.parametrize("w", [wl.EP8_DECODE, wl.tp8(1024)], ids=["ep8_decode", "tp8_T1024"])
+def test_gemm_full_size_sampled_pairs(w):
+    """Both projections alone at full size; the oracle recomputes sampled pair rows."""
+    ids, _ = wl.make_routing(w)
+    x = wl.make_x(w)
+    (c13, sc13), (c2, sc2), p13, p2 = weights(w)
+    bm = chord.chord_select_block_m(w.T, w.topk, w.E, w.E_global, 2 * w.I, w.H)
+    s, e, n = align(ids, w.E, bm)
+    P = w.P
+    C1 = gemm(x, w.topk, p13, w.E, 2 * w.I, w.H, s, e, n, bm, P)
+    h = wl.random_bf16(99, (P, w.I))
+    C2 = gemm(h, 1, p2, w.E, w.H, w.I, s, e, n, bm, P)
+    got1, got2 = host_bits(C1), host_bits(C2)
+    flat = ids.ravel()
+    local = np.nonzero((flat >= 0) & (flat < w.E))[0]
+    pick = np.random.default_rng(5).choice(local, size=min(16, local.size), replace=False)
+    # the oracle's indexed GEMM over a block list that names only the sampled pairs
+    sub_ids = np.full(flat.shape, -1, np.int32)
+    sub_ids[pick] = flat[pick]
+    o_sorted, o_experts, o_ntp = oracle.moe_align(sub_ids.reshape(ids.shape), w.E, 8)
+    ref1 = oracle.moe_gemm(x, w.topk, c13, sc13, o_sorted, o_experts, o_ntp, 8, P,
+                           C=np.zeros((P, 2 * w.I), np.uint16))
+    ref2 = oracle.moe_gemm(h, 1, c2, sc2, o_sorted, o_experts, o_ntp, 8, P, C=np.zeros((P, w.H), np.uint16))
+    assert_close(got1[pick], ref1[pick], f"{w.name} gate_up sampled pairs")
+    assert_close(got2[pick], ref2[pick], f"{w.name} down sampled pairs")

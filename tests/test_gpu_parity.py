@@ -1,0 +1,366 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle, at sizes
+the oracle finishes in seconds: several N tiles, several K stages, ragged
+blocks, every block size, edge-case routing.  Pack and align must match byte
+for byte; GEMM, SiLU*up and the layer within |gpu - ref| <= 1e-2 + 1e-2|ref|
+(bit for bit where every summation order gives the same FP32 value)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import w4a16_int4_mixture_moe_gb300 as chord
+import workloads as wl
+from gpu_util import (DEV, align, assert_close, dbf, dev, f64, gemm, host_bits, layer, pack, valid_rows)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    chord.build()
+    chord.load()
+    oracle.build()
+    chord.chord_get_device_error()
+    yield
+    assert chord.chord_get_device_error() == 0, "a test left the device error word set"
+
+
+# --------------------------------------------------------------------- pack
+
+@pytest.mark.parametrize("shape", [(8, 256, 256), (8, 256, 128), (3, 32, 128), (2, 144, 192), (1, 4096, 7168)])
+def test_pack_byte_exact(shape):
+    E, N, K = shape
+    codes = wl.random_codes(sum(shape), shape)
+    scales = wl.random_scales(sum(shape) + 1, (E, N, K // 32))
+    got = pack(codes, scales).cpu().numpy()
+    want = oracle.pack(codes, scales)
+    np.testing.assert_array_equal(got, want)
+
+
+def test_pack_bad_code_sets_error_word():
+    codes = np.zeros((1, 16, 64), np.uint8)
+    codes[0, 5, 7] = 17
+    pack(codes, np.zeros((1, 16, 2), np.uint16))
+    assert chord.chord_get_device_error() == 5  # CHORD_DEV_BAD_CODE
+    assert chord.chord_get_device_error() == 0
+
+
+# -------------------------------------------------------------------- align
+
+ALIGN_CASES = [
+    (16, 2, 8, 4, 0.0), (33, 8, 48, 16, 0.5), (7, 3, 5, 8, 0.2), (64, 8, 384, 8, 0.0), (1, 8, 384, 16, 0.0),
+    (128, 4, 6, 64, 0.3), (200, 6, 12, 256, 0.1), (4096, 8, 384, 32, 0.0), (2048, 8, 48, 256, 0.875),
+    (1000, 1, 1024, 8, 0.0), (5000, 2, 3, 1, 0.0),
+]
+
+
+@pytest.mark.parametrize("T,topk,E,bm,pnl", ALIGN_CASES)
+def test_align_bit_exact(T, topk, E, bm, pnl):
+    ids = wl.random_ids(T * 7 + E, T, topk, E, p_nonlocal=pnl)
+    s, e, n = align(ids, E, bm)
+    s2, e2, n2 = oracle.moe_align(ids, E, bm)
+    assert int(n.item()) == n2
+    np.testing.assert_array_equal(s.cpu().numpy(), s2)
+    np.testing.assert_array_equal(e.cpu().numpy(), e2)
+
+
+@pytest.mark.parametrize("wl_name", ["ep8_decode", "ep8_prefill", "skewed", "tp8_4096"])
+def test_align_workload_routing_bit_exact(wl_name):
+    w = {"ep8_decode": wl.EP8_DECODE, "ep8_prefill": wl.EP8_PREFILL, "skewed": wl.SKEWED,
+         "tp8_4096": wl.tp8(4096)}[wl_name]
+    ids, _ = wl.make_routing(w)
+    for bm in (16, 64, 256):
+        s, e, n = align(ids, w.E, bm)
+        s2, e2, n2 = oracle.moe_align(ids, w.E, bm)
+        assert int(n.item()) == n2
+        np.testing.assert_array_equal(s.cpu().numpy(), s2)
+        np.testing.assert_array_equal(e.cpu().numpy(), e2)
+
+
+def test_align_edge_counts_and_empty():
+    bm = 8
+    flat = [1] + [2] * 2 + [3] * (bm - 1) + [4] * bm + [5] * (bm + 1) + [-1, -1]
+    rng = np.random.default_rng(3)
+    flat = np.array(flat, np.int32)[rng.permutation(len(flat))]
+    flat = np.append(flat, np.int32(-1)) if flat.size % 2 else flat
+    ids = flat.astype(np.int32).reshape(-1, 2)
+    s, e, n = align(ids, 6, bm)
+    s2, e2, n2 = oracle.moe_align(ids, 6, bm)
+    assert int(n.item()) == n2
+    np.testing.assert_array_equal(s.cpu().numpy(), s2)
+    np.testing.assert_array_equal(e.cpu().numpy(), e2)
+    # no tokens at all
+    s, e, n = align(np.zeros((0, 8), np.int32), 48, 16)
+    assert int(n.item()) == 0 and s.numel() == 0
+    # nothing local
+    s, e, n = align(np.full((9, 4), -1, np.int32), 8, 4)
+    assert int(n.item()) == 0 and bool((s == 36).all()) and bool((e == -1).all())
+
+
+def test_align_validate_reports_bad_ids():
+    ids = wl.random_ids(5, 20, 4, 8)
+    ids[3, 1] = 11
+    with pytest.raises(chord.ChordError) as ei:
+        align(ids, 8, 8, opts=chord.ChordOpts(validate=1))
+    assert ei.value.status == 6
+    # without validation the id is dropped like a non-local one
+    s, e, n = align(ids, 8, 8)
+    s2, e2, n2 = oracle.moe_align(ids, 8, 8)
+    np.testing.assert_array_equal(s.cpu().numpy(), s2)
+    assert chord.chord_get_device_error() == 0
+
+
+# --------------------------------------------------------------------- GEMM
+
+def run_gemm_case(T, topk, E, N, K, bm, seed, div=None, pnl=0.2, regime=0, exact=False, x=None, codes=None,
+                  scales=None, ids=None):
+    div = topk if div is None else div
+    a_rows = T if div == topk else T * topk
+    if x is None:
+        x = wl.random_bf16(seed, (a_rows, K))
+    if codes is None:
+        codes = wl.random_codes(seed + 1, (E, N, K))
+    if scales is None:
+        scales = wl.random_scales(seed + 2, (E, N, K // 32))
+    if ids is None:
+        ids = wl.random_ids(seed + 3, T, topk, E, p_nonlocal=pnl)
+    P = T * topk
+    packed = pack(codes, scales)
+    s, e, n = align(ids, E, bm)
+    C = gemm(x, div, packed, E, N, K, s, e, n, bm, P, regime=regime)
+    s2, e2, n2 = oracle.moe_align(ids, E, bm)
+    ref = oracle.moe_gemm(x, div, codes, scales, s2, e2, n2, bm, P,
+                          C=np.full((P, N), 0xFFFF, np.uint16))
+    got = host_bits(C)
+    rows = valid_rows(ids, E)
+    other = np.setdiff1d(np.arange(P), rows)
+    assert (got[other] == 0xFFFF).all(), "rows of non-local pairs were written"
+    if exact:
+        np.testing.assert_array_equal(got[rows], ref[rows])
+    else:
+        assert_close(got[rows], ref[rows], f"gemm T={T} E={E} N={N} K={K} bm={bm}")
+    return got, ref
+
+
+@pytest.mark.parametrize("bm", [8, 16, 24, 32, 64, 128, 256])
+@pytest.mark.parametrize("K", [256, 2048])
+def test_gemm_exact_integer_regime_bit_exact(bm, K):
+    """x in {-1, 0, 1}, scales 1.0: sums are exact integers in any order, so the
+    GPU must match the oracle bit for bit (catches any wrong index, lost or
+    doubled K chunk, or token/row mix-up)."""
+    T, topk, E, N = 40, 4, 5, 256
+    rng = np.random.default_rng(bm * 100 + K)
+    xi = rng.integers(-1, 2, size=(T, K)).astype(np.float32)
+    x = wl._bf16(xi)
+    scales = np.full((E, N, K // 32), 0x3F80, np.uint16)
+    run_gemm_case(T, topk, E, N, K, bm, seed=bm + K, x=x, scales=scales, exact=True)
+
+
+@pytest.mark.parametrize("bm", [8, 16, 32, 64])
+def test_gemm_dequant_bit_exact_one_hot(bm):
+    """One-hot activation rows make C the dequantised weight column itself:
+    C[t, n] = bf16((q[n, t] - 8) * s[n, t/32]) exactly.  Every code and a wide
+    range of scale exponents go through the kernel's subtract-then-scale path."""
+    K, N, E = 128, 256, 1
+    T = K
+    x = np.zeros((T, K), np.float32)
+    x[np.arange(T), np.arange(K)] = 1.0
+    x = wl._bf16(x)
+    codes = wl.random_codes(90 + bm, (E, N, K))
+    rng = np.random.default_rng(91)
+    sc = (rng.standard_normal((E, N, K // 32)) * np.exp2(rng.integers(-20, 20, size=(E, N, K // 32))))
+    scales = wl._bf16(sc.astype(np.float32))
+    ids = np.zeros((T, 1), np.int32)
+    got, ref = run_gemm_case(T, 1, E, N, K, bm, seed=0, div=1, x=x, codes=codes, scales=scales, ids=ids,
+                             exact=True)
+    deq = oracle.dequant_pairs(codes[0].T.copy().ravel(),
+                               np.repeat(scales[0], 32, axis=1).T.copy().ravel()).reshape(K, N)
+    # a zero weight times a negative scale is -0; a sum that starts from +0 returns +0
+    deq = np.where(deq == 0x8000, np.uint16(0), deq)
+    np.testing.assert_array_equal(got, deq)
+
+
+@pytest.mark.parametrize("bm", [8, 32, 64])
+def test_gemm_f32_output(bm):
+    """FP32 output: exact integers in the exact-integer regime (bit-exact with the
+    oracle's unrounded sum), within tolerance on random data."""
+    T, topk, E, N, K = 24, 4, 5, 256, 1024
+    rng = np.random.default_rng(bm)
+    xi = rng.integers(-1, 2, size=(T, K)).astype(np.float32)
+    codes = wl.random_codes(bm + 1, (E, N, K))
+    ids = wl.random_ids(bm + 2, T, topk, E, p_nonlocal=0.2)
+    rows = valid_rows(ids, E)
+    s, e, n = align(ids, E, bm)
+    s2, e2, n2 = oracle.moe_align(ids, E, bm)
+    for x, scales, exact in [(wl._bf16(xi), np.full((E, N, K // 32), 0x3F80, np.uint16), True),
+                             (wl.random_bf16(bm + 3, (T, K)), wl.random_scales(bm + 4, (E, N, K // 32)), False)]:
+        packed = pack(codes, scales)
+        C = torch.full((T * topk, N), float("nan"), dtype=torch.float32, device=DEV)
+        chord.chord_w4a16_moe_gemm(dbf(x), topk, packed, E, N, K, s, e, n, bm, T * topk, C,
+                                   opts=chord.ChordOpts(out_dtype=chord.DTYPE_F32))
+        got = C.cpu().numpy()
+        ref = oracle.moe_gemm_f32(x, topk, codes, scales, s2, e2, n2, bm, T * topk)
+        if exact:
+            np.testing.assert_array_equal(got[rows], ref[rows])
+        else:
+            err = np.abs(got[rows].astype(np.float64) - ref[rows])
+            assert (err <= 1e-2 + 1e-2 * np.abs(ref[rows])).all(), err.max()
+        other = np.setdiff1d(np.arange(T * topk), rows)
+        assert np.isnan(got[other]).all()
+
+
+@pytest.mark.parametrize("bm", [8, 16, 32, 64])
+@pytest.mark.parametrize("shape", [(3, 128, 64), (4, 384, 320), (6, 256, 1024)])
+def test_gemm_random_vs_oracle(bm, shape):
+    E, N, K = shape
+    run_gemm_case(37, 3, E, N, K, bm, seed=E * N + K + bm)
+
+
+def test_gemm_down_projection_row_per_pair():
+    """a_row_divisor = 1: A holds one row per pair (the down projection)."""
+    run_gemm_case(30, 4, 5, 256, 256, 16, seed=77, div=1)
+
+
+def test_gemm_edge_routing():
+    """Experts with 0, 1, 2, bm-1, bm, bm+1 and 3*bm+5 rows in one call."""
+    bm = 16
+    counts = [0, 1, 2, bm - 1, bm, bm + 1, 3 * bm + 5]
+    flat = np.concatenate([np.full(c, e, np.int32) for e, c in enumerate(counts)])
+    flat = flat[np.random.default_rng(4).permutation(flat.size)]
+    pad = (-flat.size) % 2
+    flat = np.concatenate([flat, np.full(pad, -1, np.int32)])
+    ids = flat.reshape(-1, 2)
+    run_gemm_case(ids.shape[0], 2, len(counts), 128, 192, bm, seed=5, ids=ids)
+
+
+def test_gemm_nothing_local_writes_nothing():
+    ids = np.full((12, 4), -1, np.int32)
+    run_gemm_case(12, 4, 3, 128, 64, 8, seed=6, ids=ids)
+
+
+def test_gemm_header_mismatch_is_reported():
+    """A blob packed for (E, N, K) = (2, 128, 128) passed as (2, 256, 64) has the
+    right size but the wrong header: the device refuses it and writes nothing."""
+    E = 2
+    codes = wl.random_codes(1, (E, 128, 128))
+    scales = wl.random_scales(2, (E, 128, 4))
+    packed = pack(codes, scales)
+    ids = wl.random_ids(3, 8, 2, E)
+    s, e, n = align(ids, E, 8)
+    x = wl.random_bf16(4, (8, 64))
+    with pytest.raises(chord.ChordError) as ei:
+        C = torch.full((16, 256), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+        chord.chord_w4a16_moe_gemm(dbf(x), 2, packed, E, 256, 64, s, e, n, 8, 16, C,
+                                   opts=chord.ChordOpts(validate=1))
+    assert ei.value.status == 6
+    assert (host_bits(C) == 0xFFFF).all()
+
+
+# ---------------------------------------------------------------- epilogues
+
+def test_silu_mul_vs_oracle():
+    P, I, E = 50, 192, 4
+    C1 = wl.random_bf16(8, (P, 2 * I), std=4.0)
+    ids = wl.random_ids(9, P, 1, E, p_nonlocal=0.3)
+    h = torch.full((P, I), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+    chord.chord_silu_mul(dbf(C1), dev(ids.ravel().copy()), E, h)
+    ref = oracle.silu_mul(C1, ids.ravel(), E, h=np.full((P, I), 0xFFFF, np.uint16))
+    got = host_bits(h)
+    rows = valid_rows(ids, E)
+    assert_close(got[rows], ref[rows], "silu_mul")
+    other = np.setdiff1d(np.arange(P), rows)
+    assert (got[other] == 0xFFFF).all()
+    # expf may differ from the C library's by an ulp; nearly all results are identical
+    assert np.mean(got[rows] == ref[rows]) > 0.99
+
+
+def test_combine_bit_exact():
+    """Same FP32 operations in the same order as the oracle: bit-exact."""
+    T, topk, E, H = 33, 8, 16, 7168 // 4
+    C2 = wl.random_bf16(10, (T * topk, H), std=30.0)
+    ids = wl.random_ids(11, T, topk, E, p_nonlocal=0.4)
+    ids[0, :] = -1
+    w = wl.random_weights(12, T, topk)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+    chord.chord_moe_combine(dbf(C2), dev(ids), dev(w), E, out)
+    ref = oracle.combine(C2, ids, w, E)
+    np.testing.assert_array_equal(host_bits(out), ref)
+    # FP32 pair results (the layer's down projection output)
+    C2f = (np.random.default_rng(13).standard_normal((T * topk, H)) * 80).astype(np.float32)
+    chord.chord_moe_combine(dev(C2f), dev(ids), dev(w), E, out)
+    np.testing.assert_array_equal(host_bits(out), oracle.combine(C2f, ids, w, E))
+
+
+# -------------------------------------------------------------------- layer
+
+@pytest.mark.parametrize("bm", [0, 8, 16, 32, 64])
+def test_layer_tiny_vs_oracle(bm):
+    w = wl.TINY
+    ids, wts = wl.make_routing(w)
+    x = wl.make_x(w)
+    c13, s13 = wl.make_w13(w)
+    c2, s2 = wl.make_w2(w)
+    out, used_bm = layer(x, ids, wts, w.E, w.E_global, w.I, pack(c13, s13), pack(c2, s2), bm=bm)
+    ref = oracle.moe_layer(x, ids, wts, (c13, s13), (c2, s2), w.E, block_m=used_bm)
+    assert_close(host_bits(out), ref, f"tiny layer bm={used_bm}")
+
+
+def test_layer_ep_partial_and_empty_tokens():
+    """EP-style routing with most pairs non-local; tokens with no local pair are +0."""
+    T, topk, E, H, I = 24, 8, 6, 256, 128
+    ids = wl.random_ids(20, T, topk, 48)
+    ids = np.where(ids < E, ids, -1).astype(np.int32)
+    ids[5, :] = -1
+    wts = wl.random_weights(21, T, topk)
+    x = wl.random_bf16(22, (T, H))
+    c13, s13 = wl.random_codes(23, (E, 2 * I, H)), wl.random_scales(24, (E, 2 * I, H // 32))
+    c2, s2 = wl.random_codes(25, (E, H, I)), wl.random_scales(26, (E, H, I // 32))
+    out, bm = layer(x, ids, wts, E, 48, I, pack(c13, s13), pack(c2, s2))
+    ref = oracle.moe_layer(x, ids, wts, (c13, s13), (c2, s2), E, block_m=bm)
+    got = host_bits(out)
+    assert_close(got, ref, "ep partial layer")
+    assert (got[5] == 0).all()
+
+
+def test_layer_zero_tokens():
+    E, H, I = 4, 128, 64
+    p13 = pack(np.zeros((E, 2 * I, H), np.uint8), np.zeros((E, 2 * I, H // 32), np.uint16))
+    p2 = pack(np.zeros((E, H, I), np.uint8), np.zeros((E, H, I // 32), np.uint16))
+    ws = torch.empty(4096, dtype=torch.uint8, device=DEV)
+    out = torch.empty((0, H), dtype=torch.bfloat16, device=DEV)
+    chord.chord_moe_layer(torch.empty((0, H), dtype=torch.bfloat16, device=DEV),
+                          torch.empty((0, 2), dtype=torch.int32, device=DEV),
+                          torch.empty((0, 2), dtype=torch.float32, device=DEV), E, E, I, p13, p2, ws, out,
+                          block_m=8)
+
+
+def test_layer_cuda_graph_replay():
+    """The layer enqueues no host synchronisation, so it captures into a CUDA
+    graph; replays give the eager result."""
+    w = wl.TINY
+    ids, wts = wl.make_routing(w)
+    x = wl.make_x(w)
+    c13, s13 = wl.make_w13(w)
+    c2, s2 = wl.make_w2(w)
+    p13, p2 = pack(c13, s13), pack(c2, s2)
+    bm = 16
+    ws = torch.empty(chord.chord_layer_workspace_bytes(w.T, w.topk, w.E, w.H, w.I, bm), dtype=torch.uint8,
+                     device=DEV)
+    xd, idd, wd = dbf(x), dev(ids), dev(wts)
+    eager = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=DEV)
+    chord.chord_moe_layer(xd, idd, wd, w.E, w.E_global, w.I, p13, p2, ws, eager, block_m=bm)
+    out = torch.zeros((w.T, w.H), dtype=torch.bfloat16, device=DEV)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            chord.chord_moe_layer(xd, idd, wd, w.E, w.E_global, w.I, p13, p2, ws, out, block_m=bm, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(host_bits(out), host_bits(eager))

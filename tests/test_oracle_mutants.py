@@ -28,11 +28,16 @@ MUTANTS = [
      "const uint16_t *a = A + (size_t)(p % a_row_divisor) * (size_t)K;"),
     ("gemm_group_64", "uint16_t s = scales[((size_t)e * N + n) * G + k / ORC_GROUP];",
      "uint16_t s = scales[((size_t)e * N + n) * G + k / 64];"),
+    ("f32_output_rounded", "Cf[(size_t)p * N + n] = acc;",
+     "Cf[(size_t)p * N + n] = f32_from_bf16(bf16_from_f32(acc));"),
+    ("layer_rounds_down", "rc = orc_combine_f32(C2, topk_ids, topk_w, T, topk, E, H, out, nthreads);",
+     "for (int64_t i = 0; i < P * H; ++i) C2[i] = f32_from_bf16(bf16_from_f32(C2[i]));\n"
+     "    rc = orc_combine_f32(C2, topk_ids, topk_w, T, topk, E, H, out, nthreads);"),
     ("silu_sign", "float s = g / (1.0f + expf(-g));", "float s = g / (1.0f + expf(g));"),
     ("gate_up_swap", "float g = f32_from_bf16(C1[(size_t)p * 2 * I + j]);",
      "float g = f32_from_bf16(C1[(size_t)p * 2 * I + I + j]);"),
-    ("combine_nonlocal", "if (topk_ids[p] < 0 || topk_ids[p] >= E)\n                    continue;\n                acc +=",
-     "if (topk_ids[p] >= E)\n                    continue;\n                acc +="),
+    ("combine_nonlocal", "if (topk_ids[p] < 0 || topk_ids[p] >= E)\n                    continue;\n                float v",
+     "if (topk_ids[p] >= E)\n                    continue;\n                float v"),
 ]
 
 

@@ -330,6 +330,52 @@ def test_gemm_float_bound(orc):
         assert (np.abs(f64(C[p]) - ref) <= tol).all()
 
 
+def test_gemm_f32_exact_integer_and_bf16_consistency(orc):
+    """FP32 output: in the exact-integer regime it equals numpy's integer
+    matmul exactly (no rounding at all), and rounding it with torch gives the
+    bf16-output GEMM bit for bit (same sum, one rounding)."""
+    T, topk, E, N, K = 10, 3, 4, 64, 512
+    rng = np.random.default_rng(5)
+    xi = rng.integers(-1, 2, size=(T, K))
+    x = to_bf16(xi.astype(np.float32))
+    codes = wl.random_codes(6, (E, N, K))
+    ones = np.full((E, N, K // GROUP), 0x3F80, np.uint16)
+    ids = wl.random_ids(7, T, topk, E, p_nonlocal=0.2)
+    s, e, ntp = orc.moe_align(ids, E, 8)
+    Cf = orc.moe_gemm_f32(x, topk, codes, ones, s, e, ntp, 8, T * topk)
+    for p in range(T * topk):
+        if ids.ravel()[p] >= 0:
+            exact = (codes[ids.ravel()[p]].astype(np.int64) - 8) @ xi[p // topk]
+            np.testing.assert_array_equal(Cf[p], exact.astype(np.float32))
+    x = wl.random_bf16(8, (T, K))
+    scales = wl.random_scales(9, (E, N, K // GROUP))
+    Cf = orc.moe_gemm_f32(x, topk, codes, scales, s, e, ntp, 8, T * topk)
+    Cb = orc.moe_gemm(x, topk, codes, scales, s, e, ntp, 8, T * topk, C=np.zeros((T * topk, N), np.uint16))
+    rows = np.nonzero(ids.ravel() >= 0)[0]
+    np.testing.assert_array_equal(to_bf16(Cf[rows]), Cb[rows])
+
+
+def test_combine_f32_one_hot_and_bound(orc):
+    """FP32 input: a one-hot weight gives bf16(C2 row) (torch rounding); a
+    general case stays within the FP32 bound of a float64 sum."""
+    T, topk, E, H = 7, 4, 5, 96
+    rng = np.random.default_rng(10)
+    C2 = (rng.standard_normal((T * topk, H)) * 100).astype(np.float32)
+    ids = wl.random_ids(11, T, topk, E)
+    w = np.zeros((T, topk), np.float32)
+    pick = rng.integers(0, topk, size=T)
+    w[np.arange(T), pick] = 1.0
+    out = orc.combine(C2, ids, w, E)
+    for t in range(T):
+        np.testing.assert_array_equal(out[t], to_bf16(C2[t * topk + pick[t]]))
+    w = wl.random_weights(12, T, topk)
+    out = f64(orc.combine(C2, ids, w, E))
+    Y = C2.astype(np.float64).reshape(T, topk, H)
+    ref = (w.astype(np.float64)[:, :, None] * Y).sum(1)
+    mag = (np.abs(w.astype(np.float64))[:, :, None] * np.abs(Y)).sum(1)
+    assert (np.abs(out - ref) <= np.abs(ref) * 2.0 ** -8 + topk * 2.0 ** -23 * mag).all()
+
+
 # --- activation -------------------------------------------------------------
 
 def test_silu_mul_vs_expit(orc):
@@ -399,7 +445,8 @@ def test_combine_float_bound(orc):
 
 def layer_dense_reference(x, ids, w, c13, s13, c2, s2, E):
     """Dense per-token loop over each token's experts in float64, with bf16
-    rounding (torch) after gate_up, after SiLU*up and after down."""
+    rounding (torch) after gate_up and after SiLU*up; the down result enters
+    the weighted sum unrounded and the output is rounded once."""
     W13 = f64(dequant_ref(c13, s13))
     W2 = f64(dequant_ref(c2, s2))
     X = f64(x)
@@ -414,7 +461,7 @@ def layer_dense_reference(x, ids, w, c13, s13, c2, s2, E):
                 continue
             gu = bf16r(W13[e] @ X[t])
             h = bf16r(gu[:I] * expit(gu[:I]) * gu[I:])
-            y = bf16r(W2[e] @ h)
+            y = W2[e] @ h
             acc += float(w[t, k]) * y
         out[t] = bf16r(acc)
     return out

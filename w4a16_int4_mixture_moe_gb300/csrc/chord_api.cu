@@ -1,0 +1,346 @@
+// C ABI of the W4A16 MoE library (see include/chord.h): argument checks,
+// schedule choice and launches.  No device memory is allocated here; every
+// buffer, scratch included, belongs to the caller.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+#include <mutex>
+
+#include "../../include/chord.h"
+#include "chord_common.cuh"
+#include "chord_internal.h"
+
+namespace chord {
+
+// Sticky error word, one per device that loads the library.
+__device__ int g_error_word;
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_info_mu;
+DeviceInfo g_info[kMaxDevices];
+bool g_info_ok[kMaxDevices];
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+chord_status cuda_status(cudaError_t e) { return e == cudaSuccess ? CHORD_OK : CHORD_ERR_CUDA; }
+
+chord_opts opts_or_default(const chord_opts* o) {
+    chord_opts d{};
+    if (o) d = *o;
+    return d;
+}
+
+int env_int(const char* name, int dflt) {
+    const char* v = getenv(name);
+    return v && *v ? atoi(v) : dflt;
+}
+
+// After a call in validate mode: wait for it and turn the error word into a status.
+chord_status finish(const chord_opts& o, cudaStream_t stream) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return CHORD_ERR_CUDA;
+    if (!o.validate) return CHORD_OK;
+    int32_t code = 0;
+    chord_status st = chord_get_device_error(stream, &code);
+    if (st != CHORD_OK) return st;
+    if (code == CHORD_DEV_TIMEOUT) return CHORD_ERR_TIMEOUT;
+    return code ? CHORD_ERR_DEVICE_VALIDATION : CHORD_OK;
+}
+}  // namespace
+
+const DeviceInfo& device_info() {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= kMaxDevices) dev = 0;
+    std::lock_guard<std::mutex> lk(g_info_mu);
+    if (!g_info_ok[dev]) {
+        DeviceInfo d;
+        cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_error_word) == cudaSuccess) d.err = static_cast<int*>(p);
+        if (d.sm_count <= 0) d.sm_count = 1;
+        g_info[dev] = d;
+        g_info_ok[dev] = d.err != nullptr;
+    }
+    return g_info[dev];
+}
+
+}  // namespace chord
+
+using namespace chord;
+
+extern "C" {
+
+int chord_version(void) { return 100; }
+
+const char* chord_status_string(chord_status s) {
+    switch (s) {
+        case CHORD_OK: return "ok";
+        case CHORD_ERR_INVALID_ARG: return "invalid argument";
+        case CHORD_ERR_UNSUPPORTED: return "unsupported configuration";
+        case CHORD_ERR_LAYOUT_MISMATCH: return "packed weight layout does not match the call";
+        case CHORD_ERR_BUFFER_TOO_SMALL: return "buffer or workspace too small";
+        case CHORD_ERR_CUDA: return "CUDA runtime error";
+        case CHORD_ERR_DEVICE_VALIDATION: return "device-side validation failed";
+        case CHORD_ERR_TIMEOUT: return "a bounded device wait timed out";
+    }
+    return "unknown status";
+}
+
+size_t chord_packed_weight_bytes(int E, int N, int K) {
+    if (E < 0 || N <= 0 || K <= 0 || N % 16 || K % 64) return 0;
+    return (size_t)kHeaderBytes + (size_t)E * (size_t)N * (size_t)K * 9u / 16u;
+}
+
+chord_status chord_pack_weights(const uint8_t* codes, const void* scales, int E, int N, int K, int group_size,
+                                void* packed, size_t packed_bytes, void* stream) {
+    if (group_size != kGroup) return CHORD_ERR_UNSUPPORTED;
+    if (E < 0 || N <= 0 || K <= 0) return CHORD_ERR_INVALID_ARG;
+    if (N % 16 || K % 64) return CHORD_ERR_UNSUPPORTED;
+    if (!packed || !aligned16(packed) || (E > 0 && (!codes || !scales))) return CHORD_ERR_INVALID_ARG;
+    if (packed_bytes < chord_packed_weight_bytes(E, N, K)) return CHORD_ERR_BUFFER_TOO_SMALL;
+    const DeviceInfo& di = device_info();
+    if (!di.err) return CHORD_ERR_CUDA;
+    return cuda_status(launch_pack(codes, static_cast<const uint16_t*>(scales), E, N, K,
+                                   static_cast<uint8_t*>(packed), di.err, static_cast<cudaStream_t>(stream)));
+}
+
+int64_t chord_align_capacity(int T, int topk, int E, int block_m) {
+    if (T < 0 || topk <= 0 || E <= 0 || block_m <= 0) return -1;
+    const int64_t P = (int64_t)T * topk;
+    const int64_t m = P < E ? P : E;
+    const int64_t c = P + m * (block_m - 1);
+    return (c + block_m - 1) / block_m * block_m;
+}
+
+size_t chord_align_workspace_bytes(int T, int topk, int E) {
+    if (T < 0 || topk <= 0 || E <= 0) return 0;
+    return (size_t)align_slices((int64_t)T * topk) * (size_t)E * sizeof(int32_t);
+}
+
+chord_status chord_moe_align(const int32_t* topk_ids, int T, int topk, int E, int block_m, int32_t* sorted_ids,
+                             int32_t* expert_ids, int32_t* num_tokens_padded, int64_t capacity, void* workspace,
+                             size_t workspace_bytes, const chord_opts* opts, void* stream) {
+    if (T < 0 || topk <= 0 || E <= 0 || block_m <= 0) return CHORD_ERR_INVALID_ARG;
+    if (E > 1024 || block_m > 256) return CHORD_ERR_UNSUPPORTED;
+    if ((int64_t)T * topk >= INT32_MAX) return CHORD_ERR_UNSUPPORTED;
+    const int64_t cap = chord_align_capacity(T, topk, E, block_m);
+    if (capacity < cap) return CHORD_ERR_BUFFER_TOO_SMALL;
+    if (capacity % block_m) return CHORD_ERR_INVALID_ARG;
+    if (workspace_bytes < chord_align_workspace_bytes(T, topk, E)) return CHORD_ERR_BUFFER_TOO_SMALL;
+    if (!num_tokens_padded || !workspace || (T > 0 && !topk_ids) || (capacity > 0 && (!sorted_ids || !expert_ids)))
+        return CHORD_ERR_INVALID_ARG;
+    const chord_opts o = opts_or_default(opts);
+    const DeviceInfo& di = device_info();
+    if (!di.err) return CHORD_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_align(topk_ids, (int64_t)T * topk, E, block_m, sorted_ids, expert_ids, num_tokens_padded,
+                                 capacity, static_cast<int32_t*>(workspace), o.validate != 0, di.err, s);
+    if (e != cudaSuccess) return CHORD_ERR_CUDA;
+    return finish(o, s);
+}
+
+int chord_select_block_m(int T, int topk, int E_local, int E_global, int N, int K) {
+    (void)N;
+    (void)K;
+    const int forced = env_int("CHORD_BLOCK_M", 0);
+    if (forced > 0) return forced;
+    const int eg = E_global > 0 ? E_global : (E_local > 0 ? E_local : 1);
+    const double tok_e = (double)T * (double)(topk > 0 ? topk : 1) / (double)eg;
+    // Rows per expert that a block should hold without splitting an expert in two
+    // most of the time: the mean plus three standard deviations of a Poisson count.
+    const double need = tok_e + 3.0 * sqrt(tok_e) + 1.0;
+    if (prefill_available() && tok_e > 48.0) return 256;
+    if (need <= 8.0) return 8;
+    if (need <= 16.0) return 16;
+    if (need <= 32.0) return 32;
+    return 64;
+}
+
+size_t chord_gemm_workspace_bytes(int64_t num_pairs, int N, int K, int block_m, const chord_opts* opts) {
+    (void)num_pairs;
+    (void)N;
+    (void)K;
+    (void)block_m;
+    (void)opts;
+    return 0;
+}
+
+chord_status chord_w4a16_moe_gemm(const void* A, int64_t a_rows, int a_row_divisor, const void* packed,
+                                  size_t packed_bytes, int E, int N, int K, const int32_t* sorted_ids,
+                                  const int32_t* expert_ids, const int32_t* num_tokens_padded, int64_t capacity,
+                                  int block_m, int64_t num_pairs, void* C, void* workspace, size_t workspace_bytes,
+                                  const chord_opts* opts, void* stream) {
+    (void)workspace;
+    (void)workspace_bytes;
+    if (E <= 0 || N <= 0 || K <= 0 || a_rows < 0 || a_row_divisor <= 0 || block_m <= 0 || capacity < 0 ||
+        num_pairs < 0)
+        return CHORD_ERR_INVALID_ARG;
+    if (N % 128 || K % 64) return CHORD_ERR_UNSUPPORTED;
+    if (num_pairs >= INT32_MAX) return CHORD_ERR_UNSUPPORTED;
+    if (packed_bytes != chord_packed_weight_bytes(E, N, K)) return CHORD_ERR_LAYOUT_MISMATCH;
+    if (!packed || !aligned16(packed) || !num_tokens_padded || (capacity > 0 && (!sorted_ids || !expert_ids)))
+        return CHORD_ERR_INVALID_ARG;
+    if (capacity % block_m) return CHORD_ERR_INVALID_ARG;
+    if ((a_rows > 0 && (!A || !aligned16(A))) || (num_pairs > 0 && (!C || !aligned16(C))))
+        return CHORD_ERR_INVALID_ARG;
+    const chord_opts o = opts_or_default(opts);
+    int regime = o.regime ? o.regime : env_int("CHORD_FORCE_REGIME", 0);
+    if (regime == CHORD_REGIME_AUTO) regime = (block_m > 64 && prefill_available()) ? CHORD_REGIME_PREFILL
+                                                                                      : CHORD_REGIME_DECODE;
+    if (regime == CHORD_REGIME_DECODE && block_m % 8) return CHORD_ERR_UNSUPPORTED;
+    if (regime == CHORD_REGIME_PREFILL && (!prefill_available() || block_m % 16 || block_m > 256))
+        return CHORD_ERR_UNSUPPORTED;
+    if (regime != CHORD_REGIME_DECODE && regime != CHORD_REGIME_PREFILL) return CHORD_ERR_INVALID_ARG;
+    if (o.out_dtype != CHORD_DTYPE_BF16 && o.out_dtype != CHORD_DTYPE_F32) return CHORD_ERR_INVALID_ARG;
+    const DeviceInfo& di = device_info();
+    if (!di.err) return CHORD_ERR_CUDA;
+    if (capacity == 0 || num_pairs == 0) return CHORD_OK;
+    GemmArgs g{};
+    g.A = static_cast<const uint16_t*>(A);
+    g.a_rows = a_rows;
+    g.a_row_divisor = a_row_divisor;
+    g.packed = static_cast<const uint8_t*>(packed);
+    g.E = E;
+    g.N = N;
+    g.K = K;
+    g.sorted_ids = sorted_ids;
+    g.expert_ids = expert_ids;
+    g.ntp = num_tokens_padded;
+    g.capacity = capacity;
+    g.block_m = block_m;
+    g.num_pairs = num_pairs;
+    g.C = C;
+    g.out_f32 = o.out_dtype == CHORD_DTYPE_F32 ? 1 : 0;
+    g.err = di.err;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = regime == CHORD_REGIME_PREFILL ? launch_gemm_prefill(g, s) : launch_gemm_decode(g, s);
+    if (e != cudaSuccess) return CHORD_ERR_CUDA;
+    return finish(o, s);
+}
+
+chord_status chord_silu_mul(const void* C1, const int32_t* topk_ids, int64_t P, int E, int I, void* h, void* stream) {
+    if (P < 0 || E <= 0 || I <= 0) return CHORD_ERR_INVALID_ARG;
+    if (I % 8) return CHORD_ERR_UNSUPPORTED;
+    if (P > 0 && (!C1 || !topk_ids || !h || !aligned16(C1) || !aligned16(h))) return CHORD_ERR_INVALID_ARG;
+    return cuda_status(launch_silu_mul(static_cast<const uint16_t*>(C1), topk_ids, P, E, I, static_cast<uint16_t*>(h),
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+chord_status chord_moe_combine(const void* C2, int c2_dtype, const int32_t* topk_ids, const float* topk_w, int T,
+                               int topk, int E, int H, void* out, void* stream) {
+    if (T < 0 || topk <= 0 || E <= 0 || H <= 0) return CHORD_ERR_INVALID_ARG;
+    if (c2_dtype != CHORD_DTYPE_BF16 && c2_dtype != CHORD_DTYPE_F32) return CHORD_ERR_INVALID_ARG;
+    if (H % 8) return CHORD_ERR_UNSUPPORTED;
+    if (T > 0 && (!C2 || !topk_ids || !topk_w || !out || !aligned16(C2) || !aligned16(out)))
+        return CHORD_ERR_INVALID_ARG;
+    return cuda_status(launch_combine(C2, c2_dtype == CHORD_DTYPE_F32, topk_ids, topk_w, T, topk, E, H,
+                                      static_cast<uint16_t*>(out), static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"
+
+namespace {
+struct LayerWs {
+    size_t counts, sorted, experts, ntp, c1, h, c2, total;
+};
+
+size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+bool layer_ws(int T, int topk, int E, int H, int I, int block_m, LayerWs* w) {
+    const int64_t cap = chord_align_capacity(T, topk, E, block_m);
+    if (cap < 0) return false;
+    const size_t P = (size_t)T * (size_t)topk;
+    size_t off = 0;
+    w->counts = off;
+    off = up256(off + chord_align_workspace_bytes(T, topk, E));
+    w->sorted = off;
+    off = up256(off + (size_t)cap * 4);
+    w->experts = off;
+    off = up256(off + (size_t)(cap / block_m) * 4);
+    w->ntp = off;
+    off = up256(off + 4);
+    w->c1 = off;
+    off = up256(off + P * 2 * (size_t)I * 2);
+    w->h = off;
+    off = up256(off + P * (size_t)I * 2);
+    w->c2 = off;
+    off = up256(off + P * (size_t)H * 4);
+    w->total = off;
+    return true;
+}
+}  // namespace
+
+extern "C" {
+
+size_t chord_layer_workspace_bytes(int T, int topk, int E, int H, int I, int block_m) {
+    if (T < 0 || topk <= 0 || E <= 0 || H <= 0 || I <= 0) return 0;
+    if (block_m <= 0) block_m = chord_select_block_m(T, topk, E, E, 2 * I, H);
+    LayerWs w;
+    return layer_ws(T, topk, E, H, I, block_m, &w) ? w.total : 0;
+}
+
+chord_status chord_moe_layer(const void* x, const int32_t* topk_ids, const float* topk_w, int T, int topk, int E,
+                             int E_global, int H, int I, const void* packed_w13, size_t w13_bytes,
+                             const void* packed_w2, size_t w2_bytes, int block_m, void* workspace,
+                             size_t workspace_bytes, void* out, const chord_opts* opts, void* stream) {
+    if (T < 0 || topk <= 0 || E <= 0 || H <= 0 || I <= 0) return CHORD_ERR_INVALID_ARG;
+    if (E_global <= 0) E_global = E;
+    if (block_m <= 0) block_m = chord_select_block_m(T, topk, E, E_global, 2 * I, H);
+    LayerWs w;
+    if (!layer_ws(T, topk, E, H, I, block_m, &w)) return CHORD_ERR_INVALID_ARG;
+    if (workspace_bytes < w.total) return CHORD_ERR_BUFFER_TOO_SMALL;
+    if (!workspace || !aligned16(workspace)) return CHORD_ERR_INVALID_ARG;
+    if (T == 0) return CHORD_OK;
+    if (!x || !topk_ids || !topk_w || !out) return CHORD_ERR_INVALID_ARG;
+    chord_opts o = opts_or_default(opts);
+    const int validate = o.validate;
+    o.validate = 0;  // validate once, at the end
+    o.out_dtype = CHORD_DTYPE_BF16;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    int32_t* counts = reinterpret_cast<int32_t*>(ws + w.counts);
+    int32_t* sorted = reinterpret_cast<int32_t*>(ws + w.sorted);
+    int32_t* experts = reinterpret_cast<int32_t*>(ws + w.experts);
+    int32_t* ntp = reinterpret_cast<int32_t*>(ws + w.ntp);
+    void* c1 = ws + w.c1;
+    void* h = ws + w.h;
+    void* c2 = ws + w.c2;
+    const int64_t P = (int64_t)T * topk;
+    const int64_t cap = chord_align_capacity(T, topk, E, block_m);
+    chord_status st;
+    st = chord_moe_align(topk_ids, T, topk, E, block_m, sorted, experts, ntp, cap, counts,
+                         chord_align_workspace_bytes(T, topk, E), &o, stream);
+    if (st != CHORD_OK) return st;
+    st = chord_w4a16_moe_gemm(x, T, topk, packed_w13, w13_bytes, E, 2 * I, H, sorted, experts, ntp, cap, block_m, P,
+                              c1, nullptr, 0, &o, stream);
+    if (st != CHORD_OK) return st;
+    st = chord_silu_mul(c1, topk_ids, P, E, I, h, stream);
+    if (st != CHORD_OK) return st;
+    chord_opts o_down = o;
+    o_down.out_dtype = CHORD_DTYPE_F32;
+    st = chord_w4a16_moe_gemm(h, P, 1, packed_w2, w2_bytes, E, H, I, sorted, experts, ntp, cap, block_m, P, c2,
+                              nullptr, 0, &o_down, stream);
+    if (st != CHORD_OK) return st;
+    st = chord_moe_combine(c2, CHORD_DTYPE_F32, topk_ids, topk_w, T, topk, E, H, out, stream);
+    if (st != CHORD_OK) return st;
+    o.validate = validate;
+    return finish(o, static_cast<cudaStream_t>(stream));
+}
+
+chord_status chord_get_device_error(void* stream, int32_t* code) {
+    if (!code) return CHORD_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return CHORD_ERR_CUDA;
+    int32_t v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_error_word, sizeof v) != cudaSuccess) return CHORD_ERR_CUDA;
+    const int32_t zero = 0;
+    if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof zero) != cudaSuccess) return CHORD_ERR_CUDA;
+    *code = v;
+    return CHORD_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,357 @@
+// Packing, routing alignment and the element-wise epilogues (SiLU * up, top-k
+// combine) of the W4A16 MoE library, sm_103a.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "chord_common.cuh"
+#include "chord_internal.h"
+
+namespace chord {
+
+// ============================================================================
+// Pack: canonical codes [E, N, K] + scales [E, N, K/32] -> layout 1.
+// One thread writes one 32-bit word of the blob, so the writes are coalesced;
+// the gathers from the canonical arrays are not, which is fine for a one-off
+// load-time step.
+// ============================================================================
+__global__ void pack_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ scales, int E, int N,
+                            int K, uint8_t* __restrict__ packed, int* err) {
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (tid < kHeaderBytes / 4) {
+        const unsigned long long stride = (unsigned long long)N * (unsigned long long)K * 9ull / 16ull;
+        uint32_t v = 0;
+        switch ((int)tid) {
+            case 0: v = kMagic; break;
+            case 1: v = 1u; break;
+            case 2: v = kLayoutVersion; break;
+            case 3: v = (uint32_t)kGroup; break;
+            case 4: v = (uint32_t)E; break;
+            case 5: v = (uint32_t)N; break;
+            case 6: v = (uint32_t)K; break;
+            case 8: v = (uint32_t)stride; break;
+            case 9: v = (uint32_t)(stride >> 32); break;
+            case 10: v = (uint32_t)kHeaderBytes; break;
+            default: v = 0u;
+        }
+        reinterpret_cast<uint32_t*>(packed)[tid] = v;
+    }
+    const int mtiles = N / 16;
+    const int64_t chunks_per_expert = (int64_t)(K / 64) * mtiles;
+    const int64_t words = (int64_t)E * chunks_per_expert * (kChunkBytes / 4);
+    const int G = K / kGroup;
+    uint32_t* out = reinterpret_cast<uint32_t*>(packed + kHeaderBytes);
+    for (int64_t w = tid; w < words; w += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t chunk = w / (kChunkBytes / 4);
+        const int wi = (int)(w % (kChunkBytes / 4));
+        const int64_t e = chunk / chunks_per_expert;
+        const int64_t cc = chunk % chunks_per_expert;
+        const int kc = (int)(cc / mtiles);
+        const int mt = (int)(cc % mtiles);
+        uint32_t v = 0;
+        if (wi < kChunkWeightBytes / 4) {
+            const int lane = wi / 4, j = wi % 4;
+            const int g = lane / 4, c = lane % 4;
+            const int64_t r0 = (int64_t)e * N + mt * 16 + g;
+            const int col = kc * 64 + 16 * j + 2 * c;
+            const uint8_t* p0 = codes + r0 * K + col;
+            const uint8_t* p1 = codes + (r0 + 8) * K + col;
+            // nibble i of the word: i=0 (g, col), 1 (g+8, col), 2 (g, col+8), 3 (g+8, col+8),
+            // i+4: the same with col+1.
+            const uint32_t n[8] = {p0[0], p1[0], p0[8], p1[8], p0[1], p1[1], p0[9], p1[9]};
+            uint32_t bad = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                bad |= n[i] >> 4;
+                v |= (n[i] & 0xFu) << (4 * i);
+            }
+            if (bad) set_error(err, CHORD_DEV_BAD_CODE);
+        } else {
+            const int s = wi - kChunkWeightBytes / 4;
+            const int h = s / 8, g = s % 8;
+            const int64_t r0 = (int64_t)e * N + mt * 16 + g;
+            const int grp = kc * 2 + h;
+            v = (uint32_t)scales[r0 * G + grp] | ((uint32_t)scales[(r0 + 8) * G + grp] << 16);
+        }
+        out[w] = v;
+    }
+}
+
+cudaError_t launch_pack(const uint8_t* codes, const uint16_t* scales, int E, int N, int K, uint8_t* packed, int* err,
+                        cudaStream_t stream) {
+    const int64_t words = (int64_t)E * (K / 64) * (N / 16) * (kChunkBytes / 4);
+    const int threads = 256;
+    int64_t blocks = ceil_div64(words > kHeaderBytes / 4 ? words : kHeaderBytes / 4, threads);
+    const int64_t cap = (int64_t)device_info().sm_count * 16;
+    if (blocks > cap) blocks = cap;
+    pack_kernel<<<(unsigned)blocks, threads, 0, stream>>>(codes, scales, E, N, K, packed, err);
+    return cudaGetLastError();
+}
+
+// ============================================================================
+// moe_align_block_size, deterministic: pairs of each expert in ascending pair
+// id.  Three launches:
+//   count:   per slice of kSlice pairs, an expert histogram; also fills
+//            sorted_ids with the sentinel;
+//   scan:    one CTA turns the histograms into each slice's starting offset per
+//            expert, writes expert_ids and num_tokens_padded;
+//   scatter: per slice, stable ranks within the slice (warp match + per-warp
+//            counts, warps in order) place each pair.
+// ============================================================================
+constexpr int kSlice = 4096;
+constexpr int kAlignThreads = 1024;
+constexpr int kAlignWarps = kAlignThreads / 32;
+
+int align_slices(int64_t P) { return P > 0 ? (int)ceil_div64(P, kSlice) : 1; }
+
+__global__ void __launch_bounds__(kAlignThreads) align_count_kernel(const int32_t* __restrict__ ids, int64_t P, int E,
+                                                                    int32_t* __restrict__ counts,
+                                                                    int32_t* __restrict__ sorted_ids,
+                                                                    int64_t capacity, int validate, int* err) {
+    extern __shared__ int32_t hist[];
+    for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    const int64_t base = (int64_t)blockIdx.x * kSlice;
+    for (int i = threadIdx.x; i < kSlice; i += blockDim.x) {
+        const int64_t p = base + i;
+        if (p >= P) break;
+        const int e = ids[p];
+        if (e >= 0 && e < E)
+            atomicAdd(&hist[e], 1);
+        else if (validate && e != -1)
+            set_error(err, CHORD_DEV_BAD_EXPERT);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < E; i += blockDim.x) counts[(int64_t)blockIdx.x * E + i] = hist[i];
+    const int32_t sentinel = (int32_t)P;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < capacity;
+         i += (int64_t)gridDim.x * blockDim.x)
+        sorted_ids[i] = sentinel;
+}
+
+__global__ void __launch_bounds__(kAlignThreads) align_scan_kernel(int32_t* __restrict__ counts, int nslices, int E,
+                                                                   int block_m, int32_t* __restrict__ expert_ids,
+                                                                   int64_t nblocks_cap, int32_t* __restrict__ ntp) {
+    __shared__ int32_t warp_sums[kAlignWarps];
+    __shared__ int32_t total_padded;
+    const int e = threadIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int32_t total = 0;
+    if (e < E) {
+        for (int s = 0; s < nslices; ++s) {
+            const int32_t v = counts[(int64_t)s * E + e];
+            counts[(int64_t)s * E + e] = total;
+            total += v;
+        }
+    }
+    const int32_t padded = (e < E) ? (total + block_m - 1) / block_m * block_m : 0;
+    // exclusive scan of `padded` over the CTA
+    int32_t x = padded;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int32_t w = warp_sums[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        warp_sums[lane] = w;  // inclusive
+        if (lane == 31) total_padded = w;
+    }
+    __syncthreads();
+    const int32_t offset = x - padded + (warp > 0 ? warp_sums[warp - 1] : 0);
+    if (e < E) {
+        for (int s = 0; s < nslices; ++s) counts[(int64_t)s * E + e] += offset;
+        for (int32_t b = offset / block_m; b < (offset + padded) / block_m; ++b) expert_ids[b] = e;
+    }
+    const int32_t tp = total_padded;
+    for (int64_t b = tp / block_m + threadIdx.x; b < nblocks_cap; b += blockDim.x) expert_ids[b] = -1;
+    if (threadIdx.x == 0) *ntp = tp;
+}
+
+__global__ void __launch_bounds__(kAlignThreads) align_scatter_kernel(const int32_t* __restrict__ ids, int64_t P,
+                                                                      int E, const int32_t* __restrict__ counts,
+                                                                      int32_t* __restrict__ sorted_ids) {
+    extern __shared__ int32_t sm[];
+    int32_t* run = sm;           // [E]   next free slot per expert
+    int32_t* wcnt = sm + E;      // [kAlignWarps][E]
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < E; i += blockDim.x) run[i] = counts[(int64_t)blockIdx.x * E + i];
+    const unsigned lt_mask = (1u << lane) - 1u;
+    const int64_t base = (int64_t)blockIdx.x * kSlice;
+    for (int r = 0; r < kSlice / kAlignThreads; ++r) {
+        for (int i = threadIdx.x; i < kAlignWarps * E; i += blockDim.x) wcnt[i] = 0;
+        __syncthreads();
+        const int64_t p = base + (int64_t)r * kAlignThreads + threadIdx.x;
+        int e = (p < P) ? ids[p] : -1;
+        const bool valid = (e >= 0 && e < E);
+        if (!valid) e = -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int rank = __popc(peers & lt_mask);
+        if (valid && rank == 0) wcnt[warp * E + e] = __popc(peers);
+        __syncthreads();
+        for (int x = threadIdx.x; x < E; x += blockDim.x) {
+            int32_t acc = run[x];
+            for (int w = 0; w < kAlignWarps; ++w) {
+                const int32_t v = wcnt[w * E + x];
+                wcnt[w * E + x] = acc;
+                acc += v;
+            }
+            run[x] = acc;
+        }
+        __syncthreads();
+        if (valid) sorted_ids[wcnt[warp * E + e] + rank] = (int32_t)p;
+        __syncthreads();
+    }
+}
+
+cudaError_t launch_align(const int32_t* topk_ids, int64_t P, int E, int block_m, int32_t* sorted_ids,
+                         int32_t* expert_ids, int32_t* ntp, int64_t capacity, int32_t* counts, bool validate, int* err,
+                         cudaStream_t stream) {
+    const int nslices = align_slices(P);
+    const size_t hist_smem = (size_t)E * sizeof(int32_t);
+    const size_t scatter_smem = (size_t)(E + kAlignWarps * E) * sizeof(int32_t);
+    static bool attr_done[64] = {false};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !attr_done[dev]) {
+        cudaError_t e1 = cudaFuncSetAttribute(align_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              (int)((1024 + kAlignWarps * 1024) * sizeof(int32_t)));
+        if (e1 != cudaSuccess) return e1;
+        attr_done[dev] = true;
+    }
+    align_count_kernel<<<nslices, kAlignThreads, hist_smem, stream>>>(topk_ids, P, E, counts, sorted_ids, capacity,
+                                                                      validate ? 1 : 0, err);
+    cudaError_t st = cudaGetLastError();
+    if (st != cudaSuccess) return st;
+    align_scan_kernel<<<1, kAlignThreads, 0, stream>>>(counts, nslices, E, block_m, expert_ids, capacity / block_m,
+                                                       ntp);
+    st = cudaGetLastError();
+    if (st != cudaSuccess) return st;
+    if (P > 0) {
+        align_scatter_kernel<<<nslices, kAlignThreads, scatter_smem, stream>>>(topk_ids, P, E, counts, sorted_ids);
+        st = cudaGetLastError();
+    }
+    return st;
+}
+
+// ============================================================================
+// SiLU * up: h[p, j] = bf16_rne(g / (1 + exp(-g)) * u), FP32 math, 8 columns
+// per thread with 16-byte loads and stores.
+// ============================================================================
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 r = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&r);
+}
+
+__device__ __forceinline__ float silu_times(float g, float u) {
+    const float s = __fdiv_rn(g, __fadd_rn(1.0f, expf(-g)));
+    return __fmul_rn(s, u);
+}
+
+__global__ void silu_mul_kernel(const uint16_t* __restrict__ C1, const int32_t* __restrict__ ids, int64_t P, int E,
+                                int I, uint16_t* __restrict__ h) {
+    const int vpr = I / 8;  // vectors per row
+    const int64_t nvec = P * vpr;
+    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nvec; v += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t p = v / vpr;
+        const int j = (int)(v % vpr) * 8;
+        const int e = ids[p];
+        if (e < 0 || e >= E) continue;
+        const uint4 gv = *reinterpret_cast<const uint4*>(C1 + p * 2 * I + j);
+        const uint4 uv = *reinterpret_cast<const uint4*>(C1 + p * 2 * I + I + j);
+        uint4 o;
+        o.x = pack_bf16x2(silu_times(bf16_lo(gv.x), bf16_lo(uv.x)), silu_times(bf16_hi(gv.x), bf16_hi(uv.x)));
+        o.y = pack_bf16x2(silu_times(bf16_lo(gv.y), bf16_lo(uv.y)), silu_times(bf16_hi(gv.y), bf16_hi(uv.y)));
+        o.z = pack_bf16x2(silu_times(bf16_lo(gv.z), bf16_lo(uv.z)), silu_times(bf16_hi(gv.z), bf16_hi(uv.z)));
+        o.w = pack_bf16x2(silu_times(bf16_lo(gv.w), bf16_lo(uv.w)), silu_times(bf16_hi(gv.w), bf16_hi(uv.w)));
+        *reinterpret_cast<uint4*>(h + p * I + j) = o;
+    }
+}
+
+cudaError_t launch_silu_mul(const uint16_t* C1, const int32_t* topk_ids, int64_t P, int E, int I, uint16_t* h,
+                            cudaStream_t stream) {
+    const int64_t nvec = P * (I / 8);
+    if (nvec == 0) return cudaSuccess;
+    const int threads = 256;
+    int64_t blocks = ceil_div64(nvec, threads);
+    const int64_t cap = (int64_t)device_info().sm_count * 8;
+    if (blocks > cap) blocks = cap;
+    silu_mul_kernel<<<(unsigned)blocks, threads, 0, stream>>>(C1, topk_ids, P, E, I, h);
+    return cudaGetLastError();
+}
+
+// ============================================================================
+// Top-k weighted combine: out[t, n] = bf16_rne(sum_k w[t,k] * C2[t*topk+k, n])
+// over local k in ascending order, FP32 from +0, each product and each sum
+// rounded separately (no fused multiply-add), 8 columns per thread; C2 in bf16
+// or in FP32.
+// ============================================================================
+template <bool F32>
+__global__ void combine_kernel(const void* __restrict__ C2v, const int32_t* __restrict__ ids,
+                               const float* __restrict__ w, int T, int topk, int E, int H, uint16_t* __restrict__ out) {
+    const int vpr = H / 8;
+    const int64_t nvec = (int64_t)T * vpr;
+    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nvec; v += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = v / vpr;
+        const int n = (int)(v % vpr) * 8;
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+        for (int k = 0; k < topk; ++k) {
+            const int64_t p = t * topk + k;
+            const int e = ids[p];
+            if (e < 0 || e >= E) continue;
+            const float wk = w[p];
+            float c[8];
+            if constexpr (F32) {
+                const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(C2v) + p * H + n);
+                const float4 a = src[0], b = src[1];
+                c[0] = a.x; c[1] = a.y; c[2] = a.z; c[3] = a.w;
+                c[4] = b.x; c[5] = b.y; c[6] = b.z; c[7] = b.w;
+            } else {
+                const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(C2v) + p * H + n);
+                const uint32_t cw[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    c[2 * i] = bf16_lo(cw[i]);
+                    c[2 * i + 1] = bf16_hi(cw[i]);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], __fmul_rn(wk, c[i]));
+        }
+        uint4 o;
+        o.x = pack_bf16x2(acc[0], acc[1]);
+        o.y = pack_bf16x2(acc[2], acc[3]);
+        o.z = pack_bf16x2(acc[4], acc[5]);
+        o.w = pack_bf16x2(acc[6], acc[7]);
+        *reinterpret_cast<uint4*>(out + t * H + n) = o;
+    }
+}
+
+cudaError_t launch_combine(const void* C2, bool c2_f32, const int32_t* topk_ids, const float* topk_w, int T,
+                           int topk, int E, int H, uint16_t* out, cudaStream_t stream) {
+    const int64_t nvec = (int64_t)T * (H / 8);
+    if (nvec == 0) return cudaSuccess;
+    const int threads = 256;
+    int64_t blocks = ceil_div64(nvec, threads);
+    const int64_t cap = (int64_t)device_info().sm_count * 8;
+    if (blocks > cap) blocks = cap;
+    if (c2_f32)
+        combine_kernel<true><<<(unsigned)blocks, threads, 0, stream>>>(C2, topk_ids, topk_w, T, topk, E, H, out);
+    else
+        combine_kernel<false><<<(unsigned)blocks, threads, 0, stream>>>(C2, topk_ids, topk_w, T, topk, E, H, out);
+    return cudaGetLastError();
+}
+
+}  // namespace chord

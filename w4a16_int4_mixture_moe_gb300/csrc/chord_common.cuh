@@ -1,0 +1,161 @@
+// Device helpers shared by the sm_103a kernels of the W4A16 MoE library:
+// packed-layout constants, the sticky error word, mbarrier / bulk-copy
+// wrappers (inline PTX), bounded waits.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/chord.h"
+
+namespace chord {
+
+// ---- packed weight layout 1 -------------------------------------------------
+// 256-byte header, then per expert a grid of 576-byte chunks: chunk (kc, mt)
+// at ((kc * N/16) + mt) * 576 covers 16 rows of N and 64 columns of K.  Bytes
+// [0, 512) hold 128 words, word lane*4 + j (k16 step j) carrying the 8 codes of
+// the m16n8k16 A fragment of that lane; bytes [512, 576) hold 16 words of
+// scale pairs (row g, row g+8) for the two 32-column groups of the chunk.
+constexpr int kHeaderBytes = 256;
+constexpr uint32_t kMagic = 0x44524843u;  // "CHRD"
+constexpr uint32_t kLayoutVersion = 1;
+constexpr int kChunkBytes = 576;
+constexpr int kChunkWeightBytes = 512;
+constexpr int kGroup = 32;
+
+// ---- error word -----------------------------------------------------------
+__device__ __forceinline__ void set_error(int* err, int code) {
+    if (err) atomicCAS(err, 0, code);
+}
+
+// Wait bound for every spin on an mbarrier: after this many SM clocks the
+// waiter records CHORD_DEV_TIMEOUT and gives up (about 2 s at 2 GHz).
+constexpr long long kWaitLimitCycles = 4000000000LL;
+
+// ---- shared memory / mbarrier ------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete.  Returns false when
+// the bound ran out (the caller records the error and leaves).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > kWaitLimitCycles) return false;
+    }
+    return true;
+}
+
+// Bulk (non-tensor) async copy global -> this CTA's shared memory; completion
+// is counted in bytes on `bar`.  Addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(smem_dst)),
+        "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Same, with an L2 eviction-priority hint (weights are streamed once).
+__device__ __forceinline__ void bulk_g2s_hint(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar,
+                                              uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+        "%4;" ::"r"(smem_u32(smem_dst)),
+        "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// ---- packed header check ----------------------------------------------------
+__device__ __forceinline__ bool header_ok(const uint8_t* blob, int E, int N, int K) {
+    const uint32_t* h = reinterpret_cast<const uint32_t*>(blob);
+    const unsigned long long* h64 = reinterpret_cast<const unsigned long long*>(blob + 32);
+    const unsigned long long stride = (unsigned long long)N * (unsigned long long)K * 9ull / 16ull;
+    return h[0] == kMagic && h[1] == 1u && h[2] == kLayoutVersion && h[3] == (uint32_t)kGroup &&
+           h[4] == (uint32_t)E && h[5] == (uint32_t)N && h[6] == (uint32_t)K && h64[0] == stride &&
+           h64[1] == (unsigned long long)kHeaderBytes;
+}
+
+// ---- bf16 packing helpers ---------------------------------------------------
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t x, uint32_t mask, uint32_t magic) {
+    uint32_t r;
+    // (x & mask) | magic
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(x), "r"(mask), "r"(magic));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %1, %2;" : "=r"(r) : "r"(a), "r"(sel));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t bf2_as_u32(__nv_bfloat162 v) { return *reinterpret_cast<uint32_t*>(&v); }
+__device__ __forceinline__ __nv_bfloat162 u32_as_bf2(uint32_t v) { return *reinterpret_cast<__nv_bfloat162*>(&v); }
+
+// Four A-fragment registers (bf16x2) of one k16 step from the packed word `w`
+// and the scale pair `sp` (low half: scale of row g, high half: row g+8).
+// Each value is bf16_rne((q - 8) * s): 0x4300 | q is the bf16 number 128 + q,
+// subtracting 136 gives q - 8 exactly, and one bf16x2 multiply rounds the
+// exact product once, to nearest even.
+__device__ __forceinline__ void dequant_frag(uint32_t w, uint32_t sp, uint32_t (&a)[4]) {
+    const __nv_bfloat162 off = u32_as_bf2(0x43084308u);  // (136, 136)
+    const __nv_bfloat162 s_lo = u32_as_bf2(prmt(sp, 0x1010u));
+    const __nv_bfloat162 s_hi = u32_as_bf2(prmt(sp, 0x3232u));
+    const uint32_t q0 = lop3_and_or(w, 0x000F000Fu, 0x43004300u);        // n0, n4: row g,   k 2c, 2c+1
+    const uint32_t q1 = lop3_and_or(w >> 4, 0x000F000Fu, 0x43004300u);   // n1, n5: row g+8, k 2c, 2c+1
+    const uint32_t q2 = lop3_and_or(w >> 8, 0x000F000Fu, 0x43004300u);   // n2, n6: row g,   k 2c+8, 2c+9
+    const uint32_t q3 = lop3_and_or(w >> 12, 0x000F000Fu, 0x43004300u);  // n3, n7: row g+8, k 2c+8, 2c+9
+    a[0] = bf2_as_u32(__hmul2(__hsub2(u32_as_bf2(q0), off), s_lo));
+    a[1] = bf2_as_u32(__hmul2(__hsub2(u32_as_bf2(q1), off), s_hi));
+    a[2] = bf2_as_u32(__hmul2(__hsub2(u32_as_bf2(q2), off), s_lo));
+    a[3] = bf2_as_u32(__hmul2(__hsub2(u32_as_bf2(q3), off), s_hi));
+}
+
+__host__ __device__ __forceinline__ int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace chord

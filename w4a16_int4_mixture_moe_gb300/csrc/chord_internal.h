@@ -1,0 +1,60 @@
+// Host-side launchers shared between the library's translation units.  Every
+// launcher only enqueues on `stream` and returns the launch status.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace chord {
+
+struct DeviceInfo {
+    int sm_count = 0;
+    int max_smem_optin = 0;
+    int* err = nullptr;  // device address of this device's sticky error word
+};
+
+// Per-device facts, fetched once per device (thread-safe).
+const DeviceInfo& device_info();
+
+// ---- pack / align / epilogues (chord_aux.cu) -------------------------------
+cudaError_t launch_pack(const uint8_t* codes, const uint16_t* scales, int E, int N, int K, uint8_t* packed,
+                        int* err, cudaStream_t stream);
+
+int align_slices(int64_t P);
+cudaError_t launch_align(const int32_t* topk_ids, int64_t P, int E, int block_m, int32_t* sorted_ids,
+                         int32_t* expert_ids, int32_t* ntp, int64_t capacity, int32_t* counts, bool validate,
+                         int* err, cudaStream_t stream);
+
+cudaError_t launch_silu_mul(const uint16_t* C1, const int32_t* topk_ids, int64_t P, int E, int I, uint16_t* h,
+                            cudaStream_t stream);
+cudaError_t launch_combine(const void* C2, bool c2_f32, const int32_t* topk_ids, const float* topk_w, int T,
+                           int topk, int E, int H, uint16_t* out, cudaStream_t stream);
+
+// ---- GEMMs ---------------------------------------------------------------
+struct GemmArgs {
+    const uint16_t* A;
+    int64_t a_rows;
+    int a_row_divisor;
+    const uint8_t* packed;  // blob start (header at offset 0)
+    int E, N, K;
+    const int32_t* sorted_ids;
+    const int32_t* expert_ids;
+    const int32_t* ntp;
+    int64_t capacity;
+    int block_m;
+    int64_t num_pairs;
+    void* C;        // bf16 [num_pairs, N], or float when out_f32
+    int out_f32;
+    int* err;
+};
+
+// Decode regime: tokens of a block in the MMA N dimension (mma.sync m16n8k16),
+// INT4 streamed through a bulk-copy pipeline.  block_m % 8 == 0.
+cudaError_t launch_gemm_decode(const GemmArgs& a, cudaStream_t stream);
+
+// Prefill regime: tcgen05 MMA with TMEM accumulators.  block_m % 16 == 0,
+// block_m <= 256.
+cudaError_t launch_gemm_prefill(const GemmArgs& a, cudaStream_t stream);
+bool prefill_available();
+
+}  // namespace chord
