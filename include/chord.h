@@ -147,6 +147,35 @@ chord_status chord_moe_align(const int32_t *topk_ids, int T, int topk, int E, in
                              void *workspace, size_t workspace_bytes,
                              const chord_opts *opts, void *stream);
 
+/* moe_align_block_size for callers that cannot allocate device memory.  The
+ * article has no counterpart to this entry point; it exists for callers that
+ * cannot hand the library a scratch buffer: code running while a CUDA graph is
+ * captured in a mode that forbids allocation, inference-engine plugins limited
+ * to the buffers the engine gives them, and serving loops that avoid
+ * cudaMalloc / cudaFree because those synchronise the device.
+ *
+ * Same arguments, results and errors as chord_moe_align, without the
+ * workspace: the per-slice histograms live in a fixed array of
+ * CHORD_NOALLOC_ALIGN_SCRATCH_ENTRIES int32 (256 KiB) in the library's device
+ * memory, which every GPU that loads the library holds until the process
+ * exits.  The call needs ceil(T * topk / 4096) * E entries (at least E) and
+ * returns CHORD_ERR_BUFFER_TOO_SMALL above the limit (for example E = 384
+ * allows T * topk up to 696,320 pairs; E = 1024 up to 262,144).  It allocates
+ * nothing.
+ *   - The first call on a device looks up the array's device address (once per
+ *     device, with that device current); make that first call before any
+ *     stream capture.
+ *   - All calls on a device share the one array.  Calls whose work overlaps
+ *     on the GPU (on different streams, or from several threads) race on it
+ *     and may produce wrong routing; serialise them.
+ *   - Each call overwrites every scratch entry it reads, so no state from an
+ *     earlier call leaks into its result. */
+#define CHORD_NOALLOC_ALIGN_SCRATCH_ENTRIES 65536
+chord_status chord_moe_align_noalloc(const int32_t *topk_ids, int T, int topk, int E, int block_m,
+                                     int32_t *sorted_ids, int32_t *expert_ids,
+                                     int32_t *num_tokens_padded, int64_t capacity,
+                                     const chord_opts *opts, void *stream);
+
 /* Host-side block size choice from tokens per expert (the article's tok_e =
  * routed rows / experts rule, section "Indexed kernels"): tok_e = T * topk /
  * E_global is the expected number of rows per local expert, known without

@@ -55,6 +55,7 @@ _SIGS = {
     "chord_align_capacity": (_i64, [_int, _int, _int, _int]),
     "chord_align_workspace_bytes": (_sz, [_int, _int, _int]),
     "chord_moe_align": (_int, [_vp, _int, _int, _int, _int, _vp, _vp, _vp, _i64, _vp, _sz, _OPTS, _vp]),
+    "chord_moe_align_noalloc": (_int, [_vp, _int, _int, _int, _int, _vp, _vp, _vp, _i64, _OPTS, _vp]),
     "chord_select_block_m": (_int, [_int, _int, _int, _int, _int, _int]),
     "chord_gemm_workspace_bytes": (_sz, [_i64, _int, _int, _int, _OPTS]),
     "chord_w4a16_moe_gemm": (_int, [_vp, _i64, _int, _vp, _sz, _int, _int, _int, _vp, _vp, _vp, _i64, _int, _i64,
@@ -149,6 +150,17 @@ def chord_moe_align(topk_ids, E: int, block_m: int, sorted_ids, expert_ids, num_
                                   _p(num_tokens_padded), sorted_ids.numel(), _p(workspace),
                                   _nbytes(workspace) if workspace is not None else 0, _o(opts), _s(stream)),
            "chord_moe_align")
+
+
+def chord_moe_align_noalloc(topk_ids, E: int, block_m: int, sorted_ids, expert_ids, num_tokens_padded,
+                            opts=None, stream=None):
+    """chord_moe_align without a workspace, for callers that cannot allocate:
+    its scratch is a fixed 256 KiB array inside the library (see chord.h for the
+    size limit and for why overlapping calls must be serialised)."""
+    T, topk = topk_ids.shape
+    _check(load().chord_moe_align_noalloc(_p(topk_ids), T, topk, E, block_m, _p(sorted_ids), _p(expert_ids),
+                                          _p(num_tokens_padded), sorted_ids.numel(), _o(opts), _s(stream)),
+           "chord_moe_align_noalloc")
 
 
 def chord_select_block_m(T: int, topk: int, E_local: int, E_global: int, N: int, K: int) -> int:
