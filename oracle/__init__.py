@@ -75,10 +75,10 @@ def lib():
                 "orc_bf16_round": (ctypes.c_uint16, [ctypes.c_float]),
                 "orc_dequant": (ctypes.c_uint16, [ctypes.c_uint8, ctypes.c_uint16]),
                 "orc_dequant_pairs": (None, [u8p, u16p, c_sz, u16p]),
-                "orc_packed_bytes": (c_sz, [c_int, c_int, c_int]),
-                "orc_pack": (c_int, [u8p, u16p, c_int, c_int, c_int, u8p, c_sz]),
-                "orc_check_header": (c_int, [u8p, c_int, c_int, c_int]),
-                "orc_unpack": (c_int, [u8p, c_sz, c_int, c_int, c_int, u8p, u16p]),
+                "orc_packed_bytes": (c_sz, [c_int, c_int, c_int, c_int]),
+                "orc_pack": (c_int, [u8p, u16p, c_int, c_int, c_int, c_int, u8p, c_sz]),
+                "orc_check_header": (c_int, [u8p, c_int, c_int, c_int, c_int]),
+                "orc_unpack": (c_int, [u8p, c_sz, c_int, c_int, c_int, c_int, u8p, u16p]),
                 "orc_align_capacity": (c_i64, [c_int, c_int, c_int, c_int]),
                 "orc_moe_align": (c_int, [i32p, c_int, c_int, c_int, c_int, i32p, i32p, i32p, c_i64]),
                 "orc_moe_gemm": (c_int, [u16p, c_i64, c_int, u8p, u16p, c_int, c_int, c_int,
@@ -141,36 +141,36 @@ def dequant_pairs(q: np.ndarray, s: np.ndarray) -> np.ndarray:
 
 # --- packing --------------------------------------------------------------
 
-def packed_bytes(E: int, N: int, K: int) -> int:
-    return int(lib().orc_packed_bytes(E, N, K))
+def packed_bytes(E: int, N: int, K: int, layout: int = 2) -> int:
+    return int(lib().orc_packed_bytes(E, N, K, layout))
 
 
-def pack(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+def pack(codes: np.ndarray, scales: np.ndarray, layout: int = 2) -> np.ndarray:
     codes = _c(codes, np.uint8)
     scales = _c(scales, np.uint16)
     E, N, K = codes.shape
     assert scales.shape == (E, N, K // GROUP)
-    nb = packed_bytes(E, N, K)
+    nb = packed_bytes(E, N, K, layout)
     if nb == 0:
         raise OracleError("unsupported shape for packing")
     out = np.empty(nb, np.uint8)
-    _check(lib().orc_pack(_ptr(codes, ctypes.c_uint8), _ptr(scales, ctypes.c_uint16), E, N, K,
+    _check(lib().orc_pack(_ptr(codes, ctypes.c_uint8), _ptr(scales, ctypes.c_uint16), E, N, K, layout,
                           _ptr(out, ctypes.c_uint8), nb), "pack")
     return out
 
 
-def unpack(blob: np.ndarray, E: int, N: int, K: int):
+def unpack(blob: np.ndarray, E: int, N: int, K: int, layout: int = 2):
     blob = _c(blob, np.uint8)
     codes = np.empty((E, N, K), np.uint8)
     scales = np.empty((E, N, K // GROUP), np.uint16)
-    _check(lib().orc_unpack(_ptr(blob, ctypes.c_uint8), blob.size, E, N, K,
+    _check(lib().orc_unpack(_ptr(blob, ctypes.c_uint8), blob.size, E, N, K, layout,
                             _ptr(codes, ctypes.c_uint8), _ptr(scales, ctypes.c_uint16)), "unpack")
     return codes, scales
 
 
-def check_header(blob: np.ndarray, E: int, N: int, K: int) -> bool:
+def check_header(blob: np.ndarray, E: int, N: int, K: int, layout: int = 2) -> bool:
     blob = _c(blob, np.uint8)
-    return lib().orc_check_header(_ptr(blob, ctypes.c_uint8), E, N, K) == OK
+    return lib().orc_check_header(_ptr(blob, ctypes.c_uint8), E, N, K, layout) == OK
 
 
 # --- routing --------------------------------------------------------------

@@ -104,12 +104,16 @@ void orc_dequant_pairs(const uint8_t *q, const uint16_t *s, size_t n, uint16_t *
 }
 
 /* ------------------------------------------------------------------------ */
-/* Packed weight layout, version 1 ("m16 x k64 fragment chunks").
+/* Packed weight layouts.  The article records the packing mode in the
+ * prepared weight and checks it when the weight is used; here the header
+ * records the layout.
  *
  * blob  = 256-byte header, then E expert regions of N*K*9/16 bytes each.
  * header (little endian): u32 magic 0x44524843 ("CHRD"), u32 version 1,
- *        u32 layout 1, u32 group 32, u32 E, u32 N, u32 K, u32 0,
+ *        u32 layout (1 or 2), u32 group 32, u32 E, u32 N, u32 K, u32 0,
  *        u64 expert_stride = N*K*9/16, u64 data_offset = 256, then zeros.
+ *
+ * Layout 1 ("m16 x k64 fragment chunks", N % 16 == 0, K % 64 == 0).
  * An expert region is a sequence of 576-byte chunks, chunk (kc, mt) at
  * ((kc * N/16) + mt) * 576, for kc < K/64 (64 columns of K) and mt < N/16
  * (16 rows of N).  Within a chunk:
@@ -124,15 +128,38 @@ void orc_dequant_pairs(const uint8_t *q, const uint16_t *s, size_t n, uint16_t *
  *   bytes [512, 576): 16 words, word (h*8 + g) for h < 2, g < 8 holds the bf16
  *       scale of row g in its low half and of row g+8 in its high half, for
  *       the group of 32 columns 64*kc + 32*h .. +31.
+ *
+ * Layout 2 ("128-row x k64 chunks", N % 128 == 0, K % 64 == 0).
+ * An expert region is a sequence of 4608-byte chunks, chunk (nt, kc) at
+ * ((nt * K/64) + kc) * 4608, for nt < N/128 (128 rows) and kc < K/64.  Within
+ * a chunk, with r the row in the tile and c the column in the chunk:
+ *   bytes [0, 4096): half h = c/32 at h*2048, then row r at r*16, then word
+ *       j = (c%32)/8 at j*4 (little endian); column 8j + m of the half sits
+ *       in nibble i of that word with m = 2*(i%4) + i/4, i.e. nibbles
+ *       0,4,1,5,2,6,3,7 hold columns +0..+7.
+ *   bytes [4096, 4608): the bf16 scale of row r, group h (columns 32h..32h+31
+ *       of the chunk) at 4096 + r*4 + h*2.
  */
 
 #define ORC_HDR 256u
 #define ORC_MAGIC 0x44524843u
-#define ORC_CHUNK 576u
+#define ORC_CHUNK1 576u
+#define ORC_CHUNK2 4608u
 
-size_t orc_packed_bytes(int E, int N, int K)
+static int layout_ok(int layout, int N, int K)
 {
-    if (E < 0 || N <= 0 || K <= 0 || N % 16 || K % 64)
+    if (N <= 0 || K <= 0 || K % 64)
+        return 0;
+    if (layout == 1)
+        return N % 16 == 0;
+    if (layout == 2)
+        return N % 128 == 0;
+    return 0;
+}
+
+size_t orc_packed_bytes(int E, int N, int K, int layout)
+{
+    if (E < 0 || !layout_ok(layout, N, K))
         return 0;
     return (size_t)ORC_HDR + (size_t)E * (size_t)N * (size_t)K * 9u / 16u;
 }
@@ -150,40 +177,55 @@ static uint64_t get64(const uint8_t *p) { return (uint64_t)get32(p) | (uint64_t)
 
 /* Byte offset (from the start of the expert region) and nibble shift of the
  * code of row n, column k. */
-static void code_pos(int N, int n, int k, size_t *byte, int *shift)
+static void code_pos(int layout, int N, int K, int n, int k, size_t *byte, int *shift)
 {
-    int mt = n / 16, r = n % 16, kc = k / 64, kk = k % 64;
-    int j = kk / 16, kq = kk % 16;
-    int g = r % 8, lower = r / 8;             /* lower: 0 = row g, 1 = row g+8 */
-    int kpart = kq / 8, c = (kq % 8) / 2, odd = kq % 2;
-    int lane = 4 * g + c;
-    int word = lane * 4 + j;
-    int i = kpart * 2 + lower + 4 * odd;
-    *byte = ((size_t)kc * (size_t)(N / 16) + (size_t)mt) * ORC_CHUNK + (size_t)word * 4u + (size_t)(i / 2);
-    *shift = (i % 2) * 4;
+    if (layout == 1) {
+        int mt = n / 16, r = n % 16, kc = k / 64, kk = k % 64;
+        int j = kk / 16, kq = kk % 16;
+        int g = r % 8, lower = r / 8;             /* lower: 0 = row g, 1 = row g+8 */
+        int kpart = kq / 8, c = (kq % 8) / 2, odd = kq % 2;
+        int lane = 4 * g + c;
+        int word = lane * 4 + j;
+        int i = kpart * 2 + lower + 4 * odd;
+        *byte = ((size_t)kc * (size_t)(N / 16) + (size_t)mt) * ORC_CHUNK1 + (size_t)word * 4u + (size_t)(i / 2);
+        *shift = (i % 2) * 4;
+    } else {
+        int nt = n / 128, r = n % 128, kc = k / 64, c = k % 64;
+        int h = c / 32, j = (c % 32) / 8, m = c % 8;
+        int i = (m % 2) * 4 + m / 2;              /* inverse of m = 2*(i%4) + i/4 */
+        *byte = ((size_t)nt * (size_t)(K / 64) + (size_t)kc) * ORC_CHUNK2 + (size_t)h * 2048u
+                + (size_t)r * 16u + (size_t)j * 4u + (size_t)(i / 2);
+        *shift = (i % 2) * 4;
+    }
 }
 
 /* Byte offset (from the start of the expert region) of the scale of row n,
  * group grp (columns 32*grp .. 32*grp+31). */
-static size_t scale_pos(int N, int n, int grp)
+static size_t scale_pos(int layout, int N, int K, int n, int grp)
 {
-    int mt = n / 16, r = n % 16, kc = grp / 2, h = grp % 2;
-    int g = r % 8, lower = r / 8;
-    return ((size_t)kc * (size_t)(N / 16) + (size_t)mt) * ORC_CHUNK + 512u
-           + (size_t)(h * 8 + g) * 4u + (size_t)lower * 2u;
+    if (layout == 1) {
+        int mt = n / 16, r = n % 16, kc = grp / 2, h = grp % 2;
+        int g = r % 8, lower = r / 8;
+        return ((size_t)kc * (size_t)(N / 16) + (size_t)mt) * ORC_CHUNK1 + 512u
+               + (size_t)(h * 8 + g) * 4u + (size_t)lower * 2u;
+    } else {
+        int nt = n / 128, r = n % 128, kc = grp / 2, h = grp % 2;
+        return ((size_t)nt * (size_t)(K / 64) + (size_t)kc) * ORC_CHUNK2 + 4096u + (size_t)r * 4u
+               + (size_t)h * 2u;
+    }
 }
 
-int orc_pack(const uint8_t *codes, const uint16_t *scales, int E, int N, int K,
+int orc_pack(const uint8_t *codes, const uint16_t *scales, int E, int N, int K, int layout,
              uint8_t *out, size_t out_bytes)
 {
-    size_t need = orc_packed_bytes(E, N, K);
+    size_t need = orc_packed_bytes(E, N, K, layout);
     if (need == 0 || out_bytes < need)
         return ORC_EINVAL;
     memset(out, 0, need);
     uint64_t stride = (uint64_t)N * (uint64_t)K * 9u / 16u;
     put32(out + 0, ORC_MAGIC);
     put32(out + 4, 1u);
-    put32(out + 8, 1u);
+    put32(out + 8, (uint32_t)layout);
     put32(out + 12, ORC_GROUP);
     put32(out + 16, (uint32_t)E);
     put32(out + 20, (uint32_t)N);
@@ -199,12 +241,12 @@ int orc_pack(const uint8_t *codes, const uint16_t *scales, int E, int N, int K,
                 if (q > 15)
                     return ORC_ERANGE;
                 size_t b; int sh;
-                code_pos(N, n, k, &b, &sh);
+                code_pos(layout, N, K, n, k, &b, &sh);
                 reg[b] |= (uint8_t)(q << sh);
             }
             for (int grp = 0; grp < G; ++grp) {
                 uint16_t s = scales[((size_t)e * N + n) * G + grp];
-                size_t b = scale_pos(N, n, grp);
+                size_t b = scale_pos(layout, N, K, n, grp);
                 reg[b] = (uint8_t)s;
                 reg[b + 1] = (uint8_t)(s >> 8);
             }
@@ -213,9 +255,9 @@ int orc_pack(const uint8_t *codes, const uint16_t *scales, int E, int N, int K,
     return ORC_OK;
 }
 
-int orc_check_header(const uint8_t *blob, int E, int N, int K)
+int orc_check_header(const uint8_t *blob, int E, int N, int K, int layout)
 {
-    if (get32(blob + 0) != ORC_MAGIC || get32(blob + 4) != 1u || get32(blob + 8) != 1u
+    if (get32(blob + 0) != ORC_MAGIC || get32(blob + 4) != 1u || get32(blob + 8) != (uint32_t)layout
         || get32(blob + 12) != ORC_GROUP || get32(blob + 16) != (uint32_t)E
         || get32(blob + 20) != (uint32_t)N || get32(blob + 24) != (uint32_t)K
         || get64(blob + 32) != (uint64_t)N * (uint64_t)K * 9u / 16u || get64(blob + 40) != ORC_HDR)
@@ -223,13 +265,13 @@ int orc_check_header(const uint8_t *blob, int E, int N, int K)
     return ORC_OK;
 }
 
-int orc_unpack(const uint8_t *blob, size_t blob_bytes, int E, int N, int K,
+int orc_unpack(const uint8_t *blob, size_t blob_bytes, int E, int N, int K, int layout,
                uint8_t *codes, uint16_t *scales)
 {
-    size_t need = orc_packed_bytes(E, N, K);
+    size_t need = orc_packed_bytes(E, N, K, layout);
     if (need == 0 || blob_bytes < need)
         return ORC_EINVAL;
-    if (orc_check_header(blob, E, N, K) != ORC_OK)
+    if (orc_check_header(blob, E, N, K, layout) != ORC_OK)
         return ORC_ELAYOUT;
     uint64_t stride = (uint64_t)N * (uint64_t)K * 9u / 16u;
     int G = K / ORC_GROUP;
@@ -238,11 +280,11 @@ int orc_unpack(const uint8_t *blob, size_t blob_bytes, int E, int N, int K,
         for (int n = 0; n < N; ++n) {
             for (int k = 0; k < K; ++k) {
                 size_t b; int sh;
-                code_pos(N, n, k, &b, &sh);
+                code_pos(layout, N, K, n, k, &b, &sh);
                 codes[((size_t)e * N + n) * K + k] = (uint8_t)((reg[b] >> sh) & 0xf);
             }
             for (int grp = 0; grp < G; ++grp) {
-                size_t b = scale_pos(N, n, grp);
+                size_t b = scale_pos(layout, N, K, n, grp);
                 scales[((size_t)e * N + n) * G + grp] = (uint16_t)(reg[b] | (uint16_t)reg[b + 1] << 8);
             }
         }

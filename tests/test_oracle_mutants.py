@@ -20,6 +20,9 @@ MUTANTS = [
      "float p = (float)q * f32_from_bf16(s) - 8.0f * f32_from_bf16(s);"),
     ("ties_away", "if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u)))", "if (rest >= 0x8000u)"),
     ("nibble_order", "int i = kpart * 2 + lower + 4 * odd;", "int i = kpart + 2 * lower + 4 * odd;"),
+    ("nibble_order_layout2", "int i = (m % 2) * 4 + m / 2;", "int i = m;"),
+    ("scale_half_layout2", "+ 4096u + (size_t)r * 4u\n               + (size_t)h * 2u;",
+     "+ 4096u + (size_t)r * 4u\n               + (size_t)(1 - h) * 2u;"),
     ("scale_slot", "+ (size_t)(h * 8 + g) * 4u + (size_t)lower * 2u;", "+ (size_t)(g * 2 + h) * 4u + (size_t)lower * 2u;"),
     ("align_descending", "for (int64_t p = 0; p < P; ++p)\n            if (topk_ids[p] == e)",
      "for (int64_t p = P - 1; p >= 0; --p)\n            if (topk_ids[p] == e)"),

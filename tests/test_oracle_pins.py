@@ -95,72 +95,81 @@ def test_dequant_exhaustive(orc):
 # --- packing ----------------------------------------------------------------
 
 def test_packed_bytes_closed_form(orc):
-    for E, N, K in [(1, 16, 64), (8, 256, 256), (8, 256, 128), (48, 4096, 7168), (384, 7168, 256)]:
-        assert orc.packed_bytes(E, N, K) == 256 + E * N * K * 9 // 16
-    for bad in [(1, 8, 64), (1, 16, 32), (1, 0, 64)]:
+    for E, N, K in [(1, 128, 64), (8, 256, 256), (8, 256, 128), (48, 4096, 7168), (384, 7168, 256)]:
+        for layout in (1, 2):
+            assert orc.packed_bytes(E, N, K, layout) == 256 + E * N * K * 9 // 16
+    for bad in [(1, 8, 64, 1), (1, 16, 32, 1), (1, 0, 64, 1), (1, 16, 64, 2), (1, 128, 96, 2), (1, 128, 64, 3)]:
         assert orc.packed_bytes(*bad) == 0
 
 
-def test_pack_header(orc):
-    codes = wl.random_codes(1, (3, 32, 128))
-    scales = wl.random_scales(2, (3, 32, 4))
-    blob = orc.pack(codes, scales)
+@pytest.mark.parametrize("layout", [1, 2])
+def test_pack_header(orc, layout):
+    codes = wl.random_codes(1, (3, 128, 128))
+    scales = wl.random_scales(2, (3, 128, 4))
+    blob = orc.pack(codes, scales, layout)
     h = blob[:256]
     u32 = h[:32].view(np.uint32)
     assert bytes(h[:4]) == b"CHRD"
-    assert list(u32[1:8]) == [1, 1, 32, 3, 32, 128, 0]
-    assert list(h[32:48].view(np.uint64)) == [32 * 128 * 9 // 16, 256]
+    assert list(u32[1:8]) == [1, layout, 32, 3, 128, 128, 0]
+    assert list(h[32:48].view(np.uint64)) == [128 * 128 * 9 // 16, 256]
     assert not h[48:].any()
-    assert orc.check_header(blob, 3, 32, 128)
-    assert not orc.check_header(blob, 3, 128, 32)
+    assert orc.check_header(blob, 3, 128, 128, layout)
+    assert not orc.check_header(blob, 3, 128, 128, 3 - layout)
+    assert not orc.check_header(blob, 3, 64, 256, layout)
 
 
-def test_pack_positions_golden(orc):
-    """Hand-derived byte/nibble positions of the layout specification."""
-    E, N, K = 1, 32, 128
-    for r in read_golden("layout_v1_positions.txt"):
+@pytest.mark.parametrize("layout,N,K", [(1, 32, 128), (2, 256, 128)])
+def test_pack_positions_golden(orc, layout, N, K):
+    """Hand-derived byte/nibble positions of each layout's specification."""
+    E = 1
+    for r in read_golden(f"layout_v{layout}_positions.txt"):
         codes = np.zeros((E, N, K), np.uint8)
         scales = np.zeros((E, N, K // GROUP), np.uint16)
         if len(r) == 4:
             n, k, off, sh = map(int, r)
             codes[0, n, k] = 0xF
-            data = orc.pack(codes, scales)[256:]
+            data = orc.pack(codes, scales, layout)[256:]
             nz = np.nonzero(data)[0]
             assert list(nz) == [off], (n, k, list(nz))
             assert data[off] == (0xF << sh), (n, k)
         else:
             n, grp, off = map(int, r)
             scales[0, n, grp] = 0xABCD
-            data = orc.pack(codes, scales)[256:]
+            data = orc.pack(codes, scales, layout)[256:]
             assert list(np.nonzero(data)[0]) == [off, off + 1], (n, grp)
             assert data[off] == 0xCD and data[off + 1] == 0xAB
 
 
-@pytest.mark.parametrize("shape", [(1, 16, 64), (3, 32, 128), (2, 256, 256), (2, 128, 192)])
-def test_pack_roundtrip_and_coverage(orc, shape):
+@pytest.mark.parametrize("layout,shape", [(1, (1, 16, 64)), (1, (3, 32, 128)), (1, (2, 256, 256)),
+                                          (1, (2, 128, 192)), (2, (1, 128, 64)), (2, (2, 256, 192)),
+                                          (2, (1, 384, 128))])
+def test_pack_roundtrip_and_coverage(orc, layout, shape):
     """unpack(pack(x)) == x for random data, and all-ones data fills the data region
     completely: together the placement is a bijection (no overlap, no gap)."""
     E, N, K = shape
     codes = wl.random_codes(3, shape)
     scales = wl.random_scales(4, (E, N, K // GROUP))
-    blob = orc.pack(codes, scales)
-    c2, s2 = orc.unpack(blob, E, N, K)
+    blob = orc.pack(codes, scales, layout)
+    c2, s2 = orc.unpack(blob, E, N, K, layout)
     np.testing.assert_array_equal(c2, codes)
     np.testing.assert_array_equal(s2, scales)
-    full = orc.pack(np.full(shape, 15, np.uint8), np.full((E, N, K // GROUP), 0xFFFF, np.uint16))
+    full = orc.pack(np.full(shape, 15, np.uint8), np.full((E, N, K // GROUP), 0xFFFF, np.uint16), layout)
     assert (full[256:] == 0xFF).all()
     assert full.size == 256 + E * N * K * 9 // 16
 
 
 def test_pack_rejects_bad_codes_and_header(orc):
-    codes = np.zeros((1, 16, 64), np.uint8)
+    codes = np.zeros((1, 128, 64), np.uint8)
     codes[0, 3, 5] = 16
     with pytest.raises(orc.OracleError):
-        orc.pack(codes, np.zeros((1, 16, 2), np.uint16))
-    blob = orc.pack(np.zeros((1, 16, 64), np.uint8), np.zeros((1, 16, 2), np.uint16))
+        orc.pack(codes, np.zeros((1, 128, 2), np.uint16))
+    blob = orc.pack(np.zeros((1, 128, 64), np.uint8), np.zeros((1, 128, 2), np.uint16))
     blob[0] ^= 1
     with pytest.raises(orc.OracleError):
-        orc.unpack(blob, 1, 16, 64)
+        orc.unpack(blob, 1, 128, 64)
+    blob = orc.pack(np.zeros((1, 128, 64), np.uint8), np.zeros((1, 128, 2), np.uint16), 2)
+    with pytest.raises(orc.OracleError):
+        orc.unpack(blob, 1, 128, 64, 1)
 
 
 # --- align ------------------------------------------------------------------
