@@ -68,11 +68,21 @@ typedef enum chord_status {
 #define CHORD_DEV_BAD_CODE 5     /* pack: a code above 15 */
 #define CHORD_DEV_BAD_PADDED 6   /* num_tokens_padded above capacity or not a multiple of block_m */
 
-typedef enum chord_regime {
-    CHORD_REGIME_AUTO = 0,     /* from block_m: <= 64 decode, larger prefill */
-    CHORD_REGIME_DECODE = 1,   /* HBM-streaming kernel, tokens in the MMA N dimension */
-    CHORD_REGIME_PREFILL = 2   /* tensor-core kernel (tcgen05, accumulators in TMEM) */
-} chord_regime;
+/* GEMM kernel family.  Both take the block's tokens as the MMA's N side (the
+ * operand swap of the article's decode profile), so one kernel serves small
+ * and large tokens-per-expert; the block size (chord_select_block_m) carries
+ * the decode / prefill distinction.  Each family reads its own packed layout. */
+typedef enum chord_kernel {
+    CHORD_KERNEL_AUTO = 0,      /* CHORD_KERNEL_TCGEN05 */
+    CHORD_KERNEL_TCGEN05 = 1,   /* tcgen05.mma, dequantised A in tensor memory, FP32 accumulators
+                                   in tensor memory; packed layout CHORD_LAYOUT_TCGEN05 */
+    CHORD_KERNEL_WARP_MMA = 2   /* warp-level mma.sync m16n8k16 with register dequantisation;
+                                   packed layout CHORD_LAYOUT_WARP_MMA */
+} chord_kernel;
+
+/* Packed weight layouts (recorded in the blob's header, checked on the device). */
+#define CHORD_LAYOUT_WARP_MMA 1   /* 16 x 64 chunks in m16n8k16 A-fragment order, N % 16 == 0 */
+#define CHORD_LAYOUT_TCGEN05 2    /* 128 x 64 chunks, one row per 16-byte group, N % 128 == 0 */
 
 typedef enum chord_dtype {
     CHORD_DTYPE_BF16 = 0,
@@ -80,7 +90,7 @@ typedef enum chord_dtype {
 } chord_dtype;
 
 typedef struct chord_opts {
-    int32_t regime;      /* chord_regime */
+    int32_t kernel;      /* chord_kernel (the packed blobs must have its layout) */
     int32_t validate;    /* nonzero: synchronise after the call and turn a set device
                             error word into CHORD_ERR_DEVICE_VALIDATION / _TIMEOUT
                             ("trusted routing validation" of the deployment notes) */
@@ -98,23 +108,30 @@ const char *chord_status_string(chord_status status);
 
 /* ---------------------------------------------------------------- packing */
 
-/* Bytes of the packed blob for E experts of an N x K weight: a 256-byte header
- * followed by E * N * K * 9 / 16 bytes (4-bit codes plus one BF16 scale per 32
- * codes).  Returns 0 when N % 16 or K % 64 is nonzero or a size is not
- * positive.  The byte layout (layout 1) is the one written out in the
- * library's packer; it places each 16 x 16 block of codes so that one 32-bit
- * load per lane yields a tensor-core A fragment. */
-size_t chord_packed_weight_bytes(int E, int N, int K);
+/* Bytes of the packed blob for E experts of an N x K weight in `layout`: a
+ * 256-byte header followed by E * N * K * 9 / 16 bytes (4-bit codes plus one
+ * BF16 scale per 32 codes).  Returns 0 when K % 64 is nonzero, N is not a
+ * multiple of 16 (layout 1) or 128 (layout 2), a size is not positive or the
+ * layout is unknown.  The byte layouts are the ones written out in the
+ * library's packer (and in its CPU oracle): layout 1 places each 16 x 16 block
+ * of codes so that one 32-bit load per lane yields an m16n8k16 A fragment;
+ * layout 2 gives each thread of a 128-row tile its row's 32 consecutive codes
+ * in one 16-byte load. */
+size_t chord_packed_weight_bytes(int E, int N, int K, int layout);
 
-/* Offline packing of canonical weights into the sm_103a layout (the article's
+/* Offline packing of canonical weights into an sm_103a layout (the article's
  * pack step, section "Grouped SM90 kernels": weights are prepared once at load
- * time and the prepared layout is checked when it is used).
+ * time, the mode is recorded in the prepared weight and checked when it is
+ * used; a kernel given a blob of another layout refuses it on the device with
+ * CHORD_DEV_BAD_HEADER).
  *   codes   device uint8 [E, N, K], each 0..15 (uint4, offset 8)
  *   scales  device bf16 [E, N, K / group_size]
- *   packed  device output of packed_bytes >= chord_packed_weight_bytes(E, N, K)
+ *   layout  CHORD_LAYOUT_TCGEN05 (default kernel) or CHORD_LAYOUT_WARP_MMA
+ *   packed  device output of packed_bytes >= chord_packed_weight_bytes(E, N, K, layout)
  * group_size must be 32.  A code above 15 sets CHORD_DEV_BAD_CODE. */
 chord_status chord_pack_weights(const uint8_t *codes, const void *scales, int E, int N, int K,
-                                int group_size, void *packed, size_t packed_bytes, void *stream);
+                                int group_size, int layout, void *packed, size_t packed_bytes,
+                                void *stream);
 
 /* ---------------------------------------------------------------- routing */
 
@@ -197,13 +214,14 @@ size_t chord_gemm_workspace_bytes(int64_t num_pairs, int N, int K, int block_m,
  * dequantised weight bf16_rne((q - 8) * s); the sum is FP32.
  *   A        device bf16 [a_rows, K]; a_row_divisor = topk when A has one row
  *            per token (gate_up), 1 when it has one row per pair (down).
- *   packed   blob from chord_pack_weights for (E, N, K).
+ *   packed   blob from chord_pack_weights for (E, N, K) in the layout of the
+ *            kernel opts->kernel selects.
  *   C        device bf16 [num_pairs, N] (float [num_pairs, N] with
  *            opts->out_dtype = CHORD_DTYPE_F32, the sum left unrounded);
  *            rows no block names are not written.
  *   capacity length of sorted_ids (expert_ids has capacity / block_m entries).
- * block_m must equal the value given to chord_moe_align and be a multiple of 8
- * (decode regime: <= 64; prefill regime: a multiple of 16, <= 256). */
+ * block_m must equal the value given to chord_moe_align, be a multiple of 8 and
+ * at most 256; N % 128 == 0, K % 64 == 0. */
 chord_status chord_w4a16_moe_gemm(const void *A, int64_t a_rows, int a_row_divisor,
                                   const void *packed, size_t packed_bytes, int E, int N, int K,
                                   const int32_t *sorted_ids, const int32_t *expert_ids,

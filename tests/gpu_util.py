@@ -39,10 +39,14 @@ def assert_close(got_bits, ref_bits, what=""):
     return float(err.max()) if err.size else 0.0
 
 
-def pack(codes, scales):
+KERNELS = {"tcgen05": (chord.KERNEL_TCGEN05, chord.LAYOUT_TCGEN05),
+           "warp_mma": (chord.KERNEL_WARP_MMA, chord.LAYOUT_WARP_MMA)}
+
+
+def pack(codes, scales, layout=chord.LAYOUT_TCGEN05):
     E, N, K = codes.shape
-    out = torch.empty(chord.chord_packed_weight_bytes(E, N, K), dtype=torch.uint8, device=DEV)
-    chord.chord_pack_weights(dev(codes), dbf(scales), out)
+    out = torch.empty(chord.chord_packed_weight_bytes(E, N, K, layout), dtype=torch.uint8, device=DEV)
+    chord.chord_pack_weights(dev(codes), dbf(scales), out, layout=layout)
     return out
 
 
@@ -58,12 +62,12 @@ def align(ids, E, bm, opts=None):
     return s, e, n
 
 
-def gemm(A_bits, div, packed, E, N, K, s, e, n, bm, P, regime=0, C=None):
+def gemm(A_bits, div, packed, E, N, K, s, e, n, bm, P, kernel=0, C=None):
     """C rows that no block names keep the fill pattern 0xFFFF (a NaN)."""
     A = A_bits if isinstance(A_bits, torch.Tensor) else dbf(A_bits)
     if C is None:
         C = torch.full((max(P, 1), N), -1, dtype=torch.int16, device=DEV)[:P].view(torch.bfloat16)
-    opts = chord.ChordOpts(regime=regime)
+    opts = chord.ChordOpts(kernel=kernel)
     chord.chord_w4a16_moe_gemm(A, div, packed, E, N, K, s, e, n, bm, P, C, opts=opts)
     return C
 

@@ -42,9 +42,13 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_sizes_and_capacity(lib):
-    assert chord.chord_packed_weight_bytes(48, 4096, 7168) == 256 + 48 * 4096 * 7168 * 9 // 16
-    assert chord.chord_packed_weight_bytes(1, 8, 64) == 0
-    assert chord.chord_packed_weight_bytes(1, 16, 96) == 0
+    for layout in (1, 2):
+        assert chord.chord_packed_weight_bytes(48, 4096, 7168, layout) == 256 + 48 * 4096 * 7168 * 9 // 16
+        assert chord.chord_packed_weight_bytes(1, 8, 64, layout) == 0
+        assert chord.chord_packed_weight_bytes(1, 128, 96, layout) == 0
+    assert chord.chord_packed_weight_bytes(1, 16, 64, 1) == 256 + 16 * 64 * 9 // 16
+    assert chord.chord_packed_weight_bytes(1, 16, 64, 2) == 0
+    assert chord.chord_packed_weight_bytes(1, 128, 64, 3) == 0
     P = 512 * 8
     assert chord.chord_align_capacity(512, 8, 48, 16) == -(-(P + 48 * 15) // 16) * 16
     assert chord.chord_align_capacity(1, 8, 384, 8) == -(-(8 + 8 * 7) // 8) * 8
@@ -94,11 +98,14 @@ def test_argument_errors_before_any_launch(lib):
     vp = ctypes.c_void_p
     big = vp(1 << 20)
     # group size other than 32
-    assert lib.chord_pack_weights(big, big, 1, 16, 64, 64, big, 10 ** 6, None) == 2
-    # N not a multiple of 16
-    assert lib.chord_pack_weights(big, big, 1, 8, 64, 32, big, 10 ** 6, None) == 2
+    assert lib.chord_pack_weights(big, big, 1, 128, 64, 64, 2, big, 10 ** 6, None) == 2
+    # N not a multiple of 16 (layout 1) / 128 (layout 2)
+    assert lib.chord_pack_weights(big, big, 1, 8, 64, 32, 1, big, 10 ** 6, None) == 2
+    assert lib.chord_pack_weights(big, big, 1, 16, 64, 32, 2, big, 10 ** 6, None) == 2
+    # unknown layout
+    assert lib.chord_pack_weights(big, big, 1, 128, 64, 32, 7, big, 10 ** 6, None) == 1
     # packed buffer too small
-    assert lib.chord_pack_weights(big, big, 1, 16, 64, 32, big, 100, None) == 4
+    assert lib.chord_pack_weights(big, big, 1, 128, 64, 32, 2, big, 100, None) == 4
     # GEMM: packed size does not match (E, N, K) -> layout mismatch
     args = [big, 16, 1, big, 12345, 2, 128, 64, big, big, big, 16, 8, 16, big, None, 0, None, None]
     assert lib.chord_w4a16_moe_gemm(*args) == 3
@@ -110,6 +117,6 @@ def test_argument_errors_before_any_launch(lib):
     # align: too many experts for the scan
     assert lib.chord_moe_align(big, 4, 2, 2000, 8, big, big, big, 10 ** 6, big, 10 ** 8, None, None) == 2
     # misaligned activation pointer
-    nb = chord.chord_packed_weight_bytes(2, 128, 64)
+    nb = chord.chord_packed_weight_bytes(2, 128, 64, 2)
     args = [vp((1 << 20) + 2), 16, 1, big, nb, 2, 128, 64, big, big, big, 16, 8, 16, big, None, 0, None, None]
     assert lib.chord_w4a16_moe_gemm(*args) == 1

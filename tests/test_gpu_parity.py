@@ -10,7 +10,7 @@ import torch
 import oracle
 import w4a16_int4_mixture_moe_gb300 as chord
 import workloads as wl
-from gpu_util import (DEV, align, assert_close, dbf, dev, f64, gemm, host_bits, layer, pack, valid_rows)
+from gpu_util import (DEV, KERNELS, align, assert_close, dbf, dev, f64, gemm, host_bits, layer, pack, valid_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -29,20 +29,24 @@ def _lib():
 
 # --------------------------------------------------------------------- pack
 
-@pytest.mark.parametrize("shape", [(8, 256, 256), (8, 256, 128), (3, 32, 128), (2, 144, 192), (1, 4096, 7168)])
-def test_pack_byte_exact(shape):
+@pytest.mark.parametrize("layout,shape", [(1, (8, 256, 256)), (1, (8, 256, 128)), (1, (3, 32, 128)),
+                                          (1, (2, 144, 192)), (1, (1, 4096, 7168)),
+                                          (2, (8, 256, 256)), (2, (8, 256, 128)), (2, (3, 384, 192)),
+                                          (2, (1, 4096, 7168)), (2, (2, 7168, 256))])
+def test_pack_byte_exact(layout, shape):
     E, N, K = shape
     codes = wl.random_codes(sum(shape), shape)
     scales = wl.random_scales(sum(shape) + 1, (E, N, K // 32))
-    got = pack(codes, scales).cpu().numpy()
-    want = oracle.pack(codes, scales)
+    got = pack(codes, scales, layout).cpu().numpy()
+    want = oracle.pack(codes, scales, layout)
     np.testing.assert_array_equal(got, want)
 
 
-def test_pack_bad_code_sets_error_word():
-    codes = np.zeros((1, 16, 64), np.uint8)
+@pytest.mark.parametrize("layout", [1, 2])
+def test_pack_bad_code_sets_error_word(layout):
+    codes = np.zeros((1, 128, 64), np.uint8)
     codes[0, 5, 7] = 17
-    pack(codes, np.zeros((1, 16, 2), np.uint16))
+    pack(codes, np.zeros((1, 128, 2), np.uint16), layout)
     assert chord.chord_get_device_error() == 5  # CHORD_DEV_BAD_CODE
     assert chord.chord_get_device_error() == 0
 
@@ -114,8 +118,8 @@ def test_align_validate_reports_bad_ids():
 
 # --------------------------------------------------------------------- GEMM
 
-def run_gemm_case(T, topk, E, N, K, bm, seed, div=None, pnl=0.2, regime=0, exact=False, x=None, codes=None,
-                  scales=None, ids=None):
+def run_gemm_case(T, topk, E, N, K, bm, seed, div=None, pnl=0.2, kernel="tcgen05", exact=False, x=None,
+                  codes=None, scales=None, ids=None):
     div = topk if div is None else div
     a_rows = T if div == topk else T * topk
     if x is None:
@@ -127,9 +131,10 @@ def run_gemm_case(T, topk, E, N, K, bm, seed, div=None, pnl=0.2, regime=0, exact
     if ids is None:
         ids = wl.random_ids(seed + 3, T, topk, E, p_nonlocal=pnl)
     P = T * topk
-    packed = pack(codes, scales)
+    kid, layout = KERNELS[kernel]
+    packed = pack(codes, scales, layout)
     s, e, n = align(ids, E, bm)
-    C = gemm(x, div, packed, E, N, K, s, e, n, bm, P, regime=regime)
+    C = gemm(x, div, packed, E, N, K, s, e, n, bm, P, kernel=kid)
     s2, e2, n2 = oracle.moe_align(ids, E, bm)
     ref = oracle.moe_gemm(x, div, codes, scales, s2, e2, n2, bm, P,
                           C=np.full((P, N), 0xFFFF, np.uint16))
@@ -140,13 +145,17 @@ def run_gemm_case(T, topk, E, N, K, bm, seed, div=None, pnl=0.2, regime=0, exact
     if exact:
         np.testing.assert_array_equal(got[rows], ref[rows])
     else:
-        assert_close(got[rows], ref[rows], f"gemm T={T} E={E} N={N} K={K} bm={bm}")
+        assert_close(got[rows], ref[rows], f"{kernel} gemm T={T} E={E} N={N} K={K} bm={bm}")
     return got, ref
 
 
+BOTH = pytest.mark.parametrize("kernel", ["tcgen05", "warp_mma"])
+
+
+@BOTH
 @pytest.mark.parametrize("bm", [8, 16, 24, 32, 64, 128, 256])
 @pytest.mark.parametrize("K", [256, 2048])
-def test_gemm_exact_integer_regime_bit_exact(bm, K):
+def test_gemm_exact_integer_regime_bit_exact(kernel, bm, K):
     """x in {-1, 0, 1}, scales 1.0: sums are exact integers in any order, so the
     GPU must match the oracle bit for bit (catches any wrong index, lost or
     doubled K chunk, or token/row mix-up)."""
@@ -155,11 +164,12 @@ def test_gemm_exact_integer_regime_bit_exact(bm, K):
     xi = rng.integers(-1, 2, size=(T, K)).astype(np.float32)
     x = wl._bf16(xi)
     scales = np.full((E, N, K // 32), 0x3F80, np.uint16)
-    run_gemm_case(T, topk, E, N, K, bm, seed=bm + K, x=x, scales=scales, exact=True)
+    run_gemm_case(T, topk, E, N, K, bm, seed=bm + K, x=x, scales=scales, exact=True, kernel=kernel)
 
 
-@pytest.mark.parametrize("bm", [8, 16, 32, 64])
-def test_gemm_dequant_bit_exact_one_hot(bm):
+@BOTH
+@pytest.mark.parametrize("bm", [8, 16, 32, 64, 128])
+def test_gemm_dequant_bit_exact_one_hot(kernel, bm):
     """One-hot activation rows make C the dequantised weight column itself:
     C[t, n] = bf16((q[n, t] - 8) * s[n, t/32]) exactly.  Every code and a wide
     range of scale exponents go through the kernel's subtract-then-scale path."""
@@ -174,7 +184,7 @@ def test_gemm_dequant_bit_exact_one_hot(bm):
     scales = wl._bf16(sc.astype(np.float32))
     ids = np.zeros((T, 1), np.int32)
     got, ref = run_gemm_case(T, 1, E, N, K, bm, seed=0, div=1, x=x, codes=codes, scales=scales, ids=ids,
-                             exact=True)
+                             exact=True, kernel=kernel)
     deq = oracle.dequant_pairs(codes[0].T.copy().ravel(),
                                np.repeat(scales[0], 32, axis=1).T.copy().ravel()).reshape(K, N)
     # a zero weight times a negative scale is -0; a sum that starts from +0 returns +0
@@ -182,11 +192,13 @@ def test_gemm_dequant_bit_exact_one_hot(bm):
     np.testing.assert_array_equal(got, deq)
 
 
-@pytest.mark.parametrize("bm", [8, 32, 64])
-def test_gemm_f32_output(bm):
+@BOTH
+@pytest.mark.parametrize("bm", [8, 32, 64, 256])
+def test_gemm_f32_output(kernel, bm):
     """FP32 output: exact integers in the exact-integer regime (bit-exact with the
     oracle's unrounded sum), within tolerance on random data."""
     T, topk, E, N, K = 24, 4, 5, 256, 1024
+    kid, layout = KERNELS[kernel]
     rng = np.random.default_rng(bm)
     xi = rng.integers(-1, 2, size=(T, K)).astype(np.float32)
     codes = wl.random_codes(bm + 1, (E, N, K))
@@ -196,10 +208,10 @@ def test_gemm_f32_output(bm):
     s2, e2, n2 = oracle.moe_align(ids, E, bm)
     for x, scales, exact in [(wl._bf16(xi), np.full((E, N, K // 32), 0x3F80, np.uint16), True),
                              (wl.random_bf16(bm + 3, (T, K)), wl.random_scales(bm + 4, (E, N, K // 32)), False)]:
-        packed = pack(codes, scales)
+        packed = pack(codes, scales, layout)
         C = torch.full((T * topk, N), float("nan"), dtype=torch.float32, device=DEV)
         chord.chord_w4a16_moe_gemm(dbf(x), topk, packed, E, N, K, s, e, n, bm, T * topk, C,
-                                   opts=chord.ChordOpts(out_dtype=chord.DTYPE_F32))
+                                   opts=chord.ChordOpts(kernel=kid, out_dtype=chord.DTYPE_F32))
         got = C.cpu().numpy()
         ref = oracle.moe_gemm_f32(x, topk, codes, scales, s2, e2, n2, bm, T * topk)
         if exact:
@@ -211,19 +223,32 @@ def test_gemm_f32_output(bm):
         assert np.isnan(got[other]).all()
 
 
-@pytest.mark.parametrize("bm", [8, 16, 32, 64])
+@BOTH
+@pytest.mark.parametrize("bm", [8, 16, 32, 64, 96, 256])
 @pytest.mark.parametrize("shape", [(3, 128, 64), (4, 384, 320), (6, 256, 1024)])
-def test_gemm_random_vs_oracle(bm, shape):
+def test_gemm_random_vs_oracle(kernel, bm, shape):
     E, N, K = shape
-    run_gemm_case(37, 3, E, N, K, bm, seed=E * N + K + bm)
+    run_gemm_case(37, 3, E, N, K, bm, seed=E * N + K + bm, kernel=kernel)
 
 
-def test_gemm_down_projection_row_per_pair():
+@BOTH
+def test_gemm_many_rows_per_expert(kernel):
+    """Blocks full up to 256 rows and experts spanning several blocks (the
+    prefill case): 600 pairs on 3 experts, block sizes 128 and 256."""
+    T, topk, E = 300, 2, 3
+    ids = wl.random_ids(61, T, topk, E)
+    for bm in (128, 256):
+        run_gemm_case(T, topk, E, 256, 512, bm, seed=62 + bm, ids=ids, kernel=kernel)
+
+
+@BOTH
+def test_gemm_down_projection_row_per_pair(kernel):
     """a_row_divisor = 1: A holds one row per pair (the down projection)."""
-    run_gemm_case(30, 4, 5, 256, 256, 16, seed=77, div=1)
+    run_gemm_case(30, 4, 5, 256, 256, 16, seed=77, div=1, kernel=kernel)
 
 
-def test_gemm_edge_routing():
+@BOTH
+def test_gemm_edge_routing(kernel):
     """Experts with 0, 1, 2, bm-1, bm, bm+1 and 3*bm+5 rows in one call."""
     bm = 16
     counts = [0, 1, 2, bm - 1, bm, bm + 1, 3 * bm + 5]
@@ -232,30 +257,34 @@ def test_gemm_edge_routing():
     pad = (-flat.size) % 2
     flat = np.concatenate([flat, np.full(pad, -1, np.int32)])
     ids = flat.reshape(-1, 2)
-    run_gemm_case(ids.shape[0], 2, len(counts), 128, 192, bm, seed=5, ids=ids)
+    run_gemm_case(ids.shape[0], 2, len(counts), 128, 192, bm, seed=5, ids=ids, kernel=kernel)
 
 
-def test_gemm_nothing_local_writes_nothing():
+@BOTH
+def test_gemm_nothing_local_writes_nothing(kernel):
     ids = np.full((12, 4), -1, np.int32)
-    run_gemm_case(12, 4, 3, 128, 64, 8, seed=6, ids=ids)
+    run_gemm_case(12, 4, 3, 128, 64, 8, seed=6, ids=ids, kernel=kernel)
 
 
 def test_gemm_header_mismatch_is_reported():
     """A blob packed for (E, N, K) = (2, 128, 128) passed as (2, 256, 64) has the
-    right size but the wrong header: the device refuses it and writes nothing."""
+    right size but the wrong header, and a blob of the warp-MMA layout passed to
+    the tcgen05 kernel the wrong layout: the device refuses both and writes nothing."""
     E = 2
     codes = wl.random_codes(1, (E, 128, 128))
     scales = wl.random_scales(2, (E, 128, 4))
-    packed = pack(codes, scales)
     ids = wl.random_ids(3, 8, 2, E)
     s, e, n = align(ids, E, 8)
-    x = wl.random_bf16(4, (8, 64))
-    with pytest.raises(chord.ChordError) as ei:
-        C = torch.full((16, 256), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
-        chord.chord_w4a16_moe_gemm(dbf(x), 2, packed, E, 256, 64, s, e, n, 8, 16, C,
-                                   opts=chord.ChordOpts(validate=1))
-    assert ei.value.status == 6
-    assert (host_bits(C) == 0xFFFF).all()
+    for layout, N, K, kernel in [(2, 256, 64, chord.KERNEL_TCGEN05), (1, 128, 128, chord.KERNEL_TCGEN05),
+                                 (2, 128, 128, chord.KERNEL_WARP_MMA)]:
+        packed = pack(codes, scales, layout)
+        x = wl.random_bf16(4, (8, K))
+        C = torch.full((16, N), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+        with pytest.raises(chord.ChordError) as ei:
+            chord.chord_w4a16_moe_gemm(dbf(x), 2, packed, E, N, K, s, e, n, 8, 16, C,
+                                       opts=chord.ChordOpts(kernel=kernel, validate=1))
+        assert ei.value.status == 6
+        assert (host_bits(C) == 0xFFFF).all()
 
 
 # ---------------------------------------------------------------- epilogues
@@ -295,14 +324,17 @@ def test_combine_bit_exact():
 
 # -------------------------------------------------------------------- layer
 
-@pytest.mark.parametrize("bm", [0, 8, 16, 32, 64])
-def test_layer_tiny_vs_oracle(bm):
+@BOTH
+@pytest.mark.parametrize("bm", [0, 8, 16, 32, 64, 256])
+def test_layer_tiny_vs_oracle(kernel, bm):
     w = wl.TINY
     ids, wts = wl.make_routing(w)
     x = wl.make_x(w)
     c13, s13 = wl.make_w13(w)
     c2, s2 = wl.make_w2(w)
-    out, used_bm = layer(x, ids, wts, w.E, w.E_global, w.I, pack(c13, s13), pack(c2, s2), bm=bm)
+    kid, layout = KERNELS[kernel]
+    out, used_bm = layer(x, ids, wts, w.E, w.E_global, w.I, pack(c13, s13, layout), pack(c2, s2, layout), bm=bm,
+                         opts=chord.ChordOpts(kernel=kid))
     ref = oracle.moe_layer(x, ids, wts, (c13, s13), (c2, s2), w.E, block_m=used_bm)
     assert_close(host_bits(out), ref, f"tiny layer bm={used_bm}")
 

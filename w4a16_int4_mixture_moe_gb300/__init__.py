@@ -20,10 +20,12 @@ __all__ = [
     "chord_align_capacity", "chord_align_workspace_bytes", "chord_moe_align", "chord_select_block_m",
     "chord_gemm_workspace_bytes", "chord_w4a16_moe_gemm", "chord_silu_mul", "chord_moe_combine",
     "chord_layer_workspace_bytes", "chord_moe_layer", "chord_get_device_error",
-    "REGIME_AUTO", "REGIME_DECODE", "REGIME_PREFILL", "DTYPE_BF16", "DTYPE_F32",
+    "KERNEL_AUTO", "KERNEL_TCGEN05", "KERNEL_WARP_MMA", "LAYOUT_WARP_MMA", "LAYOUT_TCGEN05",
+    "DTYPE_BF16", "DTYPE_F32",
 ]
 
-REGIME_AUTO, REGIME_DECODE, REGIME_PREFILL = 0, 1, 2
+KERNEL_AUTO, KERNEL_TCGEN05, KERNEL_WARP_MMA = 0, 1, 2
+LAYOUT_WARP_MMA, LAYOUT_TCGEN05 = 1, 2
 DTYPE_BF16, DTYPE_F32 = 0, 1
 STATUS = {0: "CHORD_OK", 1: "CHORD_ERR_INVALID_ARG", 2: "CHORD_ERR_UNSUPPORTED", 3: "CHORD_ERR_LAYOUT_MISMATCH",
           4: "CHORD_ERR_BUFFER_TOO_SMALL", 5: "CHORD_ERR_CUDA", 6: "CHORD_ERR_DEVICE_VALIDATION",
@@ -37,7 +39,7 @@ class ChordError(RuntimeError):
 
 
 class ChordOpts(ctypes.Structure):
-    _fields_ = [("regime", ctypes.c_int32), ("validate", ctypes.c_int32), ("split_k", ctypes.c_int32),
+    _fields_ = [("kernel", ctypes.c_int32), ("validate", ctypes.c_int32), ("split_k", ctypes.c_int32),
                 ("out_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32 * 4)]
 
 
@@ -50,8 +52,8 @@ _OPTS = ctypes.POINTER(ChordOpts)
 _SIGS = {
     "chord_version": (_int, []),
     "chord_status_string": (ctypes.c_char_p, [_int]),
-    "chord_packed_weight_bytes": (_sz, [_int, _int, _int]),
-    "chord_pack_weights": (_int, [_vp, _vp, _int, _int, _int, _int, _vp, _sz, _vp]),
+    "chord_packed_weight_bytes": (_sz, [_int, _int, _int, _int]),
+    "chord_pack_weights": (_int, [_vp, _vp, _int, _int, _int, _int, _int, _vp, _sz, _vp]),
     "chord_align_capacity": (_i64, [_int, _int, _int, _int]),
     "chord_align_workspace_bytes": (_sz, [_int, _int, _int]),
     "chord_moe_align": (_int, [_vp, _int, _int, _int, _int, _vp, _vp, _vp, _i64, _vp, _sz, _OPTS, _vp]),
@@ -124,15 +126,15 @@ def chord_status_string(status: int) -> str:
     return load().chord_status_string(status).decode()
 
 
-def chord_packed_weight_bytes(E: int, N: int, K: int) -> int:
-    return load().chord_packed_weight_bytes(E, N, K)
+def chord_packed_weight_bytes(E: int, N: int, K: int, layout: int = LAYOUT_TCGEN05) -> int:
+    return load().chord_packed_weight_bytes(E, N, K, layout)
 
 
-def chord_pack_weights(codes, scales, packed, group_size: int = 32, stream=None):
+def chord_pack_weights(codes, scales, packed, layout: int = LAYOUT_TCGEN05, group_size: int = 32, stream=None):
     """codes uint8 [E, N, K] (0..15), scales bf16 [E, N, K/32], packed uint8 output (device tensors)."""
     E, N, K = codes.shape
-    _check(load().chord_pack_weights(_p(codes), _p(scales), E, N, K, group_size, _p(packed), _nbytes(packed),
-                                     _s(stream)), "chord_pack_weights")
+    _check(load().chord_pack_weights(_p(codes), _p(scales), E, N, K, group_size, layout, _p(packed),
+                                     _nbytes(packed), _s(stream)), "chord_pack_weights")
 
 
 def chord_align_capacity(T: int, topk: int, E: int, block_m: int) -> int:

@@ -91,21 +91,24 @@ const char* chord_status_string(chord_status s) {
     return "unknown status";
 }
 
-size_t chord_packed_weight_bytes(int E, int N, int K) {
-    if (E < 0 || N <= 0 || K <= 0 || N % 16 || K % 64) return 0;
+size_t chord_packed_weight_bytes(int E, int N, int K, int layout) {
+    if (E < 0 || N <= 0 || K <= 0 || K % 64) return 0;
+    if (!(layout == CHORD_LAYOUT_WARP_MMA && N % 16 == 0) && !(layout == CHORD_LAYOUT_TCGEN05 && N % 128 == 0))
+        return 0;
     return (size_t)kHeaderBytes + (size_t)E * (size_t)N * (size_t)K * 9u / 16u;
 }
 
 chord_status chord_pack_weights(const uint8_t* codes, const void* scales, int E, int N, int K, int group_size,
-                                void* packed, size_t packed_bytes, void* stream) {
+                                int layout, void* packed, size_t packed_bytes, void* stream) {
     if (group_size != kGroup) return CHORD_ERR_UNSUPPORTED;
     if (E < 0 || N <= 0 || K <= 0) return CHORD_ERR_INVALID_ARG;
-    if (N % 16 || K % 64) return CHORD_ERR_UNSUPPORTED;
+    if (layout != CHORD_LAYOUT_WARP_MMA && layout != CHORD_LAYOUT_TCGEN05) return CHORD_ERR_INVALID_ARG;
+    if (chord_packed_weight_bytes(E, N, K, layout) == 0) return CHORD_ERR_UNSUPPORTED;
     if (!packed || !aligned16(packed) || (E > 0 && (!codes || !scales))) return CHORD_ERR_INVALID_ARG;
-    if (packed_bytes < chord_packed_weight_bytes(E, N, K)) return CHORD_ERR_BUFFER_TOO_SMALL;
+    if (packed_bytes < chord_packed_weight_bytes(E, N, K, layout)) return CHORD_ERR_BUFFER_TOO_SMALL;
     const DeviceInfo& di = device_info();
     if (!di.err) return CHORD_ERR_CUDA;
-    return cuda_status(launch_pack(codes, static_cast<const uint16_t*>(scales), E, N, K,
+    return cuda_status(launch_pack(codes, static_cast<const uint16_t*>(scales), E, N, K, layout,
                                    static_cast<uint8_t*>(packed), di.err, static_cast<cudaStream_t>(stream)));
 }
 
@@ -151,14 +154,17 @@ int chord_select_block_m(int T, int topk, int E_local, int E_global, int N, int 
     if (forced > 0) return forced;
     const int eg = E_global > 0 ? E_global : (E_local > 0 ? E_local : 1);
     const double tok_e = (double)T * (double)(topk > 0 ? topk : 1) / (double)eg;
-    // Rows per expert that a block should hold without splitting an expert in two
-    // most of the time: the mean plus three standard deviations of a Poisson count.
+    // Rows per expert that a block should hold without splitting an expert in
+    // two most of the time (every extra block of an expert re-streams and
+    // re-dequantises that expert's weights): the mean plus three standard
+    // deviations of a Poisson count, in steps of 16 (the MMA's N granularity),
+    // at most 256 (the largest MMA N).  The kernels size each MMA to the rows a
+    // block really holds, so a generous block costs only index padding.
     const double need = tok_e + 3.0 * sqrt(tok_e) + 1.0;
-    if (prefill_available() && tok_e > 48.0) return 256;
     if (need <= 8.0) return 8;
-    if (need <= 16.0) return 16;
-    if (need <= 32.0) return 32;
-    return 64;
+    int bm = (int)ceil(need / 16.0) * 16;
+    if (bm > 256) bm = 256;
+    return bm;
 }
 
 size_t chord_gemm_workspace_bytes(int64_t num_pairs, int N, int K, int block_m, const chord_opts* opts) {
@@ -180,22 +186,19 @@ chord_status chord_w4a16_moe_gemm(const void* A, int64_t a_rows, int a_row_divis
     if (E <= 0 || N <= 0 || K <= 0 || a_rows < 0 || a_row_divisor <= 0 || block_m <= 0 || capacity < 0 ||
         num_pairs < 0)
         return CHORD_ERR_INVALID_ARG;
-    if (N % 128 || K % 64) return CHORD_ERR_UNSUPPORTED;
+    if (N % 128 || K % 64 || block_m % 8 || block_m > 256) return CHORD_ERR_UNSUPPORTED;
     if (num_pairs >= INT32_MAX) return CHORD_ERR_UNSUPPORTED;
-    if (packed_bytes != chord_packed_weight_bytes(E, N, K)) return CHORD_ERR_LAYOUT_MISMATCH;
+    const chord_opts o = opts_or_default(opts);
+    int kernel = o.kernel ? o.kernel : env_int("CHORD_KERNEL", 0);
+    if (kernel == CHORD_KERNEL_AUTO) kernel = CHORD_KERNEL_TCGEN05;
+    if (kernel != CHORD_KERNEL_TCGEN05 && kernel != CHORD_KERNEL_WARP_MMA) return CHORD_ERR_INVALID_ARG;
+    const int layout = kernel == CHORD_KERNEL_TCGEN05 ? CHORD_LAYOUT_TCGEN05 : CHORD_LAYOUT_WARP_MMA;
+    if (packed_bytes != chord_packed_weight_bytes(E, N, K, layout)) return CHORD_ERR_LAYOUT_MISMATCH;
     if (!packed || !aligned16(packed) || !num_tokens_padded || (capacity > 0 && (!sorted_ids || !expert_ids)))
         return CHORD_ERR_INVALID_ARG;
     if (capacity % block_m) return CHORD_ERR_INVALID_ARG;
     if ((a_rows > 0 && (!A || !aligned16(A))) || (num_pairs > 0 && (!C || !aligned16(C))))
         return CHORD_ERR_INVALID_ARG;
-    const chord_opts o = opts_or_default(opts);
-    int regime = o.regime ? o.regime : env_int("CHORD_FORCE_REGIME", 0);
-    if (regime == CHORD_REGIME_AUTO) regime = (block_m > 64 && prefill_available()) ? CHORD_REGIME_PREFILL
-                                                                                      : CHORD_REGIME_DECODE;
-    if (regime == CHORD_REGIME_DECODE && block_m % 8) return CHORD_ERR_UNSUPPORTED;
-    if (regime == CHORD_REGIME_PREFILL && (!prefill_available() || block_m % 16 || block_m > 256))
-        return CHORD_ERR_UNSUPPORTED;
-    if (regime != CHORD_REGIME_DECODE && regime != CHORD_REGIME_PREFILL) return CHORD_ERR_INVALID_ARG;
     if (o.out_dtype != CHORD_DTYPE_BF16 && o.out_dtype != CHORD_DTYPE_F32) return CHORD_ERR_INVALID_ARG;
     const DeviceInfo& di = device_info();
     if (!di.err) return CHORD_ERR_CUDA;
@@ -218,7 +221,7 @@ chord_status chord_w4a16_moe_gemm(const void* A, int64_t a_rows, int a_row_divis
     g.out_f32 = o.out_dtype == CHORD_DTYPE_F32 ? 1 : 0;
     g.err = di.err;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = regime == CHORD_REGIME_PREFILL ? launch_gemm_prefill(g, s) : launch_gemm_decode(g, s);
+    cudaError_t e = kernel == CHORD_KERNEL_TCGEN05 ? launch_gemm_tc(g, s) : launch_gemm_decode(g, s);
     if (e != cudaSuccess) return CHORD_ERR_CUDA;
     return finish(o, s);
 }

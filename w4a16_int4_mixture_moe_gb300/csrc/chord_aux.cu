@@ -10,21 +10,58 @@
 namespace chord {
 
 // ============================================================================
-// Pack: canonical codes [E, N, K] + scales [E, N, K/32] -> layout 1.
-// One thread writes one 32-bit word of the blob, so the writes are coalesced;
-// the gathers from the canonical arrays are not, which is fine for a one-off
-// load-time step.
+// Pack: canonical codes [E, N, K] + scales [E, N, K/32] -> layout 1 (the warp
+// MMA kernel's A fragments) or layout 2 (one row per thread for the tcgen05
+// kernel).  One thread writes one 32-bit word of the blob, so the writes are
+// coalesced; the gathers from the canonical arrays are not, which is fine for
+// a one-off load-time step.
 // ============================================================================
-__global__ void pack_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ scales, int E, int N,
-                            int K, uint8_t* __restrict__ packed, int* err) {
-    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+// Layout 2: chunk (nt, kc) of 128 rows x 64 columns is 1152 words: words
+// 0..1023 are codes (half h = w/512, row r = (w%512)/4, word j = w%4 holding
+// columns 32h + 8j + m of the chunk, m = 2*(i%4) + i/4 in nibble i), words
+// 1024..1151 the two group scales of each row.
+__global__ void pack2_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ scales, int E, int N,
+                             int K, uint32_t* __restrict__ out, int* err) {
+    constexpr int kWords = 4608 / 4;
+    const int kchunks = K / 64;
+    const int64_t chunks_per_expert = (int64_t)(N / 128) * kchunks;
+    const int64_t words = (int64_t)E * chunks_per_expert * kWords;
+    const int G = K / kGroup;
+    for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < words; w += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t chunk = w / kWords;
+        const int wi = (int)(w % kWords);
+        const int64_t e = chunk / chunks_per_expert;
+        const int64_t cc = chunk % chunks_per_expert;
+        const int nt = (int)(cc / kchunks), kc = (int)(cc % kchunks);
+        uint32_t v = 0;
+        if (wi < 1024) {
+            const int h = wi / 512, r = (wi % 512) / 4, j = wi % 4;
+            const uint8_t* p = codes + ((int64_t)e * N + nt * 128 + r) * K + kc * 64 + h * 32 + j * 8;
+            uint32_t bad = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t q = p[2 * (i & 3) + (i >> 2)];
+                bad |= q >> 4;
+                v |= (q & 0xFu) << (4 * i);
+            }
+            if (bad) set_error(err, CHORD_DEV_BAD_CODE);
+        } else {
+            const int r = wi - 1024;
+            const int64_t row = (int64_t)e * N + nt * 128 + r;
+            v = (uint32_t)scales[row * G + 2 * kc] | ((uint32_t)scales[row * G + 2 * kc + 1] << 16);
+        }
+        out[w] = v;
+    }
+}
+
+__device__ __forceinline__ void write_header(uint8_t* packed, int64_t tid, int E, int N, int K, uint32_t layout) {
     if (tid < kHeaderBytes / 4) {
         const unsigned long long stride = (unsigned long long)N * (unsigned long long)K * 9ull / 16ull;
         uint32_t v = 0;
         switch ((int)tid) {
             case 0: v = kMagic; break;
             case 1: v = 1u; break;
-            case 2: v = kLayoutVersion; break;
+            case 2: v = layout; break;
             case 3: v = (uint32_t)kGroup; break;
             case 4: v = (uint32_t)E; break;
             case 5: v = (uint32_t)N; break;
@@ -36,6 +73,15 @@ __global__ void pack_kernel(const uint8_t* __restrict__ codes, const uint16_t* _
         }
         reinterpret_cast<uint32_t*>(packed)[tid] = v;
     }
+}
+
+__global__ void header_kernel(uint8_t* packed, int E, int N, int K, uint32_t layout) {
+    write_header(packed, threadIdx.x, E, N, K, layout);
+}
+
+__global__ void pack_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ scales, int E, int N,
+                            int K, uint8_t* __restrict__ packed, int* err) {
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int mtiles = N / 16;
     const int64_t chunks_per_expert = (int64_t)(K / 64) * mtiles;
     const int64_t words = (int64_t)E * chunks_per_expert * (kChunkBytes / 4);
@@ -77,14 +123,21 @@ __global__ void pack_kernel(const uint8_t* __restrict__ codes, const uint16_t* _
     }
 }
 
-cudaError_t launch_pack(const uint8_t* codes, const uint16_t* scales, int E, int N, int K, uint8_t* packed, int* err,
-                        cudaStream_t stream) {
-    const int64_t words = (int64_t)E * (K / 64) * (N / 16) * (kChunkBytes / 4);
+cudaError_t launch_pack(const uint8_t* codes, const uint16_t* scales, int E, int N, int K, int layout,
+                        uint8_t* packed, int* err, cudaStream_t stream) {
+    header_kernel<<<1, kHeaderBytes / 4, 0, stream>>>(packed, E, N, K, (uint32_t)layout);
+    cudaError_t st = cudaGetLastError();
+    if (st != cudaSuccess || E == 0) return st;
+    const int64_t words = (int64_t)E * (K / 64) * (N / 16) * (kChunkBytes / 4);  // same count for both layouts
     const int threads = 256;
-    int64_t blocks = ceil_div64(words > kHeaderBytes / 4 ? words : kHeaderBytes / 4, threads);
+    int64_t blocks = ceil_div64(words, threads);
     const int64_t cap = (int64_t)device_info().sm_count * 16;
     if (blocks > cap) blocks = cap;
-    pack_kernel<<<(unsigned)blocks, threads, 0, stream>>>(codes, scales, E, N, K, packed, err);
+    if (layout == 2)
+        pack2_kernel<<<(unsigned)blocks, threads, 0, stream>>>(codes, scales, E, N, K,
+                                                               reinterpret_cast<uint32_t*>(packed + kHeaderBytes), err);
+    else
+        pack_kernel<<<(unsigned)blocks, threads, 0, stream>>>(codes, scales, E, N, K, packed, err);
     return cudaGetLastError();
 }
 

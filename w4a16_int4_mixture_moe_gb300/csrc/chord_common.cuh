@@ -111,13 +111,20 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
 }
 
 // ---- packed header check ----------------------------------------------------
-__device__ __forceinline__ bool header_ok(const uint8_t* blob, int E, int N, int K) {
+// The header records the layout a blob was packed for; a kernel refuses a blob
+// of another layout or shape (the article's prepared weights record their
+// packing mode and a mismatch fails loudly at dispatch).
+__device__ __forceinline__ bool header_ok_layout(const uint8_t* blob, int E, int N, int K, uint32_t layout) {
     const uint32_t* h = reinterpret_cast<const uint32_t*>(blob);
     const unsigned long long* h64 = reinterpret_cast<const unsigned long long*>(blob + 32);
     const unsigned long long stride = (unsigned long long)N * (unsigned long long)K * 9ull / 16ull;
-    return h[0] == kMagic && h[1] == 1u && h[2] == kLayoutVersion && h[3] == (uint32_t)kGroup &&
-           h[4] == (uint32_t)E && h[5] == (uint32_t)N && h[6] == (uint32_t)K && h64[0] == stride &&
+    return h[0] == kMagic && h[1] == 1u && h[2] == layout && h[3] == (uint32_t)kGroup && h[4] == (uint32_t)E &&
+           h[5] == (uint32_t)N && h[6] == (uint32_t)K && h64[0] == stride &&
            h64[1] == (unsigned long long)kHeaderBytes;
+}
+
+__device__ __forceinline__ bool header_ok(const uint8_t* blob, int E, int N, int K) {
+    return header_ok_layout(blob, E, N, K, kLayoutVersion);
 }
 
 // ---- bf16 packing helpers ---------------------------------------------------
@@ -154,6 +161,23 @@ __device__ __forceinline__ void dequant_frag(uint32_t w, uint32_t sp, uint32_t (
     a[1] = bf2_as_u32(__hmul2(__hsub2(u32_as_bf2(q1), off), s_hi));
     a[2] = bf2_as_u32(__hmul2(__hsub2(u32_as_bf2(q2), off), s_lo));
     a[3] = bf2_as_u32(__hmul2(__hsub2(u32_as_bf2(q3), off), s_hi));
+}
+
+// Eight consecutive columns of one row (layout 2: nibbles 0,4,1,5,2,6,3,7 of
+// `w` hold columns +0..+7) to four bf16x2 registers in column order, with the
+// row's group scale `sp` duplicated in both halves.  Same arithmetic as
+// dequant_frag: 128 + q, minus 136, one rounding multiply.
+__device__ __forceinline__ void dequant_row8(uint32_t w, uint32_t sp, uint32_t* out) {
+    const __nv_bfloat162 off = u32_as_bf2(0x43084308u);  // (136, 136)
+    const __nv_bfloat162 s2 = u32_as_bf2(sp);
+    const uint32_t q0 = lop3_and_or(w, 0x000F000Fu, 0x43004300u);        // columns +0, +1
+    const uint32_t q1 = lop3_and_or(w >> 4, 0x000F000Fu, 0x43004300u);   // +2, +3
+    const uint32_t q2 = lop3_and_or(w >> 8, 0x000F000Fu, 0x43004300u);   // +4, +5
+    const uint32_t q3 = lop3_and_or(w >> 12, 0x000F000Fu, 0x43004300u);  // +6, +7
+    out[0] = bf2_as_u32(__hmul2(__hsub2(u32_as_bf2(q0), off), s2));
+    out[1] = bf2_as_u32(__hmul2(__hsub2(u32_as_bf2(q1), off), s2));
+    out[2] = bf2_as_u32(__hmul2(__hsub2(u32_as_bf2(q2), off), s2));
+    out[3] = bf2_as_u32(__hmul2(__hsub2(u32_as_bf2(q3), off), s2));
 }
 
 __host__ __device__ __forceinline__ int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }

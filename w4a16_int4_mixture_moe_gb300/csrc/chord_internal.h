@@ -17,8 +17,8 @@ struct DeviceInfo {
 const DeviceInfo& device_info();
 
 // ---- pack / align / epilogues (chord_aux.cu) -------------------------------
-cudaError_t launch_pack(const uint8_t* codes, const uint16_t* scales, int E, int N, int K, uint8_t* packed,
-                        int* err, cudaStream_t stream);
+cudaError_t launch_pack(const uint8_t* codes, const uint16_t* scales, int E, int N, int K, int layout,
+                        uint8_t* packed, int* err, cudaStream_t stream);
 
 int align_slices(int64_t P);
 cudaError_t launch_align(const int32_t* topk_ids, int64_t P, int E, int block_m, int32_t* sorted_ids,
@@ -48,13 +48,14 @@ struct GemmArgs {
     int* err;
 };
 
-// Decode regime: tokens of a block in the MMA N dimension (mma.sync m16n8k16),
-// INT4 streamed through a bulk-copy pipeline.  block_m % 8 == 0.
+// Warp-MMA kernel (packed layout 1): tokens of a block in the N dimension of
+// mma.sync m16n8k16, INT4 streamed through a bulk-copy pipeline.
+// block_m % 8 == 0.
 cudaError_t launch_gemm_decode(const GemmArgs& a, cudaStream_t stream);
 
-// Prefill regime: tcgen05 MMA with TMEM accumulators.  block_m % 16 == 0,
-// block_m <= 256.
-cudaError_t launch_gemm_prefill(const GemmArgs& a, cudaStream_t stream);
-bool prefill_available();
+// tcgen05 kernel (packed layout 2): dequantised weights in tensor memory as
+// the MMA's A operand, tokens as its N side, FP32 accumulators in tensor
+// memory.  block_m % 8 == 0, block_m <= 256, N % 128 == 0.
+cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t stream);
 
 }  // namespace chord
