@@ -10,7 +10,9 @@
 //     cp.async.bulk) into a shared-memory ring;
 //   * gather warps copy the block's activation rows (row = pair id / divisor)
 //     with 16-byte cp.async into a 128-byte-swizzled K-major tile, the MMA's B
-//     operand, and publish it after a proxy fence;
+//     operand; each lane's copies arrive on the stage's barrier when they land
+//     (cp.async.mbarrier.arrive.noinc) and the MMA thread fences the async
+//     proxy before reading the tile;
 //   * dequantising warps (one row per thread) turn 32 codes per 16-byte load
 //     into bf16((q - 8) * s) and store them with tcgen05.st into a tensor
 //     memory stage, the MMA's A operand (no shared-memory round trip for the
@@ -31,23 +33,30 @@ namespace chord {
 namespace {
 
 constexpr int kTileRows = 128;   // rows of N per item = MMA M
-constexpr int kBK = 64;          // K columns per stage
+constexpr int kChunkK = 64;      // K columns of one packed chunk; a pipeline stage holds two
 constexpr int kChunk2 = 4608;    // packed bytes of one 128 x 64 chunk (layout 2)
-constexpr int kACols = 32;       // tensor-memory columns of one A stage (64 bf16 per lane)
+constexpr int kACols = 64;       // tensor-memory columns of one A stage (128 bf16 per lane)
 constexpr uint32_t kLayoutTc = 2;
 
-// SA: stages of the A (tensor memory) and B (shared memory) rings; SW: stages
-// of the packed-weight ring (deeper, to keep enough HBM bytes in flight);
-// DQ: dequantising warps (4 or 8); GW: gather warps; MAXR: token rows one
-// gather lane copies per stage (block rows / (GW * 4)).
-template <int SA, int SW, int DQ, int GW, int MAXR>
+// The A operand ring lives in tensor memory (64 columns per stage, as many
+// stages as the columns left after the accumulators allow, sized at launch);
+// GW: gather warps; MAXR: token rows one gather lane copies per stage
+// (block rows / (GW * 4)).  Eight dequantising warps form two warpgroups
+// that take alternate stages.  The B-tile and packed-weight rings live in
+// shared memory and are sized at launch.
+// NI: MMA-issuing warps.  A tcgen05.mma costs its issuing thread tens of
+// cycles whatever N is, so with few tokens per item several issuers, each
+// accumulating every NI-th stage of the item into its own accumulator, keep
+// the tensor pipe fed; the epilogue adds the partial accumulators in issuer
+// order.
+template <int GW, int MAXR, int NI>
 struct Cfg {
-    static constexpr int kProducer = DQ;      // warp index of the weight producer (owns TMEM)
-    static constexpr int kMma = DQ + 1;       // warp index of the MMA issuer
-    static constexpr int kGather0 = DQ + 2;   // first gather warp
-    static constexpr int kWarps = DQ + 2 + GW;
+    static constexpr int kDQ = 8;             // dequantising warps
+    static constexpr int kProducer = kDQ;     // warp index of the weight producer (owns TMEM)
+    static constexpr int kMma0 = kDQ + 1;     // first MMA-issuing warp
+    static constexpr int kGather0 = kDQ + 1 + NI;  // first gather warp
+    static constexpr int kWarps = kDQ + 1 + NI + GW;
     static constexpr int kThreads = kWarps * 32;
-    static constexpr int kLag = SA - 2;       // gather stages kept in flight before publishing
     static constexpr int kMaxTokens = MAXR * GW * 4;
 };
 
@@ -55,6 +64,9 @@ struct TcArgs {
     GemmArgs g;
     int tok_tile;      // rows of the B tile: block_m rounded up to 16
     uint32_t tmem_cols;
+    int nsb;           // stages of the B-tile ring (shared memory)
+    int nsw;           // stages of the packed-weight ring (shared memory)
+    int nsa;           // stages of the A ring (tensor memory)
 };
 
 // ---- tcgen05 / cp.async wrappers --------------------------------------------
@@ -90,12 +102,14 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
         : "memory");
 }
 
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* v) {
     asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
-        "%14, %15, %16};" ::"r"(taddr),
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
         "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
-        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]),
+        "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]),
+        "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
         : "memory");
 }
 
@@ -112,12 +126,16 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// Arrive on `bar` once every cp.async this thread issued so far has landed
+// (the barrier's expected count includes this arrival).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 
 // Shared-memory matrix descriptor of a K-major operand tile with 128-byte
 // swizzle: rows of 64 bf16 (128 bytes), 8-row atoms of 1024 bytes.
@@ -135,19 +153,22 @@ __device__ __forceinline__ uint32_t idesc_bf16(int n) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kTileRows >> 4) << 24);
 }
 
-// Bounded wait that also gives up once another role has aborted.
+// Bounded wait that also gives up once another role has aborted.  The abort
+// flag and the clock are checked every 64 polls only.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
-        if (*abort_flag) return false;
-        if (clock64() - t0 > kWaitLimitCycles) {
-            set_error(err, CHORD_DEV_TIMEOUT);
-            *abort_flag = 1;
-            return false;
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0) {
+            if (*abort_flag) return false;
+            if (clock64() - t0 > kWaitLimitCycles) {
+                set_error(err, CHORD_DEV_TIMEOUT);
+                *abort_flag = 1;
+                return false;
+            }
         }
     }
-    return true;
 }
 
 // Routing facts of one item, computed identically by every role from the
@@ -183,23 +204,51 @@ __device__ __forceinline__ ItemInfo item_info(const GemmArgs& a, int64_t b, int 
     return r;
 }
 
-template <int SA, int SW, int DQ, int GW, int MAXR>
-__global__ void __launch_bounds__(Cfg<SA, SW, DQ, GW, MAXR>::kThreads, 1) gemm_tc_kernel(const TcArgs ta) {
-    using C = Cfg<SA, SW, DQ, GW, MAXR>;
+// Position in a ring of n stages: slot and the parity of the slot's current
+// fill.  Producers wait for the previous fill's release (parity ^ 1),
+// consumers for the fill itself (parity).  Advanced by one stage at a time, so
+// no division on the hot path.
+struct Ring {
+    int slot = 0;
+    uint32_t phase = 0;
+    __device__ __forceinline__ void next(int n) {
+        if (++slot == n) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
+    __device__ __forceinline__ void prev(int n) {
+        if (slot == 0) {
+            slot = n - 1;
+            phase ^= 1u;
+        } else {
+            --slot;
+        }
+    }
+};
+
+template <int GW, int MAXR, int NI>
+__global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel(const TcArgs ta) {
+    using C = Cfg<GW, MAXR, NI>;
+    const int SA = ta.nsa;
     const GemmArgs& a = ta.g;
+    const int NSB = ta.nsb, NSW = ta.nsw;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    // 1024-byte alignment for the swizzled B tiles
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    const int b_tile_bytes = ta.tok_tile * 128;
-    uint8_t* sB = smem;                                   // SA x tok_tile x 128 B
-    uint8_t* sW = sB + SA * b_tile_bytes;                 // SW x 4608 B
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sW + SW * kChunk2);
+    // 1024-byte alignment for the swizzled B tiles; plain pointer arithmetic on
+    // the shared array keeps every access below a shared-memory access
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const int b_sub = ta.tok_tile * 128;              // one 64-column B sub-tile
+    const int b_stage = 2 * b_sub;
+    uint8_t* sB = smem;                               // NSB x 2 sub-tiles
+    uint8_t* sW = sB + NSB * b_stage;                 // NSW x 2 packed chunks
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sW + NSW * 2 * kChunk2);
     uint64_t* w_full = bars;
-    uint64_t* w_empty = w_full + SW;
-    uint64_t* b_full = w_empty + SW;
-    uint64_t* a_full = b_full + SA;
-    uint64_t* st_empty = a_full + SA;
-    uint64_t* acc_full = st_empty + SA;
+    uint64_t* w_empty = w_full + NSW;
+    uint64_t* b_full = w_empty + NSW;
+    uint64_t* b_empty = b_full + NSB;
+    uint64_t* a_full = b_empty + NSB;
+    uint64_t* a_empty = a_full + SA;
+    uint64_t* acc_full = a_empty + SA;
     uint64_t* acc_empty = acc_full + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 1);
     volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // [0] skip, [1] abort
@@ -210,17 +259,20 @@ __global__ void __launch_bounds__(Cfg<SA, SW, DQ, GW, MAXR>::kThreads, 1) gemm_t
         if (!ok) set_error(a.err, CHORD_DEV_BAD_HEADER);
         flags[0] = ok ? 0 : 1;
         flags[1] = 0;
-        for (int s = 0; s < SW; ++s) {
+        for (int s = 0; s < NSW; ++s) {
             mbar_init(&w_full[s], 1);
-            mbar_init(&w_empty[s], DQ);
+            mbar_init(&w_empty[s], 4);        // the 4 warps of the warpgroup that took the stage
+        }
+        for (int s = 0; s < NSB; ++s) {
+            mbar_init(&b_full[s], GW * 32);   // one cp.async-tracked arrival per gather lane
+            mbar_init(&b_empty[s], 1);
         }
         for (int s = 0; s < SA; ++s) {
-            mbar_init(&b_full[s], GW);
-            mbar_init(&a_full[s], DQ);
-            mbar_init(&st_empty[s], 1);
+            mbar_init(&a_full[s], 4);
+            mbar_init(&a_empty[s], 1);
         }
-        mbar_init(acc_full, 1);
-        mbar_init(acc_empty, DQ);
+        mbar_init(acc_full, NI);              // one arrival per MMA issuer
+        mbar_init(acc_empty, C::kDQ);
         fence_barrier_init();
     }
     __syncthreads();
@@ -233,7 +285,7 @@ __global__ void __launch_bounds__(Cfg<SA, SW, DQ, GW, MAXR>::kThreads, 1) gemm_t
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const uint32_t acc_tmem = tmem_base + SA * kACols;
+    const uint32_t acc_tmem = tmem_base + SA * kACols;   // issuer i accumulates at acc_tmem + i * tok_tile
 
     int32_t ntp = *a.ntp;
     if (ntp < 0 || ntp > a.capacity || ntp % a.block_m) {
@@ -241,7 +293,8 @@ __global__ void __launch_bounds__(Cfg<SA, SW, DQ, GW, MAXR>::kThreads, 1) gemm_t
         ntp = 0;
     }
     const int ntiles = a.N / kTileRows;
-    const int kchunks = a.K / kBK;
+    const int kchunks = a.K / kChunkK;
+    const int kstages = (kchunks + 1) / 2;   // the last stage holds one chunk when kchunks is odd
     const int64_t n_items = (int64_t)(ntp / a.block_m) * ntiles;
     const uint64_t expert_bytes = (uint64_t)a.N * (uint64_t)a.K * 9ull / 16ull;
 
@@ -249,6 +302,7 @@ __global__ void __launch_bounds__(Cfg<SA, SW, DQ, GW, MAXR>::kThreads, 1) gemm_t
         // ---------------------------------------------------------- weights
         const uint64_t pol = policy_evict_first();
         int64_t g = 0;   // stages lane 0 issued
+        Ring wr;
         bool ok = true;
         for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
             const int nt = (int)(item % ntiles);
@@ -256,32 +310,38 @@ __global__ void __launch_bounds__(Cfg<SA, SW, DQ, GW, MAXR>::kThreads, 1) gemm_t
             const ItemInfo inf = item_info(a, b, lane, false);
             if (inf.n_mma == 0) continue;
             if (lane == 0) {
+                // chunks (nt, kc) of one expert are contiguous along kc
                 const uint8_t* src = a.packed + kHeaderBytes + (uint64_t)inf.e * expert_bytes +
                                      (uint64_t)nt * (uint64_t)kchunks * kChunk2;
-                for (int kc = 0; kc < kchunks; ++kc, ++g) {
-                    const int slot = (int)(g % SW);
-                    const uint32_t par = (uint32_t)((g / SW) & 1);
-                    if (!wait_or_abort(&w_empty[slot], par ^ 1u, &flags[1], a.err)) {
+                for (int ks = 0; ks < kstages; ++ks, ++g, wr.next(NSW)) {
+                    const int nck = min(2, kchunks - 2 * ks);
+                    if (!wait_or_abort(&w_empty[wr.slot], wr.phase ^ 1u, &flags[1], a.err)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&w_full[slot], kChunk2);
-                    bulk_g2s_hint(sW + slot * kChunk2, src + (uint64_t)kc * kChunk2, kChunk2, &w_full[slot], pol);
+                    mbar_arrive_expect_tx(&w_full[wr.slot], nck * kChunk2);
+                    bulk_g2s_hint(sW + wr.slot * 2 * kChunk2, src + (uint64_t)(2 * ks) * kChunk2, nck * kChunk2,
+                                  &w_full[wr.slot], pol);
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         }
         // leave only after every copy issued here has landed
         if (lane == 0) {
-            for (int s = 0; s < SW && s < g; ++s) {
-                const int64_t last = s + ((g - 1 - s) / SW) * SW;
-                if (!mbar_wait(&w_full[s], (uint32_t)((last / SW) & 1))) set_error(a.err, CHORD_DEV_TIMEOUT);
+            for (int i = 0; i < NSW && i < g; ++i) {
+                wr.prev(NSW);
+                if (!mbar_wait(&w_full[wr.slot], wr.phase)) set_error(a.err, CHORD_DEV_TIMEOUT);
             }
         }
         __syncwarp();
-    } else if (warp == C::kMma) {
+    } else if (warp >= C::kMma0 && warp < C::kGather0) {
         // ------------------------------------------------------------- MMA
-        int64_t g = 0, nitem = 0;   // g: stages whose MMAs lane 0 issued
+        // Issuer mi takes the item's stages ks with ks % NI == mi.
+        const int mi = warp - C::kMma0;
+        const uint32_t my_acc = acc_tmem + (uint32_t)(mi * ta.tok_tile);
+        int64_t nitem = 0;
+        int issued = 0;                 // stages whose MMAs this issuer committed
+        Ring ar, br, last;
         bool ok = true;
         for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
             const int64_t b = item / ntiles;
@@ -291,42 +351,52 @@ __global__ void __launch_bounds__(Cfg<SA, SW, DQ, GW, MAXR>::kThreads, 1) gemm_t
                 if (!wait_or_abort(acc_empty, (uint32_t)((nitem & 1) ^ 1), &flags[1], a.err)) ok = false;
                 tc_fence_after();
                 const uint32_t idesc = idesc_bf16(inf.n_mma);
-                for (int kc = 0; kc < kchunks && ok; ++kc, ++g) {
-                    const int slot = (int)(g % SA);
-                    const uint32_t par = (uint32_t)((g / SA) & 1);
-                    if (!wait_or_abort(&a_full[slot], par, &flags[1], a.err) ||
-                        !wait_or_abort(&b_full[slot], par, &flags[1], a.err)) {
+                bool any = false;
+                for (int ks = 0; ks < kstages && ok; ++ks, ar.next(SA), br.next(NSB)) {
+                    if (ks % NI != mi) continue;
+                    const int nck = min(2, kchunks - 2 * ks);
+                    if (!wait_or_abort(&a_full[ar.slot], ar.phase, &flags[1], a.err) ||
+                        !wait_or_abort(&b_full[br.slot], br.phase, &flags[1], a.err)) {
                         ok = false;
                         break;
                     }
+                    // the B tile was written by cp.async (generic proxy); the MMA
+                    // reads it through the async proxy
+                    fence_proxy_async();
                     tc_fence_after();
-                    const uint32_t b_base = smem_u32(sB + slot * b_tile_bytes);
-#pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk)
-                        tc_mma_ts(acc_tmem, tmem_base + slot * kACols + kk * 8, desc_sw128(b_base + kk * 32), idesc,
-                                  (kc > 0 || kk > 0) ? 1u : 0u);
-                    tc_commit(&st_empty[slot]);
+                    const uint32_t b_base = smem_u32(sB + br.slot * b_stage);
+                    for (int kk = 0; kk < 4 * nck; ++kk)
+                        tc_mma_ts(my_acc, tmem_base + ar.slot * kACols + kk * 8,
+                                  desc_sw128(b_base + (kk >> 2) * b_sub + (kk & 3) * 32), idesc,
+                                  (any || kk > 0) ? 1u : 0u);
+                    any = true;
+                    tc_commit(&a_empty[ar.slot]);
+                    tc_commit(&b_empty[br.slot]);
+                    last = ar;
+                    ++issued;
                 }
-                if (ok) tc_commit(acc_full);
+                if (ok) {
+                    if (any)
+                        tc_commit(acc_full);
+                    else
+                        mbar_arrive(acc_full);   // no share of this item: nothing to wait for
+                }
             }
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             ++nitem;
         }
-        // wait for the last MMAs before the tensor memory is released
-        if (lane == 0 && g > 0) {
-            const int64_t last = g - 1;
-            mbar_wait(&st_empty[last % SA], (uint32_t)((last / SA) & 1));
-        }
+        // wait for this issuer's last MMAs before the tensor memory is released
+        if (lane == 0 && issued > 0) mbar_wait(&a_empty[last.slot], last.phase);
         __syncwarp();
     } else if (warp >= C::kGather0) {
         // ------------------------------------------------------ activations
         // Lane gl copies the 16-byte piece c = gl % 8 of token rows
-        // j = gl / 8 + r * (GW * 4), r < MAXR; their A row indices are read
-        // once per item.
+        // j = gl / 8 + r * (GW * 4), r < MAXR, for both chunks of a stage;
+        // their A row indices are read once per item.
         const int gl = (warp - C::kGather0) * 32 + lane;
         const int c = gl & 7;
         constexpr int kRowStep = GW * 4;
-        int64_t g = 0, published = 0;
+        Ring br;
         bool ok = true;
         for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
             const int64_t b = item / ntiles;
@@ -342,87 +412,89 @@ __global__ void __launch_bounds__(Cfg<SA, SW, DQ, GW, MAXR>::kThreads, 1) gemm_t
                     if (row_valid(a, id)) arow[r] = id / a.a_row_divisor;
                 }
             }
-            for (int kc = 0; kc < kchunks; ++kc, ++g) {
-                const int slot = (int)(g % SA);
-                const uint32_t par = (uint32_t)((g / SA) & 1);
-                if (!wait_or_abort(&st_empty[slot], par ^ 1u, &flags[1], a.err)) {
+            for (int ks = 0; ks < kstages; ++ks, br.next(NSB)) {
+                const int nck = min(2, kchunks - 2 * ks);
+                if (!wait_or_abort(&b_empty[br.slot], br.phase ^ 1u, &flags[1], a.err)) {
                     ok = false;
                     break;
                 }
-                const uint32_t tile = smem_u32(sB + slot * b_tile_bytes);
+                const uint32_t tile = smem_u32(sB + br.slot * b_stage);
+                for (int ch = 0; ch < nck; ++ch) {
 #pragma unroll
-                for (int r = 0; r < MAXR; ++r) {
-                    if (arow[r] < 0) continue;
-                    const int j = (gl >> 3) + r * kRowStep;
-                    const uint16_t* src = a.A + (int64_t)arow[r] * a.K + kc * kBK + c * 8;
-                    const uint32_t dst = tile + (uint32_t)((j >> 3) * 1024 + (j & 7) * 128 + ((c ^ (j & 7)) << 4));
-                    cp_async16(dst, src);
+                    for (int r = 0; r < MAXR; ++r) {
+                        if (arow[r] < 0) continue;
+                        const int j = (gl >> 3) + r * kRowStep;
+                        const uint16_t* src = a.A + (int64_t)arow[r] * a.K + (2 * ks + ch) * kChunkK + c * 8;
+                        const uint32_t dst = tile + (uint32_t)(ch * b_sub + (j >> 3) * 1024 + (j & 7) * 128 +
+                                                               ((c ^ (j & 7)) << 4));
+                        cp_async16(dst, src);
+                    }
                 }
-                cp_async_commit();
-                if (g - published >= C::kLag) {
-                    cp_async_wait<C::kLag>();
-                    fence_proxy_async();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&b_full[published % SA]);
-                    ++published;
-                }
+                cp_async_arrive_noinc(&b_full[br.slot]);
             }
         }
+        // every copy must land before the CTA's shared memory goes away
         cp_async_wait<0>();
-        fence_proxy_async();
         __syncwarp();
-        for (; published < g; ++published)
-            if (lane == 0) mbar_arrive(&b_full[published % SA]);
     } else {
         // --------------------------------------- dequantisation and epilogue
+        // Warpgroup wg takes the stages with (stage index & 1) == wg; each
+        // thread dequantises its row's 128 columns of the stage.
+        const int wg = warp >> 2;
         const int quarter = warp & 3;                  // tensor-memory lane quarter of this warp
         const int row = quarter * 32 + lane;           // weight row of the tile = TMEM lane
-        const int half0 = DQ == 8 ? (warp >> 2) : 0;   // 32-column halves this warp dequantises
-        const int nhalf = DQ == 8 ? 1 : 2;
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         int64_t g = 0, nitem = 0;
+        Ring wr, ar;
         bool ok = true;
         for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
             const int nt = (int)(item % ntiles);
             const int64_t b = item / ntiles;
             const ItemInfo inf = item_info(a, b, lane, false);
             if (inf.n_mma == 0) continue;
-            for (int kc = 0; kc < kchunks; ++kc, ++g) {
-                const int wslot = (int)(g % SW), aslot = (int)(g % SA);
-                if (!wait_or_abort(&w_full[wslot], (uint32_t)((g / SW) & 1), &flags[1], a.err) ||
-                    !wait_or_abort(&st_empty[aslot], (uint32_t)(((g / SA) & 1) ^ 1), &flags[1], a.err)) {
+            for (int ks = 0; ks < kstages; ++ks, ++g, wr.next(NSW), ar.next(SA)) {
+                if ((int)(g & 1) != wg) continue;
+                const int nck = min(2, kchunks - 2 * ks);
+                if (!wait_or_abort(&w_full[wr.slot], wr.phase, &flags[1], a.err) ||
+                    !wait_or_abort(&a_empty[ar.slot], ar.phase ^ 1u, &flags[1], a.err)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint8_t* wch = sW + wslot * kChunk2;
-                uint4 q[2];
+                const uint8_t* wch = sW + wr.slot * 2 * kChunk2;
+                uint4 q[4];
                 uint32_t sc[2];
 #pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    if (i < nhalf) {
-                        q[i] = *reinterpret_cast<const uint4*>(wch + (half0 + i) * 2048 + row * 16);
-                        sc[i] = *reinterpret_cast<const uint16_t*>(wch + 4096 + row * 4 + (half0 + i) * 2);
+                for (int ch = 0; ch < 2; ++ch) {
+                    if (ch < nck) {
+                        q[2 * ch] = *reinterpret_cast<const uint4*>(wch + ch * kChunk2 + row * 16);
+                        q[2 * ch + 1] = *reinterpret_cast<const uint4*>(wch + ch * kChunk2 + 2048 + row * 16);
+                        sc[ch] = *reinterpret_cast<const uint32_t*>(wch + ch * kChunk2 + 4096 + row * 4);
                     }
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&w_empty[wslot]);   // the packed chunk is in registers
+                if (lane == 0) mbar_arrive(&w_empty[wr.slot]);   // the packed chunks are in registers
 #pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    if (i < nhalf) {
-                        const uint32_t sp = sc[i] | (sc[i] << 16);
-                        uint32_t v[16];
-                        dequant_row8(q[i].x, sp, v + 0);
-                        dequant_row8(q[i].y, sp, v + 4);
-                        dequant_row8(q[i].z, sp, v + 8);
-                        dequant_row8(q[i].w, sp, v + 12);
-                        tmem_st16(tmem_base + lane_base + aslot * kACols + (half0 + i) * 16, v);
+                for (int ch = 0; ch < 2; ++ch) {
+                    if (ch < nck) {
+                        uint32_t v[32];
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const uint32_t s16 = h ? (sc[ch] >> 16) : (sc[ch] & 0xffffu);
+                            const uint32_t sp = s16 | (s16 << 16);
+                            const uint4 qq = q[2 * ch + h];
+                            dequant_row8(qq.x, sp, v + 16 * h + 0);
+                            dequant_row8(qq.y, sp, v + 16 * h + 4);
+                            dequant_row8(qq.z, sp, v + 16 * h + 8);
+                            dequant_row8(qq.w, sp, v + 16 * h + 12);
+                        }
+                        tmem_st32(tmem_base + lane_base + ar.slot * kACols + ch * 32, v);
                     }
                 }
                 tc_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&a_full[aslot]);
+                if (lane == 0) mbar_arrive(&a_full[ar.slot]);
             }
             if (!ok) break;
             // ---- epilogue: accumulator column j is token j of the block
@@ -432,11 +504,18 @@ __global__ void __launch_bounds__(Cfg<SA, SW, DQ, GW, MAXR>::kThreads, 1) gemm_t
             }
             tc_fence_after();
             const int n_out = nt * kTileRows + row;
-            const int col0 = DQ == 8 ? (warp >> 2) * 16 : 0;
-            const int col_step = DQ == 8 ? 32 : 16;
-            for (int j0 = col0; j0 < inf.n_mma; j0 += col_step) {
+            const int parts = kstages < NI ? kstages : NI;   // issuers that hold a share of this item
+            for (int j0 = wg * 16; j0 < inf.n_mma; j0 += 32) {
                 uint32_t v[16];
                 tmem_ld16(acc_tmem + lane_base + j0, v);
+                for (int pi = 1; pi < parts; ++pi) {
+                    uint32_t w2[16];
+                    tc_wait_ld();
+                    tmem_ld16(acc_tmem + (uint32_t)(pi * ta.tok_tile) + lane_base + j0, w2);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) v[u] = __float_as_uint(__uint_as_float(v[u]) + __uint_as_float(w2[u]));
+                }
                 // pair ids of tokens j0..j0+15: one load per lane, then shuffles
                 int32_t my_id = -1;
                 if (lane < 16 && j0 + lane < a.block_m) {
@@ -475,17 +554,42 @@ uint32_t pow2_cols(uint32_t c) {
     return p;
 }
 
-template <int SA, int SW, int DQ, int GW, int MAXR>
-cudaError_t launch_cfg(const GemmArgs& g, cudaStream_t stream) {
-    using C = Cfg<SA, SW, DQ, GW, MAXR>;
+template <int GW, int MAXR, int NI>
+cudaError_t launch_cfg(const GemmArgs& g, bool deep_weights, cudaStream_t stream) {
+    using C = Cfg<GW, MAXR, NI>;
+    constexpr size_t kSmemBudget = 220 * 1024;   // of the 227 KB a CTA may use
     TcArgs ta;
     ta.g = g;
     ta.tok_tile = (g.block_m < 16 ? 16 : (g.block_m + 15) / 16 * 16);
     if (ta.tok_tile > C::kMaxTokens) return cudaErrorInvalidConfiguration;
-    const uint32_t cols = SA * kACols + ta.tok_tile;
-    if (cols > 512) return cudaErrorInvalidConfiguration;
+    // A ring: every tensor-memory column the accumulators leave, at most 8 stages
+    int nsa = (int)((512 - NI * ta.tok_tile) / kACols);
+    nsa = nsa > 8 ? 8 : nsa;
+    if (nsa < 2) return cudaErrorInvalidConfiguration;
+    ta.nsa = nsa;
+    const uint32_t cols = nsa * kACols + NI * ta.tok_tile;
     ta.tmem_cols = pow2_cols(cols);
-    size_t smem = 1024 + (size_t)SA * ta.tok_tile * 128 + (size_t)SW * kChunk2 + (2 * SW + 3 * SA + 2) * 8 + 16;
+    // Ring depths.  Few tokens per item (HBM-bound): about 64 KB of B tiles and
+    // the rest of the budget for packed weights, to keep enough HBM bytes in
+    // flight.  Many tokens per item: four weight stages and the rest for B
+    // tiles, whose gather from L2 has the longer latency per byte consumed.
+    const size_t b_stage = (size_t)ta.tok_tile * 256, w_stage = 2 * kChunk2;
+    const size_t fixed = 1024 + 64;
+    int nsb, nsw;
+    if (deep_weights) {
+        nsb = (int)((64 * 1024) / b_stage);
+        nsb = nsb < 2 ? 2 : (nsb > 16 ? 16 : nsb);
+        nsw = (int)((kSmemBudget - fixed - nsb * (b_stage + 16)) / (w_stage + 16));
+        nsw = nsw > 32 ? 32 : nsw;
+    } else {
+        nsw = 4;
+        nsb = (int)((kSmemBudget - fixed - nsw * (w_stage + 16)) / (b_stage + 16));
+        nsb = nsb > 16 ? 16 : nsb;
+    }
+    if (nsw < 2 || nsb < 2) return cudaErrorInvalidConfiguration;
+    ta.nsb = nsb;
+    ta.nsw = nsw;
+    size_t smem = fixed + (size_t)nsb * b_stage + (size_t)nsw * w_stage + (2 * nsw + 2 * nsb + 2 * nsa + 2) * 8 + 16;
     // A CTA that cannot get its tensor-memory columns waits in tcgen05.alloc
     // until a co-resident CTA exits.  When two CTAs' columns do not fit in the
     // SM's 512, ask for enough shared memory that only one CTA fits per SM.
@@ -494,13 +598,13 @@ cudaError_t launch_cfg(const GemmArgs& g, cudaStream_t stream) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<SA, SW, DQ, GW, MAXR>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<GW, MAXR, NI>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         if (e != cudaSuccess) return e;
         configured_dev = dev;
     }
     int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_tc_kernel<SA, SW, DQ, GW, MAXR>,
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_tc_kernel<GW, MAXR, NI>,
                                                                   C::kThreads, smem);
     if (e != cudaSuccess) return e;
     const int tmem_fit = (int)(512 / ta.tmem_cols);
@@ -510,7 +614,7 @@ cudaError_t launch_cfg(const GemmArgs& g, cudaStream_t stream) {
     int64_t grid = (int64_t)device_info().sm_count * per_sm;
     if (grid > items_cap) grid = items_cap;
     if (grid < 1) grid = 1;
-    gemm_tc_kernel<SA, SW, DQ, GW, MAXR><<<(unsigned)grid, C::kThreads, smem, stream>>>(ta);
+    gemm_tc_kernel<GW, MAXR, NI><<<(unsigned)grid, C::kThreads, smem, stream>>>(ta);
     return cudaGetLastError();
 }
 
@@ -519,9 +623,9 @@ cudaError_t launch_cfg(const GemmArgs& g, cudaStream_t stream) {
 bool tc_available() { return true; }
 
 cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t stream) {
-    if (a.block_m % 8 || a.block_m > 256 || a.N % kTileRows || a.K % kBK) return cudaErrorInvalidValue;
-    if (a.block_m <= 64) return launch_cfg<8, 16, 8, 1, 16>(a, stream);   // up to 64 tokens per item
-    return launch_cfg<4, 8, 8, 4, 16>(a, stream);                        // up to 256 tokens per item
+    if (a.block_m % 8 || a.block_m > 256 || a.N % kTileRows || a.K % kChunkK) return cudaErrorInvalidValue;
+    if (a.block_m <= 64) return launch_cfg<1, 16, 2>(a, true, stream);   // up to 64 tokens per item
+    return launch_cfg<4, 16, 1>(a, false, stream);                       // up to 256 tokens per item
 }
 
 }  // namespace chord
