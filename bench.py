@@ -46,6 +46,7 @@ KERNEL_SRC = {
     "warp_mma": os.path.join(ROOT, "w4a16_int4_mixture_moe_gb300", "csrc", "chord_gemm_decode.cu"),
 }
 
+KERNEL_NAME = {"tc": "gemm_tc_kernel", "warp_mma": "gemm_decode_kernel"}
 
 # ----------------------------------------------------------------- accounting
 
@@ -400,17 +401,19 @@ def main():
     # bandwidth), tensor-bound above it.
     ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
     regime = "decode" if f1_ / b1 < ridge else "prefill"
+    kind = "warp_mma" if chord.chord_select_kernel(bm) == chord.KERNEL_WARP_MMA else "tc"
+    kname = KERNEL_NAME[kind] + " (gate_up)"
     if regime == "decode":
         ach = b1 / (g1 * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": profiled_traffic("tc", w.name),
-                "kernel": "gemm_tc_kernel (gate_up)", "peak_src": peaks["src"]}
+                "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": profiled_traffic(kind, w.name),
+                "kernel": kname, "peak_src": peaks["src"]}
     else:
         ach = f1_ / (g1 * 1e-3) / 1e12
         pk = peaks["bf16_tflops_sustained"]
         roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": pk, "unit": "TFLOP/s",
-                "frac": round(ach / pk, 4), "traffic": profiled_traffic("tc", w.name),
-                "kernel": "gemm_tc_kernel (gate_up)", "peak_src": peaks["src"]}
+                "frac": round(ach / pk, 4), "traffic": profiled_traffic(kind, w.name),
+                "kernel": kname, "peak_src": peaks["src"]}
     clk = sampler.summary(t_lo, t_hi)
     line = {
         "metric": METRIC, "value": round(us_per_call, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,

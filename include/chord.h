@@ -68,19 +68,23 @@ typedef enum chord_status {
 #define CHORD_DEV_BAD_CODE 5     /* pack: a code above 15 */
 #define CHORD_DEV_BAD_PADDED 6   /* num_tokens_padded above capacity or not a multiple of block_m */
 
-/* GEMM kernel family.  Both take the block's tokens as the MMA's N side (the
- * operand swap of the article's decode profile), so one kernel serves small
- * and large tokens-per-expert; the block size (chord_select_block_m) carries
- * the decode / prefill distinction.  Each family reads its own packed layout. */
+/* GEMM kernel family, picked from rows per expert (the article's two
+ * regimes, section "Indexed kernels"): both take the block's tokens as the
+ * MMA's N side (the operand swap of the article's decode profile) and read the
+ * same packed layout.  CHORD_KERNEL_AUTO picks by block size
+ * (chord_select_kernel): the warp-level kernel for decode blocks of at most 32
+ * rows, the tcgen05 kernel above. */
 typedef enum chord_kernel {
-    CHORD_KERNEL_AUTO = 0,      /* CHORD_KERNEL_TCGEN05 */
+    CHORD_KERNEL_AUTO = 0,      /* chord_select_kernel(block_m) */
     CHORD_KERNEL_TCGEN05 = 1,   /* tcgen05.mma, dequantised A in tensor memory, FP32 accumulators
-                                   in tensor memory; packed layout CHORD_LAYOUT_TCGEN05 */
-    CHORD_KERNEL_WARP_MMA = 2   /* warp-level mma.sync m16n8k16 with register dequantisation;
-                                   packed layout CHORD_LAYOUT_WARP_MMA */
+                                   in tensor memory (prefill regime) */
+    CHORD_KERNEL_WARP_MMA = 2   /* warp-level mma.sync m16n8k16 with register dequantisation
+                                   (decode regime) */
 } chord_kernel;
 
-/* Packed weight layouts (recorded in the blob's header, checked on the device). */
+/* Packed weight layouts (recorded in the blob's header, checked on the device).
+ * Both kernels read CHORD_LAYOUT_TCGEN05; layout 1 is packed for tests of the
+ * header check only and no kernel accepts it. */
 #define CHORD_LAYOUT_WARP_MMA 1   /* 16 x 64 chunks in m16n8k16 A-fragment order, N % 16 == 0 */
 #define CHORD_LAYOUT_TCGEN05 2    /* 128 x 64 chunks, one row per 16-byte group, N % 128 == 0 */
 
@@ -199,6 +203,12 @@ chord_status chord_moe_align_noalloc(const int32_t *topk_ids, int T, int topk, i
  * reading anything back.  Small tok_e gives a decode block (8..64), large
  * tok_e a prefill block.  Always returns a valid block_m. */
 int chord_select_block_m(int T, int topk, int E_local, int E_global, int N, int K);
+
+/* The kernel CHORD_KERNEL_AUTO runs for blocks of block_m rows:
+ * CHORD_KERNEL_WARP_MMA for block_m <= 32, else CHORD_KERNEL_TCGEN05.  The
+ * environment variable CHORD_KERNEL (1 or 2), when set, overrides the choice
+ * for every call whose opts leave the kernel at AUTO. */
+int chord_select_kernel(int block_m);
 
 /* ------------------------------------------------------------------- GEMM */
 

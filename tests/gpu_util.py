@@ -40,7 +40,7 @@ def assert_close(got_bits, ref_bits, what=""):
 
 
 KERNELS = {"tcgen05": (chord.KERNEL_TCGEN05, chord.LAYOUT_TCGEN05),
-           "warp_mma": (chord.KERNEL_WARP_MMA, chord.LAYOUT_WARP_MMA)}
+           "warp_mma": (chord.KERNEL_WARP_MMA, chord.LAYOUT_TCGEN05)}
 
 
 def pack(codes, scales, layout=chord.LAYOUT_TCGEN05):

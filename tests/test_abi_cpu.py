@@ -77,6 +77,25 @@ def test_select_block_m(lib):
         prev = bm
 
 
+def test_select_kernel_by_regime(lib, monkeypatch):
+    """Decode blocks (at most 32 rows) go to the warp-level kernel, larger ones
+    to the tcgen05 kernel; the decode workload's block and the prefill
+    workload's block land on different sides."""
+    monkeypatch.delenv("CHORD_KERNEL", raising=False)
+    for bm in (8, 16, 24, 32):
+        assert chord.chord_select_kernel(bm) == chord.KERNEL_WARP_MMA
+    for bm in (40, 64, 128, 256):
+        assert chord.chord_select_kernel(bm) == chord.KERNEL_TCGEN05
+    assert chord.chord_select_kernel(chord.chord_select_block_m(512, 8, 48, 384, 4096, 7168)) == chord.KERNEL_WARP_MMA
+    assert chord.chord_select_kernel(chord.chord_select_block_m(8192, 8, 48, 384, 4096, 7168)) == chord.KERNEL_TCGEN05
+    monkeypatch.setenv("CHORD_KERNEL", "1")
+    assert chord.chord_select_kernel(8) == chord.KERNEL_TCGEN05
+    monkeypatch.setenv("CHORD_KERNEL", "2")
+    assert chord.chord_select_kernel(256) == chord.KERNEL_WARP_MMA
+    monkeypatch.setenv("CHORD_KERNEL", "7")        # not a kernel: ignored
+    assert chord.chord_select_kernel(256) == chord.KERNEL_TCGEN05
+
+
 def test_layer_workspace_formula(lib):
     T, topk, E, H, I, bm = 512, 8, 48, 7168, 2048, 16
     P = T * topk

@@ -268,15 +268,15 @@ def test_gemm_nothing_local_writes_nothing(kernel):
 
 def test_gemm_header_mismatch_is_reported():
     """A blob packed for (E, N, K) = (2, 128, 128) passed as (2, 256, 64) has the
-    right size but the wrong header, and a blob of the warp-MMA layout passed to
-    the tcgen05 kernel the wrong layout: the device refuses both and writes nothing."""
+    right size but the wrong header, and a blob of packed layout 1 has the wrong
+    layout for either kernel: the device refuses each and writes nothing."""
     E = 2
     codes = wl.random_codes(1, (E, 128, 128))
     scales = wl.random_scales(2, (E, 128, 4))
     ids = wl.random_ids(3, 8, 2, E)
     s, e, n = align(ids, E, 8)
-    for layout, N, K, kernel in [(2, 256, 64, chord.KERNEL_TCGEN05), (1, 128, 128, chord.KERNEL_TCGEN05),
-                                 (2, 128, 128, chord.KERNEL_WARP_MMA)]:
+    for layout, N, K, kernel in [(2, 256, 64, chord.KERNEL_TCGEN05), (2, 256, 64, chord.KERNEL_WARP_MMA),
+                                 (1, 128, 128, chord.KERNEL_TCGEN05), (1, 128, 128, chord.KERNEL_WARP_MMA)]:
         packed = pack(codes, scales, layout)
         x = wl.random_bf16(4, (8, K))
         C = torch.full((16, N), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)

@@ -17,7 +17,7 @@ from . import build as _build
 __all__ = [
     "ChordError", "ChordOpts", "load", "build",
     "chord_version", "chord_status_string", "chord_packed_weight_bytes", "chord_pack_weights",
-    "chord_align_capacity", "chord_align_workspace_bytes", "chord_moe_align", "chord_select_block_m",
+    "chord_align_capacity", "chord_align_workspace_bytes", "chord_moe_align", "chord_select_block_m", "chord_select_kernel",
     "chord_gemm_workspace_bytes", "chord_w4a16_moe_gemm", "chord_silu_mul", "chord_moe_combine",
     "chord_layer_workspace_bytes", "chord_moe_layer", "chord_get_device_error",
     "KERNEL_AUTO", "KERNEL_TCGEN05", "KERNEL_WARP_MMA", "LAYOUT_WARP_MMA", "LAYOUT_TCGEN05",
@@ -59,6 +59,7 @@ _SIGS = {
     "chord_moe_align": (_int, [_vp, _int, _int, _int, _int, _vp, _vp, _vp, _i64, _vp, _sz, _OPTS, _vp]),
     "chord_moe_align_noalloc": (_int, [_vp, _int, _int, _int, _int, _vp, _vp, _vp, _i64, _OPTS, _vp]),
     "chord_select_block_m": (_int, [_int, _int, _int, _int, _int, _int]),
+    "chord_select_kernel": (_int, [_int]),
     "chord_gemm_workspace_bytes": (_sz, [_i64, _int, _int, _int, _OPTS]),
     "chord_w4a16_moe_gemm": (_int, [_vp, _i64, _int, _vp, _sz, _int, _int, _int, _vp, _vp, _vp, _i64, _int, _i64,
                                     _vp, _vp, _sz, _OPTS, _vp]),
@@ -167,6 +168,10 @@ def chord_moe_align_noalloc(topk_ids, E: int, block_m: int, sorted_ids, expert_i
 
 def chord_select_block_m(T: int, topk: int, E_local: int, E_global: int, N: int, K: int) -> int:
     return load().chord_select_block_m(T, topk, E_local, E_global, N, K)
+
+
+def chord_select_kernel(block_m: int) -> int:
+    return load().chord_select_kernel(block_m)
 
 
 def chord_gemm_workspace_bytes(num_pairs: int, N: int, K: int, block_m: int, opts=None) -> int:

@@ -33,6 +33,11 @@ chord_opts opts_or_default(const chord_opts* o) {
     return d;
 }
 
+// Blocks of at most this many rows (tok_e up to about 20) go to the
+// warp-level MMA kernel, whose cost per stage does not depend on a tensor-core
+// instruction's issue latency; larger blocks to the tcgen05 kernel.
+constexpr int kDecodeMaxBlockM = 32;
+
 int env_int(const char* name, int dflt) {
     const char* v = getenv(name);
     return v && *v ? atoi(v) : dflt;
@@ -167,6 +172,12 @@ int chord_select_block_m(int T, int topk, int E_local, int E_global, int N, int 
     return bm;
 }
 
+int chord_select_kernel(int block_m) {
+    const int forced = env_int("CHORD_KERNEL", 0);
+    if (forced == CHORD_KERNEL_TCGEN05 || forced == CHORD_KERNEL_WARP_MMA) return forced;
+    return block_m <= kDecodeMaxBlockM ? CHORD_KERNEL_WARP_MMA : CHORD_KERNEL_TCGEN05;
+}
+
 size_t chord_gemm_workspace_bytes(int64_t num_pairs, int N, int K, int block_m, const chord_opts* opts) {
     (void)num_pairs;
     (void)N;
@@ -189,11 +200,9 @@ chord_status chord_w4a16_moe_gemm(const void* A, int64_t a_rows, int a_row_divis
     if (N % 128 || K % 64 || block_m % 8 || block_m > 256) return CHORD_ERR_UNSUPPORTED;
     if (num_pairs >= INT32_MAX) return CHORD_ERR_UNSUPPORTED;
     const chord_opts o = opts_or_default(opts);
-    int kernel = o.kernel ? o.kernel : env_int("CHORD_KERNEL", 0);
-    if (kernel == CHORD_KERNEL_AUTO) kernel = CHORD_KERNEL_TCGEN05;
+    const int kernel = o.kernel ? o.kernel : chord_select_kernel(block_m);
     if (kernel != CHORD_KERNEL_TCGEN05 && kernel != CHORD_KERNEL_WARP_MMA) return CHORD_ERR_INVALID_ARG;
-    const int layout = kernel == CHORD_KERNEL_TCGEN05 ? CHORD_LAYOUT_TCGEN05 : CHORD_LAYOUT_WARP_MMA;
-    if (packed_bytes != chord_packed_weight_bytes(E, N, K, layout)) return CHORD_ERR_LAYOUT_MISMATCH;
+    if (packed_bytes != chord_packed_weight_bytes(E, N, K, CHORD_LAYOUT_TCGEN05)) return CHORD_ERR_LAYOUT_MISMATCH;
     if (!packed || !aligned16(packed) || !num_tokens_padded || (capacity > 0 && (!sorted_ids || !expert_ids)))
         return CHORD_ERR_INVALID_ARG;
     if (capacity % block_m) return CHORD_ERR_INVALID_ARG;

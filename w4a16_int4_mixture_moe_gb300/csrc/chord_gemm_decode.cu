@@ -1,4 +1,4 @@
-// Decode-regime indexed W4A16 GEMM for sm_103a.
+// Decode-regime indexed W4A16 GEMM for sm_103a (warp-level tensor-core MMA).
 //
 // Few routed rows per expert (tok_e of order 10) make this projection a
 // weight stream: every packed INT4 byte is read once and used for at most a
@@ -7,16 +7,21 @@
 //     Blackwell indexed decode"): dequantised weights fill the 16-row M side
 //     of a warp-level m16n8k16 BF16 MMA, the block's tokens its N side, so
 //     8 tokens cost one MMA instead of a 128-row tile of padding;
-//   * streams weights with bulk asynchronous copies (cp.async.bulk, completion
-//     counted on mbarriers) into a STAGES-deep shared-memory ring, issued by
-//     one producer warp, so tens of KB per SM are in flight;
+//   * streams the packed 128-row x 128-column weight stage (two contiguous
+//     4608-byte chunks of the 128x64-chunk layout) with one bulk asynchronous
+//     copy (cp.async.bulk, completion counted on an mbarrier) into a
+//     STAGES-deep shared-memory ring, issued by one producer warp;
 //   * gathers the block's activation rows (one 256-byte row slice per token
 //     and stage, row = pair id / a_row_divisor, sentinels skipped) into the
 //     same stage;
-//   * dequantises in registers: one 16-byte shared load gives a lane the codes
-//     of four k16 steps of its A fragment (the packed layout is built for it),
-//     0x4300|q gives 128+q, minus 136 gives q-8 exactly, one bf16x2 multiply
-//     by the group scale rounds once ("subtract then scale");
+//   * dequantises in registers: lane (g, c) of a warp owns columns
+//     [16c, 16c + 16) of every 64-column chunk for rows g and g + 8 of its
+//     16-row tile.  The MMA's K order inside a chunk is permuted to match (the
+//     k16 step s takes columns 16c + 4s .. 16c + 4s + 3 of each lane, for the
+//     A and the B fragment alike), so one 8-byte shared load gives a lane the
+//     codes of four k16 steps.  0x4300|q is 128+q, minus 136 gives q-8
+//     exactly, one bf16x2 multiply by the group scale rounds once ("subtract
+//     then scale");
 //   * runs persistently: CTA i takes work items i, i + grid, ... where an item
 //     is (align block, 8*NT-token sub-block, 128-row N tile), bounded on the
 //     device by num_tokens_padded, so nothing is read back to the host.
@@ -33,11 +38,11 @@ namespace {
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kBN = kConsumerWarps * 32;          // 128 output rows per item
-constexpr int kMtiles = kBN / 16;                 // 8 m16 tiles
 constexpr int kKS = 128;                          // K columns per stage
-constexpr int kChunkSpan = kMtiles * kChunkBytes; // 4608: one 64-column chunk of 8 m-tiles
-constexpr int kWStageBytes = (kKS / 64) * kChunkSpan;
-constexpr int kXStride = kKS * 2 + 16;            // padded token row: conflict-free ldmatrix
+constexpr int kChunk2 = 4608;                     // one 128-row x 64-column packed chunk
+constexpr int kWStageBytes = (kKS / 64) * kChunk2;
+constexpr int kXStride = kKS * 2 + 16;            // padded token row: conflict-free 16-byte loads
+constexpr uint32_t kLayoutTile = 2;
 
 template <int NT>
 struct Cfg {
@@ -51,16 +56,6 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
         "{%0,%1,%2,%3};\n"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-
-__device__ __forceinline__ void ldmatrix_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];\n" : "=r"(r0), "=r"(r1) : "r"(addr));
 }
 
 // Per-item routing facts, computed identically by the producer and the
@@ -78,8 +73,9 @@ __device__ __forceinline__ ItemRows load_item_rows(const GemmArgs& a, int64_t b,
         const int i = lane + 32 * s;
         int32_t id = -1;
         bool ok = false;
-        if (i < Cfg<NT>::kTok) {
-            id = a.sorted_ids[b * a.block_m + (int64_t)sub * Cfg<NT>::kTok + i];
+        const int slot_in_block = sub * Cfg<NT>::kTok + i;
+        if (i < Cfg<NT>::kTok && slot_in_block < a.block_m) {
+            id = a.sorted_ids[b * a.block_m + slot_in_block];
             if (id != (int32_t)a.num_pairs) {
                 ok = id >= 0 && (int64_t)id < a.num_pairs && (int64_t)(id / a.a_row_divisor) < a.a_rows;
                 if (!ok) set_error(err, CHORD_DEV_BAD_ROW);
@@ -102,7 +98,7 @@ __global__ void __launch_bounds__(kThreads) gemm_decode_kernel(const GemmArgs a)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        const bool ok = header_ok(a.packed, a.E, a.N, a.K);
+        const bool ok = header_ok_layout(a.packed, a.E, a.N, a.K, kLayoutTile);
         if (!ok) set_error(a.err, CHORD_DEV_BAD_HEADER);
         flags[0] = ok ? 0 : 1;
         flags[1] = 0;
@@ -120,11 +116,11 @@ __global__ void __launch_bounds__(kThreads) gemm_decode_kernel(const GemmArgs a)
         if (threadIdx.x == 0) set_error(a.err, CHORD_DEV_BAD_PADDED);
         ntp = 0;
     }
-    const int nsub = a.block_m / kTok;
+    const int nsub = (a.block_m + kTok - 1) / kTok;   // token sub-blocks; slots past block_m are empty
     const int ntiles = a.N / kBN;
     const int64_t n_items = (int64_t)(ntp / a.block_m) * nsub * ntiles;
     const int kstages = (a.K + kKS - 1) / kKS;
-    const int mt_total = a.N / 16;
+    const int kchunks = a.K / 64;
     const uint64_t expert_bytes = (uint64_t)a.N * (uint64_t)a.K * 9ull / 16ull;
     const uint8_t* wbase = a.packed + kHeaderBytes;
 
@@ -164,13 +160,13 @@ __global__ void __launch_bounds__(kThreads) gemm_decode_kernel(const GemmArgs a)
                 const uint32_t xbytes = (uint32_t)nchunk * 64u * 2u;
                 uint8_t* sW = smem + slot * kStage;
                 uint8_t* sX = sW + kWStageBytes;
-                if (lane == 0) mbar_arrive_expect_tx(&full[slot], (uint32_t)(nchunk * kChunkSpan) + nvalid * xbytes);
-                __syncwarp();
-                if (lane < nchunk) {
-                    const int kc = ks * 2 + lane;
-                    const uint8_t* src = wexp + ((uint64_t)kc * mt_total + (uint64_t)nt * kMtiles) * kChunkBytes;
-                    bulk_g2s_hint(sW + lane * kChunkSpan, src, kChunkSpan, &full[slot], pol);
+                if (lane == 0) {
+                    // chunks (nt, kc) of one expert are contiguous along kc
+                    mbar_arrive_expect_tx(&full[slot], (uint32_t)(nchunk * kChunk2) + nvalid * xbytes);
+                    const uint8_t* src = wexp + ((uint64_t)nt * kchunks + (uint64_t)(2 * ks)) * kChunk2;
+                    bulk_g2s_hint(sW, src, (uint32_t)(nchunk * kChunk2), &full[slot], pol);
                 }
+                __syncwarp();
 #pragma unroll
                 for (int s = 0; s < 2; ++s)
                     if (arow[s]) bulk_g2s(sX + (lane + 32 * s) * kXStride, arow[s] + ks * kKS, xbytes, &full[slot]);
@@ -190,8 +186,12 @@ __global__ void __launch_bounds__(kThreads) gemm_decode_kernel(const GemmArgs a)
     // -------------------------------------------------------------- consumers
     const int g = lane >> 2, c = lane & 3;
     int64_t stage = 0;
-    // ldmatrix lane addressing: matrix q = lane / 8 (token tile +q/2, k half q%2), row lane % 8
-    const int lm_q = lane >> 3, lm_r = lane & 7;
+    // Lane (g, c): rows g and g + 8 of each 16-row tile, chunk columns
+    // [16c, 16c + 16): the two code words (c & 1) * 2 and + 1 of the 32-column
+    // half c >> 1, and that half's scale.
+    const int half = c >> 1;
+    const uint32_t code_off = (uint32_t)(half * 2048 + (c & 1) * 8);
+    const uint32_t scale_shift = (uint32_t)(half * 16);
     for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
         const int nt = (int)(item % ntiles);
         const int64_t bs = item / ntiles;
@@ -229,41 +229,43 @@ __global__ void __launch_bounds__(kThreads) gemm_decode_kernel(const GemmArgs a)
             const uint8_t* sW = smem + slot * kStage;
             const uint32_t sX = smem_u32(sW + kWStageBytes);
             for (int ch = 0; ch < nchunk; ++ch) {
-                uint4 wv[2];
-                uint32_t sc[2][2];
+                const uint8_t* cb = sW + ch * kChunk2;
+                // A fragments of the four k16 steps for both 16-row tiles:
+                // av[mi][r][p] = bf16x2 pair p (columns 16c + 2p, +1) of row g (r = 0) or g + 8 (r = 1)
+                uint32_t av[2][2][8];
 #pragma unroll
                 for (int mi = 0; mi < 2; ++mi) {
-                    const uint8_t* cp = sW + ch * kChunkSpan + (warp * 2 + mi) * kChunkBytes;
-                    wv[mi] = *reinterpret_cast<const uint4*>(cp + lane * 16);
-                    sc[mi][0] = *reinterpret_cast<const uint32_t*>(cp + kChunkWeightBytes + g * 4);
-                    sc[mi][1] = *reinterpret_cast<const uint32_t*>(cp + kChunkWeightBytes + (8 + g) * 4);
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const int row = warp * 32 + mi * 16 + r * 8 + g;
+                        const uint2 w = *reinterpret_cast<const uint2*>(cb + code_off + row * 16);
+                        const uint32_t s32 = *reinterpret_cast<const uint32_t*>(cb + 4096 + row * 4);
+                        const uint32_t s16 = (s32 >> scale_shift) & 0xffffu;
+                        const uint32_t sp = s16 | (s16 << 16);
+                        dequant_row8(w.x, sp, av[mi][r]);
+                        dequant_row8(w.y, sp, av[mi][r] + 4);
+                    }
                 }
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int kcol = ch * 64 + j * 16;
-                    uint32_t bf[NT][2];
-                    if constexpr (NT == 1) {
-                        const int q = lm_q & 1;
-                        ldmatrix_x2(sX + (uint32_t)(lm_r * kXStride + (kcol + 8 * q) * 2), bf[0][0], bf[0][1]);
-                    } else {
+                for (int t = 0; t < NT; ++t) {
+                    if (!(tmask & (1u << t))) continue;
+                    // B fragments: token 8t + g, the same 16 columns
+                    const uint32_t xa = sX + (uint32_t)((8 * t + g) * kXStride + (ch * 64 + 16 * c) * 2);
+                    uint32_t bv[8];
+                    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(bv[0]), "=r"(bv[1]), "=r"(bv[2]), "=r"(bv[3])
+                                 : "r"(xa));
+                    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(bv[4]), "=r"(bv[5]), "=r"(bv[6]), "=r"(bv[7])
+                                 : "r"(xa + 16));
 #pragma unroll
-                        for (int tp = 0; tp < NT / 2; ++tp) {
-                            if (tmask & (3u << (2 * tp))) {
-                                const int tile = 2 * tp + (lm_q >> 1);
-                                const uint32_t addr =
-                                    sX + (uint32_t)((8 * tile + lm_r) * kXStride + (kcol + 8 * (lm_q & 1)) * 2);
-                                ldmatrix_x4(addr, bf[2 * tp][0], bf[2 * tp][1], bf[2 * tp + 1][0], bf[2 * tp + 1][1]);
-                            }
+                    for (int st = 0; st < 4; ++st) {
+#pragma unroll
+                        for (int mi = 0; mi < 2; ++mi) {
+                            const uint32_t af[4] = {av[mi][0][2 * st], av[mi][1][2 * st], av[mi][0][2 * st + 1],
+                                                    av[mi][1][2 * st + 1]};
+                            mma_bf16_16816(acc[mi][t], af, bv[2 * st], bv[2 * st + 1]);
                         }
-                    }
-#pragma unroll
-                    for (int mi = 0; mi < 2; ++mi) {
-                        const uint32_t word = j == 0 ? wv[mi].x : j == 1 ? wv[mi].y : j == 2 ? wv[mi].z : wv[mi].w;
-                        uint32_t af[4];
-                        dequant_frag(word, sc[mi][j >> 1], af);
-#pragma unroll
-                        for (int t = 0; t < NT; ++t)
-                            if (tmask & (1u << t)) mma_bf16_16816(acc[mi][t], af, bf[t][0], bf[t][1]);
                     }
                 }
             }
@@ -324,7 +326,7 @@ cudaError_t launch_nt(const GemmArgs& a, cudaStream_t stream) {
                                                                   smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
-    const int64_t items_cap = (a.capacity / a.block_m) * (a.block_m / (NT * 8)) * (a.N / kBN);
+    const int64_t items_cap = (a.capacity / a.block_m) * ((a.block_m + NT * 8 - 1) / (NT * 8)) * (a.N / kBN);
     int64_t grid = (int64_t)device_info().sm_count * per_sm;
     if (grid > items_cap) grid = items_cap;
     if (grid < 1) grid = 1;
@@ -335,11 +337,13 @@ cudaError_t launch_nt(const GemmArgs& a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_gemm_decode(const GemmArgs& a, cudaStream_t stream) {
-    // Token sub-block of the MMA N side: the largest of 64/32/16/8 dividing block_m.
-    if (a.block_m % 64 == 0) return launch_nt<8, 4>(a, stream);
-    if (a.block_m % 32 == 0) return launch_nt<4, 5>(a, stream);
-    if (a.block_m % 16 == 0) return launch_nt<2, 6>(a, stream);
-    return launch_nt<1, 6>(a, stream);
+    // Tokens per item: the smallest of 8/16/32/64 that holds the whole block
+    // (larger blocks are split into 64-token sub-blocks, each re-streaming the
+    // weights).  Ring depth: as many stages as let two CTAs share an SM.
+    if (a.block_m <= 8) return launch_nt<1, 9>(a, stream);
+    if (a.block_m <= 16) return launch_nt<2, 8>(a, stream);
+    if (a.block_m <= 32) return launch_nt<4, 6>(a, stream);
+    return launch_nt<8, 4>(a, stream);
 }
 
 }  // namespace chord
