@@ -35,19 +35,21 @@
 namespace chord {
 namespace {
 
-constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kBN = kConsumerWarps * 32;          // 128 output rows per item
+constexpr int kBN = 128;                          // output rows per item
 constexpr int kKS = 128;                          // K columns per stage
 constexpr int kChunk2 = 4608;                     // one 128-row x 64-column packed chunk
 constexpr int kWStageBytes = (kKS / 64) * kChunk2;
 constexpr int kXStride = kKS * 2 + 16;            // padded token row: conflict-free 16-byte loads
 constexpr uint32_t kLayoutTile = 2;
 
-template <int NT>
+// NT: 8-token MMA tiles per item; MI: 16-row tiles per consumer warp (the
+// item's 128 rows are split over 8 / MI consumer warps).
+template <int NT, int MI = 2>
 struct Cfg {
     static constexpr int kTok = NT * 8;
     static constexpr int kStageBytes = kWStageBytes + kTok * kXStride;
+    static constexpr int kConsumerWarps = 8 / MI;
+    static constexpr int kThreads = (kConsumerWarps + 1) * 32;
 };
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -87,8 +89,9 @@ __device__ __forceinline__ ItemRows load_item_rows(const GemmArgs& a, int64_t b,
     return r;
 }
 
-template <int NT, int STAGES>
-__global__ void __launch_bounds__(kThreads) gemm_decode_kernel(const GemmArgs a) {
+template <int NT, int STAGES, int MI, int MINB>
+__global__ void __launch_bounds__(Cfg<NT, MI>::kThreads, MINB) gemm_decode_kernel(const GemmArgs a) {
+    constexpr int kConsumerWarps = Cfg<NT, MI>::kConsumerWarps;
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int kTok = Cfg<NT>::kTok;
     constexpr int kStage = Cfg<NT>::kStageBytes;
@@ -191,7 +194,7 @@ __global__ void __launch_bounds__(kThreads) gemm_decode_kernel(const GemmArgs a)
     // half c >> 1, and that half's scale.
     const int half = c >> 1;
     const uint32_t code_off = (uint32_t)(half * 2048 + (c & 1) * 8);
-    const uint32_t scale_shift = (uint32_t)(half * 16);
+    const uint32_t scale_sel = half ? 0x3232u : 0x1010u;   // prmt: that half's scale in both halves
     for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
         const int nt = (int)(item % ntiles);
         const int64_t bs = item / ntiles;
@@ -207,9 +210,9 @@ __global__ void __launch_bounds__(kThreads) gemm_decode_kernel(const GemmArgs a)
         for (int j = 0; j < NT; ++j)
             if ((vm >> (8 * j)) & 0xffull) tmask |= 1u << j;
 
-        float acc[2][NT][4];
+        float acc[MI][NT][4];
 #pragma unroll
-        for (int mi = 0; mi < 2; ++mi)
+        for (int mi = 0; mi < MI; ++mi)
 #pragma unroll
             for (int j = 0; j < NT; ++j)
 #pragma unroll
@@ -232,16 +235,15 @@ __global__ void __launch_bounds__(kThreads) gemm_decode_kernel(const GemmArgs a)
                 const uint8_t* cb = sW + ch * kChunk2;
                 // A fragments of the four k16 steps for both 16-row tiles:
                 // av[mi][r][p] = bf16x2 pair p (columns 16c + 2p, +1) of row g (r = 0) or g + 8 (r = 1)
-                uint32_t av[2][2][8];
+                uint32_t av[MI][2][8];
 #pragma unroll
-                for (int mi = 0; mi < 2; ++mi) {
+                for (int mi = 0; mi < MI; ++mi) {
 #pragma unroll
                     for (int r = 0; r < 2; ++r) {
-                        const int row = warp * 32 + mi * 16 + r * 8 + g;
+                        const int row = (warp * MI + mi) * 16 + r * 8 + g;
                         const uint2 w = *reinterpret_cast<const uint2*>(cb + code_off + row * 16);
                         const uint32_t s32 = *reinterpret_cast<const uint32_t*>(cb + 4096 + row * 4);
-                        const uint32_t s16 = (s32 >> scale_shift) & 0xffffu;
-                        const uint32_t sp = s16 | (s16 << 16);
+                        const uint32_t sp = prmt(s32, scale_sel);
                         dequant_row8(w.x, sp, av[mi][r]);
                         dequant_row8(w.y, sp, av[mi][r] + 4);
                     }
@@ -261,7 +263,7 @@ __global__ void __launch_bounds__(kThreads) gemm_decode_kernel(const GemmArgs a)
 #pragma unroll
                     for (int st = 0; st < 4; ++st) {
 #pragma unroll
-                        for (int mi = 0; mi < 2; ++mi) {
+                        for (int mi = 0; mi < MI; ++mi) {
                             const uint32_t af[4] = {av[mi][0][2 * st], av[mi][1][2 * st], av[mi][0][2 * st + 1],
                                                     av[mi][1][2 * st + 1]};
                             mma_bf16_16816(acc[mi][t], af, bv[2 * st], bv[2 * st + 1]);
@@ -289,8 +291,8 @@ __global__ void __launch_bounds__(kThreads) gemm_decode_kernel(const GemmArgs a)
                 p[u] = i < 32 ? lo : hi;
             }
 #pragma unroll
-            for (int mi = 0; mi < 2; ++mi) {
-                const int n0 = nt * kBN + (warp * 2 + mi) * 16 + g;
+            for (int mi = 0; mi < MI; ++mi) {
+                const int n0 = nt * kBN + (warp * MI + mi) * 16 + g;
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                     if (p[u] < 0) continue;
@@ -309,28 +311,28 @@ __global__ void __launch_bounds__(kThreads) gemm_decode_kernel(const GemmArgs a)
     }
 }
 
-template <int NT, int STAGES>
+template <int NT, int STAGES, int MI, int MINB>
 cudaError_t launch_nt(const GemmArgs& a, cudaStream_t stream) {
-    constexpr int smem = STAGES * Cfg<NT>::kStageBytes + 2 * STAGES * 8 + 16;
+    using C = Cfg<NT, MI>;
+    constexpr int smem = STAGES * C::kStageBytes + 2 * STAGES * 8 + 16;
+    auto kern = gemm_decode_kernel<NT, STAGES, MI, MINB>;
     static int configured_dev = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_decode_kernel<NT, STAGES>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         configured_dev = dev;
     }
     int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_decode_kernel<NT, STAGES>, kThreads,
-                                                                  smem);
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::kThreads, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
     const int64_t items_cap = (a.capacity / a.block_m) * ((a.block_m + NT * 8 - 1) / (NT * 8)) * (a.N / kBN);
     int64_t grid = (int64_t)device_info().sm_count * per_sm;
     if (grid > items_cap) grid = items_cap;
     if (grid < 1) grid = 1;
-    gemm_decode_kernel<NT, STAGES><<<(unsigned)grid, kThreads, smem, stream>>>(a);
+    kern<<<(unsigned)grid, C::kThreads, smem, stream>>>(a);
     return cudaGetLastError();
 }
 
@@ -339,11 +341,13 @@ cudaError_t launch_nt(const GemmArgs& a, cudaStream_t stream) {
 cudaError_t launch_gemm_decode(const GemmArgs& a, cudaStream_t stream) {
     // Tokens per item: the smallest of 8/16/32/64 that holds the whole block
     // (larger blocks are split into 64-token sub-blocks, each re-streaming the
-    // weights).  Ring depth: as many stages as let two CTAs share an SM.
-    if (a.block_m <= 8) return launch_nt<1, 9>(a, stream);
-    if (a.block_m <= 16) return launch_nt<2, 8>(a, stream);
-    if (a.block_m <= 32) return launch_nt<4, 6>(a, stream);
-    return launch_nt<8, 4>(a, stream);
+    // weights).  Ring depth: as many stages as let three CTAs share an SM
+    // (more resident warps hide the dequantisation's dependency latencies;
+    // measured faster than two CTAs with deeper rings).
+    if (a.block_m <= 8) return launch_nt<1, 6, 2, 3>(a, stream);
+    if (a.block_m <= 16) return launch_nt<2, 5, 2, 3>(a, stream);
+    if (a.block_m <= 32) return launch_nt<4, 4, 2, 3>(a, stream);
+    return launch_nt<8, 3, 2, 3>(a, stream);
 }
 
 }  // namespace chord
