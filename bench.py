@@ -69,6 +69,29 @@ def gemm_algorithmic(rows_per_expert, N, K):
     return nbytes, flops
 
 
+def arm_config(w, bm, world):
+    """The config object of the JSON line (shared by both arms): the workload,
+    its routing statistics and the regime of its dominant GEMM."""
+    ids, _ = wl.make_routing(w)
+    rpe = routing_stats(ids, w.E)
+    b1, f1_ = gemm_algorithmic(rpe, 2 * w.I, w.H)
+    peaks = load_peaks()
+    # The gate_up GEMM dominates.  It is HBM-bound when its algorithmic FLOP per
+    # byte is below the machine's ridge (measured BF16 peak / measured HBM
+    # bandwidth), tensor-bound above it.
+    ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    regime = "decode" if f1_ / max(b1, 1) < ridge else "prefill"
+    packed = w.E * (2 * w.I * w.H + w.H * w.I) * 9 // 16 + 512
+    cfg = {"workload": w.name, "T": w.T, "E_local": w.E, "E_global": w.E_global, "topk": w.topk, "H": w.H,
+           "I": w.I, "block_m": bm, "regime": regime, "local_pairs": int(rpe.sum()),
+           "tok_e": round(float(rpe.sum()) / w.E, 2), "parallelism": f"ep-replica x{world}",
+           "l2": (f"inputs larger than L2: {packed / 1e6:.0f} MB of packed weights streamed per step vs "
+                  f"{L2_BYTES / 1e6:.0f} MB L2" if packed > L2_BYTES else
+                  f"inputs smaller than L2 and not flushed ({packed / 1e6:.1f} MB of packed weights): "
+                  "not a bandwidth measurement")}
+    return cfg, regime, peaks
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -207,6 +230,12 @@ def run_reference(args, w):
     if rank != 0:
         return
     steps, warmup = args.steps, args.warmup
+    try:
+        import w4a16_int4_mixture_moe_gb300 as chord
+        bm = args.block_m or chord.chord_select_block_m(w.T, w.topk, w.E, w.E_global, 2 * w.I, w.H)
+    except Exception:   # the library is not built: the config names no block size
+        bm = None
+    cfg, _, _ = arm_config(w, bm, int(os.environ.get("WORLD_SIZE", "1")))
     budget = 150.0
     per_step = max(0.5, min(20.0, budget / max(1, steps + warmup)))
     us0, desc, cores, dt, nt = oracle_sample(w, per_step)
@@ -226,7 +255,7 @@ def run_reference(args, w):
     line = {"impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": UNIT, "n_gpus": args.gpus,
             "steps": steps, "warmup": warmup, "ms_per_step": round(el / max(steps, 1) * 1e3, 3),
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic", "config": {"workload": w.name},
+            "data": "synthetic", "config": cfg,
             "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -394,13 +423,7 @@ def main():
     rpe = routing_stats(ids, E)
     b1, f1_ = gemm_algorithmic(rpe, 2 * I, H)
     b2, f2_ = gemm_algorithmic(rpe, H, I)
-    peaks = load_peaks()
-    tok_e = float(rpe.sum()) / E
-    # The gate_up GEMM dominates.  It is HBM-bound when its algorithmic FLOP per
-    # byte is below the machine's ridge (measured BF16 peak / measured HBM
-    # bandwidth), tensor-bound above it.
-    ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    regime = "decode" if f1_ / b1 < ridge else "prefill"
+    cfg, regime, peaks = arm_config(w, bm, world)
     kind = "warp_mma" if chord.chord_select_kernel(bm) == chord.KERNEL_WARP_MMA else "tc"
     kname = KERNEL_NAME[kind] + " (gate_up)"
     if regime == "decode":
@@ -419,11 +442,7 @@ def main():
         "metric": METRIC, "value": round(us_per_call, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "T": T, "E_local": E, "E_global": w.E_global, "topk": topk, "H": H,
-                   "I": I, "block_m": bm, "regime": regime, "local_pairs": int(rpe.sum()),
-                   "tok_e": round(tok_e, 2), "parallelism": f"ep-replica x{world}",
-                   "l2": f"inputs larger than L2: {(p13.numel() + p2.numel()) / 1e6:.0f} MB of packed weights "
-                         f"streamed per step vs {L2_BYTES / 1e6:.0f} MB L2"},
+        "config": cfg,
         "gemm_us": {"gate_up": round(g1 * 1e3, 2), "down": round(g2 * 1e3, 2)},
         "gemm_achieved": {
             "gate_up_GBps": round(b1 / (g1 * 1e-3) / 1e9, 1), "down_GBps": round(b2 / (g2 * 1e-3) / 1e9, 1),
