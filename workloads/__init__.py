@@ -83,11 +83,12 @@ def _softmax_rows(z: np.ndarray) -> np.ndarray:
     return e / e.sum(axis=1, keepdims=True)
 
 
-def make_routing(w: Workload):
+def make_routing(w: Workload, rank: int = 0):
     """Return (topk_ids int32 [T, topk], topk_w float32 [T, topk]).
 
-    ``topk_ids`` holds local expert ids in [0, E) and -1 for pairs routed to
-    experts outside this GPU's share (ids >= E).
+    Expert-parallel share ``rank`` holds global experts [rank*E, rank*E + E);
+    ``topk_ids`` holds their local ids in [0, E) and -1 for pairs routed to
+    experts outside this share.  Every share sees the same global routing.
     """
     st = _streams(w.seed)
     ri, rw = st[_S_ROUTE_IDS], st[_S_ROUTE_W]
@@ -114,7 +115,8 @@ def make_routing(w: Workload):
     else:
         raise ValueError(f"unknown routing {w.routing!r}")
     ids = ids.astype(np.int32)
-    ids = np.where(ids < w.E, ids, -1).astype(np.int32)
+    lo = rank * w.E
+    ids = np.where((ids >= lo) & (ids < lo + w.E), ids - lo, -1).astype(np.int32)
     return np.ascontiguousarray(ids), np.ascontiguousarray(wts)
 
 
