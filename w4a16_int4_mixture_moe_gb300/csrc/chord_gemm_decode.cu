@@ -61,32 +61,144 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
 }
 
 // Per-item routing facts, computed identically by the producer and the
-// consumers from the same global data.
+// consumers from the same global data.  At most 32 token slots per item.
 struct ItemRows {
-    int32_t id[2];    // pair id of token slots lane and lane + 32 (or -1)
-    uint32_t vmask[2];
+    int32_t id;       // pair id of token slot `lane` (or -1)
+    uint32_t vmask;   // slots holding a valid pair id
 };
 
 template <int NT>
 __device__ __forceinline__ ItemRows load_item_rows(const GemmArgs& a, int64_t b, int sub, int lane, int* err) {
+    static_assert(Cfg<NT>::kTok <= 32, "one token slot per lane");
     ItemRows r;
+    int32_t id = -1;
+    bool ok = false;
+    const int slot_in_block = sub * Cfg<NT>::kTok + lane;
+    if (lane < Cfg<NT>::kTok && slot_in_block < a.block_m) {
+        id = a.sorted_ids[b * a.block_m + slot_in_block];
+        if (id != (int32_t)a.num_pairs) {
+            ok = id >= 0 && (int64_t)id < a.num_pairs && (int64_t)(id / a.a_row_divisor) < a.a_rows;
+            if (!ok) set_error(err, CHORD_DEV_BAD_ROW);
+        }
+    }
+    r.id = ok ? id : -1;
+    r.vmask = __ballot_sync(0xffffffffu, ok);
+    return r;
+}
+
+// One 64-column chunk: dequantise the warp's MI 16-row tiles (lane (g, c):
+// rows g and g + 8, columns [16c, 16c + 16)) and accumulate them against NV
+// 8-token tiles.  `row0` = the warp's first row + g; `xa` = shared address of
+// token g's columns 16c.. of this chunk.
+template <int MI, int NV>
+__device__ __forceinline__ void chunk_mma(const uint8_t* cb, int row0, uint32_t code_off, uint32_t scale_sel,
+                                          uint32_t xa, float (&acc)[MI][NV][4]) {
+    // av[mi][r][p] = bf16x2 pair p (columns 16c + 2p, +1) of row g (r = 0) or g + 8 (r = 1)
+    uint32_t av[MI][2][8];
 #pragma unroll
-    for (int s = 0; s < 2; ++s) {
-        const int i = lane + 32 * s;
-        int32_t id = -1;
-        bool ok = false;
-        const int slot_in_block = sub * Cfg<NT>::kTok + i;
-        if (i < Cfg<NT>::kTok && slot_in_block < a.block_m) {
-            id = a.sorted_ids[b * a.block_m + slot_in_block];
-            if (id != (int32_t)a.num_pairs) {
-                ok = id >= 0 && (int64_t)id < a.num_pairs && (int64_t)(id / a.a_row_divisor) < a.a_rows;
-                if (!ok) set_error(err, CHORD_DEV_BAD_ROW);
+    for (int mi = 0; mi < MI; ++mi) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int row = row0 + mi * 16 + r * 8;
+            const uint2 w = *reinterpret_cast<const uint2*>(cb + code_off + row * 16);
+            const uint32_t sp = prmt(*reinterpret_cast<const uint32_t*>(cb + 4096 + row * 4), scale_sel);
+            dequant_row8(w.x, sp, av[mi][r]);
+            dequant_row8(w.y, sp, av[mi][r] + 4);
+        }
+    }
+    // B fragments of token 8t + g, the same 16 columns
+    uint32_t bv[NV][8];
+#pragma unroll
+    for (int t = 0; t < NV; ++t) {
+        const uint32_t x = xa + (uint32_t)(t * 8 * kXStride);
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(bv[t][0]), "=r"(bv[t][1]), "=r"(bv[t][2]), "=r"(bv[t][3])
+                     : "r"(x));
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(bv[t][4]), "=r"(bv[t][5]), "=r"(bv[t][6]), "=r"(bv[t][7])
+                     : "r"(x + 16));
+    }
+    // k16 step st takes columns 16c + 4st .. + 3 of every lane, for A and B alike
+#pragma unroll
+    for (int st = 0; st < 4; ++st) {
+#pragma unroll
+        for (int t = 0; t < NV; ++t) {
+#pragma unroll
+            for (int mi = 0; mi < MI; ++mi) {
+                const uint32_t af[4] = {av[mi][0][2 * st], av[mi][1][2 * st], av[mi][0][2 * st + 1],
+                                        av[mi][1][2 * st + 1]};
+                mma_bf16_16816(acc[mi][t], af, bv[t][2 * st], bv[t][2 * st + 1]);
             }
         }
-        r.id[s] = ok ? id : -1;
-        r.vmask[s] = __ballot_sync(0xffffffffu, ok);
     }
-    return r;
+}
+
+// Consumer side of one item whose valid token slots lie in its first NV
+// 8-token tiles (align fills a block's slots from the front): the K loop over
+// the stage ring, then the epilogue.  Returns false when a wait gave up.
+template <int NT, int STAGES, int MI, int NV>
+__device__ __forceinline__ bool consume_item(const GemmArgs& a, uint8_t* smem, uint64_t* full, uint64_t* empty,
+                                          volatile int* flags, int64_t& stage, int warp, int lane, int nt,
+                                          int32_t my_id) {
+    constexpr int kStage = Cfg<NT>::kStageBytes;
+    const int g = lane >> 2, c = lane & 3;
+    // lane (g, c) reads the two code words (c & 1) * 2, +1 of the 32-column
+    // half c >> 1 of each of its rows, and that half's scale
+    const uint32_t code_off = (uint32_t)((c >> 1) * 2048 + (c & 1) * 8);
+    const uint32_t scale_sel = (c >> 1) ? 0x3232u : 0x1010u;   // prmt: that half's scale in both halves
+    const int row0 = warp * MI * 16 + g;
+    const uint32_t x_lane = (uint32_t)(g * kXStride + 32 * c);
+
+    float acc[MI][NV][4];
+#pragma unroll
+    for (int mi = 0; mi < MI; ++mi)
+#pragma unroll
+        for (int t = 0; t < NV; ++t)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[mi][t][q] = 0.0f;
+
+    const int kstages = (a.K + kKS - 1) / kKS;
+    for (int ks = 0; ks < kstages; ++ks, ++stage) {
+        const int slot = (int)(stage % STAGES);
+        const uint32_t par = (uint32_t)((stage / STAGES) & 1);
+        if (!mbar_wait(&full[slot], par) || flags[1]) {
+            if (lane == 0) set_error(a.err, CHORD_DEV_TIMEOUT);
+            flags[1] = 1;
+            return false;
+        }
+        const uint8_t* sW = smem + slot * kStage;
+        const uint32_t xa = smem_u32(sW + kWStageBytes) + x_lane;
+        chunk_mma<MI, NV>(sW, row0, code_off, scale_sel, xa, acc);
+        if (a.K - ks * kKS >= 128) chunk_mma<MI, NV>(sW + kChunk2, row0, code_off, scale_sel, xa + 128, acc);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+    }
+
+    // ---- epilogue: C[p, n] = acc (bf16-rounded or FP32) for valid token columns
+#pragma unroll
+    for (int t = 0; t < NV; ++t) {
+        int32_t p[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) p[u] = __shfl_sync(0xffffffffu, my_id, 8 * t + 2 * c + u);
+#pragma unroll
+        for (int mi = 0; mi < MI; ++mi) {
+            const int n0 = nt * kBN + (warp * MI + mi) * 16 + g;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                if (p[u] < 0) continue;
+                if (a.out_f32) {
+                    float* crow = static_cast<float*>(a.C) + (int64_t)p[u] * a.N;
+                    crow[n0] = acc[mi][t][u];
+                    crow[n0 + 8] = acc[mi][t][2 + u];
+                } else {
+                    __nv_bfloat16* crow = static_cast<__nv_bfloat16*>(a.C) + (int64_t)p[u] * a.N;
+                    crow[n0] = __float2bfloat16_rn(acc[mi][t][u]);
+                    crow[n0 + 8] = __float2bfloat16_rn(acc[mi][t][2 + u]);
+                }
+            }
+        }
+    }
+    return true;
 }
 
 template <int NT, int STAGES, int MI, int MINB>
@@ -143,13 +255,10 @@ __global__ void __launch_bounds__(Cfg<NT, MI>::kThreads, MINB) gemm_decode_kerne
                 continue;
             }
             const ItemRows rows = load_item_rows<NT>(a, b, sub, lane, nullptr);
-            const int nvalid = __popc(rows.vmask[0]) + __popc(rows.vmask[1]);
+            const int nvalid = __popc(rows.vmask);
             if (nvalid == 0) continue;
             const uint8_t* wexp = wbase + (uint64_t)e * expert_bytes;
-            const uint16_t* arow[2];
-#pragma unroll
-            for (int s = 0; s < 2; ++s)
-                arow[s] = rows.id[s] >= 0 ? a.A + (int64_t)(rows.id[s] / a.a_row_divisor) * a.K : nullptr;
+            const uint16_t* arow = rows.id >= 0 ? a.A + (int64_t)(rows.id / a.a_row_divisor) * a.K : nullptr;
             for (int ks = 0; ks < kstages; ++ks) {
                 const int slot = (int)(stage % STAGES);
                 const uint32_t par = (uint32_t)((stage / STAGES) & 1);
@@ -170,9 +279,7 @@ __global__ void __launch_bounds__(Cfg<NT, MI>::kThreads, MINB) gemm_decode_kerne
                     bulk_g2s_hint(sW, src, (uint32_t)(nchunk * kChunk2), &full[slot], pol);
                 }
                 __syncwarp();
-#pragma unroll
-                for (int s = 0; s < 2; ++s)
-                    if (arow[s]) bulk_g2s(sX + (lane + 32 * s) * kXStride, arow[s] + ks * kKS, xbytes, &full[slot]);
+                if (arow) bulk_g2s(sX + lane * kXStride, arow + ks * kKS, xbytes, &full[slot]);
                 ++stage;
             }
         }
@@ -187,14 +294,7 @@ __global__ void __launch_bounds__(Cfg<NT, MI>::kThreads, MINB) gemm_decode_kerne
     }
 
     // -------------------------------------------------------------- consumers
-    const int g = lane >> 2, c = lane & 3;
     int64_t stage = 0;
-    // Lane (g, c): rows g and g + 8 of each 16-row tile, chunk columns
-    // [16c, 16c + 16): the two code words (c & 1) * 2 and + 1 of the 32-column
-    // half c >> 1, and that half's scale.
-    const int half = c >> 1;
-    const uint32_t code_off = (uint32_t)(half * 2048 + (c & 1) * 8);
-    const uint32_t scale_sel = half ? 0x3232u : 0x1010u;   // prmt: that half's scale in both halves
     for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
         const int nt = (int)(item % ntiles);
         const int64_t bs = item / ntiles;
@@ -203,111 +303,21 @@ __global__ void __launch_bounds__(Cfg<NT, MI>::kThreads, MINB) gemm_decode_kerne
         const int e = a.expert_ids[b];
         if (e < 0 || e >= a.E) continue;
         const ItemRows rows = load_item_rows<NT>(a, b, sub, lane, a.err);
-        const uint64_t vm = (uint64_t)rows.vmask[0] | ((uint64_t)rows.vmask[1] << 32);
-        if (vm == 0) continue;
-        uint32_t tmask = 0;  // token tiles with at least one valid row
-#pragma unroll
-        for (int j = 0; j < NT; ++j)
-            if ((vm >> (8 * j)) & 0xffull) tmask |= 1u << j;
-
-        float acc[MI][NT][4];
-#pragma unroll
-        for (int mi = 0; mi < MI; ++mi)
-#pragma unroll
-            for (int j = 0; j < NT; ++j)
-#pragma unroll
-                for (int q = 0; q < 4; ++q) acc[mi][j][q] = 0.0f;
-
-        bool aborted = false;
-        for (int ks = 0; ks < kstages; ++ks) {
-            const int slot = (int)(stage % STAGES);
-            const uint32_t par = (uint32_t)((stage / STAGES) & 1);
-            if (!mbar_wait(&full[slot], par) || flags[1]) {
-                if (lane == 0) set_error(a.err, CHORD_DEV_TIMEOUT);
-                flags[1] = 1;
-                aborted = true;
-                break;
-            }
-            const int nchunk = min(2, (a.K - ks * kKS) / 64);
-            const uint8_t* sW = smem + slot * kStage;
-            const uint32_t sX = smem_u32(sW + kWStageBytes);
-            for (int ch = 0; ch < nchunk; ++ch) {
-                const uint8_t* cb = sW + ch * kChunk2;
-                // A fragments of the four k16 steps for both 16-row tiles:
-                // av[mi][r][p] = bf16x2 pair p (columns 16c + 2p, +1) of row g (r = 0) or g + 8 (r = 1)
-                uint32_t av[MI][2][8];
-#pragma unroll
-                for (int mi = 0; mi < MI; ++mi) {
-#pragma unroll
-                    for (int r = 0; r < 2; ++r) {
-                        const int row = (warp * MI + mi) * 16 + r * 8 + g;
-                        const uint2 w = *reinterpret_cast<const uint2*>(cb + code_off + row * 16);
-                        const uint32_t s32 = *reinterpret_cast<const uint32_t*>(cb + 4096 + row * 4);
-                        const uint32_t sp = prmt(s32, scale_sel);
-                        dequant_row8(w.x, sp, av[mi][r]);
-                        dequant_row8(w.y, sp, av[mi][r] + 4);
-                    }
-                }
-#pragma unroll
-                for (int t = 0; t < NT; ++t) {
-                    if (!(tmask & (1u << t))) continue;
-                    // B fragments: token 8t + g, the same 16 columns
-                    const uint32_t xa = sX + (uint32_t)((8 * t + g) * kXStride + (ch * 64 + 16 * c) * 2);
-                    uint32_t bv[8];
-                    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                                 : "=r"(bv[0]), "=r"(bv[1]), "=r"(bv[2]), "=r"(bv[3])
-                                 : "r"(xa));
-                    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                                 : "=r"(bv[4]), "=r"(bv[5]), "=r"(bv[6]), "=r"(bv[7])
-                                 : "r"(xa + 16));
-#pragma unroll
-                    for (int st = 0; st < 4; ++st) {
-#pragma unroll
-                        for (int mi = 0; mi < MI; ++mi) {
-                            const uint32_t af[4] = {av[mi][0][2 * st], av[mi][1][2 * st], av[mi][0][2 * st + 1],
-                                                    av[mi][1][2 * st + 1]};
-                            mma_bf16_16816(acc[mi][t], af, bv[2 * st], bv[2 * st + 1]);
-                        }
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);
-            ++stage;
-        }
-        if (aborted) return;
-
-        // ---- epilogue: C[p, n] = acc (bf16-rounded or FP32) for valid token columns
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            if (!(tmask & (1u << t))) continue;
-            const int i0 = 8 * t + 2 * c;  // token slots i0, i0 + 1
-            int32_t p[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int i = i0 + u;
-                const int32_t lo = __shfl_sync(0xffffffffu, rows.id[0], i & 31);
-                const int32_t hi = __shfl_sync(0xffffffffu, rows.id[1], i & 31);
-                p[u] = i < 32 ? lo : hi;
-            }
-#pragma unroll
-            for (int mi = 0; mi < MI; ++mi) {
-                const int n0 = nt * kBN + (warp * MI + mi) * 16 + g;
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    if (p[u] < 0) continue;
-                    if (a.out_f32) {
-                        float* crow = static_cast<float*>(a.C) + (int64_t)p[u] * a.N;
-                        crow[n0] = acc[mi][t][u];
-                        crow[n0 + 8] = acc[mi][t][2 + u];
-                    } else {
-                        __nv_bfloat16* crow = static_cast<__nv_bfloat16*>(a.C) + (int64_t)p[u] * a.N;
-                        crow[n0] = __float2bfloat16_rn(acc[mi][t][u]);
-                        crow[n0 + 8] = __float2bfloat16_rn(acc[mi][t][2 + u]);
-                    }
-                }
-            }
-        }
+        if (rows.vmask == 0) continue;
+        const int nv = (32 - __clz(rows.vmask) + 7) / 8;   // 8-token tiles up to the last valid slot
+        bool ok;
+        if (nv <= 1)
+            ok = consume_item<NT, STAGES, MI, 1>(a, smem, full, empty, flags, stage, warp, lane, nt, rows.id);
+        else if (nv == 2 || NT == 2)
+            ok = consume_item<NT, STAGES, MI, (NT >= 2 ? 2 : 1)>(a, smem, full, empty, flags, stage, warp, lane,
+                                                                 nt, rows.id);
+        else if (nv == 3)
+            ok = consume_item<NT, STAGES, MI, (NT >= 4 ? 3 : 1)>(a, smem, full, empty, flags, stage, warp, lane,
+                                                                 nt, rows.id);
+        else
+            ok = consume_item<NT, STAGES, MI, (NT >= 4 ? 4 : 1)>(a, smem, full, empty, flags, stage, warp, lane,
+                                                                 nt, rows.id);
+        if (!ok) return;
     }
 }
 
@@ -339,15 +349,14 @@ cudaError_t launch_nt(const GemmArgs& a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_gemm_decode(const GemmArgs& a, cudaStream_t stream) {
-    // Tokens per item: the smallest of 8/16/32/64 that holds the whole block
-    // (larger blocks are split into 64-token sub-blocks, each re-streaming the
-    // weights).  Ring depth: as many stages as let three CTAs share an SM
+    // Tokens per item: the smallest of 8/16/32 that holds the whole block
+    // (larger blocks are split into 32-token sub-blocks, each re-streaming the
+    // weights; the tcgen05 kernel serves those blocks by default).  Ring depth: as many stages as let three CTAs share an SM
     // (more resident warps hide the dequantisation's dependency latencies;
     // measured faster than two CTAs with deeper rings).
     if (a.block_m <= 8) return launch_nt<1, 6, 2, 3>(a, stream);
     if (a.block_m <= 16) return launch_nt<2, 5, 2, 3>(a, stream);
-    if (a.block_m <= 32) return launch_nt<4, 4, 2, 3>(a, stream);
-    return launch_nt<8, 3, 2, 3>(a, stream);
+    return launch_nt<4, 4, 2, 3>(a, stream);
 }
 
 }  // namespace chord
