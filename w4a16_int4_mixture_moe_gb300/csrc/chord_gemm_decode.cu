@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(Cfg<NT, MI>::kThreads, MINB) gemm_decode_kerne
         flags[0] = ok ? 0 : 1;
         flags[1] = 0;
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], 33);        // the weight copy's expect_tx + one cp.async arrival per producer lane
             mbar_init(&empty[s], kConsumerWarps);
         }
         fence_barrier_init();
@@ -258,7 +258,11 @@ __global__ void __launch_bounds__(Cfg<NT, MI>::kThreads, MINB) gemm_decode_kerne
             const int nvalid = __popc(rows.vmask);
             if (nvalid == 0) continue;
             const uint8_t* wexp = wbase + (uint64_t)e * expert_bytes;
+            // Activation rows: lanes 0-15 copy the 16-byte pieces of token slot
+            // 2i, lanes 16-31 those of slot 2i + 1 (valid slots are a prefix).
             const uint16_t* arow = rows.id >= 0 ? a.A + (int64_t)(rows.id / a.a_row_divisor) * a.K : nullptr;
+            const int npairs = (32 - __clz(rows.vmask) + 1) / 2;
+            const int half_lane = lane >> 4, piece = lane & 15;
             for (int ks = 0; ks < kstages; ++ks) {
                 const int slot = (int)(stage % STAGES);
                 const uint32_t par = (uint32_t)((stage / STAGES) & 1);
@@ -269,21 +273,27 @@ __global__ void __launch_bounds__(Cfg<NT, MI>::kThreads, MINB) gemm_decode_kerne
                     break;
                 }
                 const int nchunk = min(2, (a.K - ks * kKS) / 64);
-                const uint32_t xbytes = (uint32_t)nchunk * 64u * 2u;
                 uint8_t* sW = smem + slot * kStage;
-                uint8_t* sX = sW + kWStageBytes;
+                const uint32_t sX = smem_u32(sW + kWStageBytes);
                 if (lane == 0) {
                     // chunks (nt, kc) of one expert are contiguous along kc
-                    mbar_arrive_expect_tx(&full[slot], (uint32_t)(nchunk * kChunk2) + nvalid * xbytes);
+                    mbar_arrive_expect_tx(&full[slot], (uint32_t)(nchunk * kChunk2));
                     const uint8_t* src = wexp + ((uint64_t)nt * kchunks + (uint64_t)(2 * ks)) * kChunk2;
                     bulk_g2s_hint(sW, src, (uint32_t)(nchunk * kChunk2), &full[slot], pol);
                 }
-                __syncwarp();
-                if (arow) bulk_g2s(sX + lane * kXStride, arow + ks * kKS, xbytes, &full[slot]);
+                const bool my_piece = piece < nchunk * 8;   // a one-chunk stage has 8 pieces per row
+                for (int i = 0; i < npairs; ++i) {
+                    const int j = 2 * i + half_lane;
+                    const uint16_t* r = reinterpret_cast<const uint16_t*>(
+                        __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(arow), j));
+                    if (r && my_piece) cp_async16(sX + (uint32_t)(j * kXStride + piece * 16), r + ks * kKS + piece * 8);
+                }
+                cp_async_arrive_noinc(&full[slot]);
                 ++stage;
             }
         }
         // Leave only after every copy this warp issued has landed.
+        cp_async_wait<0>();
         if (lane == 0) {
             for (int s = 0; s < STAGES && s < stage; ++s) {
                 const int64_t last = s + ((stage - 1 - s) / STAGES) * STAGES;
