@@ -226,6 +226,7 @@ chord_status chord_w4a16_moe_gemm(const void* A, int64_t a_rows, int a_row_divis
     g.capacity = capacity;
     g.block_m = block_m;
     g.num_pairs = num_pairs;
+    g.id_limit = a_rows * (int64_t)a_row_divisor < num_pairs ? a_rows * (int64_t)a_row_divisor : num_pairs;
     g.C = C;
     g.out_f32 = o.out_dtype == CHORD_DTYPE_F32 ? 1 : 0;
     g.err = di.err;

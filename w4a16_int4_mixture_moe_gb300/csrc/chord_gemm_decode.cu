@@ -77,7 +77,7 @@ __device__ __forceinline__ ItemRows load_item_rows(const GemmArgs& a, int64_t b,
     if (lane < Cfg<NT>::kTok && slot_in_block < a.block_m) {
         id = a.sorted_ids[b * a.block_m + slot_in_block];
         if (id != (int32_t)a.num_pairs) {
-            ok = id >= 0 && (int64_t)id < a.num_pairs && (int64_t)(id / a.a_row_divisor) < a.a_rows;
+            ok = id >= 0 && (int64_t)id < a.id_limit;
             if (!ok) set_error(err, CHORD_DEV_BAD_ROW);
         }
     }
@@ -260,7 +260,8 @@ __global__ void __launch_bounds__(Cfg<NT, MI>::kThreads, MINB) gemm_decode_kerne
             const uint8_t* wexp = wbase + (uint64_t)e * expert_bytes;
             // Activation rows: lanes 0-15 copy the 16-byte pieces of token slot
             // 2i, lanes 16-31 those of slot 2i + 1 (valid slots are a prefix).
-            const uint16_t* arow = rows.id >= 0 ? a.A + (int64_t)(rows.id / a.a_row_divisor) * a.K : nullptr;
+            const int32_t arow_i = a.a_row_divisor == 1 ? rows.id : rows.id / a.a_row_divisor;
+            const uint16_t* arow = rows.id >= 0 ? a.A + (int64_t)arow_i * a.K : nullptr;
             const int npairs = (32 - __clz(rows.vmask) + 1) / 2;
             const int half_lane = lane >> 4, piece = lane & 15;
             for (int ks = 0; ks < kstages; ++ks) {

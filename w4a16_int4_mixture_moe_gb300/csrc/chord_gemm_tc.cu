@@ -168,23 +168,31 @@ struct ItemInfo {
 };
 
 __device__ __forceinline__ bool row_valid(const GemmArgs& a, int32_t id) {
-    return id != (int32_t)a.num_pairs && id >= 0 && (int64_t)id < a.num_pairs &&
-           (int64_t)(id / a.a_row_divisor) < a.a_rows;
+    return id >= 0 && (int64_t)id < a.id_limit;   // the sentinel num_pairs is never below id_limit
 }
 
 __device__ __forceinline__ ItemInfo item_info(const GemmArgs& a, int64_t b, int lane, bool report) {
+    // All loads first (a block holds at most 256 rows: 8 per lane), so the
+    // item's routing costs one memory latency, not one per row group.
     ItemInfo r;
     r.e = a.expert_ids[b];
+    int32_t ids[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int i = lane + 32 * k;
+        ids[k] = i < a.block_m ? a.sorted_ids[b * a.block_m + i] : (int32_t)a.num_pairs;
+    }
     r.n_mma = 0;
     if (r.e < 0 || r.e >= a.E) {
         if (report && lane == 0) set_error(a.err, CHORD_DEV_BAD_EXPERT);
         return r;
     }
     int last = -1;
-    for (int i = lane; i < a.block_m; i += 32) {
-        const int32_t id = a.sorted_ids[b * a.block_m + i];
-        const bool ok = row_valid(a, id);
-        if (report && !ok && id != (int32_t)a.num_pairs) set_error(a.err, CHORD_DEV_BAD_ROW);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int i = lane + 32 * k;
+        const bool ok = row_valid(a, ids[k]);
+        if (report && !ok && ids[k] != (int32_t)a.num_pairs) set_error(a.err, CHORD_DEV_BAD_ROW);
         if (ok) last = i;
     }
     last = __reduce_max_sync(0xffffffffu, last + 1);
@@ -397,7 +405,7 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
                 arow[r] = -1;
                 if (j < inf.n_mma && j < a.block_m) {
                     const int32_t id = a.sorted_ids[b * a.block_m + j];
-                    if (row_valid(a, id)) arow[r] = id / a.a_row_divisor;
+                    if (row_valid(a, id)) arow[r] = a.a_row_divisor == 1 ? id : id / a.a_row_divisor;
                 }
             }
             for (int ks = 0; ks < kstages; ++ks, br.next(NSB)) {
@@ -485,7 +493,20 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
                 if (lane == 0) mbar_arrive(&a_full[ar.slot]);
             }
             if (!ok) break;
-            // ---- epilogue: accumulator column j is token j of the block
+            // ---- epilogue: accumulator column j is token j of the block.
+            // Pair ids first, before the accumulator is ready: lane l holds the
+            // id of token wg*16 + 32*(2k + l/16) + l%16 in pre[k].
+            int32_t pre[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int j = wg * 16 + 32 * (2 * k + (lane >> 4)) + (lane & 15);
+                int32_t id = -1;
+                if (j < inf.n_mma && j < a.block_m) {
+                    id = a.sorted_ids[b * a.block_m + j];
+                    if (!row_valid(a, id)) id = -1;
+                }
+                pre[k] = id;
+            }
             if (!wait_or_abort(acc_full, (uint32_t)(nitem & 1), &flags[1], a.err)) {
                 ok = false;
                 break;
@@ -493,7 +514,10 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
             tc_fence_after();
             const int n_out = nt * kTileRows + row;
             const int parts = kstages < NI ? kstages : NI;   // issuers that hold a share of this item
-            for (int j0 = wg * 16; j0 < inf.n_mma; j0 += 32) {
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+                const int j0 = wg * 16 + 32 * it;
+                if (j0 >= inf.n_mma) break;
                 uint32_t v[16];
                 tmem_ld16(acc_tmem + lane_base + j0, v);
                 for (int pi = 1; pi < parts; ++pi) {
@@ -504,16 +528,10 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
 #pragma unroll
                     for (int u = 0; u < 16; ++u) v[u] = __float_as_uint(__uint_as_float(v[u]) + __uint_as_float(w2[u]));
                 }
-                // pair ids of tokens j0..j0+15: one load per lane, then shuffles
-                int32_t my_id = -1;
-                if (lane < 16 && j0 + lane < a.block_m) {
-                    const int32_t id = a.sorted_ids[b * a.block_m + j0 + lane];
-                    if (row_valid(a, id)) my_id = id;
-                }
                 tc_wait_ld();
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
-                    const int32_t id = __shfl_sync(0xffffffffu, my_id, u);
+                    const int32_t id = __shfl_sync(0xffffffffu, pre[it >> 1], u + 16 * (it & 1));
                     if (id < 0) continue;
                     const float val = __uint_as_float(v[u]);
                     if (a.out_f32)

@@ -43,13 +43,14 @@ struct GemmArgs {
     int64_t capacity;
     int block_m;
     int64_t num_pairs;
+    int64_t id_limit;   // pair ids below this are valid rows: min(num_pairs, a_rows * a_row_divisor)
     void* C;        // bf16 [num_pairs, N], or float when out_f32
     int out_f32;
     int* err;
 };
 
-// Warp-MMA kernel (packed layout 1): tokens of a block in the N dimension of
-// mma.sync m16n8k16, INT4 streamed through a bulk-copy pipeline.
+// Warp-MMA kernel (decode regime, packed layout 2): tokens of a block in the N
+// dimension of mma.sync m16n8k16, INT4 streamed through a bulk-copy pipeline.
 // block_m % 8 == 0.
 cudaError_t launch_gemm_decode(const GemmArgs& a, cudaStream_t stream);
 
