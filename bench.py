@@ -435,7 +435,7 @@ def main():
     b1, f1_ = gemm_algorithmic(rpe, 2 * I, H)
     b2, f2_ = gemm_algorithmic(rpe, H, I)
     cfg, regime, peaks = arm_config(w, bm, world)
-    kind = "warp_mma" if chord.chord_select_kernel(bm) == chord.KERNEL_WARP_MMA else "tc"
+    kind = "warp_mma" if chord.chord_select_kernel(bm, 2 * I, H) == chord.KERNEL_WARP_MMA else "tc"
     kname = KERNEL_NAME[kind] + " (gate_up)"
     if regime == "decode":
         ach = b1 / (g1 * 1e-3) / 1e9

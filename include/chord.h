@@ -71,9 +71,8 @@ typedef enum chord_status {
 /* GEMM kernel family, picked from rows per expert (the article's two
  * regimes, section "Indexed kernels"): both take the block's tokens as the
  * MMA's N side (the operand swap of the article's decode profile) and read the
- * same packed layout.  CHORD_KERNEL_AUTO picks by block size
- * (chord_select_kernel): the warp-level kernel for decode blocks of at most 32
- * rows, the tcgen05 kernel above. */
+ * same packed layout.  CHORD_KERNEL_AUTO picks by block size and K
+ * (chord_select_kernel). */
 typedef enum chord_kernel {
     CHORD_KERNEL_AUTO = 0,      /* chord_select_kernel(block_m) */
     CHORD_KERNEL_TCGEN05 = 1,   /* tcgen05.mma, dequantised A in tensor memory, FP32 accumulators
@@ -204,11 +203,13 @@ chord_status chord_moe_align_noalloc(const int32_t *topk_ids, int T, int topk, i
  * tok_e a prefill block.  Always returns a valid block_m. */
 int chord_select_block_m(int T, int topk, int E_local, int E_global, int N, int K);
 
-/* The kernel CHORD_KERNEL_AUTO runs for blocks of block_m rows:
- * CHORD_KERNEL_WARP_MMA for block_m <= 32, else CHORD_KERNEL_TCGEN05.  The
- * environment variable CHORD_KERNEL (1 or 2), when set, overrides the choice
- * for every call whose opts leave the kernel at AUTO. */
-int chord_select_kernel(int block_m);
+/* The kernel CHORD_KERNEL_AUTO runs for a GEMM of blocks of block_m rows and
+ * an [N, K] weight: CHORD_KERNEL_WARP_MMA for decode blocks (block_m <= 32)
+ * and for short K (K <= 512 with block_m <= 128, where the tcgen05 kernel's
+ * fixed cost per block and N tile dominates), else CHORD_KERNEL_TCGEN05.
+ * The environment variable CHORD_KERNEL (1 or 2), when set, overrides the
+ * choice for every call whose opts leave the kernel at AUTO. */
+int chord_select_kernel(int block_m, int N, int K);
 
 /* ------------------------------------------------------------------- GEMM */
 

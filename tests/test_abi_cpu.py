@@ -78,22 +78,30 @@ def test_select_block_m(lib):
 
 
 def test_select_kernel_by_regime(lib, monkeypatch):
-    """Decode blocks (at most 32 rows) go to the warp-level kernel, larger ones
-    to the tcgen05 kernel; the decode workload's block and the prefill
-    workload's block land on different sides."""
+    """Decode blocks (at most 32 rows) and short-K GEMMs with blocks up to 128
+    rows go to the warp-level kernel, the rest to the tcgen05 kernel; the
+    decode workload's block and the prefill workload's block land on
+    different sides."""
     monkeypatch.delenv("CHORD_KERNEL", raising=False)
+    W, T = chord.KERNEL_WARP_MMA, chord.KERNEL_TCGEN05
     for bm in (8, 16, 24, 32):
-        assert chord.chord_select_kernel(bm) == chord.KERNEL_WARP_MMA
+        assert chord.chord_select_kernel(bm, 4096, 7168) == W
     for bm in (40, 64, 128, 256):
-        assert chord.chord_select_kernel(bm) == chord.KERNEL_TCGEN05
-    assert chord.chord_select_kernel(chord.chord_select_block_m(512, 8, 48, 384, 4096, 7168)) == chord.KERNEL_WARP_MMA
-    assert chord.chord_select_kernel(chord.chord_select_block_m(8192, 8, 48, 384, 4096, 7168)) == chord.KERNEL_TCGEN05
+        assert chord.chord_select_kernel(bm, 4096, 7168) == T
+    assert chord.chord_select_kernel(48, 7168, 256) == W       # TP8 down, T = 1024
+    assert chord.chord_select_kernel(128, 7168, 256) == W      # TP8 down, T = 4096
+    assert chord.chord_select_kernel(256, 7168, 256) == T
+    assert chord.chord_select_kernel(64, 7168, 1024) == T
+    bm_dec = chord.chord_select_block_m(512, 8, 48, 384, 4096, 7168)
+    bm_pre = chord.chord_select_block_m(8192, 8, 48, 384, 4096, 7168)
+    assert chord.chord_select_kernel(bm_dec, 4096, 7168) == W and chord.chord_select_kernel(bm_dec, 7168, 2048) == W
+    assert chord.chord_select_kernel(bm_pre, 4096, 7168) == T and chord.chord_select_kernel(bm_pre, 7168, 2048) == T
     monkeypatch.setenv("CHORD_KERNEL", "1")
-    assert chord.chord_select_kernel(8) == chord.KERNEL_TCGEN05
+    assert chord.chord_select_kernel(8, 4096, 7168) == T
     monkeypatch.setenv("CHORD_KERNEL", "2")
-    assert chord.chord_select_kernel(256) == chord.KERNEL_WARP_MMA
+    assert chord.chord_select_kernel(256, 4096, 7168) == W
     monkeypatch.setenv("CHORD_KERNEL", "7")        # not a kernel: ignored
-    assert chord.chord_select_kernel(256) == chord.KERNEL_TCGEN05
+    assert chord.chord_select_kernel(256, 4096, 7168) == T
 
 
 def test_layer_workspace_formula(lib):

@@ -59,7 +59,7 @@ _SIGS = {
     "chord_moe_align": (_int, [_vp, _int, _int, _int, _int, _vp, _vp, _vp, _i64, _vp, _sz, _OPTS, _vp]),
     "chord_moe_align_noalloc": (_int, [_vp, _int, _int, _int, _int, _vp, _vp, _vp, _i64, _OPTS, _vp]),
     "chord_select_block_m": (_int, [_int, _int, _int, _int, _int, _int]),
-    "chord_select_kernel": (_int, [_int]),
+    "chord_select_kernel": (_int, [_int, _int, _int]),
     "chord_gemm_workspace_bytes": (_sz, [_i64, _int, _int, _int, _OPTS]),
     "chord_w4a16_moe_gemm": (_int, [_vp, _i64, _int, _vp, _sz, _int, _int, _int, _vp, _vp, _vp, _i64, _int, _i64,
                                     _vp, _vp, _sz, _OPTS, _vp]),
@@ -170,8 +170,8 @@ def chord_select_block_m(T: int, topk: int, E_local: int, E_global: int, N: int,
     return load().chord_select_block_m(T, topk, E_local, E_global, N, K)
 
 
-def chord_select_kernel(block_m: int) -> int:
-    return load().chord_select_kernel(block_m)
+def chord_select_kernel(block_m: int, N: int, K: int) -> int:
+    return load().chord_select_kernel(block_m, N, K)
 
 
 def chord_gemm_workspace_bytes(num_pairs: int, N: int, K: int, block_m: int, opts=None) -> int:

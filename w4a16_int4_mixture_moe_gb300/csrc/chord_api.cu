@@ -35,8 +35,12 @@ chord_opts opts_or_default(const chord_opts* o) {
 
 // Blocks of at most this many rows (tok_e up to about 20) go to the
 // warp-level MMA kernel, whose cost per stage does not depend on a tensor-core
-// instruction's issue latency; larger blocks to the tcgen05 kernel.
+// instruction's issue latency; larger blocks to the tcgen05 kernel, except
+// for short K (few stages per item), where the tcgen05 kernel's fixed cost per
+// item (pipeline fill, accumulator drain) dominates.
 constexpr int kDecodeMaxBlockM = 32;
+constexpr int kShortK = 512;
+constexpr int kShortKMaxBlockM = 128;
 
 int env_int(const char* name, int dflt) {
     const char* v = getenv(name);
@@ -172,10 +176,12 @@ int chord_select_block_m(int T, int topk, int E_local, int E_global, int N, int 
     return bm;
 }
 
-int chord_select_kernel(int block_m) {
+int chord_select_kernel(int block_m, int N, int K) {
+    (void)N;
     const int forced = env_int("CHORD_KERNEL", 0);
     if (forced == CHORD_KERNEL_TCGEN05 || forced == CHORD_KERNEL_WARP_MMA) return forced;
-    return block_m <= kDecodeMaxBlockM ? CHORD_KERNEL_WARP_MMA : CHORD_KERNEL_TCGEN05;
+    if (block_m <= kDecodeMaxBlockM || (K <= kShortK && block_m <= kShortKMaxBlockM)) return CHORD_KERNEL_WARP_MMA;
+    return CHORD_KERNEL_TCGEN05;
 }
 
 size_t chord_gemm_workspace_bytes(int64_t num_pairs, int N, int K, int block_m, const chord_opts* opts) {
@@ -200,7 +206,7 @@ chord_status chord_w4a16_moe_gemm(const void* A, int64_t a_rows, int a_row_divis
     if (N % 128 || K % 64 || block_m % 8 || block_m > 256) return CHORD_ERR_UNSUPPORTED;
     if (num_pairs >= INT32_MAX) return CHORD_ERR_UNSUPPORTED;
     const chord_opts o = opts_or_default(opts);
-    const int kernel = o.kernel ? o.kernel : chord_select_kernel(block_m);
+    const int kernel = o.kernel ? o.kernel : chord_select_kernel(block_m, N, K);
     if (kernel != CHORD_KERNEL_TCGEN05 && kernel != CHORD_KERNEL_WARP_MMA) return CHORD_ERR_INVALID_ARG;
     if (packed_bytes != chord_packed_weight_bytes(E, N, K, CHORD_LAYOUT_TCGEN05)) return CHORD_ERR_LAYOUT_MISMATCH;
     if (!packed || !aligned16(packed) || !num_tokens_padded || (capacity > 0 && (!sorted_ids || !expert_ids)))
