@@ -5,21 +5,22 @@
 // (section "H200 and Blackwell indexed decode"): the 128 dequantised weight
 // rows are the MMA's M side and the block's routed tokens its N side, so a
 // block of 11 rows costs an N = 16 MMA instead of a padded 128-row tile, and
-// a block of 176 rows an N = 176 MMA.  Per 64-column K stage:
-//   * a producer warp streams the packed 128x64 weight chunk (4608 bytes, one
-//     cp.async.bulk) into a shared-memory ring;
+// a block of 176 rows an N = 176 MMA.  Per 128-column K stage:
+//   * a producer warp streams the stage's two packed 128x64 weight chunks
+//     (9216 contiguous bytes, one cp.async.bulk) into a shared-memory ring;
 //   * gather warps copy the block's activation rows (row = pair id / divisor)
 //     with 16-byte cp.async into a 128-byte-swizzled K-major tile, the MMA's B
 //     operand; each lane's copies arrive on the stage's barrier when they land
 //     (cp.async.mbarrier.arrive.noinc) and the MMA thread fences the async
 //     proxy before reading the tile;
-//   * dequantising warps (one row per thread) turn 32 codes per 16-byte load
-//     into bf16((q - 8) * s) and store them with tcgen05.st into a tensor
-//     memory stage, the MMA's A operand (no shared-memory round trip for the
-//     dequantised weights);
-//   * one thread issues four tcgen05.mma (M=128, N=tokens rounded up to 16,
-//     K=16) into an FP32 accumulator in tensor memory and commits the stage
-//     back to the producers;
+//   * dequantising warps (one row per thread, two warpgroups taking alternate
+//     stages) turn 32 codes per 16-byte load into bf16((q - 8) * s) and store
+//     them with tcgen05.st into a tensor-memory stage, the MMA's A operand (no
+//     shared-memory round trip for the dequantised weights);
+//   * an MMA-issuing thread issues eight tcgen05.mma (M=128, N=tokens rounded
+//     up to 16, K=16) into its FP32 accumulator in tensor memory and commits
+//     the stage back to the producers (several issuers take alternate stages
+//     when the blocks are small);
 // after the item's last stage the dequantising warps read the accumulator
 // with tcgen05.ld and write the pair rows of C.  Every wait is bounded.
 #include <cuda_bf16.h>
@@ -630,7 +631,11 @@ bool tc_available() { return true; }
 
 cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t stream) {
     if (a.block_m % 8 || a.block_m > 256 || a.N % kTileRows || a.K % kChunkK) return cudaErrorInvalidValue;
-    if (a.block_m <= 64) return launch_cfg<1, 16, 2>(a, true, stream);   // up to 64 tokens per item
+    // Up to 64 tokens per item: four MMA issuers (a tcgen05.mma of N <= 64 costs
+    // its issuing thread about as long as one of N = 128) and three gather warps
+    // (measured on GB300: 360 -> 290 us for the EP8 decode gate_up against two
+    // issuers and one gather warp).
+    if (a.block_m <= 64) return launch_cfg<3, 6, 4>(a, true, stream);
     return launch_cfg<4, 16, 1>(a, false, stream);                       // up to 256 tokens per item
 }
 
