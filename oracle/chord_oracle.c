@@ -110,7 +110,7 @@ void orc_dequant_pairs(const uint8_t *q, const uint16_t *s, size_t n, uint16_t *
  *
  * blob  = 256-byte header, then E expert regions of N*K*9/16 bytes each.
  * header (little endian): u32 magic 0x44524843 ("CHRD"), u32 version 1,
- *        u32 layout (1 or 2), u32 group 32, u32 E, u32 N, u32 K, u32 0,
+ *        u32 layout (1, 2 or 3), u32 group 32, u32 E, u32 N, u32 K, u32 0,
  *        u64 expert_stride = N*K*9/16, u64 data_offset = 256, then zeros.
  *
  * Layout 1 ("m16 x k64 fragment chunks", N % 16 == 0, K % 64 == 0).
@@ -139,6 +139,13 @@ void orc_dequant_pairs(const uint8_t *q, const uint16_t *s, size_t n, uint16_t *
  *       0,4,1,5,2,6,3,7 hold columns +0..+7.
  *   bytes [4096, 4608): the bf16 scale of row r, group h (columns 32h..32h+31
  *       of the chunk) at 4096 + r*4 + h*2.
+ *
+ * Layout 3 ("layout 2 with gate and up rows interleaved", for a gate_up weight
+ * of N = 2I rows: gate rows 0..I-1, up rows I..2I-1; N % 128 == 0).  Layout 2
+ * byte positions, where packed row p holds canonical row
+ *   8*(p/16) + p%16            if p%16 < 8   (gate row j = 8*(p/16) + p%16)
+ *   I + 8*(p/16) + p%16 - 8    otherwise     (the up row of the same j),
+ * so each 16-row group holds gate rows 8g'..8g'+7 followed by their up rows.
  */
 
 #define ORC_HDR 256u
@@ -152,9 +159,22 @@ static int layout_ok(int layout, int N, int K)
         return 0;
     if (layout == 1)
         return N % 16 == 0;
-    if (layout == 2)
+    if (layout == 2 || layout == 3)
         return N % 128 == 0;
     return 0;
+}
+
+/* Layout 3: the packed row holding canonical row n (the inverse of the map in
+ * the layout description); other layouts keep rows in place. */
+static int packed_row(int layout, int N, int n)
+{
+    if (layout != 3)
+        return n;
+    int half = N / 2;
+    if (n < half)
+        return 16 * (n / 8) + n % 8;
+    int m = n - half;
+    return 16 * (m / 8) + 8 + m % 8;
 }
 
 size_t orc_packed_bytes(int E, int N, int K, int layout)
@@ -179,6 +199,7 @@ static uint64_t get64(const uint8_t *p) { return (uint64_t)get32(p) | (uint64_t)
  * code of row n, column k. */
 static void code_pos(int layout, int N, int K, int n, int k, size_t *byte, int *shift)
 {
+    n = packed_row(layout, N, n);
     if (layout == 1) {
         int mt = n / 16, r = n % 16, kc = k / 64, kk = k % 64;
         int j = kk / 16, kq = kk % 16;
@@ -203,6 +224,7 @@ static void code_pos(int layout, int N, int K, int n, int k, size_t *byte, int *
  * group grp (columns 32*grp .. 32*grp+31). */
 static size_t scale_pos(int layout, int N, int K, int n, int grp)
 {
+    n = packed_row(layout, N, n);
     if (layout == 1) {
         int mt = n / 16, r = n % 16, kc = grp / 2, h = grp % 2;
         int g = r % 8, lower = r / 8;

@@ -39,6 +39,8 @@ MUTANTS = [
     ("silu_sign", "float s = g / (1.0f + expf(-g));", "float s = g / (1.0f + expf(g));"),
     ("gate_up_swap", "float g = f32_from_bf16(C1[(size_t)p * 2 * I + j]);",
      "float g = f32_from_bf16(C1[(size_t)p * 2 * I + I + j]);"),
+    ("interleave_up_first", "return 16 * (m / 8) + 8 + m % 8;", "return 16 * (m / 8) + m % 8 - 8 * (m % 8 > 7);"),
+    ("interleave_by_16", "return 16 * (n / 8) + n % 8;", "return 16 * (n / 16) + n % 16;"),
     ("combine_nonlocal", "if (topk_ids[p] < 0 || topk_ids[p] >= E)\n                    continue;\n                float v",
      "if (topk_ids[p] >= E)\n                    continue;\n                float v"),
 ]

@@ -96,13 +96,14 @@ def test_dequant_exhaustive(orc):
 
 def test_packed_bytes_closed_form(orc):
     for E, N, K in [(1, 128, 64), (8, 256, 256), (8, 256, 128), (48, 4096, 7168), (384, 7168, 256)]:
-        for layout in (1, 2):
+        for layout in (1, 2, 3):
             assert orc.packed_bytes(E, N, K, layout) == 256 + E * N * K * 9 // 16
-    for bad in [(1, 8, 64, 1), (1, 16, 32, 1), (1, 0, 64, 1), (1, 16, 64, 2), (1, 128, 96, 2), (1, 128, 64, 3)]:
+    for bad in [(1, 8, 64, 1), (1, 16, 32, 1), (1, 0, 64, 1), (1, 16, 64, 2), (1, 128, 96, 2), (1, 64, 64, 3),
+                (1, 128, 64, 4)]:
         assert orc.packed_bytes(*bad) == 0
 
 
-@pytest.mark.parametrize("layout", [1, 2])
+@pytest.mark.parametrize("layout", [1, 2, 3])
 def test_pack_header(orc, layout):
     codes = wl.random_codes(1, (3, 128, 128))
     scales = wl.random_scales(2, (3, 128, 4))
@@ -114,11 +115,12 @@ def test_pack_header(orc, layout):
     assert list(h[32:48].view(np.uint64)) == [128 * 128 * 9 // 16, 256]
     assert not h[48:].any()
     assert orc.check_header(blob, 3, 128, 128, layout)
-    assert not orc.check_header(blob, 3, 128, 128, 3 - layout)
+    for other in {1, 2, 3} - {layout}:
+        assert not orc.check_header(blob, 3, 128, 128, other)
     assert not orc.check_header(blob, 3, 64, 256, layout)
 
 
-@pytest.mark.parametrize("layout,N,K", [(1, 32, 128), (2, 256, 128)])
+@pytest.mark.parametrize("layout,N,K", [(1, 32, 128), (2, 256, 128), (3, 256, 128)])
 def test_pack_positions_golden(orc, layout, N, K):
     """Hand-derived byte/nibble positions of each layout's specification."""
     E = 1
@@ -142,7 +144,8 @@ def test_pack_positions_golden(orc, layout, N, K):
 
 @pytest.mark.parametrize("layout,shape", [(1, (1, 16, 64)), (1, (3, 32, 128)), (1, (2, 256, 256)),
                                           (1, (2, 128, 192)), (2, (1, 128, 64)), (2, (2, 256, 192)),
-                                          (2, (1, 384, 128))])
+                                          (2, (1, 384, 128)), (3, (1, 128, 64)), (3, (2, 256, 192)),
+                                          (3, (1, 512, 128))])
 def test_pack_roundtrip_and_coverage(orc, layout, shape):
     """unpack(pack(x)) == x for random data, and all-ones data fills the data region
     completely: together the placement is a bijection (no overlap, no gap)."""
@@ -156,6 +159,22 @@ def test_pack_roundtrip_and_coverage(orc, layout, shape):
     full = orc.pack(np.full(shape, 15, np.uint8), np.full((E, N, K // GROUP), 0xFFFF, np.uint16), layout)
     assert (full[256:] == 0xFF).all()
     assert full.size == 256 + E * N * K * 9 // 16
+
+
+def test_layout3_is_layout2_of_interleaved_rows(orc):
+    """Layout 3 of a gate_up weight equals layout 2 of the same weight with its
+    rows reordered gate 0-7, up 0-7, gate 8-15, up 8-15, ... (except for the
+    layout word of the header)."""
+    E, N, K = 2, 256, 128
+    codes = wl.random_codes(5, (E, N, K))
+    scales = wl.random_scales(6, (E, N, K // GROUP))
+    I = N // 2
+    order = np.concatenate([np.concatenate([np.arange(8 * g, 8 * g + 8), I + np.arange(8 * g, 8 * g + 8)])
+                            for g in range(I // 8)])
+    b3 = orc.pack(codes, scales, 3)
+    b2 = orc.pack(codes[:, order], scales[:, order], 2)
+    assert b3[8] == 3 and b2[8] == 2
+    np.testing.assert_array_equal(b3[12:], b2[12:])
 
 
 def test_pack_rejects_bad_codes_and_header(orc):
