@@ -57,14 +57,15 @@ def routing_stats(ids, E):
     return rows_per_expert
 
 
-def gemm_algorithmic(rows_per_expert, N, K):
+def gemm_algorithmic(rows_per_expert, N, K, out_cols=None):
     """Bytes and FLOPs one GEMM launch must move / do: packed INT4 + scales of
-    every expert with at least one row, activations read, outputs written,
-    sorted ids read; FLOPs over real rows only."""
+    every expert with at least one row, activations read, outputs written
+    (out_cols bf16 columns per row: N, or N/2 with the fused SiLU * up), sorted
+    ids read; FLOPs over real rows only."""
     rows = int(rows_per_expert.sum())
     used = int((rows_per_expert > 0).sum())
     wbytes = used * N * K * 9 // 16
-    nbytes = wbytes + rows * K * 2 + rows * N * 2 + rows * 4
+    nbytes = wbytes + rows * K * 2 + rows * (N if out_cols is None else out_cols) * 2 + rows * 4
     flops = 2 * rows * N * K
     return nbytes, flops
 
@@ -284,6 +285,8 @@ def main():
     ap.add_argument("--impl", default="chord", choices=["chord", "reference"])
     ap.add_argument("--block-m", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--unfused", action="store_true", help="separate SiLU * up pass instead of the fused epilogue")
+    ap.add_argument("--fused", action="store_true", help="SiLU * up in the gate_up epilogue on either kernel")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()
     w = WORKLOADS[args.workload]
@@ -316,9 +319,19 @@ def main():
     ids, wts = wl.make_routing(w, rank % shares)
     x = wl.make_x(w)
     c13, s13 = wl.make_w13(w)
-    p13 = torch.empty(chord.chord_packed_weight_bytes(w.E, 2 * w.I, w.H), dtype=torch.uint8, device=dev)
+    # Decode regime (the warp-level kernel runs gate_up): w13 packed with its
+    # gate and up rows interleaved and SiLU * up in the GEMM's epilogue.
+    # tcgen05 kernel: the separate SiLU * up pass, measured faster there (the
+    # accumulator drain is on the tensor pipe's critical path).  --unfused and
+    # --fused force either.
+    bm0 = args.block_m or chord.chord_select_block_m(w.T, w.topk, w.E, w.E_global, 2 * w.I, w.H)
+    fused = chord.chord_select_kernel(bm0, 2 * w.I, w.H) == chord.KERNEL_WARP_MMA
+    fused = (fused or args.fused) and not args.unfused
+    w13_layout = chord.LAYOUT_GATE_UP_INTERLEAVED if fused else chord.LAYOUT_TCGEN05
+    p13 = torch.empty(chord.chord_packed_weight_bytes(w.E, 2 * w.I, w.H, w13_layout), dtype=torch.uint8, device=dev)
     chord.chord_pack_weights(torch.from_numpy(c13).to(dev),
-                             torch.from_numpy(s13.view(np.int16)).to(dev).view(torch.bfloat16), p13)
+                             torch.from_numpy(s13.view(np.int16)).to(dev).view(torch.bfloat16), p13,
+                             layout=w13_layout)
     del c13, s13
     c2, s2 = wl.make_w2(w)
     p2 = torch.empty(chord.chord_packed_weight_bytes(w.E, w.H, w.I), dtype=torch.uint8, device=dev)
@@ -338,23 +351,25 @@ def main():
     expert_ids = torch.empty(cap // bm, dtype=torch.int32, device=dev)
     ntp = torch.empty(1, dtype=torch.int32, device=dev)
     aws = torch.empty(max(4, chord.chord_align_workspace_bytes(T, topk, E)), dtype=torch.uint8, device=dev)
-    C1 = torch.empty((P, 2 * I), dtype=torch.bfloat16, device=dev)
+    C1 = None if fused else torch.empty((P, 2 * I), dtype=torch.bfloat16, device=dev)
     h = torch.empty((P, I), dtype=torch.bfloat16, device=dev)
     C2 = torch.empty((P, H), dtype=torch.float32, device=dev)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
     f32_out = chord.ChordOpts(out_dtype=chord.DTYPE_F32)
+    silu_opts = chord.ChordOpts(epilogue=chord.EPILOGUE_SILU_MUL if fused else chord.EPILOGUE_NONE)
 
     def step(timed_gemms=None):
         chord.chord_moe_align(idd, E, bm, sorted_ids, expert_ids, ntp, aws, stream=stream)
         if timed_gemms is not None:
             ev[0].record(stream)
-        chord.chord_w4a16_moe_gemm(xd, topk, p13, E, 2 * I, H, sorted_ids, expert_ids, ntp, bm, P, C1,
-                                   stream=stream)
+        chord.chord_w4a16_moe_gemm(xd, topk, p13, E, 2 * I, H, sorted_ids, expert_ids, ntp, bm, P,
+                                   h if fused else C1, opts=silu_opts, stream=stream)
         if timed_gemms is not None:
             ev[1].record(stream)
-        chord.chord_silu_mul(C1, idd, E, h, stream=stream)
+        if not fused:
+            chord.chord_silu_mul(C1, idd, E, h, stream=stream)
         if timed_gemms is not None:
             ev[2].record(stream)
         chord.chord_w4a16_moe_gemm(h, 1, p2, E, H, I, sorted_ids, expert_ids, ntp, bm, P, C2, opts=f32_out,
@@ -363,7 +378,7 @@ def main():
             ev[3].record(stream)
         chord.chord_moe_combine(C2, idd, wd, E, out, stream=stream)
 
-    launches_per_step = (3 if P > 0 else 2) + 4
+    launches_per_step = (3 if P > 0 else 2) + (3 if fused else 4)
 
     def barrier():
         if pg:
@@ -411,7 +426,8 @@ def main():
         x_e.copy_(x_h, non_blocking=True)
         ids_e.copy_(ids_h, non_blocking=True)
         w_e.copy_(w_h, non_blocking=True)
-        chord.chord_moe_layer(x_e, ids_e, w_e, E, w.E_global, I, p13, p2, lws, out, block_m=bm, stream=stream)
+        chord.chord_moe_layer(x_e, ids_e, w_e, E, w.E_global, I, p13, p2, lws, out, block_m=bm, opts=silu_opts,
+                              stream=stream)
         out_h.copy_(out, non_blocking=True)
 
     for _ in range(args.warmup):
@@ -432,9 +448,10 @@ def main():
     e2e_us = e2e_ms * 1e3 / args.steps / world
 
     rpe = routing_stats(ids, E)
-    b1, f1_ = gemm_algorithmic(rpe, 2 * I, H)
+    b1, f1_ = gemm_algorithmic(rpe, 2 * I, H, out_cols=I if fused else 2 * I)
     b2, f2_ = gemm_algorithmic(rpe, H, I)
     cfg, regime, peaks = arm_config(w, bm, world)
+    cfg["silu_mul"] = "fused into gate_up" if fused else "separate pass"
     kind = "warp_mma" if chord.chord_select_kernel(bm, 2 * I, H) == chord.KERNEL_WARP_MMA else "tc"
     kname = KERNEL_NAME[kind] + " (gate_up)"
     if regime == "decode":

@@ -82,10 +82,22 @@ typedef enum chord_kernel {
 } chord_kernel;
 
 /* Packed weight layouts (recorded in the blob's header, checked on the device).
- * Both kernels read CHORD_LAYOUT_TCGEN05; layout 1 is packed for tests of the
- * header check only and no kernel accepts it. */
+ * Both kernels read CHORD_LAYOUT_TCGEN05, and CHORD_LAYOUT_GATE_UP_INTERLEAVED
+ * for the fused SiLU*up epilogue; layout 1 is packed for tests of the header
+ * check only and no kernel accepts it. */
 #define CHORD_LAYOUT_WARP_MMA 1   /* 16 x 64 chunks in m16n8k16 A-fragment order, N % 16 == 0 */
 #define CHORD_LAYOUT_TCGEN05 2    /* 128 x 64 chunks, one row per 16-byte group, N % 128 == 0 */
+#define CHORD_LAYOUT_GATE_UP_INTERLEAVED 3
+    /* layout 2 of a gate_up weight (N = 2I, gate rows 0..I-1, up rows I..2I-1)
+       with its rows reordered so that each 16-row group holds gate rows
+       8g..8g+7 and then their up rows I+8g..I+8g+7: a thread that holds rows r
+       and r+8 of an MMA tile holds a gate value and its up value */
+
+/* GEMM epilogue. */
+typedef enum chord_epilogue {
+    CHORD_EPILOGUE_NONE = 0,      /* C = the projection */
+    CHORD_EPILOGUE_SILU_MUL = 1   /* gate_up only: C = h = SiLU(gate) * up (see chord_w4a16_moe_gemm) */
+} chord_epilogue;
 
 typedef enum chord_dtype {
     CHORD_DTYPE_BF16 = 0,
@@ -100,7 +112,8 @@ typedef struct chord_opts {
     int32_t split_k;     /* 0 = automatic, 1 = off, > 1 = number of K slices (decode) */
     int32_t out_dtype;   /* GEMM output: CHORD_DTYPE_BF16 (default) or CHORD_DTYPE_F32,
                             the FP32 sums unrounded (for a consumer that keeps FP32) */
-    int32_t reserved[4]; /* must be zero */
+    int32_t epilogue;    /* chord_epilogue (GEMM and layer) */
+    int32_t reserved[3]; /* must be zero */
 } chord_opts;
 
 /* Library version (major * 10000 + minor * 100 + patch). */
@@ -225,11 +238,16 @@ size_t chord_gemm_workspace_bytes(int64_t num_pairs, int N, int K, int block_m,
  * dequantised weight bf16_rne((q - 8) * s); the sum is FP32.
  *   A        device bf16 [a_rows, K]; a_row_divisor = topk when A has one row
  *            per token (gate_up), 1 when it has one row per pair (down).
- *   packed   blob from chord_pack_weights for (E, N, K) in the layout of the
- *            kernel opts->kernel selects.
+ *   packed   blob from chord_pack_weights for (E, N, K) in CHORD_LAYOUT_TCGEN05.
  *   C        device bf16 [num_pairs, N] (float [num_pairs, N] with
  *            opts->out_dtype = CHORD_DTYPE_F32, the sum left unrounded);
  *            rows no block names are not written.
+ * With opts->epilogue = CHORD_EPILOGUE_SILU_MUL (gate_up, SiLU*up fused):
+ *   packed   in CHORD_LAYOUT_GATE_UP_INTERLEAVED, N = 2I;
+ *   C        device bf16 [num_pairs, I]: h[p, j] = bf16_rne( g / (1 + exp(-g)) * u )
+ *            with g, u the bf16-rounded gate and up sums of column j — the
+ *            values this call without the epilogue followed by chord_silu_mul
+ *            gives; out_dtype must be CHORD_DTYPE_BF16.
  *   capacity length of sorted_ids (expert_ids has capacity / block_m entries).
  * block_m must equal the value given to chord_moe_align, be a multiple of 8 and
  * at most 256; N % 128 == 0, K % 64 == 0. */
@@ -277,8 +295,12 @@ size_t chord_layer_workspace_bytes(int T, int topk, int E, int H, int I, int blo
  * to BF16 once.
  *   x          device bf16 [T, H]
  *   topk_ids   device int32 [T, topk] (local id or -1), topk_w device float [T, topk]
- *   packed_w13 blob for (E, 2 * I, H): rows 0..I-1 gate, I..2I-1 up
- *   packed_w2  blob for (E, H, I)
+ *   packed_w13 blob for (E, 2 * I, H): rows 0..I-1 gate, I..2I-1 up, in
+ *              CHORD_LAYOUT_TCGEN05, or in CHORD_LAYOUT_GATE_UP_INTERLEAVED with
+ *              opts->epilogue = CHORD_EPILOGUE_SILU_MUL (SiLU * up then runs in
+ *              the gate_up GEMM's epilogue, same results, one launch and the
+ *              [T * topk, 2I] intermediate fewer)
+ *   packed_w2  blob for (E, H, I) in CHORD_LAYOUT_TCGEN05
  *   E_global   number of experts the router chooses from (for tok_e)
  *   block_m    0 = chord_select_block_m(T, topk, E, E_global, 2 * I, H)
  *   workspace  >= chord_layer_workspace_bytes(T, topk, E, H, I, block_m) bytes

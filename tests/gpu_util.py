@@ -39,6 +39,21 @@ def assert_close(got_bits, ref_bits, what=""):
     return float(err.max()) if err.size else 0.0
 
 
+def assert_close_h(got_bits, ref_bits, what=""):
+    """For h = bf16(SiLU(g) * u) computed from this library's own bf16 gate and
+    up sums: a last-place flip of one of those roundings (an FP32 summation
+    order effect) moves h by a few bf16 ulps, more where SiLU is steep (g well
+    below zero).  The exact checks are elsewhere: the fused result equals the
+    unfused path bit for bit, whose GEMM and SiLU * up stages are each checked
+    against the oracle on the oracle's own inputs.  Here at most 0.1 % of the
+    elements may fall outside the GEMM tolerance."""
+    g, r = f64(got_bits), f64(ref_bits)
+    err = np.abs(g - r)
+    bad = ~(err <= ATOL + RTOL * np.abs(r))
+    assert bad.sum() <= max(1, bad.size // 1000), (f"{what}: {int(bad.sum())} of {bad.size} outside tolerance, "
+                                                   f"max err {np.nanmax(err):.4g}")
+
+
 KERNELS = {"tcgen05": (chord.KERNEL_TCGEN05, chord.LAYOUT_TCGEN05),
            "warp_mma": (chord.KERNEL_WARP_MMA, chord.LAYOUT_TCGEN05)}
 

@@ -42,13 +42,14 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_sizes_and_capacity(lib):
-    for layout in (1, 2):
+    for layout in (1, 2, 3):
         assert chord.chord_packed_weight_bytes(48, 4096, 7168, layout) == 256 + 48 * 4096 * 7168 * 9 // 16
         assert chord.chord_packed_weight_bytes(1, 8, 64, layout) == 0
         assert chord.chord_packed_weight_bytes(1, 128, 96, layout) == 0
     assert chord.chord_packed_weight_bytes(1, 16, 64, 1) == 256 + 16 * 64 * 9 // 16
     assert chord.chord_packed_weight_bytes(1, 16, 64, 2) == 0
-    assert chord.chord_packed_weight_bytes(1, 128, 64, 3) == 0
+    assert chord.chord_packed_weight_bytes(1, 16, 64, 3) == 0
+    assert chord.chord_packed_weight_bytes(1, 128, 64, 4) == 0
     P = 512 * 8
     assert chord.chord_align_capacity(512, 8, 48, 16) == -(-(P + 48 * 15) // 16) * 16
     assert chord.chord_align_capacity(1, 8, 384, 8) == -(-(8 + 8 * 7) // 8) * 8
@@ -147,3 +148,13 @@ def test_argument_errors_before_any_launch(lib):
     nb = chord.chord_packed_weight_bytes(2, 128, 64, 2)
     args = [vp((1 << 20) + 2), 16, 1, big, nb, 2, 128, 64, big, big, big, 16, 8, 16, big, None, 0, None, None]
     assert lib.chord_w4a16_moe_gemm(*args) == 1
+    # fused SiLU * up: an unknown epilogue, or FP32 output with the epilogue
+    args = [big, 16, 1, big, nb, 2, 128, 64, big, big, big, 16, 8, 16, big, None, 0, None, None]
+    for epi, dt in [(2, 0), (1, 1)]:
+        o = chord.ChordOpts(epilogue=epi, out_dtype=dt)
+        args[17] = ctypes.byref(o)
+        assert lib.chord_w4a16_moe_gemm(*args) == 1, (epi, dt)
+    # layout 3 (gate_up rows interleaved) has layout 2's size and needs N % 128 == 0
+    assert chord.chord_packed_weight_bytes(2, 256, 64, 3) == chord.chord_packed_weight_bytes(2, 256, 64, 2)
+    assert chord.chord_packed_weight_bytes(2, 64, 64, 3) == 0
+    assert lib.chord_pack_weights(big, big, 1, 64, 64, 32, 3, big, 10 ** 6, None) == 2

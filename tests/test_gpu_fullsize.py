@@ -10,7 +10,7 @@ import torch
 import oracle
 import w4a16_int4_mixture_moe_gb300 as chord
 import workloads as wl
-from gpu_util import DEV, align, assert_close, dbf, dev, f64, gemm, host_bits, layer, pack
+from gpu_util import DEV, align, assert_close, assert_close_h, dbf, dev, f64, gemm, host_bits, layer, pack
 
 pytestmark = pytest.mark.gpu
 
@@ -119,6 +119,42 @@ def test_layer_full_size_stagewise(w):
     out = torch.empty((sel.size, w.H), dtype=torch.bfloat16, device=DEV)
     chord.chord_moe_combine(dev(C2r), dev(ids[sel]), dev(wts[sel]), w.E, out)
     np.testing.assert_array_equal(host_bits(out), outr)
+
+
+@pytest.mark.parametrize("w", WORKLOADS, ids=[w.name for w in WORKLOADS])
+def test_fused_gate_up_full_size(w):
+    """The gate_up GEMM with the fused SiLU * up epilogue (w13 in layout 3), at
+    full size in the benchmark's launch configuration: bit for bit the unfused
+    path (the same GEMM on the layout-2 blob, whose output the stagewise test
+    checks against the oracle, then the SiLU * up pass) on every local pair.
+    Against the oracle's h directly, a last-place flip of a gate or up sum's
+    bf16 rounding moves h by a few ulps, so there at most 0.1 % of the sampled
+    elements may fall outside the tolerance."""
+    ids, wts = wl.make_routing(w)
+    x = wl.make_x(w)
+    w13, w2, p13, _ = weights(w)
+    p13i = pack(w13[0], w13[1], chord.LAYOUT_GATE_UP_INTERLEAVED)
+    bm = chord.chord_select_block_m(w.T, w.topk, w.E, w.E_global, 2 * w.I, w.H)
+    s, e, n = align(ids, w.E, bm)
+    hd = torch.empty((w.P, w.I), dtype=torch.bfloat16, device=DEV)
+    chord.chord_w4a16_moe_gemm(dbf(x), w.topk, p13i, w.E, 2 * w.I, w.H, s, e, n, bm, w.P, hd,
+                               opts=chord.ChordOpts(epilogue=chord.EPILOGUE_SILU_MUL))
+    del p13i
+    C1 = gemm(x, w.topk, p13, w.E, 2 * w.I, w.H, s, e, n, bm, w.P)
+    h2 = torch.empty((w.P, w.I), dtype=torch.bfloat16, device=DEV)
+    chord.chord_silu_mul(C1, dev(ids), w.E, h2)
+    del C1
+    local = np.nonzero(((ids >= 0) & (ids < w.E)).ravel())[0]
+    li = torch.from_numpy(local).to(DEV)
+    assert torch.equal(hd[li].view(torch.int16), h2[li].view(torch.int16)), "fused differs from unfused"
+    del h2
+    sel = sample_tokens(ids, w.E, N_SAMPLE_TOKENS, w.seed + 1)
+    _, hr, _, _ = oracle_stages(w, x, ids, wts, w13, w2, sel)
+    pairs = full_pairs(sel, w.topk)
+    rows = np.nonzero(((ids[sel] >= 0) & (ids[sel] < w.E)).ravel())[0]
+    hg = host_bits(hd)
+    del hd
+    assert_close_h(hg[pairs][rows], hr[rows], f"{w.name} fused gate_up + SiLU*up (block_m={bm})")
 
 
 @pytest.mark.parametrize("w", WORKLOADS, ids=[w.name for w in WORKLOADS])

@@ -10,7 +10,7 @@ import torch
 import oracle
 import w4a16_int4_mixture_moe_gb300 as chord
 import workloads as wl
-from gpu_util import (DEV, KERNELS, align, assert_close, dbf, dev, f64, gemm, host_bits, layer, pack, valid_rows)
+from gpu_util import (DEV, KERNELS, align, assert_close, assert_close_h, dbf, dev, f64, gemm, host_bits, layer, pack, valid_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -32,7 +32,8 @@ def _lib():
 @pytest.mark.parametrize("layout,shape", [(1, (8, 256, 256)), (1, (8, 256, 128)), (1, (3, 32, 128)),
                                           (1, (2, 144, 192)), (1, (1, 4096, 7168)),
                                           (2, (8, 256, 256)), (2, (8, 256, 128)), (2, (3, 384, 192)),
-                                          (2, (1, 4096, 7168)), (2, (2, 7168, 256))])
+                                          (2, (1, 4096, 7168)), (2, (2, 7168, 256)),
+                                          (3, (8, 256, 256)), (3, (3, 384, 192)), (3, (1, 4096, 7168))])
 def test_pack_byte_exact(layout, shape):
     E, N, K = shape
     codes = wl.random_codes(sum(shape), shape)
@@ -42,7 +43,7 @@ def test_pack_byte_exact(layout, shape):
     np.testing.assert_array_equal(got, want)
 
 
-@pytest.mark.parametrize("layout", [1, 2])
+@pytest.mark.parametrize("layout", [1, 2, 3])
 def test_pack_bad_code_sets_error_word(layout):
     codes = np.zeros((1, 128, 64), np.uint8)
     codes[0, 5, 7] = 17
@@ -287,6 +288,63 @@ def test_gemm_header_mismatch_is_reported():
         assert (host_bits(C) == 0xFFFF).all()
 
 
+# ---------------------------------------------------------- fused SiLU * up
+
+def run_fused_case(T, topk, E, I, K, bm, seed, kernel, pnl=0.2):
+    """The gate_up GEMM with the SiLU * up epilogue on a layout-3 blob, against
+    the oracle's GEMM followed by its SiLU * up, and bit for bit against this
+    library's unfused path (same sums, same rounding points)."""
+    x = wl.random_bf16(seed, (T, K))
+    codes = wl.random_codes(seed + 1, (E, 2 * I, K))
+    scales = wl.random_scales(seed + 2, (E, 2 * I, K // 32))
+    ids = wl.random_ids(seed + 3, T, topk, E, p_nonlocal=pnl)
+    P = T * topk
+    kid, layout = KERNELS[kernel]
+    s, e, n = align(ids, E, bm)
+    h = torch.full((max(P, 1), I), -1, dtype=torch.int16, device=DEV)[:P].view(torch.bfloat16)
+    chord.chord_w4a16_moe_gemm(dbf(x), topk, pack(codes, scales, chord.LAYOUT_GATE_UP_INTERLEAVED), E, 2 * I, K,
+                               s, e, n, bm, P, h, opts=chord.ChordOpts(kernel=kid, epilogue=chord.EPILOGUE_SILU_MUL))
+    got = host_bits(h)
+    s2, e2, n2 = oracle.moe_align(ids, E, bm)
+    c1 = oracle.moe_gemm(x, topk, codes, scales, s2, e2, n2, bm, P, C=np.zeros((P, 2 * I), np.uint16))
+    ref = oracle.silu_mul(c1, ids.ravel(), E, h=np.full((P, I), 0xFFFF, np.uint16))
+    rows = valid_rows(ids, E)
+    other = np.setdiff1d(np.arange(P), rows)
+    assert (got[other] == 0xFFFF).all(), "rows of non-local pairs were written"
+    assert_close_h(got[rows], ref[rows], f"{kernel} fused gate_up T={T} E={E} I={I} K={K} bm={bm}")
+    C1 = gemm(x, topk, pack(codes, scales, layout), E, 2 * I, K, s, e, n, bm, P, kernel=kid)
+    h2 = torch.full((max(P, 1), I), -1, dtype=torch.int16, device=DEV)[:P].view(torch.bfloat16)
+    chord.chord_silu_mul(C1, dev(ids.ravel().copy()), E, h2)
+    np.testing.assert_array_equal(got[rows], host_bits(h2)[rows])
+
+
+@BOTH
+@pytest.mark.parametrize("bm", [8, 16, 32, 64, 128, 256])
+@pytest.mark.parametrize("shape", [(3, 64, 128), (4, 192, 320), (2, 128, 1024)])
+def test_fused_silu_mul_vs_oracle(kernel, bm, shape):
+    E, I, K = shape
+    run_fused_case(37, 3, E, I, K, bm, seed=E * I + K + bm, kernel=kernel)
+
+
+def test_fused_silu_mul_needs_layout3_and_vice_versa():
+    """A layout-2 blob with the epilogue, and a layout-3 blob without it, are
+    refused on the device and write nothing."""
+    E, I, K = 2, 64, 128
+    codes = wl.random_codes(1, (E, 2 * I, K))
+    scales = wl.random_scales(2, (E, 2 * I, K // 32))
+    ids = wl.random_ids(3, 8, 2, E)
+    s, e, n = align(ids, E, 8)
+    x = wl.random_bf16(4, (8, K))
+    for layout, epi, width in [(2, chord.EPILOGUE_SILU_MUL, I), (3, chord.EPILOGUE_NONE, 2 * I)]:
+        for kid in (chord.KERNEL_TCGEN05, chord.KERNEL_WARP_MMA):
+            C = torch.full((16, width), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+            with pytest.raises(chord.ChordError) as ei:
+                chord.chord_w4a16_moe_gemm(dbf(x), 2, pack(codes, scales, layout), E, 2 * I, K, s, e, n, 8, 16, C,
+                                           opts=chord.ChordOpts(kernel=kid, validate=1, epilogue=epi))
+            assert ei.value.status == 6
+            assert (host_bits(C) == 0xFFFF).all()
+
+
 # ---------------------------------------------------------------- epilogues
 
 def test_silu_mul_vs_oracle():
@@ -326,20 +384,24 @@ def test_combine_bit_exact():
 
 @BOTH
 @pytest.mark.parametrize("bm", [0, 8, 16, 32, 64, 256])
-def test_layer_tiny_vs_oracle(kernel, bm):
+@pytest.mark.parametrize("fused", [False, True])
+def test_layer_tiny_vs_oracle(kernel, bm, fused):
     w = wl.TINY
     ids, wts = wl.make_routing(w)
     x = wl.make_x(w)
     c13, s13 = wl.make_w13(w)
     c2, s2 = wl.make_w2(w)
     kid, layout = KERNELS[kernel]
-    out, used_bm = layer(x, ids, wts, w.E, w.E_global, w.I, pack(c13, s13, layout), pack(c2, s2, layout), bm=bm,
-                         opts=chord.ChordOpts(kernel=kid))
+    p13 = pack(c13, s13, chord.LAYOUT_GATE_UP_INTERLEAVED if fused else layout)
+    epi = chord.EPILOGUE_SILU_MUL if fused else chord.EPILOGUE_NONE
+    out, used_bm = layer(x, ids, wts, w.E, w.E_global, w.I, p13, pack(c2, s2, layout), bm=bm,
+                         opts=chord.ChordOpts(kernel=kid, epilogue=epi))
     ref = oracle.moe_layer(x, ids, wts, (c13, s13), (c2, s2), w.E, block_m=used_bm)
     assert_close(host_bits(out), ref, f"tiny layer bm={used_bm}")
 
 
-def test_layer_ep_partial_and_empty_tokens():
+@pytest.mark.parametrize("fused", [False, True])
+def test_layer_ep_partial_and_empty_tokens(fused):
     """EP-style routing with most pairs non-local; tokens with no local pair are +0."""
     T, topk, E, H, I = 24, 8, 6, 256, 128
     ids = wl.random_ids(20, T, topk, 48)
@@ -349,7 +411,9 @@ def test_layer_ep_partial_and_empty_tokens():
     x = wl.random_bf16(22, (T, H))
     c13, s13 = wl.random_codes(23, (E, 2 * I, H)), wl.random_scales(24, (E, 2 * I, H // 32))
     c2, s2 = wl.random_codes(25, (E, H, I)), wl.random_scales(26, (E, H, I // 32))
-    out, bm = layer(x, ids, wts, E, 48, I, pack(c13, s13), pack(c2, s2))
+    p13 = pack(c13, s13, chord.LAYOUT_GATE_UP_INTERLEAVED if fused else chord.LAYOUT_TCGEN05)
+    opts = chord.ChordOpts(epilogue=chord.EPILOGUE_SILU_MUL if fused else chord.EPILOGUE_NONE)
+    out, bm = layer(x, ids, wts, E, 48, I, p13, pack(c2, s2), opts=opts)
     ref = oracle.moe_layer(x, ids, wts, (c13, s13), (c2, s2), E, block_m=bm)
     got = host_bits(out)
     assert_close(got, ref, "ep partial layer")

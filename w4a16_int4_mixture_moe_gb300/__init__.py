@@ -25,7 +25,8 @@ __all__ = [
 ]
 
 KERNEL_AUTO, KERNEL_TCGEN05, KERNEL_WARP_MMA = 0, 1, 2
-LAYOUT_WARP_MMA, LAYOUT_TCGEN05 = 1, 2
+LAYOUT_WARP_MMA, LAYOUT_TCGEN05, LAYOUT_GATE_UP_INTERLEAVED = 1, 2, 3
+EPILOGUE_NONE, EPILOGUE_SILU_MUL = 0, 1
 DTYPE_BF16, DTYPE_F32 = 0, 1
 STATUS = {0: "CHORD_OK", 1: "CHORD_ERR_INVALID_ARG", 2: "CHORD_ERR_UNSUPPORTED", 3: "CHORD_ERR_LAYOUT_MISMATCH",
           4: "CHORD_ERR_BUFFER_TOO_SMALL", 5: "CHORD_ERR_CUDA", 6: "CHORD_ERR_DEVICE_VALIDATION",
@@ -40,7 +41,7 @@ class ChordError(RuntimeError):
 
 class ChordOpts(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("validate", ctypes.c_int32), ("split_k", ctypes.c_int32),
-                ("out_dtype", ctypes.c_int32), ("reserved", ctypes.c_int32 * 4)]
+                ("out_dtype", ctypes.c_int32), ("epilogue", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
 
 
 _lock = threading.Lock()

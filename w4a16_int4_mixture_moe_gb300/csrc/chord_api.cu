@@ -102,8 +102,8 @@ const char* chord_status_string(chord_status s) {
 
 size_t chord_packed_weight_bytes(int E, int N, int K, int layout) {
     if (E < 0 || N <= 0 || K <= 0 || K % 64) return 0;
-    if (!(layout == CHORD_LAYOUT_WARP_MMA && N % 16 == 0) && !(layout == CHORD_LAYOUT_TCGEN05 && N % 128 == 0))
-        return 0;
+    const bool tile128 = layout == CHORD_LAYOUT_TCGEN05 || layout == CHORD_LAYOUT_GATE_UP_INTERLEAVED;
+    if (!(layout == CHORD_LAYOUT_WARP_MMA && N % 16 == 0) && !(tile128 && N % 128 == 0)) return 0;
     return (size_t)kHeaderBytes + (size_t)E * (size_t)N * (size_t)K * 9u / 16u;
 }
 
@@ -111,7 +111,8 @@ chord_status chord_pack_weights(const uint8_t* codes, const void* scales, int E,
                                 int layout, void* packed, size_t packed_bytes, void* stream) {
     if (group_size != kGroup) return CHORD_ERR_UNSUPPORTED;
     if (E < 0 || N <= 0 || K <= 0) return CHORD_ERR_INVALID_ARG;
-    if (layout != CHORD_LAYOUT_WARP_MMA && layout != CHORD_LAYOUT_TCGEN05) return CHORD_ERR_INVALID_ARG;
+    if (layout != CHORD_LAYOUT_WARP_MMA && layout != CHORD_LAYOUT_TCGEN05 && layout != CHORD_LAYOUT_GATE_UP_INTERLEAVED)
+        return CHORD_ERR_INVALID_ARG;
     if (chord_packed_weight_bytes(E, N, K, layout) == 0) return CHORD_ERR_UNSUPPORTED;
     if (!packed || !aligned16(packed) || (E > 0 && (!codes || !scales))) return CHORD_ERR_INVALID_ARG;
     if (packed_bytes < chord_packed_weight_bytes(E, N, K, layout)) return CHORD_ERR_BUFFER_TOO_SMALL;
@@ -215,6 +216,9 @@ chord_status chord_w4a16_moe_gemm(const void* A, int64_t a_rows, int a_row_divis
     if ((a_rows > 0 && (!A || !aligned16(A))) || (num_pairs > 0 && (!C || !aligned16(C))))
         return CHORD_ERR_INVALID_ARG;
     if (o.out_dtype != CHORD_DTYPE_BF16 && o.out_dtype != CHORD_DTYPE_F32) return CHORD_ERR_INVALID_ARG;
+    if (o.epilogue != CHORD_EPILOGUE_NONE && o.epilogue != CHORD_EPILOGUE_SILU_MUL) return CHORD_ERR_INVALID_ARG;
+    const bool silu = o.epilogue == CHORD_EPILOGUE_SILU_MUL;
+    if (silu && o.out_dtype != CHORD_DTYPE_BF16) return CHORD_ERR_INVALID_ARG;
     const DeviceInfo& di = device_info();
     if (!di.err) return CHORD_ERR_CUDA;
     if (capacity == 0 || num_pairs == 0) return CHORD_OK;
@@ -235,6 +239,8 @@ chord_status chord_w4a16_moe_gemm(const void* A, int64_t a_rows, int a_row_divis
     g.id_limit = a_rows * (int64_t)a_row_divisor < num_pairs ? a_rows * (int64_t)a_row_divisor : num_pairs;
     g.C = C;
     g.out_f32 = o.out_dtype == CHORD_DTYPE_F32 ? 1 : 0;
+    g.silu = silu ? 1 : 0;
+    g.layout = silu ? CHORD_LAYOUT_GATE_UP_INTERLEAVED : CHORD_LAYOUT_TCGEN05;
     g.err = di.err;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = kernel == CHORD_KERNEL_TCGEN05 ? launch_gemm_tc(g, s) : launch_gemm_decode(g, s);
@@ -334,13 +340,22 @@ chord_status chord_moe_layer(const void* x, const int32_t* topk_ids, const float
     st = chord_moe_align(topk_ids, T, topk, E, block_m, sorted, experts, ntp, cap, counts,
                          chord_align_workspace_bytes(T, topk, E), &o, stream);
     if (st != CHORD_OK) return st;
-    st = chord_w4a16_moe_gemm(x, T, topk, packed_w13, w13_bytes, E, 2 * I, H, sorted, experts, ntp, cap, block_m, P,
-                              c1, nullptr, 0, &o, stream);
-    if (st != CHORD_OK) return st;
-    st = chord_silu_mul(c1, topk_ids, P, E, I, h, stream);
-    if (st != CHORD_OK) return st;
+    if (o.epilogue == CHORD_EPILOGUE_SILU_MUL) {
+        // w13 in layout 3: SiLU * up in the gate_up GEMM's epilogue, h written directly
+        st = chord_w4a16_moe_gemm(x, T, topk, packed_w13, w13_bytes, E, 2 * I, H, sorted, experts, ntp, cap, block_m,
+                                  P, h, nullptr, 0, &o, stream);
+        if (st != CHORD_OK) return st;
+    } else {
+        if (o.epilogue != CHORD_EPILOGUE_NONE) return CHORD_ERR_INVALID_ARG;
+        st = chord_w4a16_moe_gemm(x, T, topk, packed_w13, w13_bytes, E, 2 * I, H, sorted, experts, ntp, cap, block_m,
+                                  P, c1, nullptr, 0, &o, stream);
+        if (st != CHORD_OK) return st;
+        st = chord_silu_mul(c1, topk_ids, P, E, I, h, stream);
+        if (st != CHORD_OK) return st;
+    }
     chord_opts o_down = o;
     o_down.out_dtype = CHORD_DTYPE_F32;
+    o_down.epilogue = CHORD_EPILOGUE_NONE;
     st = chord_w4a16_moe_gemm(h, P, 1, packed_w2, w2_bytes, E, H, I, sorted, experts, ntp, cap, block_m, P, c2,
                               nullptr, 0, &o_down, stream);
     if (st != CHORD_OK) return st;

@@ -20,8 +20,17 @@ namespace chord {
 // 0..1023 are codes (half h = w/512, row r = (w%512)/4, word j = w%4 holding
 // columns 32h + 8j + m of the chunk, m = 2*(i%4) + i/4 in nibble i), words
 // 1024..1151 the two group scales of each row.
+// Layout 3 keeps layout 2's byte positions but reorders a gate_up weight's
+// rows: packed row p holds gate row 8*(p/16) + p%16 when p%16 < 8, else the up
+// row N/2 + 8*(p/16) + p%16 - 8 (each 16-row group: 8 gate rows, their up rows).
+__device__ __forceinline__ int canonical_row(int p, int N, bool interleaved) {
+    if (!interleaved) return p;
+    const int g = p >> 4, i = p & 15;
+    return i < 8 ? 8 * g + i : (N >> 1) + 8 * g + (i - 8);
+}
+
 __global__ void pack2_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ scales, int E, int N,
-                             int K, uint32_t* __restrict__ out, int* err) {
+                             int K, bool interleaved, uint32_t* __restrict__ out, int* err) {
     constexpr int kWords = 4608 / 4;
     const int kchunks = K / 64;
     const int64_t chunks_per_expert = (int64_t)(N / 128) * kchunks;
@@ -36,7 +45,8 @@ __global__ void pack2_kernel(const uint8_t* __restrict__ codes, const uint16_t* 
         uint32_t v = 0;
         if (wi < 1024) {
             const int h = wi / 512, r = (wi % 512) / 4, j = wi % 4;
-            const uint8_t* p = codes + ((int64_t)e * N + nt * 128 + r) * K + kc * 64 + h * 32 + j * 8;
+            const int n = canonical_row(nt * 128 + r, N, interleaved);
+            const uint8_t* p = codes + ((int64_t)e * N + n) * K + kc * 64 + h * 32 + j * 8;
             uint32_t bad = 0;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -47,7 +57,7 @@ __global__ void pack2_kernel(const uint8_t* __restrict__ codes, const uint16_t* 
             if (bad) set_error(err, CHORD_DEV_BAD_CODE);
         } else {
             const int r = wi - 1024;
-            const int64_t row = (int64_t)e * N + nt * 128 + r;
+            const int64_t row = (int64_t)e * N + canonical_row(nt * 128 + r, N, interleaved);
             v = (uint32_t)scales[row * G + 2 * kc] | ((uint32_t)scales[row * G + 2 * kc + 1] << 16);
         }
         out[w] = v;
@@ -133,8 +143,8 @@ cudaError_t launch_pack(const uint8_t* codes, const uint16_t* scales, int E, int
     int64_t blocks = ceil_div64(words, threads);
     const int64_t cap = (int64_t)device_info().sm_count * 16;
     if (blocks > cap) blocks = cap;
-    if (layout == 2)
-        pack2_kernel<<<(unsigned)blocks, threads, 0, stream>>>(codes, scales, E, N, K,
+    if (layout == 2 || layout == 3)
+        pack2_kernel<<<(unsigned)blocks, threads, 0, stream>>>(codes, scales, E, N, K, layout == 3,
                                                                reinterpret_cast<uint32_t*>(packed + kHeaderBytes), err);
     else
         pack_kernel<<<(unsigned)blocks, threads, 0, stream>>>(codes, scales, E, N, K, packed, err);
@@ -304,11 +314,6 @@ __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 r = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&r);
-}
-
-__device__ __forceinline__ float silu_times(float g, float u) {
-    const float s = __fdiv_rn(g, __fadd_rn(1.0f, expf(-g)));
-    return __fmul_rn(s, u);
 }
 
 __global__ void silu_mul_kernel(const uint16_t* __restrict__ C1, const int32_t* __restrict__ ids, int64_t P, int E,

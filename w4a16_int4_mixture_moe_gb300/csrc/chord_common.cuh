@@ -197,4 +197,22 @@ __device__ __forceinline__ void dequant_row8(uint32_t w, uint32_t sp, uint32_t* 
 
 __host__ __device__ __forceinline__ int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// SiLU(g) * u in FP32: g / (1 + exp(-g)), then times u, with the fast
+// exponential and division intrinsics (a few float ulps from the correctly
+// rounded forms, far below the bf16 rounding that follows).  Large -g gives
+// exp(-g) = inf and a quotient of 0 where the exact value is a tiny negative.
+__device__ __forceinline__ float silu_times(float g, float u) {
+    const float s = __fdividef(g, __fadd_rn(1.0f, __expf(-g)));
+    return __fmul_rn(s, u);
+}
+
+// The fused gate_up epilogue's value: the gate and up FP32 sums rounded to
+// bf16 (the GEMM's output type), then bf16(SiLU(g) * u) — what the GEMM
+// followed by the SiLU * up pass computes.
+__device__ __forceinline__ __nv_bfloat16 silu_mul_bf16(float g_sum, float u_sum) {
+    const float g = __bfloat162float(__float2bfloat16_rn(g_sum));
+    const float u = __bfloat162float(__float2bfloat16_rn(u_sum));
+    return __float2bfloat16_rn(silu_times(g, u));
+}
+
 }  // namespace chord

@@ -40,7 +40,6 @@ constexpr int kKS = 128;                          // K columns per stage
 constexpr int kChunk2 = 4608;                     // one 128-row x 64-column packed chunk
 constexpr int kWStageBytes = (kKS / 64) * kChunk2;
 constexpr int kXStride = kKS * 2 + 16;            // padded token row: conflict-free 16-byte loads
-constexpr uint32_t kLayoutTile = 2;
 
 // NT: 8-token MMA tiles per item; MI: 16-row tiles per consumer warp (the
 // item's 128 rows are split over 8 / MI consumer warps).
@@ -186,7 +185,12 @@ __device__ __forceinline__ bool consume_item(const GemmArgs& a, uint8_t* smem, u
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 if (p[u] < 0) continue;
-                if (a.out_f32) {
+                if (a.silu) {
+                    // packed rows n0 = 16k + g and n0 + 8 hold gate and up of
+                    // column j = 8k + g (layout 3)
+                    __nv_bfloat16* hrow = static_cast<__nv_bfloat16*>(a.C) + (int64_t)p[u] * (a.N / 2);
+                    hrow[8 * (n0 / 16) + g] = silu_mul_bf16(acc[mi][t][u], acc[mi][t][2 + u]);
+                } else if (a.out_f32) {
                     float* crow = static_cast<float*>(a.C) + (int64_t)p[u] * a.N;
                     crow[n0] = acc[mi][t][u];
                     crow[n0 + 8] = acc[mi][t][2 + u];
@@ -213,7 +217,7 @@ __global__ void __launch_bounds__(Cfg<NT, MI>::kThreads, MINB) gemm_decode_kerne
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        const bool ok = header_ok_layout(a.packed, a.E, a.N, a.K, kLayoutTile);
+        const bool ok = header_ok_layout(a.packed, a.E, a.N, a.K, a.layout);
         if (!ok) set_error(a.err, CHORD_DEV_BAD_HEADER);
         flags[0] = ok ? 0 : 1;
         flags[1] = 0;

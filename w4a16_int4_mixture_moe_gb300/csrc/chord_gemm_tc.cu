@@ -37,7 +37,6 @@ constexpr int kTileRows = 128;   // rows of N per item = MMA M
 constexpr int kChunkK = 64;      // K columns of one packed chunk; a pipeline stage holds two
 constexpr int kChunk2 = 4608;    // packed bytes of one 128 x 64 chunk (layout 2)
 constexpr int kACols = 64;       // tensor-memory columns of one A stage (128 bf16 per lane)
-constexpr uint32_t kLayoutTc = 2;
 
 // The A operand ring lives in tensor memory (64 columns per stage, as many
 // stages as the columns left after the accumulators allow, sized at launch);
@@ -252,7 +251,7 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        const bool ok = header_ok_layout(a.packed, a.E, a.N, a.K, kLayoutTc);
+        const bool ok = header_ok_layout(a.packed, a.E, a.N, a.K, a.layout);
         if (!ok) set_error(a.err, CHORD_DEV_BAD_HEADER);
         flags[0] = ok ? 0 : 1;
         flags[1] = 0;
@@ -514,6 +513,10 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
             }
             tc_fence_after();
             const int n_out = nt * kTileRows + row;
+            // fused SiLU * up (layout 3): rows 16k + i (i < 8) and 16k + i + 8 of
+            // the tile hold gate and up of output column 64 * nt + 8k + i
+            const int h_col = nt * (kTileRows / 2) + 8 * (row / 16) + (row % 8);
+            const bool gate_row = (lane & 8) == 0;
             const int parts = kstages < NI ? kstages : NI;   // issuers that hold a share of this item
 #pragma unroll
             for (int it = 0; it < 8; ++it) {
@@ -532,9 +535,23 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
                 tc_wait_ld();
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
+                    if (a.silu) {
+                        // lanes l (gate row) and l ^ 8 (its up row) split the 16
+                        // tokens: the gate lane takes tokens 0-7, the up lane 8-15,
+                        // each receiving the partner's value for its tokens
+                        if (u >= 8) break;
+                        const int tok = gate_row ? u : 8 + u;
+                        const float mine = __uint_as_float(v[tok]);
+                        const float other = __shfl_xor_sync(0xffffffffu, __uint_as_float(v[gate_row ? 8 + u : u]), 8);
+                        const int32_t id = __shfl_sync(0xffffffffu, pre[it >> 1], tok + 16 * (it & 1));
+                        if (id >= 0)
+                            static_cast<__nv_bfloat16*>(a.C)[(int64_t)id * (a.N / 2) + h_col] =
+                                gate_row ? silu_mul_bf16(mine, other) : silu_mul_bf16(other, mine);
+                        continue;
+                    }
                     const int32_t id = __shfl_sync(0xffffffffu, pre[it >> 1], u + 16 * (it & 1));
-                    if (id < 0) continue;
                     const float val = __uint_as_float(v[u]);
+                    if (id < 0) continue;
                     if (a.out_f32)
                         static_cast<float*>(a.C)[(int64_t)id * a.N + n_out] = val;
                     else

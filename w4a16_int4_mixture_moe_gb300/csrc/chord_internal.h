@@ -44,8 +44,10 @@ struct GemmArgs {
     int block_m;
     int64_t num_pairs;
     int64_t id_limit;   // pair ids below this are valid rows: min(num_pairs, a_rows * a_row_divisor)
-    void* C;        // bf16 [num_pairs, N], or float when out_f32
+    void* C;        // bf16 [num_pairs, N], or float when out_f32; bf16 [num_pairs, N/2] when silu
     int out_f32;
+    uint32_t layout;   // packed layout the header must name: 2, or 3 with silu
+    int silu;          // fused SiLU * up epilogue (rows interleaved gate/up by 8)
     int* err;
 };
 
