@@ -85,6 +85,8 @@ def lib():
                                          i32p, i32p, ctypes.c_int32, c_int, c_i64, u16p, c_int]),
                 "orc_moe_gemm_f32": (c_int, [u16p, c_i64, c_int, u8p, u16p, c_int, c_int, c_int,
                                              i32p, i32p, ctypes.c_int32, c_int, c_i64, f32p, c_int]),
+                "orc_grouped_contiguous": (c_int, [u16p, c_i64, i32p, u8p, u16p, c_int, c_int, c_int, u16p, c_int]),
+                "orc_grouped_masked": (c_int, [u16p, c_int, c_int, i32p, u8p, u16p, c_int, c_int, u16p, c_int]),
                 "orc_silu_mul": (c_int, [u16p, i32p, c_i64, c_int, c_int, u16p, c_int]),
                 "orc_combine": (c_int, [u16p, i32p, f32p, c_int, c_int, c_int, c_int, u16p, c_int]),
                 "orc_combine_f32": (c_int, [f32p, i32p, f32p, c_int, c_int, c_int, c_int, u16p, c_int]),
@@ -214,6 +216,40 @@ def moe_gemm(A: np.ndarray, a_row_divisor: int, codes: np.ndarray, scales: np.nd
                               _ptr(sorted_ids, ctypes.c_int32), _ptr(expert_ids, ctypes.c_int32),
                               num_tokens_padded, block_m, num_pairs, _ptr(C, ctypes.c_uint16),
                               threads(nthreads)), "moe_gemm")
+    return C
+
+
+def grouped_contiguous(A: np.ndarray, m_indices: np.ndarray, codes: np.ndarray, scales: np.ndarray,
+                       C: np.ndarray = None, nthreads=None) -> np.ndarray:
+    """bf16 bits [M, N]: rows of A grouped per expert, m_indices[m] its expert (-1: padding, not written)."""
+    A = _c(A, np.uint16)
+    m_indices = _c(m_indices, np.int32)
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.uint16)
+    E, N, K = codes.shape
+    M = A.shape[0]
+    assert A.shape[1] == K and m_indices.shape == (M,)
+    C = _c(np.zeros((M, N), np.uint16) if C is None else C, np.uint16)
+    _check(lib().orc_grouped_contiguous(_ptr(A, ctypes.c_uint16), M, _ptr(m_indices, ctypes.c_int32),
+                                        _ptr(codes, ctypes.c_uint8), _ptr(scales, ctypes.c_uint16), E, N, K,
+                                        _ptr(C, ctypes.c_uint16), threads(nthreads)), "orc_grouped_contiguous")
+    return C
+
+
+def grouped_masked(A: np.ndarray, masked_m: np.ndarray, codes: np.ndarray, scales: np.ndarray,
+                   C: np.ndarray = None, nthreads=None) -> np.ndarray:
+    """bf16 bits [G * max_m, N] from A [G, max_m, K]; rows past masked_m[g] are not written."""
+    A = _c(A, np.uint16)
+    masked_m = _c(masked_m, np.int32)
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.uint16)
+    G, max_m, K = A.shape
+    E, N, K2 = codes.shape
+    assert K2 == K and E == G and masked_m.shape == (G,)
+    C = _c(np.zeros((G * max_m, N), np.uint16) if C is None else C, np.uint16)
+    _check(lib().orc_grouped_masked(_ptr(A, ctypes.c_uint16), G, max_m, _ptr(masked_m, ctypes.c_int32),
+                                    _ptr(codes, ctypes.c_uint8), _ptr(scales, ctypes.c_uint16), N, K,
+                                    _ptr(C, ctypes.c_uint16), threads(nthreads)), "orc_grouped_masked")
     return C
 
 

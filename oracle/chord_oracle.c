@@ -473,6 +473,94 @@ int orc_moe_gemm_f32(const uint16_t *A, int64_t a_rows, int a_row_divisor,
 }
 
 /* ------------------------------------------------------------------------ */
+/* Grouped contracts (the article's "Grouped SM90 kernels" section: a second
+ * routing workload besides the indexed one).
+ *
+ * Contiguous (prefill): the rows of A [M, K] are concatenated per expert, each
+ * expert's segment padded to a multiple of 128 rows; m_indices[m] is the
+ * expert of row m, -1 on padding rows.
+ *     C[m, n] = bf16_rne( sum_k A[m, k] * w[m_indices[m], n, k] )   (m_indices[m] >= 0)
+ * Padding rows of C are not written.
+ *
+ * Masked (decode): A [G, max_m, K] holds a fixed row budget per group (expert)
+ * g, of which the first masked_m[g] rows are valid; C is flat [G * max_m, N].
+ *     C[g * max_m + r, n] = bf16_rne( sum_k A[g, r, k] * w[g, n, k] )   (r < masked_m[g])
+ * Rows past a group's count are not written.
+ *
+ * Same dequantisation and sequential FP32 sum in ascending k as the indexed
+ * GEMM. */
+static void rows_times_expert(const uint16_t *A, const int64_t *rows, int64_t nr, const float *wq, int N, int K,
+                              uint16_t *C, int nthreads)
+{
+#pragma omp parallel for num_threads(nthreads) schedule(static) collapse(2)
+    for (int64_t r = 0; r < nr; ++r)
+        for (int n = 0; n < N; ++n) {
+            const uint16_t *a = A + (size_t)rows[r] * (size_t)K;
+            const float *w = wq + (size_t)n * K;
+            float acc = 0.0f;
+            for (int k = 0; k < K; ++k)
+                acc += f32_from_bf16(a[k]) * w[k];
+            C[(size_t)rows[r] * N + n] = bf16_from_f32(acc);
+        }
+}
+
+int orc_grouped_contiguous(const uint16_t *A, int64_t M, const int32_t *m_indices, const uint8_t *codes,
+                           const uint16_t *scales, int E, int N, int K, uint16_t *C, int nthreads)
+{
+    if (M < 0 || N <= 0 || K <= 0 || K % ORC_GROUP || E <= 0)
+        return ORC_EINVAL;
+    for (int64_t m = 0; m < M; ++m)
+        if (m_indices[m] < -1 || m_indices[m] >= E)
+            return ORC_ERANGE;
+    float *wq = (float *)malloc((size_t)N * (size_t)K * sizeof(float));
+    int64_t *rows = (int64_t *)malloc((size_t)(M > 0 ? M : 1) * sizeof(int64_t));
+    if (!wq || !rows) {
+        free(wq); free(rows);
+        return ORC_ENOMEM;
+    }
+    for (int e = 0; e < E; ++e) {
+        int64_t nr = 0;
+        for (int64_t m = 0; m < M; ++m)
+            if (m_indices[m] == e)
+                rows[nr++] = m;
+        if (nr == 0)
+            continue;
+        dequant_expert(codes, scales, e, N, K, wq, nthreads);
+        rows_times_expert(A, rows, nr, wq, N, K, C, nthreads);
+    }
+    free(wq);
+    free(rows);
+    return ORC_OK;
+}
+
+int orc_grouped_masked(const uint16_t *A, int G, int max_m, const int32_t *masked_m, const uint8_t *codes,
+                       const uint16_t *scales, int N, int K, uint16_t *C, int nthreads)
+{
+    if (G <= 0 || max_m < 0 || N <= 0 || K <= 0 || K % ORC_GROUP)
+        return ORC_EINVAL;
+    for (int g = 0; g < G; ++g)
+        if (masked_m[g] < 0 || masked_m[g] > max_m)
+            return ORC_ERANGE;
+    float *wq = (float *)malloc((size_t)N * (size_t)K * sizeof(float));
+    int64_t *rows = (int64_t *)malloc((size_t)(max_m > 0 ? max_m : 1) * sizeof(int64_t));
+    if (!wq || !rows) {
+        free(wq); free(rows);
+        return ORC_ENOMEM;
+    }
+    for (int g = 0; g < G; ++g) {
+        if (masked_m[g] == 0)
+            continue;
+        for (int r = 0; r < masked_m[g]; ++r)
+            rows[r] = (int64_t)g * max_m + r;
+        dequant_expert(codes, scales, g, N, K, wq, nthreads);
+        rows_times_expert(A, rows, masked_m[g], wq, N, K, C, nthreads);
+    }
+    free(wq);
+    free(rows);
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
 /* SiLU * up.  C1 holds 2I columns per pair: gate in 0..I-1, up in I..2I-1
  * (the usual concatenation of w1 and w3; the article does not show it).
  *     h[p, j] = bf16_rne( (g / (1 + exp(-g))) * u ),  g = C1[p, j], u = C1[p, I + j]

@@ -26,7 +26,10 @@ MUTANTS = [
     ("scale_slot", "+ (size_t)(h * 8 + g) * 4u + (size_t)lower * 2u;", "+ (size_t)(g * 2 + h) * 4u + (size_t)lower * 2u;"),
     ("align_descending", "for (int64_t p = 0; p < P; ++p)\n            if (topk_ids[p] == e)",
      "for (int64_t p = P - 1; p >= 0; --p)\n            if (topk_ids[p] == e)"),
-    ("gemm_k_shift", "acc += f32_from_bf16(a[k]) * w[k];", "acc += f32_from_bf16(a[k]) * w[(k + 1) % K];"),
+    ("gemm_k_shift", "                    acc += f32_from_bf16(a[k]) * w[k];",
+     "                    acc += f32_from_bf16(a[k]) * w[(k + 1) % K];"),
+    ("grouped_k_shift", "\n                acc += f32_from_bf16(a[k]) * w[k];",
+     "\n                acc += f32_from_bf16(a[k]) * w[(k + 1) % K];"),
     ("gemm_row_mod", "const uint16_t *a = A + (size_t)(p / a_row_divisor) * (size_t)K;",
      "const uint16_t *a = A + (size_t)(p % a_row_divisor) * (size_t)K;"),
     ("gemm_group_64", "uint16_t s = scales[((size_t)e * N + n) * G + k / ORC_GROUP];",
@@ -41,6 +44,9 @@ MUTANTS = [
      "float g = f32_from_bf16(C1[(size_t)p * 2 * I + I + j]);"),
     ("interleave_up_first", "return 16 * (m / 8) + 8 + m % 8;", "return 16 * (m / 8) + m % 8 - 8 * (m % 8 > 7);"),
     ("interleave_by_16", "return 16 * (n / 8) + n % 8;", "return 16 * (n / 16) + n % 16;"),
+    ("contiguous_takes_padding", "if (m_indices[m] == e)\n                rows[nr++] = m;",
+     "if (m_indices[m] == e || m_indices[m] == -1)\n                rows[nr++] = m;"),
+    ("masked_row_stride", "rows[r] = (int64_t)g * max_m + r;", "rows[r] = (int64_t)g * masked_m[g] + r;"),
     ("combine_nonlocal", "if (topk_ids[p] < 0 || topk_ids[p] >= E)\n                    continue;\n                float v",
      "if (topk_ids[p] >= E)\n                    continue;\n                float v"),
 ]

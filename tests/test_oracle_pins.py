@@ -317,6 +317,74 @@ def test_gemm_exact_integer_regime(orc, K):
         np.testing.assert_array_equal(C[p], to_bf16(exact.astype(np.float32)))
 
 
+def test_grouped_contiguous_exact_integer_and_padding(orc):
+    """Grouped contiguous: x in {-1,0,1}, scale 1, against numpy's integer
+    matmul row by row with the row's own expert; padding rows (m_indices -1)
+    keep the fill pattern.  Segments of 128 rows per expert, one expert empty."""
+    K, N, E = 256, 48, 4
+    counts = [70, 0, 128, 5]
+    m_idx = np.concatenate([np.concatenate([np.full(c, e), np.full(-(-c // 128) * 128 - c, -1)])
+                            for e, c in enumerate(counts)]).astype(np.int32)
+    M = m_idx.size
+    rng = np.random.default_rng(7)
+    xi = rng.integers(-1, 2, size=(M, K))
+    x = to_bf16(xi.astype(np.float32))
+    codes = wl.random_codes(8, (E, N, K))
+    scales = np.full((E, N, K // GROUP), 0x3F80, np.uint16)
+    C = orc.grouped_contiguous(x, m_idx, codes, scales, C=np.full((M, N), 0xFFFF, np.uint16))
+    Wi = codes.astype(np.int64) - 8
+    for m in range(M):
+        if m_idx[m] < 0:
+            assert (C[m] == 0xFFFF).all(), m
+        else:
+            np.testing.assert_array_equal(C[m], to_bf16((Wi[m_idx[m]] @ xi[m]).astype(np.float32)))
+
+
+def test_grouped_masked_exact_integer_and_budget(orc):
+    """Grouped masked: group g's first masked_m[g] rows against numpy's integer
+    matmul with expert g (flat output row g * max_m + r); rows past the count
+    keep the fill pattern, including a group with no rows and a full one."""
+    K, N, G, max_m = 128, 32, 4, 9
+    masked_m = np.array([3, 0, 9, 1], np.int32)
+    rng = np.random.default_rng(9)
+    xi = rng.integers(-1, 2, size=(G, max_m, K))
+    x = to_bf16(xi.astype(np.float32))
+    codes = wl.random_codes(10, (G, N, K))
+    scales = np.full((G, N, K // GROUP), 0x3F80, np.uint16)
+    C = orc.grouped_masked(x, masked_m, codes, scales, C=np.full((G * max_m, N), 0xFFFF, np.uint16))
+    Wi = codes.astype(np.int64) - 8
+    for g in range(G):
+        for r in range(max_m):
+            row = C[g * max_m + r]
+            if r >= masked_m[g]:
+                assert (row == 0xFFFF).all(), (g, r)
+            else:
+                np.testing.assert_array_equal(row, to_bf16((Wi[g] @ xi[g, r]).astype(np.float32)))
+
+
+def test_grouped_contracts_match_indexed_gemm(orc):
+    """With real-valued data both grouped contracts equal the indexed GEMM given
+    the equivalent routing (one row per pair, block size 8), bit for bit: same
+    dequantisation, same sequential sums."""
+    K, N, E = 320, 64, 3
+    codes = wl.random_codes(11, (E, N, K))
+    scales = wl.random_scales(12, (E, N, K // GROUP))
+    m_idx = np.array([0] * 5 + [-1] * 3 + [2] * 8 + [1] * 2 + [-1] * 6, np.int32)
+    x = wl.random_bf16(13, (m_idx.size, K))
+    got = orc.grouped_contiguous(x, m_idx, codes, scales)
+    ids = m_idx.reshape(-1, 1)
+    want = _gemm_via_align(orc, x, 1, codes, scales, ids)
+    rows = m_idx >= 0
+    np.testing.assert_array_equal(got[rows], want[rows])
+    masked_m = np.array([4, 0, 7], np.int32)
+    x3 = wl.random_bf16(14, (E, 7, K))
+    got3 = orc.grouped_masked(x3, masked_m, codes, scales)
+    ids3 = np.array([[g if r < masked_m[g] else -1] for g in range(E) for r in range(7)], np.int32)
+    want3 = _gemm_via_align(orc, x3.reshape(-1, K), 1, codes, scales, ids3)
+    rows3 = ids3.ravel() >= 0
+    np.testing.assert_array_equal(got3[rows3], want3[rows3])
+
+
 def test_gemm_identity(orc):
     """Code 9 on the diagonal, 8 elsewhere, scale 1: W = I, so C = x exactly."""
     T, topk, E, K = 5, 2, 2, 64
