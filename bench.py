@@ -276,12 +276,145 @@ def run_reference(args, w):
 
 # ------------------------------------------------------------------- GPU arm
 
+GROUPED = {
+    # the grouped contracts on the EP8 shapes: contiguous segments of the
+    # prefill routing's per-expert row counts (padded to 128 rows), and masked
+    # budgets of 32 rows holding the decode routing's counts
+    "grouped_contiguous_ep8_prefill": ("contiguous", wl.EP8_PREFILL),
+    "grouped_masked_ep8_decode": ("masked", wl.EP8_DECODE),
+}
+
+
+def run_grouped(args, name):
+    """gate_up then down through one grouped contract; value = their µs sum
+    (the pages' grouped rows time gate_up + down)."""
+    import torch
+    import w4a16_int4_mixture_moe_gb300 as chord
+    contract, w = GROUPED[name]
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    chord.build()
+    chord.load()
+    ids, _ = wl.make_routing(w)
+    counts = routing_stats(ids, w.E)
+    E, H, I = w.E, w.H, w.I
+    rng = np.random.default_rng(w.seed + 100)
+    if contract == "contiguous":
+        m_idx = np.concatenate([np.concatenate([np.full(c, e), np.full(-(-c // 128) * 128 - c, -1)])
+                                for e, c in enumerate(counts)]).astype(np.int32)
+        rows_a = m_idx.size
+        idx_h = torch.from_numpy(m_idx)
+        ws1 = chord.chord_grouped_contiguous_workspace_bytes(rows_a, E)
+        shape_a, max_m, expected_m = (rows_a,), 0, 0
+    else:
+        max_m = 32
+        expected_m = max(1, int(round(counts.mean())))
+        masked = np.minimum(counts, max_m).astype(np.int32)
+        rows_a = E * max_m
+        idx_h = torch.from_numpy(masked)
+        ws1 = chord.chord_grouped_masked_workspace_bytes(E, max_m, expected_m)
+        shape_a = (E, max_m)
+    x = torch.from_numpy(wl._bf16(rng.standard_normal((rows_a, H), dtype=np.float32)).view(np.int16))
+    x = x.view(torch.bfloat16).to(dev).reshape(*shape_a, H)
+    hmid = torch.randn((rows_a, I), device=dev).to(torch.bfloat16).reshape(*shape_a, I)
+    c13, s13 = wl.make_w13(w)
+    p13 = torch.empty(chord.chord_packed_weight_bytes(E, 2 * I, H), dtype=torch.uint8, device=dev)
+    chord.chord_pack_weights(torch.from_numpy(c13).to(dev), torch.from_numpy(s13.view(np.int16)).to(dev).view(torch.bfloat16), p13)
+    del c13, s13
+    c2, s2 = wl.make_w2(w)
+    p2 = torch.empty(chord.chord_packed_weight_bytes(E, H, I), dtype=torch.uint8, device=dev)
+    chord.chord_pack_weights(torch.from_numpy(c2).to(dev), torch.from_numpy(s2.view(np.int16)).to(dev).view(torch.bfloat16), p2)
+    del c2, s2
+    idx = idx_h.to(dev)
+    ws = torch.empty(max(ws1, 16), dtype=torch.uint8, device=dev)
+    C1 = torch.empty((rows_a, 2 * I), dtype=torch.bfloat16, device=dev)
+    C2 = torch.empty((rows_a, H), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def gemm(A, p, N, K, C):
+        if contract == "contiguous":
+            chord.chord_grouped_contiguous_gemm(A, idx, p, E, N, K, C, ws, stream=stream)
+        else:
+            chord.chord_grouped_masked_gemm(A, idx, expected_m, p, N, K, C, ws, stream=stream)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        gemm(x, p13, 2 * I, H, C1)
+        if ev:
+            ev[1].record(stream)
+        gemm(hmid, p2, H, I, C2)
+        if ev:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(gpu_id_for(torch, 0))
+    sampler.start()
+    t_lo = time.time()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    g1 = g2 = 0.0
+    for _ in range(args.steps):
+        step(ev)
+        torch.cuda.synchronize()
+        g1 += ev[0].elapsed_time(ev[1])
+        g2 += ev[1].elapsed_time(ev[2])
+    t_hi = time.time()
+    sampler.stop()
+    g1, g2 = g1 / args.steps, g2 / args.steps
+    # end to end: activations and indices from pinned host memory, outputs back
+    x_h, idx_p = x.cpu().pin_memory(), idx_h.pin_memory()
+    out_h = torch.empty_like(C2, device="cpu").pin_memory()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(args.steps):
+        x.copy_(x_h, non_blocking=True)
+        idx.copy_(idx_p, non_blocking=True)
+        step()
+        out_h.copy_(C2, non_blocking=True)
+    f1.record(stream)
+    torch.cuda.synchronize()
+    e2e_us = f0.elapsed_time(f1) * 1e3 / args.steps
+    peaks = load_peaks()
+    b1, f1_ = gemm_algorithmic(counts, 2 * I, H)
+    ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    bmg = (chord.chord_select_block_m(rows_a, 1, E, E, 2 * I, H) if contract == "contiguous" else
+           chord.chord_select_block_m(expected_m, 1, 1, 1, 2 * I, H))
+    kind = "warp_mma" if chord.chord_select_kernel(bmg, 2 * I, H) == chord.KERNEL_WARP_MMA else "tc"
+    if f1_ / b1 < ridge:
+        ach = b1 / (g1 * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": None,
+                "kernel": KERNEL_NAME[kind] + " (gate_up)", "peak_src": peaks["src"]}
+    else:
+        ach = f1_ / (g1 * 1e-3) / 1e12
+        pk = peaks["bf16_tflops_sustained"]
+        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": pk, "unit": "TFLOP/s",
+                "frac": round(ach / pk, 4), "traffic": None,
+                "kernel": KERNEL_NAME[kind] + " (gate_up)", "peak_src": peaks["src"]}
+    cfg = {"workload": name, "contract": contract, "E": E, "H": H, "I": I, "rows": int(counts.sum()),
+           "rows_with_padding": rows_a, "max_m": max_m or None, "expected_m": expected_m or None, "block_m": bmg,
+           "parallelism": "ep-replica x1",
+           "l2": "inputs larger than L2: packed weights streamed per step exceed the 129 MB L2"}
+    line = {"metric": "W4A16 MoE grouped gate_up + down µs/call", "value": round((g1 + g2) * 1e3, 2), "unit": UNIT,
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(g1 + g2, 4),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": cfg,
+            "gemm_us": {"gate_up": round(g1 * 1e3, 2), "down": round(g2 * 1e3, 2)},
+            "roofline": roof, "clocks": sampler.summary(t_lo, t_hi),
+            "e2e": {"value": round(e2e_us, 2), "unit": UNIT, "h2d_bytes_per_step": x.numel() * 2 + idx.numel() * 4,
+                    "d2h_bytes_per_step": C2.numel() * 2},
+            "gpu_launches": 4 * args.steps}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="ep8_decode", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="ep8_decode", choices=sorted(WORKLOADS) + sorted(GROUPED))
     ap.add_argument("--impl", default="chord", choices=["chord", "reference"])
     ap.add_argument("--block-m", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -289,6 +422,11 @@ def main():
     ap.add_argument("--fused", action="store_true", help="SiLU * up in the gate_up epilogue on either kernel")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()
+    if args.workload in GROUPED:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the grouped workloads have no oracle arm"}))
+            return
+        return run_grouped(args, args.workload)
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)

@@ -259,6 +259,42 @@ chord_status chord_w4a16_moe_gemm(const void *A, int64_t a_rows, int a_row_divis
                                   void *workspace, size_t workspace_bytes,
                                   const chord_opts *opts, void *stream);
 
+/* --------------------------------------------------------- grouped GEMMs */
+
+/* The article's two grouped contracts ("Grouped SM90 kernels"), served by the
+ * same kernels through routing arrays built on the device (one row per pair).
+ * Weights are packed as for chord_w4a16_moe_gemm (CHORD_LAYOUT_TCGEN05); the
+ * epilogue, out_dtype and kernel options apply as there.
+ *
+ * Contiguous (prefill): A [M, K] holds each expert's rows contiguously (the
+ * article pads each expert's segment to a multiple of 128 rows); m_indices[m]
+ * (device int32 [M]) is row m's expert, -1 on padding rows.
+ *   C[m, n] = bf16_rne( sum_k A[m, k] * w[m_indices[m], n, k] )  for m_indices[m] >= 0
+ * into C [M, N] (or [M, N/2] with the SiLU * up epilogue); padding rows are not
+ * written.  An expert whose rows are not one contiguous run sets
+ * CHORD_DEV_BAD_ROW, an id outside [-1, E) CHORD_DEV_BAD_EXPERT.  The block
+ * size follows M / E as tok_e does.  E <= 4000.
+ * workspace >= chord_grouped_contiguous_workspace_bytes(M, E). */
+size_t chord_grouped_contiguous_workspace_bytes(int64_t M, int E);
+chord_status chord_grouped_contiguous_gemm(const void *A, int64_t M, const int32_t *m_indices,
+                                           const void *packed, size_t packed_bytes, int E, int N, int K,
+                                           void *C, void *workspace, size_t workspace_bytes,
+                                           const chord_opts *opts, void *stream);
+
+/* Masked (decode): A [G, max_m, K] gives expert g a budget of max_m rows, of
+ * which the first masked_m[g] (device int32 [G]) are valid; C is flat
+ * [G * max_m, N] (or [G * max_m, N/2] with the SiLU * up epilogue):
+ *   C[g * max_m + r, n] = bf16_rne( sum_k A[g, r, k] * w[g, n, k] )  for r < masked_m[g]
+ * rows past a group's count are not written.  expected_m (> 0, a host value)
+ * is the typical count; it picks the block size as tok_e does for the indexed
+ * contract.  A count outside [0, max_m] sets CHORD_DEV_BAD_ROW (and is clamped).
+ * G <= 4000.  workspace >= chord_grouped_masked_workspace_bytes(G, max_m, expected_m). */
+size_t chord_grouped_masked_workspace_bytes(int G, int max_m, int expected_m);
+chord_status chord_grouped_masked_gemm(const void *A, int G, int max_m, const int32_t *masked_m, int expected_m,
+                                       const void *packed, size_t packed_bytes, int N, int K, void *C,
+                                       void *workspace, size_t workspace_bytes, const chord_opts *opts,
+                                       void *stream);
+
 /* ------------------------------------------------------------- epilogues */
 
 /* SiLU * up on the gate_up output:

@@ -105,6 +105,35 @@ def test_select_kernel_by_regime(lib, monkeypatch):
     assert chord.chord_select_kernel(256, 4096, 7168) == T
 
 
+def test_grouped_workspace_and_argument_errors(lib):
+    """Grouped contracts: workspace = sorted ids + expert ids + padded count,
+    each 256-byte aligned; bad arguments are refused before any launch."""
+    up = lambda x: (x + 255) // 256 * 256
+    for M, E in ((0, 4), (1, 1), (128, 2), (12288, 48)):
+        bmc = chord.chord_select_block_m(M, 1, E, E, 0, 0)
+        cap = (-(-M // bmc) + E) * bmc
+        assert chord.chord_grouped_contiguous_workspace_bytes(M, E) == up(up(up(cap * 4) + cap // bmc * 4) + 4)
+    assert chord.chord_grouped_contiguous_workspace_bytes(128, 5000) == 0
+    G, max_m, em = 48, 40, 11
+    bm = chord.chord_select_block_m(em, 1, 1, 1, 4096, 7168)
+    cap = G * -(-max_m // bm) * bm
+    assert chord.chord_grouped_masked_workspace_bytes(G, max_m, em) == up(up(up(cap * 4) + cap // bm * 4) + 4)
+    assert chord.chord_grouped_masked_workspace_bytes(0, 8, 4) == 0
+    vp = ctypes.c_void_p
+    big = vp(1 << 20)
+    # contiguous: workspace too small, negative M
+    assert lib.chord_grouped_contiguous_gemm(big, 256, big, big, 10 ** 6, 2, 128, 64, big, big, 16, None,
+                                             None) == 4
+    assert lib.chord_grouped_contiguous_gemm(big, -1, big, big, 10 ** 6, 2, 128, 64, big, big, 10 ** 6, None,
+                                             None) == 1
+    # masked: expected_m <= 0, too many groups, workspace too small
+    assert lib.chord_grouped_masked_gemm(big, 4, 8, big, 0, big, 10 ** 6, 128, 64, big, big, 10 ** 6, None,
+                                         None) == 1
+    assert lib.chord_grouped_masked_gemm(big, 4001, 8, big, 4, big, 10 ** 6, 128, 64, big, big, 10 ** 6, None,
+                                         None) == 2
+    assert lib.chord_grouped_masked_gemm(big, 4, 8, big, 4, big, 10 ** 6, 128, 64, big, big, 8, None, None) == 4
+
+
 def test_layer_workspace_formula(lib):
     T, topk, E, H, I, bm = 512, 8, 48, 7168, 2048, 16
     P = T * topk

@@ -345,6 +345,84 @@ def test_fused_silu_mul_needs_layout3_and_vice_versa():
             assert (host_bits(C) == 0xFFFF).all()
 
 
+# ----------------------------------------------------------- grouped GEMMs
+
+def contiguous_rows(counts):
+    """m_indices of experts' segments padded to 128-row multiples."""
+    return np.concatenate([np.concatenate([np.full(c, e), np.full(-(-c // 128) * 128 - c, -1)])
+                           for e, c in enumerate(counts)]).astype(np.int32)
+
+
+@BOTH
+@pytest.mark.parametrize("counts", [[70, 0, 128, 5], [1, 200, 33], [128, 128]])
+@pytest.mark.parametrize("NK", [(256, 320), (128, 1024)])
+def test_grouped_contiguous_vs_oracle(kernel, counts, NK):
+    N, K = NK
+    E = len(counts)
+    m_idx = contiguous_rows(counts)
+    M = m_idx.size
+    seed = sum(counts) + N + K
+    x = wl.random_bf16(seed, (M, K))
+    codes, scales = wl.random_codes(seed + 1, (E, N, K)), wl.random_scales(seed + 2, (E, N, K // 32))
+    ws = torch.empty(chord.chord_grouped_contiguous_workspace_bytes(M, E), dtype=torch.uint8, device=DEV)
+    C = torch.full((M, N), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+    chord.chord_grouped_contiguous_gemm(dbf(x), dev(m_idx), pack(codes, scales), E, N, K, C, ws,
+                                        opts=chord.ChordOpts(kernel=KERNELS[kernel][0]))
+    ref = oracle.grouped_contiguous(x, m_idx, codes, scales, C=np.full((M, N), 0xFFFF, np.uint16))
+    got = host_bits(C)
+    assert (got[m_idx < 0] == 0xFFFF).all(), "padding rows were written"
+    assert_close(got[m_idx >= 0], ref[m_idx >= 0], f"{kernel} grouped contiguous {counts} N={N} K={K}")
+
+
+def test_grouped_contiguous_split_expert_is_reported():
+    """An expert whose rows are not one contiguous run breaks the contract: the
+    device error word says so (validate mode turns it into a status)."""
+    E, N, K = 2, 128, 64
+    m_idx = np.array([0] * 60 + [1] * 40 + [0] * 28, np.int32)
+    x = wl.random_bf16(1, (128, K))
+    codes, scales = wl.random_codes(2, (E, N, K)), wl.random_scales(3, (E, N, K // 32))
+    ws = torch.empty(chord.chord_grouped_contiguous_workspace_bytes(128, E), dtype=torch.uint8, device=DEV)
+    C = torch.empty((128, N), dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(chord.ChordError) as ei:
+        chord.chord_grouped_contiguous_gemm(dbf(x), dev(m_idx), pack(codes, scales), E, N, K, C, ws,
+                                            opts=chord.ChordOpts(validate=1))
+    assert ei.value.status == 6
+
+
+@BOTH
+@pytest.mark.parametrize("masked,max_m,expected_m", [([3, 0, 9, 1], 9, 4), ([17, 40, 2, 33, 0, 64], 64, 20),
+                                                     ([200, 5, 256], 256, 150)])
+def test_grouped_masked_vs_oracle(kernel, masked, max_m, expected_m):
+    N, K = 256, 512
+    G = len(masked)
+    masked_m = np.array(masked, np.int32)
+    seed = sum(masked) + max_m
+    x = wl.random_bf16(seed, (G, max_m, K))
+    codes, scales = wl.random_codes(seed + 1, (G, N, K)), wl.random_scales(seed + 2, (G, N, K // 32))
+    ws = torch.empty(chord.chord_grouped_masked_workspace_bytes(G, max_m, expected_m), dtype=torch.uint8,
+                     device=DEV)
+    C = torch.full((G * max_m, N), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+    chord.chord_grouped_masked_gemm(dbf(x), dev(masked_m), expected_m, pack(codes, scales), N, K, C, ws,
+                                    opts=chord.ChordOpts(kernel=KERNELS[kernel][0]))
+    ref = oracle.grouped_masked(x, masked_m, codes, scales, C=np.full((G * max_m, N), 0xFFFF, np.uint16))
+    got = host_bits(C)
+    valid = np.array([r < masked[g] for g in range(G) for r in range(max_m)])
+    assert (got[~valid] == 0xFFFF).all(), "rows past a group's count were written"
+    assert_close(got[valid], ref[valid], f"{kernel} grouped masked {masked} max_m={max_m}")
+
+
+def test_grouped_masked_count_out_of_range_is_reported():
+    G, max_m, N, K = 2, 8, 128, 64
+    x = wl.random_bf16(1, (G, max_m, K))
+    codes, scales = wl.random_codes(2, (G, N, K)), wl.random_scales(3, (G, N, K // 32))
+    ws = torch.empty(chord.chord_grouped_masked_workspace_bytes(G, max_m, 4), dtype=torch.uint8, device=DEV)
+    C = torch.empty((G * max_m, N), dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(chord.ChordError) as ei:
+        chord.chord_grouped_masked_gemm(dbf(x), dev(np.array([3, 9], np.int32)), 4, pack(codes, scales), N, K, C,
+                                        ws, opts=chord.ChordOpts(validate=1))
+    assert ei.value.status == 6
+
+
 # ---------------------------------------------------------------- epilogues
 
 def test_silu_mul_vs_oracle():

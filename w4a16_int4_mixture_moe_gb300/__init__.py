@@ -20,6 +20,8 @@ __all__ = [
     "chord_align_capacity", "chord_align_workspace_bytes", "chord_moe_align", "chord_select_block_m", "chord_select_kernel",
     "chord_gemm_workspace_bytes", "chord_w4a16_moe_gemm", "chord_silu_mul", "chord_moe_combine",
     "chord_layer_workspace_bytes", "chord_moe_layer", "chord_get_device_error",
+    "chord_grouped_contiguous_workspace_bytes", "chord_grouped_contiguous_gemm",
+    "chord_grouped_masked_workspace_bytes", "chord_grouped_masked_gemm",
     "KERNEL_AUTO", "KERNEL_TCGEN05", "KERNEL_WARP_MMA", "LAYOUT_WARP_MMA", "LAYOUT_TCGEN05",
     "DTYPE_BF16", "DTYPE_F32",
 ]
@@ -70,6 +72,11 @@ _SIGS = {
     "chord_moe_layer": (_int, [_vp, _vp, _vp, _int, _int, _int, _int, _int, _int, _vp, _sz, _vp, _sz, _int, _vp,
                                _sz, _vp, _OPTS, _vp]),
     "chord_get_device_error": (_int, [_vp, ctypes.POINTER(_i32)]),
+    "chord_grouped_contiguous_workspace_bytes": (_sz, [_i64, _int]),
+    "chord_grouped_contiguous_gemm": (_int, [_vp, _i64, _vp, _vp, _sz, _int, _int, _int, _vp, _vp, _sz, _OPTS, _vp]),
+    "chord_grouped_masked_workspace_bytes": (_sz, [_int, _int, _int]),
+    "chord_grouped_masked_gemm": (_int, [_vp, _int, _int, _vp, _int, _vp, _sz, _int, _int, _vp, _vp, _sz, _OPTS,
+                                         _vp]),
 }
 
 
@@ -214,6 +221,31 @@ def chord_moe_layer(x, topk_ids, topk_w, E: int, E_global: int, I: int, packed_w
     _check(load().chord_moe_layer(_p(x), _p(topk_ids), _p(topk_w), T, topk, E, E_global, H, I, _p(packed_w13),
                                   _nbytes(packed_w13), _p(packed_w2), _nbytes(packed_w2), block_m, _p(workspace),
                                   _nbytes(workspace), _p(out), _o(opts), _s(stream)), "chord_moe_layer")
+
+
+def chord_grouped_contiguous_workspace_bytes(M: int, E: int) -> int:
+    return load().chord_grouped_contiguous_workspace_bytes(M, E)
+
+
+def chord_grouped_contiguous_gemm(A, m_indices, packed, E: int, N: int, K: int, C, workspace, opts=None,
+                                  stream=None):
+    """A bf16 [M, K] grouped per expert (segments padded to 128 rows), m_indices int32 [M] (-1: padding)."""
+    _check(load().chord_grouped_contiguous_gemm(_p(A), A.shape[0], _p(m_indices), _p(packed), _nbytes(packed), E, N,
+                                                K, _p(C), _p(workspace), _nbytes(workspace), _o(opts), _s(stream)),
+           "chord_grouped_contiguous_gemm")
+
+
+def chord_grouped_masked_workspace_bytes(G: int, max_m: int, expected_m: int) -> int:
+    return load().chord_grouped_masked_workspace_bytes(G, max_m, expected_m)
+
+
+def chord_grouped_masked_gemm(A, masked_m, expected_m: int, packed, N: int, K: int, C, workspace, opts=None,
+                              stream=None):
+    """A bf16 [G, max_m, K], masked_m int32 [G]; C flat [G * max_m, N]."""
+    G, max_m, _ = A.shape
+    _check(load().chord_grouped_masked_gemm(_p(A), G, max_m, _p(masked_m), expected_m, _p(packed), _nbytes(packed),
+                                            N, K, _p(C), _p(workspace), _nbytes(workspace), _o(opts), _s(stream)),
+           "chord_grouped_masked_gemm")
 
 
 def chord_get_device_error(stream=None) -> int:

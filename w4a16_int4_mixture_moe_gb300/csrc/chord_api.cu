@@ -365,6 +365,87 @@ chord_status chord_moe_layer(const void* x, const int32_t* topk_ids, const float
     return finish(o, static_cast<cudaStream_t>(stream));
 }
 
+// ---- grouped contracts: routing arrays built on the device, then the
+// indexed GEMM with one row per pair (a_row_divisor = 1).
+static size_t grouped_ws(int64_t cap, int block_m) {
+    size_t off = up256((size_t)cap * 4);
+    off = up256(off + (size_t)(cap / block_m) * 4);
+    return up256(off + 4);
+}
+
+static int masked_block_m(int expected_m, int N, int K) {
+    return chord_select_block_m(expected_m, 1, 1, 1, N, K);
+}
+
+// Contiguous: block size from the rows per expert (padding included), like
+// tok_e; capacity bounds sum_e ceil(count_e / bm) * bm.
+static int contiguous_block_m(int64_t M, int E) {
+    return chord_select_block_m((int)(M < INT32_MAX ? M : INT32_MAX), 1, E, E, 0, 0);
+}
+static int64_t contiguous_capacity(int64_t M, int E, int bm) { return ((M + bm - 1) / bm + E) * bm; }
+
+constexpr int kGroupedMaxExperts = 4000;   // the index builder's per-expert tables fit in 48 KB of shared memory
+
+size_t chord_grouped_contiguous_workspace_bytes(int64_t M, int E) {
+    if (M < 0 || E <= 0 || E > kGroupedMaxExperts) return 0;
+    const int bm = contiguous_block_m(M, E);
+    return grouped_ws(contiguous_capacity(M, E, bm), bm);
+}
+
+chord_status chord_grouped_contiguous_gemm(const void* A, int64_t M, const int32_t* m_indices, const void* packed,
+                                           size_t packed_bytes, int E, int N, int K, void* C, void* workspace,
+                                           size_t workspace_bytes, const chord_opts* opts, void* stream) {
+    if (M < 0 || E <= 0 || N <= 0 || K <= 0) return CHORD_ERR_INVALID_ARG;
+    if (M >= INT32_MAX || E > kGroupedMaxExperts) return CHORD_ERR_UNSUPPORTED;
+    const int bm = contiguous_block_m(M, E);
+    const int64_t cap = contiguous_capacity(M, E, bm);
+    if (workspace_bytes < grouped_ws(cap, bm)) return CHORD_ERR_BUFFER_TOO_SMALL;
+    if (!workspace || !aligned16(workspace) || (M > 0 && !m_indices)) return CHORD_ERR_INVALID_ARG;
+    const DeviceInfo& di = device_info();
+    if (!di.err) return CHORD_ERR_CUDA;
+    if (M == 0) return CHORD_OK;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    int32_t* sorted = reinterpret_cast<int32_t*>(ws);
+    int32_t* experts = reinterpret_cast<int32_t*>(ws + up256((size_t)cap * 4));
+    int32_t* ntp = reinterpret_cast<int32_t*>(ws + up256(up256((size_t)cap * 4) + (size_t)(cap / bm) * 4));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (launch_grouped_contiguous_index(m_indices, M, E, bm, sorted, experts, ntp, cap, di.err, s) != cudaSuccess)
+        return CHORD_ERR_CUDA;
+    return chord_w4a16_moe_gemm(A, M, 1, packed, packed_bytes, E, N, K, sorted, experts, ntp, cap, bm, M, C,
+                                nullptr, 0, opts, stream);
+}
+
+size_t chord_grouped_masked_workspace_bytes(int G, int max_m, int expected_m) {
+    if (G <= 0 || G > kGroupedMaxExperts || max_m < 0 || expected_m <= 0) return 0;
+    const int bm = masked_block_m(expected_m, 0, 0);
+    return grouped_ws((int64_t)G * ((max_m + bm - 1) / bm) * bm, bm);
+}
+
+chord_status chord_grouped_masked_gemm(const void* A, int G, int max_m, const int32_t* masked_m, int expected_m,
+                                       const void* packed, size_t packed_bytes, int N, int K, void* C,
+                                       void* workspace, size_t workspace_bytes, const chord_opts* opts,
+                                       void* stream) {
+    if (G <= 0 || max_m < 0 || expected_m <= 0 || N <= 0 || K <= 0) return CHORD_ERR_INVALID_ARG;
+    if (G > kGroupedMaxExperts || (int64_t)G * max_m >= INT32_MAX) return CHORD_ERR_UNSUPPORTED;
+    const int bm = masked_block_m(expected_m, N, K);
+    const int64_t cap = (int64_t)G * ((max_m + bm - 1) / bm) * bm;
+    if (workspace_bytes < grouped_ws(cap, bm)) return CHORD_ERR_BUFFER_TOO_SMALL;
+    if (!workspace || !aligned16(workspace) || !masked_m) return CHORD_ERR_INVALID_ARG;
+    const DeviceInfo& di = device_info();
+    if (!di.err) return CHORD_ERR_CUDA;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    int32_t* sorted = reinterpret_cast<int32_t*>(ws);
+    int32_t* experts = reinterpret_cast<int32_t*>(ws + up256((size_t)cap * 4));
+    int32_t* ntp = reinterpret_cast<int32_t*>(ws + up256(up256((size_t)cap * 4) + (size_t)(cap / bm) * 4));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cap == 0) return CHORD_OK;
+    if (launch_grouped_masked_index(masked_m, G, max_m, bm, sorted, experts, ntp, cap, di.err, s) != cudaSuccess)
+        return CHORD_ERR_CUDA;
+    const int64_t rows = (int64_t)G * max_m;
+    return chord_w4a16_moe_gemm(A, rows, 1, packed, packed_bytes, G, N, K, sorted, experts, ntp, cap, bm, rows, C,
+                                nullptr, 0, opts, stream);
+}
+
 chord_status chord_get_device_error(void* stream, int32_t* code) {
     if (!code) return CHORD_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -305,6 +305,122 @@ cudaError_t launch_align(const int32_t* topk_ids, int64_t P, int E, int block_m,
 }
 
 // ============================================================================
+// Grouped contracts -> the indexed GEMM's routing arrays (one row per pair,
+// row id = pair id, sentinel = the row count).  Both contracts give each
+// expert e a contiguous run of rows [start[e], start[e] + count[e]); its
+// ceil(count[e] / block_m) blocks are laid out expert after expert, exactly as
+// align lays out an expert's pairs, so the GEMM sees one block per expert when
+// its rows fit.  One CTA (the expert tables live in shared memory):
+//   contiguous: count and first row of each expert from m_indices (a row whose
+//               expert's rows are not one run sets CHORD_DEV_BAD_ROW, an id
+//               outside [-1, E) CHORD_DEV_BAD_EXPERT); padding rows (-1) are
+//               in no block;
+//   masked:     count = masked_m[g] (clamped to [0, max_m], CHORD_DEV_BAD_ROW
+//               when outside), first row g * max_m.
+// ============================================================================
+constexpr int kGroupedThreads = 1024;
+
+__device__ void grouped_fill(const int32_t* count, const int32_t* start, int32_t* first_block, int E, int block_m,
+                             int32_t sentinel, int32_t* sorted_ids, int32_t* expert_ids, int32_t* ntp,
+                             int64_t capacity) {
+    if (threadIdx.x == 0) {
+        int32_t acc = 0;
+        for (int e = 0; e < E; ++e) {
+            first_block[e] = acc;
+            acc += (count[e] + block_m - 1) / block_m;
+        }
+        first_block[E] = acc;
+        *ntp = acc * block_m;
+    }
+    __syncthreads();
+    const int64_t total = (int64_t)first_block[E] * block_m;
+    for (int64_t i = threadIdx.x; i < capacity; i += blockDim.x) {
+        if (i >= total) {
+            sorted_ids[i] = sentinel;
+            continue;
+        }
+        const int32_t blk = (int32_t)(i / block_m);
+        int lo = 0, hi = E - 1;   // the expert whose blocks contain blk (the last with first_block <= blk)
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (first_block[mid] <= blk) lo = mid; else hi = mid - 1;
+        }
+        const int32_t r = (blk - first_block[lo]) * block_m + (int32_t)(i % block_m);
+        sorted_ids[i] = r < count[lo] ? start[lo] + r : sentinel;
+        if (i % block_m == 0) expert_ids[blk] = lo;
+    }
+}
+
+__global__ void grouped_contiguous_index_kernel(const int32_t* __restrict__ m_indices, int64_t M, int E,
+                                                int block_m, int32_t* __restrict__ sorted_ids,
+                                                int32_t* __restrict__ expert_ids, int32_t* __restrict__ ntp,
+                                                int64_t capacity, int* err) {
+    extern __shared__ int32_t tab[];   // count[E], start[E], first_block[E + 1]
+    int32_t* count = tab;
+    int32_t* start = tab + E;
+    int32_t* first_block = tab + 2 * E;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        count[e] = 0;
+        start[e] = INT32_MAX;
+    }
+    __syncthreads();
+    for (int64_t m = threadIdx.x; m < M; m += blockDim.x) {
+        const int32_t e = m_indices[m];
+        if (e < -1 || e >= E) {
+            set_error(err, CHORD_DEV_BAD_EXPERT);
+        } else if (e >= 0) {
+            atomicAdd(&count[e], 1);
+            atomicMin(&start[e], (int32_t)m);
+        }
+    }
+    __syncthreads();
+    for (int64_t m = threadIdx.x; m < M; m += blockDim.x) {
+        const int32_t e = m_indices[m];
+        if (e >= 0 && e < E && (int64_t)m - start[e] >= count[e]) set_error(err, CHORD_DEV_BAD_ROW);
+    }
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        if (count[e] == 0) start[e] = 0;
+    __syncthreads();
+    grouped_fill(count, start, first_block, E, block_m, (int32_t)M, sorted_ids, expert_ids, ntp, capacity);
+}
+
+__global__ void grouped_masked_index_kernel(const int32_t* __restrict__ masked_m, int G, int max_m, int block_m,
+                                            int32_t* __restrict__ sorted_ids, int32_t* __restrict__ expert_ids,
+                                            int32_t* __restrict__ ntp, int64_t capacity, int* err) {
+    extern __shared__ int32_t tab[];
+    int32_t* count = tab;
+    int32_t* start = tab + G;
+    int32_t* first_block = tab + 2 * G;
+    for (int g = threadIdx.x; g < G; g += blockDim.x) {
+        int32_t c = masked_m[g];
+        if (c < 0 || c > max_m) {
+            set_error(err, CHORD_DEV_BAD_ROW);
+            c = c < 0 ? 0 : max_m;
+        }
+        count[g] = c;
+        start[g] = g * max_m;
+    }
+    __syncthreads();
+    grouped_fill(count, start, first_block, G, block_m, G * max_m, sorted_ids, expert_ids, ntp, capacity);
+}
+
+cudaError_t launch_grouped_contiguous_index(const int32_t* m_indices, int64_t M, int E, int block_m,
+                                            int32_t* sorted_ids, int32_t* expert_ids, int32_t* ntp,
+                                            int64_t capacity, int* err, cudaStream_t stream) {
+    grouped_contiguous_index_kernel<<<1, kGroupedThreads, (size_t)(3 * E + 1) * sizeof(int32_t), stream>>>(
+        m_indices, M, E, block_m, sorted_ids, expert_ids, ntp, capacity, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_grouped_masked_index(const int32_t* masked_m, int G, int max_m, int block_m, int32_t* sorted_ids,
+                                        int32_t* expert_ids, int32_t* ntp, int64_t capacity, int* err,
+                                        cudaStream_t stream) {
+    grouped_masked_index_kernel<<<1, kGroupedThreads, (size_t)(3 * G + 1) * sizeof(int32_t), stream>>>(
+        masked_m, G, max_m, block_m, sorted_ids, expert_ids, ntp, capacity, err);
+    return cudaGetLastError();
+}
+
+// ============================================================================
 // SiLU * up: h[p, j] = bf16_rne(g / (1 + exp(-g)) * u), FP32 math, 8 columns
 // per thread with 16-byte loads and stores.
 // ============================================================================

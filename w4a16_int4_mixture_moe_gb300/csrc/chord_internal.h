@@ -25,6 +25,12 @@ cudaError_t launch_align(const int32_t* topk_ids, int64_t P, int E, int block_m,
                          int32_t* expert_ids, int32_t* ntp, int64_t capacity, int32_t* counts, bool validate,
                          int* err, cudaStream_t stream);
 
+cudaError_t launch_grouped_contiguous_index(const int32_t* m_indices, int64_t M, int E, int block_m,
+                                            int32_t* sorted_ids, int32_t* expert_ids, int32_t* ntp,
+                                            int64_t capacity, int* err, cudaStream_t stream);
+cudaError_t launch_grouped_masked_index(const int32_t* masked_m, int G, int max_m, int block_m, int32_t* sorted_ids,
+                                        int32_t* expert_ids, int32_t* ntp, int64_t capacity, int* err,
+                                        cudaStream_t stream);
 cudaError_t launch_silu_mul(const uint16_t* C1, const int32_t* topk_ids, int64_t P, int E, int I, uint16_t* h,
                             cudaStream_t stream);
 cudaError_t launch_combine(const void* C2, bool c2_f32, const int32_t* topk_ids, const float* topk_w, int T,
