@@ -521,7 +521,7 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
 #pragma unroll
             for (int it = 0; it < 8; ++it) {
                 const int j0 = wg * 16 + 32 * it;
-                if (j0 >= inf.n_mma) break;
+                if (j0 >= inf.n_mma) continue;   // (not break: keeps the loop unrolled, pre[] in registers)
                 uint32_t v[16];
                 tmem_ld16(acc_tmem + lane_base + j0, v);
                 for (int pi = 1; pi < parts; ++pi) {
@@ -539,14 +539,16 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
                         // lanes l (gate row) and l ^ 8 (its up row) split the 16
                         // tokens: the gate lane takes tokens 0-7, the up lane 8-15,
                         // each receiving the partner's value for its tokens
-                        if (u >= 8) break;
-                        const int tok = gate_row ? u : 8 + u;
-                        const float mine = __uint_as_float(v[tok]);
-                        const float other = __shfl_xor_sync(0xffffffffu, __uint_as_float(v[gate_row ? 8 + u : u]), 8);
-                        const int32_t id = __shfl_sync(0xffffffffu, pre[it >> 1], tok + 16 * (it & 1));
-                        if (id >= 0)
-                            static_cast<__nv_bfloat16*>(a.C)[(int64_t)id * (a.N / 2) + h_col] =
-                                gate_row ? silu_mul_bf16(mine, other) : silu_mul_bf16(other, mine);
+                        if (u < 8) {
+                            const float lo = __uint_as_float(v[u]), hi = __uint_as_float(v[8 + u]);
+                            const float mine = gate_row ? lo : hi;
+                            const float other = __shfl_xor_sync(0xffffffffu, gate_row ? hi : lo, 8);
+                            const int tok = gate_row ? u : 8 + u;
+                            const int32_t id = __shfl_sync(0xffffffffu, pre[it >> 1], tok + 16 * (it & 1));
+                            if (id >= 0)
+                                static_cast<__nv_bfloat16*>(a.C)[(int64_t)id * (a.N / 2) + h_col] =
+                                    gate_row ? silu_mul_bf16(mine, other) : silu_mul_bf16(other, mine);
+                        }
                         continue;
                     }
                     const int32_t id = __shfl_sync(0xffffffffu, pre[it >> 1], u + 16 * (it & 1));
@@ -653,6 +655,8 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t stream) {
     // (measured on GB300: 360 -> 290 us for the EP8 decode gate_up against two
     // issuers and one gather warp).
     if (a.block_m <= 64) return launch_cfg<3, 6, 4>(a, true, stream);
+    // 65-128 tokens: two issuers (TP8 T=4096 gate_up 526 -> 363 us on GB300)
+    if (a.block_m <= 128) return launch_cfg<4, 8, 2>(a, false, stream);
     return launch_cfg<4, 16, 1>(a, false, stream);                       // up to 256 tokens per item
 }
 
