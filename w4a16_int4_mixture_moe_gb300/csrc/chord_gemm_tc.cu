@@ -592,6 +592,10 @@ cudaError_t launch_cfg(const GemmArgs& g, bool deep_weights, cudaStream_t stream
     int nsa = (int)((512 - NI * ta.tok_tile) / kACols);
     nsa = nsa > 8 ? 8 : nsa;
     if (nsa < 2) return cudaErrorInvalidConfiguration;
+    // Several issuers with a 3-stage A ring (two issuers, 160-token blocks, a
+    // configuration the table below never picks) were seen to stall until the
+    // bounded waits gave up; every configuration in use keeps >= 4 A stages.
+    if (NI > 1 && nsa < 4) return cudaErrorInvalidConfiguration;
     ta.nsa = nsa;
     const uint32_t cols = nsa * kACols + NI * ta.tok_tile;
     ta.tmem_cols = pow2_cols(cols);
