@@ -109,7 +109,9 @@ typedef struct chord_opts {
     int32_t validate;    /* nonzero: synchronise after the call and turn a set device
                             error word into CHORD_ERR_DEVICE_VALIDATION / _TIMEOUT
                             ("trusted routing validation" of the deployment notes) */
-    int32_t split_k;     /* 0 = automatic, 1 = off, > 1 = number of K slices (decode) */
+    int32_t split_k;     /* K slices of the warp-level kernel: 0 = automatic, 1 = off,
+                            > 1 = that many (capped at K / 128 rounded up); < 0 is
+                            refused.  The tcgen05 kernel never splits. */
     int32_t out_dtype;   /* GEMM output: CHORD_DTYPE_BF16 (default) or CHORD_DTYPE_F32,
                             the FP32 sums unrounded (for a consumer that keeps FP32) */
     int32_t epilogue;    /* chord_epilogue (GEMM and layer) */
@@ -218,7 +220,7 @@ int chord_select_block_m(int T, int topk, int E_local, int E_global, int N, int 
 
 /* The kernel CHORD_KERNEL_AUTO runs for a GEMM of blocks of block_m rows and
  * an [N, K] weight: CHORD_KERNEL_WARP_MMA for decode blocks (block_m <= 32)
- * and for short K (K <= 512 with block_m <= 128, where the tcgen05 kernel's
+ * and for short K (K <= 512 with block_m <= 64, where the tcgen05 kernel's
  * fixed cost per block and N tile dominates), else CHORD_KERNEL_TCGEN05.
  * The environment variable CHORD_KERNEL (1 or 2), when set, overrides the
  * choice for every call whose opts leave the kernel at AUTO. */
@@ -226,12 +228,19 @@ int chord_select_kernel(int block_m, int N, int K);
 
 /* ------------------------------------------------------------------- GEMM */
 
-/* Scratch bytes chord_w4a16_moe_gemm needs for the given call shape (split-K
- * partial sums); 0 when the chosen schedule needs none. */
+/* Scratch bytes chord_w4a16_moe_gemm needs for the given call shape: the FP32
+ * partial sums of its K slices, S * num_pairs * N * 4 bytes, 0 when S = 1.
+ * Pure host arithmetic (no device query).  The automatic S (opts->split_k =
+ * 0, the warp-level kernel chosen): items = num_pairs * N / 128 bounds the
+ * launch's (align block, 128-row tile) work items from above; when 2 * items
+ * < 456 (152 SMs x 3 resident CTAs) S = min(ceil(456 / items), 16,
+ * ceil(K / 128) / 2), else 1. */
 size_t chord_gemm_workspace_bytes(int64_t num_pairs, int N, int K, int block_m,
                                   const chord_opts *opts);
 
-/* Indexed W4A16 grouped GEMM, one projection (gate_up or down):
+/* Indexed W4A16 grouped GEMM, one projection (gate_up or down) -- the
+ * article's indexed MoE GEMM ("Indexed kernels"; vLLM's moe_align_block_size
+ * routing arrays):
  *   C[p, n] = bf16_rne( sum_k A[p / a_row_divisor, k] * w[e, n, k] )
  * for every block b < num_tokens_padded / block_m, e = expert_ids[b], and every
  * pair id p != num_pairs in sorted_ids[b * block_m .. + block_m); w is the
@@ -250,7 +259,15 @@ size_t chord_gemm_workspace_bytes(int64_t num_pairs, int N, int K, int block_m,
  *            gives; out_dtype must be CHORD_DTYPE_BF16.
  *   capacity length of sorted_ids (expert_ids has capacity / block_m entries).
  * block_m must equal the value given to chord_moe_align, be a multiple of 8 and
- * at most 256; N % 128 == 0, K % 64 == 0. */
+ * at most 256; N % 128 == 0, K % 64 == 0.
+ *   workspace  device, 16-byte aligned, >= chord_gemm_workspace_bytes(...) for
+ *            K slices.  With S > 1 slices, slice s sums K stages
+ *            [s * ks / S, (s + 1) * ks / S) (ks = ceil(K / 128)) into FP32
+ *            partials, and a second launch adds slices 0 .. S-1 in order (FP32)
+ *            and applies the output type or the SiLU * up epilogue; results
+ *            are deterministic but differ from S = 1 by FP32 summation order.
+ *            An automatic split with too small a workspace runs unsplit; an
+ *            explicit one returns CHORD_ERR_BUFFER_TOO_SMALL. */
 chord_status chord_w4a16_moe_gemm(const void *A, int64_t a_rows, int a_row_divisor,
                                   const void *packed, size_t packed_bytes, int E, int N, int K,
                                   const int32_t *sorted_ids, const int32_t *expert_ids,
@@ -319,7 +336,10 @@ chord_status chord_moe_combine(const void *C2, int c2_dtype, const int32_t *topk
 /* ------------------------------------------------------------------ layer */
 
 /* Scratch bytes chord_moe_layer needs for this shape and block_m (0 = the
- * block size chord_select_block_m picks with E_global = E). */
+ * block size chord_select_block_m picks with E_global = E), including the
+ * larger of the two GEMMs' automatic K-slice partial sums (an explicit
+ * opts->split_k larger than that makes the layer call return
+ * CHORD_ERR_BUFFER_TOO_SMALL). */
 size_t chord_layer_workspace_bytes(int T, int topk, int E, int H, int I, int block_m);
 
 /* One MoE expert layer on this GPU's E local experts:

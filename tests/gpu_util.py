@@ -77,13 +77,20 @@ def align(ids, E, bm, opts=None):
     return s, e, n
 
 
-def gemm(A_bits, div, packed, E, N, K, s, e, n, bm, P, kernel=0, C=None):
-    """C rows that no block names keep the fill pattern 0xFFFF (a NaN)."""
+def gemm(A_bits, div, packed, E, N, K, s, e, n, bm, P, kernel=0, C=None, split_k=None, epilogue=0,
+         out_dtype=0):
+    """C rows that no block names keep the fill pattern 0xFFFF (a NaN).
+    split_k=None passes no workspace (the GEMM runs unsplit); otherwise the
+    option is set and the workspace sized by chord_gemm_workspace_bytes."""
     A = A_bits if isinstance(A_bits, torch.Tensor) else dbf(A_bits)
     if C is None:
         C = torch.full((max(P, 1), N), -1, dtype=torch.int16, device=DEV)[:P].view(torch.bfloat16)
-    opts = chord.ChordOpts(kernel=kernel)
-    chord.chord_w4a16_moe_gemm(A, div, packed, E, N, K, s, e, n, bm, P, C, opts=opts)
+    opts = chord.ChordOpts(kernel=kernel, split_k=split_k or 0, epilogue=epilogue, out_dtype=out_dtype)
+    ws = None
+    if split_k is not None:
+        nb = chord.chord_gemm_workspace_bytes(P, N, K, bm, opts)
+        ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=DEV)
+    chord.chord_w4a16_moe_gemm(A, div, packed, E, N, K, s, e, n, bm, P, C, workspace=ws, opts=opts)
     return C
 
 

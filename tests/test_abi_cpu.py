@@ -79,7 +79,7 @@ def test_select_block_m(lib):
 
 
 def test_select_kernel_by_regime(lib, monkeypatch):
-    """Decode blocks (at most 32 rows) and short-K GEMMs with blocks up to 128
+    """Decode blocks (at most 32 rows) and short-K GEMMs with blocks up to 64
     rows go to the warp-level kernel, the rest to the tcgen05 kernel; the
     decode workload's block and the prefill workload's block land on
     different sides."""
@@ -90,7 +90,8 @@ def test_select_kernel_by_regime(lib, monkeypatch):
     for bm in (40, 64, 128, 256):
         assert chord.chord_select_kernel(bm, 4096, 7168) == T
     assert chord.chord_select_kernel(48, 7168, 256) == W       # TP8 down, T = 1024
-    assert chord.chord_select_kernel(128, 7168, 256) == W      # TP8 down, T = 4096
+    assert chord.chord_select_kernel(64, 7168, 256) == W
+    assert chord.chord_select_kernel(128, 7168, 256) == T      # TP8 down, T = 4096
     assert chord.chord_select_kernel(256, 7168, 256) == T
     assert chord.chord_select_kernel(64, 7168, 1024) == T
     bm_dec = chord.chord_select_block_m(512, 8, 48, 384, 4096, 7168)
@@ -146,7 +147,58 @@ def test_layer_workspace_formula(lib):
     want = up(want + P * 2 * I * 2)
     want = up(want + P * I * 2)
     want = up(want + P * H * 4)   # the down projection's FP32 sums
+    # 4096 pairs fill the GPU: no K slices, no partial-sum space
     assert chord.chord_layer_workspace_bytes(T, topk, E, H, I, bm) == want
+    # one token, TP8 shapes: the gate_up projection is cut into 15 K slices
+    T, topk, E, H, I, bm = 1, 8, 384, 7168, 256, 8
+    P = T * topk
+    cap = chord.chord_align_capacity(T, topk, E, bm)
+    want = up(chord.chord_align_workspace_bytes(T, topk, E))
+    for b in (cap * 4, cap // bm * 4, 4, P * 2 * I * 2, P * I * 2, P * H * 4):
+        want = up(want + b)
+    want = up(want + max(chord.chord_gemm_workspace_bytes(P, 2 * I, H, bm),
+                         chord.chord_gemm_workspace_bytes(P, H, I, bm)))
+    assert chord.chord_gemm_workspace_bytes(P, 2 * I, H, bm) == 15 * P * 2 * I * 4
+    assert chord.chord_layer_workspace_bytes(T, topk, E, H, I, bm) == want
+
+
+def test_split_k_choice(lib, monkeypatch):
+    """K slices of the warp-level kernel: the automatic choice cuts K only
+    when num_pairs x N / 128 items fill less than half of 456 resident CTAs,
+    into ceil(456 / items) slices, at most 16 and at most half the 128-column
+    K stages; an explicit count is capped at the number of stages; the
+    tcgen05 kernel never splits.  The workspace holds S x num_pairs x N FP32
+    partial sums."""
+    monkeypatch.delenv("CHORD_KERNEL", raising=False)
+    ws = chord.chord_gemm_workspace_bytes
+    assert ws(8, 512, 7168, 8) == 15 * 8 * 512 * 4          # 32 items -> 15 slices
+    assert ws(1, 128, 7168, 8) == 16 * 1 * 128 * 4          # 1 item -> capped at 16
+    assert ws(1, 128, 512, 8) == 2 * 1 * 128 * 4            # 4 stages -> at most 2
+    assert ws(1, 128, 256, 8) == 0                          # 2 stages -> 1 slice
+    assert ws(8, 7168, 256, 8) == 0                         # 448 items fill the GPU
+    assert ws(128, 512, 7168, 8) == 0                       # 512 items
+    assert ws(40, 512, 7168, 8) == 3 * 40 * 512 * 4         # 160 items -> 3 slices
+    assert ws(8, 512, 7168, 256) == 0                       # tcgen05 block size
+    opts = chord.ChordOpts(split_k=1)
+    assert ws(8, 512, 7168, 8, opts) == 0
+    opts = chord.ChordOpts(split_k=7)
+    assert ws(4096, 4096, 7168, 16, opts) == 7 * 4096 * 4096 * 4
+    opts = chord.ChordOpts(split_k=99)
+    assert ws(8, 512, 384, 8, opts) == 3 * 8 * 512 * 4      # 3 stages
+    opts = chord.ChordOpts(split_k=4, kernel=chord.KERNEL_TCGEN05)
+    assert ws(8, 512, 7168, 8, opts) == 0
+    monkeypatch.setenv("CHORD_KERNEL", "1")
+    assert ws(8, 512, 7168, 8) == 0
+    # an explicit split without its workspace is refused before any launch
+    vp = ctypes.c_void_p
+    big = vp(1 << 20)
+    o = chord.ChordOpts(split_k=4, kernel=chord.KERNEL_WARP_MMA)
+    nbytes = chord.chord_packed_weight_bytes(2, 128, 512)
+    assert lib.chord_w4a16_moe_gemm(big, 8, 1, big, nbytes, 2, 128, 512, big, big, big, 8, 8, 8, big, big, 16,
+                                    ctypes.byref(o), None) == 4
+    o = chord.ChordOpts(split_k=-1)
+    assert lib.chord_w4a16_moe_gemm(big, 8, 1, big, nbytes, 2, 128, 512, big, big, big, 8, 8, 8, big, None, 0,
+                                    ctypes.byref(o), None) == 1
 
 
 def test_argument_errors_before_any_launch(lib):

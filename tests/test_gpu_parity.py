@@ -288,6 +288,129 @@ def test_gemm_header_mismatch_is_reported():
         assert (host_bits(C) == 0xFFFF).all()
 
 
+# ------------------------------------------------------------------ split-K
+
+WARP = chord.KERNEL_WARP_MMA
+
+
+@pytest.mark.parametrize("bm", [8, 16, 32])
+@pytest.mark.parametrize("S", [2, 3, 7, 16])
+def test_split_k_exact_integer_regime_bit_exact(bm, S):
+    """K slices with FP32 partials and an in-order reduction: in the
+    exact-integer regime every sum is exact, so the split result equals the
+    oracle bit for bit, and rows of non-local pairs stay unwritten."""
+    T, topk, E, N, K = 12, 4, 5, 256, 2048
+    rng = np.random.default_rng(S * 10 + bm)
+    x = wl._bf16(rng.integers(-1, 2, size=(T, K)).astype(np.float32))
+    codes = wl.random_codes(S + bm, (E, N, K))
+    scales = np.full((E, N, K // 32), 0x3F80, np.uint16)
+    ids = wl.random_ids(S + bm + 1, T, topk, E, p_nonlocal=0.2)
+    P = T * topk
+    s, e, n = align(ids, E, bm)
+    got = host_bits(gemm(x, topk, pack(codes, scales), E, N, K, s, e, n, bm, P, kernel=WARP, split_k=S))
+    s2, e2, n2 = oracle.moe_align(ids, E, bm)
+    ref = oracle.moe_gemm(x, topk, codes, scales, s2, e2, n2, bm, P, C=np.full((P, N), 0xFFFF, np.uint16))
+    rows = valid_rows(ids, E)
+    np.testing.assert_array_equal(got[rows], ref[rows])
+    assert (got[np.setdiff1d(np.arange(P), rows)] == 0xFFFF).all()
+
+
+@pytest.mark.parametrize("S", [2, 5, 99])
+@pytest.mark.parametrize("shape", [(3, 128, 320), (4, 384, 1024), (2, 256, 7168)])
+def test_split_k_random_vs_oracle(S, shape):
+    """Random data, bf16 and FP32 outputs, ragged K (the last 64-column stage
+    of K = 320 lands in the last slice; S = 99 is capped at the stage count)."""
+    E, N, K = shape
+    T, topk, bm = 9, 4, 8
+    x = wl.random_bf16(S + K, (T, K))
+    codes = wl.random_codes(S + K + 1, (E, N, K))
+    scales = wl.random_scales(S + K + 2, (E, N, K // 32))
+    ids = wl.random_ids(S + K + 3, T, topk, E, p_nonlocal=0.2)
+    P = T * topk
+    packed = pack(codes, scales)
+    s, e, n = align(ids, E, bm)
+    s2, e2, n2 = oracle.moe_align(ids, E, bm)
+    rows = valid_rows(ids, E)
+    got = host_bits(gemm(x, topk, packed, E, N, K, s, e, n, bm, P, kernel=WARP, split_k=S))
+    ref = oracle.moe_gemm(x, topk, codes, scales, s2, e2, n2, bm, P, C=np.full((P, N), 0xFFFF, np.uint16))
+    assert_close(got[rows], ref[rows], f"split-K S={S} E={E} N={N} K={K}")
+    C = torch.full((P, N), float("nan"), dtype=torch.float32, device=DEV)
+    gemm(x, topk, packed, E, N, K, s, e, n, bm, P, kernel=WARP, C=C, split_k=S, out_dtype=chord.DTYPE_F32)
+    got32 = C.cpu().numpy()
+    ref32 = oracle.moe_gemm_f32(x, topk, codes, scales, s2, e2, n2, bm, P)
+    err = np.abs(got32[rows].astype(np.float64) - ref32[rows])
+    assert (err <= 1e-2 + 1e-2 * np.abs(ref32[rows])).all(), err.max()
+    assert np.isnan(got32[np.setdiff1d(np.arange(P), rows)]).all()
+
+
+@pytest.mark.parametrize("S", [3, 8])
+def test_split_k_fused_silu_mul(S):
+    """The reduction applies the SiLU * up epilogue: bit-identical to the split
+    GEMM without it followed by chord_silu_mul, close to the oracle."""
+    T, topk, E, I, K, bm = 11, 3, 4, 192, 1024, 16
+    x = wl.random_bf16(70 + S, (T, K))
+    codes = wl.random_codes(71 + S, (E, 2 * I, K))
+    scales = wl.random_scales(72 + S, (E, 2 * I, K // 32))
+    ids = wl.random_ids(73 + S, T, topk, E, p_nonlocal=0.2)
+    P = T * topk
+    s, e, n = align(ids, E, bm)
+    h = torch.full((P, I), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+    gemm(x, topk, pack(codes, scales, chord.LAYOUT_GATE_UP_INTERLEAVED), E, 2 * I, K, s, e, n, bm, P,
+         kernel=WARP, C=h, split_k=S, epilogue=chord.EPILOGUE_SILU_MUL)
+    got = host_bits(h)
+    C1 = gemm(x, topk, pack(codes, scales), E, 2 * I, K, s, e, n, bm, P, kernel=WARP, split_k=S)
+    h2 = torch.full((P, I), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+    chord.chord_silu_mul(C1, dev(ids.ravel().copy()), E, h2)
+    rows = valid_rows(ids, E)
+    np.testing.assert_array_equal(got[rows], host_bits(h2)[rows])
+    assert (got[np.setdiff1d(np.arange(P), rows)] == 0xFFFF).all()
+    s2, e2, n2 = oracle.moe_align(ids, E, bm)
+    c1 = oracle.moe_gemm(x, topk, codes, scales, s2, e2, n2, bm, P, C=np.zeros((P, 2 * I), np.uint16))
+    ref = oracle.silu_mul(c1, ids.ravel(), E, h=np.full((P, I), 0xFFFF, np.uint16))
+    assert_close_h(got[rows], ref[rows], f"split-K fused S={S}")
+
+
+def test_split_k_automatic_one_token():
+    """One token, TP8 gate_up shape (N = 512, K = 7168): the automatic choice
+    splits K (15 slices) when given its workspace, runs unsplit without one,
+    and both agree with the oracle."""
+    T, topk, E, N, K, bm = 1, 8, 16, 512, 7168, 8
+    assert chord.chord_gemm_workspace_bytes(T * topk, N, K, bm) == 15 * 8 * N * 4
+    x = wl.random_bf16(80, (T, K))
+    codes = wl.random_codes(81, (E, N, K))
+    scales = wl.random_scales(82, (E, N, K // 32))
+    ids = wl.random_ids(83, T, topk, E, p_nonlocal=0.0)
+    P = T * topk
+    packed = pack(codes, scales)
+    s, e, n = align(ids, E, bm)
+    s2, e2, n2 = oracle.moe_align(ids, E, bm)
+    ref = oracle.moe_gemm(x, topk, codes, scales, s2, e2, n2, bm, P, C=np.zeros((P, N), np.uint16))
+    rows = valid_rows(ids, E)
+    split = host_bits(gemm(x, topk, packed, E, N, K, s, e, n, bm, P, split_k=0))
+    plain = host_bits(gemm(x, topk, packed, E, N, K, s, e, n, bm, P))
+    assert_close(split[rows], ref[rows], "automatic split-K, one token")
+    assert_close(plain[rows], ref[rows], "no workspace, one token")
+    assert chord.chord_get_device_error() == 0
+
+
+def test_layer_one_token_split_k_vs_oracle():
+    """The layer with one token and TP8 widths (H = 7168, I = 256) on 16 local
+    experts: its workspace carries the gate_up split's partial sums."""
+    T, topk, E, H, I = 1, 8, 16, 7168, 256
+    ids = wl.random_ids(90, T, topk, E, p_nonlocal=0.0)
+    wts = wl.random_weights(91, T, topk)
+    x = wl.random_bf16(92, (T, H))
+    c13, s13 = wl.random_codes(93, (E, 2 * I, H)), wl.random_scales(94, (E, 2 * I, H // 32))
+    c2, s2 = wl.random_codes(95, (E, H, I)), wl.random_scales(96, (E, H, I // 32))
+    for fused in (False, True):
+        p13 = pack(c13, s13, chord.LAYOUT_GATE_UP_INTERLEAVED if fused else chord.LAYOUT_TCGEN05)
+        opts = chord.ChordOpts(epilogue=chord.EPILOGUE_SILU_MUL if fused else chord.EPILOGUE_NONE)
+        out, bm = layer(x, ids, wts, E, 384, I, p13, pack(c2, s2), opts=opts)
+        assert bm == 8
+        ref = oracle.moe_layer(x, ids, wts, (c13, s13), (c2, s2), E, block_m=bm)
+        assert_close(host_bits(out), ref, f"one-token layer fused={fused}")
+
+
 # ---------------------------------------------------------- fused SiLU * up
 
 def run_fused_case(T, topk, E, I, K, bm, seed, kernel, pnl=0.2):
@@ -425,8 +548,12 @@ def test_grouped_masked_count_out_of_range_is_reported():
 
 # ---------------------------------------------------------------- epilogues
 
-def test_silu_mul_vs_oracle():
-    P, I, E = 50, 192, 4
+@pytest.mark.parametrize("P,I", [(50, 192), (3, 8), (17, 264), (9, 2048), (12000, 64)])
+def test_silu_mul_vs_oracle(P, I):
+    """One warp per pair row: rows of 1, 24, 33 and 256 vectors of 8 columns
+    (one partial round of lanes, one full and one partial, several full) and
+    more rows than the grid's warps."""
+    E = 4
     C1 = wl.random_bf16(8, (P, 2 * I), std=4.0)
     ids = wl.random_ids(9, P, 1, E, p_nonlocal=0.3)
     h = torch.full((P, I), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
@@ -441,9 +568,12 @@ def test_silu_mul_vs_oracle():
     assert np.mean(got[rows] == ref[rows]) > 0.99
 
 
-def test_combine_bit_exact():
-    """Same FP32 operations in the same order as the oracle: bit-exact."""
-    T, topk, E, H = 33, 8, 16, 7168 // 4
+@pytest.mark.parametrize("T,topk,H", [(33, 8, 1792), (130, 8, 1792), (1, 8, 7168), (3, 20, 1024), (5, 1, 256)])
+def test_combine_bit_exact(T, topk, H):
+    """Same FP32 operations in the same order as the oracle: bit-exact, on both
+    the few-token kernel (batched top-k loads, T * H / 4 up to one wave of
+    threads) and the many-token kernel, with top-k above the batch of 8."""
+    E = 16
     C2 = wl.random_bf16(10, (T * topk, H), std=30.0)
     ids = wl.random_ids(11, T, topk, E, p_nonlocal=0.4)
     ids[0, :] = -1

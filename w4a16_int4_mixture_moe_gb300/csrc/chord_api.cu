@@ -40,7 +40,7 @@ chord_opts opts_or_default(const chord_opts* o) {
 // item (pipeline fill, accumulator drain) dominates.
 constexpr int kDecodeMaxBlockM = 32;
 constexpr int kShortK = 512;
-constexpr int kShortKMaxBlockM = 128;
+constexpr int kShortKMaxBlockM = 64;
 
 int env_int(const char* name, int dflt) {
     const char* v = getenv(name);
@@ -185,13 +185,43 @@ int chord_select_kernel(int block_m, int N, int K) {
     return CHORD_KERNEL_TCGEN05;
 }
 
+}  // extern "C"
+
+namespace {
+// Split-K for the warp-level kernel.  Work units = items x K slices; a launch
+// with fewer items than half of its resident CTAs (152 SMs x 3) leaves most
+// SMs idle and each CTA streams a long K loop through a short pipeline, so the
+// automatic choice cuts K into S slices until the units fill about one wave.
+// Each nonempty align block holds at least one pair, so num_pairs x N / 128
+// bounds the items from above without reading num_tokens_padded.
+constexpr int64_t kSplitTargetUnits = 152 * 3;
+constexpr int kSplitMax = 16;
+
+int gemm_split(int64_t num_pairs, int N, int K, int block_m, const chord_opts& o) {
+    const int kernel = o.kernel ? o.kernel : chord_select_kernel(block_m, N, K);
+    if (kernel != CHORD_KERNEL_WARP_MMA || o.split_k == 1 || num_pairs <= 0 || N <= 0 || K <= 0) return 1;
+    const int kstages = (K + 127) / 128;
+    if (o.split_k > 1) return o.split_k < kstages ? o.split_k : kstages;
+    if (o.split_k < 0) return 1;
+    const int64_t items = num_pairs * (N / 128);
+    if (items * 2 >= kSplitTargetUnits) return 1;
+    int64_t S = items > 0 ? (kSplitTargetUnits + items - 1) / items : 1;
+    if (S > kstages / 2) S = kstages / 2;
+    if (S > kSplitMax) S = kSplitMax;
+    return S < 2 ? 1 : (int)S;
+}
+
+size_t split_bytes(int S, int64_t num_pairs, int N) {
+    return S > 1 ? (size_t)S * (size_t)num_pairs * (size_t)N * 4 : 0;
+}
+}  // namespace
+
+extern "C" {
+
 size_t chord_gemm_workspace_bytes(int64_t num_pairs, int N, int K, int block_m, const chord_opts* opts) {
-    (void)num_pairs;
-    (void)N;
-    (void)K;
-    (void)block_m;
-    (void)opts;
-    return 0;
+    if (num_pairs <= 0 || N <= 0 || K <= 0 || block_m <= 0) return 0;
+    const chord_opts o = opts_or_default(opts);
+    return split_bytes(gemm_split(num_pairs, N, K, block_m, o), num_pairs, N);
 }
 
 chord_status chord_w4a16_moe_gemm(const void* A, int64_t a_rows, int a_row_divisor, const void* packed,
@@ -199,8 +229,6 @@ chord_status chord_w4a16_moe_gemm(const void* A, int64_t a_rows, int a_row_divis
                                   const int32_t* expert_ids, const int32_t* num_tokens_padded, int64_t capacity,
                                   int block_m, int64_t num_pairs, void* C, void* workspace, size_t workspace_bytes,
                                   const chord_opts* opts, void* stream) {
-    (void)workspace;
-    (void)workspace_bytes;
     if (E <= 0 || N <= 0 || K <= 0 || a_rows < 0 || a_row_divisor <= 0 || block_m <= 0 || capacity < 0 ||
         num_pairs < 0)
         return CHORD_ERR_INVALID_ARG;
@@ -219,6 +247,15 @@ chord_status chord_w4a16_moe_gemm(const void* A, int64_t a_rows, int a_row_divis
     if (o.epilogue != CHORD_EPILOGUE_NONE && o.epilogue != CHORD_EPILOGUE_SILU_MUL) return CHORD_ERR_INVALID_ARG;
     const bool silu = o.epilogue == CHORD_EPILOGUE_SILU_MUL;
     if (silu && o.out_dtype != CHORD_DTYPE_BF16) return CHORD_ERR_INVALID_ARG;
+    if (o.split_k < 0) return CHORD_ERR_INVALID_ARG;
+    // K slices: an explicit request needs its partial-sum workspace; the
+    // automatic choice falls back to one slice when the caller gave none.
+    int S = gemm_split(num_pairs, N, K, block_m, o);
+    if (S > 1 && (workspace_bytes < split_bytes(S, num_pairs, N) || !workspace || !aligned16(workspace))) {
+        if (o.split_k > 1) return workspace_bytes < split_bytes(S, num_pairs, N) ? CHORD_ERR_BUFFER_TOO_SMALL
+                                                                                 : CHORD_ERR_INVALID_ARG;
+        S = 1;
+    }
     const DeviceInfo& di = device_info();
     if (!di.err) return CHORD_ERR_CUDA;
     if (capacity == 0 || num_pairs == 0) return CHORD_OK;
@@ -242,8 +279,13 @@ chord_status chord_w4a16_moe_gemm(const void* A, int64_t a_rows, int a_row_divis
     g.silu = silu ? 1 : 0;
     g.layout = silu ? CHORD_LAYOUT_GATE_UP_INTERLEAVED : CHORD_LAYOUT_TCGEN05;
     g.err = di.err;
+    g.ksplit = S;
+    g.partial = S > 1 ? static_cast<float*>(workspace) : nullptr;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = kernel == CHORD_KERNEL_TCGEN05 ? launch_gemm_tc(g, s) : launch_gemm_decode(g, s);
+    if (e == cudaSuccess && S > 1)
+        e = launch_splitk_reduce(g.partial, S, num_pairs, g.id_limit, N, sorted_ids, num_tokens_padded, capacity, C,
+                                 g.out_f32, g.silu, s);
     if (e != cudaSuccess) return CHORD_ERR_CUDA;
     return finish(o, s);
 }
@@ -271,7 +313,7 @@ chord_status chord_moe_combine(const void* C2, int c2_dtype, const int32_t* topk
 
 namespace {
 struct LayerWs {
-    size_t counts, sorted, experts, ntp, c1, h, c2, total;
+    size_t counts, sorted, experts, ntp, c1, h, c2, split, total;
 };
 
 size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -295,6 +337,13 @@ bool layer_ws(int T, int topk, int E, int H, int I, int block_m, LayerWs* w) {
     off = up256(off + P * (size_t)I * 2);
     w->c2 = off;
     off = up256(off + P * (size_t)H * 4);
+    // FP32 partial sums of the K-sliced GEMMs (default options), shared by
+    // the gate_up and the down projection, which run one after the other
+    w->split = off;
+    const chord_opts o = opts_or_default(nullptr);
+    const size_t s13 = split_bytes(gemm_split((int64_t)P, 2 * I, H, block_m, o), (int64_t)P, 2 * I);
+    const size_t s2 = split_bytes(gemm_split((int64_t)P, H, I, block_m, o), (int64_t)P, H);
+    off = up256(off + (s13 > s2 ? s13 : s2));
     w->total = off;
     return true;
 }
@@ -334,6 +383,8 @@ chord_status chord_moe_layer(const void* x, const int32_t* topk_ids, const float
     void* c1 = ws + w.c1;
     void* h = ws + w.h;
     void* c2 = ws + w.c2;
+    void* split = ws + w.split;
+    const size_t split_len = w.total - w.split;
     const int64_t P = (int64_t)T * topk;
     const int64_t cap = chord_align_capacity(T, topk, E, block_m);
     chord_status st;
@@ -343,12 +394,12 @@ chord_status chord_moe_layer(const void* x, const int32_t* topk_ids, const float
     if (o.epilogue == CHORD_EPILOGUE_SILU_MUL) {
         // w13 in layout 3: SiLU * up in the gate_up GEMM's epilogue, h written directly
         st = chord_w4a16_moe_gemm(x, T, topk, packed_w13, w13_bytes, E, 2 * I, H, sorted, experts, ntp, cap, block_m,
-                                  P, h, nullptr, 0, &o, stream);
+                                  P, h, split, split_len, &o, stream);
         if (st != CHORD_OK) return st;
     } else {
         if (o.epilogue != CHORD_EPILOGUE_NONE) return CHORD_ERR_INVALID_ARG;
         st = chord_w4a16_moe_gemm(x, T, topk, packed_w13, w13_bytes, E, 2 * I, H, sorted, experts, ntp, cap, block_m,
-                                  P, c1, nullptr, 0, &o, stream);
+                                  P, c1, split, split_len, &o, stream);
         if (st != CHORD_OK) return st;
         st = chord_silu_mul(c1, topk_ids, P, E, I, h, stream);
         if (st != CHORD_OK) return st;
@@ -357,7 +408,7 @@ chord_status chord_moe_layer(const void* x, const int32_t* topk_ids, const float
     o_down.out_dtype = CHORD_DTYPE_F32;
     o_down.epilogue = CHORD_EPILOGUE_NONE;
     st = chord_w4a16_moe_gemm(h, P, 1, packed_w2, w2_bytes, E, H, I, sorted, experts, ntp, cap, block_m, P, c2,
-                              nullptr, 0, &o_down, stream);
+                              split, split_len, &o_down, stream);
     if (st != CHORD_OK) return st;
     st = chord_moe_combine(c2, CHORD_DTYPE_F32, topk_ids, topk_w, T, topk, E, H, out, stream);
     if (st != CHORD_OK) return st;

@@ -153,7 +153,8 @@ cudaError_t launch_pack(const uint8_t* codes, const uint16_t* scales, int E, int
 
 // ============================================================================
 // moe_align_block_size, deterministic: pairs of each expert in ascending pair
-// id.  Three launches:
+// id.  Up to kSlice pairs: one CTA does everything in one launch.  Above:
+// three launches,
 //   count:   per slice of kSlice pairs, an expert histogram; also fills
 //            sorted_ids with the sentinel;
 //   scan:    one CTA turns the histograms into each slice's starting offset per
@@ -167,14 +168,10 @@ constexpr int kAlignWarps = kAlignThreads / 32;
 
 int align_slices(int64_t P) { return P > 0 ? (int)ceil_div64(P, kSlice) : 1; }
 
-__global__ void __launch_bounds__(kAlignThreads) align_count_kernel(const int32_t* __restrict__ ids, int64_t P, int E,
-                                                                    int32_t* __restrict__ counts,
-                                                                    int32_t* __restrict__ sorted_ids,
-                                                                    int64_t capacity, int validate, int* err) {
-    extern __shared__ int32_t hist[];
-    for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
-    __syncthreads();
-    const int64_t base = (int64_t)blockIdx.x * kSlice;
+// Histogram of the local experts of pairs [base, min(base + kSlice, P)) into
+// shared `hist` (zeroed by the caller).
+__device__ __forceinline__ void slice_histogram(const int32_t* __restrict__ ids, int64_t P, int E, int64_t base,
+                                                int32_t* hist, int validate, int* err) {
     for (int i = threadIdx.x; i < kSlice; i += blockDim.x) {
         const int64_t p = base + i;
         if (p >= P) break;
@@ -184,31 +181,19 @@ __global__ void __launch_bounds__(kAlignThreads) align_count_kernel(const int32_
         else if (validate && e != -1)
             set_error(err, CHORD_DEV_BAD_EXPERT);
     }
-    __syncthreads();
-    for (int i = threadIdx.x; i < E; i += blockDim.x) counts[(int64_t)blockIdx.x * E + i] = hist[i];
-    const int32_t sentinel = (int32_t)P;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < capacity;
-         i += (int64_t)gridDim.x * blockDim.x)
-        sorted_ids[i] = sentinel;
 }
 
-__global__ void __launch_bounds__(kAlignThreads) align_scan_kernel(int32_t* __restrict__ counts, int nslices, int E,
-                                                                   int block_m, int32_t* __restrict__ expert_ids,
-                                                                   int64_t nblocks_cap, int32_t* __restrict__ ntp) {
+// Thread e < E holds expert e's pair count `total`; returns the exclusive
+// prefix sum of the block_m-padded counts (expert e's first slot), writes
+// expert_ids for every block and -1 past the padded total, and the total to
+// *ntp.  All kAlignThreads threads must call it.
+__device__ __forceinline__ int32_t padded_offsets(int32_t total, int E, int block_m, int32_t* __restrict__ expert_ids,
+                                                  int64_t nblocks_cap, int32_t* __restrict__ ntp) {
     __shared__ int32_t warp_sums[kAlignWarps];
     __shared__ int32_t total_padded;
     const int e = threadIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int32_t total = 0;
-    if (e < E) {
-        for (int s = 0; s < nslices; ++s) {
-            const int32_t v = counts[(int64_t)s * E + e];
-            counts[(int64_t)s * E + e] = total;
-            total += v;
-        }
-    }
     const int32_t padded = (e < E) ? (total + block_m - 1) / block_m * block_m : 0;
-    // exclusive scan of `padded` over the CTA
     int32_t x = padded;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -229,26 +214,23 @@ __global__ void __launch_bounds__(kAlignThreads) align_scan_kernel(int32_t* __re
     }
     __syncthreads();
     const int32_t offset = x - padded + (warp > 0 ? warp_sums[warp - 1] : 0);
-    if (e < E) {
-        for (int s = 0; s < nslices; ++s) counts[(int64_t)s * E + e] += offset;
+    if (e < E)
         for (int32_t b = offset / block_m; b < (offset + padded) / block_m; ++b) expert_ids[b] = e;
-    }
     const int32_t tp = total_padded;
     for (int64_t b = tp / block_m + threadIdx.x; b < nblocks_cap; b += blockDim.x) expert_ids[b] = -1;
     if (threadIdx.x == 0) *ntp = tp;
+    return offset;
 }
 
-__global__ void __launch_bounds__(kAlignThreads) align_scatter_kernel(const int32_t* __restrict__ ids, int64_t P,
-                                                                      int E, const int32_t* __restrict__ counts,
-                                                                      int32_t* __restrict__ sorted_ids) {
-    extern __shared__ int32_t sm[];
-    int32_t* run = sm;           // [E]   next free slot per expert
-    int32_t* wcnt = sm + E;      // [kAlignWarps][E]
+// Places the local pairs of slice [base, base + kSlice) at run[e], run[e] + 1,
+// ... in ascending pair id (run: shared, next free slot per expert, advanced;
+// wcnt: shared [kAlignWarps][E] scratch).
+__device__ __forceinline__ void slice_scatter(const int32_t* __restrict__ ids, int64_t P, int E, int64_t base,
+                                              int32_t* run, int32_t* wcnt, int32_t* __restrict__ sorted_ids) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int i = threadIdx.x; i < E; i += blockDim.x) run[i] = counts[(int64_t)blockIdx.x * E + i];
     const unsigned lt_mask = (1u << lane) - 1u;
-    const int64_t base = (int64_t)blockIdx.x * kSlice;
     for (int r = 0; r < kSlice / kAlignThreads; ++r) {
+        if (base + (int64_t)r * kAlignThreads >= P) break;   // uniform over the CTA
         for (int i = threadIdx.x; i < kAlignWarps * E; i += blockDim.x) wcnt[i] = 0;
         __syncthreads();
         const int64_t p = base + (int64_t)r * kAlignThreads + threadIdx.x;
@@ -274,6 +256,71 @@ __global__ void __launch_bounds__(kAlignThreads) align_scatter_kernel(const int3
     }
 }
 
+// P <= kSlice: histogram, offsets, sentinel fill and placement in one CTA.
+__global__ void __launch_bounds__(kAlignThreads) align_single_kernel(const int32_t* __restrict__ ids, int64_t P, int E,
+                                                                     int block_m, int32_t* __restrict__ sorted_ids,
+                                                                     int32_t* __restrict__ expert_ids,
+                                                                     int64_t nblocks_cap, int32_t* __restrict__ ntp,
+                                                                     int64_t capacity, int validate, int* err) {
+    extern __shared__ int32_t sm[];
+    int32_t* run = sm;        // [E] histogram, then next free slot per expert
+    int32_t* wcnt = sm + E;   // [kAlignWarps][E]
+    for (int i = threadIdx.x; i < E; i += blockDim.x) run[i] = 0;
+    const int32_t sentinel = (int32_t)P;
+    for (int64_t i = threadIdx.x; i < capacity; i += blockDim.x) sorted_ids[i] = sentinel;
+    __syncthreads();
+    slice_histogram(ids, P, E, 0, run, validate, err);
+    __syncthreads();
+    const int32_t total = threadIdx.x < E ? run[threadIdx.x] : 0;
+    const int32_t offset = padded_offsets(total, E, block_m, expert_ids, nblocks_cap, ntp);
+    if (threadIdx.x < E) run[threadIdx.x] = offset;
+    __syncthreads();   // also orders the sentinel fill before the placement
+    slice_scatter(ids, P, E, 0, run, wcnt, sorted_ids);
+}
+
+__global__ void __launch_bounds__(kAlignThreads) align_count_kernel(const int32_t* __restrict__ ids, int64_t P, int E,
+                                                                    int32_t* __restrict__ counts,
+                                                                    int32_t* __restrict__ sorted_ids,
+                                                                    int64_t capacity, int validate, int* err) {
+    extern __shared__ int32_t hist[];
+    for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    slice_histogram(ids, P, E, (int64_t)blockIdx.x * kSlice, hist, validate, err);
+    __syncthreads();
+    for (int i = threadIdx.x; i < E; i += blockDim.x) counts[(int64_t)blockIdx.x * E + i] = hist[i];
+    const int32_t sentinel = (int32_t)P;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < capacity;
+         i += (int64_t)gridDim.x * blockDim.x)
+        sorted_ids[i] = sentinel;
+}
+
+__global__ void __launch_bounds__(kAlignThreads) align_scan_kernel(int32_t* __restrict__ counts, int nslices, int E,
+                                                                   int block_m, int32_t* __restrict__ expert_ids,
+                                                                   int64_t nblocks_cap, int32_t* __restrict__ ntp) {
+    const int e = threadIdx.x;
+    int32_t total = 0;
+    if (e < E) {
+        for (int s = 0; s < nslices; ++s) {
+            const int32_t v = counts[(int64_t)s * E + e];
+            counts[(int64_t)s * E + e] = total;
+            total += v;
+        }
+    }
+    const int32_t offset = padded_offsets(total, E, block_m, expert_ids, nblocks_cap, ntp);
+    if (e < E)
+        for (int s = 0; s < nslices; ++s) counts[(int64_t)s * E + e] += offset;
+}
+
+__global__ void __launch_bounds__(kAlignThreads) align_scatter_kernel(const int32_t* __restrict__ ids, int64_t P,
+                                                                      int E, const int32_t* __restrict__ counts,
+                                                                      int32_t* __restrict__ sorted_ids) {
+    extern __shared__ int32_t sm[];
+    int32_t* run = sm;           // [E]   next free slot per expert
+    int32_t* wcnt = sm + E;      // [kAlignWarps][E]
+    for (int i = threadIdx.x; i < E; i += blockDim.x) run[i] = counts[(int64_t)blockIdx.x * E + i];
+    slice_scatter(ids, P, E, (int64_t)blockIdx.x * kSlice, run, wcnt, sorted_ids);
+}
+
 cudaError_t launch_align(const int32_t* topk_ids, int64_t P, int E, int block_m, int32_t* sorted_ids,
                          int32_t* expert_ids, int32_t* ntp, int64_t capacity, int32_t* counts, bool validate, int* err,
                          cudaStream_t stream) {
@@ -284,10 +331,18 @@ cudaError_t launch_align(const int32_t* topk_ids, int64_t P, int E, int block_m,
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 64 && !attr_done[dev]) {
-        cudaError_t e1 = cudaFuncSetAttribute(align_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              (int)((1024 + kAlignWarps * 1024) * sizeof(int32_t)));
+        const int most = (int)((1024 + kAlignWarps * 1024) * sizeof(int32_t));
+        cudaError_t e1 = cudaFuncSetAttribute(align_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+        if (e1 == cudaSuccess)
+            e1 = cudaFuncSetAttribute(align_single_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
         if (e1 != cudaSuccess) return e1;
         attr_done[dev] = true;
+    }
+    if (nslices == 1) {
+        align_single_kernel<<<1, kAlignThreads, scatter_smem, stream>>>(topk_ids, P, E, block_m, sorted_ids,
+                                                                       expert_ids, capacity / block_m, ntp, capacity,
+                                                                       validate ? 1 : 0, err);
+        return cudaGetLastError();
     }
     align_count_kernel<<<nslices, kAlignThreads, hist_smem, stream>>>(topk_ids, P, E, counts, sorted_ids, capacity,
                                                                       validate ? 1 : 0, err);
@@ -297,11 +352,8 @@ cudaError_t launch_align(const int32_t* topk_ids, int64_t P, int E, int block_m,
                                                        ntp);
     st = cudaGetLastError();
     if (st != cudaSuccess) return st;
-    if (P > 0) {
-        align_scatter_kernel<<<nslices, kAlignThreads, scatter_smem, stream>>>(topk_ids, P, E, counts, sorted_ids);
-        st = cudaGetLastError();
-    }
-    return st;
+    align_scatter_kernel<<<nslices, kAlignThreads, scatter_smem, stream>>>(topk_ids, P, E, counts, sorted_ids);
+    return cudaGetLastError();
 }
 
 // ============================================================================
@@ -420,10 +472,6 @@ cudaError_t launch_grouped_masked_index(const int32_t* masked_m, int G, int max_
     return cudaGetLastError();
 }
 
-// ============================================================================
-// SiLU * up: h[p, j] = bf16_rne(g / (1 + exp(-g)) * u), FP32 math, 8 columns
-// per thread with 16-byte loads and stores.
-// ============================================================================
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
@@ -432,32 +480,132 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&r);
 }
 
+// ============================================================================
+// Split-K reduction: C[p, n] = sum over slices s = 0 .. S-1, in that order,
+// of partial[s, p, n] (the GEMM's FP32 partial sums of K slice s), for every
+// pair p a block of the routing names; then the GEMM's epilogue: bf16 or FP32
+// out, or with silu the fused SiLU * up of layout 3 (h column 8k + i from the
+// packed rows 16k + i and 16k + 8 + i).  One thread per 4 output columns; the
+// loads of up to 8 slices are issued before they are added, so the in-order
+// sum costs one memory round trip per 8 slices.
+// ============================================================================
+__device__ __forceinline__ float4 add4(float4 a, float4 b) {
+    return make_float4(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y), __fadd_rn(a.z, b.z), __fadd_rn(a.w, b.w));
+}
+
+template <bool kSilu>
+__global__ void splitk_reduce_kernel(const float* __restrict__ partial, int S, int64_t num_pairs, int64_t id_limit,
+                                     int N, const int32_t* __restrict__ sorted_ids, const int32_t* __restrict__ ntp,
+                                     int64_t capacity, void* __restrict__ C, int out_f32) {
+    constexpr int kBatch = 8;
+    const int out_cols = kSilu ? N / 2 : N;
+    const int vpr = out_cols / 4;
+    int64_t slots = *ntp;
+    slots = slots < 0 ? 0 : (slots > capacity ? capacity : slots);
+    const int64_t nvec = slots * vpr;
+    const int64_t slice_stride = num_pairs * (int64_t)N / 4;   // in float4
+    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nvec; v += (int64_t)gridDim.x * blockDim.x) {
+        int jv;
+        const int32_t p = __ldg(sorted_ids + divmod_idx(v, vpr, jv));
+        if (p < 0 || (int64_t)p >= id_limit) continue;
+        const int j0 = jv * 4;
+        // packed column of output column j0 (gate; up is 8 further)
+        const int c0 = kSilu ? 16 * (j0 / 8) + j0 % 8 : j0;
+        const float4* src = reinterpret_cast<const float4*>(partial + (int64_t)p * N + c0);
+        float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
+        for (int s0 = 0; s0 < S; s0 += kBatch) {
+            float4 gv[kBatch], uv[kBatch];
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i) {
+                if (s0 + i < S) {
+                    gv[i] = __ldcg(src + (int64_t)(s0 + i) * slice_stride);
+                    if (kSilu) uv[i] = __ldcg(src + (int64_t)(s0 + i) * slice_stride + 2);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i) {
+                if (s0 + i < S) {
+                    g = add4(g, gv[i]);
+                    if (kSilu) u = add4(u, uv[i]);
+                }
+            }
+        }
+        if (kSilu) {
+            __nv_bfloat16 o[4] = {silu_mul_bf16(g.x, u.x), silu_mul_bf16(g.y, u.y), silu_mul_bf16(g.z, u.z),
+                                  silu_mul_bf16(g.w, u.w)};
+            *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(C) + (int64_t)p * out_cols + j0) =
+                *reinterpret_cast<const uint2*>(o);
+        } else if (out_f32) {
+            *reinterpret_cast<float4*>(static_cast<float*>(C) + (int64_t)p * out_cols + j0) = g;
+        } else {
+            uint2 o;
+            o.x = pack_bf16x2(g.x, g.y);
+            o.y = pack_bf16x2(g.z, g.w);
+            *reinterpret_cast<uint2*>(static_cast<uint16_t*>(C) + (int64_t)p * out_cols + j0) = o;
+        }
+    }
+}
+
+// ============================================================================
+// SiLU * up: h[p, j] = bf16_rne(g / (1 + exp(-g)) * u), FP32 math.  One warp
+// per pair row: lane 0's id decides for the whole row (a row of another GPU's
+// expert costs one load), then the warp walks the row 8 columns per lane with
+// 16-byte loads and stores, two vectors per lane in flight.
+// ============================================================================
+__device__ __forceinline__ uint4 silu_mul8(uint4 gv, uint4 uv) {
+    uint4 o;
+    o.x = pack_bf16x2(silu_times(bf16_lo(gv.x), bf16_lo(uv.x)), silu_times(bf16_hi(gv.x), bf16_hi(uv.x)));
+    o.y = pack_bf16x2(silu_times(bf16_lo(gv.y), bf16_lo(uv.y)), silu_times(bf16_hi(gv.y), bf16_hi(uv.y)));
+    o.z = pack_bf16x2(silu_times(bf16_lo(gv.z), bf16_lo(uv.z)), silu_times(bf16_hi(gv.z), bf16_hi(uv.z)));
+    o.w = pack_bf16x2(silu_times(bf16_lo(gv.w), bf16_lo(uv.w)), silu_times(bf16_hi(gv.w), bf16_hi(uv.w)));
+    return o;
+}
+
 __global__ void silu_mul_kernel(const uint16_t* __restrict__ C1, const int32_t* __restrict__ ids, int64_t P, int E,
                                 int I, uint16_t* __restrict__ h) {
-    const int vpr = I / 8;  // vectors per row
-    const int64_t nvec = P * vpr;
-    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nvec; v += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t p = v / vpr;
-        const int j = (int)(v % vpr) * 8;
-        const int e = ids[p];
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int vpr = I / 8;
+    for (int64_t p = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); p < P; p += warps) {
+        int e = lane == 0 ? __ldg(ids + p) : 0;
+        e = __shfl_sync(0xffffffffu, e, 0);
         if (e < 0 || e >= E) continue;
-        const uint4 gv = *reinterpret_cast<const uint4*>(C1 + p * 2 * I + j);
-        const uint4 uv = *reinterpret_cast<const uint4*>(C1 + p * 2 * I + I + j);
-        uint4 o;
-        o.x = pack_bf16x2(silu_times(bf16_lo(gv.x), bf16_lo(uv.x)), silu_times(bf16_hi(gv.x), bf16_hi(uv.x)));
-        o.y = pack_bf16x2(silu_times(bf16_lo(gv.y), bf16_lo(uv.y)), silu_times(bf16_hi(gv.y), bf16_hi(uv.y)));
-        o.z = pack_bf16x2(silu_times(bf16_lo(gv.z), bf16_lo(uv.z)), silu_times(bf16_hi(gv.z), bf16_hi(uv.z)));
-        o.w = pack_bf16x2(silu_times(bf16_lo(gv.w), bf16_lo(uv.w)), silu_times(bf16_hi(gv.w), bf16_hi(uv.w)));
-        *reinterpret_cast<uint4*>(h + p * I + j) = o;
+        const uint4* grow = reinterpret_cast<const uint4*>(C1 + p * 2 * I);
+        const uint4* urow = reinterpret_cast<const uint4*>(C1 + p * 2 * I + I);
+        uint4* hrow = reinterpret_cast<uint4*>(h + p * I);
+        int j = lane;
+        for (; j + 32 < vpr; j += 64) {
+            const uint4 g0 = grow[j], u0 = urow[j], g1 = grow[j + 32], u1 = urow[j + 32];
+            hrow[j] = silu_mul8(g0, u0);
+            hrow[j + 32] = silu_mul8(g1, u1);
+        }
+        if (j < vpr) hrow[j] = silu_mul8(grow[j], urow[j]);
     }
+}
+
+cudaError_t launch_splitk_reduce(const float* partial, int S, int64_t num_pairs, int64_t id_limit, int N,
+                                 const int32_t* sorted_ids, const int32_t* ntp, int64_t capacity, void* C, int out_f32,
+                                 int silu, cudaStream_t stream) {
+    const int64_t nvec = capacity * ((silu ? N / 2 : N) / 4);
+    if (nvec == 0) return cudaSuccess;
+    const int threads = 128;
+    int64_t blocks = ceil_div64(nvec, threads);
+    const int64_t cap = (int64_t)device_info().sm_count * 16;
+    if (blocks > cap) blocks = cap;
+    if (silu)
+        splitk_reduce_kernel<true><<<(unsigned)blocks, threads, 0, stream>>>(partial, S, num_pairs, id_limit, N,
+                                                                            sorted_ids, ntp, capacity, C, out_f32);
+    else
+        splitk_reduce_kernel<false><<<(unsigned)blocks, threads, 0, stream>>>(partial, S, num_pairs, id_limit, N,
+                                                                             sorted_ids, ntp, capacity, C, out_f32);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_silu_mul(const uint16_t* C1, const int32_t* topk_ids, int64_t P, int E, int I, uint16_t* h,
                             cudaStream_t stream) {
-    const int64_t nvec = P * (I / 8);
-    if (nvec == 0) return cudaSuccess;
-    const int threads = 256;
-    int64_t blocks = ceil_div64(nvec, threads);
+    if (P == 0) return cudaSuccess;
+    const int threads = 256;   // 8 warps = 8 rows per block and round
+    int64_t blocks = ceil_div64(P, threads / 32);
     const int64_t cap = (int64_t)device_info().sm_count * 8;
     if (blocks > cap) blocks = cap;
     silu_mul_kernel<<<(unsigned)blocks, threads, 0, stream>>>(C1, topk_ids, P, E, I, h);
@@ -467,17 +615,30 @@ cudaError_t launch_silu_mul(const uint16_t* C1, const int32_t* topk_ids, int64_t
 // ============================================================================
 // Top-k weighted combine: out[t, n] = bf16_rne(sum_k w[t,k] * C2[t*topk+k, n])
 // over local k in ascending order, FP32 from +0, each product and each sum
-// rounded separately (no fused multiply-add), 8 columns per thread; C2 in bf16
-// or in FP32.
+// rounded separately (no fused multiply-add); C2 in bf16 or in FP32.
 // ============================================================================
+template <bool F32>
+__device__ __forceinline__ void load4(const void* C2v, int64_t off, float (&c)[4]) {
+    if constexpr (F32) {
+        const float4 a = *reinterpret_cast<const float4*>(static_cast<const float*>(C2v) + off);
+        c[0] = a.x; c[1] = a.y; c[2] = a.z; c[3] = a.w;
+    } else {
+        const uint2 u = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(C2v) + off);
+        c[0] = bf16_lo(u.x); c[1] = bf16_hi(u.x); c[2] = bf16_lo(u.y); c[3] = bf16_hi(u.y);
+    }
+}
+
+// Many tokens: 8 columns per thread, one pair after the other; occupancy
+// keeps enough rows in flight.
 template <bool F32>
 __global__ void combine_kernel(const void* __restrict__ C2v, const int32_t* __restrict__ ids,
                                const float* __restrict__ w, int T, int topk, int E, int H, uint16_t* __restrict__ out) {
     const int vpr = H / 8;
     const int64_t nvec = (int64_t)T * vpr;
     for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nvec; v += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t t = v / vpr;
-        const int n = (int)(v % vpr) * 8;
+        int nv;
+        const int64_t t = divmod_idx(v, vpr, nv);
+        const int n = nv * 8;
         float acc[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
@@ -486,21 +647,11 @@ __global__ void combine_kernel(const void* __restrict__ C2v, const int32_t* __re
             const int e = ids[p];
             if (e < 0 || e >= E) continue;
             const float wk = w[p];
-            float c[8];
-            if constexpr (F32) {
-                const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(C2v) + p * H + n);
-                const float4 a = src[0], b = src[1];
-                c[0] = a.x; c[1] = a.y; c[2] = a.z; c[3] = a.w;
-                c[4] = b.x; c[5] = b.y; c[6] = b.z; c[7] = b.w;
-            } else {
-                const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(C2v) + p * H + n);
-                const uint32_t cw[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    c[2 * i] = bf16_lo(cw[i]);
-                    c[2 * i + 1] = bf16_hi(cw[i]);
-                }
-            }
+            float c[8], d[4];
+            load4<F32>(C2v, p * H + n, d);
+            c[0] = d[0]; c[1] = d[1]; c[2] = d[2]; c[3] = d[3];
+            load4<F32>(C2v, p * H + n + 4, d);
+            c[4] = d[0]; c[5] = d[1]; c[6] = d[2]; c[7] = d[3];
 #pragma unroll
             for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], __fmul_rn(wk, c[i]));
         }
@@ -513,18 +664,72 @@ __global__ void combine_kernel(const void* __restrict__ C2v, const int32_t* __re
     }
 }
 
+// Few tokens (latency-bound): 4 columns per thread, and the k loop in batches
+// of kBatch: the ids and weights of a batch are loaded together, then the
+// local pairs' rows together, then added in k order.
+template <bool F32>
+__global__ void combine_few_kernel(const void* __restrict__ C2v, const int32_t* __restrict__ ids,
+                               const float* __restrict__ w, int T, int topk, int E, int H, uint16_t* __restrict__ out) {
+    constexpr int kBatch = 8;
+    const int vpr = H / 4;
+    const int64_t nvec = (int64_t)T * vpr;
+    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nvec; v += (int64_t)gridDim.x * blockDim.x) {
+        int nv;
+        const int64_t t = divmod_idx(v, vpr, nv);
+        const int n = nv * 4;
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (int k0 = 0; k0 < topk; k0 += kBatch) {
+            bool local[kBatch];
+            float wk[kBatch];
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                local[j] = false;
+                wk[j] = 0.0f;
+                if (k0 + j < topk) {
+                    const int64_t p = t * topk + k0 + j;
+                    const int e = __ldg(ids + p);
+                    local[j] = e >= 0 && e < E;
+                    wk[j] = __ldg(w + p);
+                }
+            }
+            float c[kBatch][4];
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j)
+                if (local[j]) load4<F32>(C2v, (t * topk + k0 + j) * H + n, c[j]);
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j)
+                if (local[j])
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) acc[i] = __fadd_rn(acc[i], __fmul_rn(wk[j], c[j][i]));
+        }
+        uint2 o;
+        o.x = pack_bf16x2(acc[0], acc[1]);
+        o.y = pack_bf16x2(acc[2], acc[3]);
+        *reinterpret_cast<uint2*>(out + t * H + n) = o;
+    }
+}
+
 cudaError_t launch_combine(const void* C2, bool c2_f32, const int32_t* topk_ids, const float* topk_w, int T,
                            int topk, int E, int H, uint16_t* out, cudaStream_t stream) {
-    const int64_t nvec = (int64_t)T * (H / 8);
-    if (nvec == 0) return cudaSuccess;
+    if ((int64_t)T * H == 0) return cudaSuccess;
     const int threads = 256;
+    const int64_t sms = device_info().sm_count;
+    // one thread per 4 columns fits in about one wave of 256-thread blocks per SM
+    const bool few = (int64_t)T * (H / 4) <= sms * threads;
+    const int64_t nvec = few ? (int64_t)T * (H / 4) : (int64_t)T * (H / 8);
     int64_t blocks = ceil_div64(nvec, threads);
-    const int64_t cap = (int64_t)device_info().sm_count * 8;
-    if (blocks > cap) blocks = cap;
-    if (c2_f32)
+    if (blocks > sms * 8) blocks = sms * 8;
+    if (few) {
+        if (c2_f32)
+            combine_few_kernel<true><<<(unsigned)blocks, threads, 0, stream>>>(C2, topk_ids, topk_w, T, topk, E, H, out);
+        else
+            combine_few_kernel<false><<<(unsigned)blocks, threads, 0, stream>>>(C2, topk_ids, topk_w, T, topk, E, H,
+                                                                               out);
+    } else if (c2_f32) {
         combine_kernel<true><<<(unsigned)blocks, threads, 0, stream>>>(C2, topk_ids, topk_w, T, topk, E, H, out);
-    else
+    } else {
         combine_kernel<false><<<(unsigned)blocks, threads, 0, stream>>>(C2, topk_ids, topk_w, T, topk, E, H, out);
+    }
     return cudaGetLastError();
 }
 

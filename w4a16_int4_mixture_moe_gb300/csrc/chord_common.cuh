@@ -197,6 +197,19 @@ __device__ __forceinline__ void dequant_row8(uint32_t w, uint32_t sp, uint32_t* 
 
 __host__ __device__ __forceinline__ int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// q = v / d, r = v % d for v >= 0, d > 0: 32-bit division while v fits (the
+// grid-stride element loops), 64-bit above.
+__device__ __forceinline__ int64_t divmod_idx(int64_t v, int d, int& r) {
+    if (v <= 0x7fffffffLL) {
+        const uint32_t q = (uint32_t)v / (uint32_t)d;
+        r = (int)((uint32_t)v - q * (uint32_t)d);
+        return (int64_t)q;
+    }
+    const int64_t q = v / d;
+    r = (int)(v - q * d);
+    return q;
+}
+
 // SiLU(g) * u in FP32: g / (1 + exp(-g)), then times u, with the fast
 // exponential and division intrinsics (a few float ulps from the correctly
 // rounded forms, far below the bf16 rounding that follows).  Large -g gives

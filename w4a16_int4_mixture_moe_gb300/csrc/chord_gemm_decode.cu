@@ -138,7 +138,7 @@ __device__ __forceinline__ void chunk_mma(const uint8_t* cb, int row0, uint32_t 
 template <int NT, int STAGES, int MI, int NV>
 __device__ __forceinline__ bool consume_item(const GemmArgs& a, uint8_t* smem, uint64_t* full, uint64_t* empty,
                                           volatile int* flags, int64_t& stage, int warp, int lane, int nt,
-                                          int32_t my_id) {
+                                          int32_t my_id, int ks0, int ks1, int slice) {
     constexpr int kStage = Cfg<NT>::kStageBytes;
     const int g = lane >> 2, c = lane & 3;
     // lane (g, c) reads the two code words (c & 1) * 2, +1 of the 32-column
@@ -156,8 +156,7 @@ __device__ __forceinline__ bool consume_item(const GemmArgs& a, uint8_t* smem, u
 #pragma unroll
             for (int q = 0; q < 4; ++q) acc[mi][t][q] = 0.0f;
 
-    const int kstages = (a.K + kKS - 1) / kKS;
-    for (int ks = 0; ks < kstages; ++ks, ++stage) {
+    for (int ks = ks0; ks < ks1; ++ks, ++stage) {
         const int slot = (int)(stage % STAGES);
         const uint32_t par = (uint32_t)((stage / STAGES) & 1);
         if (!mbar_wait(&full[slot], par) || flags[1]) {
@@ -185,7 +184,12 @@ __device__ __forceinline__ bool consume_item(const GemmArgs& a, uint8_t* smem, u
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 if (p[u] < 0) continue;
-                if (a.silu) {
+                if (a.ksplit > 1) {
+                    // K slice `slice`: FP32 partial sums in packed row order
+                    float* prow = a.partial + ((int64_t)slice * a.num_pairs + p[u]) * a.N;
+                    prow[n0] = acc[mi][t][u];
+                    prow[n0 + 8] = acc[mi][t][2 + u];
+                } else if (a.silu) {
                     // packed rows n0 = 16k + g and n0 + 8 hold gate and up of
                     // column j = 8k + g (layout 3)
                     __nv_bfloat16* hrow = static_cast<__nv_bfloat16*>(a.C) + (int64_t)p[u] * (a.N / 2);
@@ -213,7 +217,7 @@ __global__ void __launch_bounds__(Cfg<NT, MI>::kThreads, MINB) gemm_decode_kerne
     constexpr int kStage = Cfg<NT>::kStageBytes;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * kStage);
     uint64_t* empty = full + STAGES;
-    volatile int* flags = reinterpret_cast<volatile int*>(empty + STAGES);  // [0] skip, [1] abort
+    volatile int* flags = reinterpret_cast<volatile int*>(empty + STAGES);  // [0] skip, [1] abort, [2] ntp
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -227,10 +231,11 @@ __global__ void __launch_bounds__(Cfg<NT, MI>::kThreads, MINB) gemm_decode_kerne
         }
         fence_barrier_init();
     }
+    if (threadIdx.x == 32) flags[2] = *a.ntp;   // read while thread 0 checks the header
     __syncthreads();
     if (flags[0]) return;
 
-    int32_t ntp = *a.ntp;
+    int32_t ntp = flags[2];
     if (ntp < 0 || ntp > a.capacity || ntp % a.block_m) {
         if (threadIdx.x == 0) set_error(a.err, CHORD_DEV_BAD_PADDED);
         ntp = 0;
@@ -239,6 +244,9 @@ __global__ void __launch_bounds__(Cfg<NT, MI>::kThreads, MINB) gemm_decode_kerne
     const int ntiles = a.N / kBN;
     const int64_t n_items = (int64_t)(ntp / a.block_m) * nsub * ntiles;
     const int kstages = (a.K + kKS - 1) / kKS;
+    // Work unit = (item, K slice): slice s of S takes stages [s*kstages/S, (s+1)*kstages/S)
+    const int S = a.ksplit > 1 ? a.ksplit : 1;
+    const int64_t n_units = n_items * S;
     const int kchunks = a.K / 64;
     const uint64_t expert_bytes = (uint64_t)a.N * (uint64_t)a.K * 9ull / 16ull;
     const uint8_t* wbase = a.packed + kHeaderBytes;
@@ -248,7 +256,10 @@ __global__ void __launch_bounds__(Cfg<NT, MI>::kThreads, MINB) gemm_decode_kerne
         const uint64_t pol = policy_evict_first();
         int64_t stage = 0;
         bool aborted = false;
-        for (int64_t item = blockIdx.x; item < n_items && !aborted; item += gridDim.x) {
+        for (int64_t unit = blockIdx.x; unit < n_units && !aborted; unit += gridDim.x) {
+            const int64_t item = unit / S;
+            const int slice = (int)(unit % S);
+            const int ks0 = slice * kstages / S, ks1 = (slice + 1) * kstages / S;
             const int nt = (int)(item % ntiles);
             const int64_t bs = item / ntiles;
             const int sub = (int)(bs % nsub);
@@ -268,7 +279,7 @@ __global__ void __launch_bounds__(Cfg<NT, MI>::kThreads, MINB) gemm_decode_kerne
             const uint16_t* arow = rows.id >= 0 ? a.A + (int64_t)arow_i * a.K : nullptr;
             const int npairs = (32 - __clz(rows.vmask) + 1) / 2;
             const int half_lane = lane >> 4, piece = lane & 15;
-            for (int ks = 0; ks < kstages; ++ks) {
+            for (int ks = ks0; ks < ks1; ++ks) {
                 const int slot = (int)(stage % STAGES);
                 const uint32_t par = (uint32_t)((stage / STAGES) & 1);
                 if (!mbar_wait(&empty[slot], par ^ 1u) || flags[1]) {
@@ -310,28 +321,32 @@ __global__ void __launch_bounds__(Cfg<NT, MI>::kThreads, MINB) gemm_decode_kerne
 
     // -------------------------------------------------------------- consumers
     int64_t stage = 0;
-    for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
+    for (int64_t unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
+        const int64_t item = unit / S;
+        const int slice = (int)(unit % S);
+        const int ks0 = slice * kstages / S, ks1 = (slice + 1) * kstages / S;
         const int nt = (int)(item % ntiles);
         const int64_t bs = item / ntiles;
         const int sub = (int)(bs % nsub);
         const int64_t b = bs / nsub;
         const int e = a.expert_ids[b];
         if (e < 0 || e >= a.E) continue;
-        const ItemRows rows = load_item_rows<NT>(a, b, sub, lane, a.err);
+        const ItemRows rows = load_item_rows<NT>(a, b, sub, lane, slice == 0 ? a.err : nullptr);
         if (rows.vmask == 0) continue;
         const int nv = (32 - __clz(rows.vmask) + 7) / 8;   // 8-token tiles up to the last valid slot
         bool ok;
         if (nv <= 1)
-            ok = consume_item<NT, STAGES, MI, 1>(a, smem, full, empty, flags, stage, warp, lane, nt, rows.id);
+            ok = consume_item<NT, STAGES, MI, 1>(a, smem, full, empty, flags, stage, warp, lane, nt, rows.id, ks0, ks1,
+                                                  slice);
         else if (nv == 2 || NT == 2)
             ok = consume_item<NT, STAGES, MI, (NT >= 2 ? 2 : 1)>(a, smem, full, empty, flags, stage, warp, lane,
-                                                                 nt, rows.id);
+                                                                 nt, rows.id, ks0, ks1, slice);
         else if (nv == 3)
             ok = consume_item<NT, STAGES, MI, (NT >= 4 ? 3 : 1)>(a, smem, full, empty, flags, stage, warp, lane,
-                                                                 nt, rows.id);
+                                                                 nt, rows.id, ks0, ks1, slice);
         else
             ok = consume_item<NT, STAGES, MI, (NT >= 4 ? 4 : 1)>(a, smem, full, empty, flags, stage, warp, lane,
-                                                                 nt, rows.id);
+                                                                 nt, rows.id, ks0, ks1, slice);
         if (!ok) return;
     }
 }
@@ -353,7 +368,8 @@ cudaError_t launch_nt(const GemmArgs& a, cudaStream_t stream) {
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::kThreads, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
-    const int64_t items_cap = (a.capacity / a.block_m) * ((a.block_m + NT * 8 - 1) / (NT * 8)) * (a.N / kBN);
+    const int64_t items_cap = (a.capacity / a.block_m) * ((a.block_m + NT * 8 - 1) / (NT * 8)) * (a.N / kBN) *
+                              (a.ksplit > 1 ? a.ksplit : 1);
     int64_t grid = (int64_t)device_info().sm_count * per_sm;
     if (grid > items_cap) grid = items_cap;
     if (grid < 1) grid = 1;

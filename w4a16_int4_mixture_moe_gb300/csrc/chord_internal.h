@@ -31,6 +31,9 @@ cudaError_t launch_grouped_contiguous_index(const int32_t* m_indices, int64_t M,
 cudaError_t launch_grouped_masked_index(const int32_t* masked_m, int G, int max_m, int block_m, int32_t* sorted_ids,
                                         int32_t* expert_ids, int32_t* ntp, int64_t capacity, int* err,
                                         cudaStream_t stream);
+cudaError_t launch_splitk_reduce(const float* partial, int S, int64_t num_pairs, int64_t id_limit, int N,
+                                 const int32_t* sorted_ids, const int32_t* ntp, int64_t capacity, void* C, int out_f32,
+                                 int silu, cudaStream_t stream);
 cudaError_t launch_silu_mul(const uint16_t* C1, const int32_t* topk_ids, int64_t P, int E, int I, uint16_t* h,
                             cudaStream_t stream);
 cudaError_t launch_combine(const void* C2, bool c2_f32, const int32_t* topk_ids, const float* topk_w, int T,
@@ -54,6 +57,8 @@ struct GemmArgs {
     int out_f32;
     uint32_t layout;   // packed layout the header must name: 2, or 3 with silu
     int silu;          // fused SiLU * up epilogue (rows interleaved gate/up by 8)
+    int ksplit;        // K slices (warp-level kernel): > 1 writes FP32 partial sums to `partial`
+    float* partial;    // [ksplit, num_pairs, N], reduced by launch_splitk_reduce
     int* err;
 };
 
