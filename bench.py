@@ -501,9 +501,16 @@ def main():
              chord.chord_gemm_workspace_bytes(P, H, I, bm, f32_out))
     gws = torch.empty(max(16, *split), dtype=torch.uint8, device=dev)
 
-    def gate_up(st):
+    def gemm1(st):
         chord.chord_w4a16_moe_gemm(xd, topk, p13, E, 2 * I, H, sorted_ids, expert_ids, ntp, bm, P,
                                    h if fused else C1, workspace=gws, opts=silu_opts, stream=st)
+
+    def gate_up(st, marks=None):
+        if marks:
+            marks[0].record(st)
+        gemm1(st)
+        if marks:
+            marks[1].record(st)
         if not fused:
             chord.chord_silu_mul(C1, idd, E, h, stream=st)
 
@@ -513,14 +520,12 @@ def main():
 
     def step(st, marks=None):
         chord.chord_moe_align(idd, E, bm, sorted_ids, expert_ids, ntp, aws, stream=st)
-        if marks:
-            marks[0].record(st)
-        gate_up(st)
-        if marks:
-            marks[1].record(st)
-        down(st)
+        gate_up(st, marks)
         if marks:
             marks[2].record(st)
+        down(st)
+        if marks:
+            marks[3].record(st)
         chord.chord_moe_combine(C2, idd, wd, E, out, stream=st)
 
     # align: one launch up to 4096 pairs, three above; gate_up (+ SiLU * up pass), down, combine; K-split reductions
@@ -549,7 +554,7 @@ def main():
     # The GEMMs are timed inside the step: a second capture of it carries
     # timing events around gate_up and down (event record nodes).
     try:
-        marks = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)]
+        marks = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
         g_marked = capture(lambda st: step(st, marks))
     except (TypeError, RuntimeError):
         marks = g_marked = None
@@ -603,15 +608,15 @@ def main():
             if small["step"]:
                 flush.zero_()
             g_marked.replay()
-            marks[2].synchronize()
+            marks[3].synchronize()
             g1 += marks[0].elapsed_time(marks[1])
-            g2 += marks[1].elapsed_time(marks[2])
+            g2 += marks[2].elapsed_time(marks[3])
         g1 /= nrep
         g2 /= nrep
         gemm_timing = "events inside the step's graph"
     else:
         # each GEMM's graph replayed alone
-        g1 = timed(capture(gate_up), nrep, "gate_up") / nrep
+        g1 = timed(capture(gemm1), nrep, "gate_up") / nrep
         g2 = timed(capture(down), nrep, "down") / nrep
         gemm_timing = "each GEMM's graph replayed alone"
 
@@ -658,7 +663,13 @@ def main():
                      f"one step routes to fit in the {L2_BYTES / 1e6:.0f} MB L2, so a "
                      f"{2 * L2_BYTES / 1e6:.0f} MB buffer is written between steps, outside the timed events")
     cfg["silu_mul"] = "fused into gate_up" if fused else "separate pass"
-    cfg["split_k"] = {"gate_up": split[0] // max(1, P * 2 * I * 4) or 1, "down": split[1] // max(1, P * H * 4) or 1}
+    def split_desc(nbytes, N, K):
+        if nbytes == 0:
+            return "none"
+        if chord.chord_select_kernel(bm, N, K) == chord.KERNEL_TCGEN05:
+            return "tcgen05 split tail (last partial wave in K slices, decided on the device)"
+        return f"{nbytes // (P * N * 4)} K slices"
+    cfg["split_k"] = {"gate_up": split_desc(split[0], 2 * I, H), "down": split_desc(split[1], H, I)}
     kind = "warp_mma" if chord.chord_select_kernel(bm, 2 * I, H) == chord.KERNEL_WARP_MMA else "tc"
     kname = KERNEL_NAME[kind] + " (gate_up)"
     if regime == "decode":

@@ -111,7 +111,9 @@ typedef struct chord_opts {
                             ("trusted routing validation" of the deployment notes) */
     int32_t split_k;     /* K slices of the warp-level kernel: 0 = automatic, 1 = off,
                             > 1 = that many (capped at K / 128 rounded up); < 0 is
-                            refused.  The tcgen05 kernel never splits. */
+                            refused.  tcgen05 kernel: 1 = no split tail, otherwise
+                            the tail splits when the workspace holds it (> 1: an
+                            error when it does not). */
     int32_t out_dtype;   /* GEMM output: CHORD_DTYPE_BF16 (default) or CHORD_DTYPE_F32,
                             the FP32 sums unrounded (for a consumer that keeps FP32) */
     int32_t epilogue;    /* chord_epilogue (GEMM and layer) */
@@ -228,13 +230,18 @@ int chord_select_kernel(int block_m, int N, int K);
 
 /* ------------------------------------------------------------------- GEMM */
 
-/* Scratch bytes chord_w4a16_moe_gemm needs for the given call shape: the FP32
- * partial sums of its K slices, S * num_pairs * N * 4 bytes, 0 when S = 1.
- * Pure host arithmetic (no device query).  The automatic S (opts->split_k =
- * 0, the warp-level kernel chosen): items = num_pairs * N / 128 bounds the
- * launch's (align block, 128-row tile) work items from above; when 2 * items
- * < 456 (152 SMs x 3 resident CTAs) S = min(ceil(456 / items), 16,
- * ceil(K / 128) / 2), else 1. */
+/* Scratch bytes chord_w4a16_moe_gemm needs for the given call shape.  Pure
+ * host arithmetic (no device query).
+ * Warp-level kernel: the FP32 partial sums of its K slices, S * num_pairs * N
+ * * 4 bytes, 0 when S = 1.  The automatic S (opts->split_k = 0):
+ * items = num_pairs * N / 128 bounds the launch's (align block, 128-row tile)
+ * work items from above; when 2 * items < 456 (152 SMs x 3 resident CTAs)
+ * S = min(ceil(456 / items), 16, ceil(K / 128) / 2), else 1.
+ * tcgen05 kernel: 152 * 128 * tok_tile * 4 bytes (tok_tile = block_m rounded
+ * up to 16), 0 with opts->split_k = 1.  The kernel runs its items on one
+ * persistent CTA per SM; the items of the last partial wave (known only on
+ * the device) are cut into S = min(CTAs / tail items, 16, K stages / MMA
+ * issuers) K slices whose FP32 sums a second launch adds in order. */
 size_t chord_gemm_workspace_bytes(int64_t num_pairs, int N, int K, int block_m,
                                   const chord_opts *opts);
 
@@ -261,7 +268,8 @@ size_t chord_gemm_workspace_bytes(int64_t num_pairs, int N, int K, int block_m,
  * block_m must equal the value given to chord_moe_align, be a multiple of 8 and
  * at most 256; N % 128 == 0, K % 64 == 0.
  *   workspace  device, 16-byte aligned, >= chord_gemm_workspace_bytes(...) for
- *            K slices.  With S > 1 slices, slice s sums K stages
+ *            K slices (warp-level) or the split tail (tcgen05; the same in-order
+ *            reduction, results deterministic).  With S > 1 slices, slice s sums K stages
  *            [s * ks / S, (s + 1) * ks / S) (ks = ceil(K / 128)) into FP32
  *            partials, and a second launch adds slices 0 .. S-1 in order (FP32)
  *            and applies the output type or the SiLU * up epilogue; results

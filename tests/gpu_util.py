@@ -39,6 +39,24 @@ def assert_close(got_bits, ref_bits, what=""):
     return float(err.max()) if err.size else 0.0
 
 
+def assert_close_layer(got_bits, ref_bits, what=""):
+    """A whole layer against the oracle's: the tolerance 1e-2 + 1e-2|ref| for at
+    least 99.5% of the elements; the rest may differ by the propagation of
+    one-ulp BF16 flips of the gate_up output and of SiLU*up (two valid FP32
+    summation orders round an intermediate differently; the oracle recomputed
+    with float64 sums shows the same effect), bounded by 5% of the token's
+    output RMS, with the error RMS below 0.2% of the output RMS."""
+    g, r = f64(got_bits), f64(ref_bits)
+    err = np.abs(g - r)
+    inside = err <= ATOL + RTOL * np.abs(r)
+    rms = np.sqrt((r ** 2).mean(axis=1, keepdims=True)) + 1e-30
+    msg = (f"{what}: {int((~inside).sum())} of {inside.size} outside the per-element tolerance, "
+           f"max err {err.max():.4g}, max err/rms {(err / rms).max():.4g}")
+    assert inside.mean() >= 0.995, msg
+    assert (err <= ATOL + RTOL * np.abs(r) + 0.05 * rms).all(), msg
+    assert np.sqrt((err ** 2).mean()) <= 2e-3 * np.sqrt((r ** 2).mean()) + 1e-6, msg
+
+
 def assert_close_h(got_bits, ref_bits, what=""):
     """For h = bf16(SiLU(g) * u) computed from this library's own bf16 gate and
     up sums: a last-place flip of one of those roundings (an FP32 summation

@@ -166,9 +166,11 @@ def test_split_k_choice(lib, monkeypatch):
     """K slices of the warp-level kernel: the automatic choice cuts K only
     when num_pairs x N / 128 items fill less than half of 456 resident CTAs,
     into ceil(456 / items) slices, at most 16 and at most half the 128-column
-    K stages; an explicit count is capped at the number of stages; the
-    tcgen05 kernel never splits.  The workspace holds S x num_pairs x N FP32
-    partial sums."""
+    K stages; an explicit count is capped at the number of stages.  The
+    workspace holds S x num_pairs x N FP32 partial sums.  The tcgen05 kernel
+    splits only its last partial wave; its workspace is 152 units of
+    128 x tok_tile FP32 sums (tok_tile = block_m rounded up to 16), none with
+    split_k = 1."""
     monkeypatch.delenv("CHORD_KERNEL", raising=False)
     ws = chord.chord_gemm_workspace_bytes
     assert ws(8, 512, 7168, 8) == 15 * 8 * 512 * 4          # 32 items -> 15 slices
@@ -178,7 +180,9 @@ def test_split_k_choice(lib, monkeypatch):
     assert ws(8, 7168, 256, 8) == 0                         # 448 items fill the GPU
     assert ws(128, 512, 7168, 8) == 0                       # 512 items
     assert ws(40, 512, 7168, 8) == 3 * 40 * 512 * 4         # 160 items -> 3 slices
-    assert ws(8, 512, 7168, 256) == 0                       # tcgen05 block size
+    assert ws(8, 512, 7168, 256) == 152 * 128 * 256 * 4     # tcgen05: the split tail
+    assert ws(8, 512, 7168, 200) == 152 * 128 * 208 * 4
+    assert ws(8, 512, 7168, 256, chord.ChordOpts(split_k=1)) == 0
     opts = chord.ChordOpts(split_k=1)
     assert ws(8, 512, 7168, 8, opts) == 0
     opts = chord.ChordOpts(split_k=7)
@@ -186,9 +190,9 @@ def test_split_k_choice(lib, monkeypatch):
     opts = chord.ChordOpts(split_k=99)
     assert ws(8, 512, 384, 8, opts) == 3 * 8 * 512 * 4      # 3 stages
     opts = chord.ChordOpts(split_k=4, kernel=chord.KERNEL_TCGEN05)
-    assert ws(8, 512, 7168, 8, opts) == 0
+    assert ws(8, 512, 7168, 8, opts) == 152 * 128 * 16 * 4
     monkeypatch.setenv("CHORD_KERNEL", "1")
-    assert ws(8, 512, 7168, 8) == 0
+    assert ws(8, 512, 7168, 8) == 152 * 128 * 16 * 4
     # an explicit split without its workspace is refused before any launch
     vp = ctypes.c_void_p
     big = vp(1 << 20)
@@ -199,6 +203,9 @@ def test_split_k_choice(lib, monkeypatch):
     o = chord.ChordOpts(split_k=-1)
     assert lib.chord_w4a16_moe_gemm(big, 8, 1, big, nbytes, 2, 128, 512, big, big, big, 8, 8, 8, big, None, 0,
                                     ctypes.byref(o), None) == 1
+    o = chord.ChordOpts(split_k=2, kernel=chord.KERNEL_TCGEN05)
+    assert lib.chord_w4a16_moe_gemm(big, 8, 1, big, nbytes, 2, 128, 512, big, big, big, 256, 256, 8, big, big,
+                                    1024, ctypes.byref(o), None) == 4
 
 
 def test_argument_errors_before_any_launch(lib):

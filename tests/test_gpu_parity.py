@@ -10,7 +10,8 @@ import torch
 import oracle
 import w4a16_int4_mixture_moe_gb300 as chord
 import workloads as wl
-from gpu_util import (DEV, KERNELS, align, assert_close, assert_close_h, dbf, dev, f64, gemm, host_bits, layer, pack, valid_rows)
+from gpu_util import (DEV, KERNELS, align, assert_close, assert_close_h, assert_close_layer, dbf, dev, f64, gemm, host_bits,
+                      layer, pack, valid_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -409,6 +410,109 @@ def test_layer_one_token_split_k_vs_oracle():
         assert bm == 8
         ref = oracle.moe_layer(x, ids, wts, (c13, s13), (c2, s2), E, block_m=bm)
         assert_close(host_bits(out), ref, f"one-token layer fused={fused}")
+
+
+# ------------------------------------------------- tcgen05 split tail
+
+TC = chord.KERNEL_TCGEN05
+
+
+def tail_case(bm, K, seed, exact, T=100, topk=8, E=8, N=2560):
+    """8 experts x 20 N tiles = 160 items (320 with two blocks per expert) on
+    152 persistent CTAs: whole waves plus a tail that the kernel cuts into K
+    slices."""
+    rng = np.random.default_rng(seed)
+    if exact:
+        x = wl._bf16(rng.integers(-1, 2, size=(T, K)).astype(np.float32))
+        scales = np.full((E, N, K // 32), 0x3F80, np.uint16)
+    else:
+        x = wl.random_bf16(seed, (T, K))
+        scales = wl.random_scales(seed + 2, (E, N, K // 32))
+    codes = wl.random_codes(seed + 1, (E, N, K))
+    ids = wl.random_ids(seed + 3, T, topk, E, p_nonlocal=0.1)
+    return x, codes, scales, ids
+
+
+@pytest.mark.parametrize("bm,K,exact", [(256, 512, True), (256, 320, True), (256, 1024, False), (128, 1024, True),
+                                        (128, 640, False), (64, 2048, True)])
+def test_tc_tail_split_vs_oracle(bm, K, exact):
+    """The last partial wave's items in K slices (FP32 partials, in-order
+    reduction): bit-exact with the oracle in the exact-integer regime, within
+    tolerance on random data; bf16 and FP32 outputs; rows of non-local pairs
+    untouched; the same as the unsplit launch up to FP32 order."""
+    T, topk, E, N = 100, 8, 8, 2560
+    x, codes, scales, ids = tail_case(bm, K, bm + K, exact)
+    P = T * topk
+    packed = pack(codes, scales)
+    s, e, n = align(ids, E, bm)
+    s2, e2, n2 = oracle.moe_align(ids, E, bm)
+    assert chord.chord_gemm_workspace_bytes(P, N, K, bm) == 152 * 128 * ((bm + 15) // 16 * 16) * 4
+    got = host_bits(gemm(x, topk, packed, E, N, K, s, e, n, bm, P, kernel=TC, split_k=0))
+    ref = oracle.moe_gemm(x, topk, codes, scales, s2, e2, n2, bm, P, C=np.full((P, N), 0xFFFF, np.uint16))
+    rows = valid_rows(ids, E)
+    assert (got[np.setdiff1d(np.arange(P), rows)] == 0xFFFF).all()
+    if exact:
+        np.testing.assert_array_equal(got[rows], ref[rows])
+    else:
+        assert_close(got[rows], ref[rows], f"tail split bm={bm} K={K}")
+    plain = host_bits(gemm(x, topk, packed, E, N, K, s, e, n, bm, P, kernel=TC, split_k=1))
+    if exact:
+        np.testing.assert_array_equal(plain[rows], got[rows])
+    C = torch.full((P, N), float("nan"), dtype=torch.float32, device=DEV)
+    gemm(x, topk, packed, E, N, K, s, e, n, bm, P, kernel=TC, C=C, split_k=0, out_dtype=chord.DTYPE_F32)
+    got32 = C.cpu().numpy()
+    ref32 = oracle.moe_gemm_f32(x, topk, codes, scales, s2, e2, n2, bm, P)
+    if exact:
+        np.testing.assert_array_equal(got32[rows], ref32[rows])
+    else:
+        err = np.abs(got32[rows].astype(np.float64) - ref32[rows])
+        assert (err <= 1e-2 + 1e-2 * np.abs(ref32[rows])).all(), err.max()
+    assert chord.chord_get_device_error() == 0
+
+
+@pytest.mark.parametrize("bm", [256, 128])
+@pytest.mark.parametrize("exact", [True, False])
+def test_tc_tail_split_fused_silu_mul(bm, exact):
+    """SiLU * up applied by the tail reduction (layout 3).  Layout 3 puts other
+    rows in each N tile than layout 2, so the two GEMMs split different
+    items and sum some rows in another FP32 order: bit-identical to the layout-2
+    GEMM followed by chord_silu_mul in the exact-integer regime (every order
+    gives the same sums), close to the oracle on random data."""
+    T, topk, E, I, K = 100, 8, 8, 1280, 512
+    x, codes, scales, ids = tail_case(bm, K, 7 + bm, exact, N=2 * I)
+    P = T * topk
+    s, e, n = align(ids, E, bm)
+    h = torch.full((P, I), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+    gemm(x, topk, pack(codes, scales, chord.LAYOUT_GATE_UP_INTERLEAVED), E, 2 * I, K, s, e, n, bm, P, kernel=TC,
+         C=h, split_k=0, epilogue=chord.EPILOGUE_SILU_MUL)
+    got = host_bits(h)
+    C1 = gemm(x, topk, pack(codes, scales), E, 2 * I, K, s, e, n, bm, P, kernel=TC, split_k=0)
+    h2 = torch.full((P, I), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+    chord.chord_silu_mul(C1, dev(ids.ravel().copy()), E, h2)
+    rows = valid_rows(ids, E)
+    if exact:
+        np.testing.assert_array_equal(got[rows], host_bits(h2)[rows])
+    assert (got[np.setdiff1d(np.arange(P), rows)] == 0xFFFF).all()
+    s2, e2, n2 = oracle.moe_align(ids, E, bm)
+    c1 = oracle.moe_gemm(x, topk, codes, scales, s2, e2, n2, bm, P, C=np.zeros((P, 2 * I), np.uint16))
+    ref = oracle.silu_mul(c1, ids.ravel(), E, h=np.full((P, I), 0xFFFF, np.uint16))
+    assert_close_h(got[rows], ref[rows], f"tail split fused bm={bm}")
+
+
+def test_layer_tc_tail_split_vs_oracle():
+    """A layer whose gate_up GEMM (tcgen05, 160 items) splits its tail through
+    the layer workspace."""
+    T, topk, E, H, I, bm = 100, 8, 8, 1024, 1280, 256
+    ids = wl.random_ids(30, T, topk, E, p_nonlocal=0.1)
+    wts = wl.random_weights(31, T, topk)
+    x = wl.random_bf16(32, (T, H))
+    c13, s13 = wl.random_codes(33, (E, 2 * I, H)), wl.random_scales(34, (E, 2 * I, H // 32))
+    c2, s2 = wl.random_codes(35, (E, H, I)), wl.random_scales(36, (E, H, I // 32))
+    assert chord.chord_layer_workspace_bytes(T, topk, E, H, I, bm) > 152 * 128 * 256 * 4
+    out, _ = layer(x, ids, wts, E, E, I, pack(c13, s13), pack(c2, s2), bm=bm,
+                   opts=chord.ChordOpts(kernel=TC))
+    ref = oracle.moe_layer(x, ids, wts, (c13, s13), (c2, s2), E, block_m=bm)
+    assert_close_layer(host_bits(out), ref, "layer with a split tail")
 
 
 # ---------------------------------------------------------- fused SiLU * up

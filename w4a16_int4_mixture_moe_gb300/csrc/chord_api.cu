@@ -214,14 +214,31 @@ int gemm_split(int64_t num_pairs, int N, int K, int block_m, const chord_opts& o
 size_t split_bytes(int S, int64_t num_pairs, int N) {
     return S > 1 ? (size_t)S * (size_t)num_pairs * (size_t)N * 4 : 0;
 }
+
+// tcgen05 tail split: at most one unit of 128 rows x tok_tile FP32 sums per
+// CTA of the persistent grid (one CTA per SM for the configurations that use
+// it; the launch turns the split off when the grid outgrows the workspace).
+constexpr int64_t kTailSplitCtas = 152;
+
+size_t tc_tail_bytes(int block_m) {
+    const int64_t tok_tile = block_m < 16 ? 16 : (block_m + 15) / 16 * 16;
+    return (size_t)kTailSplitCtas * 128 * (size_t)tok_tile * 4;
+}
+
+// Workspace of one GEMM call: the warp-level kernel's K-slice partial sums, or
+// the tcgen05 kernel's split-tail partial sums.
+size_t gemm_ws_bytes(int64_t num_pairs, int N, int K, int block_m, const chord_opts& o) {
+    if (num_pairs <= 0 || N <= 0 || K <= 0 || block_m <= 0) return 0;
+    const int kernel = o.kernel ? o.kernel : chord_select_kernel(block_m, N, K);
+    if (kernel == CHORD_KERNEL_TCGEN05) return o.split_k == 1 || o.split_k < 0 ? 0 : tc_tail_bytes(block_m);
+    return split_bytes(gemm_split(num_pairs, N, K, block_m, o), num_pairs, N);
+}
 }  // namespace
 
 extern "C" {
 
 size_t chord_gemm_workspace_bytes(int64_t num_pairs, int N, int K, int block_m, const chord_opts* opts) {
-    if (num_pairs <= 0 || N <= 0 || K <= 0 || block_m <= 0) return 0;
-    const chord_opts o = opts_or_default(opts);
-    return split_bytes(gemm_split(num_pairs, N, K, block_m, o), num_pairs, N);
+    return gemm_ws_bytes(num_pairs, N, K, block_m, opts_or_default(opts));
 }
 
 chord_status chord_w4a16_moe_gemm(const void* A, int64_t a_rows, int a_row_divisor, const void* packed,
@@ -256,6 +273,15 @@ chord_status chord_w4a16_moe_gemm(const void* A, int64_t a_rows, int a_row_divis
                                                                                  : CHORD_ERR_INVALID_ARG;
         S = 1;
     }
+    // tcgen05: the split tail, when the workspace holds its partial sums
+    bool tail = false;
+    if (kernel == CHORD_KERNEL_TCGEN05 && o.split_k != 1) {
+        const size_t need = tc_tail_bytes(block_m);
+        if (workspace && aligned16(workspace) && workspace_bytes >= need)
+            tail = true;
+        else if (o.split_k > 1)
+            return workspace_bytes < need ? CHORD_ERR_BUFFER_TOO_SMALL : CHORD_ERR_INVALID_ARG;
+    }
     const DeviceInfo& di = device_info();
     if (!di.err) return CHORD_ERR_CUDA;
     if (capacity == 0 || num_pairs == 0) return CHORD_OK;
@@ -280,7 +306,9 @@ chord_status chord_w4a16_moe_gemm(const void* A, int64_t a_rows, int a_row_divis
     g.layout = silu ? CHORD_LAYOUT_GATE_UP_INTERLEAVED : CHORD_LAYOUT_TCGEN05;
     g.err = di.err;
     g.ksplit = S;
-    g.partial = S > 1 ? static_cast<float*>(workspace) : nullptr;
+    g.partial = (S > 1 || tail) ? static_cast<float*>(workspace) : nullptr;
+    g.partial_bytes = workspace_bytes;
+    g.tail_split = tail ? 1 : 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = kernel == CHORD_KERNEL_TCGEN05 ? launch_gemm_tc(g, s) : launch_gemm_decode(g, s);
     if (e == cudaSuccess && S > 1)
@@ -341,8 +369,8 @@ bool layer_ws(int T, int topk, int E, int H, int I, int block_m, LayerWs* w) {
     // the gate_up and the down projection, which run one after the other
     w->split = off;
     const chord_opts o = opts_or_default(nullptr);
-    const size_t s13 = split_bytes(gemm_split((int64_t)P, 2 * I, H, block_m, o), (int64_t)P, 2 * I);
-    const size_t s2 = split_bytes(gemm_split((int64_t)P, H, I, block_m, o), (int64_t)P, H);
+    const size_t s13 = gemm_ws_bytes((int64_t)P, 2 * I, H, block_m, o);
+    const size_t s2 = gemm_ws_bytes((int64_t)P, H, I, block_m, o);
     off = up256(off + (s13 > s2 ? s13 : s2));
     w->total = off;
     return true;

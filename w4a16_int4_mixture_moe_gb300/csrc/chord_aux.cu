@@ -583,6 +583,73 @@ __global__ void silu_mul_kernel(const uint16_t* __restrict__ C1, const int32_t* 
     }
 }
 
+// ============================================================================
+// Tail split of the tcgen05 kernel: for tail item i (item full + i of the
+// launch's plan), weight row r of its 128-row tile and token column j of its
+// block, C[id, 128 nt + r] = sum over slices s = 0 .. S-1, in that order, of
+// partial[i S + s, r, j], for the valid pair id at slot j; then the GEMM's
+// epilogue (bf16, FP32, or the layout-3 SiLU * up: gate row r, up row r + 8,
+// h column 64 nt + 8 (r / 16) + r % 8).  The plan is recomputed from
+// num_tokens_padded exactly as the GEMM computed it.  One thread per (item,
+// row or gate row, token); tokens are the fastest index (contiguous partials).
+// ============================================================================
+template <bool kSilu>
+__global__ void tc_tail_reduce_kernel(const GemmArgs a, int64_t G, int kstages, int min_stages, int tok_tile) {
+    int32_t ntp = *a.ntp;
+    if (ntp < 0 || ntp > a.capacity || ntp % a.block_m) return;   // the GEMM reported it and ran nothing
+    const int ntiles = a.N / 128;
+    const TailPlan tp = tail_plan((int64_t)(ntp / a.block_m) * ntiles, G, kstages, min_stages, true);
+    if (tp.S < 2) return;
+    constexpr int kRows = kSilu ? 64 : 128;
+    const int64_t per_item = (int64_t)kRows * tok_tile;
+    const int64_t total = tp.tail * per_item;
+    const int64_t slice = (int64_t)128 * tok_tile;
+    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < total; v += (int64_t)gridDim.x * blockDim.x) {
+        int rem;
+        const int64_t i = divmod_idx(v, (int)per_item, rem);
+        const int rr = rem / tok_tile, j = rem % tok_tile;
+        if (j >= a.block_m) continue;
+        const int64_t item = tp.full + i;
+        const int nt = (int)(item % ntiles);
+        const int64_t b = item / ntiles;
+        const int e = a.expert_ids[b];
+        if (e < 0 || e >= a.E) continue;
+        const int32_t id = a.sorted_ids[b * a.block_m + j];
+        if (id < 0 || (int64_t)id >= a.id_limit) continue;
+        const int r = kSilu ? 16 * (rr / 8) + rr % 8 : rr;
+        const float* src = a.partial + (i * tp.S * 128 + r) * tok_tile + j;
+        float g = 0.0f, u = 0.0f;
+        for (int s = 0; s < tp.S; ++s) {
+            g = __fadd_rn(g, __ldcg(src + s * slice));
+            if (kSilu) u = __fadd_rn(u, __ldcg(src + s * slice + 8 * tok_tile));
+        }
+        if (kSilu) {
+            const int h_col = nt * 64 + 8 * (r / 16) + r % 8;
+            static_cast<__nv_bfloat16*>(a.C)[(int64_t)id * (a.N / 2) + h_col] = silu_mul_bf16(g, u);
+        } else if (a.out_f32) {
+            static_cast<float*>(a.C)[(int64_t)id * a.N + nt * 128 + r] = g;
+        } else {
+            static_cast<__nv_bfloat16*>(a.C)[(int64_t)id * a.N + nt * 128 + r] = __float2bfloat16_rn(g);
+        }
+    }
+}
+
+cudaError_t launch_tc_tail_reduce(const GemmArgs& a, int64_t grid, int kstages, int min_stages, int tok_tile,
+                                  cudaStream_t stream) {
+    // the tail has fewer than `grid` items
+    const int64_t total = (grid - 1) * (int64_t)(a.silu ? 64 : 128) * tok_tile;
+    if (total <= 0) return cudaSuccess;
+    const int threads = 256;
+    int64_t blocks = ceil_div64(total, threads);
+    const int64_t cap = (int64_t)device_info().sm_count * 8;
+    if (blocks > cap) blocks = cap;
+    if (a.silu)
+        tc_tail_reduce_kernel<true><<<(unsigned)blocks, threads, 0, stream>>>(a, grid, kstages, min_stages, tok_tile);
+    else
+        tc_tail_reduce_kernel<false><<<(unsigned)blocks, threads, 0, stream>>>(a, grid, kstages, min_stages, tok_tile);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_splitk_reduce(const float* partial, int S, int64_t num_pairs, int64_t id_limit, int N,
                                  const int32_t* sorted_ids, const int32_t* ntp, int64_t capacity, void* C, int out_f32,
                                  int silu, cudaStream_t stream) {

@@ -197,6 +197,36 @@ __device__ __forceinline__ void dequant_row8(uint32_t w, uint32_t sp, uint32_t* 
 
 __host__ __device__ __forceinline__ int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Tail split of a persistent launch of n_items items over G CTAs in a static
+// round robin: the `full` = floor(n_items / G) * G items of the full waves run
+// whole; the `tail` items of the last partial wave would keep `tail` CTAs busy
+// for a whole item while the other G - tail idle, so each is cut into S K
+// slices (S = G / tail, at most 16 and at most kstages / min_stages, so every
+// slice holds >= min_stages stages), S = 1 when that gives fewer than two.
+// Work units: u < full -> item u; else v = u - full, item full + v / S, slice
+// v % S.  Computed from the device-side item count by every kernel that needs
+// it, so no plan is stored.
+struct TailPlan {
+    int64_t full, tail;
+    int S;
+};
+
+__host__ __device__ __forceinline__ TailPlan tail_plan(int64_t n_items, int64_t G, int kstages, int min_stages,
+                                                       bool enabled) {
+    TailPlan t;
+    t.full = G > 0 ? n_items / G * G : n_items;
+    t.tail = n_items - t.full;
+    t.S = 1;
+    if (enabled && t.tail > 0 && min_stages > 0) {
+        int64_t S = G / t.tail;
+        const int64_t cap = kstages / min_stages;
+        if (S > cap) S = cap;
+        if (S > 16) S = 16;
+        t.S = S < 2 ? 1 : (int)S;
+    }
+    return t;
+}
+
 // q = v / d, r = v % d for v >= 0, d > 0: 32-bit division while v fits (the
 // grid-stride element loops), 64-bit above.
 __device__ __forceinline__ int64_t divmod_idx(int64_t v, int d, int& r) {

@@ -223,6 +223,33 @@ struct Ring {
     }
 };
 
+// A work unit: an item with the K stages [ks0, ks1) it covers; pidx >= 0
+// marks a unit of the split tail (tail_plan), whose FP32 sums go to
+// partial[pidx] instead of C.
+struct Unit {
+    int64_t item;
+    int ks0, ks1;
+    int64_t pidx;
+};
+
+__device__ __forceinline__ Unit unit_at(int64_t u, const TailPlan& tp, int kstages) {
+    Unit r;
+    if (u < tp.full || tp.S == 1) {
+        r.item = u;
+        r.ks0 = 0;
+        r.ks1 = kstages;
+        r.pidx = -1;
+    } else {
+        const int64_t v = u - tp.full;
+        const int sl = (int)(v % tp.S);
+        r.item = tp.full + v / tp.S;
+        r.ks0 = sl * kstages / tp.S;
+        r.ks1 = (sl + 1) * kstages / tp.S;
+        r.pidx = v;
+    }
+    return r;
+}
+
 template <int GW, int MAXR, int NI>
 __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel(const TcArgs ta) {
     using C = Cfg<GW, MAXR, NI>;
@@ -292,6 +319,8 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
     const int kchunks = a.K / kChunkK;
     const int kstages = (kchunks + 1) / 2;   // the last stage holds one chunk when kchunks is odd
     const int64_t n_items = (int64_t)(ntp / a.block_m) * ntiles;
+    const TailPlan tplan = tail_plan(n_items, gridDim.x, kstages, NI, a.tail_split != 0);
+    const int64_t n_units = tplan.full + tplan.tail * tplan.S;
     const uint64_t expert_bytes = (uint64_t)a.N * (uint64_t)a.K * 9ull / 16ull;
 
     if (warp == C::kProducer) {
@@ -300,16 +329,17 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
         int64_t g = 0;   // stages lane 0 issued
         Ring wr;
         bool ok = true;
-        for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-            const int nt = (int)(item % ntiles);
-            const int64_t b = item / ntiles;
+        for (int64_t wu = blockIdx.x; wu < n_units && ok; wu += gridDim.x) {
+            const Unit un = unit_at(wu, tplan, kstages);
+            const int nt = (int)(un.item % ntiles);
+            const int64_t b = un.item / ntiles;
             const ItemInfo inf = item_info(a, b, lane, false);
             if (inf.n_mma == 0) continue;
             if (lane == 0) {
                 // chunks (nt, kc) of one expert are contiguous along kc
                 const uint8_t* src = a.packed + kHeaderBytes + (uint64_t)inf.e * expert_bytes +
                                      (uint64_t)nt * (uint64_t)kchunks * kChunk2;
-                for (int ks = 0; ks < kstages; ++ks, ++g, wr.next(NSW)) {
+                for (int ks = un.ks0; ks < un.ks1; ++ks, ++g, wr.next(NSW)) {
                     const int nck = min(2, kchunks - 2 * ks);
                     if (!wait_or_abort(&w_empty[wr.slot], wr.phase ^ 1u, &flags[1], a.err)) {
                         ok = false;
@@ -339,8 +369,9 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
         int issued = 0;                 // stages whose MMAs this issuer committed
         Ring ar, br, last;
         bool ok = true;
-        for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-            const int64_t b = item / ntiles;
+        for (int64_t wu = blockIdx.x; wu < n_units && ok; wu += gridDim.x) {
+            const Unit un = unit_at(wu, tplan, kstages);
+            const int64_t b = un.item / ntiles;
             const ItemInfo inf = item_info(a, b, lane, false);
             if (inf.n_mma == 0) continue;
             if (lane == 0) {
@@ -348,7 +379,7 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
                 tc_fence_after();
                 const uint32_t idesc = idesc_bf16(inf.n_mma);
                 bool any = false;
-                for (int ks = 0; ks < kstages && ok; ++ks, ar.next(SA), br.next(NSB)) {
+                for (int ks = un.ks0; ks < un.ks1 && ok; ++ks, ar.next(SA), br.next(NSB)) {
                     if (ks % NI != mi) continue;
                     const int nck = min(2, kchunks - 2 * ks);
                     if (!wait_or_abort(&a_full[ar.slot], ar.phase, &flags[1], a.err) ||
@@ -394,9 +425,10 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
         constexpr int kRowStep = GW * 4;
         Ring br;
         bool ok = true;
-        for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-            const int64_t b = item / ntiles;
-            const ItemInfo inf = item_info(a, b, lane, warp == C::kGather0);
+        for (int64_t wu = blockIdx.x; wu < n_units && ok; wu += gridDim.x) {
+            const Unit un = unit_at(wu, tplan, kstages);
+            const int64_t b = un.item / ntiles;
+            const ItemInfo inf = item_info(a, b, lane, warp == C::kGather0 && un.ks0 == 0);
             if (inf.n_mma == 0) continue;
             int32_t arow[MAXR];
 #pragma unroll
@@ -408,7 +440,7 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
                     if (row_valid(a, id)) arow[r] = a.a_row_divisor == 1 ? id : id / a.a_row_divisor;
                 }
             }
-            for (int ks = 0; ks < kstages; ++ks, br.next(NSB)) {
+            for (int ks = un.ks0; ks < un.ks1; ++ks, br.next(NSB)) {
                 const int nck = min(2, kchunks - 2 * ks);
                 if (!wait_or_abort(&b_empty[br.slot], br.phase ^ 1u, &flags[1], a.err)) {
                     ok = false;
@@ -443,12 +475,13 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
         int64_t g = 0, nitem = 0;
         Ring wr, ar;
         bool ok = true;
-        for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-            const int nt = (int)(item % ntiles);
-            const int64_t b = item / ntiles;
+        for (int64_t wu = blockIdx.x; wu < n_units && ok; wu += gridDim.x) {
+            const Unit un = unit_at(wu, tplan, kstages);
+            const int nt = (int)(un.item % ntiles);
+            const int64_t b = un.item / ntiles;
             const ItemInfo inf = item_info(a, b, lane, false);
             if (inf.n_mma == 0) continue;
-            for (int ks = 0; ks < kstages; ++ks, ++g, wr.next(NSW), ar.next(SA)) {
+            for (int ks = un.ks0; ks < un.ks1; ++ks, ++g, wr.next(NSW), ar.next(SA)) {
                 if ((int)(g & 1) != wg) continue;
                 const int nck = min(2, kchunks - 2 * ks);
                 if (!wait_or_abort(&w_full[wr.slot], wr.phase, &flags[1], a.err) ||
@@ -517,7 +550,8 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
             // the tile hold gate and up of output column 64 * nt + 8k + i
             const int h_col = nt * (kTileRows / 2) + 8 * (row / 16) + (row % 8);
             const bool gate_row = (lane & 8) == 0;
-            const int parts = kstages < NI ? kstages : NI;   // issuers that hold a share of this item
+            const int nst = un.ks1 - un.ks0;
+            const int parts = nst < NI ? nst : NI;   // issuers that hold a share of this unit
 #pragma unroll
             for (int it = 0; it < 8; ++it) {
                 const int j0 = wg * 16 + 32 * it;
@@ -533,6 +567,16 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
                     for (int u = 0; u < 16; ++u) v[u] = __float_as_uint(__uint_as_float(v[u]) + __uint_as_float(w2[u]));
                 }
                 tc_wait_ld();
+                if (un.pidx >= 0) {
+                    // a slice of a split tail item: its FP32 sums, row-major [row][token]
+                    float4* dst = reinterpret_cast<float4*>(
+                        a.partial + ((int64_t)un.pidx * kTileRows + row) * ta.tok_tile + j0);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                             __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+                    continue;
+                }
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
                     if (a.silu) {
@@ -644,8 +688,14 @@ cudaError_t launch_cfg(const GemmArgs& g, bool deep_weights, cudaStream_t stream
     int64_t grid = (int64_t)device_info().sm_count * per_sm;
     if (grid > items_cap) grid = items_cap;
     if (grid < 1) grid = 1;
+    // The split tail writes at most grid units of 128 x tok_tile FP32 sums (S * tail <= grid).
+    const size_t tail_bytes = (size_t)grid * kTileRows * (size_t)ta.tok_tile * sizeof(float);
+    ta.g.tail_split = (g.tail_split && g.partial && g.partial_bytes >= tail_bytes) ? 1 : 0;
     gemm_tc_kernel<GW, MAXR, NI><<<(unsigned)grid, C::kThreads, smem, stream>>>(ta);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    if (e != cudaSuccess || !ta.g.tail_split) return e;
+    const int kstages = (g.K / kChunkK + 1) / 2;
+    return launch_tc_tail_reduce(ta.g, grid, kstages, NI, ta.tok_tile, stream);
 }
 
 }  // namespace

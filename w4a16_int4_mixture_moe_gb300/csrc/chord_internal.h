@@ -58,7 +58,10 @@ struct GemmArgs {
     uint32_t layout;   // packed layout the header must name: 2, or 3 with silu
     int silu;          // fused SiLU * up epilogue (rows interleaved gate/up by 8)
     int ksplit;        // K slices (warp-level kernel): > 1 writes FP32 partial sums to `partial`
-    float* partial;    // [ksplit, num_pairs, N], reduced by launch_splitk_reduce
+    float* partial;    // warp-level: [ksplit, num_pairs, N], reduced by launch_splitk_reduce;
+                       // tcgen05 tail split: [tail units, 128, tok_tile], reduced by launch_tc_tail_reduce
+    size_t partial_bytes;
+    int tail_split;    // tcgen05: cut the last partial wave's items into K slices (needs `partial`)
     int* err;
 };
 
@@ -71,5 +74,11 @@ cudaError_t launch_gemm_decode(const GemmArgs& a, cudaStream_t stream);
 // the MMA's A operand, tokens as its N side, FP32 accumulators in tensor
 // memory.  block_m % 8 == 0, block_m <= 256, N % 128 == 0.
 cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t stream);
+
+// Tail split of the tcgen05 kernel (see tail_plan): partial[u, r, j] of tail
+// unit u = item_in_tail * S + slice, weight row r of the 128-row tile, token
+// column j < tok_tile; slices added in order, then the GEMM's epilogue.
+cudaError_t launch_tc_tail_reduce(const GemmArgs& a, int64_t grid, int kstages, int min_stages, int tok_tile,
+                                  cudaStream_t stream);
 
 }  // namespace chord
