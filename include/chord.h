@@ -216,8 +216,11 @@ chord_status chord_moe_align_noalloc(const int32_t *topk_ids, int T, int topk, i
 /* Host-side block size choice from tokens per expert (the article's tok_e =
  * routed rows / experts rule, section "Indexed kernels"): tok_e = T * topk /
  * E_global is the expected number of rows per local expert, known without
- * reading anything back.  Small tok_e gives a decode block (8..64), large
- * tok_e a prefill block.  Always returns a valid block_m. */
+ * reading anything back.  The block holds tok_e + 3 sqrt(tok_e) + 1 rows (a
+ * Poisson count's mean plus three standard deviations) rounded up to 16, 8 when
+ * that is at most 8, at most 256; 32 when that exceeds 32 but the mean plus two
+ * standard deviations fits 32 (the warp-level kernel's largest block).
+ * CHORD_BLOCK_M (environment) overrides.  Always returns a valid block_m. */
 int chord_select_block_m(int T, int topk, int E_local, int E_global, int N, int K);
 
 /* The kernel CHORD_KERNEL_AUTO runs for a GEMM of blocks of block_m rows and

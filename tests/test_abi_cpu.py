@@ -68,6 +68,10 @@ def test_select_block_m(lib):
     # tokens per expert (tok_e = T * topk / E_global) decides, not the token count
     assert chord.chord_select_block_m(512, 8, 48, 384, 4096, 7168) in (16, 32)   # tok_e ~ 10.7
     assert chord.chord_select_block_m(1, 8, 384, 384, 512, 7168) == 8
+    # tok_e 21.3: mean + 3 sd = 36.2 rows, mean + 2 sd = 31.6 -> the 32-row warp-level block
+    assert chord.chord_select_block_m(1024, 8, 384, 384, 512, 7168) == 32
+    # tok_e 24: mean + 2 sd = 34.8 -> 48
+    assert chord.chord_select_block_m(1152, 8, 384, 384, 512, 7168) == 48
     assert chord.chord_select_block_m(16, 2, 8, 8, 256, 256) in (8, 16)          # tok_e = 4
     prev = 0
     for T in (1, 16, 128, 512, 1024, 4096, 8192, 16384):

@@ -172,6 +172,12 @@ int chord_select_block_m(int T, int topk, int E_local, int E_global, int N, int 
     // block really holds, so a generous block costs only index padding.
     const double need = tok_e + 3.0 * sqrt(tok_e) + 1.0;
     if (need <= 8.0) return 8;
+    // Blocks of up to 32 rows run on the warp-level kernel, which streams
+    // weights faster than the tcgen05 kernel at these row counts (TP8 T=1024,
+    // tok_e 21: 542 us per layer with 32-row blocks against 580 with 48): when
+    // the mean plus two standard deviations still fits 32 rows, take 32 and let
+    // the rare larger expert use a second block.
+    if (need > 32.0 && tok_e + 2.0 * sqrt(tok_e) + 1.0 <= 32.0) return 32;
     int bm = (int)ceil(need / 16.0) * 16;
     if (bm > 256) bm = 256;
     return bm;

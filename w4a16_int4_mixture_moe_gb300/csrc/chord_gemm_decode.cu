@@ -209,6 +209,24 @@ __device__ __forceinline__ bool consume_item(const GemmArgs& a, uint8_t* smem, u
     return true;
 }
 
+// Work unit -> (align block b, token sub-block, 128-row N tile, K slice and
+// its stage range); 32-bit divisions while the unit index fits (always, in
+// practice), no slice arithmetic when K is not split.
+__device__ __forceinline__ int64_t unit_coords(int64_t unit, int S, int ntiles, int nsub, int kstages, int& slice,
+                                               int& nt, int& sub, int& ks0, int& ks1) {
+    int64_t item = unit;
+    slice = 0;
+    ks0 = 0;
+    ks1 = kstages;
+    if (S > 1) {
+        item = divmod_idx(unit, S, slice);
+        ks0 = slice * kstages / S;
+        ks1 = (slice + 1) * kstages / S;
+    }
+    const int64_t bs = divmod_idx(item, ntiles, nt);
+    return divmod_idx(bs, nsub, sub);
+}
+
 template <int NT, int STAGES, int MI, int MINB>
 __global__ void __launch_bounds__(Cfg<NT, MI>::kThreads, MINB) gemm_decode_kernel(const GemmArgs a) {
     constexpr int kConsumerWarps = Cfg<NT, MI>::kConsumerWarps;
@@ -257,13 +275,8 @@ __global__ void __launch_bounds__(Cfg<NT, MI>::kThreads, MINB) gemm_decode_kerne
         int64_t stage = 0;
         bool aborted = false;
         for (int64_t unit = blockIdx.x; unit < n_units && !aborted; unit += gridDim.x) {
-            const int64_t item = unit / S;
-            const int slice = (int)(unit % S);
-            const int ks0 = slice * kstages / S, ks1 = (slice + 1) * kstages / S;
-            const int nt = (int)(item % ntiles);
-            const int64_t bs = item / ntiles;
-            const int sub = (int)(bs % nsub);
-            const int64_t b = bs / nsub;
+            int slice, nt, sub, ks0, ks1;
+            const int64_t b = unit_coords(unit, S, ntiles, nsub, kstages, slice, nt, sub, ks0, ks1);
             const int e = a.expert_ids[b];
             if (e < 0 || e >= a.E) {
                 if (lane == 0) set_error(a.err, CHORD_DEV_BAD_EXPERT);
@@ -322,13 +335,8 @@ __global__ void __launch_bounds__(Cfg<NT, MI>::kThreads, MINB) gemm_decode_kerne
     // -------------------------------------------------------------- consumers
     int64_t stage = 0;
     for (int64_t unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
-        const int64_t item = unit / S;
-        const int slice = (int)(unit % S);
-        const int ks0 = slice * kstages / S, ks1 = (slice + 1) * kstages / S;
-        const int nt = (int)(item % ntiles);
-        const int64_t bs = item / ntiles;
-        const int sub = (int)(bs % nsub);
-        const int64_t b = bs / nsub;
+        int slice, nt, sub, ks0, ks1;
+        const int64_t b = unit_coords(unit, S, ntiles, nsub, kstages, slice, nt, sub, ks0, ks1);
         const int e = a.expert_ids[b];
         if (e < 0 || e >= a.E) continue;
         const ItemRows rows = load_item_rows<NT>(a, b, sub, lane, slice == 0 ? a.err : nullptr);

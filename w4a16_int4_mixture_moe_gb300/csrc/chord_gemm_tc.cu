@@ -331,8 +331,8 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
         bool ok = true;
         for (int64_t wu = blockIdx.x; wu < n_units && ok; wu += gridDim.x) {
             const Unit un = unit_at(wu, tplan, kstages);
-            const int nt = (int)(un.item % ntiles);
-            const int64_t b = un.item / ntiles;
+            int nt;
+            const int64_t b = divmod_idx(un.item, ntiles, nt);
             const ItemInfo inf = item_info(a, b, lane, false);
             if (inf.n_mma == 0) continue;
             if (lane == 0) {
@@ -371,7 +371,8 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
         bool ok = true;
         for (int64_t wu = blockIdx.x; wu < n_units && ok; wu += gridDim.x) {
             const Unit un = unit_at(wu, tplan, kstages);
-            const int64_t b = un.item / ntiles;
+            int nt_unused;
+            const int64_t b = divmod_idx(un.item, ntiles, nt_unused);
             const ItemInfo inf = item_info(a, b, lane, false);
             if (inf.n_mma == 0) continue;
             if (lane == 0) {
@@ -427,7 +428,8 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
         bool ok = true;
         for (int64_t wu = blockIdx.x; wu < n_units && ok; wu += gridDim.x) {
             const Unit un = unit_at(wu, tplan, kstages);
-            const int64_t b = un.item / ntiles;
+            int nt_unused;
+            const int64_t b = divmod_idx(un.item, ntiles, nt_unused);
             const ItemInfo inf = item_info(a, b, lane, warp == C::kGather0 && un.ks0 == 0);
             if (inf.n_mma == 0) continue;
             int32_t arow[MAXR];
@@ -477,8 +479,8 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
         bool ok = true;
         for (int64_t wu = blockIdx.x; wu < n_units && ok; wu += gridDim.x) {
             const Unit un = unit_at(wu, tplan, kstages);
-            const int nt = (int)(un.item % ntiles);
-            const int64_t b = un.item / ntiles;
+            int nt;
+            const int64_t b = divmod_idx(un.item, ntiles, nt);
             const ItemInfo inf = item_info(a, b, lane, false);
             if (inf.n_mma == 0) continue;
             for (int ks = un.ks0; ks < un.ks1; ++ks, ++g, wr.next(NSW), ar.next(SA)) {
