@@ -262,6 +262,8 @@ __global__ void __launch_bounds__(kAlignThreads) align_single_kernel(const int32
                                                                      int32_t* __restrict__ expert_ids,
                                                                      int64_t nblocks_cap, int32_t* __restrict__ ntp,
                                                                      int64_t capacity, int validate, int* err) {
+    pdl_trigger();
+    pdl_wait();
     extern __shared__ int32_t sm[];
     int32_t* run = sm;        // [E] histogram, then next free slot per expert
     int32_t* wcnt = sm + E;   // [kAlignWarps][E]
@@ -339,10 +341,8 @@ cudaError_t launch_align(const int32_t* topk_ids, int64_t P, int E, int block_m,
         attr_done[dev] = true;
     }
     if (nslices == 1) {
-        align_single_kernel<<<1, kAlignThreads, scatter_smem, stream>>>(topk_ids, P, E, block_m, sorted_ids,
-                                                                       expert_ids, capacity / block_m, ntp, capacity,
-                                                                       validate ? 1 : 0, err);
-        return cudaGetLastError();
+        return launch_pdl(pdl_for(P), align_single_kernel, dim3(1), dim3(kAlignThreads), scatter_smem, stream, topk_ids, P, E,
+                          block_m, sorted_ids, expert_ids, capacity / block_m, ntp, capacity, validate ? 1 : 0, err);
     }
     align_count_kernel<<<nslices, kAlignThreads, hist_smem, stream>>>(topk_ids, P, E, counts, sorted_ids, capacity,
                                                                       validate ? 1 : 0, err);
@@ -497,6 +497,8 @@ template <bool kSilu>
 __global__ void splitk_reduce_kernel(const float* __restrict__ partial, int S, int64_t num_pairs, int64_t id_limit,
                                      int N, const int32_t* __restrict__ sorted_ids, const int32_t* __restrict__ ntp,
                                      int64_t capacity, void* __restrict__ C, int out_f32) {
+    pdl_trigger();
+    pdl_wait();
     constexpr int kBatch = 8;
     const int out_cols = kSilu ? N / 2 : N;
     const int vpr = out_cols / 4;
@@ -563,6 +565,8 @@ __device__ __forceinline__ uint4 silu_mul8(uint4 gv, uint4 uv) {
 
 __global__ void silu_mul_kernel(const uint16_t* __restrict__ C1, const int32_t* __restrict__ ids, int64_t P, int E,
                                 int I, uint16_t* __restrict__ h) {
+    pdl_trigger();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
     const int vpr = I / 8;
@@ -595,6 +599,8 @@ __global__ void silu_mul_kernel(const uint16_t* __restrict__ C1, const int32_t* 
 // ============================================================================
 template <bool kSilu>
 __global__ void tc_tail_reduce_kernel(const GemmArgs a, int64_t G, int kstages, int min_stages, int tok_tile) {
+    pdl_trigger();
+    pdl_wait();
     int32_t ntp = *a.ntp;
     if (ntp < 0 || ntp > a.capacity || ntp % a.block_m) return;   // the GEMM reported it and ran nothing
     const int ntiles = a.N / 128;
@@ -643,11 +649,8 @@ cudaError_t launch_tc_tail_reduce(const GemmArgs& a, int64_t grid, int kstages, 
     int64_t blocks = ceil_div64(total, threads);
     const int64_t cap = (int64_t)device_info().sm_count * 8;
     if (blocks > cap) blocks = cap;
-    if (a.silu)
-        tc_tail_reduce_kernel<true><<<(unsigned)blocks, threads, 0, stream>>>(a, grid, kstages, min_stages, tok_tile);
-    else
-        tc_tail_reduce_kernel<false><<<(unsigned)blocks, threads, 0, stream>>>(a, grid, kstages, min_stages, tok_tile);
-    return cudaGetLastError();
+    return launch_pdl(pdl_for(a.num_pairs), a.silu ? tc_tail_reduce_kernel<true> : tc_tail_reduce_kernel<false>, dim3((unsigned)blocks),
+                      dim3(threads), 0, stream, a, grid, kstages, min_stages, tok_tile);
 }
 
 cudaError_t launch_splitk_reduce(const float* partial, int S, int64_t num_pairs, int64_t id_limit, int N,
@@ -659,13 +662,9 @@ cudaError_t launch_splitk_reduce(const float* partial, int S, int64_t num_pairs,
     int64_t blocks = ceil_div64(nvec, threads);
     const int64_t cap = (int64_t)device_info().sm_count * 16;
     if (blocks > cap) blocks = cap;
-    if (silu)
-        splitk_reduce_kernel<true><<<(unsigned)blocks, threads, 0, stream>>>(partial, S, num_pairs, id_limit, N,
-                                                                            sorted_ids, ntp, capacity, C, out_f32);
-    else
-        splitk_reduce_kernel<false><<<(unsigned)blocks, threads, 0, stream>>>(partial, S, num_pairs, id_limit, N,
-                                                                             sorted_ids, ntp, capacity, C, out_f32);
-    return cudaGetLastError();
+    return launch_pdl(pdl_for(num_pairs), silu ? splitk_reduce_kernel<true> : splitk_reduce_kernel<false>, dim3((unsigned)blocks),
+                      dim3(threads), 0, stream, partial, S, num_pairs, id_limit, N, sorted_ids, ntp, capacity, C,
+                      out_f32);
 }
 
 cudaError_t launch_silu_mul(const uint16_t* C1, const int32_t* topk_ids, int64_t P, int E, int I, uint16_t* h,
@@ -675,8 +674,7 @@ cudaError_t launch_silu_mul(const uint16_t* C1, const int32_t* topk_ids, int64_t
     int64_t blocks = ceil_div64(P, threads / 32);
     const int64_t cap = (int64_t)device_info().sm_count * 8;
     if (blocks > cap) blocks = cap;
-    silu_mul_kernel<<<(unsigned)blocks, threads, 0, stream>>>(C1, topk_ids, P, E, I, h);
-    return cudaGetLastError();
+    return launch_pdl(pdl_for(P), silu_mul_kernel, dim3((unsigned)blocks), dim3(threads), 0, stream, C1, topk_ids, P, E, I, h);
 }
 
 // ============================================================================
@@ -700,6 +698,8 @@ __device__ __forceinline__ void load4(const void* C2v, int64_t off, float (&c)[4
 template <bool F32>
 __global__ void combine_kernel(const void* __restrict__ C2v, const int32_t* __restrict__ ids,
                                const float* __restrict__ w, int T, int topk, int E, int H, uint16_t* __restrict__ out) {
+    pdl_trigger();
+    pdl_wait();
     const int vpr = H / 8;
     const int64_t nvec = (int64_t)T * vpr;
     for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nvec; v += (int64_t)gridDim.x * blockDim.x) {
@@ -737,6 +737,8 @@ __global__ void combine_kernel(const void* __restrict__ C2v, const int32_t* __re
 template <bool F32>
 __global__ void combine_few_kernel(const void* __restrict__ C2v, const int32_t* __restrict__ ids,
                                const float* __restrict__ w, int T, int topk, int E, int H, uint16_t* __restrict__ out) {
+    pdl_trigger();
+    pdl_wait();
     constexpr int kBatch = 8;
     const int vpr = H / 4;
     const int64_t nvec = (int64_t)T * vpr;
@@ -786,18 +788,10 @@ cudaError_t launch_combine(const void* C2, bool c2_f32, const int32_t* topk_ids,
     const int64_t nvec = few ? (int64_t)T * (H / 4) : (int64_t)T * (H / 8);
     int64_t blocks = ceil_div64(nvec, threads);
     if (blocks > sms * 8) blocks = sms * 8;
-    if (few) {
-        if (c2_f32)
-            combine_few_kernel<true><<<(unsigned)blocks, threads, 0, stream>>>(C2, topk_ids, topk_w, T, topk, E, H, out);
-        else
-            combine_few_kernel<false><<<(unsigned)blocks, threads, 0, stream>>>(C2, topk_ids, topk_w, T, topk, E, H,
-                                                                               out);
-    } else if (c2_f32) {
-        combine_kernel<true><<<(unsigned)blocks, threads, 0, stream>>>(C2, topk_ids, topk_w, T, topk, E, H, out);
-    } else {
-        combine_kernel<false><<<(unsigned)blocks, threads, 0, stream>>>(C2, topk_ids, topk_w, T, topk, E, H, out);
-    }
-    return cudaGetLastError();
+    auto kern = few ? (c2_f32 ? combine_few_kernel<true> : combine_few_kernel<false>)
+                    : (c2_f32 ? combine_kernel<true> : combine_kernel<false>);
+    return launch_pdl(pdl_for((int64_t)T * topk), kern, dim3((unsigned)blocks), dim3(threads), 0, stream, C2, topk_ids,
+                      topk_w, T, topk, E, H, out);
 }
 
 }  // namespace chord

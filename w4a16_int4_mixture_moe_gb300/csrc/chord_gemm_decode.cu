@@ -229,6 +229,8 @@ __device__ __forceinline__ int64_t unit_coords(int64_t unit, int S, int ntiles, 
 
 template <int NT, int STAGES, int MI, int MINB>
 __global__ void __launch_bounds__(Cfg<NT, MI>::kThreads, MINB) gemm_decode_kernel(const GemmArgs a) {
+    pdl_trigger();
+    pdl_wait();
     constexpr int kConsumerWarps = Cfg<NT, MI>::kConsumerWarps;
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int kTok = Cfg<NT>::kTok;
@@ -381,8 +383,7 @@ cudaError_t launch_nt(const GemmArgs& a, cudaStream_t stream) {
     int64_t grid = (int64_t)device_info().sm_count * per_sm;
     if (grid > items_cap) grid = items_cap;
     if (grid < 1) grid = 1;
-    kern<<<(unsigned)grid, C::kThreads, smem, stream>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(pdl_for(a.num_pairs), kern, dim3((unsigned)grid), dim3(C::kThreads), (size_t)smem, stream, a);
 }
 
 }  // namespace

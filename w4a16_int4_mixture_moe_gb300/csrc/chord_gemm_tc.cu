@@ -252,6 +252,8 @@ __device__ __forceinline__ Unit unit_at(int64_t u, const TailPlan& tp, int kstag
 
 template <int GW, int MAXR, int NI>
 __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel(const TcArgs ta) {
+    pdl_trigger();
+    pdl_wait();
     using C = Cfg<GW, MAXR, NI>;
     const int SA = ta.nsa;
     const GemmArgs& a = ta.g;
@@ -693,8 +695,7 @@ cudaError_t launch_cfg(const GemmArgs& g, bool deep_weights, cudaStream_t stream
     // The split tail writes at most grid units of 128 x tok_tile FP32 sums (S * tail <= grid).
     const size_t tail_bytes = (size_t)grid * kTileRows * (size_t)ta.tok_tile * sizeof(float);
     ta.g.tail_split = (g.tail_split && g.partial && g.partial_bytes >= tail_bytes) ? 1 : 0;
-    gemm_tc_kernel<GW, MAXR, NI><<<(unsigned)grid, C::kThreads, smem, stream>>>(ta);
-    e = cudaGetLastError();
+    e = launch_pdl(pdl_for(g.num_pairs), gemm_tc_kernel<GW, MAXR, NI>, dim3((unsigned)grid), dim3(C::kThreads), smem, stream, ta);
     if (e != cudaSuccess || !ta.g.tail_split) return e;
     const int kstages = (g.K / kChunkK + 1) / 2;
     return launch_tc_tail_reduce(ta.g, grid, kstages, NI, ta.tok_tile, stream);
