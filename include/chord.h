@@ -292,7 +292,12 @@ chord_status chord_w4a16_moe_gemm(const void *A, int64_t a_rows, int a_row_divis
 /* The article's two grouped contracts ("Grouped SM90 kernels"), served by the
  * same kernels through routing arrays built on the device (one row per pair).
  * Weights are packed as for chord_w4a16_moe_gemm (CHORD_LAYOUT_TCGEN05); the
- * epilogue, out_dtype and kernel options apply as there.
+ * epilogue, out_dtype and kernel options apply as there.  The workspace sizes
+ * below hold the routing arrays (sorted ids, expert ids, padded count, each
+ * 256-byte aligned) and, when the block size exceeds 32 rows (the tcgen05
+ * kernel), the GEMM's split-tail partial sums (152 * 128 * tok_tile * 4
+ * bytes); a workspace holding only the routing arrays is accepted and runs the
+ * GEMM without the split tail.
  *
  * Contiguous (prefill): A [M, K] holds each expert's rows contiguously (the
  * article pads each expert's segment to a multiple of 128 rows); m_indices[m]

@@ -112,17 +112,22 @@ def test_select_kernel_by_regime(lib, monkeypatch):
 
 def test_grouped_workspace_and_argument_errors(lib):
     """Grouped contracts: workspace = sorted ids + expert ids + padded count,
-    each 256-byte aligned; bad arguments are refused before any launch."""
+    each 256-byte aligned, plus the tcgen05 split tail (152 x 128 x tok_tile
+    FP32) for blocks of more than 32 rows; bad arguments are refused before
+    any launch."""
     up = lambda x: (x + 255) // 256 * 256
+    tail = lambda bm: 152 * 128 * ((bm + 15) // 16 * 16) * 4 if bm > 32 else 0
     for M, E in ((0, 4), (1, 1), (128, 2), (12288, 48)):
         bmc = chord.chord_select_block_m(M, 1, E, E, 0, 0)
         cap = (-(-M // bmc) + E) * bmc
-        assert chord.chord_grouped_contiguous_workspace_bytes(M, E) == up(up(up(cap * 4) + cap // bmc * 4) + 4)
+        assert chord.chord_grouped_contiguous_workspace_bytes(M, E) == (up(up(up(cap * 4) + cap // bmc * 4) + 4)
+                                                                         + tail(bmc))
+    assert chord.chord_select_block_m(12288, 1, 48, 48, 0, 0) > 32   # the EP8 prefill case carries the tail
     assert chord.chord_grouped_contiguous_workspace_bytes(128, 5000) == 0
     G, max_m, em = 48, 40, 11
     bm = chord.chord_select_block_m(em, 1, 1, 1, 4096, 7168)
     cap = G * -(-max_m // bm) * bm
-    assert chord.chord_grouped_masked_workspace_bytes(G, max_m, em) == up(up(up(cap * 4) + cap // bm * 4) + 4)
+    assert chord.chord_grouped_masked_workspace_bytes(G, max_m, em) == up(up(up(cap * 4) + cap // bm * 4) + 4) + tail(bm)
     assert chord.chord_grouped_masked_workspace_bytes(0, 8, 4) == 0
     vp = ctypes.c_void_p
     big = vp(1 << 20)

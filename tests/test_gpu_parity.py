@@ -601,6 +601,34 @@ def test_grouped_contiguous_vs_oracle(kernel, counts, NK):
     assert_close(got[m_idx >= 0], ref[m_idx >= 0], f"{kernel} grouped contiguous {counts} N={N} K={K}")
 
 
+def test_grouped_contiguous_split_tail_exact():
+    """Eight experts of 100 rows (128-row segments, one block each) x 20 N
+    tiles = 160 tcgen05 items on 152 CTAs: the tail splits through the grouped
+    workspace.  Exact-integer regime: bit-exact with the oracle, and with a
+    workspace that holds only the routing arrays (no split)."""
+    counts = [100] * 8
+    E, N, K = 8, 2560, 1024
+    m_idx = contiguous_rows(counts)
+    M = m_idx.size
+    rng = np.random.default_rng(5)
+    x = wl._bf16(rng.integers(-1, 2, size=(M, K)).astype(np.float32))
+    codes = wl.random_codes(6, (E, N, K))
+    scales = np.full((E, N, K // 32), 0x3F80, np.uint16)
+    packed = pack(codes, scales)
+    ref = oracle.grouped_contiguous(x, m_idx, codes, scales, C=np.full((M, N), 0xFFFF, np.uint16))
+    full = chord.chord_grouped_contiguous_workspace_bytes(M, E)
+    bm = chord.chord_select_block_m(M, 1, E, E, 0, 0)
+    assert 128 <= bm <= 256
+    for nbytes in (full, full - 152 * 128 * ((bm + 15) // 16 * 16) * 4):
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+        C = torch.full((M, N), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+        chord.chord_grouped_contiguous_gemm(dbf(x), dev(m_idx), packed, E, N, K, C, ws)
+        got = host_bits(C)
+        assert (got[m_idx < 0] == 0xFFFF).all()
+        np.testing.assert_array_equal(got[m_idx >= 0], ref[m_idx >= 0])
+    assert chord.chord_get_device_error() == 0
+
+
 def test_grouped_contiguous_split_expert_is_reported():
     """An expert whose rows are not one contiguous run breaks the contract: the
     device error word says so (validate mode turns it into a status)."""

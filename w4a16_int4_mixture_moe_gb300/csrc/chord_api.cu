@@ -458,6 +458,13 @@ static size_t grouped_ws(int64_t cap, int block_m) {
     return up256(off + 4);
 }
 
+// Routing arrays plus, for blocks the tcgen05 kernel takes (more than 32
+// rows), room for its split tail; a workspace with only the routing arrays
+// runs the GEMM without the split.
+static size_t grouped_ws_total(int64_t cap, int block_m) {
+    return grouped_ws(cap, block_m) + (block_m > kDecodeMaxBlockM ? tc_tail_bytes(block_m) : 0);
+}
+
 static int masked_block_m(int expected_m, int N, int K) {
     return chord_select_block_m(expected_m, 1, 1, 1, N, K);
 }
@@ -474,7 +481,7 @@ constexpr int kGroupedMaxExperts = 4000;   // the index builder's per-expert tab
 size_t chord_grouped_contiguous_workspace_bytes(int64_t M, int E) {
     if (M < 0 || E <= 0 || E > kGroupedMaxExperts) return 0;
     const int bm = contiguous_block_m(M, E);
-    return grouped_ws(contiguous_capacity(M, E, bm), bm);
+    return grouped_ws_total(contiguous_capacity(M, E, bm), bm);
 }
 
 chord_status chord_grouped_contiguous_gemm(const void* A, int64_t M, const int32_t* m_indices, const void* packed,
@@ -496,14 +503,15 @@ chord_status chord_grouped_contiguous_gemm(const void* A, int64_t M, const int32
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (launch_grouped_contiguous_index(m_indices, M, E, bm, sorted, experts, ntp, cap, di.err, s) != cudaSuccess)
         return CHORD_ERR_CUDA;
-    return chord_w4a16_moe_gemm(A, M, 1, packed, packed_bytes, E, N, K, sorted, experts, ntp, cap, bm, M, C,
-                                nullptr, 0, opts, stream);
+    const size_t idx = grouped_ws(cap, bm);
+    return chord_w4a16_moe_gemm(A, M, 1, packed, packed_bytes, E, N, K, sorted, experts, ntp, cap, bm, M, C, ws + idx,
+                                workspace_bytes - idx, opts, stream);
 }
 
 size_t chord_grouped_masked_workspace_bytes(int G, int max_m, int expected_m) {
     if (G <= 0 || G > kGroupedMaxExperts || max_m < 0 || expected_m <= 0) return 0;
     const int bm = masked_block_m(expected_m, 0, 0);
-    return grouped_ws((int64_t)G * ((max_m + bm - 1) / bm) * bm, bm);
+    return grouped_ws_total((int64_t)G * ((max_m + bm - 1) / bm) * bm, bm);
 }
 
 chord_status chord_grouped_masked_gemm(const void* A, int G, int max_m, const int32_t* masked_m, int expected_m,
@@ -527,8 +535,9 @@ chord_status chord_grouped_masked_gemm(const void* A, int G, int max_m, const in
     if (launch_grouped_masked_index(masked_m, G, max_m, bm, sorted, experts, ntp, cap, di.err, s) != cudaSuccess)
         return CHORD_ERR_CUDA;
     const int64_t rows = (int64_t)G * max_m;
+    const size_t idx = grouped_ws(cap, bm);
     return chord_w4a16_moe_gemm(A, rows, 1, packed, packed_bytes, G, N, K, sorted, experts, ntp, cap, bm, rows, C,
-                                nullptr, 0, opts, stream);
+                                ws + idx, workspace_bytes - idx, opts, stream);
 }
 
 chord_status chord_get_device_error(void* stream, int32_t* code) {
