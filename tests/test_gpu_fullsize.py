@@ -93,8 +93,8 @@ def test_layer_full_size_stagewise(w):
     bm = chord.chord_select_block_m(w.T, w.topk, w.E, w.E_global, 2 * w.I, w.H)
     s, e, n = align(ids, w.E, bm)
     P = w.P
-    # gate_up on the real activations
-    C1 = host_bits(gemm(x, w.topk, p13, w.E, 2 * w.I, w.H, s, e, n, bm, P))
+    # gate_up on the real activations (with its workspace: split-K or split tail as the bench runs it)
+    C1 = host_bits(gemm(x, w.topk, p13, w.E, 2 * w.I, w.H, s, e, n, bm, P, split_k=0))
     assert_close(C1[pairs][rows], C1r[rows], f"{w.name} gate_up (block_m={bm})")
     del C1
     # SiLU*up on the oracle's C1
@@ -109,8 +109,7 @@ def test_layer_full_size_stagewise(w):
     hin = wl.random_bf16(w.seed + 17, (P, w.I))
     hin[pairs] = hr
     C2d = torch.full((P, w.H), float("nan"), dtype=torch.float32, device=DEV)
-    chord.chord_w4a16_moe_gemm(dbf(hin), 1, p2, w.E, w.H, w.I, s, e, n, bm, P, C2d,
-                               opts=chord.ChordOpts(out_dtype=chord.DTYPE_F32))
+    gemm(hin, 1, p2, w.E, w.H, w.I, s, e, n, bm, P, C=C2d, split_k=0, out_dtype=chord.DTYPE_F32)
     C2g = C2d[torch.from_numpy(pairs).to(DEV)].cpu().numpy()
     del C2d
     err = np.abs(C2g[rows].astype(np.float64) - C2r[rows])
@@ -137,11 +136,13 @@ def test_fused_gate_up_full_size(w):
     p13i = pack(w13[0], w13[1], chord.LAYOUT_GATE_UP_INTERLEAVED)
     bm = chord.chord_select_block_m(w.T, w.topk, w.E, w.E_global, 2 * w.I, w.H)
     s, e, n = align(ids, w.E, bm)
+    # The warp-level kernel runs with its workspace (K slices where the bench splits); the tcgen05
+    # kernel without, since its split tail cuts other rows for layout 3 than for layout 2.
+    split = 0 if chord.chord_select_kernel(bm, 2 * w.I, w.H) == chord.KERNEL_WARP_MMA else None
     hd = torch.empty((w.P, w.I), dtype=torch.bfloat16, device=DEV)
-    chord.chord_w4a16_moe_gemm(dbf(x), w.topk, p13i, w.E, 2 * w.I, w.H, s, e, n, bm, w.P, hd,
-                               opts=chord.ChordOpts(epilogue=chord.EPILOGUE_SILU_MUL))
+    gemm(x, w.topk, p13i, w.E, 2 * w.I, w.H, s, e, n, bm, w.P, C=hd, split_k=split, epilogue=chord.EPILOGUE_SILU_MUL)
     del p13i
-    C1 = gemm(x, w.topk, p13, w.E, 2 * w.I, w.H, s, e, n, bm, w.P)
+    C1 = gemm(x, w.topk, p13, w.E, 2 * w.I, w.H, s, e, n, bm, w.P, split_k=split)
     h2 = torch.empty((w.P, w.I), dtype=torch.bfloat16, device=DEV)
     chord.chord_silu_mul(C1, dev(ids), w.E, h2)
     del C1
@@ -188,9 +189,9 @@ def test_gemm_full_size_sampled_pairs(w):
     bm = chord.chord_select_block_m(w.T, w.topk, w.E, w.E_global, 2 * w.I, w.H)
     s, e, n = align(ids, w.E, bm)
     P = w.P
-    C1 = gemm(x, w.topk, p13, w.E, 2 * w.I, w.H, s, e, n, bm, P)
+    C1 = gemm(x, w.topk, p13, w.E, 2 * w.I, w.H, s, e, n, bm, P, split_k=0)
     h = wl.random_bf16(99, (P, w.I))
-    C2 = gemm(h, 1, p2, w.E, w.H, w.I, s, e, n, bm, P)
+    C2 = gemm(h, 1, p2, w.E, w.H, w.I, s, e, n, bm, P, split_k=0)
     got1, got2 = host_bits(C1), host_bits(C2)
     flat = ids.ravel()
     local = np.nonzero((flat >= 0) & (flat < w.E))[0]
