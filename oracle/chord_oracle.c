@@ -110,8 +110,12 @@ void orc_dequant_pairs(const uint8_t *q, const uint16_t *s, size_t n, uint16_t *
  *
  * blob  = 256-byte header, then E expert regions of N*K*9/16 bytes each.
  * header (little endian): u32 magic 0x44524843 ("CHRD"), u32 version 1,
- *        u32 layout (1, 2 or 3), u32 group 32, u32 E, u32 N, u32 K, u32 0,
- *        u64 expert_stride = N*K*9/16, u64 data_offset = 256, then zeros.
+ *        u32 layout (1, 2 or 3), u32 group 32, u32 E, u32 N, u32 K,
+ *        u32 scale_range, u64 expert_stride = N*K*9/16, u64 data_offset = 256,
+ *        then zeros.  scale_range is 1 when every scale of the blob is a
+ *        positive normal bf16 below 0.5 (2^-126 <= s < 0.5), else 0: a fact
+ *        about the weights that the header records so that a kernel may pick a
+ *        dequantisation valid on that range; it does not change any value.
  *
  * Layout 1 ("m16 x k64 fragment chunks", N % 16 == 0, K % 64 == 0).
  * An expert region is a sequence of 576-byte chunks, chunk (kc, mt) at
@@ -237,6 +241,18 @@ static size_t scale_pos(int layout, int N, int K, int n, int grp)
     }
 }
 
+/* 1 when every one of the n scales is a positive normal bf16 below 0.5, read
+ * from its value: sign clear, biased exponent between 1 and 125. */
+uint32_t orc_scale_range(const uint16_t *scales, size_t n)
+{
+    for (size_t i = 0; i < n; ++i) {
+        unsigned sign = scales[i] >> 15, expo = (scales[i] >> 7) & 0xFFu;
+        if (sign != 0 || expo < 1 || expo > 125)
+            return 0u;
+    }
+    return 1u;
+}
+
 int orc_pack(const uint8_t *codes, const uint16_t *scales, int E, int N, int K, int layout,
              uint8_t *out, size_t out_bytes)
 {
@@ -252,6 +268,7 @@ int orc_pack(const uint8_t *codes, const uint16_t *scales, int E, int N, int K, 
     put32(out + 16, (uint32_t)E);
     put32(out + 20, (uint32_t)N);
     put32(out + 24, (uint32_t)K);
+    put32(out + 28, orc_scale_range(scales, (size_t)E * (size_t)N * (size_t)(K / ORC_GROUP)));
     put64(out + 32, stride);
     put64(out + 40, ORC_HDR);
     int G = K / ORC_GROUP;

@@ -45,6 +45,22 @@ def test_pack_byte_exact(layout, shape):
 
 
 @pytest.mark.parametrize("layout", [1, 2, 3])
+@pytest.mark.parametrize("planted", [0x3C00, 0x3EFF, 0x0080, 0x3F00, 0x0040, 0x0000, 0x8000, 0xBC00, 0x7FC0])
+def test_pack_scale_range_word_byte_exact(layout, planted):
+    """Header word 7 (every scale in [2^-126, 0.5)) is set by the packer that
+    sees all scales: one planted scale in the last expert decides it, on the
+    GPU as in the oracle, and the rest of the blob is unchanged."""
+    E, N, K = 3, 256, 128
+    codes = wl.random_codes(7, (E, N, K))
+    scales = wl.random_scales(8, (E, N, K // 32))
+    scales[E - 1, N - 3, 1] = planted
+    got = pack(codes, scales, layout).cpu().numpy()
+    want = oracle.pack(codes, scales, layout)
+    np.testing.assert_array_equal(got, want)
+    assert int(got[28:32].view(np.uint32)[0]) == int(planted in (0x3C00, 0x3EFF, 0x0080))
+
+
+@pytest.mark.parametrize("layout", [1, 2, 3])
 def test_pack_bad_code_sets_error_word(layout):
     codes = np.zeros((1, 128, 64), np.uint8)
     codes[0, 5, 7] = 17
@@ -157,15 +173,18 @@ BOTH = pytest.mark.parametrize("kernel", ["tcgen05", "warp_mma"])
 @BOTH
 @pytest.mark.parametrize("bm", [8, 16, 24, 32, 64, 128, 256])
 @pytest.mark.parametrize("K", [256, 2048])
-def test_gemm_exact_integer_regime_bit_exact(kernel, bm, K):
-    """x in {-1, 0, 1}, scales 1.0: sums are exact integers in any order, so the
-    GPU must match the oracle bit for bit (catches any wrong index, lost or
-    doubled K chunk, or token/row mix-up)."""
+@pytest.mark.parametrize("scale", [0x3F80, 0x3E80])
+def test_gemm_exact_integer_regime_bit_exact(kernel, bm, K, scale):
+    """x in {-1, 0, 1}, scales 1.0 or 0.25: sums are exact multiples of the
+    scale in any order, so the GPU must match the oracle bit for bit (catches
+    any wrong index, lost or doubled K chunk, or token/row mix-up).  Scale 1.0
+    lies outside [2^-126, 0.5) and takes the subtract-then-scale instructions,
+    0.25 the warp-level kernel's one-FMA dequantisation."""
     T, topk, E, N = 40, 4, 5, 256
     rng = np.random.default_rng(bm * 100 + K)
     xi = rng.integers(-1, 2, size=(T, K)).astype(np.float32)
     x = wl._bf16(xi)
-    scales = np.full((E, N, K // 32), 0x3F80, np.uint16)
+    scales = np.full((E, N, K // 32), scale, np.uint16)
     run_gemm_case(T, topk, E, N, K, bm, seed=bm + K, x=x, scales=scales, exact=True, kernel=kernel)
 
 
@@ -191,6 +210,37 @@ def test_gemm_dequant_bit_exact_one_hot(kernel, bm):
                                np.repeat(scales[0], 32, axis=1).T.copy().ravel()).reshape(K, N)
     # a zero weight times a negative scale is -0; a sum that starts from +0 returns +0
     deq = np.where(deq == 0x8000, np.uint16(0), deq)
+    np.testing.assert_array_equal(got, deq)
+
+
+@BOTH
+@pytest.mark.parametrize("bm", [8, 16, 32, 64, 128])
+def test_gemm_dequant_bit_exact_one_hot_fma_range(kernel, bm):
+    """As above with every scale a positive bf16 in [2^-126, 0.5): the packer
+    sets header word 7 and the warp-level kernel takes the one-FMA
+    dequantisation (the tcgen05 kernel keeps subtract-then-scale; both must
+    agree).  Exponents over that whole range, random mantissas, and both ends
+    (2^-126 and the largest bf16 below 0.5).  Every code times every such scale
+    must equal the oracle's bf16((q - 8) * s), q = 8 giving +0."""
+    K, N, E = 128, 256, 1
+    T = K
+    x = np.zeros((T, K), np.float32)
+    x[np.arange(T), np.arange(K)] = 1.0
+    x = wl._bf16(x)
+    codes = wl.random_codes(95 + bm, (E, N, K))
+    rng = np.random.default_rng(96)
+    expo = rng.integers(1, 126, size=(E, N, K // 32)).astype(np.uint16)
+    mant = rng.integers(0, 128, size=(E, N, K // 32)).astype(np.uint16)
+    scales = (expo << 7) | mant
+    scales[0, 0, :] = [0x0080, 0x3EFF, 0x0080, 0x3EFF]
+    scales[0, 1, :] = [0x3EFF, 0x0080, 0x00FF, 0x3E80]
+    ids = np.zeros((T, 1), np.int32)
+    packed = pack(codes, scales, KERNELS[kernel][1])
+    assert int(packed[28:32].cpu().numpy().view(np.uint32)[0]) == 1
+    got, ref = run_gemm_case(T, 1, E, N, K, bm, seed=0, div=1, x=x, codes=codes, scales=scales, ids=ids,
+                             exact=True, kernel=kernel)
+    deq = oracle.dequant_pairs(codes[0].T.copy().ravel(),
+                               np.repeat(scales[0], 32, axis=1).T.copy().ravel()).reshape(K, N)
     np.testing.assert_array_equal(got, deq)
 
 

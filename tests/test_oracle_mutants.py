@@ -47,6 +47,9 @@ MUTANTS = [
     ("contiguous_takes_padding", "if (m_indices[m] == e)\n                rows[nr++] = m;",
      "if (m_indices[m] == e || m_indices[m] == -1)\n                rows[nr++] = m;"),
     ("masked_row_stride", "rows[r] = (int64_t)g * max_m + r;", "rows[r] = (int64_t)g * masked_m[g] + r;"),
+    ("scale_range_half_included", "if (sign != 0 || expo < 1 || expo > 125)", "if (sign != 0 || expo < 1 || expo > 126)"),
+    ("scale_range_subnormal_included", "if (sign != 0 || expo < 1 || expo > 125)", "if (sign != 0 || expo > 125)"),
+    ("scale_range_sign_ignored", "if (sign != 0 || expo < 1 || expo > 125)", "if (expo < 1 || expo > 125)"),
     ("combine_nonlocal", "if (topk_ids[p] < 0 || topk_ids[p] >= E)\n                    continue;\n                float v",
      "if (topk_ids[p] >= E)\n                    continue;\n                float v"),
 ]

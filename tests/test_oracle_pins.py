@@ -111,13 +111,40 @@ def test_pack_header(orc, layout):
     h = blob[:256]
     u32 = h[:32].view(np.uint32)
     assert bytes(h[:4]) == b"CHRD"
-    assert list(u32[1:8]) == [1, layout, 32, 3, 128, 128, 0]
+    # word 7: every random scale (|N(0, 0.02)| + 1e-3) is a positive normal bf16 below 0.5
+    assert list(u32[1:8]) == [1, layout, 32, 3, 128, 128, 1]
     assert list(h[32:48].view(np.uint64)) == [128 * 128 * 9 // 16, 256]
     assert not h[48:].any()
     assert orc.check_header(blob, 3, 128, 128, layout)
     for other in {1, 2, 3} - {layout}:
         assert not orc.check_header(blob, 3, 128, 128, other)
     assert not orc.check_header(blob, 3, 64, 256, layout)
+
+
+# (one scale planted among scales of 2^-7, header word 7 expected): the bf16
+# bit patterns by hand — 0.5 = 0x3F00 (exponent 126), the largest bf16 below
+# 0.5 = 0x3EFF (exponent 125, mantissa 127), the smallest normal 2^-126 =
+# 0x0080, 2^-127 is subnormal (0x0040).
+SCALE_RANGE_CASES = [(0x3C00, 1), (0x3EFF, 1), (0x0080, 1), (0x3F00, 0), (0x3F80, 0), (0x0040, 0), (0x0000, 0),
+                     (0x8000, 0), (0xBC00, 0), (0x8080, 0), (0x7F80, 0), (0x7FC0, 0)]
+
+
+@pytest.mark.parametrize("layout", [1, 2, 3])
+@pytest.mark.parametrize("planted,flag", SCALE_RANGE_CASES)
+def test_pack_header_scale_range(orc, layout, planted, flag):
+    """Header word 7 is 1 exactly when every scale lies in [2^-126, 0.5) and is
+    positive; one planted scale anywhere decides it, and nothing else in the
+    blob depends on it (codes and scales unpack unchanged)."""
+    assert wl._bf16(np.array([0.5, 0.498046875, 2.0 ** -126, 2.0 ** -127, 2.0 ** -7], np.float32)).tolist() == [
+        0x3F00, 0x3EFF, 0x0080, 0x0040, 0x3C00]
+    codes = wl.random_codes(3, (2, 128, 128))
+    scales = np.full((2, 128, 4), 0x3C00, np.uint16)
+    scales[1, 77, 2] = planted
+    blob = orc.pack(codes, scales, layout)
+    assert int(blob[28:32].view(np.uint32)[0]) == flag
+    c2, s2 = orc.unpack(blob, 2, 128, 128, layout)
+    np.testing.assert_array_equal(c2, codes)
+    np.testing.assert_array_equal(s2, scales)
 
 
 @pytest.mark.parametrize("layout,N,K", [(1, 32, 128), (2, 256, 128), (3, 256, 128)])

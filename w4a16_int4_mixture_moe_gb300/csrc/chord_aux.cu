@@ -29,6 +29,13 @@ __device__ __forceinline__ int canonical_row(int p, int N, bool interleaved) {
     return i < 8 ? 8 * g + i : (N >> 1) + 8 * g + (i - 8);
 }
 
+// Header word 7 (written as 1 by header_kernel, earlier on the stream) drops
+// to 0 when any scale lies outside [2^-126, 0.5); every writer stores the same
+// 0, so the unordered stores agree.  `data` is the first word after the header.
+__device__ __forceinline__ void clear_scale_range(uint32_t* data) {
+    reinterpret_cast<volatile uint32_t*>(data - kHeaderBytes / 4)[kHdrScaleRangeWord] = 0u;
+}
+
 __global__ void pack2_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ scales, int E, int N,
                              int K, bool interleaved, uint32_t* __restrict__ out, int* err) {
     constexpr int kWords = 4608 / 4;
@@ -59,6 +66,7 @@ __global__ void pack2_kernel(const uint8_t* __restrict__ codes, const uint16_t* 
             const int r = wi - 1024;
             const int64_t row = (int64_t)e * N + canonical_row(nt * 128 + r, N, interleaved);
             v = (uint32_t)scales[row * G + 2 * kc] | ((uint32_t)scales[row * G + 2 * kc + 1] << 16);
+            if (!scale_in_fma_range(v & 0xffffu) || !scale_in_fma_range(v >> 16)) clear_scale_range(out);
         }
         out[w] = v;
     }
@@ -76,6 +84,7 @@ __device__ __forceinline__ void write_header(uint8_t* packed, int64_t tid, int E
             case 4: v = (uint32_t)E; break;
             case 5: v = (uint32_t)N; break;
             case 6: v = (uint32_t)K; break;
+            case kHdrScaleRangeWord: v = 1u; break;   // cleared by the pack kernel on an out-of-range scale
             case 8: v = (uint32_t)stride; break;
             case 9: v = (uint32_t)(stride >> 32); break;
             case 10: v = (uint32_t)kHeaderBytes; break;
@@ -128,6 +137,7 @@ __global__ void pack_kernel(const uint8_t* __restrict__ codes, const uint16_t* _
             const int64_t r0 = (int64_t)e * N + mt * 16 + g;
             const int grp = kc * 2 + h;
             v = (uint32_t)scales[r0 * G + grp] | ((uint32_t)scales[(r0 + 8) * G + grp] << 16);
+            if (!scale_in_fma_range(v & 0xffffu) || !scale_in_fma_range(v >> 16)) clear_scale_range(out);
         }
         out[w] = v;
     }

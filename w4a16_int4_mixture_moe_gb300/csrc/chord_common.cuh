@@ -244,6 +244,48 @@ __device__ __forceinline__ void dequant_row8(uint32_t w, uint32_t sp, uint32_t* 
     out[3] = bf2_as_u32(__hmul2(__hsub2(u32_as_bf2(q3), off), s2));
 }
 
+// ---- one-instruction dequantisation for scales in [2^-126, 0.5) ---------------
+// Header word 7 of a packed blob is 1 when every group scale is a positive
+// normal bf16 below 0.5 (bit patterns 0x0080 .. 0x3EFF), else 0; the packer
+// writes it.  For such scales a code q costs one bf16x2 FMA per pair:
+//   * a nibble in bits 4..7 of a half-word whose other bits are zero is the
+//     bf16 number q * 2^-129 exactly (exponent field 0 or 1: both have the
+//     spacing 2^-133, so the value is linear in all four bits);
+//   * b = s * 2^129 is exact and finite for s in range (an exponent add);
+//   * c = -8 * s is exact;
+//   * fma(a, b, c) = q*s - 8*s = (q - 8) * s exactly before its single
+//     rounding to nearest even, i.e. bf16((q - 8) * s), the subtract-then-scale
+//     value; q = 8 gives +0, as (q - 8) * s does for s > 0.
+constexpr int kHdrScaleRangeWord = 7;
+
+__host__ __device__ __forceinline__ bool scale_in_fma_range(uint32_t s16) {
+    return s16 - 0x0080u <= 0x3EFFu - 0x0080u;
+}
+
+__device__ __forceinline__ bool header_scales_in_fma_range(const uint8_t* blob) {
+    return reinterpret_cast<const uint32_t*>(blob)[kHdrScaleRangeWord] == 1u;
+}
+
+// (b, c) = (s * 2^129, -8 * s) in both halves, from the scale pair `sp`.
+__device__ __forceinline__ void fma_scale_pair(uint32_t sp, uint32_t& b2, uint32_t& c2) {
+    b2 = sp + 0x40804080u;   // exponent field + 129 in each half (normal s below 0.5: no carry out)
+    c2 = bf2_as_u32(__hmul2(u32_as_bf2(sp), u32_as_bf2(0xC100C100u)));   // times -8, exact
+}
+
+// dequant_row8 for a blob whose header says every scale is in range: the
+// same four bf16x2 registers, nibble i moved to bits 4..7 of each half.
+__device__ __forceinline__ void dequant_row8_fma(uint32_t w, uint32_t b2u, uint32_t c2u, uint32_t* out) {
+    const __nv_bfloat162 b2 = u32_as_bf2(b2u), c2 = u32_as_bf2(c2u);
+    const uint32_t q0 = (w << 4) & 0x00F000F0u;   // columns +0, +1
+    const uint32_t q1 = w & 0x00F000F0u;          // +2, +3
+    const uint32_t q2 = (w >> 4) & 0x00F000F0u;   // +4, +5
+    const uint32_t q3 = (w >> 8) & 0x00F000F0u;   // +6, +7
+    out[0] = bf2_as_u32(__hfma2(u32_as_bf2(q0), b2, c2));
+    out[1] = bf2_as_u32(__hfma2(u32_as_bf2(q1), b2, c2));
+    out[2] = bf2_as_u32(__hfma2(u32_as_bf2(q2), b2, c2));
+    out[3] = bf2_as_u32(__hfma2(u32_as_bf2(q3), b2, c2));
+}
+
 __host__ __device__ __forceinline__ int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // Tail split of a persistent launch of n_items items over G CTAs in a static

@@ -21,7 +21,9 @@
 //     A and the B fragment alike), so one 8-byte shared load gives a lane the
 //     codes of four k16 steps.  0x4300|q is 128+q, minus 136 gives q-8
 //     exactly, one bf16x2 multiply by the group scale rounds once ("subtract
-//     then scale");
+//     then scale"); when the blob's header says every scale lies in
+//     [2^-126, 0.5), one bf16x2 FMA per pair computes the same value
+//     (dequant_row8_fma);
 //   * runs persistently: CTA i takes work items i, i + grid, ... where an item
 //     is (align block, 8*NT-token sub-block, 128-row N tile), bounded on the
 //     device by num_tokens_padded, so nothing is read back to the host.
@@ -88,8 +90,9 @@ __device__ __forceinline__ ItemRows load_item_rows(const GemmArgs& a, int64_t b,
 // One 64-column chunk: dequantise the warp's MI 16-row tiles (lane (g, c):
 // rows g and g + 8, columns [16c, 16c + 16)) and accumulate them against NV
 // 8-token tiles.  `row0` = the warp's first row + g; `xa` = shared address of
-// token g's columns 16c.. of this chunk.
-template <int MI, int NV>
+// token g's columns 16c.. of this chunk.  FD: the blob's scales all lie in
+// [2^-126, 0.5) and each weight pair costs one FMA (dequant_row8_fma).
+template <int MI, int NV, bool FD>
 __device__ __forceinline__ void chunk_mma(const uint8_t* cb, int row0, uint32_t code_off, uint32_t scale_sel,
                                           uint32_t xa, float (&acc)[MI][NV][4]) {
     // av[mi][r][p] = bf16x2 pair p (columns 16c + 2p, +1) of row g (r = 0) or g + 8 (r = 1)
@@ -101,8 +104,15 @@ __device__ __forceinline__ void chunk_mma(const uint8_t* cb, int row0, uint32_t 
             const int row = row0 + mi * 16 + r * 8;
             const uint2 w = *reinterpret_cast<const uint2*>(cb + code_off + row * 16);
             const uint32_t sp = prmt(*reinterpret_cast<const uint32_t*>(cb + 4096 + row * 4), scale_sel);
-            dequant_row8(w.x, sp, av[mi][r]);
-            dequant_row8(w.y, sp, av[mi][r] + 4);
+            if (FD) {
+                uint32_t b2, c2;
+                fma_scale_pair(sp, b2, c2);
+                dequant_row8_fma(w.x, b2, c2, av[mi][r]);
+                dequant_row8_fma(w.y, b2, c2, av[mi][r] + 4);
+            } else {
+                dequant_row8(w.x, sp, av[mi][r]);
+                dequant_row8(w.y, sp, av[mi][r] + 4);
+            }
         }
     }
     // B fragments of token 8t + g, the same 16 columns
@@ -135,7 +145,7 @@ __device__ __forceinline__ void chunk_mma(const uint8_t* cb, int row0, uint32_t 
 // Consumer side of one item whose valid token slots lie in its first NV
 // 8-token tiles (align fills a block's slots from the front): the K loop over
 // the stage ring, then the epilogue.  Returns false when a wait gave up.
-template <int NT, int STAGES, int MI, int NV>
+template <int NT, int STAGES, int MI, int NV, bool FD>
 __device__ __forceinline__ bool consume_item(const GemmArgs& a, uint8_t* smem, uint64_t* full, uint64_t* empty,
                                           volatile int* flags, int64_t& stage, int warp, int lane, int nt,
                                           int32_t my_id, int ks0, int ks1, int slice) {
@@ -166,8 +176,8 @@ __device__ __forceinline__ bool consume_item(const GemmArgs& a, uint8_t* smem, u
         }
         const uint8_t* sW = smem + slot * kStage;
         const uint32_t xa = smem_u32(sW + kWStageBytes) + x_lane;
-        chunk_mma<MI, NV>(sW, row0, code_off, scale_sel, xa, acc);
-        if (a.K - ks * kKS >= 128) chunk_mma<MI, NV>(sW + kChunk2, row0, code_off, scale_sel, xa + 128, acc);
+        chunk_mma<MI, NV, FD>(sW, row0, code_off, scale_sel, xa, acc);
+        if (a.K - ks * kKS >= 128) chunk_mma<MI, NV, FD>(sW + kChunk2, row0, code_off, scale_sel, xa + 128, acc);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
     }
@@ -209,6 +219,24 @@ __device__ __forceinline__ bool consume_item(const GemmArgs& a, uint8_t* smem, u
     return true;
 }
 
+// consume_item instantiated for the item's count of 8-token tiles.
+template <int NT, int STAGES, int MI, bool FD>
+__device__ __forceinline__ bool consume_nv(const GemmArgs& a, uint8_t* smem, uint64_t* full, uint64_t* empty,
+                                           volatile int* flags, int64_t& stage, int warp, int lane, int nt,
+                                           int32_t my_id, int ks0, int ks1, int slice, int nv) {
+    if (nv <= 1)
+        return consume_item<NT, STAGES, MI, 1, FD>(a, smem, full, empty, flags, stage, warp, lane, nt, my_id, ks0,
+                                                   ks1, slice);
+    if (nv == 2 || NT == 2)
+        return consume_item<NT, STAGES, MI, (NT >= 2 ? 2 : 1), FD>(a, smem, full, empty, flags, stage, warp, lane,
+                                                                   nt, my_id, ks0, ks1, slice);
+    if (nv == 3)
+        return consume_item<NT, STAGES, MI, (NT >= 4 ? 3 : 1), FD>(a, smem, full, empty, flags, stage, warp, lane,
+                                                                   nt, my_id, ks0, ks1, slice);
+    return consume_item<NT, STAGES, MI, (NT >= 4 ? 4 : 1), FD>(a, smem, full, empty, flags, stage, warp, lane, nt,
+                                                               my_id, ks0, ks1, slice);
+}
+
 // Work unit -> (align block b, token sub-block, 128-row N tile, K slice and
 // its stage range); 32-bit divisions while the unit index fits (always, in
 // practice), no slice arithmetic when K is not split.
@@ -237,7 +265,8 @@ __global__ void __launch_bounds__(Cfg<NT, MI>::kThreads, MINB) gemm_decode_kerne
     constexpr int kStage = Cfg<NT>::kStageBytes;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * kStage);
     uint64_t* empty = full + STAGES;
-    volatile int* flags = reinterpret_cast<volatile int*>(empty + STAGES);  // [0] skip, [1] abort, [2] ntp
+    // [0] skip, [1] abort, [2] num_tokens_padded, [3] every scale in the one-FMA dequantisation's range
+    volatile int* flags = reinterpret_cast<volatile int*>(empty + STAGES);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -245,6 +274,7 @@ __global__ void __launch_bounds__(Cfg<NT, MI>::kThreads, MINB) gemm_decode_kerne
         if (!ok) set_error(a.err, CHORD_DEV_BAD_HEADER);
         flags[0] = ok ? 0 : 1;
         flags[1] = 0;
+        flags[3] = ok && header_scales_in_fma_range(a.packed) ? 1 : 0;
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 33);        // the weight copy's expect_tx + one cp.async arrival per producer lane
             mbar_init(&empty[s], kConsumerWarps);
@@ -335,6 +365,7 @@ __global__ void __launch_bounds__(Cfg<NT, MI>::kThreads, MINB) gemm_decode_kerne
     }
 
     // -------------------------------------------------------------- consumers
+    const bool fma_dequant = flags[3] != 0;
     int64_t stage = 0;
     for (int64_t unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
         int slice, nt, sub, ks0, ks1;
@@ -344,19 +375,11 @@ __global__ void __launch_bounds__(Cfg<NT, MI>::kThreads, MINB) gemm_decode_kerne
         const ItemRows rows = load_item_rows<NT>(a, b, sub, lane, slice == 0 ? a.err : nullptr);
         if (rows.vmask == 0) continue;
         const int nv = (32 - __clz(rows.vmask) + 7) / 8;   // 8-token tiles up to the last valid slot
-        bool ok;
-        if (nv <= 1)
-            ok = consume_item<NT, STAGES, MI, 1>(a, smem, full, empty, flags, stage, warp, lane, nt, rows.id, ks0, ks1,
-                                                  slice);
-        else if (nv == 2 || NT == 2)
-            ok = consume_item<NT, STAGES, MI, (NT >= 2 ? 2 : 1)>(a, smem, full, empty, flags, stage, warp, lane,
-                                                                 nt, rows.id, ks0, ks1, slice);
-        else if (nv == 3)
-            ok = consume_item<NT, STAGES, MI, (NT >= 4 ? 3 : 1)>(a, smem, full, empty, flags, stage, warp, lane,
-                                                                 nt, rows.id, ks0, ks1, slice);
-        else
-            ok = consume_item<NT, STAGES, MI, (NT >= 4 ? 4 : 1)>(a, smem, full, empty, flags, stage, warp, lane,
-                                                                 nt, rows.id, ks0, ks1, slice);
+        const bool ok = fma_dequant
+                            ? consume_nv<NT, STAGES, MI, true>(a, smem, full, empty, flags, stage, warp, lane, nt,
+                                                               rows.id, ks0, ks1, slice, nv)
+                            : consume_nv<NT, STAGES, MI, false>(a, smem, full, empty, flags, stage, warp, lane, nt,
+                                                                rows.id, ks0, ks1, slice, nv);
         if (!ok) return;
     }
 }
@@ -391,11 +414,12 @@ cudaError_t launch_nt(const GemmArgs& a, cudaStream_t stream) {
 cudaError_t launch_gemm_decode(const GemmArgs& a, cudaStream_t stream) {
     // Tokens per item: the smallest of 8/16/32 that holds the whole block
     // (larger blocks are split into 32-token sub-blocks, each re-streaming the
-    // weights; the tcgen05 kernel serves those blocks by default).  Ring depth: as many stages as let three CTAs share an SM
-    // (more resident warps hide the dequantisation's dependency latencies;
-    // measured faster than two CTAs with deeper rings).
+    // weights; the tcgen05 kernel serves those blocks by default).  Ring depth
+    // and CTAs per SM as measured fastest on GB300 among 2-5 CTAs per SM and
+    // 3-6 stages: three CTAs for 8- and 32-token items, four with four stages
+    // for 16-token items (TP8 T=128 gate_up + down 289 -> 272 us).
     if (a.block_m <= 8) return launch_nt<1, 6, 2, 3>(a, stream);
-    if (a.block_m <= 16) return launch_nt<2, 5, 2, 3>(a, stream);
+    if (a.block_m <= 16) return launch_nt<2, 4, 2, 4>(a, stream);
     return launch_nt<4, 4, 2, 3>(a, stream);
 }
 
