@@ -91,30 +91,13 @@ __device__ __forceinline__ ItemRows load_item_rows(const GemmArgs& a, int64_t b,
 // rows g and g + 8, columns [16c, 16c + 16)) and accumulate them against NV
 // 8-token tiles.  `row0` = the warp's first row + g; `xa` = shared address of
 // token g's columns 16c.. of this chunk.  FD: the blob's scales all lie in
-// [2^-126, 0.5) and each weight pair costs one FMA (dequant_row8_fma).
+// [2^-126, 0.5) and each weight pair costs one FMA (dequant_row8_fma).  The
+// B fragments are loaded first; each 16-row tile's MMAs follow its own
+// dequantisation, so only one tile's A registers are live at a time
+// (measured 3 % faster on EP8 decode than dequantising both tiles first).
 template <int MI, int NV, bool FD>
 __device__ __forceinline__ void chunk_mma(const uint8_t* cb, int row0, uint32_t code_off, uint32_t scale_sel,
                                           uint32_t xa, float (&acc)[MI][NV][4]) {
-    // av[mi][r][p] = bf16x2 pair p (columns 16c + 2p, +1) of row g (r = 0) or g + 8 (r = 1)
-    uint32_t av[MI][2][8];
-#pragma unroll
-    for (int mi = 0; mi < MI; ++mi) {
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const int row = row0 + mi * 16 + r * 8;
-            const uint2 w = *reinterpret_cast<const uint2*>(cb + code_off + row * 16);
-            const uint32_t sp = prmt(*reinterpret_cast<const uint32_t*>(cb + 4096 + row * 4), scale_sel);
-            if (FD) {
-                uint32_t b2, c2;
-                fma_scale_pair(sp, b2, c2);
-                dequant_row8_fma(w.x, b2, c2, av[mi][r]);
-                dequant_row8_fma(w.y, b2, c2, av[mi][r] + 4);
-            } else {
-                dequant_row8(w.x, sp, av[mi][r]);
-                dequant_row8(w.y, sp, av[mi][r] + 4);
-            }
-        }
-    }
     // B fragments of token 8t + g, the same 16 columns
     uint32_t bv[NV][8];
 #pragma unroll
@@ -127,15 +110,31 @@ __device__ __forceinline__ void chunk_mma(const uint8_t* cb, int row0, uint32_t 
                      : "=r"(bv[t][4]), "=r"(bv[t][5]), "=r"(bv[t][6]), "=r"(bv[t][7])
                      : "r"(x + 16));
     }
-    // k16 step st takes columns 16c + 4st .. + 3 of every lane, for A and B alike
 #pragma unroll
-    for (int st = 0; st < 4; ++st) {
+    for (int mi = 0; mi < MI; ++mi) {
+        // av[r][p] = bf16x2 pair p (columns 16c + 2p, +1) of row g (r = 0) or g + 8 (r = 1)
+        uint32_t av[2][8];
 #pragma unroll
-        for (int t = 0; t < NV; ++t) {
+        for (int r = 0; r < 2; ++r) {
+            const int row = row0 + mi * 16 + r * 8;
+            const uint2 w = *reinterpret_cast<const uint2*>(cb + code_off + row * 16);
+            const uint32_t sp = prmt(*reinterpret_cast<const uint32_t*>(cb + 4096 + row * 4), scale_sel);
+            if (FD) {
+                uint32_t b2, c2;
+                fma_scale_pair(sp, b2, c2);
+                dequant_row8_fma(w.x, b2, c2, av[r]);
+                dequant_row8_fma(w.y, b2, c2, av[r] + 4);
+            } else {
+                dequant_row8(w.x, sp, av[r]);
+                dequant_row8(w.y, sp, av[r] + 4);
+            }
+        }
+        // k16 step st takes columns 16c + 4st .. + 3 of every lane, for A and B alike
 #pragma unroll
-            for (int mi = 0; mi < MI; ++mi) {
-                const uint32_t af[4] = {av[mi][0][2 * st], av[mi][1][2 * st], av[mi][0][2 * st + 1],
-                                        av[mi][1][2 * st + 1]};
+        for (int st = 0; st < 4; ++st) {
+#pragma unroll
+            for (int t = 0; t < NV; ++t) {
+                const uint32_t af[4] = {av[0][2 * st], av[1][2 * st], av[0][2 * st + 1], av[1][2 * st + 1]};
                 mma_bf16_16816(acc[mi][t], af, bv[t][2 * st], bv[t][2 * st + 1]);
             }
         }
