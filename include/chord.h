@@ -148,7 +148,13 @@ size_t chord_packed_weight_bytes(int E, int N, int K, int layout);
  *   scales  device bf16 [E, N, K / group_size]
  *   layout  CHORD_LAYOUT_TCGEN05 (default kernel) or CHORD_LAYOUT_WARP_MMA
  *   packed  device output of packed_bytes >= chord_packed_weight_bytes(E, N, K, layout)
- * group_size must be 32.  A code above 15 sets CHORD_DEV_BAD_CODE. */
+ * group_size must be 32.  A code above 15 sets CHORD_DEV_BAD_CODE.
+ * The header (little-endian 32-bit words) holds the magic "CHRD", version 1,
+ * the layout, the group size, E, N, K, then in word 7 a 1 when every scale is
+ * a positive normal bf16 below 0.5 (else 0), then the 64-bit expert stride
+ * N * K * 9 / 16 and data offset 256.  Word 7 changes no result: with it set,
+ * the decode kernel forms each bf16((q - 8) * s) with one FMA per pair instead
+ * of a subtract and a multiply (the same value, bit for bit). */
 chord_status chord_pack_weights(const uint8_t *codes, const void *scales, int E, int N, int K,
                                 int group_size, int layout, void *packed, size_t packed_bytes,
                                 void *stream);
