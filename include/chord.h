@@ -396,6 +396,15 @@ chord_status chord_moe_layer(const void *x, const int32_t *topk_ids, const float
  * *code (CHORD_DEV_*) and clears it. */
 chord_status chord_get_device_error(void *stream, int32_t *code);
 
+/* Self-test of the device-side failure detection (no counterpart in the
+ * article): launches one thread that waits, through the same bounded wait
+ * every GEMM pipeline uses, on an mbarrier that nothing arrives on.  After the
+ * bound (about 2 s) it sets CHORD_DEV_TIMEOUT in the device error word and
+ * returns; the context stays usable.  A later chord_get_device_error reads the
+ * code, and a call with opts->validate != 0 returns CHORD_ERR_TIMEOUT.
+ * Asynchronous on `stream`; returns CHORD_ERR_CUDA if the launch fails. */
+chord_status chord_selftest_wait_timeout(void *stream);
+
 #ifdef __cplusplus
 }
 #endif

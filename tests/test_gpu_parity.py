@@ -318,6 +318,36 @@ def test_gemm_nothing_local_writes_nothing(kernel):
     run_gemm_case(12, 4, 3, 128, 64, 8, seed=6, ids=ids, kernel=kernel)
 
 
+def test_bounded_wait_times_out_and_context_survives():
+    """Failure detection without a fault: a pipeline wait that can never end
+    (an mbarrier nothing arrives on, waited on through the helper every GEMM
+    pipeline uses) gives up after its bound, leaves CHORD_DEV_TIMEOUT in the
+    error word, and the context keeps working; a validating call reports the
+    code as CHORD_ERR_TIMEOUT."""
+    assert chord.chord_get_device_error() == 0
+    chord.chord_selftest_wait_timeout()
+    assert chord.chord_get_device_error() == 4          # CHORD_DEV_TIMEOUT, read and cleared
+    assert chord.chord_get_device_error() == 0
+    # the context still computes: an exact-integer GEMM matches the oracle bit for bit
+    T, topk, E, N, K, bm = 12, 2, 3, 256, 256, 16
+    rng = np.random.default_rng(77)
+    x = wl._bf16(rng.integers(-1, 2, size=(T, K)).astype(np.float32))
+    scales = np.full((E, N, K // 32), 0x3F80, np.uint16)
+    run_gemm_case(T, topk, E, N, K, bm, seed=77, x=x, scales=scales, exact=True, kernel="warp_mma")
+    # a validating call reads the word and maps the timeout to CHORD_ERR_TIMEOUT
+    chord.chord_selftest_wait_timeout()
+    codes = wl.random_codes(78, (E, N, K))
+    packed = pack(codes, scales)
+    ids = wl.random_ids(79, T, topk, E)
+    s, e, n = align(ids, E, bm)
+    C = torch.empty((T * topk, N), dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(chord.ChordError) as ei:
+        chord.chord_w4a16_moe_gemm(dbf(x), topk, packed, E, N, K, s, e, n, bm, T * topk, C,
+                                   opts=chord.ChordOpts(kernel=chord.KERNEL_WARP_MMA, validate=1))
+    assert ei.value.status == 7                           # CHORD_ERR_TIMEOUT
+    assert chord.chord_get_device_error() == 0
+
+
 def test_gemm_header_mismatch_is_reported():
     """A blob packed for (E, N, K) = (2, 128, 128) passed as (2, 256, 64) has the
     right size but the wrong header, and a blob of packed layout 1 has the wrong

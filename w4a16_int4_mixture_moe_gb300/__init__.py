@@ -19,7 +19,7 @@ __all__ = [
     "chord_version", "chord_status_string", "chord_packed_weight_bytes", "chord_pack_weights",
     "chord_align_capacity", "chord_align_workspace_bytes", "chord_moe_align", "chord_select_block_m", "chord_select_kernel",
     "chord_gemm_workspace_bytes", "chord_w4a16_moe_gemm", "chord_silu_mul", "chord_moe_combine",
-    "chord_layer_workspace_bytes", "chord_moe_layer", "chord_get_device_error",
+    "chord_layer_workspace_bytes", "chord_moe_layer", "chord_get_device_error", "chord_selftest_wait_timeout",
     "chord_grouped_contiguous_workspace_bytes", "chord_grouped_contiguous_gemm",
     "chord_grouped_masked_workspace_bytes", "chord_grouped_masked_gemm",
     "KERNEL_AUTO", "KERNEL_TCGEN05", "KERNEL_WARP_MMA", "LAYOUT_WARP_MMA", "LAYOUT_TCGEN05",
@@ -72,6 +72,7 @@ _SIGS = {
     "chord_moe_layer": (_int, [_vp, _vp, _vp, _int, _int, _int, _int, _int, _int, _vp, _sz, _vp, _sz, _int, _vp,
                                _sz, _vp, _OPTS, _vp]),
     "chord_get_device_error": (_int, [_vp, ctypes.POINTER(_i32)]),
+    "chord_selftest_wait_timeout": (_int, [_vp]),
     "chord_grouped_contiguous_workspace_bytes": (_sz, [_i64, _int]),
     "chord_grouped_contiguous_gemm": (_int, [_vp, _i64, _vp, _vp, _sz, _int, _int, _int, _vp, _vp, _sz, _OPTS, _vp]),
     "chord_grouped_masked_workspace_bytes": (_sz, [_int, _int, _int]),
@@ -246,6 +247,10 @@ def chord_grouped_masked_gemm(A, masked_m, expected_m: int, packed, N: int, K: i
     _check(load().chord_grouped_masked_gemm(_p(A), G, max_m, _p(masked_m), expected_m, _p(packed), _nbytes(packed),
                                             N, K, _p(C), _p(workspace), _nbytes(workspace), _o(opts), _s(stream)),
            "chord_grouped_masked_gemm")
+
+
+def chord_selftest_wait_timeout(stream=None):
+    _check(load().chord_selftest_wait_timeout(_s(stream)), "chord_selftest_wait_timeout")
 
 
 def chord_get_device_error(stream=None) -> int:

@@ -540,6 +540,12 @@ chord_status chord_grouped_masked_gemm(const void* A, int G, int max_m, const in
                                 ws + idx, workspace_bytes - idx, opts, stream);
 }
 
+chord_status chord_selftest_wait_timeout(void* stream) {
+    const DeviceInfo& di = device_info();
+    if (!di.err) return CHORD_ERR_CUDA;
+    return cuda_status(launch_wait_timeout_selftest(di.err, static_cast<cudaStream_t>(stream)));
+}
+
 chord_status chord_get_device_error(void* stream, int32_t* code) {
     if (!code) return CHORD_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -598,6 +598,28 @@ __global__ void silu_mul_kernel(const uint16_t* __restrict__ C1, const int32_t* 
 }
 
 // ============================================================================
+// Self-test of the bounded pipeline wait: one thread initialises an mbarrier
+// that nothing will ever arrive on and waits for its first phase through
+// mbar_wait, the helper every GEMM pipeline waits with.  After the helper's
+// bound (kWaitLimitCycles, about 2 s) the thread records CHORD_DEV_TIMEOUT in
+// the error word and the kernel returns: a wait that cannot end becomes an
+// error the host reads, with no fault and a context that stays usable.
+// ============================================================================
+__global__ void wait_timeout_selftest_kernel(int* err) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+        if (!mbar_wait(&bar, 0)) set_error(err, CHORD_DEV_TIMEOUT);
+    }
+}
+
+cudaError_t launch_wait_timeout_selftest(int* err, cudaStream_t stream) {
+    wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(err);
+    return cudaGetLastError();
+}
+
+// ============================================================================
 // Tail split of the tcgen05 kernel: for tail item i (item full + i of the
 // launch's plan), weight row r of its 128-row tile and token column j of its
 // block, C[id, 128 nt + r] = sum over slices s = 0 .. S-1, in that order, of

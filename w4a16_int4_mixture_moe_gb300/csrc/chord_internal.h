@@ -34,6 +34,7 @@ cudaError_t launch_grouped_masked_index(const int32_t* masked_m, int G, int max_
 cudaError_t launch_splitk_reduce(const float* partial, int S, int64_t num_pairs, int64_t id_limit, int N,
                                  const int32_t* sorted_ids, const int32_t* ntp, int64_t capacity, void* C, int out_f32,
                                  int silu, cudaStream_t stream);
+cudaError_t launch_wait_timeout_selftest(int* err, cudaStream_t stream);
 cudaError_t launch_silu_mul(const uint16_t* C1, const int32_t* topk_ids, int64_t P, int E, int I, uint16_t* h,
                             cudaStream_t stream);
 cudaError_t launch_combine(const void* C2, bool c2_f32, const int32_t* topk_ids, const float* topk_w, int T,
