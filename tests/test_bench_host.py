@@ -54,3 +54,47 @@ def test_regime_follows_the_measured_ridge():
 
 def test_reduce_max_without_a_process_group():
     assert bench.reduce_max([1.5, 2.0], None, None) == [1.5, 2.0]
+
+
+def test_host_block_size_rule_matches_the_library():
+    """bench.select_block_m (the reference arm's config label, computed without
+    loading the CUDA library) equals chord_select_block_m over a grid of
+    token counts, top-k and expert counts, including the five workloads."""
+    import w4a16_int4_mixture_moe_gb300 as chord
+    chord.build()
+    chord.load()
+    shapes = [(w.T, w.topk, w.E, w.E_global) for w in bench.WORKLOADS.values()]
+    for T in (0, 1, 2, 5, 16, 100, 128, 512, 1000, 1024, 3000, 4096, 8192, 16384, 65536):
+        for topk in (1, 2, 6, 8):
+            for E_local, E_global in ((8, 8), (48, 384), (384, 384), (64, 256), (1, 1)):
+                shapes.append((T, topk, E_local, E_global))
+    for T, topk, el, eg in shapes:
+        assert bench.select_block_m(T, topk, el, eg) == chord.chord_select_block_m(T, topk, el, eg, 0, 0), \
+            (T, topk, el, eg)
+
+
+def test_time_per_call_is_not_divided_by_ranks():
+    """N ranks run N expert-parallel shares of one call concurrently: the time
+    per call is the max-over-ranks time over the steps, whatever N is."""
+    assert bench.per_call_us(318.5, 1000) == 318.5
+    assert bench.per_call_us(0.0, 0) == 0.0
+
+
+def test_reference_arm_loads_no_cuda_library():
+    """The reference arm (the oracle on the host cores) runs without importing
+    the CUDA package, so only the oracle's library is loaded in it; its config
+    equals the one the GPU arm builds for the same workload and block size."""
+    import subprocess
+    import sys
+    code = ("import sys, json, io, contextlib; sys.argv = ['bench.py', '--impl', 'reference', '--workload', 'tiny', "
+            "'--steps', '1', '--warmup', '0']; import bench; buf = io.StringIO()\n"
+            "with contextlib.redirect_stdout(buf): bench.main()\n"
+            "line = json.loads(buf.getvalue().strip().splitlines()[-1])\n"
+            "assert 'w4a16_int4_mixture_moe_gb300' not in sys.modules, 'CUDA package imported'\n"
+            "maps = open('/proc/self/maps').read()\n"
+            "assert 'libchord' not in maps, 'libchord.so mapped'\n"
+            "cfg, _, _ = bench.arm_config(bench.WORKLOADS['tiny'], line['config']['block_m'], 1)\n"
+            "assert cfg == line['config'], (cfg, line['config'])\n"
+            "print('ok', line['value'])")
+    r = subprocess.run([sys.executable, "-c", code], cwd=bench.ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr

@@ -78,6 +78,60 @@ const DeviceInfo& device_info() {
     return g_info[dev];
 }
 
+namespace {
+struct LaunchFacts {
+    int dev;
+    const void* func;
+    int threads;
+    size_t smem, limit;
+    int ctas;   // 0: only the limit was set
+};
+std::mutex g_facts_mu;
+LaunchFacts g_facts[256];
+int g_nfacts = 0;
+
+// Entry for (device, func, threads, smem, limit), or nullptr; g_facts_mu held.
+LaunchFacts* find_facts(int dev, const void* func, int threads, size_t smem, size_t limit) {
+    for (int i = 0; i < g_nfacts; ++i) {
+        LaunchFacts& f = g_facts[i];
+        if (f.dev == dev && f.func == func && f.threads == threads && f.smem == smem && f.limit == limit) return &f;
+    }
+    return nullptr;
+}
+}  // namespace
+
+cudaError_t ensure_smem_limit(const void* func, size_t smem_limit) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(g_facts_mu);
+    if (find_facts(dev, func, 0, 0, smem_limit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_limit);
+    if (e != cudaSuccess) return e;
+    if (g_nfacts < 256) g_facts[g_nfacts++] = LaunchFacts{dev, func, 0, 0, smem_limit, 0};
+    return cudaSuccess;
+}
+
+cudaError_t kernel_ctas_per_sm(const void* func, int threads, size_t smem, size_t smem_limit, int* ctas) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(g_facts_mu);
+    if (const LaunchFacts* f = find_facts(dev, func, threads, smem, smem_limit)) {
+        *ctas = f->ctas;
+        return cudaSuccess;
+    }
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_limit);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, func, threads, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    if (g_nfacts < 256) g_facts[g_nfacts++] = LaunchFacts{dev, func, threads, smem, smem_limit, per_sm};
+    *ctas = per_sm;
+    return cudaSuccess;
+}
+
 }  // namespace chord
 
 using namespace chord;

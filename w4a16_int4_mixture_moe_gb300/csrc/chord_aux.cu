@@ -339,16 +339,11 @@ cudaError_t launch_align(const int32_t* topk_ids, int64_t P, int E, int block_m,
     const int nslices = align_slices(P);
     const size_t hist_smem = (size_t)E * sizeof(int32_t);
     const size_t scatter_smem = (size_t)(E + kAlignWarps * E) * sizeof(int32_t);
-    static bool attr_done[64] = {false};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 64 && !attr_done[dev]) {
-        const int most = (int)((1024 + kAlignWarps * 1024) * sizeof(int32_t));
-        cudaError_t e1 = cudaFuncSetAttribute(align_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
-        if (e1 == cudaSuccess)
-            e1 = cudaFuncSetAttribute(align_single_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    {
+        const size_t most = (1024 + kAlignWarps * 1024) * sizeof(int32_t);
+        cudaError_t e1 = ensure_smem_limit(reinterpret_cast<const void*>(align_scatter_kernel), most);
+        if (e1 == cudaSuccess) e1 = ensure_smem_limit(reinterpret_cast<const void*>(align_single_kernel), most);
         if (e1 != cudaSuccess) return e1;
-        attr_done[dev] = true;
     }
     if (nslices == 1) {
         return launch_pdl(pdl_for(P), align_single_kernel, dim3(1), dim3(kAlignThreads), scatter_smem, stream, topk_ids, P, E,

@@ -388,18 +388,9 @@ cudaError_t launch_nt(const GemmArgs& a, cudaStream_t stream) {
     using C = Cfg<NT, MI>;
     constexpr int smem = STAGES * C::kStageBytes + 2 * STAGES * 8 + 16;
     auto kern = gemm_decode_kernel<NT, STAGES, MI, MINB>;
-    static int configured_dev = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        configured_dev = dev;
-    }
-    int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::kThreads, smem);
+    int per_sm = 1;
+    cudaError_t e = kernel_ctas_per_sm(reinterpret_cast<const void*>(kern), C::kThreads, smem, smem, &per_sm);
     if (e != cudaSuccess) return e;
-    if (per_sm < 1) per_sm = 1;
     const int64_t items_cap = (a.capacity / a.block_m) * ((a.block_m + NT * 8 - 1) / (NT * 8)) * (a.N / kBN) *
                               (a.ksplit > 1 ? a.ksplit : 1);
     int64_t grid = (int64_t)device_info().sm_count * per_sm;

@@ -672,18 +672,9 @@ cudaError_t launch_cfg(const GemmArgs& g, bool deep_weights, cudaStream_t stream
     // until a co-resident CTA exits.  When two CTAs' columns do not fit in the
     // SM's 512, ask for enough shared memory that only one CTA fits per SM.
     if (2 * ta.tmem_cols > 512 && smem < 120 * 1024) smem = 120 * 1024;
-    static int configured_dev = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<GW, MAXR, NI>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-        if (e != cudaSuccess) return e;
-        configured_dev = dev;
-    }
-    int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gemm_tc_kernel<GW, MAXR, NI>,
-                                                                  C::kThreads, smem);
+    int per_sm = 1;
+    cudaError_t e = kernel_ctas_per_sm(reinterpret_cast<const void*>(gemm_tc_kernel<GW, MAXR, NI>), C::kThreads,
+                                       smem, 227 * 1024, &per_sm);
     if (e != cudaSuccess) return e;
     const int tmem_fit = (int)(512 / ta.tmem_cols);
     if (per_sm > tmem_fit) per_sm = tmem_fit;

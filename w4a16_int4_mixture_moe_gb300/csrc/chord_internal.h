@@ -16,6 +16,16 @@ struct DeviceInfo {
 // Per-device facts, fetched once per device (thread-safe).
 const DeviceInfo& device_info();
 
+// Launch facts of one kernel on the current device, computed once per
+// (device, kernel, arguments) and cached behind a mutex, so a launch costs no
+// runtime query after the first: the kernel's dynamic shared-memory limit is
+// raised to `smem_limit` and the resident CTAs per SM at `threads` x `smem`
+// are stored in *ctas (at least 1).
+cudaError_t kernel_ctas_per_sm(const void* func, int threads, size_t smem, size_t smem_limit, int* ctas);
+
+// Raise a kernel's dynamic shared-memory limit once per (device, kernel, limit).
+cudaError_t ensure_smem_limit(const void* func, size_t smem_limit);
+
 // ---- pack / align / epilogues (chord_aux.cu) -------------------------------
 cudaError_t launch_pack(const uint8_t* codes, const uint16_t* scales, int E, int N, int K, int layout,
                         uint8_t* packed, int* err, cudaStream_t stream);
