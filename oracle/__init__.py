@@ -68,6 +68,7 @@ def lib():
         if _lib is None:
             L = ctypes.CDLL(build())
             u8p, u16p, i32p, f32p = _P(ctypes.c_uint8), _P(ctypes.c_uint16), _P(ctypes.c_int32), _P(ctypes.c_float)
+            f64p = _P(ctypes.c_double)
             c_int, c_i64, c_sz = ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
             sig = {
                 "orc_version": (c_int, []),
@@ -92,6 +93,14 @@ def lib():
                 "orc_combine_f32": (c_int, [f32p, i32p, f32p, c_int, c_int, c_int, c_int, u16p, c_int]),
                 "orc_moe_layer": (c_int, [u16p, i32p, f32p, c_int, c_int, c_int, c_int, c_int,
                                           u8p, u16p, u8p, u16p, c_int, u16p, c_int]),
+                "orc_bf16_round_f64": (ctypes.c_uint16, [ctypes.c_double]),
+                "orc_moe_gemm_f64sum": (c_int, [u16p, c_i64, c_int, u8p, u16p, c_int, c_int, c_int,
+                                                i32p, i32p, ctypes.c_int32, c_int, c_i64, u16p, c_int]),
+                "orc_moe_gemm_f64": (c_int, [u16p, c_i64, c_int, u8p, u16p, c_int, c_int, c_int,
+                                             i32p, i32p, ctypes.c_int32, c_int, c_i64, f64p, c_int]),
+                "orc_combine_f64": (c_int, [f64p, i32p, f32p, c_int, c_int, c_int, c_int, u16p, c_int]),
+                "orc_moe_layer_f64sum": (c_int, [u16p, i32p, f32p, c_int, c_int, c_int, c_int, c_int,
+                                                 u8p, u16p, u8p, u16p, c_int, u16p, c_int]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(L, name)
@@ -325,4 +334,78 @@ def moe_layer(x, topk_ids, topk_w, w13, w2, E: int, block_m: int = 16, nthreads=
                                _ptr(c13, ctypes.c_uint8), _ptr(s13, ctypes.c_uint16),
                                _ptr(c2, ctypes.c_uint8), _ptr(s2, ctypes.c_uint16),
                                block_m, _ptr(out, ctypes.c_uint16), threads(nthreads)), "moe_layer")
+    return out
+
+
+# --- the binary64-sum variant (a second valid summation order) ----------------
+
+def bf16_round_f64(d: float) -> int:
+    """bf16 bits of a binary64 value, rounded once to nearest even."""
+    return int(lib().orc_bf16_round_f64(float(d)))
+
+
+def moe_gemm_f64sum(A, a_row_divisor, codes, scales, sorted_ids, expert_ids, num_tokens_padded, block_m,
+                    num_pairs, C=None, nthreads=None):
+    """As moe_gemm, with each dot product summed in binary64 and rounded to bf16 once
+    (orc_moe_gemm_f64sum)."""
+    return _gemm_variant("orc_moe_gemm_f64sum", np.uint16, ctypes.c_uint16, A, a_row_divisor, codes, scales,
+                         sorted_ids, expert_ids, num_tokens_padded, block_m, num_pairs, C, nthreads)
+
+
+def moe_gemm_f64(A, a_row_divisor, codes, scales, sorted_ids, expert_ids, num_tokens_padded, block_m,
+                 num_pairs, C=None, nthreads=None):
+    """The binary64 sums themselves, float64 [num_pairs, N] (orc_moe_gemm_f64)."""
+    return _gemm_variant("orc_moe_gemm_f64", np.float64, ctypes.c_double, A, a_row_divisor, codes, scales,
+                         sorted_ids, expert_ids, num_tokens_padded, block_m, num_pairs, C, nthreads)
+
+
+def _gemm_variant(name, dtype, ctype, A, a_row_divisor, codes, scales, sorted_ids, expert_ids,
+                  num_tokens_padded, block_m, num_pairs, C, nthreads):
+    A = _c(A, np.uint16)
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.uint16)
+    E, N, K = codes.shape
+    assert A.shape[1] == K
+    sorted_ids = _c(sorted_ids, np.int32)
+    expert_ids = _c(expert_ids, np.int32)
+    if C is None:
+        C = np.zeros((max(num_pairs, 1), N), dtype)[:num_pairs]
+    C = _c(C, dtype)
+    _check(getattr(lib(), name)(_ptr(A, ctypes.c_uint16), A.shape[0], a_row_divisor,
+                                _ptr(codes, ctypes.c_uint8), _ptr(scales, ctypes.c_uint16), E, N, K,
+                                _ptr(sorted_ids, ctypes.c_int32), _ptr(expert_ids, ctypes.c_int32),
+                                num_tokens_padded, block_m, num_pairs, _ptr(C, ctype), threads(nthreads)), name)
+    return C
+
+
+def combine_f64(C2: np.ndarray, topk_ids: np.ndarray, topk_w: np.ndarray, E: int, nthreads=None):
+    """Weighted sum of float64 C2 rows in binary64, rounded to bf16 once (orc_combine_f64)."""
+    C2 = _c(C2, np.float64)
+    ids = _c(topk_ids, np.int32)
+    w = _c(topk_w, np.float32)
+    T, topk = ids.shape
+    H = C2.shape[1]
+    out = np.empty((T, H), np.uint16)
+    _check(lib().orc_combine_f64(_ptr(C2, ctypes.c_double), _ptr(ids, ctypes.c_int32), _ptr(w, ctypes.c_float),
+                                 T, topk, E, H, _ptr(out, ctypes.c_uint16), threads(nthreads)), "combine_f64")
+    return out
+
+
+def moe_layer_f64sum(x, topk_ids, topk_w, w13, w2, E: int, block_m: int = 16, nthreads=None):
+    """The layer with binary64 sums at the plain layer's rounding points (orc_moe_layer_f64sum)."""
+    x = _c(x, np.uint16)
+    ids = _c(topk_ids, np.int32)
+    w = _c(topk_w, np.float32)
+    c13, s13 = (_c(w13[0], np.uint8), _c(w13[1], np.uint16))
+    c2, s2 = (_c(w2[0], np.uint8), _c(w2[1], np.uint16))
+    T, H = x.shape
+    topk = ids.shape[1]
+    I = c2.shape[2]
+    assert c13.shape == (E, 2 * I, H) and c2.shape == (E, H, I)
+    out = np.empty((T, H), np.uint16)
+    _check(lib().orc_moe_layer_f64sum(_ptr(x, ctypes.c_uint16), _ptr(ids, ctypes.c_int32),
+                                      _ptr(w, ctypes.c_float), T, topk, E, H, I,
+                                      _ptr(c13, ctypes.c_uint8), _ptr(s13, ctypes.c_uint16),
+                                      _ptr(c2, ctypes.c_uint8), _ptr(s2, ctypes.c_uint16),
+                                      block_m, _ptr(out, ctypes.c_uint16), threads(nthreads)), "moe_layer_f64sum")
     return out

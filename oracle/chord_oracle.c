@@ -32,6 +32,11 @@
  *             w[t, k] * C2[t * topk + k, n] ), C2 in bf16 or binary32.
  *   layer     the steps above, with the down projection's FP32 sums fed to
  *             the combine unrounded (see orc_moe_layer).
+ *   f64 sums  a second valid evaluation of the same definitions: every dot
+ *             product and the weighted sum in binary64, rounded to bf16 at the
+ *             same points (orc_*_f64sum).  It is nearly the exact result, and
+ *             the parity tests use it to measure how far two valid summation
+ *             orders fall apart after a bf16 rounding.
  *   pack      the byte layout the CUDA library reads (its own specification,
  *             written out below), so the GPU packer can be checked byte for
  *             byte; and its inverse.
@@ -83,6 +88,30 @@ static uint16_t bf16_from_f32(float f)
 }
 
 uint16_t orc_bf16_round(float f) { return bf16_from_f32(f); }
+
+/* Round a binary64 to the nearest bf16, ties to even, with one rounding.
+ * (float)d rounds to the nearest binary32 first; that differs from rounding d
+ * itself only when the binary32 result is exactly halfway between two bf16
+ * values: d then lies on one side of that midpoint (or on it), and the sign of
+ * the exact residual d - (float)d (exact by Sterbenz's lemma) says which.
+ * Finite values in the binary32 range only (the layer's values are). */
+static uint16_t bf16_from_f64(double d)
+{
+    float f = (float)d;
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0xffffu) == 0x8000u && (u & 0x7fffffffu) < 0x7f800000u) {
+        double r = d - (double)f;
+        if (r != 0.0) {
+            uint32_t keep = u >> 16;
+            int away = (r > 0.0) == (f > 0.0);   /* |d| above the midpoint */
+            return (uint16_t)(away ? keep + 1u : keep);
+        }
+    }
+    return bf16_from_f32(f);
+}
+
+uint16_t orc_bf16_round_f64(double d) { return bf16_from_f64(d); }
 
 /* ------------------------------------------------------------------------ */
 /* Dequantisation: subtract the offset 8, then multiply by the group scale,
@@ -406,12 +435,16 @@ static void dequant_expert(const uint8_t *codes, const uint16_t *scales, int e, 
         }
 }
 
-/* Shared body of the two output precisions: exactly one of Cb (bf16, one
- * rounding of the FP32 sum) and Cf (the FP32 sum itself) is non-NULL. */
+/* Shared body of the output precisions: exactly one of Cb (bf16, one
+ * rounding of the sum), Cf (the FP32 sum itself) and Cd (the binary64 sum) is
+ * non-NULL.  f64sum selects a binary64 sum (each bf16 x bf16 product is exact
+ * in binary64 too) in the same ascending order; Cf goes with the FP32 sum
+ * only, Cd with the binary64 sum only. */
 static int gemm_indexed(const uint16_t *A, int64_t a_rows, int a_row_divisor,
                         const uint8_t *codes, const uint16_t *scales, int E, int N, int K,
                         const int32_t *sorted_ids, const int32_t *expert_ids, int32_t num_tokens_padded,
-                        int block_m, int64_t num_pairs, uint16_t *Cb, float *Cf, int nthreads)
+                        int block_m, int64_t num_pairs, uint16_t *Cb, float *Cf, double *Cd, int f64sum,
+                        int nthreads)
 {
     if (N <= 0 || K <= 0 || K % ORC_GROUP || block_m <= 0 || a_row_divisor <= 0
         || num_tokens_padded < 0 || num_tokens_padded % block_m)
@@ -454,6 +487,16 @@ static int gemm_indexed(const uint16_t *A, int64_t a_rows, int a_row_divisor,
                 int32_t p = rows[r];
                 const uint16_t *a = A + (size_t)(p / a_row_divisor) * (size_t)K;
                 const float *w = wq + (size_t)n * K;
+                if (f64sum) {
+                    double dacc = 0.0;
+                    for (int k = 0; k < K; ++k)
+                        dacc += (double)f32_from_bf16(a[k]) * (double)w[k];
+                    if (Cb)
+                        Cb[(size_t)p * N + n] = bf16_from_f64(dacc);
+                    else
+                        Cd[(size_t)p * N + n] = dacc;
+                    continue;
+                }
                 float acc = 0.0f;
                 for (int k = 0; k < K; ++k)
                     acc += f32_from_bf16(a[k]) * w[k];
@@ -475,7 +518,7 @@ int orc_moe_gemm(const uint16_t *A, int64_t a_rows, int a_row_divisor,
                  int block_m, int64_t num_pairs, uint16_t *C, int nthreads)
 {
     return gemm_indexed(A, a_rows, a_row_divisor, codes, scales, E, N, K, sorted_ids, expert_ids,
-                        num_tokens_padded, block_m, num_pairs, C, NULL, nthreads);
+                        num_tokens_padded, block_m, num_pairs, C, NULL, NULL, 0, nthreads);
 }
 
 /* FP32 output: the sum before any rounding, for a consumer that keeps FP32
@@ -486,7 +529,28 @@ int orc_moe_gemm_f32(const uint16_t *A, int64_t a_rows, int a_row_divisor,
                      int block_m, int64_t num_pairs, float *C, int nthreads)
 {
     return gemm_indexed(A, a_rows, a_row_divisor, codes, scales, E, N, K, sorted_ids, expert_ids,
-                        num_tokens_padded, block_m, num_pairs, NULL, C, nthreads);
+                        num_tokens_padded, block_m, num_pairs, NULL, C, NULL, 0, nthreads);
+}
+
+/* The binary64-sum variant: C[p, n] = bf16_rne( binary64 sum ), one rounding. */
+int orc_moe_gemm_f64sum(const uint16_t *A, int64_t a_rows, int a_row_divisor,
+                        const uint8_t *codes, const uint16_t *scales, int E, int N, int K,
+                        const int32_t *sorted_ids, const int32_t *expert_ids, int32_t num_tokens_padded,
+                        int block_m, int64_t num_pairs, uint16_t *C, int nthreads)
+{
+    return gemm_indexed(A, a_rows, a_row_divisor, codes, scales, E, N, K, sorted_ids, expert_ids,
+                        num_tokens_padded, block_m, num_pairs, C, NULL, NULL, 1, nthreads);
+}
+
+/* The binary64 sums themselves (the variant's down projection feeding its
+ * weighted sum). */
+int orc_moe_gemm_f64(const uint16_t *A, int64_t a_rows, int a_row_divisor,
+                     const uint8_t *codes, const uint16_t *scales, int E, int N, int K,
+                     const int32_t *sorted_ids, const int32_t *expert_ids, int32_t num_tokens_padded,
+                     int block_m, int64_t num_pairs, double *C, int nthreads)
+{
+    return gemm_indexed(A, a_rows, a_row_divisor, codes, scales, E, N, K, sorted_ids, expert_ids,
+                        num_tokens_padded, block_m, num_pairs, NULL, NULL, C, 1, nthreads);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -642,6 +706,29 @@ int orc_combine_f32(const float *C2, const int32_t *topk_ids, const float *topk_
     return combine_any(NULL, C2, topk_ids, topk_w, T, topk, E, H, out, nthreads);
 }
 
+/* The binary64-sum variant of the combine: the same weighted sum over local k
+ * in ascending order from +0, in binary64 (each weight times value product is
+ * exact there), rounded to bf16 once. */
+int orc_combine_f64(const double *C2, const int32_t *topk_ids, const float *topk_w,
+                    int T, int topk, int E, int H, uint16_t *out, int nthreads)
+{
+    if (T < 0 || topk <= 0 || H <= 0)
+        return ORC_EINVAL;
+#pragma omp parallel for num_threads(nthreads) schedule(static)
+    for (int t = 0; t < T; ++t)
+        for (int n = 0; n < H; ++n) {
+            double acc = 0.0;
+            for (int k = 0; k < topk; ++k) {
+                int64_t p = (int64_t)t * topk + k;
+                if (topk_ids[p] < 0 || topk_ids[p] >= E)
+                    continue;
+                acc += (double)topk_w[p] * C2[(size_t)p * H + n];
+            }
+            out[(size_t)t * H + n] = bf16_from_f64(acc);
+        }
+    return ORC_OK;
+}
+
 /* ------------------------------------------------------------------------ */
 /* One MoE layer: align -> gate_up GEMM (A = x, one row per token) -> SiLU*up
  * -> down GEMM (A = h, one row per pair) -> top-k combine.  The gate_up
@@ -685,6 +772,45 @@ int orc_moe_layer(const uint16_t *x, const int32_t *topk_ids, const float *topk_
                           block_m, P, C2, nthreads);
     if (rc) goto done;
     rc = orc_combine_f32(C2, topk_ids, topk_w, T, topk, E, H, out, nthreads);
+done:
+    free(sorted_ids); free(expert_ids); free(C1); free(hb); free(C2);
+    return rc;
+}
+
+/* The layer with binary64 sums at the plain layer's rounding points: gate_up
+ * rounded to bf16 from its binary64 sum, SiLU*up exactly as in the plain layer
+ * (binary32, rounded to bf16), the down projection's binary64 sums fed to the
+ * binary64 weighted sum unrounded, the output rounded to bf16 once. */
+int orc_moe_layer_f64sum(const uint16_t *x, const int32_t *topk_ids, const float *topk_w,
+                         int T, int topk, int E, int H, int I,
+                         const uint8_t *codes13, const uint16_t *scales13,
+                         const uint8_t *codes2, const uint16_t *scales2,
+                         int block_m, uint16_t *out, int nthreads)
+{
+    int64_t cap = orc_align_capacity(T, topk, E, block_m);
+    if (cap < 0 || H <= 0 || I <= 0 || H % ORC_GROUP || I % ORC_GROUP)
+        return ORC_EINVAL;
+    int64_t P = (int64_t)T * topk;
+    int32_t *sorted_ids = (int32_t *)malloc((size_t)(cap > 0 ? cap : 1) * sizeof(int32_t));
+    int32_t *expert_ids = (int32_t *)malloc((size_t)(cap / block_m > 0 ? cap / block_m : 1) * sizeof(int32_t));
+    uint16_t *C1 = (uint16_t *)calloc((size_t)(P > 0 ? P : 1) * 2 * I, sizeof(uint16_t));
+    uint16_t *hb = (uint16_t *)calloc((size_t)(P > 0 ? P : 1) * I, sizeof(uint16_t));
+    double *C2 = (double *)calloc((size_t)(P > 0 ? P : 1) * H, sizeof(double));
+    int rc = ORC_ENOMEM;
+    int32_t ntp = 0;
+    if (!sorted_ids || !expert_ids || !C1 || !hb || !C2)
+        goto done;
+    rc = orc_moe_align(topk_ids, T, topk, E, block_m, sorted_ids, expert_ids, &ntp, cap);
+    if (rc) goto done;
+    rc = orc_moe_gemm_f64sum(x, T, topk, codes13, scales13, E, 2 * I, H, sorted_ids, expert_ids, ntp,
+                             block_m, P, C1, nthreads);
+    if (rc) goto done;
+    rc = orc_silu_mul(C1, topk_ids, P, E, I, hb, nthreads);
+    if (rc) goto done;
+    rc = orc_moe_gemm_f64(hb, P, 1, codes2, scales2, E, H, I, sorted_ids, expert_ids, ntp,
+                          block_m, P, C2, nthreads);
+    if (rc) goto done;
+    rc = orc_combine_f64(C2, topk_ids, topk_w, T, topk, E, H, out, nthreads);
 done:
     free(sorted_ids); free(expert_ids); free(C1); free(hb); free(C2);
     return rc;

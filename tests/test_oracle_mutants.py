@@ -50,6 +50,11 @@ MUTANTS = [
     ("scale_range_half_included", "if (sign != 0 || expo < 1 || expo > 125)", "if (sign != 0 || expo < 1 || expo > 126)"),
     ("scale_range_subnormal_included", "if (sign != 0 || expo < 1 || expo > 125)", "if (sign != 0 || expo > 125)"),
     ("scale_range_sign_ignored", "if (sign != 0 || expo < 1 || expo > 125)", "if (expo < 1 || expo > 125)"),
+    ("f64sum_binary32_accumulator", "double dacc = 0.0;", "float dacc = 0.0f;"),
+    ("f64_rounds_through_binary32", "        if (r != 0.0) {\n            uint32_t keep", "        if (0) {\n            uint32_t keep"),
+    ("f64_layer_rounds_down_sums", "rc = orc_combine_f64(C2, topk_ids, topk_w, T, topk, E, H, out, nthreads);",
+     "for (int64_t i = 0; i < P * H; ++i) C2[i] = (double)(float)C2[i];\n"
+     "    rc = orc_combine_f64(C2, topk_ids, topk_w, T, topk, E, H, out, nthreads);"),
     ("combine_nonlocal", "if (topk_ids[p] < 0 || topk_ids[p] >= E)\n                    continue;\n                float v",
      "if (topk_ids[p] >= E)\n                    continue;\n                float v"),
 ]

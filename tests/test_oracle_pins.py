@@ -613,3 +613,228 @@ def test_layer_block_m_invariance(orc):
     a = orc.moe_layer(x, ids, wts, w13, w2, w.E, block_m=1)
     b = orc.moe_layer(x, ids, wts, w13, w2, w.E, block_m=16)
     np.testing.assert_array_equal(a, b)
+
+
+# --- the binary64-sum variant -----------------------------------------------
+# A second valid evaluation of the same definitions (dot products and the
+# weighted sum in binary64, bf16 at the same rounding points).  Pinned against
+# exact rational arithmetic (Python's fractions: every bf16 and binary32 value
+# is a dyadic rational, so sums of their products are exact there) and against
+# a hand-worked table of one-rounding cases.
+
+from fractions import Fraction  # noqa: E402
+
+
+def bf16_rne_exact(fr):
+    """bf16 bits of the exact rational `fr`, rounded once to nearest even
+    (normal range): pure integer arithmetic, independent of the oracle."""
+    if fr == 0:
+        return 0
+    sign = 0x8000 if fr < 0 else 0
+    m = abs(fr)
+    e = m.numerator.bit_length() - m.denominator.bit_length()
+    if Fraction(2) ** e > m:
+        e -= 1
+    if m >= Fraction(2) ** (e + 1):
+        e += 1
+    assert -126 <= e <= 127
+    ulp = Fraction(2) ** (e - 7)
+    q = m / ulp
+    n = q.numerator // q.denominator
+    r = q - n
+    if r > Fraction(1, 2) or (r == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    val = n * ulp
+    return sign | int(np.array([float(val)], np.float32).view(np.uint32)[0] >> 16)
+
+
+def test_bf16_round_f64_hand_table(orc):
+    """One rounding from binary64, including values that a binary32 step would
+    put exactly on a midpoint (catches rounding through binary32 twice)."""
+    for r in read_golden("bf16_round_f64.txt"):
+        v = float.fromhex(r[0]) if "0x" in r[0] else float(r[0])
+        assert orc.bf16_round_f64(v) == int(r[1], 16), r
+        assert bf16_rne_exact(Fraction(v)) == int(r[1], 16), r
+
+
+def test_bf16_round_f64_matches_exact_rounding(orc):
+    """Random binary64 values, and values a few binary64 ulps from bf16
+    midpoints, against the exact rounding of the rational value."""
+    rng = np.random.default_rng(11)
+    vals = list(rng.standard_normal(2000) * 10.0 ** rng.integers(-20, 20, 2000))
+    lo = rng.integers(0x0080, 0x7f00, 500, dtype=np.uint16)
+    mids = ((f64(lo) + f64(lo + 1)) / 2.0).tolist()   # midpoints of neighbouring bf16 values (exact in binary64)
+    for m in mids:
+        vals += [np.nextafter(m, np.inf), m, np.nextafter(m, -np.inf), -m]
+    for v in vals:
+        assert orc.bf16_round_f64(float(v)) == bf16_rne_exact(Fraction(float(v))), v
+
+
+def _small_gemm_case(seed, T=5, topk=2, E=2, N=16, K=256):
+    x = wl.random_bf16(seed, (T, K))
+    codes = wl.random_codes(seed + 1, (E, N, K))
+    scales = wl.random_scales(seed + 2, (E, N, K // GROUP))
+    ids = wl.random_ids(seed + 3, T, topk, E, p_nonlocal=0.2)
+    return x, codes, scales, ids
+
+
+def test_gemm_f64sum_against_exact_sums(orc):
+    """Every output of the binary64-sum GEMM is the exact sum rounded once to
+    bf16 (fractions), and its binary64 output is within the binary64
+    summation bound K * 2^-53 * sum|x w| of the exact sum.  Catches a binary32
+    accumulator, a second rounding, or a dropped / shifted term."""
+    x, codes, scales, ids = _small_gemm_case(21)
+    T, K = x.shape
+    E, N, _ = codes.shape
+    topk = ids.shape[1]
+    P = T * topk
+    s, e, n = orc.moe_align(ids, E, 4)
+    got = orc.moe_gemm_f64sum(x, topk, codes, scales, s, e, n, 4, P, C=np.zeros((P, N), np.uint16))
+    got64 = orc.moe_gemm_f64(x, topk, codes, scales, s, e, n, 4, P)
+    W = f64(dequant_ref(codes, scales))
+    X = f64(x)
+    checked = 0
+    for p in range(P):
+        ex = ids.ravel()[p]
+        if ex < 0:
+            continue
+        t = p // topk
+        for j in range(N):
+            terms = [Fraction(float(X[t, k])) * Fraction(float(W[ex, j, k])) for k in range(K)]
+            exact = sum(terms, Fraction(0))
+            assert got[p, j] == bf16_rne_exact(exact), (p, j)
+            bound = K * 2.0 ** -53 * float(sum(abs(a) for a in terms))
+            assert abs(Fraction(float(got64[p, j])) - exact) <= Fraction(bound), (p, j)
+            checked += 1
+    assert checked > 100
+
+
+def test_gemm_f64sum_cancellation(orc):
+    """x = (2^24, 1, -2^24, 0, ...) against unit weights: the exact sum is 1.
+    A binary32 sum in ascending k loses the 1 (2^24 + 1 rounds to 2^24); the
+    binary64 sum keeps it.  Catches a binary32 accumulator in the variant."""
+    K, N, E = 64, 16, 1
+    x = np.zeros((1, K), np.uint16)
+    x[0, 0], x[0, 1], x[0, 2] = to_bf16([2.0 ** 24, 1.0, -(2.0 ** 24)])
+    codes = np.full((E, N, K), 9, np.uint8)                # q - 8 = 1
+    scales = np.full((E, N, K // GROUP), 0x3F80, np.uint16)  # 1.0
+    ids = np.zeros((1, 1), np.int32)
+    s, e, n = orc.moe_align(ids, E, 1)
+    v64 = orc.moe_gemm_f64sum(x, 1, codes, scales, s, e, n, 1, 1, C=np.zeros((1, N), np.uint16))
+    v32 = orc.moe_gemm(x, 1, codes, scales, s, e, n, 1, 1, C=np.zeros((1, N), np.uint16))
+    assert (v64 == 0x3F80).all() and (v32 == 0).all()
+    d64 = orc.moe_gemm_f64(x, 1, codes, scales, s, e, n, 1, 1)
+    assert (d64 == 1.0).all()
+
+
+def test_gemm_f64sum_exact_integer_regime_equals_plain(orc):
+    """x in {-1, 0, 1}, scale 1, K = 2048: every partial sum is an integer
+    below 2^24, so both evaluations are exact and agree bit for bit."""
+    rng = np.random.default_rng(3)
+    T, topk, E, N, K = 6, 2, 3, 32, 2048
+    x = to_bf16(rng.integers(-1, 2, (T, K)).astype(np.float32))
+    codes = wl.random_codes(5, (E, N, K))
+    scales = np.full((E, N, K // GROUP), 0x3F80, np.uint16)
+    ids = wl.random_ids(6, T, topk, E)
+    s, e, n = orc.moe_align(ids, E, 8)
+    a = orc.moe_gemm(x, topk, codes, scales, s, e, n, 8, T * topk, C=np.zeros((T * topk, N), np.uint16))
+    b = orc.moe_gemm_f64sum(x, topk, codes, scales, s, e, n, 8, T * topk, C=np.zeros((T * topk, N), np.uint16))
+    np.testing.assert_array_equal(a, b)
+
+
+def test_combine_f64_against_exact_sums(orc):
+    """The binary64 weighted sum over local k, rounded once: against exact
+    fractions of w * C2 (C2 binary64 values with many significant bits)."""
+    rng = np.random.default_rng(8)
+    T, topk, E, H = 6, 4, 5, 16
+    ids = wl.random_ids(9, T, topk, E, p_nonlocal=0.3)
+    ids[2, :] = -1
+    w = wl.random_weights(10, T, topk)
+    C2 = rng.standard_normal((T * topk, H)) * 37.0
+    out = orc.combine_f64(C2, ids, w, E)
+    for t in range(T):
+        for j in range(H):
+            ex = sum((Fraction(float(w[t, k])) * Fraction(float(C2[t * topk + k, j]))
+                      for k in range(topk) if 0 <= ids[t, k] < E), Fraction(0))
+            assert out[t, j] == bf16_rne_exact(ex), (t, j)
+    assert (out[2] == 0).all()
+
+
+def test_layer_f64sum_is_the_composition_and_close_to_dense(orc):
+    """The variant's layer equals align -> binary64-sum gate_up (bf16) -> SiLU*up
+    -> binary64 down sums -> binary64 combine, bit for bit (catches a rounding
+    of the down sums or a wrong stage order), and agrees with the float64
+    dense per-token loop within the tolerance."""
+    w = wl.TINY
+    ids, wts = wl.make_routing(w)
+    x = wl.make_x(w)
+    c13, s13 = wl.make_w13(w)
+    c2, s2 = wl.make_w2(w)
+    got = orc.moe_layer_f64sum(x, ids, wts, (c13, s13), (c2, s2), w.E, block_m=4)
+    P = w.P
+    s, e, n = orc.moe_align(ids, w.E, 4)
+    C1 = orc.moe_gemm_f64sum(x, w.topk, c13, s13, s, e, n, 4, P, C=np.zeros((P, 2 * w.I), np.uint16))
+    h = orc.silu_mul(C1, ids.ravel(), w.E, h=np.zeros((P, w.I), np.uint16))
+    C2 = orc.moe_gemm_f64(h, 1, c2, s2, s, e, n, 4, P, C=np.zeros((P, w.H), np.float64))
+    np.testing.assert_array_equal(got, orc.combine_f64(C2, ids, wts, w.E))
+    ref = layer_dense_reference(x, ids, wts, c13, s13, c2, s2, w.E)
+    err = np.abs(f64(got) - ref)
+    assert (err <= 1e-2 + 1e-2 * np.abs(ref)).all(), err.max()
+
+
+def test_plain_and_f64_sums_differ_by_at_most_one_bf16_step(orc):
+    """At the Kimi-K2 gate_up depth (K = 7168, x ~ N(0,1), the workloads'
+    weights), the plain oracle's binary32 sums and the binary64 sums round to
+    bf16 values at most one step apart, and most agree exactly: the binary32
+    summation error is far below half a bf16 step, so only values near a
+    rounding midpoint can flip."""
+    T, topk, E, N, K = 4, 2, 2, 256, 7168
+    x = wl.random_bf16(41, (T, K))
+    codes = wl.random_codes(42, (E, N, K))
+    scales = wl.random_scales(43, (E, N, K // GROUP))
+    ids = wl.random_ids(44, T, topk, E)
+    s, e, n = orc.moe_align(ids, E, 8)
+    P = T * topk
+    a = orc.moe_gemm(x, topk, codes, scales, s, e, n, 8, P, C=np.zeros((P, N), np.uint16))
+    b = orc.moe_gemm_f64sum(x, topk, codes, scales, s, e, n, 8, P, C=np.zeros((P, N), np.uint16))
+    d = np.abs(bf16_order(a) - bf16_order(b))
+    assert d.max() <= 1
+    assert (d == 0).mean() > 0.99
+
+
+def bf16_order(bits):
+    """bf16 bit patterns -> integers in value order (one step per representable value; +0 = -0 = 0)."""
+    b = np.asarray(bits, np.uint16).astype(np.int64)
+    mag = b & 0x7FFF
+    return np.where(b & 0x8000, -mag, mag)
+
+
+def test_layer_closed_form_down_sum_needs_binary64(orc):
+    """A layer built so that every down sum is exactly 1 + 2^-8 + 2^-30:
+    x = (128, 0, ...); gate rows j < 3 have weight 1 on k = 0, so g = 128 and
+    SiLU(g) = 128 (exp(-128) underflows in binary32); up rows j < 3 have
+    weight 2^-14, 2^-22, 2^-44 on k = 0, so h = 128 * 128 * w = 1, 2^-8, 2^-30;
+    every down row has weight 1 on j < 3.  The weighted sum (weight 1) of
+    1 + 2^-8 + 2^-30 lies just above the bf16 midpoint of 1 and 1 + 2^-7:
+    the binary64 layer rounds it to 1 + 2^-7 (0x3f81); the plain layer's
+    binary32 down sum is 1 + 2^-8 (a tie) and rounds to the even 1 (0x3f80).
+    Catches a binary32 step anywhere in the variant's down sum or combine."""
+    H, I, E = 64, 64, 1
+    x = np.zeros((1, H), np.uint16)
+    x[0, 0] = to_bf16([128.0])[0]
+    c13 = np.full((E, 2 * I, H), 8, np.uint8)
+    s13 = np.full((E, 2 * I, H // GROUP), 0x3F80, np.uint16)
+    up_scale = to_bf16([2.0 ** -14, 2.0 ** -22, 2.0 ** -44])
+    for j in range(3):
+        c13[0, j, 0] = 9                     # gate weight 1
+        c13[0, I + j, 0] = 9                 # up weight = its group's scale
+        s13[0, I + j, 0] = up_scale[j]
+    c2 = np.full((E, H, I), 8, np.uint8)
+    c2[0, :, :3] = 9
+    s2 = np.full((E, H, I // GROUP), 0x3F80, np.uint16)
+    ids = np.zeros((1, 1), np.int32)
+    wts = np.ones((1, 1), np.float32)
+    got64 = orc.moe_layer_f64sum(x, ids, wts, (c13, s13), (c2, s2), E, block_m=1)
+    got32 = orc.moe_layer(x, ids, wts, (c13, s13), (c2, s2), E, block_m=1)
+    assert (got64 == 0x3F81).all(), got64
+    assert (got32 == 0x3F80).all(), got32
