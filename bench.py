@@ -42,6 +42,7 @@ METRIC = "W4A16 MoE µs/call; achieved HBM GB/s (decode) & BF16 TFLOP/s (prefill
 UNIT = "µs/call"
 WORKLOADS = {
     "ep8_decode": wl.EP8_DECODE, "ep8_prefill": wl.EP8_PREFILL, "skewed": wl.SKEWED, "tiny": wl.TINY,
+    "skewed_cold": wl.SKEWED_COLD,
     **{f"tp8_T{t}": wl.tp8(t) for t in wl.TP8_T},
 }
 L2_BYTES = 129 * 2 ** 20
@@ -501,15 +502,20 @@ class LayerRig:
         self.C2 = torch.empty((P, H), dtype=torch.float32, device=dev)
         self.out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
         self.stream = torch.cuda.current_stream()
-        self.f32_out = chord.ChordOpts(out_dtype=chord.DTYPE_F32)
-        self.silu_opts = chord.ChordOpts(epilogue=chord.EPILOGUE_SILU_MUL if fused else chord.EPILOGUE_NONE)
+        mixed = getattr(args, "mixed", 0)
+        self.f32_out = chord.ChordOpts(out_dtype=chord.DTYPE_F32, mixed=mixed)
+        self.silu_opts = chord.ChordOpts(epilogue=chord.EPILOGUE_SILU_MUL if fused else chord.EPILOGUE_NONE,
+                                         mixed=mixed)
         # K-slice / split-tail partial sums (workspace of each GEMM)
         self.split = (chord.chord_gemm_workspace_bytes(P, 2 * I, H, bm, self.silu_opts),
                       chord.chord_gemm_workspace_bytes(P, H, I, bm, self.f32_out))
         self.gws = torch.empty(max(16, *self.split), dtype=torch.uint8, device=dev)
-        # align: one launch up to 4096 pairs, three above; gate_up (+ SiLU * up pass),
-        # down, combine; one reduction per split GEMM
-        self.launches_per_step = (1 if P <= 4096 else 3) + (3 if fused else 4) + sum(1 for b in self.split if b > 0)
+        # align: one launch up to 4096 pairs, three above; each GEMM's launches as the
+        # library reports them (the GEMM, the mixed regime's warp-level launch, a
+        # split reduction); the SiLU * up pass when unfused; combine
+        self.launches_per_step = ((1 if P <= 4096 else 3) + (0 if fused else 1) + 1 +
+                                  chord.chord_gemm_launch_count(P, 2 * I, H, bm, self.split[0], self.silu_opts) +
+                                  chord.chord_gemm_launch_count(P, H, I, bm, self.split[1], self.f32_out))
         # public layer call: its own workspace and copies of the inputs
         self.lws = torch.empty(chord.chord_layer_workspace_bytes(T, topk, E, H, I, bm), dtype=torch.uint8,
                                device=dev)
@@ -760,6 +766,8 @@ def main():
     ap.add_argument("--unfused", action="store_true", help="separate SiLU * up pass instead of the fused epilogue")
     ap.add_argument("--fused", action="store_true", help="SiLU * up in the gate_up epilogue on either kernel")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--mixed", type=int, default=0, choices=[-1, 0, 1],
+                    help="per-block regime of tcgen05-regime GEMMs: 0 automatic, 1 on, -1 off")
     args = ap.parse_args()
     if args.workload in GROUPED:
         if args.impl == "reference":

@@ -117,8 +117,20 @@ typedef struct chord_opts {
     int32_t out_dtype;   /* GEMM output: CHORD_DTYPE_BF16 (default) or CHORD_DTYPE_F32,
                             the FP32 sums unrounded (for a consumer that keeps FP32) */
     int32_t epilogue;    /* chord_epilogue (GEMM and layer) */
-    int32_t reserved[3]; /* must be zero */
+    int32_t mixed;       /* per-block regime in the tcgen05 regime (the article's rule that
+                            an expert's row count tok_e picks its kernel, section
+                            "Indexed kernels"), decided on the device from the align
+                            output: blocks holding at most CHORD_MIXED_SMALL_ROWS valid
+                            rows run on the warp-level kernel (launched first), the
+                            others on the tcgen05 kernel.  0 = automatic (on when the
+                            call runs the tcgen05 kernel by automatic choice with
+                            block_m > CHORD_MIXED_SMALL_ROWS), 1 = on (also with the
+                            kernel forced to tcgen05), -1 = off. */
+    int32_t reserved[2]; /* must be zero */
 } chord_opts;
+
+/* Blocks with at most this many valid rows count as small for opts.mixed. */
+#define CHORD_MIXED_SMALL_ROWS 32
 
 /* Library version (major * 10000 + minor * 100 + patch). */
 int chord_version(void);
@@ -207,7 +219,10 @@ chord_status chord_moe_align(const int32_t *topk_ids, int T, int topk, int E, in
  * nothing.
  *   - The first call on a device looks up the array's device address (once per
  *     device, with that device current); make that first call before any
- *     stream capture.
+ *     stream capture.  The address is kept for the life of the process, so a
+ *     cudaDeviceReset after the first call on that device is not supported
+ *     (the library's module, and the array with it, is reloaded at a new
+ *     address).
  *   - All calls on a device share the one array.  Calls whose work overlaps
  *     on the GPU (on different streams, or from several threads) race on it
  *     and may produce wrong routing; serialise them.
@@ -238,6 +253,15 @@ int chord_select_block_m(int T, int topk, int E_local, int E_global, int N, int 
 int chord_select_kernel(int block_m, int N, int K);
 
 /* ------------------------------------------------------------------- GEMM */
+
+/* Kernel launches one chord_w4a16_moe_gemm call with these arguments makes,
+ * from host arithmetic only (the same decisions the call takes, with a
+ * 16-byte aligned workspace of workspace_bytes): the GEMM kernel, plus the
+ * warp-level launch of the mixed regime (opts->mixed), plus the reduction of
+ * its K slices or of the tcgen05 split tail when the workspace holds them.
+ * 0 when the call would do nothing or be refused. */
+int chord_gemm_launch_count(int64_t num_pairs, int N, int K, int block_m, size_t workspace_bytes,
+                            const chord_opts *opts);
 
 /* Scratch bytes chord_w4a16_moe_gemm needs for the given call shape.  Pure
  * host arithmetic (no device query).

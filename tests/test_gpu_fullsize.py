@@ -1,8 +1,16 @@
 """Parity at the measured workloads' full sizes, in the launch configuration
-the benchmark times (automatic block size, the whole layer): the GPU runs
-every token; the oracle recomputes a sample of tokens one by one (a token's
-output depends only on its own pairs), and the GEMM outputs of a sample of
-pairs.  Tolerance |gpu - ref| <= 1e-2 + 1e-2|ref| on every sampled element."""
+the benchmark times (automatic block size and kernel, SiLU * up fused into
+gate_up where the benchmark fuses it, each GEMM with its workspace so K slices
+and split tails run as they do there).
+
+The GPU runs every token.  The oracle checks every element of every local
+pair and every output of the checked tokens: all tokens for the EP8 decode and
+the five TP8 sizes; for EP8 prefill and the skewed layer, at least 16 local
+pairs of every expert (all of an expert's pairs when it has fewer) plus a
+random share of the other tokens.  Each stage is checked against the oracle's
+result on the GPU's own previous stage, and the end-to-end output against the
+plain oracle's layer with the bound that chain implies (check_layer_chain).
+A second set of checks feeds each GPU stage the oracle's own previous stage."""
 import numpy as np
 import pytest
 import torch
@@ -10,12 +18,10 @@ import torch
 import oracle
 import w4a16_int4_mixture_moe_gb300 as chord
 import workloads as wl
-from gpu_util import (DEV, align, assert_close, assert_close_h, assert_close_layer, dbf, dev, f64, gemm, host_bits, layer,
-                      pack)
+from gpu_util import (DEV, align, assert_close, assert_close_f32, check_layer_chain, dbf, dev, gemm, host_bits,
+                      layer, pack, pair_rows, run_layer_steps)
 
 pytestmark = pytest.mark.gpu
-
-N_SAMPLE_TOKENS = 12
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -44,164 +50,138 @@ def weights(w):
     return _cache[key]
 
 
-def sample_tokens(ids, E, n, seed):
-    local = np.nonzero(((ids >= 0) & (ids < E)).any(axis=1))[0]
-    rng = np.random.default_rng(seed)
-    pick = rng.choice(local, size=min(n, local.size), replace=False)
-    # always include the first and last token and one token with no local pair, if any
-    extra = [0, ids.shape[0] - 1]
-    nonlocal_t = np.nonzero(~((ids >= 0) & (ids < E)).any(axis=1))[0]
-    if nonlocal_t.size:
-        extra.append(int(nonlocal_t[0]))
-    return np.unique(np.concatenate([pick, np.array(extra, dtype=pick.dtype)]))
+WORKLOADS = [wl.EP8_DECODE, *[wl.tp8(t) for t in wl.TP8_T], wl.EP8_PREFILL, wl.SKEWED, wl.SKEWED_COLD]
+# EP8 prefill and skewed: at least this many local pairs of every expert among
+# the checked tokens, plus this many other tokens drawn at random
+COVER_PAIRS = 16
+EXTRA_TOKENS = {wl.EP8_PREFILL.name: 1024, wl.SKEWED.name: 512, wl.SKEWED_COLD.name: 512}
 
 
-WORKLOADS = [wl.EP8_DECODE, wl.EP8_PREFILL, *[wl.tp8(t) for t in wl.TP8_T], wl.SKEWED]
-
-
-def oracle_stages(w, x, ids, wts, w13, w2, sel):
-    """The oracle's intermediates for the sampled tokens (a token's results depend
-    only on its own pairs): C1 (bf16), h (bf16), C2 (FP32 sums), out (bf16)."""
-    ids_s, wts_s = ids[sel], wts[sel]
-    Ps = ids_s.size
-    s, e, n = oracle.moe_align(ids_s, w.E, 8)
-    C1 = oracle.moe_gemm(x[sel], w.topk, w13[0], w13[1], s, e, n, 8, Ps, C=np.zeros((Ps, 2 * w.I), np.uint16))
-    h = oracle.silu_mul(C1, ids_s.ravel(), w.E, h=np.zeros((Ps, w.I), np.uint16))
-    C2 = oracle.moe_gemm_f32(h, 1, w2[0], w2[1], s, e, n, 8, Ps, C=np.zeros((Ps, w.H), np.float32))
-    out = oracle.combine(C2, ids_s, wts_s, w.E)
-    return C1, h, C2, out
+def checked_tokens(w, ids):
+    """Every token, or (EP8 prefill, skewed) a covering sample: for each local
+    expert min(COVER_PAIRS, its pairs) of its pairs' tokens, seeded random
+    extra tokens, the first and last token and a token with no local pair."""
+    T = ids.shape[0]
+    if w.name not in EXTRA_TOKENS:
+        return np.arange(T)
+    rng = np.random.default_rng(w.seed + 7)
+    pick = []
+    for e in range(w.E):
+        toks = np.nonzero((ids == e).any(axis=1))[0]
+        pick.extend(rng.choice(toks, size=min(COVER_PAIRS, toks.size), replace=False).tolist())
+    pick.extend(rng.choice(T, size=EXTRA_TOKENS[w.name], replace=False).tolist())
+    pick.extend([0, T - 1])
+    none = np.nonzero(~((ids >= 0) & (ids < w.E)).any(axis=1))[0]
+    if none.size:
+        pick.append(int(none[0]))
+    sel = np.unique(np.array(pick, dtype=np.int64))
+    counts = np.bincount(ids[sel][(ids[sel] >= 0) & (ids[sel] < w.E)], minlength=w.E)
+    full = np.bincount(ids[(ids >= 0) & (ids < w.E)], minlength=w.E)
+    assert (counts >= np.minimum(full, COVER_PAIRS)).all()
+    return sel
 
 
 def full_pairs(sel, topk):
-    """Pair ids of the sampled tokens in the full batch, in subset pair order."""
+    """Pair ids of the checked tokens in the full batch, in subset pair order."""
     return (sel[:, None] * topk + np.arange(topk)[None, :]).ravel()
 
 
 @pytest.mark.parametrize("w", WORKLOADS, ids=[w.name for w in WORKLOADS])
-def test_layer_full_size_stagewise(w):
-    """Every stage at full size, in the benchmark's launch configuration, fed the
-    oracle's own result of the previous stage, within |gpu - ref| <= 1e-2 +
-    1e-2|ref| on every sampled element (the SiLU*up and combine stages bit for
-    bit but for the odd last-place difference of expf)."""
+def test_full_size_layer_chain(w):
+    """The benchmark's step at full size (align -> gate_up [+ fused SiLU * up]
+    -> down -> combine through the C ABI):
+      * chord_moe_layer returns the step's output bit for bit;
+      * where the step fuses SiLU * up, the fused h equals the unfused GEMM
+        followed by the SiLU * up pass bit for bit on every local pair;
+      * on the checked tokens, every element of every stage passes the chain
+        check (gate_up within tolerance of the plain and the binary64-sum
+        oracle, SiLU * up, down and combine against the oracle on the GPU's own
+        inputs, the output against the plain oracle's layer);
+      * tokens with no local pair output +0."""
     ids, wts = wl.make_routing(w)
     x = wl.make_x(w)
     w13, w2, p13, p2 = weights(w)
-    sel = sample_tokens(ids, w.E, N_SAMPLE_TOKENS, w.seed)
-    C1r, hr, C2r, outr = oracle_stages(w, x, ids, wts, w13, w2, sel)
-    pairs = full_pairs(sel, w.topk)
-    rows = np.nonzero(((ids[sel] >= 0) & (ids[sel] < w.E)).ravel())[0]
-    bm = chord.chord_select_block_m(w.T, w.topk, w.E, w.E_global, 2 * w.I, w.H)
-    s, e, n = align(ids, w.E, bm)
-    P = w.P
-    # gate_up on the real activations (with its workspace: split-K or split tail as the bench runs it)
-    C1 = host_bits(gemm(x, w.topk, p13, w.E, 2 * w.I, w.H, s, e, n, bm, P, split_k=0))
-    assert_close(C1[pairs][rows], C1r[rows], f"{w.name} gate_up (block_m={bm})")
-    del C1
-    # SiLU*up on the oracle's C1
-    C1in = np.zeros((P, 2 * w.I), np.uint16)
-    C1in[pairs] = C1r
-    hd = torch.empty((P, w.I), dtype=torch.bfloat16, device=DEV)
-    chord.chord_silu_mul(dbf(C1in), dev(ids), w.E, hd)
-    hg = host_bits(hd)
-    del hd, C1in
-    assert_close(hg[pairs][rows], hr[rows], f"{w.name} silu_mul")
-    # down (FP32 out) on the oracle's h; other rows get seeded activations
-    hin = wl.random_bf16(w.seed + 17, (P, w.I))
-    hin[pairs] = hr
-    C2d = torch.full((P, w.H), float("nan"), dtype=torch.float32, device=DEV)
-    gemm(hin, 1, p2, w.E, w.H, w.I, s, e, n, bm, P, C=C2d, split_k=0, out_dtype=chord.DTYPE_F32)
-    C2g = C2d[torch.from_numpy(pairs).to(DEV)].cpu().numpy()
-    del C2d
-    err = np.abs(C2g[rows].astype(np.float64) - C2r[rows])
-    bad = err > 1e-2 + 1e-2 * np.abs(C2r[rows])
-    assert not bad.any(), f"{w.name} down: {int(bad.sum())} elements outside tolerance, max err {err.max()}"
-    # combine on the oracle's C2
-    out = torch.empty((sel.size, w.H), dtype=torch.bfloat16, device=DEV)
-    chord.chord_moe_combine(dev(C2r), dev(ids[sel]), dev(wts[sel]), w.E, out)
-    np.testing.assert_array_equal(host_bits(out), outr)
-
-
-@pytest.mark.parametrize("w", WORKLOADS, ids=[w.name for w in WORKLOADS])
-def test_fused_gate_up_full_size(w):
-    """The gate_up GEMM with the fused SiLU * up epilogue (w13 in layout 3), at
-    full size in the benchmark's launch configuration: bit for bit the unfused
-    path (the same GEMM on the layout-2 blob, whose output the stagewise test
-    checks against the oracle, then the SiLU * up pass) on every local pair.
-    Against the oracle's h directly, a last-place flip of a gate or up sum's
-    bf16 rounding moves h by a few ulps, so there at most 0.1 % of the sampled
-    elements may fall outside the tolerance."""
-    ids, wts = wl.make_routing(w)
-    x = wl.make_x(w)
-    w13, w2, p13, _ = weights(w)
-    p13i = pack(w13[0], w13[1], chord.LAYOUT_GATE_UP_INTERLEAVED)
-    bm = chord.chord_select_block_m(w.T, w.topk, w.E, w.E_global, 2 * w.I, w.H)
-    s, e, n = align(ids, w.E, bm)
-    # The warp-level kernel runs with its workspace (K slices where the bench splits); the tcgen05
-    # kernel without, since its split tail cuts other rows for layout 3 than for layout 2.
-    split = 0 if chord.chord_select_kernel(bm, 2 * w.I, w.H) == chord.KERNEL_WARP_MMA else None
-    hd = torch.empty((w.P, w.I), dtype=torch.bfloat16, device=DEV)
-    gemm(x, w.topk, p13i, w.E, 2 * w.I, w.H, s, e, n, bm, w.P, C=hd, split_k=split, epilogue=chord.EPILOGUE_SILU_MUL)
-    del p13i
-    C1 = gemm(x, w.topk, p13, w.E, 2 * w.I, w.H, s, e, n, bm, w.P, split_k=split)
-    h2 = torch.empty((w.P, w.I), dtype=torch.bfloat16, device=DEV)
-    chord.chord_silu_mul(C1, dev(ids), w.E, h2)
-    del C1
-    local = np.nonzero(((ids >= 0) & (ids < w.E)).ravel())[0]
-    li = torch.from_numpy(local).to(DEV)
-    assert torch.equal(hd[li].view(torch.int16), h2[li].view(torch.int16)), "fused differs from unfused"
-    del h2
-    sel = sample_tokens(ids, w.E, N_SAMPLE_TOKENS, w.seed + 1)
-    _, hr, _, _ = oracle_stages(w, x, ids, wts, w13, w2, sel)
-    pairs = full_pairs(sel, w.topk)
-    rows = np.nonzero(((ids[sel] >= 0) & (ids[sel] < w.E)).ravel())[0]
-    hg = host_bits(hd)
-    del hd
-    assert_close_h(hg[pairs][rows], hr[rows], f"{w.name} fused gate_up + SiLU*up (block_m={bm})")
-
-
-@pytest.mark.parametrize("w", WORKLOADS, ids=[w.name for w in WORKLOADS])
-def test_layer_full_size_end_to_end(w):
-    """The whole layer through chord_moe_layer at full size against the oracle's
-    layer on sampled tokens (assert_close_layer: the per-element tolerance on
-    at least 99.5% of the elements, the rest within 5% of the token's output
-    RMS)."""
-    ids, wts = wl.make_routing(w)
-    x = wl.make_x(w)
-    w13, w2, p13, p2 = weights(w)
-    out, bm = layer(x, ids, wts, w.E, w.E_global, w.I, p13, p2)
-    torch.cuda.synchronize()
-    got = host_bits(out)
-    del out
-    sel = sample_tokens(ids, w.E, N_SAMPLE_TOKENS, w.seed)
-    ref = oracle.moe_layer(x[sel], ids[sel], wts[sel], w13, w2, w.E, block_m=bm)
-    assert_close_layer(got[sel], ref, f"{w.name} layer (block_m={bm})")
-    # tokens with no local pair are exactly +0
-    none = ~((ids[sel] >= 0) & (ids[sel] < w.E)).any(axis=1)
-    assert (got[sel][none] == 0).all()
-
-
-@pytest.mark.parametrize("w", [wl.EP8_DECODE, wl.tp8(1024)], ids=["ep8_decode", "tp8_T1024"])
-def test_gemm_full_size_sampled_pairs(w):
-    """Both projections alone at full size; the oracle recomputes sampled pair rows."""
-    ids, _ = wl.make_routing(w)
-    x = wl.make_x(w)
-    (c13, sc13), (c2, sc2), p13, p2 = weights(w)
-    bm = chord.chord_select_block_m(w.T, w.topk, w.E, w.E_global, 2 * w.I, w.H)
-    s, e, n = align(ids, w.E, bm)
-    P = w.P
-    C1 = gemm(x, w.topk, p13, w.E, 2 * w.I, w.H, s, e, n, bm, P, split_k=0)
-    h = wl.random_bf16(99, (P, w.I))
-    C2 = gemm(h, 1, p2, w.E, w.H, w.I, s, e, n, bm, P, split_k=0)
-    got1, got2 = host_bits(C1), host_bits(C2)
+    T, topk, E, H, I = w.T, w.topk, w.E, w.H, w.I
+    P = T * topk
+    bm = chord.chord_select_block_m(T, topk, E, w.E_global, 2 * I, H)
+    fused = chord.chord_select_kernel(bm, 2 * I, H) == chord.KERNEL_WARP_MMA
+    p13_run = pack(w13[0], w13[1], chord.LAYOUT_GATE_UP_INTERLEAVED) if fused else p13
+    st = run_layer_steps(x, ids, wts, E, I, p13_run, p2, bm, fused)
+    opts = chord.ChordOpts(epilogue=chord.EPILOGUE_SILU_MUL if fused else chord.EPILOGUE_NONE)
+    out_layer, _ = layer(x, ids, wts, E, w.E_global, I, p13_run, p2, bm=bm, opts=opts)
+    assert torch.equal(out_layer.view(torch.int16), st["out"].view(torch.int16)), "layer call differs from its steps"
+    del out_layer
+    # the gate_up output itself: the unfused GEMM on the layout-2 blob, same workspace
+    C1 = st["C1"] if st["C1"] is not None else gemm(x, topk, p13, E, 2 * I, H, st["sorted"], st["experts"],
+                                                  st["ntp"], bm, P, split_k=0)
     flat = ids.ravel()
-    local = np.nonzero((flat >= 0) & (flat < w.E))[0]
-    pick = np.random.default_rng(5).choice(local, size=min(16, local.size), replace=False)
-    # the oracle's indexed GEMM over a block list that names only the sampled pairs
-    sub_ids = np.full(flat.shape, -1, np.int32)
-    sub_ids[pick] = flat[pick]
-    o_sorted, o_experts, o_ntp = oracle.moe_align(sub_ids.reshape(ids.shape), w.E, 8)
-    ref1 = oracle.moe_gemm(x, w.topk, c13, sc13, o_sorted, o_experts, o_ntp, 8, P,
-                           C=np.zeros((P, 2 * w.I), np.uint16))
-    ref2 = oracle.moe_gemm(h, 1, c2, sc2, o_sorted, o_experts, o_ntp, 8, P, C=np.zeros((P, w.H), np.uint16))
-    assert_close(got1[pick], ref1[pick], f"{w.name} gate_up sampled pairs")
-    assert_close(got2[pick], ref2[pick], f"{w.name} down sampled pairs")
+    local = np.nonzero((flat >= 0) & (flat < E))[0]
+    li = torch.from_numpy(local).to(DEV)
+    if fused:
+        h2 = torch.empty((P, I), dtype=torch.bfloat16, device=DEV)
+        chord.chord_silu_mul(C1, dev(ids), E, h2)
+        assert torch.equal(st["h"][li].view(torch.int16), h2[li].view(torch.int16)), "fused differs from unfused"
+        del h2
+    sel = checked_tokens(w, ids)
+    pairs = full_pairs(sel, topk)
+    C1g = host_bits(pair_rows(C1, pairs))
+    hg = host_bits(pair_rows(st["h"], pairs))
+    C2g = pair_rows(st["C2"], pairs).cpu().numpy()
+    outg = host_bits(st["out"][torch.from_numpy(sel).to(DEV)])
+    del st, C1
+    torch.cuda.empty_cache()
+    rep = check_layer_chain(x[sel], ids[sel], wts[sel], w13, w2, E, C1g, hg, C2g, outg,
+                            what=f"{w.name} (block_m={bm}, {'fused' if fused else 'unfused'})")
+    none = ~((ids[sel] >= 0) & (ids[sel] < E)).any(axis=1)
+    assert (outg[none] == 0).all()
+    print(f"\n{w.name}: {sel.size} of {T} tokens, {rep['pairs']} pairs; gate_up values differing from the "
+          f"oracle (count, max bf16 steps) {rep['c1_flips']}, from the binary64-sum oracle "
+          f"{rep['c1_flips_vs_f64']}; outputs outside the plain tolerance {rep['out_outside_plain_tol']} of "
+          f"{rep['outputs']}")
+
+
+@pytest.mark.parametrize("w", WORKLOADS, ids=[w.name for w in WORKLOADS])
+def test_full_size_stages_on_oracle_inputs(w):
+    """Each GPU stage at full size fed the oracle's own result of the previous
+    stage (pairs outside the checked tokens get seeded values), on every
+    element of the checked tokens: SiLU * up on the oracle's gate_up, the
+    down projection (FP32 output, with its workspace) on the oracle's h, and
+    the combine on the oracle's down sums, bit for bit."""
+    ids, wts = wl.make_routing(w)
+    x = wl.make_x(w)
+    w13, w2, _, p2 = weights(w)
+    T, topk, E, H, I = w.T, w.topk, w.E, w.H, w.I
+    P = T * topk
+    sel = checked_tokens(w, ids)
+    pairs = full_pairs(sel, topk)
+    ids_s, wts_s = ids[sel], wts[sel]
+    Ps = ids_s.size
+    rows = np.nonzero(((ids_s >= 0) & (ids_s < E)).ravel())[0]
+    s, e, n = oracle.moe_align(ids_s, E, 8)
+    C1r = oracle.moe_gemm(x[sel], topk, w13[0], w13[1], s, e, n, 8, Ps, C=np.zeros((Ps, 2 * I), np.uint16))
+    hr = oracle.silu_mul(C1r, ids_s.ravel(), E, h=np.zeros((Ps, I), np.uint16))
+    C2r = oracle.moe_gemm_f32(hr, 1, w2[0], w2[1], s, e, n, 8, Ps, C=np.zeros((Ps, H), np.float32))
+    outr = oracle.combine(C2r, ids_s, wts_s, E)
+    bm = chord.chord_select_block_m(T, topk, E, w.E_global, 2 * I, H)
+    sd, ed, nd = align(ids, E, bm)
+    # SiLU*up on the oracle's C1 (full size; other pairs seeded)
+    C1in = wl.random_bf16(w.seed + 16, (P, 2 * I))
+    C1in[pairs] = C1r
+    hd = torch.empty((P, I), dtype=torch.bfloat16, device=DEV)
+    chord.chord_silu_mul(dbf(C1in), dev(ids), E, hd)
+    del C1in
+    assert_close(host_bits(pair_rows(hd, pairs))[rows], hr[rows], f"{w.name} silu_mul")
+    del hd
+    # down (FP32 out, the bench's workspace) on the oracle's h
+    hin = wl.random_bf16(w.seed + 17, (P, I))
+    hin[pairs] = hr
+    C2d = torch.full((P, H), float("nan"), dtype=torch.float32, device=DEV)
+    gemm(hin, 1, p2, E, H, I, sd, ed, nd, bm, P, C=C2d, split_k=0, out_dtype=chord.DTYPE_F32)
+    del hin
+    assert_close_f32(pair_rows(C2d, pairs).cpu().numpy()[rows], C2r[rows], f"{w.name} down (block_m={bm})")
+    del C2d
+    torch.cuda.empty_cache()
+    # combine on the oracle's C2
+    out = torch.empty((sel.size, H), dtype=torch.bfloat16, device=DEV)
+    chord.chord_moe_combine(dev(C2r), dev(ids_s), dev(wts_s), E, out)
+    np.testing.assert_array_equal(host_bits(out), outr)

@@ -10,7 +10,8 @@ import torch
 import oracle
 import w4a16_int4_mixture_moe_gb300 as chord
 import workloads as wl
-from gpu_util import (DEV, KERNELS, align, assert_close, assert_close_h, assert_close_layer, dbf, dev, f64, gemm, host_bits,
+from gpu_util import (DEV, KERNELS, align, assert_close, check_h_from_gpu_c1, check_layer_chain, dbf, dev, f64, gemm,
+                      host_bits, run_layer_steps,
                       layer, pack, valid_rows)
 
 pytestmark = pytest.mark.gpu
@@ -447,8 +448,7 @@ def test_split_k_fused_silu_mul(S):
     assert (got[np.setdiff1d(np.arange(P), rows)] == 0xFFFF).all()
     s2, e2, n2 = oracle.moe_align(ids, E, bm)
     c1 = oracle.moe_gemm(x, topk, codes, scales, s2, e2, n2, bm, P, C=np.zeros((P, 2 * I), np.uint16))
-    ref = oracle.silu_mul(c1, ids.ravel(), E, h=np.full((P, I), 0xFFFF, np.uint16))
-    assert_close_h(got[rows], ref[rows], f"split-K fused S={S}")
+    check_h_from_gpu_c1(got, host_bits(C1), c1, ids.ravel(), E, rows, f"split-K fused S={S}")
 
 
 def test_split_k_automatic_one_token():
@@ -575,8 +575,7 @@ def test_tc_tail_split_fused_silu_mul(bm, exact):
     assert (got[np.setdiff1d(np.arange(P), rows)] == 0xFFFF).all()
     s2, e2, n2 = oracle.moe_align(ids, E, bm)
     c1 = oracle.moe_gemm(x, topk, codes, scales, s2, e2, n2, bm, P, C=np.zeros((P, 2 * I), np.uint16))
-    ref = oracle.silu_mul(c1, ids.ravel(), E, h=np.full((P, I), 0xFFFF, np.uint16))
-    assert_close_h(got[rows], ref[rows], f"tail split fused bm={bm}")
+    check_h_from_gpu_c1(got, host_bits(C1), c1, ids.ravel(), E, rows, f"tail split fused bm={bm}")
 
 
 def test_layer_tc_tail_split_vs_oracle():
@@ -589,10 +588,12 @@ def test_layer_tc_tail_split_vs_oracle():
     c13, s13 = wl.random_codes(33, (E, 2 * I, H)), wl.random_scales(34, (E, 2 * I, H // 32))
     c2, s2 = wl.random_codes(35, (E, H, I)), wl.random_scales(36, (E, H, I // 32))
     assert chord.chord_layer_workspace_bytes(T, topk, E, H, I, bm) > 152 * 128 * 256 * 4
-    out, _ = layer(x, ids, wts, E, E, I, pack(c13, s13), pack(c2, s2), bm=bm,
-                   opts=chord.ChordOpts(kernel=TC))
-    ref = oracle.moe_layer(x, ids, wts, (c13, s13), (c2, s2), E, block_m=bm)
-    assert_close_layer(host_bits(out), ref, "layer with a split tail")
+    p13, p2 = pack(c13, s13), pack(c2, s2)
+    out, _ = layer(x, ids, wts, E, E, I, p13, p2, bm=bm, opts=chord.ChordOpts(kernel=TC))
+    st = run_layer_steps(x, ids, wts, E, I, p13, p2, bm, fused=False, kernel=TC)
+    assert torch.equal(out.view(torch.int16), st["out"].view(torch.int16)), "layer call differs from its steps"
+    check_layer_chain(x, ids, wts, (c13, s13), (c2, s2), E, host_bits(st["C1"]), host_bits(st["h"]),
+                      st["C2"].cpu().numpy(), host_bits(st["out"]), "layer with a split tail")
 
 
 # ---------------------------------------------------------- fused SiLU * up
@@ -614,12 +615,12 @@ def run_fused_case(T, topk, E, I, K, bm, seed, kernel, pnl=0.2):
     got = host_bits(h)
     s2, e2, n2 = oracle.moe_align(ids, E, bm)
     c1 = oracle.moe_gemm(x, topk, codes, scales, s2, e2, n2, bm, P, C=np.zeros((P, 2 * I), np.uint16))
-    ref = oracle.silu_mul(c1, ids.ravel(), E, h=np.full((P, I), 0xFFFF, np.uint16))
     rows = valid_rows(ids, E)
     other = np.setdiff1d(np.arange(P), rows)
     assert (got[other] == 0xFFFF).all(), "rows of non-local pairs were written"
-    assert_close_h(got[rows], ref[rows], f"{kernel} fused gate_up T={T} E={E} I={I} K={K} bm={bm}")
     C1 = gemm(x, topk, pack(codes, scales, layout), E, 2 * I, K, s, e, n, bm, P, kernel=kid)
+    check_h_from_gpu_c1(got, host_bits(C1), c1, ids.ravel(), E, rows,
+                        f"{kernel} fused gate_up T={T} E={E} I={I} K={K} bm={bm}")
     h2 = torch.full((max(P, 1), I), -1, dtype=torch.int16, device=DEV)[:P].view(torch.bfloat16)
     chord.chord_silu_mul(C1, dev(ids.ravel().copy()), E, h2)
     np.testing.assert_array_equal(got[rows], host_bits(h2)[rows])
@@ -880,3 +881,94 @@ def test_layer_cuda_graph_replay():
         g.replay()
     torch.cuda.synchronize()
     np.testing.assert_array_equal(host_bits(out), host_bits(eager))
+
+
+# ------------------------------------------------- mixed regime (per-block kernel)
+
+def skewed_ids(seed, T, topk, E, s=2.0):
+    """Zipf-skewed routing without replacement (Gumbel top-k over log rank^-s):
+    a few hot experts with hundreds of rows and a cold tail with a handful."""
+    rng = np.random.default_rng(seed)
+    logp = -s * np.log(np.arange(1, E + 1, dtype=np.float64))
+    keys = logp[None, :] - np.log(-np.log(rng.random((T, E))))
+    return np.ascontiguousarray(np.argsort(-keys, axis=1)[:, :topk].astype(np.int32))
+
+
+@pytest.mark.parametrize("bm,K,exact,silu", [(128, 1024, True, False), (128, 1024, False, False),
+                                             (256, 640, True, False), (64, 2048, False, False),
+                                             (128, 1024, False, True), (256, 1024, True, True)])
+def test_mixed_regime_vs_oracle(bm, K, exact, silu):
+    """Skewed routing (hot experts over several blocks, cold experts with 1-20
+    rows) in the tcgen05 regime with the per-block split on: blocks of at most
+    32 valid rows run on the warp-level kernel, the rest on tcgen05 with its
+    split tail (the reduction must leave the small blocks' rows alone).
+    Bit-exact with the oracle and with the split off in the exact-integer
+    regime; within tolerance on random data; FP32 output and the fused SiLU * up
+    epilogue; rows of non-local pairs untouched."""
+    T, topk, E, N = 300, 4, 24, 1024 if not silu else 512
+    ids = skewed_ids(bm + K, T, topk, E)
+    ids = np.where(np.random.default_rng(bm).random(ids.shape) < 0.05, -1, ids).astype(np.int32)
+    counts = np.bincount(ids[ids >= 0], minlength=E)
+    assert (counts > bm).any() and ((counts > 0) & (counts <= 32)).sum() >= 5
+    rng = np.random.default_rng(K + bm)
+    if exact:
+        x = wl._bf16(rng.integers(-1, 2, size=(T, K)).astype(np.float32))
+        scales = np.full((E, N, K // 32), 0x3F80, np.uint16)
+    else:
+        x = wl.random_bf16(K + 1, (T, K))
+        scales = wl.random_scales(K + 2, (E, N, K // 32))
+    codes = wl.random_codes(K + 3, (E, N, K))
+    P = T * topk
+    s, e, n = align(ids, E, bm)
+    s2, e2, n2 = oracle.moe_align(ids, E, bm)
+    rows = valid_rows(ids, E)
+    other = np.setdiff1d(np.arange(P), rows)
+    ref = oracle.moe_gemm(x, topk, codes, scales, s2, e2, n2, bm, P, C=np.full((P, N), 0xFFFF, np.uint16))
+    if silu:
+        I = N // 2
+        p3 = pack(codes, scales, chord.LAYOUT_GATE_UP_INTERLEAVED)
+        h = torch.full((P, I), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+        gemm(x, topk, p3, E, N, K, s, e, n, bm, P, C=h, split_k=0, epilogue=chord.EPILOGUE_SILU_MUL, mixed=1)
+        got = host_bits(h)
+        assert (got[other] == 0xFFFF).all()
+        C1 = gemm(x, topk, pack(codes, scales), E, N, K, s, e, n, bm, P, split_k=0, mixed=1)
+        check_h_from_gpu_c1(got, host_bits(C1), ref, ids.ravel(), E, rows, f"mixed fused bm={bm}")
+        if exact:
+            # exact sums in any order: the fused epilogue equals the SiLU * up pass on the same C1
+            h2 = torch.full((P, I), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+            chord.chord_silu_mul(C1, dev(ids.ravel().copy()), E, h2)
+            np.testing.assert_array_equal(got[rows], host_bits(h2)[rows])
+        return
+    packed = pack(codes, scales)
+    got = host_bits(gemm(x, topk, packed, E, N, K, s, e, n, bm, P, split_k=0, mixed=1))
+    off = host_bits(gemm(x, topk, packed, E, N, K, s, e, n, bm, P, split_k=0, mixed=-1))
+    assert (got[other] == 0xFFFF).all(), "rows of non-local pairs were written"
+    if exact:
+        np.testing.assert_array_equal(got[rows], ref[rows])
+        np.testing.assert_array_equal(off[rows], ref[rows])
+    else:
+        assert_close(got[rows], ref[rows], f"mixed bm={bm} K={K}")
+        assert_close(off[rows], ref[rows], f"mixed off bm={bm} K={K}")
+    C = torch.full((P, N), float("nan"), dtype=torch.float32, device=DEV)
+    gemm(x, topk, packed, E, N, K, s, e, n, bm, P, C=C, split_k=0, out_dtype=chord.DTYPE_F32, mixed=1)
+    got32 = C.cpu().numpy()
+    ref32 = oracle.moe_gemm_f32(x, topk, codes, scales, s2, e2, n2, bm, P)
+    if exact:
+        np.testing.assert_array_equal(got32[rows], ref32[rows])
+    else:
+        err = np.abs(got32[rows].astype(np.float64) - ref32[rows])
+        assert (err <= 1e-2 + 1e-2 * np.abs(ref32[rows])).all(), err.max()
+    assert np.isnan(got32[other]).all()
+    assert chord.chord_get_device_error() == 0
+
+
+def test_mixed_regime_option_is_checked():
+    """opts.mixed outside -1..1 is refused before anything is enqueued."""
+    E, N, K, bm = 2, 256, 1024, 64
+    codes = wl.random_codes(1, (E, N, K))
+    scales = wl.random_scales(2, (E, N, K // 32))
+    ids = wl.random_ids(3, 8, 2, E)
+    s, e, n = align(ids, E, bm)
+    with pytest.raises(chord.ChordError) as ei:
+        gemm(wl.random_bf16(4, (8, K)), 2, pack(codes, scales), E, N, K, s, e, n, bm, 16, mixed=2)
+    assert ei.value.status == 1

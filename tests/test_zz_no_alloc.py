@@ -11,6 +11,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import w4a16_int4_mixture_moe_gb300 as chord
 import workloads as wl
 
@@ -24,6 +25,7 @@ def _lib():
         pytest.skip("no CUDA device")
     chord.build()
     chord.load()
+    oracle.build()
     chord.chord_get_device_error()
 
 
@@ -50,18 +52,27 @@ def _no_alloc(ids_d, E, bm):
     return s.cpu().numpy(), e.cpu().numpy(), int(n.item())
 
 
+def _oracle(ids, E, bm):
+    s, e, n = oracle.moe_align(ids, E, bm)
+    return np.asarray(s), np.asarray(e), int(n)
+
+
 def test_no_alloc_align_matches_workspace_align_on_two_calls():
-    # first a large call (many slices, many experts), then a smaller one that
-    # reads fewer scratch entries than the first left behind
-    cases = [(wl.SKEWED, 256), (wl.EP8_DECODE, 16)]
-    for w, bm in cases:
-        ids, _ = wl.make_routing(w)
+    # first a large call (32 slices of 4096 pairs x 48 experts of scratch),
+    # then smaller ones: one slice (EP8 decode: 4096 pairs) and two slices of
+    # 64 experts, which read fewer scratch entries than the first left filled
+    cases = [(wl.make_routing(wl.SKEWED)[0], wl.SKEWED.E, 256),
+             (wl.make_routing(wl.EP8_DECODE)[0], wl.EP8_DECODE.E, 16),
+             (wl.random_ids(5, 1024, 8, 64, p_nonlocal=0.1), 64, 32)]
+    for ids, E, bm in cases:
         ids_d = torch.from_numpy(ids).to(DEV)
-        got = _no_alloc(ids_d, w.E, bm)
-        want = _with_workspace(ids_d, w.E, bm)
-        assert got[2] == want[2]
-        np.testing.assert_array_equal(got[0], want[0])
-        np.testing.assert_array_equal(got[1], want[1])
+        got = _no_alloc(ids_d, E, bm)
+        want = _with_workspace(ids_d, E, bm)
+        orc = _oracle(ids, E, bm)
+        assert got[2] == want[2] == orc[2]
+        for i in (0, 1):
+            np.testing.assert_array_equal(got[i], want[i])
+            np.testing.assert_array_equal(got[i], orc[i])
     assert chord.chord_get_device_error() == 0
 
 
@@ -81,4 +92,7 @@ def test_no_alloc_align_repeat_and_limit():
     with pytest.raises(chord.ChordError) as ei:
         chord.chord_moe_align_noalloc(big, 1024, 8, s, e, n)
     assert ei.value.status == 4  # CHORD_ERR_BUFFER_TOO_SMALL
+    torch.cuda.synchronize()
+    # no kernel ran: the outputs still hold their fill
+    assert (s == -7).all() and (e == -7).all() and (n == -7).all()
     assert chord.chord_get_device_error() == 0

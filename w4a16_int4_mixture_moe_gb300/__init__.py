@@ -18,7 +18,7 @@ __all__ = [
     "ChordError", "ChordOpts", "load", "build",
     "chord_version", "chord_status_string", "chord_packed_weight_bytes", "chord_pack_weights",
     "chord_align_capacity", "chord_align_workspace_bytes", "chord_moe_align", "chord_select_block_m", "chord_select_kernel",
-    "chord_gemm_workspace_bytes", "chord_w4a16_moe_gemm", "chord_silu_mul", "chord_moe_combine",
+    "chord_gemm_workspace_bytes", "chord_gemm_launch_count", "chord_w4a16_moe_gemm", "chord_silu_mul", "chord_moe_combine",
     "chord_layer_workspace_bytes", "chord_moe_layer", "chord_get_device_error", "chord_selftest_wait_timeout",
     "chord_grouped_contiguous_workspace_bytes", "chord_grouped_contiguous_gemm",
     "chord_grouped_masked_workspace_bytes", "chord_grouped_masked_gemm",
@@ -43,7 +43,8 @@ class ChordError(RuntimeError):
 
 class ChordOpts(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("validate", ctypes.c_int32), ("split_k", ctypes.c_int32),
-                ("out_dtype", ctypes.c_int32), ("epilogue", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
+                ("out_dtype", ctypes.c_int32), ("epilogue", ctypes.c_int32), ("mixed", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 2)]
 
 
 _lock = threading.Lock()
@@ -64,6 +65,7 @@ _SIGS = {
     "chord_select_block_m": (_int, [_int, _int, _int, _int, _int, _int]),
     "chord_select_kernel": (_int, [_int, _int, _int]),
     "chord_gemm_workspace_bytes": (_sz, [_i64, _int, _int, _int, _OPTS]),
+    "chord_gemm_launch_count": (_int, [_i64, _int, _int, _int, _sz, _OPTS]),
     "chord_w4a16_moe_gemm": (_int, [_vp, _i64, _int, _vp, _sz, _int, _int, _int, _vp, _vp, _vp, _i64, _int, _i64,
                                     _vp, _vp, _sz, _OPTS, _vp]),
     "chord_silu_mul": (_int, [_vp, _vp, _i64, _int, _int, _vp, _vp]),
@@ -185,6 +187,10 @@ def chord_select_kernel(block_m: int, N: int, K: int) -> int:
 
 def chord_gemm_workspace_bytes(num_pairs: int, N: int, K: int, block_m: int, opts=None) -> int:
     return load().chord_gemm_workspace_bytes(num_pairs, N, K, block_m, _o(opts))
+
+
+def chord_gemm_launch_count(num_pairs: int, N: int, K: int, block_m: int, workspace_bytes: int, opts=None) -> int:
+    return int(load().chord_gemm_launch_count(num_pairs, N, K, block_m, workspace_bytes, _o(opts)))
 
 
 def chord_w4a16_moe_gemm(A, a_row_divisor: int, packed, E: int, N: int, K: int, sorted_ids, expert_ids,

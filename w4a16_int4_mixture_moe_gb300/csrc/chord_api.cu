@@ -39,6 +39,8 @@ chord_opts opts_or_default(const chord_opts* o) {
 // for short K (few stages per item), where the tcgen05 kernel's fixed cost per
 // item (pipeline fill, accumulator drain) dominates.
 constexpr int kDecodeMaxBlockM = 32;
+// opts.mixed = 0 (automatic) splits tcgen05-regime calls by block size.
+constexpr bool kMixedByDefault = true;
 constexpr int kShortK = 512;
 constexpr int kShortKMaxBlockM = 64;
 
@@ -293,9 +295,55 @@ size_t gemm_ws_bytes(int64_t num_pairs, int N, int K, int block_m, const chord_o
     if (kernel == CHORD_KERNEL_TCGEN05) return o.split_k == 1 || o.split_k < 0 ? 0 : tc_tail_bytes(block_m);
     return split_bytes(gemm_split(num_pairs, N, K, block_m, o), num_pairs, N);
 }
+
+// What one GEMM call launches, decided on the host from its arguments.
+struct GemmPlan {
+    chord_status status;
+    int kernel;
+    int S;        // K slices of the warp-level kernel
+    bool tail;    // tcgen05 split tail (its reduction is a second launch)
+    bool mixed;   // the small blocks on the warp-level kernel, launched first
+};
+
+GemmPlan plan_gemm(int64_t num_pairs, int N, int K, int block_m, bool ws_ok, size_t workspace_bytes,
+                   const chord_opts& o) {
+    GemmPlan p{CHORD_OK, o.kernel ? o.kernel : chord_select_kernel(block_m, N, K), 1, false, false};
+    // Mixed regime: the small blocks of a tcgen05-regime call on the warp-level kernel.
+    p.mixed = p.kernel == CHORD_KERNEL_TCGEN05 && block_m > CHORD_MIXED_SMALL_ROWS &&
+              (o.mixed > 0 || (o.mixed == 0 && o.kernel == CHORD_KERNEL_AUTO && kMixedByDefault));
+    // K slices: an explicit request needs its partial-sum workspace; the
+    // automatic choice falls back to one slice when the caller gave none.
+    p.S = gemm_split(num_pairs, N, K, block_m, o);
+    if (p.S > 1 && (workspace_bytes < split_bytes(p.S, num_pairs, N) || !ws_ok)) {
+        if (o.split_k > 1) {
+            p.status = workspace_bytes < split_bytes(p.S, num_pairs, N) ? CHORD_ERR_BUFFER_TOO_SMALL
+                                                                         : CHORD_ERR_INVALID_ARG;
+            return p;
+        }
+        p.S = 1;
+    }
+    // tcgen05: the split tail, when the workspace holds its partial sums
+    if (p.kernel == CHORD_KERNEL_TCGEN05 && o.split_k != 1) {
+        const size_t need = tc_tail_bytes(block_m);
+        if (ws_ok && workspace_bytes >= need)
+            p.tail = true;
+        else if (o.split_k > 1)
+            p.status = workspace_bytes < need ? CHORD_ERR_BUFFER_TOO_SMALL : CHORD_ERR_INVALID_ARG;
+    }
+    return p;
+}
 }  // namespace
 
 extern "C" {
+
+int chord_gemm_launch_count(int64_t num_pairs, int N, int K, int block_m, size_t workspace_bytes,
+                            const chord_opts* opts) {
+    if (num_pairs <= 0 || N <= 0 || K <= 0 || block_m <= 0) return 0;
+    const chord_opts o = opts_or_default(opts);
+    const GemmPlan p = plan_gemm(num_pairs, N, K, block_m, workspace_bytes > 0, workspace_bytes, o);
+    if (p.status != CHORD_OK) return 0;
+    return 1 + (p.mixed ? 1 : 0) + (p.S > 1 ? 1 : 0) + (p.tail ? 1 : 0);
+}
 
 size_t chord_gemm_workspace_bytes(int64_t num_pairs, int N, int K, int block_m, const chord_opts* opts) {
     return gemm_ws_bytes(num_pairs, N, K, block_m, opts_or_default(opts));
@@ -325,23 +373,11 @@ chord_status chord_w4a16_moe_gemm(const void* A, int64_t a_rows, int a_row_divis
     const bool silu = o.epilogue == CHORD_EPILOGUE_SILU_MUL;
     if (silu && o.out_dtype != CHORD_DTYPE_BF16) return CHORD_ERR_INVALID_ARG;
     if (o.split_k < 0) return CHORD_ERR_INVALID_ARG;
-    // K slices: an explicit request needs its partial-sum workspace; the
-    // automatic choice falls back to one slice when the caller gave none.
-    int S = gemm_split(num_pairs, N, K, block_m, o);
-    if (S > 1 && (workspace_bytes < split_bytes(S, num_pairs, N) || !workspace || !aligned16(workspace))) {
-        if (o.split_k > 1) return workspace_bytes < split_bytes(S, num_pairs, N) ? CHORD_ERR_BUFFER_TOO_SMALL
-                                                                                 : CHORD_ERR_INVALID_ARG;
-        S = 1;
-    }
-    // tcgen05: the split tail, when the workspace holds its partial sums
-    bool tail = false;
-    if (kernel == CHORD_KERNEL_TCGEN05 && o.split_k != 1) {
-        const size_t need = tc_tail_bytes(block_m);
-        if (workspace && aligned16(workspace) && workspace_bytes >= need)
-            tail = true;
-        else if (o.split_k > 1)
-            return workspace_bytes < need ? CHORD_ERR_BUFFER_TOO_SMALL : CHORD_ERR_INVALID_ARG;
-    }
+    if (o.mixed < -1 || o.mixed > 1) return CHORD_ERR_INVALID_ARG;
+    const GemmPlan plan = plan_gemm(num_pairs, N, K, block_m, workspace && aligned16(workspace), workspace_bytes, o);
+    if (plan.status != CHORD_OK) return plan.status;
+    const int S = plan.S;
+    const bool tail = plan.tail, mixed = plan.mixed;
     const DeviceInfo& di = device_info();
     if (!di.err) return CHORD_ERR_CUDA;
     if (capacity == 0 || num_pairs == 0) return CHORD_OK;
@@ -370,7 +406,18 @@ chord_status chord_w4a16_moe_gemm(const void* A, int64_t a_rows, int a_row_divis
     g.partial_bytes = workspace_bytes;
     g.tail_split = tail ? 1 : 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = kernel == CHORD_KERNEL_TCGEN05 ? launch_gemm_tc(g, s) : launch_gemm_decode(g, s);
+    cudaError_t e = cudaSuccess;
+    if (mixed) {
+        GemmArgs gs = g;
+        gs.block_filter = kBlocksSmall;
+        gs.ksplit = 1;
+        gs.partial = nullptr;
+        gs.partial_bytes = 0;
+        gs.tail_split = 0;
+        e = launch_gemm_decode(gs, s);
+        g.block_filter = kBlocksLarge;
+    }
+    if (e == cudaSuccess) e = kernel == CHORD_KERNEL_TCGEN05 ? launch_gemm_tc(g, s) : launch_gemm_decode(g, s);
     if (e == cudaSuccess && S > 1)
         e = launch_splitk_reduce(g.partial, S, num_pairs, g.id_limit, N, sorted_ids, num_tokens_padded, capacity, C,
                                  g.out_f32, g.silu, s);

@@ -647,6 +647,10 @@ __global__ void tc_tail_reduce_kernel(const GemmArgs a, int64_t G, int kstages, 
         const int64_t b = item / ntiles;
         const int e = a.expert_ids[b];
         if (e < 0 || e >= a.E) continue;
+        // mixed regime: small blocks (sentinel in slot 32) were computed by the warp-level launch
+        if (a.block_filter == kBlocksLarge &&
+            a.sorted_ids[b * a.block_m + CHORD_MIXED_SMALL_ROWS] == (int32_t)a.num_pairs)
+            continue;
         const int32_t id = a.sorted_ids[b * a.block_m + j];
         if (id < 0 || (int64_t)id >= a.id_limit) continue;
         const int r = kSilu ? 16 * (rr / 8) + rr % 8 : rr;

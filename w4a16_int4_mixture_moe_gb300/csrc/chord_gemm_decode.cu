@@ -236,6 +236,13 @@ __device__ __forceinline__ bool consume_nv(const GemmArgs& a, uint8_t* smem, uin
                                                                my_id, ks0, ks1, slice);
 }
 
+// Mixed regime: whether align block b is one of the small blocks this launch
+// takes (at most 32 valid rows; the valid rows of a block are a prefix).
+__device__ __forceinline__ bool block_taken(const GemmArgs& a, int64_t b) {
+    if (a.block_filter != kBlocksSmall || a.block_m <= CHORD_MIXED_SMALL_ROWS) return true;
+    return a.sorted_ids[b * a.block_m + CHORD_MIXED_SMALL_ROWS] == (int32_t)a.num_pairs;
+}
+
 // Work unit -> (align block b, token sub-block, 128-row N tile, K slice and
 // its stage range); 32-bit divisions while the unit index fits (always, in
 // practice), no slice arithmetic when K is not split.
@@ -289,7 +296,9 @@ __global__ void __launch_bounds__(Cfg<NT, MI>::kThreads, MINB) gemm_decode_kerne
         if (threadIdx.x == 0) set_error(a.err, CHORD_DEV_BAD_PADDED);
         ntp = 0;
     }
-    const int nsub = (a.block_m + kTok - 1) / kTok;   // token sub-blocks; slots past block_m are empty
+    // token sub-blocks (slots past block_m are empty); the mixed regime's small
+    // blocks have all their rows in the first
+    const int nsub = a.block_filter == kBlocksSmall ? 1 : (a.block_m + kTok - 1) / kTok;
     const int ntiles = a.N / kBN;
     const int64_t n_items = (int64_t)(ntp / a.block_m) * nsub * ntiles;
     const int kstages = (a.K + kKS - 1) / kKS;
@@ -308,6 +317,7 @@ __global__ void __launch_bounds__(Cfg<NT, MI>::kThreads, MINB) gemm_decode_kerne
         for (int64_t unit = blockIdx.x; unit < n_units && !aborted; unit += gridDim.x) {
             int slice, nt, sub, ks0, ks1;
             const int64_t b = unit_coords(unit, S, ntiles, nsub, kstages, slice, nt, sub, ks0, ks1);
+            if (!block_taken(a, b)) continue;
             const int e = a.expert_ids[b];
             if (e < 0 || e >= a.E) {
                 if (lane == 0) set_error(a.err, CHORD_DEV_BAD_EXPERT);
@@ -369,6 +379,7 @@ __global__ void __launch_bounds__(Cfg<NT, MI>::kThreads, MINB) gemm_decode_kerne
     for (int64_t unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
         int slice, nt, sub, ks0, ks1;
         const int64_t b = unit_coords(unit, S, ntiles, nsub, kstages, slice, nt, sub, ks0, ks1);
+        if (!block_taken(a, b)) continue;
         const int e = a.expert_ids[b];
         if (e < 0 || e >= a.E) continue;
         const ItemRows rows = load_item_rows<NT>(a, b, sub, lane, slice == 0 ? a.err : nullptr);
@@ -391,8 +402,8 @@ cudaError_t launch_nt(const GemmArgs& a, cudaStream_t stream) {
     int per_sm = 1;
     cudaError_t e = kernel_ctas_per_sm(reinterpret_cast<const void*>(kern), C::kThreads, smem, smem, &per_sm);
     if (e != cudaSuccess) return e;
-    const int64_t items_cap = (a.capacity / a.block_m) * ((a.block_m + NT * 8 - 1) / (NT * 8)) * (a.N / kBN) *
-                              (a.ksplit > 1 ? a.ksplit : 1);
+    const int64_t nsub = a.block_filter == kBlocksSmall ? 1 : (a.block_m + NT * 8 - 1) / (NT * 8);
+    const int64_t items_cap = (a.capacity / a.block_m) * nsub * (a.N / kBN) * (a.ksplit > 1 ? a.ksplit : 1);
     int64_t grid = (int64_t)device_info().sm_count * per_sm;
     if (grid > items_cap) grid = items_cap;
     if (grid < 1) grid = 1;

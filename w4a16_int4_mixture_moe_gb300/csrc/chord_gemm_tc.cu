@@ -196,6 +196,9 @@ __device__ __forceinline__ ItemInfo item_info(const GemmArgs& a, int64_t b, int 
         if (ok) last = i;
     }
     last = __reduce_max_sync(0xffffffffu, last + 1);
+    // mixed regime: a block whose slot 32 holds the sentinel has at most 32
+    // valid rows (they are a prefix) and belongs to the warp-level launch
+    if (a.block_filter == kBlocksLarge && __shfl_sync(0xffffffffu, ids[1], 0) == (int32_t)a.num_pairs) last = 0;
     r.n_mma = (last + 15) / 16 * 16;
     return r;
 }

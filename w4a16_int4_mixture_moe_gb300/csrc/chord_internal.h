@@ -51,6 +51,13 @@ cudaError_t launch_combine(const void* C2, bool c2_f32, const int32_t* topk_ids,
                            int topk, int E, int H, uint16_t* out, cudaStream_t stream);
 
 // ---- GEMMs ---------------------------------------------------------------
+// GemmArgs::block_filter.  The valid rows of an align block are a prefix of
+// its slots (align fills each expert's blocks from the front), so a block is
+// small exactly when its slot CHORD_MIXED_SMALL_ROWS holds the sentinel (or
+// the block has no such slot).
+constexpr int kBlocksAll = 0;
+constexpr int kBlocksSmall = 1;   // warp-level kernel, first 32-row sub-block only
+constexpr int kBlocksLarge = 2;   // tcgen05 kernel
 struct GemmArgs {
     const uint16_t* A;
     int64_t a_rows;
@@ -73,6 +80,8 @@ struct GemmArgs {
                        // tcgen05 tail split: [tail units, 128, tok_tile], reduced by launch_tc_tail_reduce
     size_t partial_bytes;
     int tail_split;    // tcgen05: cut the last partial wave's items into K slices (needs `partial`)
+    int block_filter;  // kBlocksAll, or (mixed regime) only blocks with at most / more than
+                       // CHORD_MIXED_SMALL_ROWS valid rows
     int* err;
 };
 

@@ -204,7 +204,15 @@ def tp8(T: int) -> Workload:
 SKEWED = Workload("skewed_zipf1.2_T16384_E48of384_top8_H7168_I2048", T=16384, E=48,
                   E_global=384, topk=8, H=7168, I=2048, routing="zipf", seed=4)
 
-ALL = {w.name: w for w in (TINY, EP8_DECODE, EP8_PREFILL, *[tp8(t) for t in TP8_T], SKEWED)}
+# The skewed configuration's own description has cold experts with 0-2 rows,
+# which Zipf(1.2) over 384 experts does not produce for the 48 local ones
+# (their fewest rows are about 30).  A steeper Zipf(2.0) does: hot experts with
+# thousands of rows, about twenty local experts with 0-8 rows and one with none
+# (seed 5).  It is a parity case and a measurement of the per-block regime.
+SKEWED_COLD = Workload("skewed_cold_zipf2.0_T16384_E48of384_top8_H7168_I2048", T=16384, E=48,
+                       E_global=384, topk=8, H=7168, I=2048, routing="zipf", seed=5, zipf_s=2.0)
+
+ALL = {w.name: w for w in (TINY, EP8_DECODE, EP8_PREFILL, *[tp8(t) for t in TP8_T], SKEWED, SKEWED_COLD)}
 
 
 def by_name(name: str) -> Optional[Workload]:
