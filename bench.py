@@ -500,12 +500,16 @@ class LayerRig:
         self.C1 = None if fused else torch.empty((P, 2 * I), dtype=torch.bfloat16, device=dev)
         self.h = torch.empty((P, I), dtype=torch.bfloat16, device=dev)
         self.C2 = torch.empty((P, H), dtype=torch.float32, device=dev)
+        # top-k combine fused into the down GEMM (as chord_moe_layer runs it), or the separate pass
+        self.fuse_combine = getattr(args, "fused_combine", False) and topk <= 32
+        self.pair_w = torch.empty(P, dtype=torch.float32, device=dev)
         self.out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
         self.stream = torch.cuda.current_stream()
         mixed = getattr(args, "mixed", 0)
-        self.f32_out = chord.ChordOpts(out_dtype=chord.DTYPE_F32, mixed=mixed)
+        fc = 1 if self.fuse_combine else -1
+        self.f32_out = chord.ChordOpts(out_dtype=chord.DTYPE_F32, mixed=mixed, fuse_combine=fc)
         self.silu_opts = chord.ChordOpts(epilogue=chord.EPILOGUE_SILU_MUL if fused else chord.EPILOGUE_NONE,
-                                         mixed=mixed)
+                                         mixed=mixed, fuse_combine=fc)
         # K-slice / split-tail partial sums (workspace of each GEMM)
         self.split = (chord.chord_gemm_workspace_bytes(P, 2 * I, H, bm, self.silu_opts),
                       chord.chord_gemm_workspace_bytes(P, H, I, bm, self.f32_out))
@@ -513,7 +517,9 @@ class LayerRig:
         # align: one launch up to 4096 pairs, three above; each GEMM's launches as the
         # library reports them (the GEMM, the mixed regime's warp-level launch, a
         # split reduction); the SiLU * up pass when unfused; combine
-        self.launches_per_step = ((1 if P <= 4096 else 3) + (0 if fused else 1) + 1 +
+        # split reduction); the SiLU * up pass when unfused; the combine (plan and
+        # finishing pass when fused into the down GEMM)
+        self.launches_per_step = ((1 if P <= 4096 else 3) + (0 if fused else 1) + (2 if self.fuse_combine else 1) +
                                   chord.chord_gemm_launch_count(P, 2 * I, H, bm, self.split[0], self.silu_opts) +
                                   chord.chord_gemm_launch_count(P, H, I, bm, self.split[1], self.f32_out))
         # public layer call: its own workspace and copies of the inputs
@@ -539,6 +545,11 @@ class LayerRig:
 
     def down(self, st):
         w = self.w
+        if self.fuse_combine:
+            self.chord.chord_w4a16_moe_gemm_combine(self.h, self.p2, w.E, w.H, w.I, self.sorted_ids, self.expert_ids,
+                                                    self.ntp, self.bm, w.topk, self.pair_w, self.C2, self.out,
+                                                    workspace=self.gws, opts=self.f32_out, stream=st)
+            return
         self.chord.chord_w4a16_moe_gemm(self.h, 1, self.p2, w.E, w.H, w.I, self.sorted_ids, self.expert_ids,
                                         self.ntp, self.bm, w.P, self.C2, workspace=self.gws, opts=self.f32_out,
                                         stream=st)
@@ -553,12 +564,17 @@ class LayerRig:
             marks[1].record(st)
         if not self.fused:
             c.chord_silu_mul(self.C1, self.idd, w.E, self.h, stream=st)
+        if self.fuse_combine:
+            c.chord_combine_plan(self.idd, self.wd, w.E, self.pair_w, stream=st)
         if marks:
             marks[2].record(st)
         self.down(st)
         if marks:
             marks[3].record(st)
-        c.chord_moe_combine(self.C2, self.idd, self.wd, w.E, self.out, stream=st)
+        if self.fuse_combine:
+            c.chord_combine_finish(self.C2, self.idd, self.wd, w.E, self.out, stream=st)
+        else:
+            c.chord_moe_combine(self.C2, self.idd, self.wd, w.E, self.out, stream=st)
 
     def capture(self, fn):
         torch = self.torch
@@ -711,7 +727,7 @@ def measure_prefill_regime(chord, torch, dev, rank, world, args, pg):
     fractions of the burst and sustained BF16 rates, end to end through the
     public call."""
     w = wl.EP8_PREFILL
-    sub = argparse.Namespace(**{**vars(args), "block_m": 0, "fused": False, "unfused": False})
+    sub = argparse.Namespace(**{**vars(args), "block_m": 0, "fused": False, "unfused": False, "mixed": 0})
     rig = LayerRig(chord, torch, w, dev, rank, sub)
     peaks = load_peaks()
 
@@ -746,6 +762,7 @@ def measure_prefill_regime(chord, torch, dev, rank, world, args, pg):
                    "d2h_bytes_per_step": db},
            "details": {"timing": f"CUDA graph replay per step, device events; GEMMs: {how}",
                        "silu_mul": "fused into gate_up" if rig.fused else "separate pass",
+                       "combine": "fused into the down GEMM" if rig.fuse_combine else "separate pass",
                        "split_k": rig.split_desc()},
            "gpu_launches": rig.launches_per_step * steps}
     rig.release()
@@ -766,8 +783,12 @@ def main():
     ap.add_argument("--unfused", action="store_true", help="separate SiLU * up pass instead of the fused epilogue")
     ap.add_argument("--fused", action="store_true", help="SiLU * up in the gate_up epilogue on either kernel")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--mixed", type=int, default=0, choices=[-1, 0, 1],
-                    help="per-block regime of tcgen05-regime GEMMs: 0 automatic, 1 on, -1 off")
+    ap.add_argument("--fused-combine", action="store_true",
+                    help="the top-k combine fused into the down GEMM (chord_moe_layer opts.fuse_combine = 1) "
+                         "instead of the separate pass")
+    ap.add_argument("--mixed", type=int, default=None, choices=[-1, 0, 1],
+                    help="per-block regime of tcgen05-regime GEMMs (opts.mixed): 1 on, -1 off, 0 the library's "
+                         "choice; default: on for the cold-tail skewed workload, the library's choice otherwise")
     args = ap.parse_args()
     if args.workload in GROUPED:
         if args.impl == "reference":
@@ -775,6 +796,9 @@ def main():
             return
         return run_grouped(args, args.workload)
     w = WORKLOADS[args.workload]
+    if args.mixed is None:
+        # the caller that knows its routing has a cold tail asks for the split
+        args.mixed = 1 if w.name == wl.SKEWED_COLD.name else 0
     if args.impl == "reference":
         return run_reference(args, w)
     args.warmup = max(args.warmup, 3)
@@ -837,6 +861,7 @@ def main():
     clk = sampler.summary(t_lo, t_hi)
     details = {"timing": f"CUDA graph replay per step (align, GEMMs, combine), device events; GEMMs: {gemm_timing}",
                "silu_mul": "fused into gate_up" if rig.fused else "separate pass", "split_k": rig.split_desc(),
+               "combine": "fused into the down GEMM" if rig.fuse_combine else "separate pass",
                "host_us_per_call": "median CPU time of one eager chord_moe_layer enqueue through the Python binding"}
     line = {
         "metric": METRIC, "value": round(us_per_call, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,

@@ -122,11 +122,19 @@ typedef struct chord_opts {
                             "Indexed kernels"), decided on the device from the align
                             output: blocks holding at most CHORD_MIXED_SMALL_ROWS valid
                             rows run on the warp-level kernel (launched first), the
-                            others on the tcgen05 kernel.  0 = automatic (on when the
-                            call runs the tcgen05 kernel by automatic choice with
-                            block_m > CHORD_MIXED_SMALL_ROWS), 1 = on (also with the
-                            kernel forced to tcgen05), -1 = off. */
-    int32_t reserved[2]; /* must be zero */
+                            others on the tcgen05 kernel, for calls in the tcgen05
+                            regime with block_m > CHORD_MIXED_SMALL_ROWS.  1 = on (also
+                            with the kernel forced to tcgen05); 0 = the library's
+                            choice, currently off (it pays only when many experts are
+                            cold, which the host cannot see without a readback);
+                            -1 = off. */
+    int32_t fuse_combine; /* chord_moe_layer: 1 = the top-k combine fused into the down
+                             GEMM (chord_combine_plan, chord_w4a16_moe_gemm_combine,
+                             chord_combine_finish; topk <= 32); 0 (the library's
+                             choice, measured faster on GB300) or -1 = the separate
+                             chord_moe_combine pass.  The result is the same bit for
+                             bit. */
+    int32_t reserved[1]; /* must be zero */
 } chord_opts;
 
 /* Blocks with at most this many valid rows count as small for opts.mixed. */
@@ -379,11 +387,50 @@ chord_status chord_moe_combine(const void *C2, int c2_dtype, const int32_t *topk
                                const float *topk_w, int T, int topk, int E, int H, void *out,
                                void *stream);
 
+/* The top-k combine fused into the down GEMM (the benchmark spec's gather/scatter
+ * epilogue with top-k weights): the same out as chord_moe_combine of the down
+ * GEMM's FP32 output, bit for bit, in three calls.  A token with exactly one
+ * local pair gets its output straight from the GEMM's epilogue,
+ * bf16(0 + w * sum), which is the weighted sum over that one pair; the FP32
+ * rows of the other local pairs go to C2 and chord_combine_finish adds them
+ * in ascending k as the combine does.  No atomics, so the result does not
+ * depend on the order in which blocks finish.  topk <= 32.
+ *
+ * chord_combine_plan: pair_w device float [T * topk] (caller's scratch):
+ *   pair_w[p] = topk_w[p] for the local pair of a token with one local pair,
+ *   NaN for the local pairs of tokens with several; other entries untouched. */
+chord_status chord_combine_plan(const int32_t *topk_ids, const float *topk_w, int T, int topk, int E,
+                                float *pair_w, void *stream);
+
+/* The down projection with the fused combine: chord_w4a16_moe_gemm with one A
+ * row per pair (a_rows = num_pairs = T * topk, a_row_divisor = 1), FP32 sums,
+ * opts->epilogue = CHORD_EPILOGUE_NONE (opts->out_dtype is ignored), and the
+ * plan's pair_w: rows of pairs whose pair_w is a number are written to
+ *   out[p / topk, n] = bf16_rne( 0 + pair_w[p] * sum )   (out bf16 [T, N])
+ * and the others' FP32 sums to C2 [T * topk, N].  Same workspace, kernels,
+ * splits, status codes and device errors as chord_w4a16_moe_gemm. */
+chord_status chord_w4a16_moe_gemm_combine(const void *A, const void *packed, size_t packed_bytes, int E, int N,
+                                          int K, const int32_t *sorted_ids, const int32_t *expert_ids,
+                                          const int32_t *num_tokens_padded, int64_t capacity, int block_m, int T,
+                                          int topk, const float *pair_w, float *C2, void *out, void *workspace,
+                                          size_t workspace_bytes, const chord_opts *opts, void *stream);
+
+/* Finishing pass of the fused combine: for every token with several local
+ * pairs (or one whose weight is not a number),
+ *   out[t, n] = bf16_rne( sum over local k ascending of topk_w[t, k] * C2[t * topk + k, n] )
+ * (FP32 from +0, products and sums rounded separately); +0 for tokens with no
+ * local pair; tokens with one local pair are left to the GEMM.  C2 device
+ * float [T * topk, H], out bf16 [T, H], H % 8 == 0, topk <= 32. */
+chord_status chord_combine_finish(const float *C2, const int32_t *topk_ids, const float *topk_w, int T, int topk,
+                                  int E, int H, void *out, void *stream);
+
 /* ------------------------------------------------------------------ layer */
 
 /* Scratch bytes chord_moe_layer needs for this shape and block_m (0 = the
- * block size chord_select_block_m picks with E_global = E), including the
- * larger of the two GEMMs' automatic K-slice partial sums (an explicit
+ * block size chord_select_block_m picks with E_global = E): the routing
+ * arrays, the gate_up output, h, the down projection's FP32 rows, the fused
+ * combine's per-pair weights (T * topk floats), and the larger of the two
+ * GEMMs' automatic K-slice partial sums (an explicit
  * opts->split_k larger than that makes the layer call return
  * CHORD_ERR_BUFFER_TOO_SMALL). */
 size_t chord_layer_workspace_bytes(int T, int topk, int E, int H, int I, int block_m);

@@ -200,7 +200,7 @@ def valid_rows(ids, E):
     return np.nonzero((flat >= 0) & (flat < E))[0]
 
 
-def run_layer_steps(x_bits, ids, wts, E, I, p13, p2, bm, fused, kernel=0, split=True):
+def run_layer_steps(x_bits, ids, wts, E, I, p13, p2, bm, fused, kernel=0, split=True, mixed=0):
     """The layer as the benchmark's step runs it, every call through the C ABI:
     align -> gate_up (SiLU * up fused when `fused`, w13 then in layout 3) ->
     SiLU * up pass (unfused) -> down with FP32 output -> combine.  Each GEMM
@@ -216,13 +216,14 @@ def run_layer_steps(x_bits, ids, wts, E, I, p13, p2, bm, fused, kernel=0, split=
     C1 = None
     if fused:
         gemm(xd, topk, p13, E, 2 * I, H, s, e, n, bm, P, kernel=kernel, C=h, split_k=0 if split else None,
-             epilogue=epi)
+             epilogue=epi, mixed=mixed)
     else:
-        C1 = gemm(xd, topk, p13, E, 2 * I, H, s, e, n, bm, P, kernel=kernel, split_k=0 if split else None)
+        C1 = gemm(xd, topk, p13, E, 2 * I, H, s, e, n, bm, P, kernel=kernel, split_k=0 if split else None,
+                  mixed=mixed)
         chord.chord_silu_mul(C1, idd, E, h)
     C2 = torch.full((max(P, 1), H), float("nan"), dtype=torch.float32, device=DEV)[:P]
     gemm(h, 1, p2, E, H, I, s, e, n, bm, P, kernel=kernel, C=C2, split_k=0 if split else None,
-         out_dtype=chord.DTYPE_F32)
+         out_dtype=chord.DTYPE_F32, mixed=mixed)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
     chord.chord_moe_combine(C2, idd, wd, E, out)
     return {"sorted": s, "experts": e, "ntp": n, "C1": C1, "h": h, "C2": C2, "out": out}

@@ -156,6 +156,7 @@ def test_layer_workspace_formula(lib):
     want = up(want + P * 2 * I * 2)
     want = up(want + P * I * 2)
     want = up(want + P * H * 4)   # the down projection's FP32 sums
+    want = up(want + P * 4)       # the fused combine's per-pair weights
     # 4096 pairs fill the GPU: no K slices, no partial-sum space
     assert chord.chord_layer_workspace_bytes(T, topk, E, H, I, bm) == want
     # one token, TP8 shapes: the gate_up projection is cut into 15 K slices
@@ -163,7 +164,7 @@ def test_layer_workspace_formula(lib):
     P = T * topk
     cap = chord.chord_align_capacity(T, topk, E, bm)
     want = up(chord.chord_align_workspace_bytes(T, topk, E))
-    for b in (cap * 4, cap // bm * 4, 4, P * 2 * I * 2, P * I * 2, P * H * 4):
+    for b in (cap * 4, cap // bm * 4, 4, P * 2 * I * 2, P * I * 2, P * H * 4, P * 4):
         want = up(want + b)
     want = up(want + max(chord.chord_gemm_workspace_bytes(P, 2 * I, H, bm),
                          chord.chord_gemm_workspace_bytes(P, H, I, bm)))

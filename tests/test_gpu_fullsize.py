@@ -90,7 +90,8 @@ def full_pairs(sel, topk):
 def test_full_size_layer_chain(w):
     """The benchmark's step at full size (align -> gate_up [+ fused SiLU * up]
     -> down -> combine through the C ABI):
-      * chord_moe_layer returns the step's output bit for bit;
+      * chord_moe_layer returns the step's output bit for bit, with the top-k
+        combine as a separate pass and fused into the down GEMM;
       * where the step fuses SiLU * up, the fused h equals the unfused GEMM
         followed by the SiLU * up pass bit for bit on every local pair;
       * on the checked tokens, every element of every stage passes the chain
@@ -106,14 +107,20 @@ def test_full_size_layer_chain(w):
     bm = chord.chord_select_block_m(T, topk, E, w.E_global, 2 * I, H)
     fused = chord.chord_select_kernel(bm, 2 * I, H) == chord.KERNEL_WARP_MMA
     p13_run = pack(w13[0], w13[1], chord.LAYOUT_GATE_UP_INTERLEAVED) if fused else p13
-    st = run_layer_steps(x, ids, wts, E, I, p13_run, p2, bm, fused)
-    opts = chord.ChordOpts(epilogue=chord.EPILOGUE_SILU_MUL if fused else chord.EPILOGUE_NONE)
+    # the cold-tail routing runs with the per-block regime split on, as its benchmark does
+    mixed = 1 if w.name == wl.SKEWED_COLD.name else 0
+    st = run_layer_steps(x, ids, wts, E, I, p13_run, p2, bm, fused, mixed=mixed)
+    opts = chord.ChordOpts(epilogue=chord.EPILOGUE_SILU_MUL if fused else chord.EPILOGUE_NONE, mixed=mixed)
     out_layer, _ = layer(x, ids, wts, E, w.E_global, I, p13_run, p2, bm=bm, opts=opts)
     assert torch.equal(out_layer.view(torch.int16), st["out"].view(torch.int16)), "layer call differs from its steps"
-    del out_layer
+    # the same layer with the top-k combine fused into the down GEMM: bit for bit
+    opts.fuse_combine = 1
+    out_fc, _ = layer(x, ids, wts, E, w.E_global, I, p13_run, p2, bm=bm, opts=opts)
+    assert torch.equal(out_fc.view(torch.int16), st["out"].view(torch.int16)), "fused combine differs"
+    del out_layer, out_fc
     # the gate_up output itself: the unfused GEMM on the layout-2 blob, same workspace
     C1 = st["C1"] if st["C1"] is not None else gemm(x, topk, p13, E, 2 * I, H, st["sorted"], st["experts"],
-                                                  st["ntp"], bm, P, split_k=0)
+                                                  st["ntp"], bm, P, split_k=0, mixed=mixed)
     flat = ids.ravel()
     local = np.nonzero((flat >= 0) & (flat < E))[0]
     li = torch.from_numpy(local).to(DEV)

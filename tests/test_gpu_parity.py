@@ -972,3 +972,114 @@ def test_mixed_regime_option_is_checked():
     with pytest.raises(chord.ChordError) as ei:
         gemm(wl.random_bf16(4, (8, K)), 2, pack(codes, scales), E, N, K, s, e, n, bm, 16, mixed=2)
     assert ei.value.status == 1
+
+
+# ------------------------------------------------- top-k combine fused into the down GEMM
+
+def _combine_case(seed, T, topk, E, none_token=3):
+    ids = wl.random_ids(seed, T, topk, 4 * E)
+    ids = np.where(ids < E, ids, -1).astype(np.int32)     # about 1/4 of the pairs local
+    ids[none_token, :] = -1                               # a token with no local pair
+    ids[none_token + 1, :] = -1
+    ids[none_token + 1, 2] = 0                            # a token with exactly one
+    ids[none_token + 2, :] = np.arange(topk) % E          # a token with all pairs local
+    return np.ascontiguousarray(ids)
+
+
+@pytest.mark.parametrize("kernel,bm,K,split", [("warp_mma", 16, 1024, None), ("warp_mma", 8, 2048, 0),
+                                               ("tcgen05", 64, 1024, 0), ("tcgen05", 128, 512, None),
+                                               ("auto", 256, 1024, 0)])
+def test_fused_combine_matches_the_separate_pass(kernel, bm, K, split):
+    """chord_combine_plan -> chord_w4a16_moe_gemm_combine -> chord_combine_finish
+    gives exactly what the down GEMM's FP32 output followed by the combine pass
+    gives (bit for bit, also against the oracle's combine of that output), on
+    routing with tokens that have no, one and several local pairs; with K
+    slices (warp-level), the tcgen05 split tail, and the mixed regime (auto,
+    256-row blocks)."""
+    T, topk, E, N = 120, 8, 6, 512
+    ids = _combine_case(bm + K, T, topk, E)
+    w = wl.random_weights(K, T, topk)
+    P = T * topk
+    A = wl.random_bf16(bm, (P, K))
+    codes = wl.random_codes(bm + 1, (E, N, K))
+    scales = wl.random_scales(bm + 2, (E, N, K // 32))
+    packed = pack(codes, scales)
+    kid = 0 if kernel == "auto" else KERNELS[kernel][0]
+    s, e, n = align(ids, E, bm)
+    idd, wd = dev(ids), dev(w)
+    opts = chord.ChordOpts(kernel=kid, split_k=split or 0, out_dtype=chord.DTYPE_F32,
+                           mixed=1 if kernel == "auto" else 0)
+    nb = chord.chord_gemm_workspace_bytes(P, N, K, bm, opts) if split is not None else 0
+    ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=DEV) if split is not None else None
+    # the separate path
+    C2 = torch.full((P, N), float("nan"), dtype=torch.float32, device=DEV)
+    chord.chord_w4a16_moe_gemm(dbf(A), 1, packed, E, N, K, s, e, n, bm, P, C2, workspace=ws, opts=opts)
+    out_sep = torch.empty((T, N), dtype=torch.bfloat16, device=DEV)
+    chord.chord_moe_combine(C2, idd, wd, E, out_sep)
+    # the fused path
+    pair_w = torch.full((P,), 7.0, dtype=torch.float32, device=DEV)
+    chord.chord_combine_plan(idd, wd, E, pair_w)
+    flat = ids.ravel()
+    local = (flat >= 0) & (flat < E)
+    cnt = local.reshape(T, topk).sum(axis=1)
+    pw = pair_w.cpu().numpy()
+    single = local & (np.repeat(cnt, topk) == 1)
+    multi = local & (np.repeat(cnt, topk) > 1)
+    np.testing.assert_array_equal(pw[single], w.ravel()[single])
+    assert np.isnan(pw[multi]).all() and (pw[~local] == 7.0).all()
+    C2f = torch.full((P, N), float("nan"), dtype=torch.float32, device=DEV)
+    out = torch.full((T, N), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+    chord.chord_w4a16_moe_gemm_combine(dbf(A), packed, E, N, K, s, e, n, bm, topk, pair_w, C2f, out, workspace=ws,
+                                       opts=opts)
+    c2 = C2.cpu().numpy()
+    c2f = C2f.cpu().numpy()
+    np.testing.assert_array_equal(c2f[multi], c2[multi])       # several local pairs: FP32 rows as before
+    assert np.isnan(c2f[~multi]).all()                          # the others: nothing written to C2
+    chord.chord_combine_finish(C2f, idd, wd, E, out)
+    got = host_bits(out)
+    np.testing.assert_array_equal(got, host_bits(out_sep))
+    np.testing.assert_array_equal(got, oracle.combine(c2, ids, w, E))
+    assert (got[cnt == 0] == 0).all()
+    assert chord.chord_get_device_error() == 0
+
+
+@BOTH
+@pytest.mark.parametrize("silu", [False, True])
+def test_layer_fused_combine_bit_identical(kernel, silu):
+    """chord_moe_layer with the fused combine (opts.fuse_combine = 1) equals
+    the layer with the separate combine pass bit for bit; EP-like routing with tokens
+    that have no, one and several local pairs."""
+    T, topk, E, H, I = 40, 8, 6, 256, 128
+    ids = _combine_case(9, T, topk, E)
+    wts = wl.random_weights(10, T, topk)
+    x = wl.random_bf16(11, (T, H))
+    c13, s13 = wl.random_codes(12, (E, 2 * I, H)), wl.random_scales(13, (E, 2 * I, H // 32))
+    c2, s2 = wl.random_codes(14, (E, H, I)), wl.random_scales(15, (E, H, I // 32))
+    kid, layout = KERNELS[kernel]
+    p13 = pack(c13, s13, chord.LAYOUT_GATE_UP_INTERLEAVED if silu else layout)
+    p2 = pack(c2, s2, layout)
+    epi = chord.EPILOGUE_SILU_MUL if silu else chord.EPILOGUE_NONE
+    a, bm = layer(x, ids, wts, E, 4 * E, I, p13, p2, bm=16,
+                  opts=chord.ChordOpts(kernel=kid, epilogue=epi, fuse_combine=1))
+    b, _ = layer(x, ids, wts, E, 4 * E, I, p13, p2, bm=16,
+                 opts=chord.ChordOpts(kernel=kid, epilogue=epi, fuse_combine=-1))
+    np.testing.assert_array_equal(host_bits(a), host_bits(b))
+    got = host_bits(a)
+    none = ~((ids >= 0) & (ids < E)).any(axis=1)
+    assert (got[none] == 0).all()
+
+
+def test_fused_combine_rejects_bad_arguments():
+    """topk above 32 and an out pointer that is not 16-byte aligned are refused
+    before anything is enqueued."""
+    ids = torch.zeros((4, 33), dtype=torch.int32, device=DEV)
+    w = torch.zeros((4, 33), dtype=torch.float32, device=DEV)
+    pw = torch.zeros(4 * 33, dtype=torch.float32, device=DEV)
+    with pytest.raises(chord.ChordError) as ei:
+        chord.chord_combine_plan(ids, w, 2, pw)
+    assert ei.value.status == 2
+    C2 = torch.zeros((4 * 33, 256), dtype=torch.float32, device=DEV)
+    out = torch.zeros((4, 256), dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(chord.ChordError) as ei:
+        chord.chord_combine_finish(C2, ids, w, 2, out)
+    assert ei.value.status == 2

@@ -19,6 +19,7 @@ __all__ = [
     "chord_version", "chord_status_string", "chord_packed_weight_bytes", "chord_pack_weights",
     "chord_align_capacity", "chord_align_workspace_bytes", "chord_moe_align", "chord_select_block_m", "chord_select_kernel",
     "chord_gemm_workspace_bytes", "chord_gemm_launch_count", "chord_w4a16_moe_gemm", "chord_silu_mul", "chord_moe_combine",
+    "chord_combine_plan", "chord_w4a16_moe_gemm_combine", "chord_combine_finish",
     "chord_layer_workspace_bytes", "chord_moe_layer", "chord_get_device_error", "chord_selftest_wait_timeout",
     "chord_grouped_contiguous_workspace_bytes", "chord_grouped_contiguous_gemm",
     "chord_grouped_masked_workspace_bytes", "chord_grouped_masked_gemm",
@@ -44,7 +45,7 @@ class ChordError(RuntimeError):
 class ChordOpts(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("validate", ctypes.c_int32), ("split_k", ctypes.c_int32),
                 ("out_dtype", ctypes.c_int32), ("epilogue", ctypes.c_int32), ("mixed", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 2)]
+                ("fuse_combine", ctypes.c_int32), ("reserved", ctypes.c_int32 * 1)]
 
 
 _lock = threading.Lock()
@@ -69,6 +70,10 @@ _SIGS = {
     "chord_w4a16_moe_gemm": (_int, [_vp, _i64, _int, _vp, _sz, _int, _int, _int, _vp, _vp, _vp, _i64, _int, _i64,
                                     _vp, _vp, _sz, _OPTS, _vp]),
     "chord_silu_mul": (_int, [_vp, _vp, _i64, _int, _int, _vp, _vp]),
+    "chord_combine_plan": (_int, [_vp, _vp, _int, _int, _int, _vp, _vp]),
+    "chord_w4a16_moe_gemm_combine": (_int, [_vp, _vp, _sz, _int, _int, _int, _vp, _vp, _vp, _i64, _int, _int, _int,
+                                            _vp, _vp, _vp, _vp, _sz, _OPTS, _vp]),
+    "chord_combine_finish": (_int, [_vp, _vp, _vp, _int, _int, _int, _int, _vp, _vp]),
     "chord_moe_combine": (_int, [_vp, _int, _vp, _vp, _int, _int, _int, _int, _vp, _vp]),
     "chord_layer_workspace_bytes": (_sz, [_int, _int, _int, _int, _int, _int]),
     "chord_moe_layer": (_int, [_vp, _vp, _vp, _int, _int, _int, _int, _int, _int, _vp, _sz, _vp, _sz, _int, _vp,
@@ -206,6 +211,28 @@ def chord_w4a16_moe_gemm(A, a_row_divisor: int, packed, E: int, N: int, K: int, 
 def chord_silu_mul(C1, topk_ids, E: int, h, stream=None):
     P, I2 = C1.shape
     _check(load().chord_silu_mul(_p(C1), _p(topk_ids), P, E, I2 // 2, _p(h), _s(stream)), "chord_silu_mul")
+
+
+def chord_combine_plan(topk_ids, topk_w, E: int, pair_w, stream=None):
+    T, topk = topk_ids.shape
+    _check(load().chord_combine_plan(_p(topk_ids), _p(topk_w), T, topk, E, _p(pair_w), _s(stream)),
+           "chord_combine_plan")
+
+
+def chord_w4a16_moe_gemm_combine(A, packed, E: int, N: int, K: int, sorted_ids, expert_ids, num_tokens_padded,
+                                 block_m: int, topk: int, pair_w, C2, out, workspace=None, opts=None, stream=None):
+    T = out.shape[0]
+    _check(load().chord_w4a16_moe_gemm_combine(
+        _p(A), _p(packed), _nbytes(packed), E, N, K, _p(sorted_ids), _p(expert_ids), _p(num_tokens_padded),
+        sorted_ids.numel(), block_m, T, topk, _p(pair_w), _p(C2), _p(out), _p(workspace),
+        0 if workspace is None else _nbytes(workspace), _o(opts), _s(stream)), "chord_w4a16_moe_gemm_combine")
+
+
+def chord_combine_finish(C2, topk_ids, topk_w, E: int, out, stream=None):
+    T, topk = topk_ids.shape
+    H = out.shape[1]
+    _check(load().chord_combine_finish(_p(C2), _p(topk_ids), _p(topk_w), T, topk, E, H, _p(out), _s(stream)),
+           "chord_combine_finish")
 
 
 def chord_moe_combine(C2, topk_ids, topk_w, E: int, out, stream=None):

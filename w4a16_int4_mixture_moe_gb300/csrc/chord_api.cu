@@ -39,8 +39,12 @@ chord_opts opts_or_default(const chord_opts* o) {
 // for short K (few stages per item), where the tcgen05 kernel's fixed cost per
 // item (pipeline fill, accumulator drain) dominates.
 constexpr int kDecodeMaxBlockM = 32;
-// opts.mixed = 0 (automatic) splits tcgen05-regime calls by block size.
-constexpr bool kMixedByDefault = true;
+// opts.mixed = 0 (the library's choice) leaves the per-block split off.  The
+// host cannot see the routing's skew without reading it back, and the split
+// measured faster only where many experts are cold (GB300, 16384 tokens, 48
+// of 384 experts: Zipf(2.0) routing 3606 -> 3373 us per layer; Zipf(1.2),
+// three small blocks, 2359 -> 2427 us; uniform EP8 prefill 1034 -> 1048 us).
+constexpr bool kMixedByDefault = false;
 constexpr int kShortK = 512;
 constexpr int kShortKMaxBlockM = 64;
 
@@ -349,11 +353,21 @@ size_t chord_gemm_workspace_bytes(int64_t num_pairs, int N, int K, int block_m, 
     return gemm_ws_bytes(num_pairs, N, K, block_m, opts_or_default(opts));
 }
 
-chord_status chord_w4a16_moe_gemm(const void* A, int64_t a_rows, int a_row_divisor, const void* packed,
-                                  size_t packed_bytes, int E, int N, int K, const int32_t* sorted_ids,
-                                  const int32_t* expert_ids, const int32_t* num_tokens_padded, int64_t capacity,
-                                  int block_m, int64_t num_pairs, void* C, void* workspace, size_t workspace_bytes,
-                                  const chord_opts* opts, void* stream) {
+}  // extern "C"
+
+namespace {
+// The fused combine's extra operands of a down-projection call (topk = 0: none).
+struct CombineArgs {
+    int topk = 0;
+    const float* pair_w = nullptr;
+    void* out = nullptr;
+};
+
+chord_status moe_gemm(const void* A, int64_t a_rows, int a_row_divisor, const void* packed, size_t packed_bytes,
+                      int E, int N, int K, const int32_t* sorted_ids, const int32_t* expert_ids,
+                      const int32_t* num_tokens_padded, int64_t capacity, int block_m, int64_t num_pairs, void* C,
+                      void* workspace, size_t workspace_bytes, const chord_opts* opts, const CombineArgs& cmb,
+                      void* stream) {
     if (E <= 0 || N <= 0 || K <= 0 || a_rows < 0 || a_row_divisor <= 0 || block_m <= 0 || capacity < 0 ||
         num_pairs < 0)
         return CHORD_ERR_INVALID_ARG;
@@ -400,6 +414,10 @@ chord_status chord_w4a16_moe_gemm(const void* A, int64_t a_rows, int a_row_divis
     g.out_f32 = o.out_dtype == CHORD_DTYPE_F32 ? 1 : 0;
     g.silu = silu ? 1 : 0;
     g.layout = silu ? CHORD_LAYOUT_GATE_UP_INTERLEAVED : CHORD_LAYOUT_TCGEN05;
+    g.combine = cmb.topk > 0 ? 1 : 0;
+    g.topk = cmb.topk;
+    g.pair_w = cmb.pair_w;
+    g.out = static_cast<uint16_t*>(cmb.out);
     g.err = di.err;
     g.ksplit = S;
     g.partial = (S > 1 || tail) ? static_cast<float*>(workspace) : nullptr;
@@ -419,10 +437,61 @@ chord_status chord_w4a16_moe_gemm(const void* A, int64_t a_rows, int a_row_divis
     }
     if (e == cudaSuccess) e = kernel == CHORD_KERNEL_TCGEN05 ? launch_gemm_tc(g, s) : launch_gemm_decode(g, s);
     if (e == cudaSuccess && S > 1)
-        e = launch_splitk_reduce(g.partial, S, num_pairs, g.id_limit, N, sorted_ids, num_tokens_padded, capacity, C,
-                                 g.out_f32, g.silu, s);
+        e = launch_splitk_reduce(g.partial, S, g, s);
     if (e != cudaSuccess) return CHORD_ERR_CUDA;
     return finish(o, s);
+}
+}  // namespace
+
+extern "C" {
+
+chord_status chord_w4a16_moe_gemm(const void* A, int64_t a_rows, int a_row_divisor, const void* packed,
+                                  size_t packed_bytes, int E, int N, int K, const int32_t* sorted_ids,
+                                  const int32_t* expert_ids, const int32_t* num_tokens_padded, int64_t capacity,
+                                  int block_m, int64_t num_pairs, void* C, void* workspace, size_t workspace_bytes,
+                                  const chord_opts* opts, void* stream) {
+    return moe_gemm(A, a_rows, a_row_divisor, packed, packed_bytes, E, N, K, sorted_ids, expert_ids,
+                    num_tokens_padded, capacity, block_m, num_pairs, C, workspace, workspace_bytes, opts,
+                    CombineArgs{}, stream);
+}
+
+chord_status chord_combine_plan(const int32_t* topk_ids, const float* topk_w, int T, int topk, int E, float* pair_w,
+                                void* stream) {
+    if (T < 0 || topk <= 0 || E <= 0) return CHORD_ERR_INVALID_ARG;
+    if (topk > 32) return CHORD_ERR_UNSUPPORTED;
+    if (T > 0 && (!topk_ids || !topk_w || !pair_w)) return CHORD_ERR_INVALID_ARG;
+    return cuda_status(launch_combine_plan(topk_ids, topk_w, T, topk, E, pair_w, static_cast<cudaStream_t>(stream)));
+}
+
+chord_status chord_w4a16_moe_gemm_combine(const void* A, const void* packed, size_t packed_bytes, int E, int N, int K,
+                                          const int32_t* sorted_ids, const int32_t* expert_ids,
+                                          const int32_t* num_tokens_padded, int64_t capacity, int block_m, int T,
+                                          int topk, const float* pair_w, float* C2, void* out, void* workspace,
+                                          size_t workspace_bytes, const chord_opts* opts, void* stream) {
+    if (T < 0 || topk <= 0) return CHORD_ERR_INVALID_ARG;
+    if (topk > 32) return CHORD_ERR_UNSUPPORTED;
+    chord_opts o = opts_or_default(opts);
+    if (o.epilogue != CHORD_EPILOGUE_NONE) return CHORD_ERR_INVALID_ARG;
+    if (T > 0 && (!pair_w || !out || !aligned16(out))) return CHORD_ERR_INVALID_ARG;
+    o.out_dtype = CHORD_DTYPE_F32;
+    const int64_t P = (int64_t)T * topk;
+    CombineArgs cmb;
+    cmb.topk = topk;
+    cmb.pair_w = pair_w;
+    cmb.out = out;
+    return moe_gemm(A, P, 1, packed, packed_bytes, E, N, K, sorted_ids, expert_ids, num_tokens_padded, capacity,
+                    block_m, P, C2, workspace, workspace_bytes, &o, cmb, stream);
+}
+
+chord_status chord_combine_finish(const float* C2, const int32_t* topk_ids, const float* topk_w, int T, int topk,
+                                  int E, int H, void* out, void* stream) {
+    if (T < 0 || topk <= 0 || E <= 0 || H <= 0) return CHORD_ERR_INVALID_ARG;
+    if (topk > 32) return CHORD_ERR_UNSUPPORTED;
+    if (H % 8) return CHORD_ERR_UNSUPPORTED;
+    if (T > 0 && (!C2 || !topk_ids || !topk_w || !out || !aligned16(C2) || !aligned16(out)))
+        return CHORD_ERR_INVALID_ARG;
+    return cuda_status(launch_combine_finish(C2, topk_ids, topk_w, T, topk, E, H, static_cast<uint16_t*>(out),
+                                             static_cast<cudaStream_t>(stream)));
 }
 
 chord_status chord_silu_mul(const void* C1, const int32_t* topk_ids, int64_t P, int E, int I, void* h, void* stream) {
@@ -448,7 +517,7 @@ chord_status chord_moe_combine(const void* C2, int c2_dtype, const int32_t* topk
 
 namespace {
 struct LayerWs {
-    size_t counts, sorted, experts, ntp, c1, h, c2, split, total;
+    size_t counts, sorted, experts, ntp, c1, h, c2, pair_w, split, total;
 };
 
 size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -472,6 +541,8 @@ bool layer_ws(int T, int topk, int E, int H, int I, int block_m, LayerWs* w) {
     off = up256(off + P * (size_t)I * 2);
     w->c2 = off;
     off = up256(off + P * (size_t)H * 4);
+    w->pair_w = off;   // the fused combine's per-pair weights
+    off = up256(off + P * 4);
     // FP32 partial sums of the K-sliced GEMMs (default options), shared by
     // the gate_up and the down projection, which run one after the other
     w->split = off;
@@ -542,11 +613,26 @@ chord_status chord_moe_layer(const void* x, const int32_t* topk_ids, const float
     chord_opts o_down = o;
     o_down.out_dtype = CHORD_DTYPE_F32;
     o_down.epilogue = CHORD_EPILOGUE_NONE;
-    st = chord_w4a16_moe_gemm(h, P, 1, packed_w2, w2_bytes, E, H, I, sorted, experts, ntp, cap, block_m, P, c2,
-                              split, split_len, &o_down, stream);
-    if (st != CHORD_OK) return st;
-    st = chord_moe_combine(c2, CHORD_DTYPE_F32, topk_ids, topk_w, T, topk, E, H, out, stream);
-    if (st != CHORD_OK) return st;
+    if (o.fuse_combine < -1 || o.fuse_combine > 1) return CHORD_ERR_INVALID_ARG;
+    if (o.fuse_combine > 0 && topk <= 32) {
+        // top-k combine fused into the down GEMM: tokens with one local pair are
+        // written by its epilogue, the others summed by the finishing pass
+        float* pair_w = reinterpret_cast<float*>(ws + w.pair_w);
+        st = chord_combine_plan(topk_ids, topk_w, T, topk, E, pair_w, stream);
+        if (st != CHORD_OK) return st;
+        st = chord_w4a16_moe_gemm_combine(h, packed_w2, w2_bytes, E, H, I, sorted, experts, ntp, cap, block_m, T,
+                                          topk, pair_w, static_cast<float*>(c2), out, split, split_len, &o_down,
+                                          stream);
+        if (st != CHORD_OK) return st;
+        st = chord_combine_finish(static_cast<const float*>(c2), topk_ids, topk_w, T, topk, E, H, out, stream);
+        if (st != CHORD_OK) return st;
+    } else {
+        st = chord_w4a16_moe_gemm(h, P, 1, packed_w2, w2_bytes, E, H, I, sorted, experts, ntp, cap, block_m, P, c2,
+                                  split, split_len, &o_down, stream);
+        if (st != CHORD_OK) return st;
+        st = chord_moe_combine(c2, CHORD_DTYPE_F32, topk_ids, topk_w, T, topk, E, H, out, stream);
+        if (st != CHORD_OK) return st;
+    }
     o.validate = validate;
     return finish(o, static_cast<cudaStream_t>(stream));
 }

@@ -499,22 +499,22 @@ __device__ __forceinline__ float4 add4(float4 a, float4 b) {
 }
 
 template <bool kSilu>
-__global__ void splitk_reduce_kernel(const float* __restrict__ partial, int S, int64_t num_pairs, int64_t id_limit,
-                                     int N, const int32_t* __restrict__ sorted_ids, const int32_t* __restrict__ ntp,
-                                     int64_t capacity, void* __restrict__ C, int out_f32) {
+__global__ void splitk_reduce_kernel(const float* __restrict__ partial, int S, const GemmArgs a) {
     pdl_trigger();
     pdl_wait();
     constexpr int kBatch = 8;
+    const int N = a.N;
     const int out_cols = kSilu ? N / 2 : N;
     const int vpr = out_cols / 4;
-    int64_t slots = *ntp;
-    slots = slots < 0 ? 0 : (slots > capacity ? capacity : slots);
+    int64_t slots = *a.ntp;
+    slots = slots < 0 ? 0 : (slots > a.capacity ? a.capacity : slots);
     const int64_t nvec = slots * vpr;
-    const int64_t slice_stride = num_pairs * (int64_t)N / 4;   // in float4
+    const int64_t slice_stride = a.num_pairs * (int64_t)N / 4;   // in float4
+    void* __restrict__ C = a.C;
     for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nvec; v += (int64_t)gridDim.x * blockDim.x) {
         int jv;
-        const int32_t p = __ldg(sorted_ids + divmod_idx(v, vpr, jv));
-        if (p < 0 || (int64_t)p >= id_limit) continue;
+        const int32_t p = __ldg(a.sorted_ids + divmod_idx(v, vpr, jv));
+        if (p < 0 || (int64_t)p >= a.id_limit) continue;
         const int j0 = jv * 4;
         // packed column of output column j0 (gate; up is 8 further)
         const int c0 = kSilu ? 16 * (j0 / 8) + j0 % 8 : j0;
@@ -542,7 +542,15 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ partial, int S, i
                                   silu_mul_bf16(g.w, u.w)};
             *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(C) + (int64_t)p * out_cols + j0) =
                 *reinterpret_cast<const uint2*>(o);
-        } else if (out_f32) {
+        } else if (a.combine) {
+            const float w = __ldg(a.pair_w + p);
+            const int64_t tok = p / a.topk;
+            float* C2 = static_cast<float*>(C);
+            combine_store(C2, a.out, N, p, tok, w, j0, g.x);
+            combine_store(C2, a.out, N, p, tok, w, j0 + 1, g.y);
+            combine_store(C2, a.out, N, p, tok, w, j0 + 2, g.z);
+            combine_store(C2, a.out, N, p, tok, w, j0 + 3, g.w);
+        } else if (a.out_f32) {
             *reinterpret_cast<float4*>(static_cast<float*>(C) + (int64_t)p * out_cols + j0) = g;
         } else {
             uint2 o;
@@ -663,6 +671,9 @@ __global__ void tc_tail_reduce_kernel(const GemmArgs a, int64_t G, int kstages, 
         if (kSilu) {
             const int h_col = nt * 64 + 8 * (r / 16) + r % 8;
             static_cast<__nv_bfloat16*>(a.C)[(int64_t)id * (a.N / 2) + h_col] = silu_mul_bf16(g, u);
+        } else if (a.combine) {
+            combine_store(static_cast<float*>(a.C), a.out, a.N, id, id / a.topk, __ldg(a.pair_w + id), nt * 128 + r,
+                          g);
         } else if (a.out_f32) {
             static_cast<float*>(a.C)[(int64_t)id * a.N + nt * 128 + r] = g;
         } else {
@@ -684,18 +695,15 @@ cudaError_t launch_tc_tail_reduce(const GemmArgs& a, int64_t grid, int kstages, 
                       dim3(threads), 0, stream, a, grid, kstages, min_stages, tok_tile);
 }
 
-cudaError_t launch_splitk_reduce(const float* partial, int S, int64_t num_pairs, int64_t id_limit, int N,
-                                 const int32_t* sorted_ids, const int32_t* ntp, int64_t capacity, void* C, int out_f32,
-                                 int silu, cudaStream_t stream) {
-    const int64_t nvec = capacity * ((silu ? N / 2 : N) / 4);
+cudaError_t launch_splitk_reduce(const float* partial, int S, const GemmArgs& a, cudaStream_t stream) {
+    const int64_t nvec = a.capacity * ((a.silu ? a.N / 2 : a.N) / 4);
     if (nvec == 0) return cudaSuccess;
     const int threads = 128;
     int64_t blocks = ceil_div64(nvec, threads);
     const int64_t cap = (int64_t)device_info().sm_count * 16;
     if (blocks > cap) blocks = cap;
-    return launch_pdl(pdl_for(num_pairs), silu ? splitk_reduce_kernel<true> : splitk_reduce_kernel<false>, dim3((unsigned)blocks),
-                      dim3(threads), 0, stream, partial, S, num_pairs, id_limit, N, sorted_ids, ntp, capacity, C,
-                      out_f32);
+    return launch_pdl(pdl_for(a.num_pairs), a.silu ? splitk_reduce_kernel<true> : splitk_reduce_kernel<false>,
+                      dim3((unsigned)blocks), dim3(threads), 0, stream, partial, S, a);
 }
 
 cudaError_t launch_silu_mul(const uint16_t* C1, const int32_t* topk_ids, int64_t P, int E, int I, uint16_t* h,
@@ -823,6 +831,103 @@ cudaError_t launch_combine(const void* C2, bool c2_f32, const int32_t* topk_ids,
                     : (c2_f32 ? combine_kernel<true> : combine_kernel<false>);
     return launch_pdl(pdl_for((int64_t)T * topk), kern, dim3((unsigned)blocks), dim3(threads), 0, stream, C2, topk_ids,
                       topk_w, T, topk, E, H, out);
+}
+
+// ============================================================================
+// Fused top-k combine.  The down GEMM writes the output of a token whose only
+// local pair it computes directly (bf16(0 + w * sum), what the combine would
+// compute for one pair); the plan below tells it which pairs those are, and
+// the finishing pass sums the tokens with several local pairs exactly as the
+// combine does (FP32 from +0 over local k in ascending order, each product and
+// sum rounded separately) and writes +0 for tokens with none.
+// ============================================================================
+
+// pair_w[p] = topk_w[p] for the local pair of a token with exactly one local
+// pair; NaN for the local pairs of tokens with several.  One thread per token.
+__global__ void combine_plan_kernel(const int32_t* __restrict__ ids, const float* __restrict__ w, int T, int topk,
+                                    int E, float* __restrict__ pair_w) {
+    pdl_trigger();
+    pdl_wait();
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < T; t += (int64_t)gridDim.x * blockDim.x) {
+        int cnt = 0;
+        for (int k = 0; k < topk; ++k) {
+            const int e = __ldg(ids + t * topk + k);
+            cnt += (e >= 0 && e < E) ? 1 : 0;
+        }
+        for (int k = 0; k < topk; ++k) {
+            const int64_t p = t * topk + k;
+            const int e = __ldg(ids + p);
+            if (e >= 0 && e < E) pair_w[p] = cnt == 1 ? __ldg(w + p) : __int_as_float(0x7fc00000);
+        }
+    }
+}
+
+// One warp per token (topk <= 32): its local pairs from a ballot; a token with
+// one local pair of finite weight was written by the GEMM; otherwise 8 columns
+// per lane, the local pairs' FP32 rows added in ascending k.
+__global__ void combine_finish_kernel(const float* __restrict__ C2, const int32_t* __restrict__ ids,
+                                      const float* __restrict__ w, int T, int topk, int E, int H,
+                                      uint16_t* __restrict__ out) {
+    pdl_trigger();
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps) {
+        int e = -1;
+        float wk = 0.0f;
+        if (lane < topk) {
+            e = __ldg(ids + t * topk + lane);
+            wk = __ldg(w + t * topk + lane);
+        }
+        const uint32_t mask = __ballot_sync(0xffffffffu, e >= 0 && e < E);
+        if (__popc(mask) == 1) {
+            const float w1 = __shfl_sync(0xffffffffu, wk, __ffs(mask) - 1);
+            if (w1 == w1) continue;   // written by the down GEMM's epilogue
+        }
+        for (int n = lane * 8; n < H; n += 256) {
+            float acc[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+            for (uint32_t m = mask; m; m &= m - 1) {
+                const int k = __ffs(m) - 1;
+                const int64_t p = t * topk + k;
+                const float wv = __ldg(w + p);
+                const float4 c0 = __ldcg(reinterpret_cast<const float4*>(C2 + p * H + n));
+                const float4 c1 = __ldcg(reinterpret_cast<const float4*>(C2 + p * H + n + 4));
+                const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], __fmul_rn(wv, c[i]));
+            }
+            uint4 o;
+            o.x = pack_bf16x2(acc[0], acc[1]);
+            o.y = pack_bf16x2(acc[2], acc[3]);
+            o.z = pack_bf16x2(acc[4], acc[5]);
+            o.w = pack_bf16x2(acc[6], acc[7]);
+            *reinterpret_cast<uint4*>(out + t * H + n) = o;
+        }
+    }
+}
+
+cudaError_t launch_combine_plan(const int32_t* topk_ids, const float* topk_w, int T, int topk, int E, float* pair_w,
+                                cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    const int threads = 256;
+    int64_t blocks = ceil_div64(T, threads);
+    const int64_t cap = (int64_t)device_info().sm_count * 4;
+    if (blocks > cap) blocks = cap;
+    return launch_pdl(pdl_for((int64_t)T * topk), combine_plan_kernel, dim3((unsigned)blocks), dim3(threads), 0,
+                      stream, topk_ids, topk_w, T, topk, E, pair_w);
+}
+
+cudaError_t launch_combine_finish(const float* C2, const int32_t* topk_ids, const float* topk_w, int T, int topk,
+                                  int E, int H, uint16_t* out, cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    const int threads = 256;   // 8 tokens per block and round
+    int64_t blocks = ceil_div64(T, threads / 32);
+    const int64_t cap = (int64_t)device_info().sm_count * 8;
+    if (blocks > cap) blocks = cap;
+    return launch_pdl(pdl_for((int64_t)T * topk), combine_finish_kernel, dim3((unsigned)blocks), dim3(threads), 0,
+                      stream, C2, topk_ids, topk_w, T, topk, E, H, out);
 }
 
 }  // namespace chord

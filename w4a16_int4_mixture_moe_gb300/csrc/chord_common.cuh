@@ -349,4 +349,19 @@ __device__ __forceinline__ __nv_bfloat16 silu_mul_bf16(float g_sum, float u_sum)
     return __float2bfloat16_rn(silu_times(g, u));
 }
 
+// The fused combine's write for one FP32 result `v` of pair p, column n:
+// when p is its token's only local pair (pair_w[p] a number) the token's
+// output is the weighted sum over that one pair, bf16(0 + w * v) with the
+// product and the sum rounded separately as in the combine pass; otherwise
+// the FP32 value goes to C2 for the finishing sum.  Returns nothing.
+__device__ __forceinline__ void combine_store(float* C2, uint16_t* out, int64_t N, int64_t p, int64_t t, float w,
+                                              int n, float v) {
+    if (w == w) {
+        const float o = __fadd_rn(0.0f, __fmul_rn(w, v));
+        out[t * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+    } else {
+        C2[p * N + n] = v;
+    }
+}
+
 }  // namespace chord

@@ -185,8 +185,12 @@ __device__ __forceinline__ bool consume_item(const GemmArgs& a, uint8_t* smem, u
 #pragma unroll
     for (int t = 0; t < NV; ++t) {
         int32_t p[2];
+        float pw[2] = {0.0f, 0.0f};   // fused combine: the pair's weight when it is its token's only local pair
 #pragma unroll
-        for (int u = 0; u < 2; ++u) p[u] = __shfl_sync(0xffffffffu, my_id, 8 * t + 2 * c + u);
+        for (int u = 0; u < 2; ++u) {
+            p[u] = __shfl_sync(0xffffffffu, my_id, 8 * t + 2 * c + u);
+            if (a.combine && a.ksplit <= 1 && p[u] >= 0) pw[u] = a.pair_w[p[u]];
+        }
 #pragma unroll
         for (int mi = 0; mi < MI; ++mi) {
             const int n0 = nt * kBN + (warp * MI + mi) * 16 + g;
@@ -203,6 +207,10 @@ __device__ __forceinline__ bool consume_item(const GemmArgs& a, uint8_t* smem, u
                     // column j = 8k + g (layout 3)
                     __nv_bfloat16* hrow = static_cast<__nv_bfloat16*>(a.C) + (int64_t)p[u] * (a.N / 2);
                     hrow[8 * (n0 / 16) + g] = silu_mul_bf16(acc[mi][t][u], acc[mi][t][2 + u]);
+                } else if (a.combine) {
+                    const int64_t tok = p[u] / a.topk;
+                    combine_store(static_cast<float*>(a.C), a.out, a.N, p[u], tok, pw[u], n0, acc[mi][t][u]);
+                    combine_store(static_cast<float*>(a.C), a.out, a.N, p[u], tok, pw[u], n0 + 8, acc[mi][t][2 + u]);
                 } else if (a.out_f32) {
                     float* crow = static_cast<float*>(a.C) + (int64_t)p[u] * a.N;
                     crow[n0] = acc[mi][t][u];

@@ -537,6 +537,8 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
             // Pair ids first, before the accumulator is ready: lane l holds the
             // id of token wg*16 + 32*(2k + l/16) + l%16 in pre[k].
             int32_t pre[4];
+            float prew[4];    // fused combine: the pair's weight (a number: its token's only local pair)
+            int32_t pret[4];  // fused combine: the pair's token
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int j = wg * 16 + 32 * (2 * k + (lane >> 4)) + (lane & 15);
@@ -546,6 +548,12 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
                     if (!row_valid(a, id)) id = -1;
                 }
                 pre[k] = id;
+                prew[k] = 0.0f;
+                pret[k] = 0;
+                if (a.combine && id >= 0) {
+                    prew[k] = a.pair_w[id];
+                    pret[k] = id / a.topk;
+                }
             }
             if (!wait_or_abort(acc_full, (uint32_t)(nitem & 1), &flags[1], a.err)) {
                 ok = false;
@@ -604,6 +612,12 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
                     }
                     const int32_t id = __shfl_sync(0xffffffffu, pre[it >> 1], u + 16 * (it & 1));
                     const float val = __uint_as_float(v[u]);
+                    if (a.combine) {
+                        const float w = __shfl_sync(0xffffffffu, prew[it >> 1], u + 16 * (it & 1));
+                        const int32_t tok = __shfl_sync(0xffffffffu, pret[it >> 1], u + 16 * (it & 1));
+                        if (id >= 0) combine_store(static_cast<float*>(a.C), a.out, a.N, id, tok, w, n_out, val);
+                        continue;
+                    }
                     if (id < 0) continue;
                     if (a.out_f32)
                         static_cast<float*>(a.C)[(int64_t)id * a.N + n_out] = val;

@@ -41,14 +41,17 @@ cudaError_t launch_grouped_contiguous_index(const int32_t* m_indices, int64_t M,
 cudaError_t launch_grouped_masked_index(const int32_t* masked_m, int G, int max_m, int block_m, int32_t* sorted_ids,
                                         int32_t* expert_ids, int32_t* ntp, int64_t capacity, int* err,
                                         cudaStream_t stream);
-cudaError_t launch_splitk_reduce(const float* partial, int S, int64_t num_pairs, int64_t id_limit, int N,
-                                 const int32_t* sorted_ids, const int32_t* ntp, int64_t capacity, void* C, int out_f32,
-                                 int silu, cudaStream_t stream);
 cudaError_t launch_wait_timeout_selftest(int* err, cudaStream_t stream);
 cudaError_t launch_silu_mul(const uint16_t* C1, const int32_t* topk_ids, int64_t P, int E, int I, uint16_t* h,
                             cudaStream_t stream);
 cudaError_t launch_combine(const void* C2, bool c2_f32, const int32_t* topk_ids, const float* topk_w, int T,
                            int topk, int E, int H, uint16_t* out, cudaStream_t stream);
+// Fused combine: the per-pair plan before the down GEMM, and the weighted sum of
+// the tokens with several local pairs (plus the +0 rows of tokens with none) after it.
+cudaError_t launch_combine_plan(const int32_t* topk_ids, const float* topk_w, int T, int topk, int E, float* pair_w,
+                                cudaStream_t stream);
+cudaError_t launch_combine_finish(const float* C2, const int32_t* topk_ids, const float* topk_w, int T, int topk,
+                                  int E, int H, uint16_t* out, cudaStream_t stream);
 
 // ---- GEMMs ---------------------------------------------------------------
 // GemmArgs::block_filter.  The valid rows of an align block are a prefix of
@@ -82,8 +85,21 @@ struct GemmArgs {
     int tail_split;    // tcgen05: cut the last partial wave's items into K slices (needs `partial`)
     int block_filter;  // kBlocksAll, or (mixed regime) only blocks with at most / more than
                        // CHORD_MIXED_SMALL_ROWS valid rows
+    // Fused top-k combine (FP32 output only): a pair whose pair_w entry is a
+    // number is its token's only local pair, and its weighted result
+    // bf16(0 + w * sum) goes to out[pair / topk, n] instead of C; the others
+    // (NaN) write their FP32 sums to C for chord_combine_finish.
+    int combine;
+    int topk;
+    const float* pair_w;
+    uint16_t* out;
     int* err;
 };
+
+// Split-K reduction of the warp-level kernel: adds the S slices of partial
+// [S, num_pairs, N] in slice order and applies the GEMM's epilogue (bf16,
+// FP32, SiLU * up or the fused combine) for every valid row.
+cudaError_t launch_splitk_reduce(const float* partial, int S, const GemmArgs& a, cudaStream_t stream);
 
 // Warp-MMA kernel (decode regime, packed layout 2): tokens of a block in the N
 // dimension of mma.sync m16n8k16, INT4 streamed through a bulk-copy pipeline.
