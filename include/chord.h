@@ -134,7 +134,12 @@ typedef struct chord_opts {
                              choice, measured faster on GB300) or -1 = the separate
                              chord_moe_combine pass.  The result is the same bit for
                              bit. */
-    int32_t reserved[1]; /* must be zero */
+    int32_t tc_pairs;    /* tcgen05 kernel: 1 = clusters of two CTAs on neighbouring SMs
+                            computing M = 256 items with tcgen05 cta_group::2 (each CTA
+                            dequantises its 128 weight rows into its own tensor memory and
+                            gathers half of the block's tokens; N % 256 == 0, no split
+                            tail); 0 (the library's choice) or -1 = one CTA per item.
+                            Same results up to FP32 summation order. */
 } chord_opts;
 
 /* Blocks with at most this many valid rows count as small for opts.mixed. */

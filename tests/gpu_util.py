@@ -167,14 +167,15 @@ def align(ids, E, bm, opts=None):
 
 
 def gemm(A_bits, div, packed, E, N, K, s, e, n, bm, P, kernel=0, C=None, split_k=None, epilogue=0,
-         out_dtype=0, mixed=0):
+         out_dtype=0, mixed=0, tc_pairs=0):
     """C rows that no block names keep the fill pattern 0xFFFF (a NaN).
     split_k=None passes no workspace (the GEMM runs unsplit); otherwise the
     option is set and the workspace sized by chord_gemm_workspace_bytes."""
     A = A_bits if isinstance(A_bits, torch.Tensor) else dbf(A_bits)
     if C is None:
         C = torch.full((max(P, 1), N), -1, dtype=torch.int16, device=DEV)[:P].view(torch.bfloat16)
-    opts = chord.ChordOpts(kernel=kernel, split_k=split_k or 0, epilogue=epilogue, out_dtype=out_dtype, mixed=mixed)
+    opts = chord.ChordOpts(kernel=kernel, split_k=split_k or 0, epilogue=epilogue, out_dtype=out_dtype, mixed=mixed,
+                           tc_pairs=tc_pairs)
     ws = None
     if split_k is not None:
         nb = chord.chord_gemm_workspace_bytes(P, N, K, bm, opts)

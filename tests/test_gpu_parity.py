@@ -1083,3 +1083,81 @@ def test_fused_combine_rejects_bad_arguments():
     with pytest.raises(chord.ChordError) as ei:
         chord.chord_combine_finish(C2, ids, w, 2, out)
     assert ei.value.status == 2
+
+
+# ------------------------------------------------- tcgen05 in clusters of two CTAs
+
+@pytest.mark.parametrize("bm,K,exact", [(256, 1024, True), (256, 320, True), (128, 640, True), (64, 2048, True),
+                                        (256, 1024, False), (128, 512, False), (24, 256, True)])
+def test_tc_pairs_vs_oracle(bm, K, exact):
+    """opts.tc_pairs = 1 (cta_group::2: a cluster of two CTAs per 256-row item,
+    each CTA's 128 dequantised rows in its own tensor memory, each gathering half
+    of the block's tokens): bit-exact with the oracle in the exact-integer
+    regime, within tolerance on random data, bf16 and FP32 outputs, the fused
+    SiLU * up and the mixed regime; one, two and four MMA issuers (blocks of up
+    to 256, 128 and 64 rows); a ragged last K stage."""
+    T, topk, E, N = 100, 8, 8, 1024
+    x, codes, scales, ids = tail_case(bm, K, 11 + bm + K, exact, N=N)
+    P = T * topk
+    packed = pack(codes, scales)
+    s, e, n = align(ids, E, bm)
+    s2, e2, n2 = oracle.moe_align(ids, E, bm)
+    rows = valid_rows(ids, E)
+    other = np.setdiff1d(np.arange(P), rows)
+    ref = oracle.moe_gemm(x, topk, codes, scales, s2, e2, n2, bm, P, C=np.full((P, N), 0xFFFF, np.uint16))
+    for mixed in (0, 1):
+        got = host_bits(gemm(x, topk, packed, E, N, K, s, e, n, bm, P, kernel=TC, split_k=0, mixed=mixed,
+                             tc_pairs=1))
+        assert (got[other] == 0xFFFF).all(), "rows of non-local pairs were written"
+        if exact:
+            np.testing.assert_array_equal(got[rows], ref[rows])
+        else:
+            assert_close(got[rows], ref[rows], f"pairs bm={bm} K={K} mixed={mixed}")
+    C = torch.full((P, N), float("nan"), dtype=torch.float32, device=DEV)
+    gemm(x, topk, packed, E, N, K, s, e, n, bm, P, kernel=TC, C=C, split_k=0, out_dtype=chord.DTYPE_F32, tc_pairs=1)
+    got32 = C.cpu().numpy()
+    ref32 = oracle.moe_gemm_f32(x, topk, codes, scales, s2, e2, n2, bm, P)
+    if exact:
+        np.testing.assert_array_equal(got32[rows], ref32[rows])
+    else:
+        err = np.abs(got32[rows].astype(np.float64) - ref32[rows])
+        assert (err <= 1e-2 + 1e-2 * np.abs(ref32[rows])).all(), err.max()
+    # the fused SiLU * up epilogue (layout 3), against this library's SiLU * up of the pairs' C1
+    I = N // 2
+    h = torch.full((P, I), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+    gemm(x, topk, pack(codes, scales, chord.LAYOUT_GATE_UP_INTERLEAVED), E, N, K, s, e, n, bm, P, kernel=TC, C=h,
+         split_k=0, epilogue=chord.EPILOGUE_SILU_MUL, tc_pairs=1)
+    C1 = gemm(x, topk, packed, E, N, K, s, e, n, bm, P, kernel=TC, split_k=0, tc_pairs=1)
+    check_h_from_gpu_c1(host_bits(h), host_bits(C1), ref, ids.ravel(), E, rows, f"pairs fused bm={bm}")
+    if exact:
+        h2 = torch.full((P, I), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+        chord.chord_silu_mul(C1, dev(ids.ravel().copy()), E, h2)
+        np.testing.assert_array_equal(host_bits(h)[rows], host_bits(h2)[rows])
+    assert chord.chord_get_device_error() == 0
+
+
+def test_layer_tc_pairs_and_fused_combine():
+    """A layer on the tcgen05 kernel in clusters of two CTAs, with the top-k
+    combine fused into the down GEMM, checked through the chain of definitions
+    against the oracle (its ABI steps with the same options give the same
+    output bit for bit)."""
+    T, topk, E, H, I, bm = 100, 8, 8, 1024, 1280, 256
+    ids = wl.random_ids(40, T, topk, E, p_nonlocal=0.1)
+    wts = wl.random_weights(41, T, topk)
+    x = wl.random_bf16(42, (T, H))
+    c13, s13 = wl.random_codes(43, (E, 2 * I, H)), wl.random_scales(44, (E, 2 * I, H // 32))
+    c2, s2 = wl.random_codes(45, (E, H, I)), wl.random_scales(46, (E, H, I // 32))
+    p13, p2 = pack(c13, s13), pack(c2, s2)
+    out, _ = layer(x, ids, wts, E, E, I, p13, p2, bm=bm,
+                   opts=chord.ChordOpts(kernel=TC, tc_pairs=1, fuse_combine=1))
+    sep, _ = layer(x, ids, wts, E, E, I, p13, p2, bm=bm, opts=chord.ChordOpts(kernel=TC, tc_pairs=1))
+    np.testing.assert_array_equal(host_bits(out), host_bits(sep))
+    s, e, n = align(ids, E, bm)
+    P = T * topk
+    C1 = gemm(x, topk, p13, E, 2 * I, H, s, e, n, bm, P, kernel=TC, tc_pairs=1)
+    h = torch.full((P, I), -1, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+    chord.chord_silu_mul(C1, dev(ids), E, h)
+    C2 = torch.full((P, H), float("nan"), dtype=torch.float32, device=DEV)
+    gemm(h, 1, p2, E, H, I, s, e, n, bm, P, kernel=TC, C=C2, out_dtype=chord.DTYPE_F32, tc_pairs=1)
+    check_layer_chain(x, ids, wts, (c13, s13), (c2, s2), E, host_bits(C1), host_bits(h), C2.cpu().numpy(),
+                      host_bits(out), "layer on CTA pairs")

@@ -45,7 +45,7 @@ class ChordError(RuntimeError):
 class ChordOpts(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("validate", ctypes.c_int32), ("split_k", ctypes.c_int32),
                 ("out_dtype", ctypes.c_int32), ("epilogue", ctypes.c_int32), ("mixed", ctypes.c_int32),
-                ("fuse_combine", ctypes.c_int32), ("reserved", ctypes.c_int32 * 1)]
+                ("fuse_combine", ctypes.c_int32), ("tc_pairs", ctypes.c_int32)]
 
 
 _lock = threading.Lock()

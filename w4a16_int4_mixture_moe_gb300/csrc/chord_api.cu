@@ -326,8 +326,9 @@ GemmPlan plan_gemm(int64_t num_pairs, int N, int K, int block_m, bool ws_ok, siz
         }
         p.S = 1;
     }
-    // tcgen05: the split tail, when the workspace holds its partial sums
-    if (p.kernel == CHORD_KERNEL_TCGEN05 && o.split_k != 1) {
+    // tcgen05: the split tail, when the workspace holds its partial sums (one CTA per item only)
+    const bool pairs = o.tc_pairs > 0 && N % 256 == 0;
+    if (p.kernel == CHORD_KERNEL_TCGEN05 && o.split_k != 1 && !pairs) {
         const size_t need = tc_tail_bytes(block_m);
         if (ws_ok && workspace_bytes >= need)
             p.tail = true;
@@ -387,7 +388,7 @@ chord_status moe_gemm(const void* A, int64_t a_rows, int a_row_divisor, const vo
     const bool silu = o.epilogue == CHORD_EPILOGUE_SILU_MUL;
     if (silu && o.out_dtype != CHORD_DTYPE_BF16) return CHORD_ERR_INVALID_ARG;
     if (o.split_k < 0) return CHORD_ERR_INVALID_ARG;
-    if (o.mixed < -1 || o.mixed > 1) return CHORD_ERR_INVALID_ARG;
+    if (o.mixed < -1 || o.mixed > 1 || o.tc_pairs < -1 || o.tc_pairs > 1) return CHORD_ERR_INVALID_ARG;
     const GemmPlan plan = plan_gemm(num_pairs, N, K, block_m, workspace && aligned16(workspace), workspace_bytes, o);
     if (plan.status != CHORD_OK) return plan.status;
     const int S = plan.S;
@@ -414,6 +415,7 @@ chord_status moe_gemm(const void* A, int64_t a_rows, int a_row_divisor, const vo
     g.out_f32 = o.out_dtype == CHORD_DTYPE_F32 ? 1 : 0;
     g.silu = silu ? 1 : 0;
     g.layout = silu ? CHORD_LAYOUT_GATE_UP_INTERLEAVED : CHORD_LAYOUT_TCGEN05;
+    g.tc_pairs = o.tc_pairs > 0 ? 1 : 0;
     g.combine = cmb.topk > 0 ? 1 : 0;
     g.topk = cmb.topk;
     g.pair_w = cmb.pair_w;

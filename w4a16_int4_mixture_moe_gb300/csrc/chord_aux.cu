@@ -862,49 +862,49 @@ __global__ void combine_plan_kernel(const int32_t* __restrict__ ids, const float
     }
 }
 
-// One warp per token (topk <= 32): its local pairs from a ballot; a token with
-// one local pair of finite weight was written by the GEMM; otherwise 8 columns
-// per lane, the local pairs' FP32 rows added in ascending k.
+// One thread per (token, 8 columns), as in the combine pass (one warp per
+// token walked its columns serially and was latency-bound): a token with one
+// local pair of finite weight was written by the GEMM and is skipped;
+// otherwise its local pairs' FP32 rows are added in ascending k (+0 when it
+// has none).  topk <= 32.
 __global__ void combine_finish_kernel(const float* __restrict__ C2, const int32_t* __restrict__ ids,
                                       const float* __restrict__ w, int T, int topk, int E, int H,
                                       uint16_t* __restrict__ out) {
     pdl_trigger();
     pdl_wait();
-    const int lane = threadIdx.x & 31;
-    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nwarps) {
-        int e = -1;
-        float wk = 0.0f;
-        if (lane < topk) {
-            e = __ldg(ids + t * topk + lane);
-            wk = __ldg(w + t * topk + lane);
+    const int vpr = H / 8;
+    const int64_t nvec = (int64_t)T * vpr;
+    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nvec; v += (int64_t)gridDim.x * blockDim.x) {
+        int nv;
+        const int64_t t = divmod_idx(v, vpr, nv);
+        const int n = nv * 8;
+        uint32_t mask = 0;
+        for (int k = 0; k < topk; ++k) {
+            const int e = __ldg(ids + t * topk + k);
+            if (e >= 0 && e < E) mask |= 1u << k;
         }
-        const uint32_t mask = __ballot_sync(0xffffffffu, e >= 0 && e < E);
         if (__popc(mask) == 1) {
-            const float w1 = __shfl_sync(0xffffffffu, wk, __ffs(mask) - 1);
+            const float w1 = __ldg(w + t * topk + (__ffs(mask) - 1));
             if (w1 == w1) continue;   // written by the down GEMM's epilogue
         }
-        for (int n = lane * 8; n < H; n += 256) {
-            float acc[8];
+        float acc[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-            for (uint32_t m = mask; m; m &= m - 1) {
-                const int k = __ffs(m) - 1;
-                const int64_t p = t * topk + k;
-                const float wv = __ldg(w + p);
-                const float4 c0 = __ldcg(reinterpret_cast<const float4*>(C2 + p * H + n));
-                const float4 c1 = __ldcg(reinterpret_cast<const float4*>(C2 + p * H + n + 4));
-                const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+        for (uint32_t m = mask; m; m &= m - 1) {
+            const int64_t p = t * topk + (__ffs(m) - 1);
+            const float wv = __ldg(w + p);
+            const float4 c0 = __ldcg(reinterpret_cast<const float4*>(C2 + p * H + n));
+            const float4 c1 = __ldcg(reinterpret_cast<const float4*>(C2 + p * H + n + 4));
+            const float c[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
-                for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], __fmul_rn(wv, c[i]));
-            }
-            uint4 o;
-            o.x = pack_bf16x2(acc[0], acc[1]);
-            o.y = pack_bf16x2(acc[2], acc[3]);
-            o.z = pack_bf16x2(acc[4], acc[5]);
-            o.w = pack_bf16x2(acc[6], acc[7]);
-            *reinterpret_cast<uint4*>(out + t * H + n) = o;
+            for (int i = 0; i < 8; ++i) acc[i] = __fadd_rn(acc[i], __fmul_rn(wv, c[i]));
         }
+        uint4 o;
+        o.x = pack_bf16x2(acc[0], acc[1]);
+        o.y = pack_bf16x2(acc[2], acc[3]);
+        o.z = pack_bf16x2(acc[4], acc[5]);
+        o.w = pack_bf16x2(acc[6], acc[7]);
+        *reinterpret_cast<uint4*>(out + t * H + n) = o;
     }
 }
 
@@ -921,9 +921,9 @@ cudaError_t launch_combine_plan(const int32_t* topk_ids, const float* topk_w, in
 
 cudaError_t launch_combine_finish(const float* C2, const int32_t* topk_ids, const float* topk_w, int T, int topk,
                                   int E, int H, uint16_t* out, cudaStream_t stream) {
-    if (T == 0) return cudaSuccess;
-    const int threads = 256;   // 8 tokens per block and round
-    int64_t blocks = ceil_div64(T, threads / 32);
+    if ((int64_t)T * H == 0) return cudaSuccess;
+    const int threads = 256;
+    int64_t blocks = ceil_div64((int64_t)T * (H / 8), threads);
     const int64_t cap = (int64_t)device_info().sm_count * 8;
     if (blocks > cap) blocks = cap;
     return launch_pdl(pdl_for((int64_t)T * topk), combine_finish_kernel, dim3((unsigned)blocks), dim3(threads), 0,

@@ -27,6 +27,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "chord_common.cuh"
 #include "chord_internal.h"
 
@@ -125,6 +127,90 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
 
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// ---- pairs of CTAs (cta_group::2) ------------------------------------------
+// With PAIR, a cluster of two CTAs on neighbouring SMs computes one
+// M = 256 product: every tcgen05 instruction of the kernel then names
+// cta_group::2 (alloc, relinquish and dealloc by the producer warp of both
+// CTAs; MMAs and their commits by the leader CTA's issuing thread, the commits
+// arriving on the same barrier of both CTAs).
+template <bool PAIR>
+__device__ __forceinline__ void tmem_alloc_g(uint32_t* slot, uint32_t ncols) {
+    if constexpr (PAIR)
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+                     "r"(ncols)
+                     : "memory");
+    else
+        tmem_alloc(slot, ncols);
+}
+template <bool PAIR>
+__device__ __forceinline__ void tmem_relinquish_g() {
+    if constexpr (PAIR)
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    else
+        tmem_relinquish();
+}
+template <bool PAIR>
+__device__ __forceinline__ void tmem_dealloc_g(uint32_t taddr, uint32_t ncols) {
+    if constexpr (PAIR)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+    else
+        tmem_dealloc(taddr, ncols);
+}
+// Arrive on `bar` (the same barrier of both CTAs of a pair) once this
+// thread's MMAs so far have completed.
+template <bool PAIR>
+__device__ __forceinline__ void tc_commit_g(uint64_t* bar) {
+    if constexpr (PAIR)
+        asm volatile(
+            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                smem_u32(bar)),
+            "h"((uint16_t)3)
+            : "memory");
+    else
+        tc_commit(bar);
+}
+template <bool PAIR>
+__device__ __forceinline__ void tc_mma_ts_g(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    if constexpr (PAIR)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    else
+        tc_mma_ts(d_tmem, a_tmem, b_desc, idesc, accumulate);
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Every thread of both CTAs of the cluster.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Arrive on the leader CTA's copy of `bar` (the same shared-memory offset in
+// CTA 0 of the cluster), releasing this thread's writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_leader(uint64_t* bar) {
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(ra) : "r"(smem_u32(bar)));
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(ra) : "memory");
+}
+// try_wait acquiring at cluster scope (for phases completed by the peer CTA's arrivals)
+__device__ __forceinline__ bool mbar_try_wait_cl(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Shared-memory matrix descriptor of a K-major operand tile with 128-byte
 // swizzle: rows of 64 bf16 (128 bytes), 8-row atoms of 1024 bytes.
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
@@ -136,18 +222,22 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
     return d;
 }
 
-// Instruction descriptor, kind::f16: D F32, A and B BF16, both K-major, M = 128.
-__device__ __forceinline__ uint32_t idesc_bf16(int n) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kTileRows >> 4) << 24);
+// Instruction descriptor, kind::f16: D F32, A and B BF16, both K-major, M = 128
+// (M = 256 for a pair of CTAs).
+__device__ __forceinline__ uint32_t idesc_bf16(int n, int m = kTileRows) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
 // Bounded wait that also gives up once another role has aborted.  The abort
-// flag and the clock are checked every 64 polls only.
+// flag and the clock are checked every 64 polls only.  CL: acquire at cluster
+// scope (a phase that the peer CTA's arrivals complete).
+template <bool CL = false>
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err) {
-    if (mbar_try_wait(bar, parity)) return true;
+    auto tw = [&]() { return CL ? mbar_try_wait_cl(bar, parity) : mbar_try_wait(bar, parity); };
+    if (tw()) return true;
     const long long t0 = clock64();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (tw()) return true;
         if ((it & 63u) == 0) {
             if (*abort_flag) return false;
             if (clock64() - t0 > kWaitLimitCycles) {
@@ -253,7 +343,7 @@ __device__ __forceinline__ Unit unit_at(int64_t u, const TailPlan& tp, int kstag
     return r;
 }
 
-template <int GW, int MAXR, int NI>
+template <int GW, int MAXR, int NI, bool PAIR>
 __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel(const TcArgs ta) {
     pdl_trigger();
     pdl_wait();
@@ -265,7 +355,10 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
     // 1024-byte alignment for the swizzled B tiles; plain pointer arithmetic on
     // the shared array keeps every access below a shared-memory access
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const int b_sub = ta.tok_tile * 128;              // one 64-column B sub-tile
+    // PAIR: CTA `rank` of the cluster holds weight rows [128 rank, 128 rank + 128)
+    // of the item's 256 and tokens [rank n / 2, (rank + 1) n / 2) of its B tile
+    const uint32_t rank = PAIR ? cluster_rank() : 0u;
+    const int b_sub = (PAIR ? ta.tok_tile / 2 : ta.tok_tile) * 128;   // one 64-column B sub-tile
     const int b_stage = 2 * b_sub;
     uint8_t* sB = smem;                               // NSB x 2 sub-tiles
     uint8_t* sW = sB + NSB * b_stage;                 // NSW x 2 packed chunks
@@ -292,22 +385,25 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
             mbar_init(&w_empty[s], 4);        // the 4 warps of the warpgroup that took the stage
         }
         for (int s = 0; s < NSB; ++s) {
-            mbar_init(&b_full[s], GW * 32);   // one cp.async-tracked arrival per gather lane
+            // one cp.async-tracked arrival per gather lane (+ the peer's forwarded half in a pair's leader)
+            mbar_init(&b_full[s], GW * 32 + (PAIR && rank == 0 ? 1 : 0));
             mbar_init(&b_empty[s], 1);
         }
         for (int s = 0; s < SA; ++s) {
-            mbar_init(&a_full[s], 4);
+            mbar_init(&a_full[s], PAIR ? 8 : 4);   // the warpgroup's 4 warps (of both CTAs in a pair)
             mbar_init(&a_empty[s], 1);
         }
         mbar_init(acc_full, NI);              // one arrival per MMA issuer
-        mbar_init(acc_empty, C::kDQ);
+        mbar_init(acc_empty, PAIR ? 2 * C::kDQ : C::kDQ);
         fence_barrier_init();
     }
     __syncthreads();
-    if (flags[0]) return;
+    if (flags[0]) return;   // both CTAs of a pair read the same header
+    // a pair's barriers must be initialised in both CTAs before any remote arrival
+    if constexpr (PAIR) cluster_sync();
     if (warp == C::kProducer) {
-        tmem_alloc(tmem_slot, ta.tmem_cols);
-        tmem_relinquish();
+        tmem_alloc_g<PAIR>(tmem_slot, ta.tmem_cols);
+        tmem_relinquish_g<PAIR>();
     }
     tc_fence_before();
     __syncthreads();
@@ -320,11 +416,22 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
         if (threadIdx.x == 0) set_error(a.err, CHORD_DEV_BAD_PADDED);
         ntp = 0;
     }
-    const int ntiles = a.N / kTileRows;
+    // An item is (align block, 128-row tile of N), or for a pair (align block,
+    // 256-row tile) with CTA `rank` on its 128-row half; units run over the
+    // CTAs (pairs) of the persistent grid in a static round robin.
+    const int ntiles = a.N / (PAIR ? 2 * kTileRows : kTileRows);
+    const int64_t G = PAIR ? gridDim.x / 2 : gridDim.x;
+    const int64_t u0 = PAIR ? blockIdx.x / 2 : blockIdx.x;
+    auto item_coords = [&](int64_t item, int& nt) {
+        int q;
+        const int64_t b = divmod_idx(item, ntiles, q);
+        nt = PAIR ? 2 * q + (int)rank : q;
+        return b;
+    };
     const int kchunks = a.K / kChunkK;
     const int kstages = (kchunks + 1) / 2;   // the last stage holds one chunk when kchunks is odd
     const int64_t n_items = (int64_t)(ntp / a.block_m) * ntiles;
-    const TailPlan tplan = tail_plan(n_items, gridDim.x, kstages, NI, a.tail_split != 0);
+    const TailPlan tplan = tail_plan(n_items, G, kstages, NI, a.tail_split != 0);
     const int64_t n_units = tplan.full + tplan.tail * tplan.S;
     const uint64_t expert_bytes = (uint64_t)a.N * (uint64_t)a.K * 9ull / 16ull;
 
@@ -334,10 +441,10 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
         int64_t g = 0;   // stages lane 0 issued
         Ring wr;
         bool ok = true;
-        for (int64_t wu = blockIdx.x; wu < n_units && ok; wu += gridDim.x) {
+        for (int64_t wu = u0; wu < n_units && ok; wu += G) {
             const Unit un = unit_at(wu, tplan, kstages);
             int nt;
-            const int64_t b = divmod_idx(un.item, ntiles, nt);
+            const int64_t b = item_coords(un.item, nt);
             const ItemInfo inf = item_info(a, b, lane, false);
             if (inf.n_mma == 0) continue;
             if (lane == 0) {
@@ -367,6 +474,34 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
         __syncwarp();
     } else if (warp >= C::kMma0 && warp < C::kGather0) {
         // ------------------------------------------------------------- MMA
+        if (PAIR && rank == 1) {
+            // The peer CTA issues no MMA: one thread forwards each B stage of
+            // its gather warps (complete in this CTA) to the leader's barrier.
+            if (warp == C::kMma0) {
+                Ring br;
+                bool ok = true;
+                for (int64_t wu = u0; wu < n_units && ok; wu += G) {
+                    const Unit un = unit_at(wu, tplan, kstages);
+                    int nt_unused;
+                    const ItemInfo inf = item_info(a, item_coords(un.item, nt_unused), lane, false);
+                    if (inf.n_mma == 0) continue;
+                    if (lane == 0) {
+                        for (int ks = un.ks0; ks < un.ks1; ++ks, br.next(NSB)) {
+                            if (!wait_or_abort(&b_full[br.slot], br.phase, &flags[1], a.err)) {
+                                ok = false;
+                                break;
+                            }
+                            // the tile was written by cp.async (generic proxy); the
+                            // leader's MMA reads it through the async proxy
+                            fence_proxy_async();
+                            mbar_arrive_leader(&b_full[br.slot]);
+                        }
+                    }
+                    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                }
+            }
+            __syncwarp();
+        } else {
         // Issuer mi takes the item's stages ks with ks % NI == mi.
         const int mi = warp - C::kMma0;
         const uint32_t my_acc = acc_tmem + (uint32_t)(mi * ta.tok_tile);
@@ -374,22 +509,22 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
         int issued = 0;                 // stages whose MMAs this issuer committed
         Ring ar, br, last;
         bool ok = true;
-        for (int64_t wu = blockIdx.x; wu < n_units && ok; wu += gridDim.x) {
+        for (int64_t wu = u0; wu < n_units && ok; wu += G) {
             const Unit un = unit_at(wu, tplan, kstages);
             int nt_unused;
-            const int64_t b = divmod_idx(un.item, ntiles, nt_unused);
+            const int64_t b = item_coords(un.item, nt_unused);
             const ItemInfo inf = item_info(a, b, lane, false);
             if (inf.n_mma == 0) continue;
             if (lane == 0) {
-                if (!wait_or_abort(acc_empty, (uint32_t)((nitem & 1) ^ 1), &flags[1], a.err)) ok = false;
+                if (!wait_or_abort<PAIR>(acc_empty, (uint32_t)((nitem & 1) ^ 1), &flags[1], a.err)) ok = false;
                 tc_fence_after();
-                const uint32_t idesc = idesc_bf16(inf.n_mma);
+                const uint32_t idesc = idesc_bf16(inf.n_mma, PAIR ? 2 * kTileRows : kTileRows);
                 bool any = false;
                 for (int ks = un.ks0; ks < un.ks1 && ok; ++ks, ar.next(SA), br.next(NSB)) {
                     if (ks % NI != mi) continue;
                     const int nck = min(2, kchunks - 2 * ks);
-                    if (!wait_or_abort(&a_full[ar.slot], ar.phase, &flags[1], a.err) ||
-                        !wait_or_abort(&b_full[br.slot], br.phase, &flags[1], a.err)) {
+                    if (!wait_or_abort<PAIR>(&a_full[ar.slot], ar.phase, &flags[1], a.err) ||
+                        !wait_or_abort<PAIR>(&b_full[br.slot], br.phase, &flags[1], a.err)) {
                         ok = false;
                         break;
                     }
@@ -399,20 +534,22 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
                     tc_fence_after();
                     const uint32_t b_base = smem_u32(sB + br.slot * b_stage);
                     for (int kk = 0; kk < 4 * nck; ++kk)
-                        tc_mma_ts(my_acc, tmem_base + ar.slot * kACols + kk * 8,
-                                  desc_sw128(b_base + (kk >> 2) * b_sub + (kk & 3) * 32), idesc,
-                                  (any || kk > 0) ? 1u : 0u);
+                        tc_mma_ts_g<PAIR>(my_acc, tmem_base + ar.slot * kACols + kk * 8,
+                                          desc_sw128(b_base + (kk >> 2) * b_sub + (kk & 3) * 32), idesc,
+                                          (any || kk > 0) ? 1u : 0u);
                     any = true;
-                    tc_commit(&a_empty[ar.slot]);
-                    tc_commit(&b_empty[br.slot]);
+                    tc_commit_g<PAIR>(&a_empty[ar.slot]);
+                    tc_commit_g<PAIR>(&b_empty[br.slot]);
                     last = ar;
                     ++issued;
                 }
                 if (ok) {
-                    if (any)
-                        tc_commit(acc_full);
+                    // no share of this item: the commit arrives at once (on both
+                    // CTAs' barrier in a pair)
+                    if (any || PAIR)
+                        tc_commit_g<PAIR>(acc_full);
                     else
-                        mbar_arrive(acc_full);   // no share of this item: nothing to wait for
+                        mbar_arrive(acc_full);
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -421,35 +558,44 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
         // wait for this issuer's last MMAs before the tensor memory is released
         if (lane == 0 && issued > 0) mbar_wait(&a_empty[last.slot], last.phase);
         __syncwarp();
+        }
     } else if (warp >= C::kGather0) {
         // ------------------------------------------------------ activations
         // Lane gl copies the 16-byte piece c = gl % 8 of token rows
         // j = gl / 8 + r * (GW * 4), r < MAXR, for both chunks of a stage;
-        // their A row indices are read once per item.
+        // their A row indices are read once per item.  Each lane's copies
+        // arrive on the stage's barrier when they land, so a stage is full as
+        // soon as its copies are (a warp-level arrival after waiting for the
+        // previous stage's copies measured slower: it shortens the B ring by a
+        // stage, and the ring holds only three at 224 tokens).
         const int gl = (warp - C::kGather0) * 32 + lane;
         const int c = gl & 7;
         constexpr int kRowStep = GW * 4;
         Ring br;
         bool ok = true;
-        for (int64_t wu = blockIdx.x; wu < n_units && ok; wu += gridDim.x) {
+        for (int64_t wu = u0; wu < n_units && ok; wu += G) {
             const Unit un = unit_at(wu, tplan, kstages);
             int nt_unused;
-            const int64_t b = divmod_idx(un.item, ntiles, nt_unused);
-            const ItemInfo inf = item_info(a, b, lane, warp == C::kGather0 && un.ks0 == 0);
+            const int64_t b = item_coords(un.item, nt_unused);
+            const ItemInfo inf = item_info(a, b, lane, warp == C::kGather0 && un.ks0 == 0 && rank == 0);
             if (inf.n_mma == 0) continue;
+            // a pair's CTA gathers its half of the block's first n_mma tokens
+            const int rows = PAIR ? inf.n_mma / 2 : inf.n_mma;
+            const int j0 = PAIR ? (int)rank * rows : 0;
             int32_t arow[MAXR];
 #pragma unroll
             for (int r = 0; r < MAXR; ++r) {
-                const int j = (gl >> 3) + r * kRowStep;
+                const int jl = (gl >> 3) + r * kRowStep;
+                const int j = j0 + jl;
                 arow[r] = -1;
-                if (j < inf.n_mma && j < a.block_m) {
+                if (jl < rows && j < a.block_m) {
                     const int32_t id = a.sorted_ids[b * a.block_m + j];
                     if (row_valid(a, id)) arow[r] = a.a_row_divisor == 1 ? id : id / a.a_row_divisor;
                 }
             }
             for (int ks = un.ks0; ks < un.ks1; ++ks, br.next(NSB)) {
                 const int nck = min(2, kchunks - 2 * ks);
-                if (!wait_or_abort(&b_empty[br.slot], br.phase ^ 1u, &flags[1], a.err)) {
+                if (!wait_or_abort<PAIR>(&b_empty[br.slot], br.phase ^ 1u, &flags[1], a.err)) {
                     ok = false;
                     break;
                 }
@@ -482,17 +628,17 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
         int64_t g = 0, nitem = 0;
         Ring wr, ar;
         bool ok = true;
-        for (int64_t wu = blockIdx.x; wu < n_units && ok; wu += gridDim.x) {
+        for (int64_t wu = u0; wu < n_units && ok; wu += G) {
             const Unit un = unit_at(wu, tplan, kstages);
             int nt;
-            const int64_t b = divmod_idx(un.item, ntiles, nt);
+            const int64_t b = item_coords(un.item, nt);
             const ItemInfo inf = item_info(a, b, lane, false);
             if (inf.n_mma == 0) continue;
             for (int ks = un.ks0; ks < un.ks1; ++ks, ++g, wr.next(NSW), ar.next(SA)) {
                 if ((int)(g & 1) != wg) continue;
                 const int nck = min(2, kchunks - 2 * ks);
                 if (!wait_or_abort(&w_full[wr.slot], wr.phase, &flags[1], a.err) ||
-                    !wait_or_abort(&a_empty[ar.slot], ar.phase ^ 1u, &flags[1], a.err)) {
+                    !wait_or_abort<PAIR>(&a_empty[ar.slot], ar.phase ^ 1u, &flags[1], a.err)) {
                     ok = false;
                     break;
                 }
@@ -530,7 +676,14 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
                 tc_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&a_full[ar.slot]);
+                if (lane == 0) {
+                    // the stage's A rows are in this CTA's tensor memory; the MMA
+                    // thread (the leader's, in a pair) may read them
+                    if (PAIR && rank == 1)
+                        mbar_arrive_leader(&a_full[ar.slot]);
+                    else
+                        mbar_arrive(&a_full[ar.slot]);
+                }
             }
             if (!ok) break;
             // ---- epilogue: accumulator column j is token j of the block.
@@ -555,7 +708,7 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
                     pret[k] = id / a.topk;
                 }
             }
-            if (!wait_or_abort(acc_full, (uint32_t)(nitem & 1), &flags[1], a.err)) {
+            if (!wait_or_abort<PAIR>(acc_full, (uint32_t)(nitem & 1), &flags[1], a.err)) {
                 ok = false;
                 break;
             }
@@ -627,16 +780,24 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty);
+            if (lane == 0) {
+                if (PAIR && rank == 1)
+                    mbar_arrive_leader(acc_empty);
+                else
+                    mbar_arrive(acc_empty);
+            }
             ++nitem;
         }
     }
 
     // ------------------------------------------------------------ teardown
+    // (every role reaches this point, also after an aborted wait, so the
+    // cluster barrier below always completes)
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();   // the leader's last MMAs into the peer's tensor memory are done
     tc_fence_after();
-    if (warp == C::kProducer) tmem_dealloc(tmem_base, ta.tmem_cols);
+    if (warp == C::kProducer) tmem_dealloc_g<PAIR>(tmem_base, ta.tmem_cols);
 }
 
 uint32_t pow2_cols(uint32_t c) {
@@ -645,9 +806,69 @@ uint32_t pow2_cols(uint32_t c) {
     return p;
 }
 
-template <int GW, int MAXR, int NI>
+// Launch of a kernel in clusters of two CTAs (with programmatic stream
+// serialization when `pdl`).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pairs(bool pdl, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                         Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+// Clusters of two CTAs of `kern` that can be resident at once on this device
+// (cached per device, kernel and shared-memory size); 0 when the query fails.
+int max_active_pairs(const void* kern, int threads, size_t smem) {
+    struct Entry {
+        int dev;
+        const void* kern;
+        size_t smem;
+        int n;
+    };
+    static std::mutex mu;
+    static Entry cache[64];
+    static int ncache = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < ncache; ++i)
+        if (cache[i].dev == dev && cache[i].kern == kern && cache[i].smem == smem) return cache[i].n;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * 76);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+    }
+    if (ncache < 64) cache[ncache++] = Entry{dev, kern, smem, n};
+    return n;
+}
+
+template <int GW, int MAXR, int NI, bool PAIR>
 cudaError_t launch_cfg(const GemmArgs& g, bool deep_weights, cudaStream_t stream) {
     using C = Cfg<GW, MAXR, NI>;
+    auto kern = gemm_tc_kernel<GW, MAXR, NI, PAIR>;
     constexpr size_t kSmemBudget = 220 * 1024;   // of the 227 KB a CTA may use
     TcArgs ta;
     ta.g = g;
@@ -668,7 +889,8 @@ cudaError_t launch_cfg(const GemmArgs& g, bool deep_weights, cudaStream_t stream
     // the rest of the budget for packed weights, to keep enough HBM bytes in
     // flight.  Many tokens per item: four weight stages and the rest for B
     // tiles, whose gather from L2 has the longer latency per byte consumed.
-    const size_t b_stage = (size_t)ta.tok_tile * 256, w_stage = 2 * kChunk2;
+    // (a pair's CTA holds half of each B tile)
+    const size_t b_stage = (size_t)(PAIR ? ta.tok_tile / 2 : ta.tok_tile) * 256, w_stage = 2 * kChunk2;
     const size_t fixed = 1024 + 64;
     int nsb, nsw;
     if (deep_weights) {
@@ -690,20 +912,30 @@ cudaError_t launch_cfg(const GemmArgs& g, bool deep_weights, cudaStream_t stream
     // SM's 512, ask for enough shared memory that only one CTA fits per SM.
     if (2 * ta.tmem_cols > 512 && smem < 120 * 1024) smem = 120 * 1024;
     int per_sm = 1;
-    cudaError_t e = kernel_ctas_per_sm(reinterpret_cast<const void*>(gemm_tc_kernel<GW, MAXR, NI>), C::kThreads,
-                                       smem, 227 * 1024, &per_sm);
+    cudaError_t e = kernel_ctas_per_sm(reinterpret_cast<const void*>(kern), C::kThreads, smem, 227 * 1024, &per_sm);
     if (e != cudaSuccess) return e;
     const int tmem_fit = (int)(512 / ta.tmem_cols);
     if (per_sm > tmem_fit) per_sm = tmem_fit;
     if (per_sm < 1) per_sm = 1;
-    const int64_t items_cap = (g.capacity / g.block_m) * (g.N / kTileRows);
-    int64_t grid = (int64_t)device_info().sm_count * per_sm;
+    const int64_t items_cap = (g.capacity / g.block_m) * (g.N / (PAIR ? 2 * kTileRows : kTileRows));
+    int64_t grid = (int64_t)device_info().sm_count * per_sm / (PAIR ? 2 : 1);   // CTAs, or pairs of CTAs
+    if (PAIR) {
+        // only as many pairs as can be resident at once: a pair that starts
+        // late would run its whole share of the static round robin late
+        const int clusters = max_active_pairs(reinterpret_cast<const void*>(kern), C::kThreads, smem);
+        if (clusters > 0 && grid > clusters) grid = clusters;
+    }
     if (grid > items_cap) grid = items_cap;
     if (grid < 1) grid = 1;
+    if (PAIR) {
+        ta.g.tail_split = 0;   // the split tail is built for single CTAs
+        return launch_pairs(pdl_for(g.num_pairs), kern, dim3((unsigned)(2 * grid)), dim3(C::kThreads), smem, stream,
+                            ta);
+    }
     // The split tail writes at most grid units of 128 x tok_tile FP32 sums (S * tail <= grid).
     const size_t tail_bytes = (size_t)grid * kTileRows * (size_t)ta.tok_tile * sizeof(float);
     ta.g.tail_split = (g.tail_split && g.partial && g.partial_bytes >= tail_bytes) ? 1 : 0;
-    e = launch_pdl(pdl_for(g.num_pairs), gemm_tc_kernel<GW, MAXR, NI>, dim3((unsigned)grid), dim3(C::kThreads), smem, stream, ta);
+    e = launch_pdl(pdl_for(g.num_pairs), kern, dim3((unsigned)grid), dim3(C::kThreads), smem, stream, ta);
     if (e != cudaSuccess || !ta.g.tail_split) return e;
     const int kstages = (g.K / kChunkK + 1) / 2;
     return launch_tc_tail_reduce(ta.g, grid, kstages, NI, ta.tok_tile, stream);
@@ -713,16 +945,27 @@ cudaError_t launch_cfg(const GemmArgs& g, bool deep_weights, cudaStream_t stream
 
 bool tc_available() { return true; }
 
-cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t stream) {
-    if (a.block_m % 8 || a.block_m > 256 || a.N % kTileRows || a.K % kChunkK) return cudaErrorInvalidValue;
+
+template <bool PAIR>
+cudaError_t launch_tc_shape(const GemmArgs& a, cudaStream_t stream) {
     // Up to 64 tokens per item: four MMA issuers (a tcgen05.mma of N <= 64 costs
     // its issuing thread about as long as one of N = 128) and three gather warps
     // (measured on GB300: 360 -> 290 us for the EP8 decode gate_up against two
     // issuers and one gather warp).
-    if (a.block_m <= 64) return launch_cfg<3, 6, 4>(a, true, stream);
+    if (a.block_m <= 64) return launch_cfg<3, 6, 4, PAIR>(a, true, stream);
     // 65-128 tokens: two issuers (TP8 T=4096 gate_up 526 -> 363 us on GB300)
-    if (a.block_m <= 128) return launch_cfg<4, 8, 2>(a, false, stream);
-    return launch_cfg<4, 16, 1>(a, false, stream);                       // up to 256 tokens per item
+    if (a.block_m <= 128) return launch_cfg<4, 8, 2, PAIR>(a, false, stream);
+    return launch_cfg<4, 16, 1, PAIR>(a, false, stream);                 // up to 256 tokens per item
+}
+
+cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t stream) {
+    if (a.block_m % 8 || a.block_m > 256 || a.N % kTileRows || a.K % kChunkK) return cudaErrorInvalidValue;
+    // Pairs of CTAs on request only: measured on GB300 they lose on long-K items
+    // (EP8 prefill gate_up, K = 7168: 562 -> 760 us) and gain little on short ones
+    // (down, K = 2048: 421 -> 409 us): the cross-CTA hand-offs of every stage add
+    // more latency than halving each SM's share of the activation gather saves.
+    if (a.tc_pairs && a.N % (2 * kTileRows) == 0) return launch_tc_shape<true>(a, stream);
+    return launch_tc_shape<false>(a, stream);
 }
 
 }  // namespace chord

@@ -89,6 +89,7 @@ struct GemmArgs {
     // number is its token's only local pair, and its weighted result
     // bf16(0 + w * sum) goes to out[pair / topk, n] instead of C; the others
     // (NaN) write their FP32 sums to C for chord_combine_finish.
+    int tc_pairs;      // tcgen05 kernel in clusters of two CTAs (cta_group::2)
     int combine;
     int topk;
     const float* pair_w;
