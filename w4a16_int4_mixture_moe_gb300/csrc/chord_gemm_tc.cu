@@ -231,13 +231,20 @@ __device__ __forceinline__ uint32_t idesc_bf16(int n, int m = kTileRows) {
 // Bounded wait that also gives up once another role has aborted.  The abort
 // flag and the clock are checked every 64 polls only.  CL: acquire at cluster
 // scope (a phase that the peer CTA's arrivals complete).
+template <bool CL>
+__device__ __forceinline__ bool try_wait_g(uint64_t* bar, uint32_t parity) {
+    if constexpr (CL)
+        return mbar_try_wait_cl(bar, parity);
+    else
+        return mbar_try_wait(bar, parity);
+}
+
 template <bool CL = false>
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err) {
-    auto tw = [&]() { return CL ? mbar_try_wait_cl(bar, parity) : mbar_try_wait(bar, parity); };
-    if (tw()) return true;
+    if (try_wait_g<CL>(bar, parity)) return true;
     const long long t0 = clock64();
     for (uint32_t it = 1;; ++it) {
-        if (tw()) return true;
+        if (try_wait_g<CL>(bar, parity)) return true;
         if ((it & 63u) == 0) {
             if (*abort_flag) return false;
             if (clock64() - t0 > kWaitLimitCycles) {
@@ -341,6 +348,103 @@ __device__ __forceinline__ Unit unit_at(int64_t u, const TailPlan& tp, int kstag
         r.pidx = v;
     }
     return r;
+}
+
+// Accumulator drain of one unit by a dequantising warp (its 32 tensor-memory
+// lanes = weight rows, warpgroup wg taking tokens j with (j / 16) % 2 == wg):
+// the FP32 sums of the issuers added in issuer order, then the split tail's
+// partial slice, SiLU * up (layout 3), the fused combine (CMB), or the bf16 /
+// FP32 output by pair id.  pre[k]: pair id of token wg*16 + 32*(2k + l/16) +
+// l%16 held by lane l (-1: none).
+template <bool CMB, int NI>
+__device__ __forceinline__ void drain_item(const TcArgs& ta, const Unit& un, int n_mma, int nt, int wg, int lane,
+                                           uint32_t acc_tmem, const int32_t (&pre)[4]) {
+    const GemmArgs& a = ta.g;
+    const int quarter = (threadIdx.x >> 5) & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    const int n_out = nt * kTileRows + row;
+    // fused SiLU * up (layout 3): rows 16k + i (i < 8) and 16k + i + 8 of
+    // the tile hold gate and up of output column 64 * nt + 8k + i
+    const int h_col = nt * (kTileRows / 2) + 8 * (row / 16) + (row % 8);
+    const bool gate_row = (lane & 8) == 0;
+    const int nst = un.ks1 - un.ks0;
+    const int parts = nst < NI ? nst : NI;   // issuers that hold a share of this unit
+    float prew[4];    // fused combine: the pair's weight (a number: its token's only local pair)
+    int32_t pret[4];  // fused combine: the pair's token
+    if (CMB) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            prew[k] = pre[k] >= 0 ? a.pair_w[pre[k]] : 0.0f;
+            pret[k] = pre[k] >= 0 ? pre[k] / a.topk : 0;
+        }
+    }
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int j0 = wg * 16 + 32 * it;
+        if (j0 >= n_mma) continue;   // (not break: keeps the loop unrolled, pre[] in registers)
+        uint32_t v[16];
+        tmem_ld16(acc_tmem + lane_base + j0, v);
+        for (int pi = 1; pi < parts; ++pi) {
+            uint32_t w2[16];
+            tc_wait_ld();
+            tmem_ld16(acc_tmem + (uint32_t)(pi * ta.tok_tile) + lane_base + j0, w2);
+            tc_wait_ld();
+#pragma unroll
+            for (int u = 0; u < 16; ++u) v[u] = __float_as_uint(__uint_as_float(v[u]) + __uint_as_float(w2[u]));
+        }
+        tc_wait_ld();
+        if (un.pidx >= 0) {
+            // a slice of a split tail item: its FP32 sums, row-major [row][token]
+            float4* dst = reinterpret_cast<float4*>(a.partial + ((int64_t)un.pidx * kTileRows + row) * ta.tok_tile + j0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                     __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+            continue;
+        }
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            if (!CMB && a.silu) {
+                // lanes l (gate row) and l ^ 8 (its up row) split the 16
+                // tokens: the gate lane takes tokens 0-7, the up lane 8-15,
+                // each receiving the partner's value for its tokens
+                if (u < 8) {
+                    const float lo = __uint_as_float(v[u]), hi = __uint_as_float(v[8 + u]);
+                    const float mine = gate_row ? lo : hi;
+                    const float other = __shfl_xor_sync(0xffffffffu, gate_row ? hi : lo, 8);
+                    const int tok = gate_row ? u : 8 + u;
+                    const int32_t id = __shfl_sync(0xffffffffu, pre[it >> 1], tok + 16 * (it & 1));
+                    if (id >= 0)
+                        static_cast<__nv_bfloat16*>(a.C)[(int64_t)id * (a.N / 2) + h_col] =
+                            gate_row ? silu_mul_bf16(mine, other) : silu_mul_bf16(other, mine);
+                }
+                continue;
+            }
+            const int32_t id = __shfl_sync(0xffffffffu, pre[it >> 1], u + 16 * (it & 1));
+            const float val = __uint_as_float(v[u]);
+            if (CMB) {
+                const float w = __shfl_sync(0xffffffffu, prew[it >> 1], u + 16 * (it & 1));
+                const int32_t tok = __shfl_sync(0xffffffffu, pret[it >> 1], u + 16 * (it & 1));
+                if (id >= 0) combine_store(static_cast<float*>(a.C), a.out, a.N, id, tok, w, n_out, val);
+                continue;
+            }
+            if (id < 0) continue;
+            if (a.out_f32)
+                static_cast<float*>(a.C)[(int64_t)id * a.N + n_out] = val;
+            else
+                static_cast<__nv_bfloat16*>(a.C)[(int64_t)id * a.N + n_out] = __float2bfloat16_rn(val);
+        }
+    }
+}
+
+// The fused combine's drain, kept out of line: inlined next to the plain drain
+// it made the dequantising warps' loop longer than the instruction cache holds
+// (the EP8 prefill down GEMM, 2688 short items, measured 361 -> 423 us).
+template <int NI>
+__device__ __noinline__ void drain_item_combine(const TcArgs& ta, const Unit& un, int n_mma, int nt, int wg, int lane,
+                                                uint32_t acc_tmem, const int32_t (&pre)[4]) {
+    drain_item<true, NI>(ta, un, n_mma, nt, wg, lane, acc_tmem, pre);
 }
 
 template <int GW, int MAXR, int NI, bool PAIR>
@@ -690,8 +794,6 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
             // Pair ids first, before the accumulator is ready: lane l holds the
             // id of token wg*16 + 32*(2k + l/16) + l%16 in pre[k].
             int32_t pre[4];
-            float prew[4];    // fused combine: the pair's weight (a number: its token's only local pair)
-            int32_t pret[4];  // fused combine: the pair's token
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int j = wg * 16 + 32 * (2 * k + (lane >> 4)) + (lane & 15);
@@ -701,83 +803,18 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
                     if (!row_valid(a, id)) id = -1;
                 }
                 pre[k] = id;
-                prew[k] = 0.0f;
-                pret[k] = 0;
-                if (a.combine && id >= 0) {
-                    prew[k] = a.pair_w[id];
-                    pret[k] = id / a.topk;
-                }
             }
             if (!wait_or_abort<PAIR>(acc_full, (uint32_t)(nitem & 1), &flags[1], a.err)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const int n_out = nt * kTileRows + row;
-            // fused SiLU * up (layout 3): rows 16k + i (i < 8) and 16k + i + 8 of
-            // the tile hold gate and up of output column 64 * nt + 8k + i
-            const int h_col = nt * (kTileRows / 2) + 8 * (row / 16) + (row % 8);
-            const bool gate_row = (lane & 8) == 0;
-            const int nst = un.ks1 - un.ks0;
-            const int parts = nst < NI ? nst : NI;   // issuers that hold a share of this unit
-#pragma unroll
-            for (int it = 0; it < 8; ++it) {
-                const int j0 = wg * 16 + 32 * it;
-                if (j0 >= inf.n_mma) continue;   // (not break: keeps the loop unrolled, pre[] in registers)
-                uint32_t v[16];
-                tmem_ld16(acc_tmem + lane_base + j0, v);
-                for (int pi = 1; pi < parts; ++pi) {
-                    uint32_t w2[16];
-                    tc_wait_ld();
-                    tmem_ld16(acc_tmem + (uint32_t)(pi * ta.tok_tile) + lane_base + j0, w2);
-                    tc_wait_ld();
-#pragma unroll
-                    for (int u = 0; u < 16; ++u) v[u] = __float_as_uint(__uint_as_float(v[u]) + __uint_as_float(w2[u]));
-                }
-                tc_wait_ld();
-                if (un.pidx >= 0) {
-                    // a slice of a split tail item: its FP32 sums, row-major [row][token]
-                    float4* dst = reinterpret_cast<float4*>(
-                        a.partial + ((int64_t)un.pidx * kTileRows + row) * ta.tok_tile + j0);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                             __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
-                    continue;
-                }
-#pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    if (a.silu) {
-                        // lanes l (gate row) and l ^ 8 (its up row) split the 16
-                        // tokens: the gate lane takes tokens 0-7, the up lane 8-15,
-                        // each receiving the partner's value for its tokens
-                        if (u < 8) {
-                            const float lo = __uint_as_float(v[u]), hi = __uint_as_float(v[8 + u]);
-                            const float mine = gate_row ? lo : hi;
-                            const float other = __shfl_xor_sync(0xffffffffu, gate_row ? hi : lo, 8);
-                            const int tok = gate_row ? u : 8 + u;
-                            const int32_t id = __shfl_sync(0xffffffffu, pre[it >> 1], tok + 16 * (it & 1));
-                            if (id >= 0)
-                                static_cast<__nv_bfloat16*>(a.C)[(int64_t)id * (a.N / 2) + h_col] =
-                                    gate_row ? silu_mul_bf16(mine, other) : silu_mul_bf16(other, mine);
-                        }
-                        continue;
-                    }
-                    const int32_t id = __shfl_sync(0xffffffffu, pre[it >> 1], u + 16 * (it & 1));
-                    const float val = __uint_as_float(v[u]);
-                    if (a.combine) {
-                        const float w = __shfl_sync(0xffffffffu, prew[it >> 1], u + 16 * (it & 1));
-                        const int32_t tok = __shfl_sync(0xffffffffu, pret[it >> 1], u + 16 * (it & 1));
-                        if (id >= 0) combine_store(static_cast<float*>(a.C), a.out, a.N, id, tok, w, n_out, val);
-                        continue;
-                    }
-                    if (id < 0) continue;
-                    if (a.out_f32)
-                        static_cast<float*>(a.C)[(int64_t)id * a.N + n_out] = val;
-                    else
-                        static_cast<__nv_bfloat16*>(a.C)[(int64_t)id * a.N + n_out] = __float2bfloat16_rn(val);
-                }
-            }
+            // the fused combine's drain is a separate instantiation, so the
+            // plain drain carries none of its registers or branches
+            if (a.combine)
+                drain_item_combine<NI>(ta, un, inf.n_mma, nt, wg, lane, acc_tmem, pre);
+            else
+                drain_item<false, NI>(ta, un, inf.n_mma, nt, wg, lane, acc_tmem, pre);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
