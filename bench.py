@@ -632,16 +632,20 @@ class LayerRig:
             g2 += marks[2].elapsed_time(marks[3])
         return g1 / nrep, g2 / nrep, "events inside the step's graph"
 
-    def layer_call(self):
+    def layer_call(self, cached=True):
+        """The public layer call: chord_moe_layer_cached (the layer's launches
+        recorded once into a CUDA graph, replayed), or the eager chord_moe_layer."""
         w = self.w
-        self.chord.chord_moe_layer(self.x_e, self.ids_e, self.w_e, w.E, w.E_global, w.I, self.p13, self.p2,
-                                   self.lws, self.out, block_m=self.bm, opts=self.silu_opts, stream=self.stream)
+        fn = self.chord.chord_moe_layer_cached if cached else self.chord.chord_moe_layer
+        fn(self.x_e, self.ids_e, self.w_e, w.E, w.E_global, w.I, self.p13, self.p2, self.lws, self.out,
+           block_m=self.bm, opts=self.silu_opts, stream=self.stream)
 
-    def e2e(self, steps, warmup, barrier):
-        """The public chord_moe_layer call end to end: x, ids and weights copied
-        from pinned host memory, the output copied back, all inside the timed
-        region (CUDA events on the launching stream).  Returns (ms summed over
-        steps, h2d bytes per step, d2h bytes per step)."""
+    def e2e(self, steps, warmup, barrier, cached=True):
+        """The public layer call end to end (chord_moe_layer_cached, or the eager
+        chord_moe_layer): x, ids and weights copied from pinned host memory, the
+        output copied back, all inside the timed region (CUDA events on the
+        launching stream).  Returns (ms summed over steps, h2d bytes per step,
+        d2h bytes per step)."""
         torch = self.torch
         x_h = torch.from_numpy(self.x.view(np.int16)).view(torch.bfloat16).pin_memory()
         ids_h = torch.from_numpy(self.ids).pin_memory()
@@ -652,7 +656,7 @@ class LayerRig:
             self.x_e.copy_(x_h, non_blocking=True)
             self.ids_e.copy_(ids_h, non_blocking=True)
             self.w_e.copy_(w_h, non_blocking=True)
-            self.layer_call()
+            self.layer_call(cached)
             out_h.copy_(self.out, non_blocking=True)
 
         for _ in range(warmup):
@@ -666,17 +670,18 @@ class LayerRig:
         barrier()
         return f0.elapsed_time(f1), self.x.nbytes + self.ids.nbytes + self.wts.nbytes, self.w.T * self.w.H * 2
 
-    def host_us_per_call(self, calls=200):
-        """Host (CPU) time of one eager chord_moe_layer enqueue through the public
-        binding: the median over `calls` calls, each issued after the stream has
-        drained, so no call waits on a full launch queue."""
+    def host_us_per_call(self, calls=200, cached=True):
+        """Host (CPU) time of one layer enqueue through the public binding
+        (cached: a graph replay after the first call; else the eager call): the
+        median over `calls` calls, each issued after the stream has drained, so
+        no call waits on a full launch queue."""
         torch = self.torch
-        self.layer_call()
+        self.layer_call(cached)
         torch.cuda.synchronize()
         ts = []
         for _ in range(calls):
             t0 = time.perf_counter()
-            self.layer_call()
+            self.layer_call(cached)
             ts.append(time.perf_counter() - t0)
             torch.cuda.synchronize()
         return float(np.median(ts)) * 1e6
@@ -849,10 +854,14 @@ def main():
 
     # ---- end to end through the public layer call, host buffers, copies timed
     e2e_ms, h2d, d2h = rig.e2e(args.steps, args.warmup, barrier)
+    e2e_eager_steps = max(1, min(args.steps, 200))
+    e2e_eager_ms, _, _ = rig.e2e(e2e_eager_steps, args.warmup, barrier, cached=False)
     host_us = rig.host_us_per_call()
+    host_eager_us = rig.host_us_per_call(cached=False)
     assert chord.chord_get_device_error(rig.stream) == 0
 
-    total_ms, e2e_ms, g1, g2, host_us = reduce_max([total_ms, e2e_ms, g1, g2, host_us], pg, dev)
+    total_ms, e2e_ms, e2e_eager_ms, g1, g2, host_us, host_eager_us = reduce_max(
+        [total_ms, e2e_ms, e2e_eager_ms, g1, g2, host_us, host_eager_us], pg, dev)
     us_per_call = per_call_us(total_ms, args.steps)
     e2e_us = per_call_us(e2e_ms, args.steps)
 
@@ -862,7 +871,10 @@ def main():
     details = {"timing": f"CUDA graph replay per step (align, GEMMs, combine), device events; GEMMs: {gemm_timing}",
                "silu_mul": "fused into gate_up" if rig.fused else "separate pass", "split_k": rig.split_desc(),
                "combine": "fused into the down GEMM" if rig.fuse_combine else "separate pass",
-               "host_us_per_call": "median CPU time of one eager chord_moe_layer enqueue through the Python binding"}
+               "e2e": "chord_moe_layer_cached (the layer's launches recorded once into a CUDA graph, replayed) with "
+                      "pinned host buffers, the copies in and out inside the timed region",
+               "host_us_per_call": "median CPU time of one chord_moe_layer_cached enqueue through the Python binding "
+                                   "(a graph replay); host_us_per_call_eager: the same for the eager chord_moe_layer"}
     line = {
         "metric": METRIC, "value": round(us_per_call, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": False,
@@ -874,7 +886,9 @@ def main():
         "roofline_down": r2,
         "clocks": clk,
         "e2e": {"value": round(e2e_us, 2), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e_eager": {"value": round(per_call_us(e2e_eager_ms, e2e_eager_steps), 2), "unit": UNIT},
         "host_us_per_call": round(host_us, 2),
+        "host_us_per_call_eager": round(host_eager_us, 2),
         "gpu_launches": rig.launches_per_step * args.steps,
         "details": details,
     }

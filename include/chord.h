@@ -466,6 +466,34 @@ chord_status chord_moe_layer(const void *x, const int32_t *topk_ids, const float
                              void *workspace, size_t workspace_bytes, void *out,
                              const chord_opts *opts, void *stream);
 
+/* chord_moe_layer with its launches recorded once into a CUDA graph and
+ * replayed: the host cost of a call becomes a lookup and one graph launch
+ * (the article memoises its kernel resolution to remove host overhead from
+ * small decode calls, section "Grouped SM90 kernels"; this removes the
+ * per-kernel launch calls as well).  Same arguments, results and status codes
+ * as chord_moe_layer, except:
+ *   - opts->validate must be 0 (CHORD_ERR_UNSUPPORTED otherwise: validation
+ *     synchronises, which a graph cannot record);
+ *   - the first call with a given set of arguments (every pointer, size and
+ *     option, on the current device) records the layer on a capture stream of
+ *     the library and instantiates it: that call costs a capture, must not be
+ *     made while the calling thread is capturing a stream itself, and leaves
+ *     the graph cached; later calls with the same arguments replay it on
+ *     `stream`, reading the buffers' current contents;
+ *   - the library keeps at most 64 graphs (the least recently used is dropped)
+ *     until chord_moe_layer_cache_clear.
+ * Thread-safe; calls that overlap on the GPU race on the workspace as with
+ * chord_moe_layer. */
+chord_status chord_moe_layer_cached(const void *x, const int32_t *topk_ids, const float *topk_w,
+                                    int T, int topk, int E, int E_global, int H, int I,
+                                    const void *packed_w13, size_t w13_bytes,
+                                    const void *packed_w2, size_t w2_bytes, int block_m,
+                                    void *workspace, size_t workspace_bytes, void *out,
+                                    const chord_opts *opts, void *stream);
+
+/* Destroys every graph chord_moe_layer_cached holds; returns how many. */
+int chord_moe_layer_cache_clear(void);
+
 /* ------------------------------------------------------------------ errors */
 
 /* Synchronises `stream`, returns the current device's sticky error word in

@@ -1161,3 +1161,54 @@ def test_layer_tc_pairs_and_fused_combine():
     gemm(h, 1, p2, E, H, I, s, e, n, bm, P, kernel=TC, C=C2, out_dtype=chord.DTYPE_F32, tc_pairs=1)
     check_layer_chain(x, ids, wts, (c13, s13), (c2, s2), E, host_bits(C1), host_bits(h), C2.cpu().numpy(),
                       host_bits(out), "layer on CTA pairs")
+
+
+# ------------------------------------------------- the layer replayed from a CUDA graph
+
+def test_layer_cached_matches_eager_and_rereads_inputs():
+    """chord_moe_layer_cached records the layer once per argument set and
+    replays the graph: bit for bit the eager layer on calls whose input
+    contents change at the same addresses (the replay reads the buffers
+    anew), for two argument sets (each its own graph) used alternately, on
+    another stream than the one it recorded on; validation is refused; the
+    cache is cleared at the end."""
+    chord.chord_moe_layer_cache_clear()
+    cases = []
+    for T, topk, E, H, I, fused in ((24, 4, 6, 256, 128, True), (40, 8, 6, 256, 256, False)):
+        c13, s13 = wl.random_codes(T + 1, (E, 2 * I, H)), wl.random_scales(T + 2, (E, 2 * I, H // 32))
+        c2, s2 = wl.random_codes(T + 3, (E, H, I)), wl.random_scales(T + 4, (E, H, I // 32))
+        p13 = pack(c13, s13, chord.LAYOUT_GATE_UP_INTERLEAVED if fused else chord.LAYOUT_TCGEN05)
+        p2 = pack(c2, s2)
+        bm = 16
+        ws = torch.empty(chord.chord_layer_workspace_bytes(T, topk, E, H, I, bm), dtype=torch.uint8, device=DEV)
+        xd = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+        idd = torch.empty((T, topk), dtype=torch.int32, device=DEV)
+        wd = torch.empty((T, topk), dtype=torch.float32, device=DEV)
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+        opts = chord.ChordOpts(epilogue=chord.EPILOGUE_SILU_MUL if fused else chord.EPILOGUE_NONE)
+        cases.append((T, topk, E, H, I, p13, p2, bm, ws, xd, idd, wd, out, opts))
+    s = torch.cuda.Stream()
+    for rnd in range(3):
+        for (T, topk, E, H, I, p13, p2, bm, ws, xd, idd, wd, out, opts) in cases:
+            ids = wl.random_ids(100 * rnd + T, T, topk, 4 * E)
+            ids = np.where(ids < E, ids, -1).astype(np.int32)
+            xd.copy_(dbf(wl.random_bf16(100 * rnd + T + 1, (T, H))))
+            idd.copy_(dev(ids))
+            wd.copy_(dev(wl.random_weights(100 * rnd + T + 2, T, topk)))
+            torch.cuda.synchronize()
+            with torch.cuda.stream(s):
+                chord.chord_moe_layer_cached(xd, idd, wd, E, 4 * E, I, p13, p2, ws, out, block_m=bm, opts=opts,
+                                             stream=s)
+            s.synchronize()
+            got = host_bits(out).copy()
+            ref = torch.empty_like(out)
+            chord.chord_moe_layer(xd, idd, wd, E, 4 * E, I, p13, p2, ws, ref, block_m=bm, opts=opts)
+            torch.cuda.synchronize()
+            np.testing.assert_array_equal(got, host_bits(ref))
+    T, topk, E, H, I, p13, p2, bm, ws, xd, idd, wd, out, opts = cases[0]
+    with pytest.raises(chord.ChordError) as ei:
+        chord.chord_moe_layer_cached(xd, idd, wd, E, 4 * E, I, p13, p2, ws, out, block_m=bm,
+                                     opts=chord.ChordOpts(validate=1))
+    assert ei.value.status == 2
+    assert chord.chord_moe_layer_cache_clear() == 2
+    assert chord.chord_get_device_error() == 0

@@ -20,7 +20,7 @@ __all__ = [
     "chord_align_capacity", "chord_align_workspace_bytes", "chord_moe_align", "chord_select_block_m", "chord_select_kernel",
     "chord_gemm_workspace_bytes", "chord_gemm_launch_count", "chord_w4a16_moe_gemm", "chord_silu_mul", "chord_moe_combine",
     "chord_combine_plan", "chord_w4a16_moe_gemm_combine", "chord_combine_finish",
-    "chord_layer_workspace_bytes", "chord_moe_layer", "chord_get_device_error", "chord_selftest_wait_timeout",
+    "chord_layer_workspace_bytes", "chord_moe_layer", "chord_moe_layer_cached", "chord_moe_layer_cache_clear", "chord_get_device_error", "chord_selftest_wait_timeout",
     "chord_grouped_contiguous_workspace_bytes", "chord_grouped_contiguous_gemm",
     "chord_grouped_masked_workspace_bytes", "chord_grouped_masked_gemm",
     "KERNEL_AUTO", "KERNEL_TCGEN05", "KERNEL_WARP_MMA", "LAYOUT_WARP_MMA", "LAYOUT_TCGEN05",
@@ -78,6 +78,9 @@ _SIGS = {
     "chord_layer_workspace_bytes": (_sz, [_int, _int, _int, _int, _int, _int]),
     "chord_moe_layer": (_int, [_vp, _vp, _vp, _int, _int, _int, _int, _int, _int, _vp, _sz, _vp, _sz, _int, _vp,
                                _sz, _vp, _OPTS, _vp]),
+    "chord_moe_layer_cached": (_int, [_vp, _vp, _vp, _int, _int, _int, _int, _int, _int, _vp, _sz, _vp, _sz, _int,
+                                      _vp, _sz, _vp, _OPTS, _vp]),
+    "chord_moe_layer_cache_clear": (_int, []),
     "chord_get_device_error": (_int, [_vp, ctypes.POINTER(_i32)]),
     "chord_selftest_wait_timeout": (_int, [_vp]),
     "chord_grouped_contiguous_workspace_bytes": (_sz, [_i64, _int]),
@@ -255,6 +258,20 @@ def chord_moe_layer(x, topk_ids, topk_w, E: int, E_global: int, I: int, packed_w
     _check(load().chord_moe_layer(_p(x), _p(topk_ids), _p(topk_w), T, topk, E, E_global, H, I, _p(packed_w13),
                                   _nbytes(packed_w13), _p(packed_w2), _nbytes(packed_w2), block_m, _p(workspace),
                                   _nbytes(workspace), _p(out), _o(opts), _s(stream)), "chord_moe_layer")
+
+
+def chord_moe_layer_cached(x, topk_ids, topk_w, E: int, E_global: int, I: int, packed_w13, packed_w2, workspace,
+                           out, block_m: int = 0, opts=None, stream=None):
+    T, H = x.shape
+    topk = topk_ids.shape[1]
+    _check(load().chord_moe_layer_cached(_p(x), _p(topk_ids), _p(topk_w), T, topk, E, E_global, H, I,
+                                         _p(packed_w13), _nbytes(packed_w13), _p(packed_w2), _nbytes(packed_w2),
+                                         block_m, _p(workspace), _nbytes(workspace), _p(out), _o(opts), _s(stream)),
+           "chord_moe_layer_cached")
+
+
+def chord_moe_layer_cache_clear() -> int:
+    return int(load().chord_moe_layer_cache_clear())
 
 
 def chord_grouped_contiguous_workspace_bytes(M: int, E: int) -> int:

@@ -5,6 +5,7 @@
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
+#include <string.h>
 
 #include <mutex>
 
@@ -637,6 +638,124 @@ chord_status chord_moe_layer(const void* x, const int32_t* topk_ids, const float
     }
     o.validate = validate;
     return finish(o, static_cast<cudaStream_t>(stream));
+}
+
+// ---- the layer replayed from a CUDA graph (chord_moe_layer_cached)
+}  // extern "C"
+
+namespace {
+// One recorded layer: the call's arguments (the graph reads the same buffers
+// every replay) and the instantiated graph.  The key is compared as bytes, so
+// it is zero-filled before its fields are set.
+struct LayerKey {
+    int dev;
+    const void* x;
+    const int32_t* topk_ids;
+    const float* topk_w;
+    int T, topk, E, E_global, H, I, block_m;
+    const void* w13;
+    size_t w13_bytes;
+    const void* w2;
+    size_t w2_bytes;
+    void* workspace;
+    size_t workspace_bytes;
+    void* out;
+    chord_opts opts;
+};
+struct LayerGraph {
+    LayerKey key;
+    cudaGraphExec_t exec;
+    uint64_t last_use;
+};
+constexpr int kMaxLayerGraphs = 64;
+std::mutex g_graph_mu;
+LayerGraph g_graphs[kMaxLayerGraphs];
+int g_ngraphs = 0;
+uint64_t g_graph_clock = 0;
+cudaStream_t g_capture_stream[kMaxDevices];
+}  // namespace
+
+extern "C" {
+
+chord_status chord_moe_layer_cached(const void* x, const int32_t* topk_ids, const float* topk_w, int T, int topk,
+                                    int E, int E_global, int H, int I, const void* packed_w13, size_t w13_bytes,
+                                    const void* packed_w2, size_t w2_bytes, int block_m, void* workspace,
+                                    size_t workspace_bytes, void* out, const chord_opts* opts, void* stream) {
+    const chord_opts o = opts_or_default(opts);
+    if (o.validate) return CHORD_ERR_UNSUPPORTED;   // validation synchronises, which a graph cannot record
+    if (T == 0) return chord_moe_layer(x, topk_ids, topk_w, T, topk, E, E_global, H, I, packed_w13, w13_bytes,
+                                       packed_w2, w2_bytes, block_m, workspace, workspace_bytes, out, &o, stream);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CHORD_ERR_CUDA;
+    LayerKey key;
+    memset(&key, 0, sizeof key);
+    key.dev = dev;
+    key.x = x;
+    key.topk_ids = topk_ids;
+    key.topk_w = topk_w;
+    key.T = T;
+    key.topk = topk;
+    key.E = E;
+    key.E_global = E_global;
+    key.H = H;
+    key.I = I;
+    key.block_m = block_m;
+    key.w13 = packed_w13;
+    key.w13_bytes = w13_bytes;
+    key.w2 = packed_w2;
+    key.w2_bytes = w2_bytes;
+    key.workspace = workspace;
+    key.workspace_bytes = workspace_bytes;
+    key.out = out;
+    key.opts = o;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    std::lock_guard<std::mutex> lk(g_graph_mu);
+    for (int i = 0; i < g_ngraphs; ++i) {
+        if (memcmp(&g_graphs[i].key, &key, sizeof key) == 0) {
+            g_graphs[i].last_use = ++g_graph_clock;
+            return cudaGraphLaunch(g_graphs[i].exec, s) == cudaSuccess ? CHORD_OK : CHORD_ERR_CUDA;
+        }
+    }
+    // first call with these arguments: record the layer's launches on a
+    // capture stream of this device, instantiate, keep
+    if (!g_capture_stream[dev] && cudaStreamCreateWithFlags(&g_capture_stream[dev], cudaStreamNonBlocking) != cudaSuccess)
+        return CHORD_ERR_CUDA;
+    cudaStream_t cs = g_capture_stream[dev];
+    if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return CHORD_ERR_CUDA;
+    const chord_status st = chord_moe_layer(x, topk_ids, topk_w, T, topk, E, E_global, H, I, packed_w13, w13_bytes,
+                                            packed_w2, w2_bytes, block_m, workspace, workspace_bytes, out, &o, cs);
+    cudaGraph_t graph = nullptr;
+    const cudaError_t ce = cudaStreamEndCapture(cs, &graph);
+    if (st != CHORD_OK || ce != cudaSuccess || !graph) {
+        if (graph) cudaGraphDestroy(graph);
+        cudaGetLastError();
+        return st != CHORD_OK ? st : CHORD_ERR_CUDA;
+    }
+    cudaGraphExec_t exec = nullptr;
+    const cudaError_t ie = cudaGraphInstantiate(&exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (ie != cudaSuccess) return CHORD_ERR_CUDA;
+    int slot = g_ngraphs;
+    if (g_ngraphs == kMaxLayerGraphs) {   // full: the least recently used graph goes
+        slot = 0;
+        for (int i = 1; i < g_ngraphs; ++i)
+            if (g_graphs[i].last_use < g_graphs[slot].last_use) slot = i;
+        cudaGraphExecDestroy(g_graphs[slot].exec);
+    } else {
+        ++g_ngraphs;
+    }
+    g_graphs[slot].key = key;
+    g_graphs[slot].exec = exec;
+    g_graphs[slot].last_use = ++g_graph_clock;
+    return cudaGraphLaunch(exec, s) == cudaSuccess ? CHORD_OK : CHORD_ERR_CUDA;
+}
+
+int chord_moe_layer_cache_clear(void) {
+    std::lock_guard<std::mutex> lk(g_graph_mu);
+    const int n = g_ngraphs;
+    for (int i = 0; i < g_ngraphs; ++i) cudaGraphExecDestroy(g_graphs[i].exec);
+    g_ngraphs = 0;
+    return n;
 }
 
 // ---- grouped contracts: routing arrays built on the device, then the
