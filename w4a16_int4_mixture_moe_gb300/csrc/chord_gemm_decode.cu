@@ -61,6 +61,17 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Epilogue of a launch, fixed at compile time so that each kernel carries
+// only its own store path (the consumer loop is instantiated once per token
+// tile count and dequantisation form; every store path inlined into each of
+// those copies made the loop longer than the instruction cache holds).
+enum Epi : int {
+    kEpiStore = 0,     // C[pair, n]: bf16, or FP32 with out_f32
+    kEpiSilu = 1,      // h[pair, j] = SiLU(gate) * up (packed layout 3)
+    kEpiPartial = 2,   // FP32 partial sums of one K slice
+    kEpiCombine = 3,   // fused top-k combine (FP32 sums of multi-pair tokens)
+};
+
 // Per-item routing facts, computed identically by the producer and the
 // consumers from the same global data.  At most 32 token slots per item.
 struct ItemRows {
@@ -144,7 +155,7 @@ __device__ __forceinline__ void chunk_mma(const uint8_t* cb, int row0, uint32_t 
 // Consumer side of one item whose valid token slots lie in its first NV
 // 8-token tiles (align fills a block's slots from the front): the K loop over
 // the stage ring, then the epilogue.  Returns false when a wait gave up.
-template <int NT, int STAGES, int MI, int NV, bool FD>
+template <int NT, int STAGES, int MI, int NV, bool FD, int EPI>
 __device__ __forceinline__ bool consume_item(const GemmArgs& a, uint8_t* smem, uint64_t* full, uint64_t* empty,
                                           volatile int* flags, int64_t& stage, int warp, int lane, int nt,
                                           int32_t my_id, int ks0, int ks1, int slice) {
@@ -189,7 +200,7 @@ __device__ __forceinline__ bool consume_item(const GemmArgs& a, uint8_t* smem, u
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
             p[u] = __shfl_sync(0xffffffffu, my_id, 8 * t + 2 * c + u);
-            if (a.combine && a.ksplit <= 1 && p[u] >= 0) pw[u] = a.pair_w[p[u]];
+            if (EPI == kEpiCombine && p[u] >= 0) pw[u] = a.pair_w[p[u]];
         }
 #pragma unroll
         for (int mi = 0; mi < MI; ++mi) {
@@ -197,17 +208,17 @@ __device__ __forceinline__ bool consume_item(const GemmArgs& a, uint8_t* smem, u
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 if (p[u] < 0) continue;
-                if (a.ksplit > 1) {
+                if (EPI == kEpiPartial) {
                     // K slice `slice`: FP32 partial sums in packed row order
                     float* prow = a.partial + ((int64_t)slice * a.num_pairs + p[u]) * a.N;
                     prow[n0] = acc[mi][t][u];
                     prow[n0 + 8] = acc[mi][t][2 + u];
-                } else if (a.silu) {
+                } else if (EPI == kEpiSilu) {
                     // packed rows n0 = 16k + g and n0 + 8 hold gate and up of
                     // column j = 8k + g (layout 3)
                     __nv_bfloat16* hrow = static_cast<__nv_bfloat16*>(a.C) + (int64_t)p[u] * (a.N / 2);
                     hrow[8 * (n0 / 16) + g] = silu_mul_bf16(acc[mi][t][u], acc[mi][t][2 + u]);
-                } else if (a.combine) {
+                } else if (EPI == kEpiCombine) {
                     const int64_t tok = p[u] / a.topk;
                     combine_store(static_cast<float*>(a.C), a.out, a.N, p[u], tok, pw[u], n0, acc[mi][t][u]);
                     combine_store(static_cast<float*>(a.C), a.out, a.N, p[u], tok, pw[u], n0 + 8, acc[mi][t][2 + u]);
@@ -227,20 +238,20 @@ __device__ __forceinline__ bool consume_item(const GemmArgs& a, uint8_t* smem, u
 }
 
 // consume_item instantiated for the item's count of 8-token tiles.
-template <int NT, int STAGES, int MI, bool FD>
+template <int NT, int STAGES, int MI, bool FD, int EPI>
 __device__ __forceinline__ bool consume_nv(const GemmArgs& a, uint8_t* smem, uint64_t* full, uint64_t* empty,
                                            volatile int* flags, int64_t& stage, int warp, int lane, int nt,
                                            int32_t my_id, int ks0, int ks1, int slice, int nv) {
     if (nv <= 1)
-        return consume_item<NT, STAGES, MI, 1, FD>(a, smem, full, empty, flags, stage, warp, lane, nt, my_id, ks0,
+        return consume_item<NT, STAGES, MI, 1, FD, EPI>(a, smem, full, empty, flags, stage, warp, lane, nt, my_id, ks0,
                                                    ks1, slice);
     if (nv == 2 || NT == 2)
-        return consume_item<NT, STAGES, MI, (NT >= 2 ? 2 : 1), FD>(a, smem, full, empty, flags, stage, warp, lane,
+        return consume_item<NT, STAGES, MI, (NT >= 2 ? 2 : 1), FD, EPI>(a, smem, full, empty, flags, stage, warp, lane,
                                                                    nt, my_id, ks0, ks1, slice);
     if (nv == 3)
-        return consume_item<NT, STAGES, MI, (NT >= 4 ? 3 : 1), FD>(a, smem, full, empty, flags, stage, warp, lane,
+        return consume_item<NT, STAGES, MI, (NT >= 4 ? 3 : 1), FD, EPI>(a, smem, full, empty, flags, stage, warp, lane,
                                                                    nt, my_id, ks0, ks1, slice);
-    return consume_item<NT, STAGES, MI, (NT >= 4 ? 4 : 1), FD>(a, smem, full, empty, flags, stage, warp, lane, nt,
+    return consume_item<NT, STAGES, MI, (NT >= 4 ? 4 : 1), FD, EPI>(a, smem, full, empty, flags, stage, warp, lane, nt,
                                                                my_id, ks0, ks1, slice);
 }
 
@@ -269,7 +280,7 @@ __device__ __forceinline__ int64_t unit_coords(int64_t unit, int S, int ntiles, 
     return divmod_idx(bs, nsub, sub);
 }
 
-template <int NT, int STAGES, int MI, int MINB>
+template <int NT, int STAGES, int MI, int MINB, int EPI>
 __global__ void __launch_bounds__(Cfg<NT, MI>::kThreads, MINB) gemm_decode_kernel(const GemmArgs a) {
     pdl_trigger();
     pdl_wait();
@@ -394,19 +405,19 @@ __global__ void __launch_bounds__(Cfg<NT, MI>::kThreads, MINB) gemm_decode_kerne
         if (rows.vmask == 0) continue;
         const int nv = (32 - __clz(rows.vmask) + 7) / 8;   // 8-token tiles up to the last valid slot
         const bool ok = fma_dequant
-                            ? consume_nv<NT, STAGES, MI, true>(a, smem, full, empty, flags, stage, warp, lane, nt,
+                            ? consume_nv<NT, STAGES, MI, true, EPI>(a, smem, full, empty, flags, stage, warp, lane, nt,
                                                                rows.id, ks0, ks1, slice, nv)
-                            : consume_nv<NT, STAGES, MI, false>(a, smem, full, empty, flags, stage, warp, lane, nt,
+                            : consume_nv<NT, STAGES, MI, false, EPI>(a, smem, full, empty, flags, stage, warp, lane, nt,
                                                                 rows.id, ks0, ks1, slice, nv);
         if (!ok) return;
     }
 }
 
-template <int NT, int STAGES, int MI, int MINB>
-cudaError_t launch_nt(const GemmArgs& a, cudaStream_t stream) {
+template <int NT, int STAGES, int MI, int MINB, int EPI>
+cudaError_t launch_epi(const GemmArgs& a, cudaStream_t stream) {
     using C = Cfg<NT, MI>;
     constexpr int smem = STAGES * C::kStageBytes + 2 * STAGES * 8 + 16;
-    auto kern = gemm_decode_kernel<NT, STAGES, MI, MINB>;
+    auto kern = gemm_decode_kernel<NT, STAGES, MI, MINB, EPI>;
     int per_sm = 1;
     cudaError_t e = kernel_ctas_per_sm(reinterpret_cast<const void*>(kern), C::kThreads, smem, smem, &per_sm);
     if (e != cudaSuccess) return e;
@@ -416,6 +427,14 @@ cudaError_t launch_nt(const GemmArgs& a, cudaStream_t stream) {
     if (grid > items_cap) grid = items_cap;
     if (grid < 1) grid = 1;
     return launch_pdl(pdl_for(a.num_pairs), kern, dim3((unsigned)grid), dim3(C::kThreads), (size_t)smem, stream, a);
+}
+
+template <int NT, int STAGES, int MI, int MINB>
+cudaError_t launch_nt(const GemmArgs& a, cudaStream_t stream) {
+    if (a.ksplit > 1) return launch_epi<NT, STAGES, MI, MINB, kEpiPartial>(a, stream);
+    if (a.silu) return launch_epi<NT, STAGES, MI, MINB, kEpiSilu>(a, stream);
+    if (a.combine) return launch_epi<NT, STAGES, MI, MINB, kEpiCombine>(a, stream);
+    return launch_epi<NT, STAGES, MI, MINB, kEpiStore>(a, stream);
 }
 
 }  // namespace
