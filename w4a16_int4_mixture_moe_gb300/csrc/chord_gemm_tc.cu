@@ -39,6 +39,7 @@ constexpr int kTileRows = 128;   // rows of N per item = MMA M
 constexpr int kChunkK = 64;      // K columns of one packed chunk; a pipeline stage holds two
 constexpr int kChunk2 = 4608;    // packed bytes of one 128 x 64 chunk (layout 2)
 constexpr int kACols = 64;       // tensor-memory columns of one A stage (128 bf16 per lane)
+constexpr int kStgWarpBytes = 2048;   // drain buffer of one dequantising warp: 16 tokens x 32 rows x FP32
 
 // The A operand ring lives in tensor memory (64 columns per stage, as many
 // stages as the columns left after the accumulators allow, sized at launch);
@@ -358,7 +359,7 @@ __device__ __forceinline__ Unit unit_at(int64_t u, const TailPlan& tp, int kstag
 // l%16 held by lane l (-1: none).
 template <bool CMB, int NI>
 __device__ __forceinline__ void drain_item(const TcArgs& ta, const Unit& un, int n_mma, int nt, int wg, int lane,
-                                           uint32_t acc_tmem, const int32_t (&pre)[4]) {
+                                           uint32_t acc_tmem, const int32_t (&pre)[4], uint8_t* stg) {
     const GemmArgs& a = ta.g;
     const int quarter = (threadIdx.x >> 5) & 3;
     const int row = quarter * 32 + lane;
@@ -403,6 +404,48 @@ __device__ __forceinline__ void drain_item(const TcArgs& ta, const Unit& un, int
                                      __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
             continue;
         }
+        if (!CMB && !a.silu) {
+            // Plain bf16 / FP32 output.  One warp store of a 32-row column
+            // slice per token wrote 64 (128) bytes per instruction, and the
+            // drain took longer than the item's MMAs it delays (the write
+            // requests, not their bytes, are what an SM has few of in flight).
+            // So the 16 x 32 tile goes through this warp's shared-memory
+            // buffer, token-major, and leaves in 16-byte pieces: piece q
+            // holds `per` consecutive rows of token q / (32 / per).
+            const int esz = a.out_f32 ? 4 : 2;
+            const int per = 16 / esz;              // rows per 16-byte piece
+            const int pieces_tok = 32 / per;       // pieces per token
+            const uint32_t sbase = smem_u32(stg);
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const uint32_t addr = sbase + (uint32_t)((u * 32 + lane) * esz);
+                if (a.out_f32)
+                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v[u]) : "memory");
+                else
+                    asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr),
+                                 "h"(__bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[u]))))
+                                 : "memory");
+            }
+            __syncwarp();
+            const int npieces = 16 * pieces_tok;   // 64 (bf16) or 128 (FP32) per warp
+            for (int q = lane; q < npieces; q += 32) {
+                const int u = q / pieces_tok;
+                const int r0 = (q % pieces_tok) * per;
+                const int32_t id = __shfl_sync(0xffffffffu, pre[it >> 1], u + 16 * (it & 1));
+                uint4 w4;
+                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(w4.x), "=r"(w4.y), "=r"(w4.z), "=r"(w4.w)
+                             : "r"(sbase + (uint32_t)(q * 16))
+                             : "memory");
+                if (id >= 0) {
+                    const int64_t col = (int64_t)nt * kTileRows + quarter * 32 + r0;
+                    uint8_t* dst = static_cast<uint8_t*>(a.C) + ((int64_t)id * a.N + col) * esz;
+                    *reinterpret_cast<uint4*>(dst) = w4;
+                }
+            }
+            __syncwarp();
+            continue;
+        }
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
             if (!CMB && a.silu) {
@@ -444,7 +487,7 @@ __device__ __forceinline__ void drain_item(const TcArgs& ta, const Unit& un, int
 template <int NI>
 __device__ __noinline__ void drain_item_combine(const TcArgs& ta, const Unit& un, int n_mma, int nt, int wg, int lane,
                                                 uint32_t acc_tmem, const int32_t (&pre)[4]) {
-    drain_item<true, NI>(ta, un, n_mma, nt, wg, lane, acc_tmem, pre);
+    drain_item<true, NI>(ta, un, n_mma, nt, wg, lane, acc_tmem, pre, nullptr);
 }
 
 template <int GW, int MAXR, int NI, bool PAIR>
@@ -466,7 +509,8 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
     const int b_stage = 2 * b_sub;
     uint8_t* sB = smem;                               // NSB x 2 sub-tiles
     uint8_t* sW = sB + NSB * b_stage;                 // NSW x 2 packed chunks
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sW + NSW * 2 * kChunk2);
+    uint8_t* sStg = sW + NSW * 2 * kChunk2;           // the dequantising warps' drain buffers
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sStg + C::kDQ * kStgWarpBytes);
     uint64_t* w_full = bars;
     uint64_t* w_empty = w_full + NSW;
     uint64_t* b_full = w_empty + NSW;
@@ -636,11 +680,21 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
                     // reads it through the async proxy
                     fence_proxy_async();
                     tc_fence_after();
-                    const uint32_t b_base = smem_u32(sB + br.slot * b_stage);
-                    for (int kk = 0; kk < 4 * nck; ++kk)
-                        tc_mma_ts_g<PAIR>(my_acc, tmem_base + ar.slot * kACols + kk * 8,
-                                          desc_sw128(b_base + (kk >> 2) * b_sub + (kk & 3) * 32), idesc,
-                                          (any || kk > 0) ? 1u : 0u);
+                    // Eight K = 16 steps per stage, unrolled: step kk reads A
+                    // columns 8 kk of the stage and the B descriptor advanced by
+                    // (kk / 4) sub-tiles and (kk % 4) 32-byte K slices (the
+                    // descriptor's address field counts 16-byte units and stays
+                    // below 2^14 inside the 227 KB of shared memory, so the sum
+                    // never carries into the next field).
+                    const uint64_t d0 = desc_sw128(smem_u32(sB + br.slot * b_stage));
+                    const uint32_t a0 = tmem_base + ar.slot * kACols;
+                    const uint32_t sub16 = (uint32_t)b_sub >> 4;
+                    const uint32_t acc0 = any ? 1u : 0u;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        if (kk < 4 * nck)
+                            tc_mma_ts_g<PAIR>(my_acc, a0 + kk * 8, d0 + (uint64_t)((kk >> 2) * sub16 + (kk & 3) * 2),
+                                              idesc, kk > 0 ? 1u : acc0);
                     any = true;
                     tc_commit_g<PAIR>(&a_empty[ar.slot]);
                     tc_commit_g<PAIR>(&b_empty[br.slot]);
@@ -814,7 +868,7 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
             if (a.combine)
                 drain_item_combine<NI>(ta, un, inf.n_mma, nt, wg, lane, acc_tmem, pre);
             else
-                drain_item<false, NI>(ta, un, inf.n_mma, nt, wg, lane, acc_tmem, pre);
+                drain_item<false, NI>(ta, un, inf.n_mma, nt, wg, lane, acc_tmem, pre, sStg + warp * kStgWarpBytes);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
@@ -906,7 +960,7 @@ template <int GW, int MAXR, int NI, bool PAIR>
 cudaError_t launch_cfg(const GemmArgs& g, bool deep_weights, cudaStream_t stream) {
     using C = Cfg<GW, MAXR, NI>;
     auto kern = gemm_tc_kernel<GW, MAXR, NI, PAIR>;
-    constexpr size_t kSmemBudget = 220 * 1024;   // of the 227 KB a CTA may use
+    constexpr size_t kSmemBudget = 227 * 1024;   // the dynamic shared memory a CTA may use
     TcArgs ta;
     ta.g = g;
     ta.tok_tile = (g.block_m < 16 ? 16 : (g.block_m + 15) / 16 * 16);
@@ -928,7 +982,8 @@ cudaError_t launch_cfg(const GemmArgs& g, bool deep_weights, cudaStream_t stream
     // tiles, whose gather from L2 has the longer latency per byte consumed.
     // (a pair's CTA holds half of each B tile)
     const size_t b_stage = (size_t)(PAIR ? ta.tok_tile / 2 : ta.tok_tile) * 256, w_stage = 2 * kChunk2;
-    const size_t fixed = 1024 + 64;
+    // 1 KB of alignment slack, the barriers' margin and the drain buffers
+    const size_t fixed = 1024 + 64 + (size_t)C::kDQ * kStgWarpBytes;
     int nsb, nsw;
     if (deep_weights) {
         nsb = (int)((64 * 1024) / b_stage);
