@@ -180,7 +180,7 @@ def test_gemm_exact_integer_regime_bit_exact(kernel, bm, K, scale):
     scale in any order, so the GPU must match the oracle bit for bit (catches
     any wrong index, lost or doubled K chunk, or token/row mix-up).  Scale 1.0
     lies outside [2^-126, 0.5) and takes the subtract-then-scale instructions,
-    0.25 the warp-level kernel's one-FMA dequantisation."""
+    0.25 the one-FMA dequantisation (both kernels)."""
     T, topk, E, N = 40, 4, 5, 256
     rng = np.random.default_rng(bm * 100 + K)
     xi = rng.integers(-1, 2, size=(T, K)).astype(np.float32)
@@ -218,9 +218,8 @@ def test_gemm_dequant_bit_exact_one_hot(kernel, bm):
 @pytest.mark.parametrize("bm", [8, 16, 32, 64, 128])
 def test_gemm_dequant_bit_exact_one_hot_fma_range(kernel, bm):
     """As above with every scale a positive bf16 in [2^-126, 0.5): the packer
-    sets header word 7 and the warp-level kernel takes the one-FMA
-    dequantisation (the tcgen05 kernel keeps subtract-then-scale; both must
-    agree).  Exponents over that whole range, random mantissas, and both ends
+    sets header word 7 and both kernels take the one-FMA dequantisation, which
+    must equal subtract-then-scale.  Exponents over that whole range, random mantissas, and both ends
     (2^-126 and the largest bf16 below 0.5).  Every code times every such scale
     must equal the oracle's bf16((q - 8) * s), q = 8 giving +0."""
     K, N, E = 128, 256, 1

@@ -14,8 +14,10 @@
 //     (cp.async.mbarrier.arrive.noinc) and the MMA thread fences the async
 //     proxy before reading the tile;
 //   * dequantising warps (one row per thread, two warpgroups taking alternate
-//     stages) turn 32 codes per 16-byte load into bf16((q - 8) * s) and store
-//     them with tcgen05.st into a tensor-memory stage, the MMA's A operand (no
+//     stages) turn 32 codes per 16-byte load into bf16((q - 8) * s) (one
+//     bf16x2 FMA per pair when the blob's header says every scale lies in
+//     [2^-126, 0.5), as in the warp-level kernel) and store them with
+//     tcgen05.st into a tensor-memory stage, the MMA's A operand (no
 //     shared-memory round trip for the dequantised weights);
 //   * an MMA-issuing thread issues eight tcgen05.mma (M=128, N=tokens rounded
 //     up to 16, K=16) into its FP32 accumulator in tensor memory and commits
@@ -520,7 +522,8 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
     uint64_t* acc_full = a_empty + SA;
     uint64_t* acc_empty = acc_full + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 1);
-    volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // [0] skip, [1] abort
+    // [0] skip, [1] abort, [2] every scale in the one-FMA dequantisation's range
+    volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -528,6 +531,7 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
         if (!ok) set_error(a.err, CHORD_DEV_BAD_HEADER);
         flags[0] = ok ? 0 : 1;
         flags[1] = 0;
+        flags[2] = ok && header_scales_in_fma_range(a.packed) ? 1 : 0;
         for (int s = 0; s < NSW; ++s) {
             mbar_init(&w_full[s], 1);
             mbar_init(&w_empty[s], 4);        // the 4 warps of the warpgroup that took the stage
@@ -783,6 +787,7 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
         const int quarter = warp & 3;                  // tensor-memory lane quarter of this warp
         const int row = quarter * 32 + lane;           // weight row of the tile = TMEM lane
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        const bool fma_dequant = flags[2] != 0;   // the blob's header: one FMA per weight pair
         int64_t g = 0, nitem = 0;
         Ring wr, ar;
         bool ok = true;
@@ -823,10 +828,19 @@ __global__ void __launch_bounds__(Cfg<GW, MAXR, NI>::kThreads, 1) gemm_tc_kernel
                             const uint32_t s16 = h ? (sc[ch] >> 16) : (sc[ch] & 0xffffu);
                             const uint32_t sp = s16 | (s16 << 16);
                             const uint4 qq = q[2 * ch + h];
-                            dequant_row8(qq.x, sp, v + 16 * h + 0);
-                            dequant_row8(qq.y, sp, v + 16 * h + 4);
-                            dequant_row8(qq.z, sp, v + 16 * h + 8);
-                            dequant_row8(qq.w, sp, v + 16 * h + 12);
+                            if (fma_dequant) {
+                                uint32_t b2, c2;
+                                fma_scale_pair(sp, b2, c2);
+                                dequant_row8_fma(qq.x, b2, c2, v + 16 * h + 0);
+                                dequant_row8_fma(qq.y, b2, c2, v + 16 * h + 4);
+                                dequant_row8_fma(qq.z, b2, c2, v + 16 * h + 8);
+                                dequant_row8_fma(qq.w, b2, c2, v + 16 * h + 12);
+                            } else {
+                                dequant_row8(qq.x, sp, v + 16 * h + 0);
+                                dequant_row8(qq.y, sp, v + 16 * h + 4);
+                                dequant_row8(qq.z, sp, v + 16 * h + 8);
+                                dequant_row8(qq.w, sp, v + 16 * h + 12);
+                            }
                         }
                         tmem_st32(tmem_base + lane_base + ar.slot * kACols + ch * 32, v);
                     }
