@@ -179,7 +179,8 @@ __device__ __forceinline__ bool consume_item(const GemmArgs& a, uint8_t* smem, u
     for (int ks = ks0; ks < ks1; ++ks, ++stage) {
         const int slot = (int)(stage % STAGES);
         const uint32_t par = (uint32_t)((stage / STAGES) & 1);
-        if (!mbar_wait(&full[slot], par) || flags[1]) {
+        // the abort flag is read only when the stage has not landed yet
+        if (!mbar_try_wait(&full[slot], par) && (!mbar_wait(&full[slot], par) || flags[1])) {
             if (lane == 0) set_error(a.err, CHORD_DEV_TIMEOUT);
             flags[1] = 1;
             return false;
@@ -348,14 +349,26 @@ __global__ void __launch_bounds__(Cfg<NT, MI>::kThreads, MINB) gemm_decode_kerne
             const uint8_t* wexp = wbase + (uint64_t)e * expert_bytes;
             // Activation rows: lanes 0-15 copy the 16-byte pieces of token slot
             // 2i, lanes 16-31 those of slot 2i + 1 (valid slots are a prefix).
-            const int32_t arow_i = a.a_row_divisor == 1 ? rows.id : rows.id / a.a_row_divisor;
-            const uint16_t* arow = rows.id >= 0 ? a.A + (int64_t)arow_i * a.K : nullptr;
+            // Each lane's source pieces are found once per item, so a stage
+            // costs the producer one copy instruction per token and lane (its
+            // loop paces the whole ring: a shuffle and an address per token and
+            // stage made it issue a stage in about 1200 cycles on EP8 decode).
             const int npairs = (32 - __clz(rows.vmask) + 1) / 2;
             const int half_lane = lane >> 4, piece = lane & 15;
+            const int32_t my_row = rows.id < 0 ? -1 : (a.a_row_divisor == 1 ? rows.id : rows.id / a.a_row_divisor);
+            const uint16_t* src[kTok / 2];
+#pragma unroll
+            for (int i = 0; i < kTok / 2; ++i) {
+                if (i >= npairs) break;   // npairs is the same in every lane
+                const int32_t r = __shfl_sync(0xffffffffu, my_row, 2 * i + half_lane);
+                src[i] = r >= 0 ? a.A + (int64_t)r * a.K + piece * 8 : nullptr;
+            }
+            const uint32_t xlane = (uint32_t)(half_lane * kXStride + piece * 16);
             for (int ks = ks0; ks < ks1; ++ks) {
                 const int slot = (int)(stage % STAGES);
                 const uint32_t par = (uint32_t)((stage / STAGES) & 1);
-                if (!mbar_wait(&empty[slot], par ^ 1u) || flags[1]) {
+                // the abort flag is read only when the slot is not free yet
+                if (!mbar_try_wait(&empty[slot], par ^ 1u) && (!mbar_wait(&empty[slot], par ^ 1u) || flags[1])) {
                     if (lane == 0) set_error(a.err, CHORD_DEV_TIMEOUT);
                     flags[1] = 1;
                     aborted = true;
@@ -370,12 +383,13 @@ __global__ void __launch_bounds__(Cfg<NT, MI>::kThreads, MINB) gemm_decode_kerne
                     const uint8_t* src = wexp + ((uint64_t)nt * kchunks + (uint64_t)(2 * ks)) * kChunk2;
                     bulk_g2s_hint(sW, src, (uint32_t)(nchunk * kChunk2), &full[slot], pol);
                 }
-                const bool my_piece = piece < nchunk * 8;   // a one-chunk stage has 8 pieces per row
-                for (int i = 0; i < npairs; ++i) {
-                    const int j = 2 * i + half_lane;
-                    const uint16_t* r = reinterpret_cast<const uint16_t*>(
-                        __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(arow), j));
-                    if (r && my_piece) cp_async16(sX + (uint32_t)(j * kXStride + piece * 16), r + ks * kKS + piece * 8);
+                if (piece < nchunk * 8) {   // a one-chunk stage has 8 pieces per row
+                    const int off = ks * kKS;
+#pragma unroll
+                    for (int i = 0; i < kTok / 2; ++i) {
+                        if (i >= npairs) break;
+                        if (src[i]) cp_async16(sX + xlane + (uint32_t)(i * 2 * kXStride), src[i] + off);
+                    }
                 }
                 cp_async_arrive_noinc(&full[slot]);
                 ++stage;
