@@ -176,6 +176,7 @@ __device__ __forceinline__ bool consume_item(const GemmArgs& a, uint8_t* smem, u
 #pragma unroll
             for (int q = 0; q < 4; ++q) acc[mi][t][q] = 0.0f;
 
+    const int ks_full = a.K / kKS;   // stages holding both 64-column chunks
     for (int ks = ks0; ks < ks1; ++ks, ++stage) {
         const int slot = (int)(stage % STAGES);
         const uint32_t par = (uint32_t)((stage / STAGES) & 1);
@@ -187,8 +188,14 @@ __device__ __forceinline__ bool consume_item(const GemmArgs& a, uint8_t* smem, u
         }
         const uint8_t* sW = smem + slot * kStage;
         const uint32_t xa = smem_u32(sW + kWStageBytes) + x_lane;
-        chunk_mma<MI, NV, FD>(sW, row0, code_off, scale_sel, xa, acc);
-        if (a.K - ks * kKS >= 128) chunk_mma<MI, NV, FD>(sW + kChunk2, row0, code_off, scale_sel, xa + 128, acc);
+        // both chunks' code in one block for a full stage, so the compiler can
+        // schedule the second chunk's loads with the first chunk's math
+        if (ks < ks_full) {
+            chunk_mma<MI, NV, FD>(sW, row0, code_off, scale_sel, xa, acc);
+            chunk_mma<MI, NV, FD>(sW + kChunk2, row0, code_off, scale_sel, xa + 128, acc);
+        } else {
+            chunk_mma<MI, NV, FD>(sW, row0, code_off, scale_sel, xa, acc);
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[slot]);
     }
