@@ -367,6 +367,10 @@ __device__ __forceinline__ void drain_item(const TcArgs& ta, const Unit& un, int
     const int row = quarter * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     const int n_out = nt * kTileRows + row;
+    // fused SiLU * up (layout 3): rows 16k + i (i < 8) and 16k + i + 8 of
+    // the tile hold gate and up of output column 64 * nt + 8k + i
+    const int h_col = nt * (kTileRows / 2) + 8 * (row / 16) + (row % 8);
+    const bool gate_row = (lane & 8) == 0;
     const int nst = un.ks1 - un.ks0;
     const int parts = nst < NI ? nst : NI;   // issuers that hold a share of this unit
     float prew[4];    // fused combine: the pair's weight (a number: its token's only local pair)
@@ -400,45 +404,6 @@ __device__ __forceinline__ void drain_item(const TcArgs& ta, const Unit& un, int
             for (int q = 0; q < 4; ++q)
                 dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
                                      __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
-            continue;
-        }
-        if (!CMB && a.silu) {
-            // SiLU * up (layout 3): rows 16k + i (i < 8) and 16k + 8 + i of the
-            // tile are gate and up of h column 64 nt + 8k + i, so this warp's
-            // 32 rows give h columns [16 quarter, 16 quarter + 16) of every
-            // token.  The FP32 sums go through the warp's buffer token-major;
-            // lane l then takes token l / 2 and the 8 columns 8 (l % 2) ..,
-            // reads their 8 gate and 8 up sums, and stores 8 bf16 results as
-            // one 16-byte piece (the same arithmetic as the separate pass).
-            const uint32_t sbase = smem_u32(stg);
-#pragma unroll
-            for (int u = 0; u < 16; ++u)
-                asm volatile("st.shared.b32 [%0], %1;" ::"r"(sbase + (uint32_t)((u * 32 + lane) * 4)), "r"(v[u])
-                             : "memory");
-            __syncwarp();
-            const int tu = lane >> 1, hh = lane & 1;
-            const int32_t id = __shfl_sync(0xffffffffu, pre[it >> 1], tu + 16 * (it & 1));
-            float gv[8], uv[8];
-            const uint32_t gaddr = sbase + (uint32_t)((tu * 32 + 16 * hh) * 4);
-            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                         : "=f"(gv[0]), "=f"(gv[1]), "=f"(gv[2]), "=f"(gv[3]) : "r"(gaddr) : "memory");
-            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                         : "=f"(gv[4]), "=f"(gv[5]), "=f"(gv[6]), "=f"(gv[7]) : "r"(gaddr + 16) : "memory");
-            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                         : "=f"(uv[0]), "=f"(uv[1]), "=f"(uv[2]), "=f"(uv[3]) : "r"(gaddr + 32) : "memory");
-            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                         : "=f"(uv[4]), "=f"(uv[5]), "=f"(uv[6]), "=f"(uv[7]) : "r"(gaddr + 48) : "memory");
-            __syncwarp();
-            if (id >= 0) {
-                uint32_t hw[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    hw[q] = (uint32_t)__bfloat16_as_ushort(silu_mul_bf16(gv[2 * q], uv[2 * q])) |
-                            ((uint32_t)__bfloat16_as_ushort(silu_mul_bf16(gv[2 * q + 1], uv[2 * q + 1])) << 16);
-                const int64_t col = (int64_t)nt * (kTileRows / 2) + quarter * 16 + hh * 8;
-                *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.C) + (int64_t)id * (a.N / 2) + col) =
-                    make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            }
             continue;
         }
         if (!CMB && !a.silu) {
@@ -485,6 +450,22 @@ __device__ __forceinline__ void drain_item(const TcArgs& ta, const Unit& un, int
         }
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
+            if (!CMB && a.silu) {
+                // lanes l (gate row) and l ^ 8 (its up row) split the 16
+                // tokens: the gate lane takes tokens 0-7, the up lane 8-15,
+                // each receiving the partner's value for its tokens
+                if (u < 8) {
+                    const float lo = __uint_as_float(v[u]), hi = __uint_as_float(v[8 + u]);
+                    const float mine = gate_row ? lo : hi;
+                    const float other = __shfl_xor_sync(0xffffffffu, gate_row ? hi : lo, 8);
+                    const int tok = gate_row ? u : 8 + u;
+                    const int32_t id = __shfl_sync(0xffffffffu, pre[it >> 1], tok + 16 * (it & 1));
+                    if (id >= 0)
+                        static_cast<__nv_bfloat16*>(a.C)[(int64_t)id * (a.N / 2) + h_col] =
+                            gate_row ? silu_mul_bf16(mine, other) : silu_mul_bf16(other, mine);
+                }
+                continue;
+            }
             const int32_t id = __shfl_sync(0xffffffffu, pre[it >> 1], u + 16 * (it & 1));
             const float val = __uint_as_float(v[u]);
             if (CMB) {
