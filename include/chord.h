@@ -178,7 +178,7 @@ size_t chord_packed_weight_bytes(int E, int N, int K, int layout);
  * the layout, the group size, E, N, K, then in word 7 a 1 when every scale is
  * a positive normal bf16 below 0.5 (else 0), then the 64-bit expert stride
  * N * K * 9 / 16 and data offset 256.  Word 7 changes no result: with it set,
- * the decode kernel forms each bf16((q - 8) * s) with one FMA per pair instead
+ * both GEMM kernels form each bf16((q - 8) * s) with one FMA per pair instead
  * of a subtract and a multiply (the same value, bit for bit). */
 chord_status chord_pack_weights(const uint8_t *codes, const void *scales, int E, int N, int K,
                                 int group_size, int layout, void *packed, size_t packed_bytes,
