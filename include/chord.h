@@ -392,8 +392,8 @@ chord_status chord_moe_combine(const void *C2, int c2_dtype, const int32_t *topk
                                const float *topk_w, int T, int topk, int E, int H, void *out,
                                void *stream);
 
-/* The top-k combine fused into the down GEMM (the benchmark spec's gather/scatter
- * epilogue with top-k weights): the same out as chord_moe_combine of the down
+/* The top-k combine fused into the down GEMM (a scatter epilogue that applies
+ * the top-k weights): the same out as chord_moe_combine of the down
  * GEMM's FP32 output, bit for bit, in three calls.  A token with exactly one
  * local pair gets its output straight from the GEMM's epilogue,
  * bf16(0 + w * sum), which is the weighted sum over that one pair; the FP32
